@@ -1,0 +1,92 @@
+"""ctypes declarations for libadasum_gb300.so (the C ABI of include/adasum.h).
+
+Argument marshalling only: no arithmetic of the method happens in Python.  Loading
+fails loudly when the library has not been built; there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import enum
+import os
+import threading
+
+from . import _build
+
+_lock = threading.Lock()
+_lib = None
+
+
+class Status(enum.IntEnum):
+    OK = 0
+    ERR_INVALID_ARG = 1
+    ERR_UNSUPPORTED = 2
+    ERR_ALIAS = 3
+    ERR_NO_MEMORY = 4
+    ERR_CUDA = 5
+    ERR_TIMEOUT = 6
+
+
+class AdasumError(RuntimeError):
+    """A non-OK status returned by the native library."""
+
+    def __init__(self, status: int, where: str):
+        self.status = Status(status) if status in Status._value2member_map_ else status
+        super().__init__(f"{where}: {getattr(self.status, 'name', status)}")
+
+
+class KernelStat(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char * 64), ("launches", ctypes.c_int64),
+                ("total_ms", ctypes.c_double)]
+
+
+#: Every symbol include/adasum.h declares, with (restype, argtypes).
+SIGNATURES = {
+    "adasum_reduce": (ctypes.c_int, [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int,
+                                     ctypes.POINTER(ctypes.c_int64), ctypes.c_int,
+                                     ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]),
+    "adasum_pair": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
+                                   ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]),
+    "adasum_reduce_momentum_sgd": (ctypes.c_int, [
+        ctypes.POINTER(ctypes.c_void_p), ctypes.c_int, ctypes.POINTER(ctypes.c_int64),
+        ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_float,
+        ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p]),
+    "adasum_get_last_error": (ctypes.c_int, []),
+    "adasum_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "adasum_release_workspace": (ctypes.c_int, []),
+    "adasum_version": (ctypes.c_int, []),
+    "adasum_launch_count": (ctypes.c_int64, []),
+    "adasum_recomputed_segments": (ctypes.c_int64, []),
+    "adasum_profile_enable": (ctypes.c_int, [ctypes.c_int]),
+    "adasum_profile_collect": (ctypes.c_int, [ctypes.POINTER(KernelStat), ctypes.c_int]),
+}
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load_library(build_if_missing: bool = False):
+    """Load (and declare) the native library.  Raises if it is not built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB_PATH
+        if not os.path.exists(path):
+            if not build_if_missing:
+                raise RuntimeError(
+                    f"{os.path.basename(path)} is not built; run "
+                    "`python -c 'import __graft_entry__ as g; g.build()'` first")
+            _build.build()
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+        return lib
+
+
+def check(status: int, where: str) -> None:
+    if status != 0:
+        raise AdasumError(status, where)

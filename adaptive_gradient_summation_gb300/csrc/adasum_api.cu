@@ -1,0 +1,628 @@
+// adasum_api.cu -- host side of the C ABI declared in include/adasum.h.
+//
+// Validation, tiling plans, the per-device workspace, stage scheduling and launches.
+// "Scaling Distributed Training with Adaptive Summation", Section 3: the K worker
+// gradients are combined per layer segment by a binary tree of the Adasum pair
+// operator.  The device computes it in coefficient space (see adasum_internal.h):
+// for every stage, pass 1 (Gram partials per tile) -> coefficients per segment ->
+// pass 2 (out = sum_k c_k g_k).  Trees of more than 16 leaves run as stages: 16-leaf
+// subtrees first (fp32 intermediates in the workspace), then the tree over their roots.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdlib>
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <list>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "../../include/adasum.h"
+#include "adasum_internal.h"
+
+namespace adasum {
+namespace {
+
+constexpr int kVersion = 100;  // 0.1.0
+
+int elem_size(int dt) { return dt == kBF16 ? 2 : 4; }
+
+// ------------------------------------------------------------------------ profiler
+
+struct ProfRecord {
+  const char* name;
+  cudaEvent_t start, stop;
+};
+
+std::mutex g_mu;                   // serialises every entry point
+std::atomic<int64_t> g_launches{0};
+bool g_profiling = false;
+std::vector<ProfRecord> g_prof_pending;
+std::vector<cudaEvent_t> g_event_pool;
+
+cudaEvent_t pool_event() {
+  if (!g_event_pool.empty()) {
+    cudaEvent_t e = g_event_pool.back();
+    g_event_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+
+// ----------------------------------------------------------------------- workspace
+
+// A tiling plan: tiles never straddle segments; inside a segment, tile boundaries sit
+// on multiples of 32 positions (so 16-byte vectors never straddle two tiles) except at
+// the segment's own ends.
+struct Plan {
+  std::vector<int64_t> offsets;
+  int Kg0 = 0;        // workers per group in the first stage
+  int dtype = 0;
+  int ntiles = 0;
+  int nsegs = 0;
+  int nchunks = 0;
+  TileDesc* d_tiles = nullptr;
+  SegDesc* d_segs = nullptr;
+  ChunkDesc* d_chunks = nullptr;
+};
+
+struct Workspace {
+  int device = -1;
+  void* buf = nullptr;
+  size_t cap = 0;
+  std::list<Plan> plans;            // most recently used first
+  int* last_flag_counts = nullptr;  // device counters of the last call's fp64 lists
+};
+
+std::vector<Workspace> g_ws;
+
+Workspace& workspace_for(int device) {
+  for (auto& w : g_ws)
+    if (w.device == device) return w;
+  g_ws.push_back(Workspace{});
+  g_ws.back().device = device;
+  return g_ws.back();
+}
+
+void free_plan(Plan& p) {
+  if (p.d_tiles) cudaFree(p.d_tiles);
+  if (p.d_segs) cudaFree(p.d_segs);
+  if (p.d_chunks) cudaFree(p.d_chunks);
+  p.d_tiles = nullptr;
+  p.d_segs = nullptr;
+  p.d_chunks = nullptr;
+}
+
+int64_t tile_positions(int Kg, int dtype, int64_t N, int num_sms) {
+  // About 256 KiB of input per tile, but enough tiles to give every SM a few.
+  const int64_t bytes_per_pos = static_cast<int64_t>(Kg) * elem_size(dtype);
+  int64_t T = (int64_t(256) << 10) / bytes_per_pos;
+  const int64_t want = std::max<int64_t>(1, N / (4 * static_cast<int64_t>(num_sms)));
+  T = std::min(T, want);
+  T = std::max<int64_t>(256, std::min<int64_t>(T, 65536));
+  return (T + 255) / 256 * 256;
+}
+
+adasum_status_t get_plan(Workspace& ws, const int64_t* offs, int L, int Kg0, int dtype,
+                         Plan** out) {
+  for (auto it = ws.plans.begin(); it != ws.plans.end(); ++it) {
+    if (it->Kg0 == Kg0 && it->dtype == dtype &&
+        it->offsets.size() == static_cast<size_t>(L + 1) &&
+        std::memcmp(it->offsets.data(), offs, sizeof(int64_t) * (L + 1)) == 0) {
+      ws.plans.splice(ws.plans.begin(), ws.plans, it);
+      *out = &ws.plans.front();
+      return ADASUM_OK;
+    }
+  }
+  int num_sms = 148;
+  cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, ws.device);
+  const int64_t N = offs[L];
+  const int64_t T = tile_positions(Kg0, dtype, N, num_sms);
+  std::vector<TileDesc> tiles;
+  std::vector<SegDesc> segs(L);
+  std::vector<ChunkDesc> chunks;
+  for (int s = 0; s < L; ++s) {
+    const int64_t lo = offs[s], hi = offs[s + 1];
+    segs[s].start = lo;
+    segs[s].len = hi - lo;
+    segs[s].first_tile = static_cast<int32_t>(tiles.size());
+    if (hi > lo) {
+      const int64_t base = lo / 32 * 32;
+      for (int64_t b = base; b < hi; b += T) {
+        const int64_t t0 = std::max(lo, b), t1 = std::min(hi, b + T);
+        if (t1 <= t0) continue;
+        tiles.push_back(TileDesc{t0, static_cast<int32_t>(t1 - t0), s});
+      }
+    }
+    segs[s].ntiles = static_cast<int32_t>(tiles.size()) - segs[s].first_tile;
+    segs[s].first_chunk = static_cast<int32_t>(chunks.size());
+    for (int32_t t = 0; t < segs[s].ntiles; t += kChunkTiles)
+      chunks.push_back(ChunkDesc{segs[s].first_tile + t, std::min(kChunkTiles, segs[s].ntiles - t)});
+    segs[s].nchunks = static_cast<int32_t>(chunks.size()) - segs[s].first_chunk;
+  }
+  if (tiles.size() > static_cast<size_t>(INT32_MAX)) return ADASUM_ERR_UNSUPPORTED;
+  if (ws.plans.size() >= 8) {
+    free_plan(ws.plans.back());
+    ws.plans.pop_back();
+  }
+  Plan p;
+  p.offsets.assign(offs, offs + L + 1);
+  p.Kg0 = Kg0;
+  p.dtype = dtype;
+  p.ntiles = static_cast<int>(tiles.size());
+  p.nsegs = L;
+  p.nchunks = static_cast<int>(chunks.size());
+  if (cudaMalloc(&p.d_tiles, std::max<size_t>(1, tiles.size()) * sizeof(TileDesc)) != cudaSuccess ||
+      cudaMalloc(&p.d_segs, std::max<size_t>(1, segs.size()) * sizeof(SegDesc)) != cudaSuccess ||
+      cudaMalloc(&p.d_chunks, std::max<size_t>(1, chunks.size()) * sizeof(ChunkDesc)) != cudaSuccess) {
+    free_plan(p);
+    cudaGetLastError();
+    return ADASUM_ERR_NO_MEMORY;
+  }
+  // Synchronous copies: the plan is immutable once built, so no later call can race
+  // with them.  A new plan is built only for offsets not seen among the last eight.
+  if (cudaMemcpy(p.d_tiles, tiles.data(), tiles.size() * sizeof(TileDesc),
+                 cudaMemcpyHostToDevice) != cudaSuccess ||
+      cudaMemcpy(p.d_segs, segs.data(), segs.size() * sizeof(SegDesc),
+                 cudaMemcpyHostToDevice) != cudaSuccess ||
+      cudaMemcpy(p.d_chunks, chunks.data(), chunks.size() * sizeof(ChunkDesc),
+                 cudaMemcpyHostToDevice) != cudaSuccess) {
+    free_plan(p);
+    cudaGetLastError();
+    return ADASUM_ERR_CUDA;
+  }
+  ws.plans.push_front(std::move(p));
+  *out = &ws.plans.front();
+  return ADASUM_OK;
+}
+
+adasum_status_t ensure_capacity(Workspace& ws, size_t bytes) {
+  if (bytes <= ws.cap) return ADASUM_OK;
+  if (ws.buf) {
+    cudaDeviceSynchronize();  // earlier calls may still use the old buffer
+    cudaFree(ws.buf);
+    ws.buf = nullptr;
+    ws.cap = 0;
+    ws.last_flag_counts = nullptr;
+  }
+  const size_t rounded = (bytes + (size_t(1) << 21) - 1) & ~((size_t(1) << 21) - 1);
+  if (cudaMalloc(&ws.buf, rounded) != cudaSuccess) {
+    cudaGetLastError();
+    ws.buf = nullptr;
+    return ADASUM_ERR_NO_MEMORY;
+  }
+  ws.cap = rounded;
+  return ADASUM_OK;
+}
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Host-side fault injection for the error-path tests: ADASUM_FAULT_INJECT=alloc makes
+// the next workspace growth fail as if cudaMalloc had.
+bool inject_alloc_failure() {
+  const char* v = std::getenv("ADASUM_FAULT_INJECT");
+  return v != nullptr && std::strcmp(v, "alloc") == 0;
+}
+
+int record_launch(int rc, const char* name, cudaEvent_t start, cudaStream_t stream) {
+  if (rc != 0) return rc;
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  if (g_profiling && start) {
+    cudaEvent_t stop = pool_event();
+    cudaEventRecord(stop, stream);
+    g_prof_pending.push_back(ProfRecord{name, start, stop});
+  }
+  return 0;
+}
+
+cudaEvent_t maybe_start(cudaStream_t stream) {
+  if (!g_profiling) return nullptr;
+  cudaEvent_t e = pool_event();
+  cudaEventRecord(e, stream);
+  return e;
+}
+
+// Launch wrapper: counts launches and, when profiling, brackets them with events.
+template <typename F>
+adasum_status_t launch_one(cudaStream_t stream, F&& f) {
+  const char* name = "";
+  cudaEvent_t e = maybe_start(stream);
+  const int rc = f(&name);
+  return record_launch(rc, name, e, stream) ? ADASUM_ERR_CUDA : ADASUM_OK;
+}
+
+// fp32 pass of one stage (all groups): Gram partials, chunk sums, coefficients with the
+// conditioning check, combine (flagged segments are skipped and left to the fp64 path).
+adasum_status_t run_stage(StageArgs& a, int in_dtype, int out_dtype, int momentum,
+                          cudaStream_t stream) {
+  if (a.Kg > 1) {
+    if (adasum_status_t st = launch_one(stream, [&](const char** n) {
+          return in_dtype == kBF16 ? launch_gram_bf16(a, stream, n) : launch_gram_f32(a, stream, n);
+        }))
+      return st;
+    if (adasum_status_t st = launch_one(stream, [&](const char** n) {
+          return launch_reduce_chunks(a, stream, n);
+        }))
+      return st;
+    if (adasum_status_t st = launch_one(stream, [&](const char** n) { return launch_coef(a, stream, n); }))
+      return st;
+  }
+  return launch_one(stream, [&](const char** n) {
+    return in_dtype == kBF16 ? launch_combine_bf16in(a, out_dtype, momentum, stream, n)
+                             : launch_combine_f32in(a, out_dtype, momentum, stream, n);
+  });
+}
+
+// fp64 pass of one stage over the flagged lists.
+adasum_status_t run_stage64(StageArgs& a, int in_dtype, int out_dtype, int momentum, int grid,
+                            cudaStream_t stream) {
+  if (a.Kg > 1) {
+    if (adasum_status_t st = launch_one(stream, [&](const char** n) {
+          return launch_gram64(a, in_dtype, grid, stream, n);
+        }))
+      return st;
+    if (adasum_status_t st = launch_one(stream, [&](const char** n) {
+          return launch_coef64(a, grid, stream, n);
+        }))
+      return st;
+  }
+  return launch_one(stream, [&](const char** n) {
+    return launch_combine64(a, in_dtype, out_dtype, momentum, grid, stream, n);
+  });
+}
+
+// Carves the workspace: returns the byte offset of a region of `bytes` and advances.
+struct Carver {
+  size_t off = 0;
+  size_t take(size_t bytes) {
+    const size_t at = off;
+    off = align_up(off + bytes, 256);
+    return at;
+  }
+};
+
+adasum_status_t reduce_impl(const void* const* grads, int K, const int64_t* offs, int L,
+                            int dtype, void* out, float* master_w, float* momentum,
+                            float lr, float mu, cudaStream_t stream) {
+  const bool mom = master_w != nullptr;
+  if (dtype != kF32 && dtype != kBF16) return ADASUM_ERR_INVALID_ARG;
+  if (L < 0 || (L > 0 && offs == nullptr) || K < 1 || grads == nullptr)
+    return ADASUM_ERR_INVALID_ARG;
+  if (K > ADASUM_MAX_K || (K & (K - 1)) != 0) return ADASUM_ERR_UNSUPPORTED;
+  if (L == 0) return ADASUM_OK;
+  if (offs[0] != 0) return ADASUM_ERR_INVALID_ARG;
+  for (int s = 0; s < L; ++s)
+    if (offs[s + 1] < offs[s]) return ADASUM_ERR_INVALID_ARG;
+  const int64_t N = offs[L];
+  if (N == 0) return ADASUM_OK;
+  if (!mom && out == nullptr) return ADASUM_ERR_INVALID_ARG;
+  if (mom && momentum == nullptr) return ADASUM_ERR_INVALID_ARG;
+  for (int k = 0; k < K; ++k)
+    if (grads[k] == nullptr) return ADASUM_ERR_INVALID_ARG;
+
+  const size_t es = elem_size(dtype);
+  const size_t nbytes = static_cast<size_t>(N) * es;
+  if (out) {
+    for (int k = 0; k < K; ++k)
+      if (out != grads[k] && overlaps(out, nbytes, grads[k], nbytes)) return ADASUM_ERR_ALIAS;
+  }
+  if (mom) {
+    const size_t fb = static_cast<size_t>(N) * sizeof(float);
+    if (overlaps(master_w, fb, momentum, fb)) return ADASUM_ERR_ALIAS;
+    for (int k = 0; k < K; ++k)
+      if (overlaps(master_w, fb, grads[k], nbytes) || overlaps(momentum, fb, grads[k], nbytes))
+        return ADASUM_ERR_ALIAS;
+    if (out && (overlaps(master_w, fb, out, nbytes) || overlaps(momentum, fb, out, nbytes)))
+      return ADASUM_ERR_ALIAS;
+  }
+  if (!mom && K == 1 && out == grads[0]) return ADASUM_OK;  // in-place copy of one input
+
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess) {
+    cudaGetLastError();
+    return ADASUM_ERR_CUDA;
+  }
+  Workspace& ws = workspace_for(device);
+  int num_sms = 148;
+  cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, device);
+
+  // Stage structure: groups of at most 16 workers; K=1 is a single pass-2 "copy".
+  std::vector<int> kg;  // workers per group, per stage
+  for (int rem = K; rem > 1;) {
+    const int g = std::min(rem, kMaxGroup);
+    kg.push_back(g);
+    rem /= g;
+  }
+  if (kg.empty()) kg.push_back(1);
+  std::vector<int> groups(kg.size());
+  {
+    int rem = K;
+    for (size_t s = 0; s < kg.size(); ++s) {
+      rem /= kg[s];
+      groups[s] = rem;
+    }
+  }
+
+  Plan* plan = nullptr;
+  if (adasum_status_t st = get_plan(ws, offs, L, kg[0], dtype, &plan)) return st;
+
+  // Workspace layout.
+  size_t max_e_tiles = 0, max_e_chunks = 0, max_coef = 0, max_g = 1;
+  for (size_t s = 0; s < kg.size(); ++s) {
+    const size_t E = static_cast<size_t>(kg[s]) * (kg[s] + 1) / 2;
+    max_e_tiles = std::max(max_e_tiles, groups[s] * plan->ntiles * E);
+    max_e_chunks = std::max(max_e_chunks, groups[s] * plan->nchunks * E);
+    max_coef = std::max(max_coef, static_cast<size_t>(groups[s]) * L * kg[s]);
+    max_g = std::max(max_g, static_cast<size_t>(groups[s]));
+  }
+  const size_t inter32 = align_up(static_cast<size_t>(N) * sizeof(float), 256);
+  const size_t inter64 = align_up(static_cast<size_t>(N) * sizeof(double), 256);
+  Carver cv;
+  const size_t o_flags = cv.take((static_cast<size_t>(L) + 3) * sizeof(int));  // flags + 3 counters
+  const size_t o_part = cv.take(max_e_tiles * sizeof(float));
+  const size_t o_chunk = cv.take(max_e_chunks * sizeof(double));
+  const size_t o_coef = cv.take(max_coef * sizeof(float));
+  const size_t o_rel0 = cv.take(max_g * L * sizeof(float));
+  const size_t o_rel1 = cv.take(max_g * L * sizeof(float));
+  const size_t o_part64 = cv.take(max_e_tiles * sizeof(double));
+  const size_t o_coef64 = cv.take(max_coef * sizeof(double));
+  const size_t o_ltiles = cv.take(static_cast<size_t>(plan->ntiles) * sizeof(int));
+  const size_t o_lsegs = cv.take(static_cast<size_t>(L) * sizeof(int));
+  const size_t o_ltiny = cv.take(static_cast<size_t>(L) * sizeof(int));
+  // Stage outputs of every non-final stage: fp32 (fast pass) and fp64 (recompute).
+  std::vector<size_t> off32(kg.size(), 0), off64(kg.size(), 0);
+  for (size_t s = 0; s + 1 < kg.size(); ++s) {
+    off32[s] = cv.take(groups[s] * inter32);
+    off64[s] = cv.take(groups[s] * inter64);
+  }
+  const size_t total = cv.off;
+  if (total > ws.cap && inject_alloc_failure()) return ADASUM_ERR_NO_MEMORY;
+  if (adasum_status_t st = ensure_capacity(ws, total)) return st;
+  char* base = static_cast<char*>(ws.buf);
+  int* seg_flag = reinterpret_cast<int*>(base + o_flags);
+  int* list_count = seg_flag + L;
+
+  bool all_aligned = aligned16(out) && (!mom || (aligned16(master_w) && aligned16(momentum)));
+  for (int k = 0; k < K; ++k) all_aligned = all_aligned && aligned16(grads[k]);
+
+  if (cudaMemsetAsync(seg_flag, 0, (static_cast<size_t>(L) + 3) * sizeof(int), stream) != cudaSuccess)
+    return ADASUM_ERR_CUDA;
+
+  auto make_args = [&](size_t s) {
+    StageArgs a;
+    std::memset(&a, 0, sizeof a);
+    a.Kg = kg[s];
+    a.G = groups[s];
+    a.aligned = all_aligned ? 1 : 0;
+    a.ntiles = plan->ntiles;
+    a.nsegs = plan->nsegs;
+    a.nchunks = plan->nchunks;
+    a.tiles = plan->d_tiles;
+    a.segs = plan->d_segs;
+    a.chunks = plan->d_chunks;
+    a.partials = reinterpret_cast<float*>(base + o_part);
+    a.chunk_sums = reinterpret_cast<double*>(base + o_chunk);
+    a.coef = reinterpret_cast<float*>(base + o_coef);
+    a.seg_flag = seg_flag;
+    a.partials64 = reinterpret_cast<double*>(base + o_part64);
+    a.coef64 = reinterpret_cast<double*>(base + o_coef64);
+    a.list_tiles = reinterpret_cast<int*>(base + o_ltiles);
+    a.list_segs = reinterpret_cast<int*>(base + o_lsegs);
+    a.list_tiny = reinterpret_cast<int*>(base + o_ltiny);
+    a.list_count = list_count;
+    a.Ktotal = K;
+    const bool last = s + 1 == kg.size();
+    if (last && mom) {
+      a.master_w = master_w;
+      a.momentum = momentum;
+      a.lr = lr;
+      a.mu = mu;
+    }
+    return a;
+  };
+
+  // fp32 pass, stage by stage.
+  for (size_t s = 0; s < kg.size(); ++s) {
+    const bool last = s + 1 == kg.size();
+    StageArgs a = make_args(s);
+    if (s == 0) {
+      for (int k = 0; k < K; ++k) a.in[k] = grads[k];
+    } else {
+      for (int i = 0; i < groups[s] * kg[s]; ++i) a.in[i] = base + off32[s - 1] + i * inter32;
+      a.in_relerr = reinterpret_cast<float*>(base + ((s - 1) % 2 ? o_rel1 : o_rel0));
+    }
+    if (last) {
+      a.out[0] = out;
+    } else {
+      for (int q = 0; q < groups[s]; ++q) a.out[q] = base + off32[s] + q * inter32;
+    }
+    a.relerr = reinterpret_cast<float*>(base + (s % 2 ? o_rel1 : o_rel0));
+    a.skip_flagged = 1;
+    const int in_dt = s == 0 ? dtype : kF32;
+    const int out_dt = last ? dtype : kF32;
+    if (adasum_status_t st = run_stage(a, in_dt, out_dt, (last && mom) ? 1 : 0, stream)) return st;
+  }
+
+  // fp64 recompute of the flagged segments (usually none: every kernel returns at once).
+  const int grid64 = std::max(1, std::min(plan->ntiles, 2 * num_sms));
+  {
+    StageArgs a = make_args(0);
+    if (adasum_status_t st = launch_one(stream, [&](const char** n) {
+          return launch_collect(a, std::max(1, std::min((L + kThreads - 1) / kThreads, 4 * num_sms)),
+                                stream, n);
+        }))
+      return st;
+  }
+  {
+    // flagged segments of at most kTinySeg positions: the whole tree, vector space
+    StageArgs a = make_args(kg.size() - 1);
+    for (int k = 0; k < K; ++k) a.in[k] = grads[k];
+    a.out[0] = out;
+    if (adasum_status_t st = launch_one(stream, [&](const char** n) {
+          return launch_tiny64(a, dtype, dtype, mom ? 1 : 0, grid64, stream, n);
+        }))
+      return st;
+  }
+  for (size_t s = 0; s < kg.size(); ++s) {
+    const bool last = s + 1 == kg.size();
+    StageArgs a = make_args(s);
+    if (s == 0) {
+      for (int k = 0; k < K; ++k) a.in[k] = grads[k];
+    } else {
+      for (int i = 0; i < groups[s] * kg[s]; ++i)
+        a.in[i] = base + off64[s - 1] + i * inter64;
+      a.in_f64 = 1;
+    }
+    if (last) {
+      a.out[0] = out;
+    } else {
+      for (int q = 0; q < groups[s]; ++q)
+        a.out[q] = base + off64[s] + q * inter64;
+      a.out_f64 = 1;
+    }
+    const int in_dt = s == 0 ? dtype : kF32;
+    const int out_dt = last ? dtype : kF32;
+    if (adasum_status_t st = run_stage64(a, in_dt, out_dt, (last && mom) ? 1 : 0, grid64, stream))
+      return st;
+  }
+  ws.last_flag_counts = list_count;
+  return ADASUM_OK;
+}
+
+}  // namespace
+}  // namespace adasum
+
+using namespace adasum;
+
+extern "C" {
+
+adasum_status_t adasum_reduce(const void* const* grads, int K, const int64_t* seg_offsets,
+                              int L, adasum_dtype_t dtype, void* out,
+                              adasum_stream_t stream) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  return reduce_impl(grads, K, seg_offsets, L, static_cast<int>(dtype), out, nullptr,
+                     nullptr, 0.f, 0.f, reinterpret_cast<cudaStream_t>(stream));
+}
+
+adasum_status_t adasum_pair(const void* a, const void* b, int64_t n, adasum_dtype_t dtype,
+                            void* out, adasum_stream_t stream) {
+  if (n < 0 || a == nullptr || b == nullptr) return ADASUM_ERR_INVALID_ARG;
+  const void* g[2] = {a, b};
+  const int64_t offs[2] = {0, n};
+  std::lock_guard<std::mutex> lock(g_mu);
+  return reduce_impl(g, 2, offs, 1, static_cast<int>(dtype), out, nullptr, nullptr, 0.f,
+                     0.f, reinterpret_cast<cudaStream_t>(stream));
+}
+
+adasum_status_t adasum_reduce_momentum_sgd(const void* const* grads, int K,
+                                           const int64_t* seg_offsets, int L,
+                                           adasum_dtype_t grad_dtype, float* master_w,
+                                           float* momentum, float lr, float mu,
+                                           void* out_or_null, adasum_stream_t stream) {
+  if (master_w == nullptr || momentum == nullptr) {
+    // Nothing to update is only fine when there is nothing at all to do.
+    if (L > 0 && seg_offsets != nullptr && seg_offsets[L] > 0) return ADASUM_ERR_INVALID_ARG;
+  }
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (master_w == nullptr) return ADASUM_OK;
+  return reduce_impl(grads, K, seg_offsets, L, static_cast<int>(grad_dtype), out_or_null,
+                     master_w, momentum, lr, mu, reinterpret_cast<cudaStream_t>(stream));
+}
+
+adasum_status_t adasum_get_last_error(void) {
+  // The current kernels contain no bounded waits, so no device-side status exists yet;
+  // report any sticky CUDA error instead.
+  std::lock_guard<std::mutex> lock(g_mu);
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? ADASUM_OK : ADASUM_ERR_CUDA;
+}
+
+const char* adasum_status_string(adasum_status_t s) {
+  switch (s) {
+    case ADASUM_OK: return "ADASUM_OK";
+    case ADASUM_ERR_INVALID_ARG: return "ADASUM_ERR_INVALID_ARG";
+    case ADASUM_ERR_UNSUPPORTED: return "ADASUM_ERR_UNSUPPORTED";
+    case ADASUM_ERR_ALIAS: return "ADASUM_ERR_ALIAS";
+    case ADASUM_ERR_NO_MEMORY: return "ADASUM_ERR_NO_MEMORY";
+    case ADASUM_ERR_CUDA: return "ADASUM_ERR_CUDA";
+    case ADASUM_ERR_TIMEOUT: return "ADASUM_ERR_TIMEOUT";
+  }
+  return "ADASUM_ERR_UNKNOWN";
+}
+
+adasum_status_t adasum_release_workspace(void) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess) return ADASUM_ERR_CUDA;
+  Workspace& ws = workspace_for(device);
+  if (cudaDeviceSynchronize() != cudaSuccess) return ADASUM_ERR_CUDA;
+  if (ws.buf) cudaFree(ws.buf);
+  ws.buf = nullptr;
+  ws.cap = 0;
+  ws.last_flag_counts = nullptr;
+  for (auto& p : ws.plans) free_plan(p);
+  ws.plans.clear();
+  return ADASUM_OK;
+}
+
+int adasum_version(void) { return kVersion; }
+
+int64_t adasum_recomputed_segments(void) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess) return -1;
+  Workspace& ws = workspace_for(device);
+  if (ws.last_flag_counts == nullptr) return 0;
+  int counts[3] = {0, 0, 0};
+  if (cudaDeviceSynchronize() != cudaSuccess ||
+      cudaMemcpy(counts, ws.last_flag_counts, sizeof counts, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return -1;
+  return static_cast<int64_t>(counts[1]) + counts[2];
+}
+
+int64_t adasum_launch_count(void) { return g_launches.load(); }
+
+adasum_status_t adasum_profile_enable(int on) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  g_profiling = on != 0;
+  return ADASUM_OK;
+}
+
+int adasum_profile_collect(adasum_kernel_stat_t* stats, int max_stats) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  std::vector<adasum_kernel_stat_t> agg;
+  for (auto& r : g_prof_pending) {
+    float ms = 0.f;
+    cudaEventSynchronize(r.stop);
+    cudaEventElapsedTime(&ms, r.start, r.stop);
+    adasum_kernel_stat_t* slot = nullptr;
+    for (auto& s : agg)
+      if (std::strncmp(s.name, r.name, sizeof s.name) == 0) slot = &s;
+    if (!slot) {
+      agg.push_back(adasum_kernel_stat_t{});
+      slot = &agg.back();
+      std::strncpy(slot->name, r.name, sizeof slot->name - 1);
+    }
+    slot->launches += 1;
+    slot->total_ms += ms;
+    g_event_pool.push_back(r.start);
+    g_event_pool.push_back(r.stop);
+  }
+  g_prof_pending.clear();
+  const int n = std::min<int>(max_stats, static_cast<int>(agg.size()));
+  for (int i = 0; i < n; ++i) stats[i] = agg[i];
+  return static_cast<int>(agg.size());
+}
+
+}  // extern "C"

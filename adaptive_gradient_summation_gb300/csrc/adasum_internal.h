@@ -1,0 +1,127 @@
+// adasum_internal.h -- declarations shared by the host side (adasum_api.cu) and the
+// kernel translation units of the GB300 Adasum library.  Not part of the public ABI.
+//
+// Method ("Scaling Distributed Training with Adaptive Summation", Section 3): per layer
+// segment, K worker gradients are combined by a binary tree of the pair operator
+//     Adasum(a, b) = (1 - a.b/(2|a|^2)) a + (1 - a.b/(2|b|^2)) b.
+// Every node of the tree is a linear combination of the leaves, so the whole tree
+// result is  out = sum_k c_k g_k,  and every dot product the tree needs is a quadratic
+// form in the segment's Gram matrix G_ij = g_i . g_j.  The library therefore runs
+//   pass 1  Gram partials per tile          (one read of the K inputs)
+//   coef    per segment: reduce partials, run the tree on G in fp64 -> c_0..c_{K-1}
+//   pass 2  out = sum_k c_k g_k per tile     (second read of the K inputs, one write)
+// which is the same tree, in the same order, evaluated in coefficient space.  Groups
+// of at most 16 workers form one stage; larger K runs stages of 16-leaf subtrees whose
+// fp32 results feed the next stage (the tree's top levels).
+#pragma once
+
+#include <cstdint>
+
+namespace adasum {
+
+constexpr int kMaxK = 256;        // largest worker count accepted
+constexpr int kMaxGroup = 16;     // workers combined in one Gram stage
+constexpr int kThreads = 256;     // threads per CTA of the tile kernels
+
+enum Dtype : int { kF32 = 0, kBF16 = 1 };
+
+// One tile: a contiguous run of positions inside one segment.
+struct TileDesc {
+  int64_t start;   // first position (absolute index into the flat gradient)
+  int32_t len;     // positions in the tile (> 0)
+  int32_t seg;     // owning segment
+};
+
+// One segment (layer) of the flat gradient.
+struct SegDesc {
+  int64_t start;
+  int64_t len;
+  int32_t first_tile;   // index of its first tile
+  int32_t ntiles;       // 0 for an empty segment
+  int32_t first_chunk;  // its tiles' partial Gram matrices are summed in chunks
+  int32_t nchunks;
+};
+
+// A run of at most kChunkTiles consecutive tiles of one segment.
+struct ChunkDesc {
+  int32_t first_tile;
+  int32_t ntiles;
+};
+constexpr int kChunkTiles = 32;
+
+// Arguments of one stage: G independent groups of Kg workers each, over the same
+// segments and tiles.  Group q reads in[q*Kg + k], k < Kg, and writes out[q].
+struct StageArgs {
+  const void* in[kMaxK];
+  void* out[kMaxK / kMaxGroup];
+  int Kg;          // workers per group: 1, 2, 4, 8 or 16
+  int G;           // groups
+  int aligned;     // every in/out pointer is 16-byte aligned
+  int ntiles;
+  int nsegs;
+  int nchunks;
+  const TileDesc* tiles;
+  const SegDesc* segs;
+  const ChunkDesc* chunks;
+  float* partials;   // [G][ntiles][E] Gram partials, E = Kg(Kg+1)/2 (upper triangle)
+  double* chunk_sums; // [G][nchunks][E] compensated sums of the partials of each chunk
+  float* coef;       // [G][nsegs][Kg] tree coefficients
+  // Fused heavy-ball step (final stage of adasum_reduce_momentum_sgd only).
+  float* master_w;
+  float* momentum;
+  float lr;
+  float mu;
+
+  // Conditioning check and fp64 recompute (see coef_kernel).
+  int* seg_flag;              // [nsegs] 1: the segment is recomputed in fp64
+  float* relerr;              // [G][nsegs] estimated relative error of this stage's output
+  const float* in_relerr;     // [G*Kg][nsegs] same, of this stage's inputs (null = exact)
+  int skip_flagged;           // combine: leave flagged segments to the fp64 path
+
+  // fp64 path (only the segments listed by collect_kernel).
+  double* partials64;         // [G][ntiles][E]
+  double* coef64;             // [G][nsegs][Kg]
+  int* list_tiles;            // flagged tiles, list_count[0] of them
+  int* list_segs;             // flagged segments, list_count[1] of them
+  int* list_tiny;             // flagged segments of at most kTinySeg positions, list_count[2]
+  int* list_count;            // [3]
+  int Ktotal;                 // all workers (the tiny-segment recompute runs the whole tree)
+  int in_f64;                 // stage inputs are fp64 intermediates
+  int out_f64;                // stage outputs are fp64 intermediates
+};
+
+// Gram-entry error model of the fp32 pass, relative to |g_i| |g_j|: products and
+// bounded-length fp32 sums, then compensated sums (a typical-case constant).
+constexpr double kGramRelErr = 4.0 * 5.9604644775390625e-08;   // 4 u, u = 2^-24
+// Estimated relative output error above which a segment is recomputed in fp64.  The
+// estimate is a conservative first-order bound: over random, correlated and nearly
+// cancelling test sets the realised error of the fp32 pass stayed below 0.16 times it,
+// so an estimate of 2.5e-5 keeps the realised error below 4e-6.
+constexpr double kRelErrBudget = 2.5e-5;
+// Flagged segments of at most this many positions are recomputed in vector space (the
+// tree level by level on the values themselves, one warp per segment): there, nodes can
+// cancel almost exactly, which a Gram-matrix quadratic form cannot follow even in fp64.
+constexpr int kTinySeg = 32;
+
+// Launchers, one translation unit per input element type (compiled in parallel).
+// Each enqueues one kernel on `stream` and returns its cudaError_t as int (0 = ok);
+// `name` receives a static string naming the kernel, for the optional profiler.
+int launch_gram_f32(const StageArgs& a, void* stream, const char** name);
+int launch_gram_bf16(const StageArgs& a, void* stream, const char** name);
+int launch_coef(const StageArgs& a, void* stream, const char** name);
+int launch_combine_f32in(const StageArgs& a, int out_dtype, int momentum, void* stream,
+                         const char** name);
+int launch_combine_bf16in(const StageArgs& a, int out_dtype, int momentum, void* stream,
+                          const char** name);
+// Partial-Gram chunk sums (segments with many tiles), then coefficients.
+int launch_reduce_chunks(const StageArgs& a, void* stream, const char** name);
+// fp64 path: build the flagged lists, then Gram / coefficients / combine over them.
+int launch_collect(const StageArgs& a, int grid, void* stream, const char** name);
+int launch_tiny64(const StageArgs& a, int in_dtype, int out_dtype, int momentum, int grid,
+                  void* stream, const char** name);
+int launch_gram64(const StageArgs& a, int in_dtype, int grid, void* stream, const char** name);
+int launch_coef64(const StageArgs& a, int grid, void* stream, const char** name);
+int launch_combine64(const StageArgs& a, int in_dtype, int out_dtype, int momentum, int grid,
+                     void* stream, const char** name);
+
+}  // namespace adasum

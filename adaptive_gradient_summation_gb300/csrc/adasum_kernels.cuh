@@ -1,0 +1,810 @@
+// adasum_kernels.cuh -- device code of the GB300 Adasum library (sm_103a).
+//
+// "Scaling Distributed Training with Adaptive Summation", Section 3: per layer segment,
+// the K worker gradients are combined by a binary tree of
+//     Adasum(a, b) = (1 - a.b/(2|a|^2)) a + (1 - a.b/(2|b|^2)) b,
+// pairs (2i, 2i+1) at every level.  The tree is linear in the leaves, so its result is
+// out = sum_k c_k g_k, and every dot product it needs is a quadratic form of the
+// segment's Gram matrix.  The kernels here are:
+//   gram_*     pass 1: Gram partials of one tile (upper triangle, fp32), one HBM read
+//   coef       per segment: sum the tile partials (compensated fp32, fixed order), run
+//              the tree on the Gram matrix in fp64, emit c_0..c_{K-1}
+//   combine    pass 2: out = sum_k c_k g_k, evaluated as a pairwise tree that mirrors
+//              the Adasum tree (so swapping sibling subtrees is bitwise symmetric),
+//              optionally followed by a heavy-ball Momentum-SGD step
+// This path is HBM-bound (a few FMAs per byte), so it is written around coalesced
+// 128-bit loads and a grid of tiles that keeps every SM streaming.  The bf16 Gram uses
+// the tensor cores through mma.sync: bf16 x bf16 products are exact in fp32, and the
+// 16x16 Gram of a 16-worker group is a true (tiny) dense contraction.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "adasum_internal.h"
+
+namespace adasum {
+
+constexpr int kWarps = kThreads / 32;
+
+__host__ __device__ constexpr int tri_count(int K) { return K * (K + 1) / 2; }
+// Row-major index of (i, j), i <= j, in the packed upper triangle of a K x K matrix.
+__host__ __device__ constexpr int tri_index(int K, int i, int j) {
+  return i * K - (i * (i - 1)) / 2 + (j - i);
+}
+
+// ------------------------------------------------------------------ element access
+
+struct F32Tag {};
+struct BF16Tag {};
+
+template <typename Tag> struct ElemTraits;
+template <> struct ElemTraits<F32Tag> {
+  using Storage = float;
+  static constexpr int kVW = 4;  // elements per 16-byte vector
+};
+template <> struct ElemTraits<BF16Tag> {
+  using Storage = uint16_t;
+  static constexpr int kVW = 8;
+};
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t h) {
+  return __uint_as_float(static_cast<uint32_t>(h) << 16);
+}
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);  // round to nearest even
+  return *reinterpret_cast<uint32_t*>(&p);
+}
+__device__ __forceinline__ uint16_t float_to_bf16_bits(float x) {
+  __nv_bfloat16 h = __float2bfloat16_rn(x);
+  return *reinterpret_cast<uint16_t*>(&h);
+}
+
+// Cache policies: pass 1 reads through the non-coherent path without allocating in L1;
+// pass 2 reads and writes with the streaming (evict-first) policy because nothing is
+// reused after it.
+enum LoadPolicy { kLoadKeep = 0, kLoadStream = 1 };
+
+template <int P>
+__device__ __forceinline__ uint4 ld16(const void* p) {
+  if constexpr (P == kLoadStream) {
+    return __ldcs(reinterpret_cast<const uint4*>(p));
+  } else {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+  }
+}
+
+// The raw 16-byte vector v (elements [v*VW, v*VW + VW)) of a gradient, with every
+// element outside [lo, hi) replaced by +0.  Positions outside [lo, hi) are never
+// dereferenced, so partial vectors at buffer ends stay in bounds.
+template <typename Tag, int P>
+__device__ __forceinline__ uint4 load_vec_raw(const typename ElemTraits<Tag>::Storage* x,
+                                              int64_t v, int64_t lo, int64_t hi,
+                                              bool aligned) {
+  constexpr int VW = ElemTraits<Tag>::kVW;
+  const int64_t p0 = v * VW;
+  if (aligned && p0 >= lo && p0 + VW <= hi) return ld16<P>(x + p0);
+  uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+  for (int e = 0; e < VW; ++e) {
+    const int64_t p = p0 + e;
+    if (p >= lo && p < hi) {
+      if constexpr (VW == 4) {
+        w[e] = __float_as_uint(x[p]);
+      } else {
+        const uint32_t h = static_cast<uint32_t>(x[p]);
+        w[e >> 1] |= (e & 1) ? (h << 16) : h;
+      }
+    }
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Element e (0..VW-1) of a raw vector, widened to fp32.
+template <typename Tag>
+__device__ __forceinline__ float vec_elem(const uint4& r, int e) {
+  const uint32_t w = (e >> (ElemTraits<Tag>::kVW == 8 ? 1 : 0)) == 0   ? r.x
+                     : (e >> (ElemTraits<Tag>::kVW == 8 ? 1 : 0)) == 1 ? r.y
+                     : (e >> (ElemTraits<Tag>::kVW == 8 ? 1 : 0)) == 2 ? r.z
+                                                                         : r.w;
+  if constexpr (ElemTraits<Tag>::kVW == 4) {
+    return __uint_as_float(w);
+  } else {
+    return (e & 1) ? bf16_hi(w) : bf16_lo(w);
+  }
+}
+
+// Kahan-compensated fp32 accumulation: sum - comp tracks the exact running sum to
+// about one rounding, whatever the number of terms.
+__device__ __forceinline__ void kahan_add(float& sum, float& comp, float x) {
+  const float y = __fsub_rn(x, comp);
+  const float t = __fadd_rn(sum, y);
+  comp = __fsub_rn(__fsub_rn(t, sum), y);
+  sum = t;
+}
+
+// ------------------------------------------------------------- pass 1: Gram (SIMT)
+
+// Sum E per-thread values over the CTA in a fixed order (butterfly within a warp, then
+// warps in index order) and write them to dst[0..E).  fp32 throughout: each per-thread
+// value already covers a bounded run of products.
+template <int E>
+__device__ __forceinline__ void block_reduce_store(float (&acc)[E], float* __restrict__ dst) {
+  __shared__ float red[kWarps][E];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    float v = acc[e];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, off));
+    if (lane == 0) red[warp][e] = v;
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += kThreads) {
+    float s = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) s = __fadd_rn(s, red[w][e]);
+    dst[e] = s;
+  }
+}
+
+// Gram partial of one tile with CUDA-core FMAs: every thread owns whole 16-byte
+// vectors (VW positions of all Kg workers) and accumulates the Kg(Kg+1)/2 products.
+template <typename Tag, int KG>
+__global__ void __launch_bounds__(kThreads) gram_simt_kernel(const StageArgs a) {
+  using S = typename ElemTraits<Tag>::Storage;
+  constexpr int VW = ElemTraits<Tag>::kVW;
+  constexpr int E = tri_count(KG);
+  const int tile_id = blockIdx.x, q = blockIdx.y;
+  const TileDesc t = a.tiles[tile_id];
+  const S* x[KG];
+#pragma unroll
+  for (int k = 0; k < KG; ++k) x[k] = static_cast<const S*>(a.in[q * KG + k]);
+  const bool aligned = a.aligned != 0;
+  const int64_t lo = t.start, hi = t.start + t.len;
+  const int64_t v0 = lo / VW, v1 = (hi + VW - 1) / VW;
+
+  float acc[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) acc[e] = 0.f;
+
+  for (int64_t v = v0 + threadIdx.x; v < v1; v += kThreads) {
+    uint4 r[KG];
+#pragma unroll
+    for (int k = 0; k < KG; ++k) r[k] = load_vec_raw<Tag, kLoadKeep>(x[k], v, lo, hi, aligned);
+#pragma unroll
+    for (int e = 0; e < VW; ++e) {
+      float xe[KG];
+#pragma unroll
+      for (int k = 0; k < KG; ++k) xe[k] = vec_elem<Tag>(r[k], e);
+#pragma unroll
+      for (int i = 0; i < KG; ++i)
+#pragma unroll
+        for (int j = i; j < KG; ++j)
+          acc[tri_index(KG, i, j)] = __fmaf_rn(xe[i], xe[j], acc[tri_index(KG, i, j)]);
+    }
+  }
+  block_reduce_store<E>(acc, a.partials + (static_cast<size_t>(q) * a.ntiles + tile_id) * E);
+}
+
+// --------------------------------------------------- pass 1: Gram (tensor cores, bf16)
+
+// D += A * B for one m16n8k16 bf16 tile with fp32 accumulation.
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
+                                               uint32_t a2, uint32_t a3, uint32_t b0,
+                                               uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Gram partial of one tile of bf16 gradients on the tensor cores (Kg = 8 or 16).
+//
+// A warp takes 32 consecutive positions at a time.  Lane (g, t) = (lane/4, lane%4)
+// loads positions [8t, 8t+8) of worker g and of worker g+8: 16 bytes each.  Because the
+// Gram matrix is a sum over positions, any assignment of positions to the k index of
+// the MMA works as long as it is the same for every worker; the one used here puts the
+// lane's own elements where the m16n8k16 fragment layout expects row g / row g+8, so
+// the same registers serve as the A operand (workers x positions) and as the B operand
+// (positions x workers).  Two k-steps of 16 cover the 32 positions; the two n-tiles
+// give columns 0-7 and 8-15 of G.
+template <int KG>
+__global__ void __launch_bounds__(kThreads) gram_mma_bf16_kernel(const StageArgs a) {
+  static_assert(KG == 8 || KG == 16, "tensor-core Gram handles 8 or 16 workers");
+  constexpr int E = tri_count(KG);
+  constexpr int U = 4;        // chunks of 32 positions loaded per warp iteration
+  constexpr int kFold = 4;    // iterations accumulated in the MMA before a Kahan fold
+  const int tile_id = blockIdx.x, q = blockIdx.y;
+  const TileDesc t = a.tiles[tile_id];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g = lane >> 2, tq = lane & 3;
+  const uint16_t* xg = static_cast<const uint16_t*>(a.in[q * KG + g]);
+  const uint16_t* xh = KG == 16 ? static_cast<const uint16_t*>(a.in[q * KG + g + 8]) : nullptr;
+  const bool aligned = a.aligned != 0;
+  const int64_t lo = t.start, hi = t.start + t.len;
+  const int64_t c0 = lo >> 5, c1 = (hi + 31) >> 5;  // 32-position chunks
+
+  float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+  float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+  float e0[4] = {0.f, 0.f, 0.f, 0.f}, e1[4] = {0.f, 0.f, 0.f, 0.f};
+  int pending = 0;
+  for (int64_t c = c0 + warp; c < c1; c += kWarps * U) {
+    uint4 rg[U], rh[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t cu = c + static_cast<int64_t>(u) * kWarps;
+      const int64_t v = cu * 4 + tq;
+      if (cu < c1) {
+        rg[u] = load_vec_raw<BF16Tag, kLoadKeep>(xg, v, lo, hi, aligned);
+        rh[u] = KG == 16 ? load_vec_raw<BF16Tag, kLoadKeep>(xh, v, lo, hi, aligned)
+                         : make_uint4(0u, 0u, 0u, 0u);
+      } else {
+        rg[u] = make_uint4(0u, 0u, 0u, 0u);
+        rh[u] = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      mma_bf16_16816(d0, rg[u].x, rh[u].x, rg[u].y, rh[u].y, rg[u].x, rg[u].y);
+      mma_bf16_16816(d0, rg[u].z, rh[u].z, rg[u].w, rh[u].w, rg[u].z, rg[u].w);
+      if constexpr (KG == 16) {
+        mma_bf16_16816(d1, rg[u].x, rh[u].x, rg[u].y, rh[u].y, rh[u].x, rh[u].y);
+        mma_bf16_16816(d1, rg[u].z, rh[u].z, rg[u].w, rh[u].w, rh[u].z, rh[u].w);
+      }
+    }
+    if (++pending == kFold) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        kahan_add(s0[i], e0[i], d0[i]);
+        kahan_add(s1[i], e1[i], d1[i]);
+        d0[i] = 0.f;
+        d1[i] = 0.f;
+      }
+      pending = 0;
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    kahan_add(s0[i], e0[i], d0[i]);
+    kahan_add(s1[i], e1[i], d1[i]);
+  }
+
+  // Each warp now holds its full KG x KG partial, one distinct entry per register:
+  // s0[0..1] = G[g][2t..2t+1], s0[2..3] = G[g+8][2t..2t+1], s1 likewise for columns
+  // 8 + 2t.  Sum the warps in index order.
+  __shared__ float red[kWarps][KG * KG];
+  {
+    const int r0 = g, r1 = g + 8, cA = 2 * tq;
+    red[warp][r0 * KG + cA] = __fsub_rn(s0[0], e0[0]);
+    red[warp][r0 * KG + cA + 1] = __fsub_rn(s0[1], e0[1]);
+    if constexpr (KG == 16) {
+      red[warp][r1 * KG + cA] = __fsub_rn(s0[2], e0[2]);
+      red[warp][r1 * KG + cA + 1] = __fsub_rn(s0[3], e0[3]);
+      red[warp][r0 * KG + 8 + cA] = __fsub_rn(s1[0], e1[0]);
+      red[warp][r0 * KG + 8 + cA + 1] = __fsub_rn(s1[1], e1[1]);
+      red[warp][r1 * KG + 8 + cA] = __fsub_rn(s1[2], e1[2]);
+      red[warp][r1 * KG + 8 + cA + 1] = __fsub_rn(s1[3], e1[3]);
+    }
+  }
+  __syncthreads();
+  float* dst = a.partials + (static_cast<size_t>(q) * a.ntiles + tile_id) * E;
+  for (int idx = threadIdx.x; idx < KG * KG; idx += kThreads) {
+    const int i = idx / KG, j = idx % KG;
+    if (j < i) continue;
+    float s = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) s = __fadd_rn(s, red[w][idx]);
+    dst[tri_index(KG, i, j)] = s;
+  }
+}
+
+// ----------------------------------------------------------- coefficients (per segment)
+
+// Sum the fp32 tile partials of one chunk of at most kChunkTiles tiles (compensated,
+// in tile order) into one fp64 value per Gram entry.
+template <int KG>
+__global__ void __launch_bounds__(kThreads) reduce_chunks_kernel(const StageArgs a) {
+  constexpr int E = tri_count(KG);
+  const int c = blockIdx.x, q = blockIdx.y;
+  const ChunkDesc ch = a.chunks[c];
+  for (int e = threadIdx.x; e < E; e += kThreads) {
+    const float* p = a.partials + (static_cast<size_t>(q) * a.ntiles + ch.first_tile) * E + e;
+    float v[kChunkTiles];
+#pragma unroll
+    for (int t = 0; t < kChunkTiles; ++t)
+      v[t] = t < ch.ntiles ? p[static_cast<size_t>(t) * E] : 0.f;  // loads issued together
+    float sum = 0.f, comp = 0.f;
+#pragma unroll
+    for (int t = 0; t < kChunkTiles; ++t) kahan_add(sum, comp, v[t]);
+    a.chunk_sums[(static_cast<size_t>(q) * a.nchunks + c) * E + e] =
+        static_cast<double>(sum) - static_cast<double>(comp);
+  }
+}
+
+// Unpacks entry e of the packed upper triangle into (i, j), i <= j.
+__device__ __forceinline__ void tri_unpack(int K, int e, int& i, int& j) {
+  i = 0;
+  int rem = e;
+  while (rem >= K - i) {
+    rem -= K - i;
+    ++i;
+  }
+  j = i + rem;
+}
+
+// The Adasum tree of one segment in coefficient space, in fp64.  Every tree node u is
+// sum_{k in u} c_k g_k over 2^level consecutive leaves; pairing u = [a0, a0+w) with
+// v = [a0+w, a0+2w):
+//     d = c_u^T G c_v,  pu = c_u^T G c_u,  pv = c_v^T G c_v
+//     alpha = 1 - d / (2 pu)   (alpha = 1 when pu == 0: a zero node contributes a plain sum)
+//     beta  = 1 - d / (2 pv)
+//     c_u *= alpha,  c_v *= beta.
+//
+// Alongside, a first-order estimate of the error of the fp32 pass.  Gram entries carry
+// errors of about gram_err |g_i||g_j| (independent, so quadratic forms add them in
+// quadrature), inputs carry relative errors eps_in (earlier stages), and the combine
+// rounds at each of the log2(K)+1 levels of its pairwise sum.  The estimate follows
+// every node's norm and cross term through the tree: when a node's norm is no larger
+// than its own error (cancellation), or the estimated relative error of the output
+// exceeds the budget, the segment is flagged for the fp64 recompute.
+//   returns the estimated relative output error (1e30 when flagged as ill-conditioned).
+template <int KG>
+__device__ double coefficient_tree(const double (&G)[KG][KG], const double* eps_in,
+                                   double gram_err, double (&c)[KG], bool& ill) {
+  double s[KG], dc[KG];
+#pragma unroll
+  for (int k = 0; k < KG; ++k) {
+    c[k] = 1.0;
+    dc[k] = 0.0;
+    s[k] = sqrt(fmax(G[k][k], 0.0));
+  }
+  ill = false;
+  for (int w = 1; w < KG; w *= 2) {
+    for (int a0 = 0; a0 < KG; a0 += 2 * w) {
+      double d = 0.0, pu = 0.0, pv = 0.0;
+      for (int i = a0; i < a0 + w; ++i)
+        for (int j = a0 + w; j < a0 + 2 * w; ++j) d += c[i] * c[j] * G[i][j];
+      for (int i = a0; i < a0 + w; ++i)
+        for (int j = a0; j < a0 + w; ++j) pu += c[i] * c[j] * G[i][j];
+      for (int i = a0 + w; i < a0 + 2 * w; ++i)
+        for (int j = a0 + w; j < a0 + 2 * w; ++j) pv += c[i] * c[j] * G[i][j];
+      // error model of the two nodes
+      double Su = 0.0, Sv = 0.0, Du = 0.0, Dv = 0.0;
+      for (int i = a0; i < a0 + w; ++i) {
+        const double e = eps_in ? eps_in[i] : 0.0;
+        Su += c[i] * c[i] * s[i] * s[i];
+        Du += (dc[i] * dc[i] + c[i] * c[i] * e * e) * s[i] * s[i];
+      }
+      for (int j = a0 + w; j < a0 + 2 * w; ++j) {
+        const double e = eps_in ? eps_in[j] : 0.0;
+        Sv += c[j] * c[j] * s[j] * s[j];
+        Dv += (dc[j] * dc[j] + c[j] * c[j] * e * e) * s[j] * s[j];
+      }
+      Du = sqrt(Du);
+      Dv = sqrt(Dv);
+      const double nu = sqrt(fmax(pu, 0.0)), nv = sqrt(fmax(pv, 0.0));
+      const double err_pu = gram_err * Su + 2.0 * nu * Du;
+      const double err_pv = gram_err * Sv + 2.0 * nv * Dv;
+      const double err_d = gram_err * sqrt(Su * Sv) + nu * Dv + nv * Du;
+      double alpha = 1.0, beta = 1.0, dalpha = 0.0, dbeta = 0.0;
+      if (pu != 0.0) {
+        alpha = 1.0 - d / (2.0 * pu);
+        dalpha = (err_d + fabs(d) * err_pu / fabs(pu)) / (2.0 * fabs(pu));
+        if (pu <= err_pu) ill = true;
+      } else if (Su > 0.0) {
+        ill = true;  // a non-zero subtree cancelled to an exact zero norm
+      }
+      if (pv != 0.0) {
+        beta = 1.0 - d / (2.0 * pv);
+        dbeta = (err_d + fabs(d) * err_pv / fabs(pv)) / (2.0 * fabs(pv));
+        if (pv <= err_pv) ill = true;
+      } else if (Sv > 0.0) {
+        ill = true;
+      }
+      for (int i = a0; i < a0 + w; ++i) {
+        dc[i] = fabs(alpha) * dc[i] + fabs(c[i]) * dalpha;
+        c[i] *= alpha;
+      }
+      for (int j = a0 + w; j < a0 + 2 * w; ++j) {
+        dc[j] = fabs(beta) * dc[j] + fabs(c[j]) * dbeta;
+        c[j] *= beta;
+      }
+    }
+  }
+  // output: norm^2 = c^T G c, and its error terms
+  double P = 0.0, S = 0.0, D = 0.0;
+  for (int i = 0; i < KG; ++i) {
+    const double e = eps_in ? eps_in[i] : 0.0;
+    S += c[i] * c[i] * s[i] * s[i];
+    D += (dc[i] * dc[i] + c[i] * c[i] * e * e) * s[i] * s[i];
+    for (int j = 0; j < KG; ++j) P += c[i] * c[j] * G[i][j];
+  }
+  D = sqrt(D);
+  if (S == 0.0) return 0.0;  // every leaf is zero: the output is exactly zero
+  int levels = 1;
+  for (int k = KG; k > 1; k >>= 1) ++levels;
+  const double err_P = gram_err * S + 2.0 * sqrt(fmax(P, 0.0)) * D;
+  if (P <= err_P) {
+    ill = true;
+    return 1e30;
+  }
+  const double rel = (D + levels * 5.9604644775390625e-08 * sqrt(S)) / sqrt(P);
+  return ill ? 1e30 : rel;
+}
+
+// Per segment: the Gram matrix from the chunk sums (fp64, chunk order), the tree
+// coefficients, and the conditioning check (see coefficient_tree).
+template <int KG>
+__global__ void __launch_bounds__(128) coef_kernel(const StageArgs a) {
+  constexpr int E = tri_count(KG);
+  const int seg = blockIdx.x, q = blockIdx.y;
+  const SegDesc sd = a.segs[seg];
+  __shared__ double G[KG][KG];
+  __shared__ double eps[KG];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    double sum = 0.0;
+    const double* p = a.chunk_sums + (static_cast<size_t>(q) * a.nchunks + sd.first_chunk) * E + e;
+    for (int t = 0; t < sd.nchunks; ++t) sum += p[static_cast<size_t>(t) * E];
+    int i, j;
+    tri_unpack(KG, e, i, j);
+    G[i][j] = sum;
+    G[j][i] = sum;
+  }
+  for (int k = threadIdx.x; k < KG; k += blockDim.x)
+    eps[k] = a.in_relerr ? static_cast<double>(a.in_relerr[static_cast<size_t>(q * KG + k) * a.nsegs + seg]) : 0.0;
+  __syncthreads();
+  if (threadIdx.x != 0) return;
+  double c[KG];
+  bool ill = false;
+  const double rel = coefficient_tree<KG>(G, a.in_relerr ? eps : nullptr, kGramRelErr, c, ill);
+  float* dst = a.coef + (static_cast<size_t>(q) * a.nsegs + seg) * KG;
+#pragma unroll
+  for (int k = 0; k < KG; ++k) dst[k] = static_cast<float>(c[k]);
+  if (a.relerr) a.relerr[static_cast<size_t>(q) * a.nsegs + seg] = static_cast<float>(fmin(rel, 1e30));
+  if (a.seg_flag && sd.len > 0 && (ill || !(rel <= kRelErrBudget))) a.seg_flag[seg] = 1;
+}
+
+// ----------------------------------------------------------- pass 2: combine (+ step)
+
+// sum over leaves [LO, LO+CNT) of c_k * x_k[e], as a balanced pairwise tree of
+// explicitly rounded products and sums (never contracted into FMAs), so that the value
+// is symmetric under swapping the two halves of any subtree.
+template <typename Tag, int LO, int CNT, int KG>
+__device__ __forceinline__ float tree_combine(const float (&c)[KG], const uint4 (&r)[KG], int e) {
+  if constexpr (CNT == 1) {
+    return __fmul_rn(c[LO], vec_elem<Tag>(r[LO], e));
+  } else {
+    return __fadd_rn(tree_combine<Tag, LO, CNT / 2, KG>(c, r, e),
+                     tree_combine<Tag, LO + CNT / 2, CNT / 2, KG>(c, r, e));
+  }
+}
+
+// Store VW fp32 values as elements [p0, p0 + VW) of an output array, only positions in
+// [lo, hi); full aligned vectors are written with streaming vector stores.
+template <typename OutTag, int VW>
+__device__ __forceinline__ void store_vec(typename ElemTraits<OutTag>::Storage* y, int64_t p0,
+                                          int64_t lo, int64_t hi, bool aligned,
+                                          const float (&val)[VW]) {
+  const bool full = aligned && p0 >= lo && p0 + VW <= hi;
+  if constexpr (ElemTraits<OutTag>::kVW == 8) {  // bf16 output
+    if (full) {
+      if constexpr (VW == 8) {
+        uint4 w = make_uint4(pack_bf16x2(val[0], val[1]), pack_bf16x2(val[2], val[3]),
+                             pack_bf16x2(val[4], val[5]), pack_bf16x2(val[6], val[7]));
+        __stcs(reinterpret_cast<uint4*>(y + p0), w);
+      } else {
+        uint2 w = make_uint2(pack_bf16x2(val[0], val[1]), pack_bf16x2(val[2], val[3]));
+        __stcs(reinterpret_cast<uint2*>(y + p0), w);
+      }
+      return;
+    }
+#pragma unroll
+    for (int e = 0; e < VW; ++e) {
+      const int64_t p = p0 + e;
+      if (p >= lo && p < hi) y[p] = float_to_bf16_bits(val[e]);
+    }
+  } else {  // fp32 output
+    if (full) {
+#pragma unroll
+      for (int h = 0; h < VW; h += 4)
+        __stcs(reinterpret_cast<float4*>(y + p0 + h),
+               make_float4(val[h], val[h + 1], val[h + 2], val[h + 3]));
+      return;
+    }
+#pragma unroll
+    for (int e = 0; e < VW; ++e) {
+      const int64_t p = p0 + e;
+      if (p >= lo && p < hi) y[p] = val[e];
+    }
+  }
+}
+
+// Load VW fp32 values [p0, p0+VW) (positions outside [lo, hi) read as 0).
+template <int VW>
+__device__ __forceinline__ void load_f32_vec(const float* x, int64_t p0, int64_t lo, int64_t hi,
+                                             bool aligned, float (&val)[VW]) {
+  if (aligned && p0 >= lo && p0 + VW <= hi) {
+#pragma unroll
+    for (int h = 0; h < VW; h += 4) {
+      const float4 f = __ldcs(reinterpret_cast<const float4*>(x + p0 + h));
+      val[h] = f.x;
+      val[h + 1] = f.y;
+      val[h + 2] = f.z;
+      val[h + 3] = f.w;
+    }
+    return;
+  }
+#pragma unroll
+  for (int e = 0; e < VW; ++e) {
+    const int64_t p = p0 + e;
+    val[e] = (p >= lo && p < hi) ? x[p] : 0.f;
+  }
+}
+
+// out = sum_k c_k g_k over one tile; with MOM, also v' = mu v + out, w' = w - lr v'
+// (fp32), and out is written only when a.out[q] is not null.
+template <typename InTag, typename OutTag, int KG, bool MOM>
+__global__ void __launch_bounds__(kThreads) combine_kernel(const StageArgs a) {
+  using SI = typename ElemTraits<InTag>::Storage;
+  using SO = typename ElemTraits<OutTag>::Storage;
+  constexpr int VW = ElemTraits<InTag>::kVW;
+  const int tile_id = blockIdx.x, q = blockIdx.y;
+  const TileDesc t = a.tiles[tile_id];
+  if (a.skip_flagged && a.seg_flag[t.seg]) return;  // left to the fp64 path
+  const bool aligned = a.aligned != 0;
+  float c[KG];
+  if constexpr (KG == 1) {
+    c[0] = 1.f;
+  } else {
+    const float* cp = a.coef + (static_cast<size_t>(q) * a.nsegs + t.seg) * KG;
+#pragma unroll
+    for (int k = 0; k < KG; ++k) c[k] = cp[k];
+  }
+  const SI* x[KG];
+#pragma unroll
+  for (int k = 0; k < KG; ++k) x[k] = static_cast<const SI*>(a.in[q * KG + k]);
+  SO* y = static_cast<SO*>(a.out[q]);
+  const int64_t lo = t.start, hi = t.start + t.len;
+  const int64_t v0 = lo / VW, v1 = (hi + VW - 1) / VW;
+  for (int64_t v = v0 + threadIdx.x; v < v1; v += kThreads) {
+    uint4 r[KG];
+#pragma unroll
+    for (int k = 0; k < KG; ++k) r[k] = load_vec_raw<InTag, kLoadStream>(x[k], v, lo, hi, aligned);
+    float val[VW];
+#pragma unroll
+    for (int e = 0; e < VW; ++e) val[e] = tree_combine<InTag, 0, KG, KG>(c, r, e);
+    const int64_t p0 = v * VW;
+    if constexpr (MOM) {
+      float wv[VW], mv[VW];
+      load_f32_vec<VW>(a.momentum, p0, lo, hi, aligned, mv);
+      load_f32_vec<VW>(a.master_w, p0, lo, hi, aligned, wv);
+#pragma unroll
+      for (int e = 0; e < VW; ++e) {
+        mv[e] = __fmaf_rn(a.mu, mv[e], val[e]);
+        wv[e] = __fmaf_rn(-a.lr, mv[e], wv[e]);
+      }
+      store_vec<F32Tag, VW>(a.momentum, p0, lo, hi, aligned, mv);
+      store_vec<F32Tag, VW>(a.master_w, p0, lo, hi, aligned, wv);
+      if (y != nullptr) store_vec<OutTag, VW>(y, p0, lo, hi, aligned, val);
+    } else {
+      store_vec<OutTag, VW>(y, p0, lo, hi, aligned, val);
+    }
+  }
+}
+
+// ---------------------------------------------------------------- fp64 recompute path
+//
+// Segments flagged by coef_kernel are recomputed here entirely in fp64: exact products
+// of the stored inputs (fp32 x fp32 and bf16 x bf16 products are exact in fp64), fp64
+// Gram sums, the fp64 tree, and an fp64 combine rounded once to the output type.  These
+// kernels walk the flagged lists with a small persistent grid and return at once when
+// the lists are empty, which is the normal case.
+
+enum Kind { kKindF32 = 0, kKindBF16 = 1, kKindF64 = 2 };
+
+template <int IN>
+__device__ __forceinline__ double load_f64(const void* base, int64_t i) {
+  if constexpr (IN == kKindF32) return static_cast<double>(static_cast<const float*>(base)[i]);
+  if constexpr (IN == kKindBF16)
+    return static_cast<double>(bf16_bits_to_float(static_cast<const uint16_t*>(base)[i]));
+  return static_cast<const double*>(base)[i];
+}
+
+// Builds the lists of flagged tiles and segments (order of the lists is irrelevant:
+// every tile and segment is computed on its own).
+static __global__ void collect_kernel(const StageArgs a) {
+  for (int s = blockIdx.x * blockDim.x + threadIdx.x; s < a.nsegs; s += gridDim.x * blockDim.x) {
+    if (!a.seg_flag[s]) continue;
+    const SegDesc sd = a.segs[s];
+    if (sd.ntiles == 0) continue;
+    if (sd.len <= kTinySeg) {
+      a.list_tiny[atomicAdd(&a.list_count[2], 1)] = s;
+      continue;
+    }
+    const int base = atomicAdd(&a.list_count[0], sd.ntiles);
+    for (int t = 0; t < sd.ntiles; ++t) a.list_tiles[base + t] = sd.first_tile + t;
+    a.list_segs[atomicAdd(&a.list_count[1], 1)] = s;
+  }
+}
+
+// Sum over the warp in a fixed butterfly order (every lane gets the same value).
+__device__ __forceinline__ double warp_sum64(double v) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
+  return v;
+}
+
+// Vector-space fp64 recompute of a flagged segment of at most 32 positions: one warp,
+// lane j holds position j of every node.  The tree is evaluated depth first (leaves
+// left to right, a node is formed as soon as both children exist), which visits the
+// same pairs (2i, 2i+1) at every level as the level-by-level definition.  Norms are
+// recomputed from the node values themselves, as in the definition.
+template <int IN, int OUT, bool MOM>
+__global__ void __launch_bounds__(kThreads) tiny64_kernel(const StageArgs a) {
+  constexpr int kMaxDepth = 10;  // log2(kMaxK) + 2
+  const int lane = threadIdx.x & 31;
+  const int wid = (blockIdx.x * kThreads + threadIdx.x) >> 5;
+  const int nwarps = (gridDim.x * kThreads) >> 5;
+  const int count = a.list_count[2];
+  for (int li = wid; li < count; li += nwarps) {
+    const SegDesc sd = a.segs[a.list_tiny[li]];
+    const int n = static_cast<int>(sd.len);
+    const int64_t p = sd.start + lane;
+    const bool on = lane < n;
+    double val[kMaxDepth];
+    int lvl[kMaxDepth];
+    int top = 0;
+    for (int k = 0; k < a.Ktotal; ++k) {
+      val[top] = on ? load_f64<IN>(a.in[k], p) : 0.0;
+      lvl[top] = 0;
+      ++top;
+      while (top >= 2 && lvl[top - 1] == lvl[top - 2]) {
+        const double x = val[top - 2], y = val[top - 1];
+        const double d = warp_sum64(x * y), pa = warp_sum64(x * x), pb = warp_sum64(y * y);
+        const double alpha = 1.0 - (pa == 0.0 ? 0.0 : d / (2.0 * pa));
+        const double beta = 1.0 - (pb == 0.0 ? 0.0 : d / (2.0 * pb));
+        val[top - 2] = alpha * x + beta * y;
+        lvl[top - 2] += 1;
+        --top;
+      }
+    }
+    if (!on) continue;
+    const double yv = val[0];
+    if constexpr (MOM) {
+      const double v = static_cast<double>(a.mu) * static_cast<double>(a.momentum[p]) + yv;
+      const double w = static_cast<double>(a.master_w[p]) - static_cast<double>(a.lr) * v;
+      a.momentum[p] = static_cast<float>(v);
+      a.master_w[p] = static_cast<float>(w);
+      if (a.out[0] == nullptr) continue;
+    }
+    if constexpr (OUT == kKindF32) {
+      static_cast<float*>(a.out[0])[p] = static_cast<float>(yv);
+    } else {
+      __nv_bfloat16 h = __double2bfloat16(yv);
+      static_cast<uint16_t*>(a.out[0])[p] = *reinterpret_cast<uint16_t*>(&h);
+    }
+  }
+}
+
+// fp64 Gram of every flagged tile: the tile is staged through shared memory 64
+// positions at a time; thread e owns Gram entry e.
+template <int IN, int KG>
+__global__ void __launch_bounds__(kThreads) gram64_kernel(const StageArgs a) {
+  constexpr int E = tri_count(KG);
+  constexpr int P = 64;
+  __shared__ double xs[KG][P];
+  const int q = blockIdx.y;
+  const int count = a.list_count[0];
+  int ei = 0, ej = 0;
+  if (threadIdx.x < E) tri_unpack(KG, threadIdx.x, ei, ej);
+  for (int li = blockIdx.x; li < count; li += gridDim.x) {
+    const int tile_id = a.list_tiles[li];
+    const TileDesc t = a.tiles[tile_id];
+    double acc = 0.0;
+    for (int64_t p0 = t.start; p0 < t.start + t.len; p0 += P) {
+      const int64_t left = t.start + t.len - p0;
+      const int np = left < P ? static_cast<int>(left) : P;
+      __syncthreads();
+      for (int idx = threadIdx.x; idx < KG * P; idx += kThreads) {
+        const int k = idx / P, p = idx % P;
+        xs[k][p] = p < np ? load_f64<IN>(a.in[q * KG + k], p0 + p) : 0.0;
+      }
+      __syncthreads();
+      if (threadIdx.x < E)
+        for (int p = 0; p < np; ++p) acc = fma(xs[ei][p], xs[ej][p], acc);
+    }
+    if (threadIdx.x < E)
+      a.partials64[(static_cast<size_t>(q) * a.ntiles + tile_id) * E + threadIdx.x] = acc;
+    __syncthreads();
+  }
+}
+
+// fp64 coefficients of every flagged segment (plain tree, no error estimate needed).
+template <int KG>
+__global__ void __launch_bounds__(128) coef64_kernel(const StageArgs a) {
+  constexpr int E = tri_count(KG);
+  __shared__ double G[KG][KG];
+  const int q = blockIdx.y;
+  const int count = a.list_count[1];
+  for (int li = blockIdx.x; li < count; li += gridDim.x) {
+    const int seg = a.list_segs[li];
+    const SegDesc sd = a.segs[seg];
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+      double sum = 0.0;
+      const double* p = a.partials64 + (static_cast<size_t>(q) * a.ntiles + sd.first_tile) * E + e;
+      for (int t = 0; t < sd.ntiles; ++t) sum += p[static_cast<size_t>(t) * E];
+      int i, j;
+      tri_unpack(KG, e, i, j);
+      G[i][j] = sum;
+      G[j][i] = sum;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      double c[KG];
+      bool ill = false;
+      coefficient_tree<KG>(G, nullptr, 0.0, c, ill);
+      double* dst = a.coef64 + (static_cast<size_t>(q) * a.nsegs + seg) * KG;
+#pragma unroll
+      for (int k = 0; k < KG; ++k) dst[k] = c[k];
+    }
+  }
+}
+
+template <int IN, int LO, int CNT, int KG>
+__device__ __forceinline__ double tree_combine64(const double (&c)[KG], const StageArgs& a, int q,
+                                                 int64_t p) {
+  if constexpr (CNT == 1) {
+    return c[LO] * load_f64<IN>(a.in[q * KG + LO], p);
+  } else {
+    return tree_combine64<IN, LO, CNT / 2, KG>(c, a, q, p) +
+           tree_combine64<IN, LO + CNT / 2, CNT / 2, KG>(c, a, q, p);
+  }
+}
+
+// fp64 combine of every flagged tile (plus the fp64 heavy-ball step when requested).
+template <int IN, int OUT, int KG, bool MOM>
+__global__ void __launch_bounds__(kThreads) combine64_kernel(const StageArgs a) {
+  const int q = blockIdx.y;
+  const int count = a.list_count[0];
+  for (int li = blockIdx.x; li < count; li += gridDim.x) {
+    const TileDesc t = a.tiles[a.list_tiles[li]];
+    double c[KG];
+    if constexpr (KG == 1) {
+      c[0] = 1.0;
+    } else {
+      const double* cp = a.coef64 + (static_cast<size_t>(q) * a.nsegs + t.seg) * KG;
+#pragma unroll
+      for (int k = 0; k < KG; ++k) c[k] = cp[k];
+    }
+    for (int64_t p = t.start + threadIdx.x; p < t.start + t.len; p += kThreads) {
+      const double y = tree_combine64<IN, 0, KG, KG>(c, a, q, p);
+      if constexpr (MOM) {
+        const double v = static_cast<double>(a.mu) * static_cast<double>(a.momentum[p]) + y;
+        const double w = static_cast<double>(a.master_w[p]) - static_cast<double>(a.lr) * v;
+        a.momentum[p] = static_cast<float>(v);
+        a.master_w[p] = static_cast<float>(w);
+        if (a.out[q] == nullptr) continue;
+      }
+      if constexpr (OUT == kKindF64) {
+        static_cast<double*>(a.out[q])[p] = y;
+      } else if constexpr (OUT == kKindF32) {
+        static_cast<float*>(a.out[q])[p] = static_cast<float>(y);
+      } else {
+        __nv_bfloat16 h = __double2bfloat16(y);
+        static_cast<uint16_t*>(a.out[q])[p] = *reinterpret_cast<uint16_t*>(&h);
+      }
+    }
+  }
+}
+
+}  // namespace adasum

@@ -1,0 +1,48 @@
+// launch_bf16.cu -- launchers for bf16 gradients (tensor-core Gram for 8 and 16
+// workers, CUDA-core Gram for 2 and 4).
+#include "adasum_kernels.cuh"
+
+namespace adasum {
+
+namespace {
+template <typename Kernel>
+int launch(Kernel k, dim3 grid, dim3 block, const StageArgs& a, void* stream) {
+  k<<<grid, block, 0, static_cast<cudaStream_t>(stream)>>>(a);
+  return static_cast<int>(cudaGetLastError());
+}
+}  // namespace
+
+int launch_gram_bf16(const StageArgs& a, void* stream, const char** name) {
+  const dim3 grid(a.ntiles, a.G), block(kThreads);
+  switch (a.Kg) {
+    case 2: *name = "gram_simt<bf16,2>"; return launch(gram_simt_kernel<BF16Tag, 2>, grid, block, a, stream);
+    case 4: *name = "gram_simt<bf16,4>"; return launch(gram_simt_kernel<BF16Tag, 4>, grid, block, a, stream);
+    case 8: *name = "gram_mma<bf16,8>"; return launch(gram_mma_bf16_kernel<8>, grid, block, a, stream);
+    case 16: *name = "gram_mma<bf16,16>"; return launch(gram_mma_bf16_kernel<16>, grid, block, a, stream);
+    default: return static_cast<int>(cudaErrorInvalidValue);
+  }
+}
+
+template <typename OutTag, bool MOM>
+static int combine_bf16_k(const StageArgs& a, void* stream, const char** name) {
+  const dim3 grid(a.ntiles, a.G), block(kThreads);
+  switch (a.Kg) {
+    case 1: *name = "combine<bf16,1>"; return launch(combine_kernel<BF16Tag, OutTag, 1, MOM>, grid, block, a, stream);
+    case 2: *name = "combine<bf16,2>"; return launch(combine_kernel<BF16Tag, OutTag, 2, MOM>, grid, block, a, stream);
+    case 4: *name = "combine<bf16,4>"; return launch(combine_kernel<BF16Tag, OutTag, 4, MOM>, grid, block, a, stream);
+    case 8: *name = "combine<bf16,8>"; return launch(combine_kernel<BF16Tag, OutTag, 8, MOM>, grid, block, a, stream);
+    case 16: *name = "combine<bf16,16>"; return launch(combine_kernel<BF16Tag, OutTag, 16, MOM>, grid, block, a, stream);
+    default: return static_cast<int>(cudaErrorInvalidValue);
+  }
+}
+
+int launch_combine_bf16in(const StageArgs& a, int out_dtype, int momentum, void* stream,
+                          const char** name) {
+  if (out_dtype == kF32)
+    return momentum ? combine_bf16_k<F32Tag, true>(a, stream, name)
+                    : combine_bf16_k<F32Tag, false>(a, stream, name);
+  return momentum ? combine_bf16_k<BF16Tag, true>(a, stream, name)
+                  : combine_bf16_k<BF16Tag, false>(a, stream, name);
+}
+
+}  // namespace adasum

@@ -1,0 +1,70 @@
+// launch_f32.cu -- launchers for fp32 inputs (user fp32 gradients and the fp32
+// intermediates of multi-stage trees) and for the per-segment coefficient kernel.
+#include "adasum_kernels.cuh"
+
+namespace adasum {
+
+namespace {
+template <typename Kernel>
+int launch(Kernel k, dim3 grid, dim3 block, const StageArgs& a, void* stream) {
+  k<<<grid, block, 0, static_cast<cudaStream_t>(stream)>>>(a);
+  return static_cast<int>(cudaGetLastError());
+}
+}  // namespace
+
+int launch_gram_f32(const StageArgs& a, void* stream, const char** name) {
+  const dim3 grid(a.ntiles, a.G), block(kThreads);
+  switch (a.Kg) {
+    case 2: *name = "gram_simt<f32,2>"; return launch(gram_simt_kernel<F32Tag, 2>, grid, block, a, stream);
+    case 4: *name = "gram_simt<f32,4>"; return launch(gram_simt_kernel<F32Tag, 4>, grid, block, a, stream);
+    case 8: *name = "gram_simt<f32,8>"; return launch(gram_simt_kernel<F32Tag, 8>, grid, block, a, stream);
+    case 16: *name = "gram_simt<f32,16>"; return launch(gram_simt_kernel<F32Tag, 16>, grid, block, a, stream);
+    default: return static_cast<int>(cudaErrorInvalidValue);
+  }
+}
+
+int launch_reduce_chunks(const StageArgs& a, void* stream, const char** name) {
+  const dim3 grid(a.nchunks, a.G), block(kThreads);
+  switch (a.Kg) {
+    case 2: *name = "reduce_chunks<2>"; return launch(reduce_chunks_kernel<2>, grid, block, a, stream);
+    case 4: *name = "reduce_chunks<4>"; return launch(reduce_chunks_kernel<4>, grid, block, a, stream);
+    case 8: *name = "reduce_chunks<8>"; return launch(reduce_chunks_kernel<8>, grid, block, a, stream);
+    case 16: *name = "reduce_chunks<16>"; return launch(reduce_chunks_kernel<16>, grid, block, a, stream);
+    default: return static_cast<int>(cudaErrorInvalidValue);
+  }
+}
+
+int launch_coef(const StageArgs& a, void* stream, const char** name) {
+  const dim3 grid(a.nsegs, a.G), block(128);
+  switch (a.Kg) {
+    case 2: *name = "coef<2>"; return launch(coef_kernel<2>, grid, block, a, stream);
+    case 4: *name = "coef<4>"; return launch(coef_kernel<4>, grid, block, a, stream);
+    case 8: *name = "coef<8>"; return launch(coef_kernel<8>, grid, block, a, stream);
+    case 16: *name = "coef<16>"; return launch(coef_kernel<16>, grid, block, a, stream);
+    default: return static_cast<int>(cudaErrorInvalidValue);
+  }
+}
+
+template <typename OutTag, bool MOM>
+static int combine_f32_k(const StageArgs& a, void* stream, const char** name) {
+  const dim3 grid(a.ntiles, a.G), block(kThreads);
+  switch (a.Kg) {
+    case 1: *name = "combine<f32,1>"; return launch(combine_kernel<F32Tag, OutTag, 1, MOM>, grid, block, a, stream);
+    case 2: *name = "combine<f32,2>"; return launch(combine_kernel<F32Tag, OutTag, 2, MOM>, grid, block, a, stream);
+    case 4: *name = "combine<f32,4>"; return launch(combine_kernel<F32Tag, OutTag, 4, MOM>, grid, block, a, stream);
+    case 8: *name = "combine<f32,8>"; return launch(combine_kernel<F32Tag, OutTag, 8, MOM>, grid, block, a, stream);
+    case 16: *name = "combine<f32,16>"; return launch(combine_kernel<F32Tag, OutTag, 16, MOM>, grid, block, a, stream);
+    default: return static_cast<int>(cudaErrorInvalidValue);
+  }
+}
+
+int launch_combine_f32in(const StageArgs& a, int out_dtype, int momentum, void* stream,
+                         const char** name) {
+  if (out_dtype == kF32)
+    return momentum ? combine_f32_k<F32Tag, true>(a, stream, name)
+                    : combine_f32_k<F32Tag, false>(a, stream, name);
+  return momentum ? combine_f32_k<BF16Tag, true>(a, stream, name)
+                  : combine_f32_k<BF16Tag, false>(a, stream, name);
+}
+
+}  // namespace adasum

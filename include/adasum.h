@@ -1,0 +1,201 @@
+/*
+ * adasum.h -- C ABI of the GB300 Adasum library (libadasum_gb300.so).
+ *
+ * Adasum ("Scaling Distributed Training with Adaptive Summation", Maleki et al., arXiv
+ * 2006.02924) combines the gradients of K data-parallel workers.  For two gradients
+ * (Section 3, Equations 1-2 and the average of the two emulated SGD orders):
+ *
+ *     Adasum(a, b) = (1 - a.b / (2 |a|^2)) a + (1 - a.b / (2 |b|^2)) b
+ *
+ * with a zero-norm operand's quotient taken as 0 (its coefficient is 1).  K gradients
+ * are combined as a binary tree over workers (Section 3, recursive application): level
+ * 0 combines pairs (2i, 2i+1), every further level pairs the previous level's results
+ * the same way, log2(K) levels in all.  Every layer segment of the flat gradient is
+ * combined on its own, with its own dot products and norms (Section 3, after Figure 1).
+ *
+ * On one GPU the K worker gradients are K device buffers.  All entry points:
+ *   - take DEVICE pointers for gradient, output and optimizer-state buffers and HOST
+ *     pointers for the small descriptor arrays (the pointer list and the offsets);
+ *     the library copies the descriptor arrays before it returns, so the caller may
+ *     free or reuse them at once;
+ *   - are asynchronous and stream-ordered on `stream` (a cudaStream_t; NULL means the
+ *     legacy default stream).  They return once the work is enqueued;
+ *   - never modify the gradient buffers (unless `out` is one of them) and never
+ *     allocate or free caller memory; the library keeps its own per-device workspace,
+ *     grown on demand with cudaMalloc and reused by later calls (see Workspace below);
+ *   - throw nothing across the ABI: every failure is a status code.  Argument errors
+ *     are detected on the host before anything is enqueued; device-side conditions
+ *     (a bounded wait that ran out) are reported by adasum_get_last_error() once the
+ *     stream has been synchronised;
+ *   - propagate NaN and Inf rather than check for them.
+ *
+ * Element types: ADASUM_F32 (fp32 storage and fp32 math) and ADASUM_BF16 (bf16 storage,
+ * fp32 math: inputs are widened exactly, every intermediate is fp32, the final result is
+ * rounded once to bf16, to nearest even).  Dot products and norms are accumulated from
+ * fp32 products (exact for bf16 inputs) in fp32 partial sums of bounded length, then
+ * combined across warps and tiles with compensated fp32 sums, in a fixed order, so
+ * results are bitwise reproducible run to run.  The tree coefficients are computed in
+ * fp64.
+ *
+ * Alignment: buffers aligned to 16 bytes take the vectorised path; others are accepted
+ * and take a scalar-load path inside the same kernels (slower, same results).
+ *
+ * Workspace: each device gets one library-owned workspace, reused across calls.  Calls
+ * that overlap on the GPU (different streams without ordering between them) must not
+ * share a device; order them with events or use one stream.  adasum_release_workspace()
+ * frees it (after synchronising the device).
+ *
+ * Thread safety: the entry points may be called from several host threads; calls are
+ * serialised inside the library.
+ */
+#ifndef ADASUM_GB300_H
+#define ADASUM_GB300_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define ADASUM_API __attribute__((visibility("default")))
+#else
+#define ADASUM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st *adasum_stream_t;
+
+typedef enum {
+  ADASUM_F32 = 0,  /* fp32 storage, fp32 math */
+  ADASUM_BF16 = 1  /* bf16 storage, fp32 math */
+} adasum_dtype_t;
+
+typedef enum {
+  ADASUM_OK = 0,
+  ADASUM_ERR_INVALID_ARG = 1,  /* null pointer, bad offsets, bad dtype, n < 0, ... */
+  ADASUM_ERR_UNSUPPORTED = 2,  /* K not a power of two in [1, 256] */
+  ADASUM_ERR_ALIAS = 3,        /* an output overlaps an input other than as allowed */
+  ADASUM_ERR_NO_MEMORY = 4,    /* the workspace could not be grown */
+  ADASUM_ERR_CUDA = 5,         /* a CUDA runtime call failed (launch, copy, ...) */
+  ADASUM_ERR_TIMEOUT = 6       /* a device-side bounded wait gave up */
+} adasum_status_t;
+
+/* Largest worker count accepted. */
+#define ADASUM_MAX_K 256
+
+/*
+ * adasum_reduce -- Adasum of K worker gradients, per segment, as a binary tree.
+ *
+ *   grads        host array of K device pointers; grads[k] points to N = seg_offsets[L]
+ *                elements of `dtype` (worker k's flat gradient).  K must be a power of
+ *                two, 1 <= K <= ADASUM_MAX_K; K = 1 copies grads[0] to out.
+ *   seg_offsets  host array of L+1 int64 offsets, seg_offsets[0] = 0, non-decreasing;
+ *                segment s is positions [seg_offsets[s], seg_offsets[s+1]).  Empty
+ *                segments are allowed.  L = 0 (or N = 0) is a no-op.
+ *   out          device pointer to N elements of `dtype`.  It may be exactly equal to
+ *                one of the grads[k] (in-place); any other overlap with a gradient
+ *                buffer is ADASUM_ERR_ALIAS.
+ * Result: out[p] for p in segment s is the tree combination of g_0..g_{K-1} restricted
+ * to segment s.
+ */
+ADASUM_API adasum_status_t adasum_reduce(const void *const *grads, int K, const int64_t *seg_offsets,
+                              int L, adasum_dtype_t dtype, void *out,
+                              adasum_stream_t stream);
+
+/*
+ * adasum_pair -- Adasum(a, b) of two device vectors of n elements (one segment).
+ * Equivalent to adasum_reduce with K = 2 and L = 1.  The combine is evaluated
+ * symmetrically, so adasum_pair(a, b) and adasum_pair(b, a) agree bit for bit.
+ */
+ADASUM_API adasum_status_t adasum_pair(const void *a, const void *b, int64_t n, adasum_dtype_t dtype,
+                            void *out, adasum_stream_t stream);
+
+/*
+ * adasum_reduce_momentum_sgd -- adasum_reduce followed, in the same pass over the data,
+ * by one heavy-ball Momentum-SGD step on fp32 master weights:
+ *
+ *     A  = Adasum tree of the K gradients (fp32, not rounded to the gradient dtype)
+ *     v' = mu * v + A,     w' = w - lr * v'
+ *
+ * The paper applies Adasum to the optimizer's output when a distributed optimizer is
+ * used (Section 3, Figure 3); this entry point is the allreduce-then-step form the paper
+ * also exposes, and for zero initial momentum its first step equals that ordering
+ * because the tree is scale-equivariant.
+ *   master_w, momentum  device fp32 arrays of N elements, updated in place.  They must
+ *                       not overlap each other, the gradients or out.
+ *   out_or_null         optional device pointer to N elements of `grad_dtype` receiving A
+ *                       (rounded to grad_dtype); NULL skips that write.
+ */
+ADASUM_API adasum_status_t adasum_reduce_momentum_sgd(const void *const *grads, int K,
+                                           const int64_t *seg_offsets, int L,
+                                           adasum_dtype_t grad_dtype, float *master_w,
+                                           float *momentum, float lr, float mu,
+                                           void *out_or_null, adasum_stream_t stream);
+
+/*
+ * adasum_get_last_error -- the sticky device-side status of the current device
+ * (ADASUM_OK or ADASUM_ERR_TIMEOUT), read after the caller has synchronised the stream
+ * of the calls in question.  Reading clears it.  Host-side failures are returned by the
+ * entry points themselves and are not repeated here.
+ */
+ADASUM_API adasum_status_t adasum_get_last_error(void);
+
+/* adasum_status_string -- a static, human-readable name for a status code. */
+ADASUM_API const char *adasum_status_string(adasum_status_t status);
+
+/*
+ * adasum_release_workspace -- synchronise the current device and free the library's
+ * workspace on it.  Later calls grow a new one.
+ */
+ADASUM_API adasum_status_t adasum_release_workspace(void);
+
+/*
+ * adasum_version -- library version as 10000*major + 100*minor + patch.
+ */
+ADASUM_API int adasum_version(void);
+
+/* ---- Instrumentation (used by the benchmark; not needed for normal use) ---------- */
+
+/*
+ * adasum_recomputed_segments -- synchronises the current device and returns how many
+ * segments the last call on it recomputed in fp64 (-1 on a CUDA error).
+ *
+ * Every call first runs the fp32 pass; its per-segment coefficient step also estimates,
+ * in fp64 from the Gram matrix, the relative error the fp32 pass will reach (Gram
+ * rounding, error amplification through cancelling tree nodes, combine rounding).
+ * Segments whose estimate exceeds 2.5e-5, or whose tree has a node norm at or below its
+ * own error, are recomputed from the inputs entirely in fp64 and written over.
+ */
+ADASUM_API int64_t adasum_recomputed_segments(void);
+
+/* Aggregated timing of one kernel kind. */
+typedef struct {
+  char name[64];      /* kernel kind, e.g. "gram_mma<bf16,16>" */
+  int64_t launches;   /* launches recorded since the last collect */
+  double total_ms;    /* summed device time between CUDA events around each launch */
+} adasum_kernel_stat_t;
+
+/*
+ * adasum_launch_count -- number of kernels this library has launched in this process.
+ */
+ADASUM_API int64_t adasum_launch_count(void);
+
+/*
+ * adasum_profile_enable -- when `on` is nonzero, every later launch is bracketed by two
+ * CUDA events recorded on the launch stream.  Costs two event records per launch.
+ */
+ADASUM_API adasum_status_t adasum_profile_enable(int on);
+
+/*
+ * adasum_profile_collect -- waits for the recorded events, aggregates them per kernel
+ * kind into `stats` (at most `max_stats` entries, in first-seen order), clears the
+ * record, and returns the number of kinds seen (which may exceed max_stats).
+ */
+ADASUM_API int adasum_profile_collect(adasum_kernel_stat_t *stats, int max_stats);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ADASUM_GB300_H */

@@ -1,0 +1,343 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 CPU oracle.
+
+Sizes are small enough for the oracle to finish in seconds but span many tiles,
+ragged tails, unaligned segment boundaries and every stage structure (K up to 256).
+"""
+import numpy as np
+import pytest
+import torch
+
+import adaptive_gradient_summation_gb300 as ags
+from adaptive_gradient_summation_gb300 import workloads
+from parity import (check_against_oracle, check_bf16_elements, check_fp32_segments,
+                    check_momentum, oracle_reduce, to_f64, to_oracle_input)
+
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+def rand_grads(K, n, dtype, seed, corr=0.6):
+    gen = torch.Generator(device=DEV).manual_seed(seed)
+    s = torch.randn(n, generator=gen, device=DEV)
+    out = []
+    for _ in range(K):
+        z = torch.randn(n, generator=gen, device=DEV)
+        out.append((corr * s + (1 - corr * corr) ** 0.5 * z).to(dtype))
+    return out
+
+
+# ------------------------------------------------------------------ workload families
+
+def test_pair_1m_full_size(native):
+    wl = workloads.make("pair_1m", device=DEV)
+    out = ags.pair(wl.grads[0], wl.grads[1])
+    torch.cuda.synchronize()
+    check_against_oracle(wl.grads, wl.seg_offsets, out)
+
+
+@pytest.mark.parametrize("name,shrink", [("resnet50_k8", 16), ("bert_large_k16", 256),
+                                         ("small_segments_k64", 25), ("gpt_k8_momentum", 2048)])
+def test_workload_shapes_small(native, name, shrink):
+    wl = workloads.make(name, device=DEV, shrink=shrink)
+    out = ags.reduce(wl.grads, wl.seg_offsets)
+    torch.cuda.synchronize()
+    check_against_oracle(wl.grads, wl.seg_offsets, out)
+
+
+@pytest.mark.parametrize("init", ["zero", "random"])
+def test_momentum_small(native, init):
+    wl = workloads.make("gpt_k8_momentum", device=DEV, shrink=2048, momentum_init=init)
+    w0 = wl.master_w.clone()
+    v0 = wl.momentum.clone()
+    out = torch.empty_like(wl.grads[0])
+    ags.reduce_momentum_sgd(wl.grads, wl.seg_offsets, wl.master_w, wl.momentum,
+                            lr=wl.lr, mu=wl.mu, out=out)
+    torch.cuda.synchronize()
+    ref = oracle_reduce(wl.grads, wl.seg_offsets, want_mag=True)
+    check_bf16_elements(to_f64(out), ref["out64"], ref["mag"], wl.K)
+    lr32, mu32 = float(np.float32(wl.lr)), float(np.float32(wl.mu))
+    w_ref, v_ref = oracle.momentum_sgd(ref["out64"], w0.cpu().numpy(), v0.cpu().numpy(),
+                                       lr32, mu32)
+    check_momentum(wl.master_w, wl.momentum, w_ref, v_ref, wl.seg_offsets, wl.lr)
+
+
+def test_momentum_without_out(native):
+    wl = workloads.make("gpt_k8_momentum", device=DEV, shrink=4096, momentum_init="random")
+    w0, v0 = wl.master_w.clone(), wl.momentum.clone()
+    ags.reduce_momentum_sgd(wl.grads, wl.seg_offsets, wl.master_w, wl.momentum,
+                            lr=wl.lr, mu=wl.mu, out=None)
+    torch.cuda.synchronize()
+    ref = oracle_reduce(wl.grads, wl.seg_offsets)
+    w_ref, v_ref = oracle.momentum_sgd(ref["out64"], w0.cpu().numpy(), v0.cpu().numpy(),
+                                       float(np.float32(wl.lr)), float(np.float32(wl.mu)))
+    check_momentum(wl.master_w, wl.momentum, w_ref, v_ref, wl.seg_offsets, wl.lr)
+
+
+# ------------------------------------------------------------------------- shapes / K
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("K", [1, 2, 4, 8, 16, 32, 64, 128, 256])
+def test_all_worker_counts(native, K, dtype):
+    lengths = [1, 7, 0, 31, 33, 4097, 300, 65537, 5, 12345]
+    if K >= 64:
+        lengths = lengths[:7]
+    offs = workloads.offsets_from_numels(lengths)
+    grads = rand_grads(K, int(offs[-1]), dtype, seed=K)
+    out = ags.reduce(grads, offs)
+    torch.cuda.synchronize()
+    check_against_oracle(grads, offs, out)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_unaligned_pointers(native, dtype):
+    K, n = 8, 5003
+    base = rand_grads(K, n + 3, dtype, seed=5)
+    grads = [g[1 + (k % 3): 1 + (k % 3) + n] for k, g in enumerate(base)]  # odd offsets
+    offs = np.array([0, 3, 1000, 1001, 4000, n], dtype=np.int64)
+    out_buf = torch.empty(n + 1, dtype=dtype, device=DEV)
+    out = out_buf[1:]
+    ags.reduce(grads, offs, out=out)
+    torch.cuda.synchronize()
+    check_against_oracle(grads, offs, out)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_in_place(native, dtype):
+    K = 4
+    offs = np.array([0, 100, 5000, 70001], dtype=np.int64)
+    grads = rand_grads(K, 70001, dtype, seed=9)
+    keep = [g.clone() for g in grads]
+    ags.reduce(grads, offs, out=grads[2])
+    torch.cuda.synchronize()
+    check_against_oracle(keep, offs, grads[2])
+
+
+def test_many_tiny_segments(native):
+    rs = np.random.default_rng(3)
+    lengths = rs.integers(0, 40, size=3000)
+    offs = workloads.offsets_from_numels(lengths)
+    grads = rand_grads(16, int(offs[-1]), torch.bfloat16, seed=11)
+    out = ags.reduce(grads, offs)
+    torch.cuda.synchronize()
+    check_against_oracle(grads, offs, out)
+
+
+def test_large_segment_many_tiles(native):
+    n = 3_000_001
+    grads = rand_grads(16, n, torch.bfloat16, seed=12)
+    offs = np.array([0, 17, n], dtype=np.int64)
+    out = ags.reduce(grads, offs)
+    torch.cuda.synchronize()
+    check_against_oracle(grads, offs, out)
+
+
+def test_empty_and_noop(native):
+    g = [torch.empty(0, device=DEV) for _ in range(4)]
+    out = ags.reduce(g, [0])
+    assert out.numel() == 0
+    out = ags.reduce(g, [0, 0, 0])
+    assert out.numel() == 0
+
+
+# ----------------------------------------------------------- exact properties on the GPU
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_orthogonal_is_bit_exact_sum(native, dtype):
+    K, n = 16, 40_000
+    gen = torch.Generator(device=DEV).manual_seed(21)
+    owner = torch.randint(0, K, (n,), generator=gen, device=DEV)
+    vals = torch.randn(n, generator=gen, device=DEV).to(dtype)
+    grads = [torch.where(owner == k, vals, torch.zeros_like(vals)) for k in range(K)]
+    out = ags.reduce(grads, [0, n])
+    torch.cuda.synchronize()
+    assert torch.equal(out, vals)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_identical_inputs_return_the_input(native, dtype):
+    g = rand_grads(1, 123_457, dtype, seed=22)[0]
+    for K in (2, 8, 16, 64):
+        out = ags.reduce([g] * K, [0, g.numel()])
+        torch.cuda.synchronize()
+        assert torch.equal(out, g), K
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_zero_operand_is_plain_sum(native, dtype):
+    b = rand_grads(1, 10_001, dtype, seed=23)[0]
+    z = torch.zeros_like(b)
+    assert torch.equal(ags.pair(z, b), b)
+    assert torch.equal(ags.pair(b, z), b)
+    zz = ags.reduce([z] * 8, [0, b.numel()])
+    torch.cuda.synchronize()
+    assert torch.equal(zz, z)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_pair_commutes_bitwise(native, dtype):
+    a, b = rand_grads(2, 77_777, dtype, seed=24)
+    assert torch.equal(ags.pair(a, b), ags.pair(b, a))
+
+
+def test_sibling_swap_symmetry(native):
+    """Swapping the two halves of the worker list mirrors the top of the tree; the
+    pairwise combine makes the result bitwise identical."""
+    grads = rand_grads(8, 50_000, torch.float32, seed=25)
+    offs = [0, 10, 20_000, 50_000]
+    a = ags.reduce(grads, offs)
+    b = ags.reduce(grads[4:] + grads[:4], offs)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+
+
+def test_tree_order_matches_oracle_only(native):
+    """Adasum is not associative: the GPU matches the oracle's (2i, 2i+1) tree and not
+    the tree of another pairing (workers 0,2 and 1,3)."""
+    grads = rand_grads(4, 2_000, torch.float32, seed=26, corr=0.3)
+    out = ags.reduce(grads, [0, 2000])
+    torch.cuda.synchronize()
+    check_against_oracle(grads, [0, 2000], out)
+    other = oracle_reduce([grads[0], grads[2], grads[1], grads[3]], [0, 2000])["out64"]
+    assert np.linalg.norm(to_f64(out) - other) > 1e-4 * np.linalg.norm(other)
+
+
+def test_deterministic(native):
+    wl = workloads.make("bert_large_k16", device=DEV, shrink=64)
+    a = ags.reduce(wl.grads, wl.seg_offsets).clone()
+    for _ in range(3):
+        b = ags.reduce(wl.grads, wl.seg_offsets)
+        torch.cuda.synchronize()
+        assert torch.equal(a, b)
+
+
+def test_segments_are_independent(native):
+    """Per-layer application: one call over L segments agrees with L one-segment calls.
+    (Bit-exact agreement is not expected: the GPU groups its partial sums by absolute
+    16-byte alignment, which shifts when a segment is moved.)"""
+    grads = rand_grads(8, 30_000, torch.float32, seed=27)
+    offs = [0, 5, 12_000, 12_001, 30_000]
+    whole = ags.reduce(grads, offs)
+    for s in range(len(offs) - 1):
+        lo, hi = offs[s], offs[s + 1]
+        part = ags.reduce([g[lo:hi].contiguous() for g in grads], [0, hi - lo])
+        torch.cuda.synchronize()
+        ref = to_f64(part)
+        err = np.linalg.norm(to_f64(whole[lo:hi]) - ref)
+        assert err <= 2e-5 * np.linalg.norm(ref), s
+
+
+def test_scale_equivariance_power_of_two(native):
+    grads = rand_grads(4, 9_999, torch.float32, seed=28)
+    a = ags.reduce(grads, [0, 9_999])
+    b = ags.reduce([4.0 * g for g in grads], [0, 9_999])
+    torch.cuda.synchronize()
+    assert torch.equal(4.0 * a, b)
+
+
+def test_repeated_calls_reuse_plans(native):
+    wl = workloads.make("resnet50_k8", device=DEV, shrink=32)
+    outs = [ags.reduce(wl.grads, wl.seg_offsets).clone() for _ in range(3)]
+    other = workloads.make("bert_large_k16", device=DEV, shrink=512)
+    ags.reduce(other.grads, other.seg_offsets)
+    outs.append(ags.reduce(wl.grads, wl.seg_offsets))
+    torch.cuda.synchronize()
+    for o in outs[1:]:
+        assert torch.equal(outs[0], o)
+
+
+# ------------------------------------------------------------------------ error paths
+
+def _raw_reduce(ptrs, K, offs, dtype_code, out):
+    import ctypes
+    lib = ags.load_library()
+    arr = (ctypes.c_void_p * len(ptrs))(*ptrs)
+    o = np.asarray(offs, dtype=np.int64)
+    return lib.adasum_reduce(arr, K, o.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
+                             len(o) - 1, dtype_code, out, None)
+
+
+def test_error_codes(native):
+    g = rand_grads(4, 1000, torch.float32, seed=30)
+    p = [t.data_ptr() for t in g]
+    out = torch.empty(1000, device=DEV)
+    assert _raw_reduce(p[:3], 3, [0, 1000], 0, out.data_ptr()) == ags.Status.ERR_UNSUPPORTED
+    assert _raw_reduce(p, 4, [0, 600, 500, 1000], 0, out.data_ptr()) == ags.Status.ERR_INVALID_ARG
+    assert _raw_reduce(p, 4, [1, 1000], 0, out.data_ptr()) == ags.Status.ERR_INVALID_ARG
+    assert _raw_reduce(p, 4, [0, 1000], 7, out.data_ptr()) == ags.Status.ERR_INVALID_ARG
+    assert _raw_reduce(p, 4, [0, 1000], 0, None) == ags.Status.ERR_INVALID_ARG
+    assert _raw_reduce(p[:3] + [None], 4, [0, 1000], 0, out.data_ptr()) == ags.Status.ERR_INVALID_ARG
+    # output overlapping an input partially
+    assert _raw_reduce(p, 4, [0, 1000], 0, g[1].data_ptr() + 8) == ags.Status.ERR_ALIAS
+    with pytest.raises(ags.AdasumError):
+        ags.reduce(g[:3], [0, 1000])
+    assert ags.get_last_error() == ags.Status.OK
+
+
+def test_alloc_failure_is_reported(native, monkeypatch):
+    ags.release_workspace()
+    monkeypatch.setenv("ADASUM_FAULT_INJECT", "alloc")
+    g = rand_grads(4, 100_000, torch.float32, seed=31)
+    with pytest.raises(ags.AdasumError) as ei:
+        ags.reduce(g, [0, 100_000])
+    assert ei.value.status == ags.Status.ERR_NO_MEMORY
+    monkeypatch.delenv("ADASUM_FAULT_INJECT")
+    out = ags.reduce(g, [0, 100_000])
+    torch.cuda.synchronize()
+    check_against_oracle(g, [0, 100_000], out)
+
+
+def test_host_end_to_end(native):
+    wl = workloads.make("resnet50_k8", device="cpu", shrink=64)
+    host = [g.pin_memory() for g in wl.grads]
+    out = ags.reduce_from_host(host, wl.seg_offsets, device=DEV)
+    check_against_oracle(wl.grads, wl.seg_offsets, out)
+
+
+# ------------------------------------------------------- ill-conditioned segments (fp64)
+
+def _cancelling_set(K, n, dtype, seed, eps=1e-3):
+    """Workers in nearly opposite pairs: g_{2i+1} = -(1 - eps) g_{2i} + small noise, so
+    every level-0 node nearly cancels and the next level sees tiny nodes."""
+    gen = torch.Generator(device=DEV).manual_seed(seed)
+    out = []
+    for i in range(K // 2):
+        a = torch.randn(n, generator=gen, device=DEV)
+        b = -(1 - eps) * a + eps * 0.1 * torch.randn(n, generator=gen, device=DEV)
+        out += [a.to(dtype), b.to(dtype)]
+    return out
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("K", [2, 4, 16, 64])
+def test_cancelling_pairs_are_recomputed(native, K, dtype):
+    lengths = [1, 2, 3, 17, 1000]
+    offs = workloads.offsets_from_numels(lengths)
+    grads = _cancelling_set(K, int(offs[-1]), dtype, seed=40 + K)
+    out = ags.reduce(grads, offs)
+    torch.cuda.synchronize()
+    check_against_oracle(grads, offs, out)
+    if K >= 4:
+        assert ags.recomputed_segments() > 0
+
+
+@pytest.mark.parametrize("K", [8, 64])
+def test_scalar_segments(native, K):
+    """Length-1 segments: all workers are parallel, the tree averages them, and random
+    signs make nodes cancel."""
+    offs = np.arange(0, 2001, dtype=np.int64)
+    grads = rand_grads(K, 2000, torch.float32, seed=50 + K, corr=0.0)
+    out = ags.reduce(grads, offs)
+    torch.cuda.synchronize()
+    check_against_oracle(grads, offs, out)
+
+
+def test_well_conditioned_data_stays_on_the_fast_path(native):
+    wl = workloads.make("bert_large_k16", device=DEV, shrink=64)
+    ags.reduce(wl.grads, wl.seg_offsets)
+    assert ags.recomputed_segments() == 0
+    wl = workloads.make("resnet50_k8", device=DEV, shrink=16)
+    ags.reduce(wl.grads, wl.seg_offsets)
+    assert ags.recomputed_segments() == 0
