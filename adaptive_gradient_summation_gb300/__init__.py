@@ -22,7 +22,7 @@ import torch
 
 from ._native import AdasumError, KernelStat, Status, check, library_path, load_library
 
-__all__ = ["reduce", "pair", "reduce_momentum_sgd", "reduce_from_host", "AdasumError",
+__all__ = ["reduce", "pair", "pair_noalloc", "reduce_momentum_sgd", "reduce_from_host", "AdasumError",
            "Status", "load_library", "library_path", "get_last_error", "release_workspace",
            "launch_count", "recomputed_segments", "profile_enable", "profile_collect", "version"]
 
@@ -115,6 +115,23 @@ def pair(a: torch.Tensor, b: torch.Tensor, *, out: torch.Tensor | None = None,
                              _DTYPE_CODE[dtype], ctypes.c_void_p(out.data_ptr()),
                              _stream_handle(device, stream))
     check(st, "adasum_pair")
+    return out
+
+
+def pair_noalloc(a: torch.Tensor, b: torch.Tensor, out: torch.Tensor, *,
+                 stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+    """Adasum(a, b) without any device allocation (``adasum_pair_noalloc``), for callers
+    that cannot allocate device memory.  ``out`` must be provided; n is limited to
+    ADASUM_NOALLOC_MAX_N (33,554,432) elements."""
+    dtype, device, n = _check_grads([a, b])
+    if out.dtype != dtype or out.device != device or out.numel() != n or not out.is_contiguous():
+        raise ValueError("out must be a contiguous tensor like the inputs")
+    lib = load_library()
+    with torch.cuda.device(device):
+        st = lib.adasum_pair_noalloc(ctypes.c_void_p(a.data_ptr()), ctypes.c_void_p(b.data_ptr()),
+                                     n, _DTYPE_CODE[dtype], ctypes.c_void_p(out.data_ptr()),
+                                     _stream_handle(device, stream))
+    check(st, "adasum_pair_noalloc")
     return out
 
 

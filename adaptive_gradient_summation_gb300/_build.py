@@ -20,7 +20,8 @@ BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_NAME = "libadasum_gb300.so"
 LIB_PATH = os.path.join(PKG, LIB_NAME)
 
-SOURCES = ["adasum_api.cu", "launch_f32.cu", "launch_bf16.cu", "launch_f64.cu"]
+SOURCES = ["adasum_api.cu", "launch_f32.cu", "launch_bf16.cu", "launch_f64.cu",
+           "adasum_noalloc.cu"]
 HEADERS = ["adasum_internal.h", "adasum_kernels.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -155,6 +155,38 @@ ADASUM_API adasum_status_t adasum_release_workspace(void);
  */
 ADASUM_API int adasum_version(void);
 
+/*
+ * adasum_pair_noalloc -- adasum_pair for callers that cannot allocate device memory.
+ *
+ * The paper has no counterpart to this entry point: it is a deployment variant of the
+ * two-worker combine, not a different method.
+ *
+ * Who needs it: code that must not call cudaMalloc when it reduces -- for example a
+ * process whose framework allocator already holds nearly all of the GPU's memory (a new
+ * cudaMalloc fails, or makes the framework release and re-fragment its pool), a
+ * latency-sensitive loop that cannot afford the device synchronisation cudaMalloc and
+ * cudaFree imply, or a serving process that fixes its memory footprint at start-up.
+ * The other entry points grow a library workspace with cudaMalloc on first use; this
+ * one allocates nothing, ever.  The caller passes inputs and output as for adasum_pair.
+ *
+ * Scratch: a fixed file-scope device array of 64 KiB (plus a few bytes) inside the
+ * library, present on every GPU that loads the library until the process exits.  The
+ * first call on a device looks up that array's device address (cudaGetSymbolAddress,
+ * with the device current); make that first call before any stream capture.  Every
+ * call reuses the same array: calls that overlap on the GPU (different streams with no
+ * ordering between them) race and give wrong results; order them.  Each call writes
+ * every scratch slot it reads before reading it, so no state carries over between calls.
+ *
+ * Limits and errors: 0 <= n <= ADASUM_NOALLOC_MAX_N, else ADASUM_ERR_INVALID_ARG (n < 0)
+ * or ADASUM_ERR_UNSUPPORTED (n too large); out may equal a or b, other overlap is
+ * ADASUM_ERR_ALIAS.  It runs the fp32 pass only: unlike adasum_pair it does not detect
+ * and recompute ill-conditioned (strongly cancelling) inputs in fp64.
+ */
+#define ADASUM_NOALLOC_MAX_N 33554432
+ADASUM_API adasum_status_t adasum_pair_noalloc(const void *a, const void *b, int64_t n,
+                                               adasum_dtype_t dtype, void *out,
+                                               adasum_stream_t stream);
+
 /* ---- Instrumentation (used by the benchmark; not needed for normal use) ---------- */
 
 /*
