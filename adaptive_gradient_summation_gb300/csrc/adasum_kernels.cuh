@@ -341,94 +341,94 @@ __device__ __forceinline__ void tri_unpack(int K, int e, int& i, int& j) {
   j = i + rem;
 }
 
-// The Adasum tree of one segment in coefficient space, in fp64.  Every tree node u is
-// sum_{k in u} c_k g_k over 2^level consecutive leaves; pairing u = [a0, a0+w) with
-// v = [a0+w, a0+2w):
+// Sum over the aligned block of W lanes that contains this lane (butterfly with
+// offsets W/2 .. 1); every lane of the block gets the same value.
+__device__ __forceinline__ double block_lane_sum(double x, int W) {
+  for (int off = W >> 1; off > 0; off >>= 1) x += __shfl_xor_sync(0xFFFFFFFFu, x, off);
+  return x;
+}
+
+// The Adasum tree of one segment in coefficient space, in fp64, evaluated by one warp:
+// lane k < KG owns leaf k (its coefficient c_k).  Every tree node u is
+// sum_{k in u} c_k g_k over W = 2^level consecutive leaves; pairing u = [a0, a0+W) with
+// v = [a0+W, a0+2W):
 //     d = c_u^T G c_v,  pu = c_u^T G c_u,  pv = c_v^T G c_v
 //     alpha = 1 - d / (2 pu)   (alpha = 1 when pu == 0: a zero node contributes a plain sum)
 //     beta  = 1 - d / (2 pv)
 //     c_u *= alpha,  c_v *= beta.
+// d is taken as the sum of the two halves' partial sums (one from each side), so
+// exchanging u and v gives bitwise the same d.
 //
 // Alongside, a first-order estimate of the error of the fp32 pass.  Gram entries carry
 // errors of about gram_err |g_i||g_j| (independent, so quadratic forms add them in
-// quadrature), inputs carry relative errors eps_in (earlier stages), and the combine
+// quadrature), inputs carry relative errors eps (earlier stages), and the combine
 // rounds at each of the log2(K)+1 levels of its pairwise sum.  The estimate follows
 // every node's norm and cross term through the tree: when a node's norm is no larger
 // than its own error (cancellation), or the estimated relative error of the output
 // exceeds the budget, the segment is flagged for the fp64 recompute.
-//   returns the estimated relative output error (1e30 when flagged as ill-conditioned).
+//
+// Called by all 32 lanes of one warp.  G and eps are in shared memory, c_sh is shared
+// scratch of KG doubles.  Returns (in every lane) the estimated relative output error
+// (1e30 when ill-conditioned); lane k < KG receives its coefficient in `c`.
 template <int KG>
-__device__ double coefficient_tree(const double (&G)[KG][KG], const double* eps_in,
-                                   double gram_err, double (&c)[KG], bool& ill) {
-  double s[KG], dc[KG];
-#pragma unroll
-  for (int k = 0; k < KG; ++k) {
-    c[k] = 1.0;
-    dc[k] = 0.0;
-    s[k] = sqrt(fmax(G[k][k], 0.0));
-  }
-  ill = false;
-  for (int w = 1; w < KG; w *= 2) {
-    for (int a0 = 0; a0 < KG; a0 += 2 * w) {
-      double d = 0.0, pu = 0.0, pv = 0.0;
-      for (int i = a0; i < a0 + w; ++i)
-        for (int j = a0 + w; j < a0 + 2 * w; ++j) d += c[i] * c[j] * G[i][j];
-      for (int i = a0; i < a0 + w; ++i)
-        for (int j = a0; j < a0 + w; ++j) pu += c[i] * c[j] * G[i][j];
-      for (int i = a0 + w; i < a0 + 2 * w; ++i)
-        for (int j = a0 + w; j < a0 + 2 * w; ++j) pv += c[i] * c[j] * G[i][j];
-      // error model of the two nodes
-      double Su = 0.0, Sv = 0.0, Du = 0.0, Dv = 0.0;
-      for (int i = a0; i < a0 + w; ++i) {
-        const double e = eps_in ? eps_in[i] : 0.0;
-        Su += c[i] * c[i] * s[i] * s[i];
-        Du += (dc[i] * dc[i] + c[i] * c[i] * e * e) * s[i] * s[i];
-      }
-      for (int j = a0 + w; j < a0 + 2 * w; ++j) {
-        const double e = eps_in ? eps_in[j] : 0.0;
-        Sv += c[j] * c[j] * s[j] * s[j];
-        Dv += (dc[j] * dc[j] + c[j] * c[j] * e * e) * s[j] * s[j];
-      }
-      Du = sqrt(Du);
-      Dv = sqrt(Dv);
-      const double nu = sqrt(fmax(pu, 0.0)), nv = sqrt(fmax(pv, 0.0));
-      const double err_pu = gram_err * Su + 2.0 * nu * Du;
-      const double err_pv = gram_err * Sv + 2.0 * nv * Dv;
-      const double err_d = gram_err * sqrt(Su * Sv) + nu * Dv + nv * Du;
-      double alpha = 1.0, beta = 1.0, dalpha = 0.0, dbeta = 0.0;
-      if (pu != 0.0) {
-        alpha = 1.0 - d / (2.0 * pu);
-        dalpha = (err_d + fabs(d) * err_pu / fabs(pu)) / (2.0 * fabs(pu));
-        if (pu <= err_pu) ill = true;
-      } else if (Su > 0.0) {
-        ill = true;  // a non-zero subtree cancelled to an exact zero norm
-      }
-      if (pv != 0.0) {
-        beta = 1.0 - d / (2.0 * pv);
-        dbeta = (err_d + fabs(d) * err_pv / fabs(pv)) / (2.0 * fabs(pv));
-        if (pv <= err_pv) ill = true;
-      } else if (Sv > 0.0) {
-        ill = true;
-      }
-      for (int i = a0; i < a0 + w; ++i) {
-        dc[i] = fabs(alpha) * dc[i] + fabs(c[i]) * dalpha;
-        c[i] *= alpha;
-      }
-      for (int j = a0 + w; j < a0 + 2 * w; ++j) {
-        dc[j] = fabs(beta) * dc[j] + fabs(c[j]) * dbeta;
-        c[j] *= beta;
+__device__ double coefficient_tree(const double (&G)[KG][KG], const double* eps,
+                                   double gram_err, double* c_sh, double& c, bool& ill) {
+  static_assert(KG <= 32, "one lane per leaf");
+  const int lane = threadIdx.x & 31;
+  const bool on = lane < KG;
+  const int row = on ? lane : 0;
+  const double s = on ? sqrt(fmax(G[row][row], 0.0)) : 0.0;
+  const double e = on ? eps[row] : 0.0;
+  c = on ? 1.0 : 0.0;
+  double dc = 0.0;
+  bool bad = false;
+  if (on) c_sh[lane] = c;
+  __syncwarp();
+  for (int W = 1; W < KG; W *= 2) {
+    const int self0 = (lane / W) * W, sib0 = self0 ^ W;
+    double row_self = 0.0, row_sib = 0.0;
+    if (on) {
+      for (int j = 0; j < W; ++j) {
+        row_self = fma(c_sh[self0 + j], G[row][self0 + j], row_self);
+        row_sib = fma(c_sh[sib0 + j], G[row][sib0 + j], row_sib);
       }
     }
+    const double p_self = block_lane_sum(c * row_self, W);
+    const double d_half = block_lane_sum(c * row_sib, W);
+    const double d = d_half + __shfl_xor_sync(0xFFFFFFFFu, d_half, W);
+    const double dd = 0.5 * d;  // the two halves each hold the full cross term
+    const double S_self = block_lane_sum(c * c * s * s, W);
+    const double D_self = sqrt(block_lane_sum((dc * dc + c * c * e * e) * s * s, W));
+    const double S_sib = __shfl_xor_sync(0xFFFFFFFFu, S_self, W);
+    const double D_sib = __shfl_xor_sync(0xFFFFFFFFu, D_self, W);
+    const double p_sib = __shfl_xor_sync(0xFFFFFFFFu, p_self, W);
+    const double n_self = sqrt(fmax(p_self, 0.0)), n_sib = sqrt(fmax(p_sib, 0.0));
+    const double err_p = gram_err * S_self + 2.0 * n_self * D_self;
+    const double err_d = gram_err * sqrt(S_self * S_sib) + (n_self * D_sib + n_sib * D_self);
+    double coef = 1.0, dcoef = 0.0;
+    if (p_self != 0.0) {
+      coef = 1.0 - dd / (2.0 * p_self);
+      dcoef = (err_d + fabs(dd) * err_p / fabs(p_self)) / (2.0 * fabs(p_self));
+      if (p_self <= err_p) bad = true;
+    } else if (S_self > 0.0) {
+      bad = true;  // a non-zero subtree cancelled to an exact zero norm
+    }
+    if (on) {
+      dc = fma(fabs(coef), dc, fabs(c) * dcoef);
+      c *= coef;
+    }
+    __syncwarp();
+    if (on) c_sh[lane] = c;
+    __syncwarp();
   }
   // output: norm^2 = c^T G c, and its error terms
-  double P = 0.0, S = 0.0, D = 0.0;
-  for (int i = 0; i < KG; ++i) {
-    const double e = eps_in ? eps_in[i] : 0.0;
-    S += c[i] * c[i] * s[i] * s[i];
-    D += (dc[i] * dc[i] + c[i] * c[i] * e * e) * s[i] * s[i];
-    for (int j = 0; j < KG; ++j) P += c[i] * c[j] * G[i][j];
-  }
-  D = sqrt(D);
+  double full = 0.0;
+  if (on)
+    for (int j = 0; j < KG; ++j) full = fma(c_sh[j], G[row][j], full);
+  const double P = block_lane_sum(c * full, 32);
+  const double S = block_lane_sum(c * c * s * s, 32);
+  const double D = sqrt(block_lane_sum((dc * dc + c * c * e * e) * s * s, 32));
+  ill = __any_sync(0xFFFFFFFFu, bad);
   if (S == 0.0) return 0.0;  // every leaf is zero: the output is exactly zero
   int levels = 1;
   for (int k = KG; k > 1; k >>= 1) ++levels;
@@ -450,6 +450,7 @@ __global__ void __launch_bounds__(128) coef_kernel(const StageArgs a) {
   const SegDesc sd = a.segs[seg];
   __shared__ double G[KG][KG];
   __shared__ double eps[KG];
+  __shared__ double snorm[KG];
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     double sum = 0.0;
     const double* p = a.chunk_sums + (static_cast<size_t>(q) * a.nchunks + sd.first_chunk) * E + e;
@@ -462,15 +463,16 @@ __global__ void __launch_bounds__(128) coef_kernel(const StageArgs a) {
   for (int k = threadIdx.x; k < KG; k += blockDim.x)
     eps[k] = a.in_relerr ? static_cast<double>(a.in_relerr[static_cast<size_t>(q * KG + k) * a.nsegs + seg]) : 0.0;
   __syncthreads();
-  if (threadIdx.x != 0) return;
-  double c[KG];
+  if (threadIdx.x >= 32) return;
+  double c = 0.0;
   bool ill = false;
-  const double rel = coefficient_tree<KG>(G, a.in_relerr ? eps : nullptr, kGramRelErr, c, ill);
-  float* dst = a.coef + (static_cast<size_t>(q) * a.nsegs + seg) * KG;
-#pragma unroll
-  for (int k = 0; k < KG; ++k) dst[k] = static_cast<float>(c[k]);
-  if (a.relerr) a.relerr[static_cast<size_t>(q) * a.nsegs + seg] = static_cast<float>(fmin(rel, 1e30));
-  if (a.seg_flag && sd.len > 0 && (ill || !(rel <= kRelErrBudget))) a.seg_flag[seg] = 1;
+  const double rel = coefficient_tree<KG>(G, eps, kGramRelErr, snorm, c, ill);
+  if (threadIdx.x < KG)
+    a.coef[(static_cast<size_t>(q) * a.nsegs + seg) * KG + threadIdx.x] = static_cast<float>(c);
+  if (threadIdx.x == 0) {
+    if (a.relerr) a.relerr[static_cast<size_t>(q) * a.nsegs + seg] = static_cast<float>(fmin(rel, 1e30));
+    if (a.seg_flag && sd.len > 0 && (ill || !(rel <= kRelErrBudget))) a.seg_flag[seg] = 1;
+  }
 }
 
 // ----------------------------------------------------------- pass 2: combine (+ step)
@@ -733,8 +735,11 @@ template <int KG>
 __global__ void __launch_bounds__(128) coef64_kernel(const StageArgs a) {
   constexpr int E = tri_count(KG);
   __shared__ double G[KG][KG];
+  __shared__ double zeros[KG];
+  __shared__ double snorm[KG];
   const int q = blockIdx.y;
   const int count = a.list_count[1];
+  for (int k = threadIdx.x; k < KG; k += blockDim.x) zeros[k] = 0.0;
   for (int li = blockIdx.x; li < count; li += gridDim.x) {
     const int seg = a.list_segs[li];
     const SegDesc sd = a.segs[seg];
@@ -749,13 +754,11 @@ __global__ void __launch_bounds__(128) coef64_kernel(const StageArgs a) {
       G[j][i] = sum;
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-      double c[KG];
+    if (threadIdx.x < 32) {
+      double c = 0.0;
       bool ill = false;
-      coefficient_tree<KG>(G, nullptr, 0.0, c, ill);
-      double* dst = a.coef64 + (static_cast<size_t>(q) * a.nsegs + seg) * KG;
-#pragma unroll
-      for (int k = 0; k < KG; ++k) dst[k] = c[k];
+      coefficient_tree<KG>(G, zeros, 0.0, snorm, c, ill);
+      if (threadIdx.x < KG) a.coef64[(static_cast<size_t>(q) * a.nsegs + seg) * KG + threadIdx.x] = c;
     }
   }
 }
