@@ -21,7 +21,7 @@ LIB_NAME = "libadasum_gb300.so"
 LIB_PATH = os.path.join(PKG, LIB_NAME)
 
 SOURCES = ["adasum_api.cu", "launch_f32.cu", "launch_bf16.cu", "launch_f64.cu",
-           "adasum_noalloc.cu"]
+           "launch_pipe.cu", "adasum_noalloc.cu"]
 HEADERS = ["adasum_internal.h", "adasum_kernels.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

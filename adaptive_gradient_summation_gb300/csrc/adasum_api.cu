@@ -29,6 +29,22 @@ constexpr int kVersion = 100;  // 0.1.0
 
 int elem_size(int dt) { return dt == kBF16 ? 2 : 4; }
 
+// Single-stage calls run the three-kernel route (Gram / coefficients / combine as
+// separate launches); ADASUM_ROUTE=fused selects the fused persistent kernel instead.
+bool route_fused() {
+  const char* v = std::getenv("ADASUM_ROUTE");
+  return v != nullptr && std::strcmp(v, "fused") == 0;
+}
+
+// A positive integer from the environment (tuning knobs), else `dflt`.
+int64_t env_int(const char* name, int64_t dflt) {
+  const char* v = std::getenv(name);
+  if (v == nullptr) return dflt;
+  const long long x = std::atoll(v);
+  return x > 0 ? x : dflt;
+}
+
+
 // ------------------------------------------------------------------------ profiler
 
 struct ProfRecord {
@@ -68,6 +84,12 @@ struct Plan {
   TileDesc* d_tiles = nullptr;
   SegDesc* d_segs = nullptr;
   ChunkDesc* d_chunks = nullptr;
+  // task list of the fused single-stage kernel (built when K <= 16)
+  int ntasks = 0;
+  int* d_tasks = nullptr;
+  int64_t wave_bytes = 0;
+  int64_t tile_kb = 0;
+  int64_t delay_pct = 0;
 };
 
 struct Workspace {
@@ -76,6 +98,7 @@ struct Workspace {
   size_t cap = 0;
   std::list<Plan> plans;            // most recently used first
   int* last_flag_counts = nullptr;  // device counters of the last call's fp64 lists
+  int* d_error = nullptr;           // device status word (bounded waits), kept for good
 };
 
 std::vector<Workspace> g_ws;
@@ -92,15 +115,89 @@ void free_plan(Plan& p) {
   if (p.d_tiles) cudaFree(p.d_tiles);
   if (p.d_segs) cudaFree(p.d_segs);
   if (p.d_chunks) cudaFree(p.d_chunks);
+  if (p.d_tasks) cudaFree(p.d_tasks);
   p.d_tiles = nullptr;
   p.d_segs = nullptr;
   p.d_chunks = nullptr;
+  p.d_tasks = nullptr;
 }
 
-int64_t tile_positions(int Kg, int dtype, int64_t N, int num_sms) {
-  // About 256 KiB of input per tile, but enough tiles to give every SM a few.
+// Wave budget of the fused kernel (bytes of input per wave); ADASUM_WAVE_MB overrides.
+int64_t wave_budget_bytes() { return env_int("ADASUM_WAVE_MB", 32) << 20; }
+
+// Task order of the fused kernel: consecutive segments are grouped into waves of about
+// wave_bytes of input; the list is  A(0), A(1)[:delay], A(1)[delay:] merged with B(0),
+// A(2)[:delay], A(2)[delay:] merged with B(1), ..., B(last), where A(w) are the Gram
+// tiles of wave w in order and B(w) its combine tiles in reverse order (the most
+// recently loaded data first).  `delay` Gram tasks separate a wave's last Gram task
+// from its first combine task, so a combine task rarely finds its segment unfinished.
+std::vector<int> build_tasks(const std::vector<SegDesc>& segs, int64_t bytes_per_pos,
+                             int64_t wave_bytes, int delay) {
+  std::vector<std::vector<int>> waves;
+  int64_t cur = 0;
+  for (int s = 0; s < static_cast<int>(segs.size()); ++s) {
+    if (segs[s].ntiles == 0) continue;
+    const int64_t b = segs[s].len * bytes_per_pos;
+    if (waves.empty() || (cur > 0 && cur + b > wave_bytes)) {
+      waves.emplace_back();
+      cur = 0;
+    }
+    waves.back().push_back(s);
+    cur += b;
+  }
+  auto gram_of = [&](const std::vector<int>& w) {
+    std::vector<int> t;
+    for (int s : w)
+      for (int i = 0; i < segs[s].ntiles; ++i) t.push_back(segs[s].first_tile + i);
+    return t;
+  };
+  auto combine_of = [&](const std::vector<int>& w) {
+    std::vector<int> t;
+    for (auto it = w.rbegin(); it != w.rend(); ++it)
+      for (int i = segs[*it].ntiles - 1; i >= 0; --i)
+        t.push_back(static_cast<int>(0x80000000u | static_cast<uint32_t>(segs[*it].first_tile + i)));
+    return t;
+  };
+  std::vector<int> tasks;
+  std::vector<int> pending_b;
+  for (size_t w = 0; w < waves.size(); ++w) {
+    const std::vector<int> A = gram_of(waves[w]);
+    size_t ia = 0;
+    if (!pending_b.empty()) {
+      const size_t d = std::min(A.size(), static_cast<size_t>(delay));
+      for (; ia < d; ++ia) tasks.push_back(A[ia]);
+      // merge the rest of A with pending_b in proportion
+      const size_t na = A.size() - ia, nb = pending_b.size();
+      size_t ea = 0, eb = 0;
+      while (ea < na || eb < nb) {
+        if (eb >= nb || (ea < na && ea * nb <= eb * na)) {
+          tasks.push_back(A[ia + ea]);
+          ++ea;
+        } else {
+          tasks.push_back(pending_b[eb]);
+          ++eb;
+        }
+      }
+    } else {
+      for (; ia < A.size(); ++ia) tasks.push_back(A[ia]);
+    }
+    pending_b = combine_of(waves[w]);
+  }
+  tasks.insert(tasks.end(), pending_b.begin(), pending_b.end());
+  return tasks;
+}
+
+// Input bytes per tile.  The fused kernel uses small tiles: the L2 has to hold every
+// byte read between a tile's Gram task and its combine task, and that distance grows
+// with (resident CTAs x tile size).  ADASUM_PIPE_TILE_KB overrides (for tuning).
+int64_t tile_bytes(bool fused) {
+  return fused ? env_int("ADASUM_PIPE_TILE_KB", 64) << 10 : int64_t(256) << 10;
+}
+
+int64_t tile_positions(int Kg, int dtype, int64_t N, int num_sms, bool fused) {
+  // About tile_bytes of input per tile, but enough tiles to give every SM a few.
   const int64_t bytes_per_pos = static_cast<int64_t>(Kg) * elem_size(dtype);
-  int64_t T = (int64_t(256) << 10) / bytes_per_pos;
+  int64_t T = tile_bytes(fused) / bytes_per_pos;
   const int64_t want = std::max<int64_t>(1, N / (4 * static_cast<int64_t>(num_sms)));
   T = std::min(T, want);
   T = std::max<int64_t>(256, std::min<int64_t>(T, 65536));
@@ -110,7 +207,10 @@ int64_t tile_positions(int Kg, int dtype, int64_t N, int num_sms) {
 adasum_status_t get_plan(Workspace& ws, const int64_t* offs, int L, int Kg0, int dtype,
                          Plan** out) {
   for (auto it = ws.plans.begin(); it != ws.plans.end(); ++it) {
-    if (it->Kg0 == Kg0 && it->dtype == dtype &&
+    if (it->Kg0 == Kg0 && it->dtype == dtype && (it->d_tasks != nullptr) == route_fused() &&
+        (it->d_tasks == nullptr || (it->wave_bytes == wave_budget_bytes() &&
+                                    it->tile_kb == (tile_bytes(true) >> 10) &&
+                                    it->delay_pct == env_int("ADASUM_PIPE_DELAY_PCT", 100))) &&
         it->offsets.size() == static_cast<size_t>(L + 1) &&
         std::memcmp(it->offsets.data(), offs, sizeof(int64_t) * (L + 1)) == 0) {
       ws.plans.splice(ws.plans.begin(), ws.plans, it);
@@ -121,7 +221,8 @@ adasum_status_t get_plan(Workspace& ws, const int64_t* offs, int L, int Kg0, int
   int num_sms = 148;
   cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, ws.device);
   const int64_t N = offs[L];
-  const int64_t T = tile_positions(Kg0, dtype, N, num_sms);
+  const bool fused = Kg0 <= kMaxGroup && Kg0 > 1 && route_fused();
+  const int64_t T = tile_positions(Kg0, dtype, N, num_sms, fused);
   std::vector<TileDesc> tiles;
   std::vector<SegDesc> segs(L);
   std::vector<ChunkDesc> chunks;
@@ -175,6 +276,27 @@ adasum_status_t get_plan(Workspace& ws, const int64_t* offs, int L, int Kg0, int
     cudaGetLastError();
     return ADASUM_ERR_CUDA;
   }
+  if (fused) {
+    const int delay = static_cast<int>(
+        env_int("ADASUM_PIPE_DELAY_PCT", 100) * pipeline_grid(dtype, dtype, Kg0, 0, num_sms) / 100);
+    p.wave_bytes = wave_budget_bytes();
+    p.tile_kb = tile_bytes(true) >> 10;
+    p.delay_pct = env_int("ADASUM_PIPE_DELAY_PCT", 100);
+    const std::vector<int> tasks =
+        build_tasks(segs, static_cast<int64_t>(Kg0) * elem_size(dtype), p.wave_bytes, delay);
+    p.ntasks = static_cast<int>(tasks.size());
+    if (cudaMalloc(&p.d_tasks, std::max<size_t>(1, tasks.size()) * sizeof(int)) != cudaSuccess) {
+      free_plan(p);
+      cudaGetLastError();
+      return ADASUM_ERR_NO_MEMORY;
+    }
+    if (cudaMemcpy(p.d_tasks, tasks.data(), tasks.size() * sizeof(int), cudaMemcpyHostToDevice) !=
+        cudaSuccess) {
+      free_plan(p);
+      cudaGetLastError();
+      return ADASUM_ERR_CUDA;
+    }
+  }
   ws.plans.push_front(std::move(p));
   *out = &ws.plans.front();
   return ADASUM_OK;
@@ -209,10 +331,16 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Host-side fault injection for the error-path tests: ADASUM_FAULT_INJECT=alloc makes
-// the next workspace growth fail as if cudaMalloc had.
+// the next workspace growth fail as if cudaMalloc had; ADASUM_FAULT_INJECT=timeout makes
+// the fused kernel never publish segment coefficients and shortens its bounded wait, so
+// the wait runs out and the device status reports ADASUM_ERR_TIMEOUT.
 bool inject_alloc_failure() {
   const char* v = std::getenv("ADASUM_FAULT_INJECT");
   return v != nullptr && std::strcmp(v, "alloc") == 0;
+}
+bool inject_timeout() {
+  const char* v = std::getenv("ADASUM_FAULT_INJECT");
+  return v != nullptr && std::strcmp(v, "timeout") == 0;
 }
 
 int record_launch(int rc, const char* name, cudaEvent_t start, cudaStream_t stream) {
@@ -369,7 +497,10 @@ adasum_status_t reduce_impl(const void* const* grads, int K, const int64_t* offs
   const size_t inter32 = align_up(static_cast<size_t>(N) * sizeof(float), 256);
   const size_t inter64 = align_up(static_cast<size_t>(N) * sizeof(double), 256);
   Carver cv;
-  const size_t o_flags = cv.take((static_cast<size_t>(L) + 3) * sizeof(int));  // flags + 3 counters
+  // One zeroed int region per call: segment flags, the 3 fp64-list counters, and the
+  // fused kernel's task counter, chunk counters, segment counters and ready flags.
+  const size_t n_ints = static_cast<size_t>(L) + 3 + 1 + plan->nchunks + 2 * static_cast<size_t>(L);
+  const size_t o_flags = cv.take(n_ints * sizeof(int));
   const size_t o_part = cv.take(max_e_tiles * sizeof(float));
   const size_t o_chunk = cv.take(max_e_chunks * sizeof(double));
   const size_t o_coef = cv.take(max_coef * sizeof(float));
@@ -392,11 +523,23 @@ adasum_status_t reduce_impl(const void* const* grads, int K, const int64_t* offs
   char* base = static_cast<char*>(ws.buf);
   int* seg_flag = reinterpret_cast<int*>(base + o_flags);
   int* list_count = seg_flag + L;
+  int* task_counter = list_count + 3;
+  int* chunk_done = task_counter + 1;
+  int* seg_done = chunk_done + plan->nchunks;
+  int* seg_ready = seg_done + L;
+  if (ws.d_error == nullptr) {
+    if (cudaMalloc(&ws.d_error, sizeof(int)) != cudaSuccess ||
+        cudaMemset(ws.d_error, 0, sizeof(int)) != cudaSuccess) {
+      cudaGetLastError();
+      ws.d_error = nullptr;
+      return ADASUM_ERR_NO_MEMORY;
+    }
+  }
 
   bool all_aligned = aligned16(out) && (!mom || (aligned16(master_w) && aligned16(momentum)));
   for (int k = 0; k < K; ++k) all_aligned = all_aligned && aligned16(grads[k]);
 
-  if (cudaMemsetAsync(seg_flag, 0, (static_cast<size_t>(L) + 3) * sizeof(int), stream) != cudaSuccess)
+  if (cudaMemsetAsync(seg_flag, 0, n_ints * sizeof(int), stream) != cudaSuccess)
     return ADASUM_ERR_CUDA;
 
   auto make_args = [&](size_t s) {
@@ -432,8 +575,34 @@ adasum_status_t reduce_impl(const void* const* grads, int K, const int64_t* offs
     return a;
   };
 
-  // fp32 pass, stage by stage.
-  for (size_t s = 0; s < kg.size(); ++s) {
+  // fp32 pass: one fused kernel for a single stage, else stage by stage.
+  const bool fused = kg.size() == 1 && kg[0] > 1 && plan->d_tasks != nullptr && route_fused();
+  if (fused) {
+    StageArgs a = make_args(0);
+    for (int k = 0; k < K; ++k) a.in[k] = grads[k];
+    a.out[0] = out;
+    a.skip_flagged = 1;
+    PipeArgs pa;
+    std::memset(&pa, 0, sizeof pa);
+    pa.tasks = plan->d_tasks;
+    pa.ntasks = plan->ntasks;
+    pa.task_counter = task_counter;
+    pa.chunk_done = chunk_done;
+    pa.seg_done = seg_done;
+    pa.seg_ready = seg_ready;
+    pa.error = ws.d_error;
+    pa.spin_budget = 2000000000LL;  // about one second of SM clock
+    if (inject_timeout()) {
+      pa.inject_no_ready = 1;
+      pa.spin_budget = 200000LL;
+    }
+    const int grid = pipeline_grid(dtype, dtype, kg[0], mom ? 1 : 0, num_sms);
+    if (adasum_status_t st = launch_one(stream, [&](const char** n) {
+          return launch_pipeline(a, pa, dtype, dtype, mom ? 1 : 0, grid, stream, n);
+        }))
+      return st;
+  }
+  for (size_t s = 0; s < kg.size() && !fused; ++s) {
     const bool last = s + 1 == kg.size();
     StageArgs a = make_args(s);
     if (s == 0) {
@@ -541,11 +710,17 @@ adasum_status_t adasum_reduce_momentum_sgd(const void* const* grads, int K,
 }
 
 adasum_status_t adasum_get_last_error(void) {
-  // The current kernels contain no bounded waits, so no device-side status exists yet;
-  // report any sticky CUDA error instead.
   std::lock_guard<std::mutex> lock(g_mu);
-  const cudaError_t e = cudaGetLastError();
-  return e == cudaSuccess ? ADASUM_OK : ADASUM_ERR_CUDA;
+  if (cudaGetLastError() != cudaSuccess) return ADASUM_ERR_CUDA;
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess) return ADASUM_ERR_CUDA;
+  Workspace& ws = workspace_for(device);
+  if (ws.d_error == nullptr) return ADASUM_OK;
+  int h = 0;
+  if (cudaMemcpy(&h, ws.d_error, sizeof h, cudaMemcpyDeviceToHost) != cudaSuccess ||
+      cudaMemset(ws.d_error, 0, sizeof h) != cudaSuccess)
+    return ADASUM_ERR_CUDA;
+  return h ? ADASUM_ERR_TIMEOUT : ADASUM_OK;
 }
 
 const char* adasum_status_string(adasum_status_t s) {

@@ -103,6 +103,23 @@ constexpr double kRelErrBudget = 2.5e-5;
 // cancel almost exactly, which a Gram-matrix quadratic form cannot follow even in fp64.
 constexpr int kTinySeg = 32;
 
+// Work list and synchronisation of the fused single-stage kernel (pipeline_kernel).
+// tasks[i] >= 0 is "Gram partial of tile tasks[i]"; tasks[i] < 0 is "combine of tile
+// tasks[i] & 0x7fffffff".  Every combine task comes after all Gram tasks of its
+// segment, and tasks are claimed in list order, so a combine task only ever waits for
+// work already claimed by a running CTA.
+struct PipeArgs {
+  const int* tasks;
+  int ntasks;
+  int* task_counter;        // next task to claim
+  int* chunk_done;          // [nchunks] Gram tiles finished per chunk
+  int* seg_done;            // [nsegs] chunks reduced per segment
+  int* seg_ready;           // [nsegs] 1 once the segment's coefficients are published
+  int* error;               // device status word: 1 = a bounded wait gave up
+  long long spin_budget;    // clock64 cycles a combine task waits before giving up
+  int inject_no_ready;      // test hook: never publish (exercises the bounded wait)
+};
+
 // Launchers, one translation unit per input element type (compiled in parallel).
 // Each enqueues one kernel on `stream` and returns its cudaError_t as int (0 = ok);
 // `name` receives a static string naming the kernel, for the optional profiler.
@@ -113,6 +130,10 @@ int launch_combine_f32in(const StageArgs& a, int out_dtype, int momentum, void* 
                          const char** name);
 int launch_combine_bf16in(const StageArgs& a, int out_dtype, int momentum, void* stream,
                           const char** name);
+// Fused single-stage kernel (K <= 16): grid = persistent CTAs, see PipeArgs.
+int launch_pipeline(const StageArgs& a, const PipeArgs& p, int in_dtype, int out_dtype,
+                    int momentum, int grid, void* stream, const char** name);
+int pipeline_grid(int in_dtype, int out_dtype, int Kg, int momentum, int num_sms);
 // Partial-Gram chunk sums (segments with many tiles), then coefficients.
 int launch_reduce_chunks(const StageArgs& a, void* stream, const char** name);
 // fp64 path: build the flagged lists, then Gram / coefficients / combine over them.

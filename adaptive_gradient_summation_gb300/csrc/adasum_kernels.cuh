@@ -158,11 +158,10 @@ __device__ __forceinline__ void block_reduce_store(float (&acc)[E], float* __res
 // Gram partial of one tile with CUDA-core FMAs: every thread owns whole 16-byte
 // vectors (VW positions of all Kg workers) and accumulates the Kg(Kg+1)/2 products.
 template <typename Tag, int KG>
-__global__ void __launch_bounds__(kThreads) gram_simt_kernel(const StageArgs a) {
+__device__ __forceinline__ void gram_tile_simt(const StageArgs& a, int tile_id, int q) {
   using S = typename ElemTraits<Tag>::Storage;
   constexpr int VW = ElemTraits<Tag>::kVW;
   constexpr int E = tri_count(KG);
-  const int tile_id = blockIdx.x, q = blockIdx.y;
   const TileDesc t = a.tiles[tile_id];
   const S* x[KG];
 #pragma unroll
@@ -194,6 +193,11 @@ __global__ void __launch_bounds__(kThreads) gram_simt_kernel(const StageArgs a) 
   block_reduce_store<E>(acc, a.partials + (static_cast<size_t>(q) * a.ntiles + tile_id) * E);
 }
 
+template <typename Tag, int KG>
+__global__ void __launch_bounds__(kThreads) gram_simt_kernel(const StageArgs a) {
+  gram_tile_simt<Tag, KG>(a, blockIdx.x, blockIdx.y);
+}
+
 // --------------------------------------------------- pass 1: Gram (tensor cores, bf16)
 
 // D += A * B for one m16n8k16 bf16 tile with fp32 accumulation.
@@ -218,12 +222,11 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
 // (positions x workers).  Two k-steps of 16 cover the 32 positions; the two n-tiles
 // give columns 0-7 and 8-15 of G.
 template <int KG>
-__global__ void __launch_bounds__(kThreads) gram_mma_bf16_kernel(const StageArgs a) {
+__device__ __forceinline__ void gram_tile_mma(const StageArgs& a, int tile_id, int q) {
   static_assert(KG == 8 || KG == 16, "tensor-core Gram handles 8 or 16 workers");
   constexpr int E = tri_count(KG);
   constexpr int U = 4;        // chunks of 32 positions loaded per warp iteration
   constexpr int kFold = 4;    // iterations accumulated in the MMA before a Kahan fold
-  const int tile_id = blockIdx.x, q = blockIdx.y;
   const TileDesc t = a.tiles[tile_id];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, tq = lane & 3;
@@ -307,27 +310,47 @@ __global__ void __launch_bounds__(kThreads) gram_mma_bf16_kernel(const StageArgs
   }
 }
 
+template <int KG>
+__global__ void __launch_bounds__(kThreads) gram_mma_bf16_kernel(const StageArgs a) {
+  gram_tile_mma<KG>(a, blockIdx.x, blockIdx.y);
+}
+
+// Gram partial of one tile with the best engine for the element type and group size.
+template <typename Tag, int KG>
+__device__ __forceinline__ void gram_tile(const StageArgs& a, int tile_id, int q) {
+  if constexpr (ElemTraits<Tag>::kVW == 8 && (KG == 8 || KG == 16)) {
+    gram_tile_mma<KG>(a, tile_id, q);
+  } else {
+    gram_tile_simt<Tag, KG>(a, tile_id, q);
+  }
+}
+
 // ----------------------------------------------------------- coefficients (per segment)
 
 // Sum the fp32 tile partials of one chunk of at most kChunkTiles tiles (compensated,
 // in tile order) into one fp64 value per Gram entry.
+// (Partials written by other CTAs are read through L2, never a possibly stale L1.)
 template <int KG>
-__global__ void __launch_bounds__(kThreads) reduce_chunks_kernel(const StageArgs a) {
+__device__ __forceinline__ void reduce_chunk(const StageArgs& a, int c, int q) {
   constexpr int E = tri_count(KG);
-  const int c = blockIdx.x, q = blockIdx.y;
   const ChunkDesc ch = a.chunks[c];
-  for (int e = threadIdx.x; e < E; e += kThreads) {
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
     const float* p = a.partials + (static_cast<size_t>(q) * a.ntiles + ch.first_tile) * E + e;
     float v[kChunkTiles];
 #pragma unroll
     for (int t = 0; t < kChunkTiles; ++t)
-      v[t] = t < ch.ntiles ? p[static_cast<size_t>(t) * E] : 0.f;  // loads issued together
+      v[t] = t < ch.ntiles ? __ldcg(p + static_cast<size_t>(t) * E) : 0.f;  // issued together
     float sum = 0.f, comp = 0.f;
 #pragma unroll
     for (int t = 0; t < kChunkTiles; ++t) kahan_add(sum, comp, v[t]);
     a.chunk_sums[(static_cast<size_t>(q) * a.nchunks + c) * E + e] =
         static_cast<double>(sum) - static_cast<double>(comp);
   }
+}
+
+template <int KG>
+__global__ void __launch_bounds__(kThreads) reduce_chunks_kernel(const StageArgs a) {
+  reduce_chunk<KG>(a, blockIdx.x, blockIdx.y);
 }
 
 // Unpacks entry e of the packed upper triangle into (i, j), i <= j.
@@ -443,10 +466,10 @@ __device__ double coefficient_tree(const double (&G)[KG][KG], const double* eps,
 
 // Per segment: the Gram matrix from the chunk sums (fp64, chunk order), the tree
 // coefficients, and the conditioning check (see coefficient_tree).
+// Called by a whole CTA.
 template <int KG>
-__global__ void __launch_bounds__(128) coef_kernel(const StageArgs a) {
+__device__ __forceinline__ void segment_coefficients(const StageArgs& a, int seg, int q) {
   constexpr int E = tri_count(KG);
-  const int seg = blockIdx.x, q = blockIdx.y;
   const SegDesc sd = a.segs[seg];
   __shared__ double G[KG][KG];
   __shared__ double eps[KG];
@@ -454,7 +477,7 @@ __global__ void __launch_bounds__(128) coef_kernel(const StageArgs a) {
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     double sum = 0.0;
     const double* p = a.chunk_sums + (static_cast<size_t>(q) * a.nchunks + sd.first_chunk) * E + e;
-    for (int t = 0; t < sd.nchunks; ++t) sum += p[static_cast<size_t>(t) * E];
+    for (int t = 0; t < sd.nchunks; ++t) sum += __ldcg(p + static_cast<size_t>(t) * E);
     int i, j;
     tri_unpack(KG, e, i, j);
     G[i][j] = sum;
@@ -463,16 +486,23 @@ __global__ void __launch_bounds__(128) coef_kernel(const StageArgs a) {
   for (int k = threadIdx.x; k < KG; k += blockDim.x)
     eps[k] = a.in_relerr ? static_cast<double>(a.in_relerr[static_cast<size_t>(q * KG + k) * a.nsegs + seg]) : 0.0;
   __syncthreads();
-  if (threadIdx.x >= 32) return;
-  double c = 0.0;
-  bool ill = false;
-  const double rel = coefficient_tree<KG>(G, eps, kGramRelErr, snorm, c, ill);
-  if (threadIdx.x < KG)
-    a.coef[(static_cast<size_t>(q) * a.nsegs + seg) * KG + threadIdx.x] = static_cast<float>(c);
-  if (threadIdx.x == 0) {
-    if (a.relerr) a.relerr[static_cast<size_t>(q) * a.nsegs + seg] = static_cast<float>(fmin(rel, 1e30));
-    if (a.seg_flag && sd.len > 0 && (ill || !(rel <= kRelErrBudget))) a.seg_flag[seg] = 1;
+  if (threadIdx.x < 32) {
+    double c = 0.0;
+    bool ill = false;
+    const double rel = coefficient_tree<KG>(G, eps, kGramRelErr, snorm, c, ill);
+    if (threadIdx.x < KG)
+      a.coef[(static_cast<size_t>(q) * a.nsegs + seg) * KG + threadIdx.x] = static_cast<float>(c);
+    if (threadIdx.x == 0) {
+      if (a.relerr) a.relerr[static_cast<size_t>(q) * a.nsegs + seg] = static_cast<float>(fmin(rel, 1e30));
+      if (a.seg_flag && sd.len > 0 && (ill || !(rel <= kRelErrBudget))) a.seg_flag[seg] = 1;
+    }
   }
+  __syncthreads();
+}
+
+template <int KG>
+__global__ void __launch_bounds__(128) coef_kernel(const StageArgs a) {
+  segment_coefficients<KG>(a, blockIdx.x, blockIdx.y);
 }
 
 // ----------------------------------------------------------- pass 2: combine (+ step)
@@ -554,14 +584,14 @@ __device__ __forceinline__ void load_f32_vec(const float* x, int64_t p0, int64_t
 
 // out = sum_k c_k g_k over one tile; with MOM, also v' = mu v + out, w' = w - lr v'
 // (fp32), and out is written only when a.out[q] is not null.
+// (Coefficients and flags written by other CTAs are read through L2.)
 template <typename InTag, typename OutTag, int KG, bool MOM>
-__global__ void __launch_bounds__(kThreads) combine_kernel(const StageArgs a) {
+__device__ __forceinline__ void combine_tile(const StageArgs& a, int tile_id, int q) {
   using SI = typename ElemTraits<InTag>::Storage;
   using SO = typename ElemTraits<OutTag>::Storage;
   constexpr int VW = ElemTraits<InTag>::kVW;
-  const int tile_id = blockIdx.x, q = blockIdx.y;
   const TileDesc t = a.tiles[tile_id];
-  if (a.skip_flagged && a.seg_flag[t.seg]) return;  // left to the fp64 path
+  if (a.skip_flagged && __ldcg(a.seg_flag + t.seg)) return;  // left to the fp64 path
   const bool aligned = a.aligned != 0;
   float c[KG];
   if constexpr (KG == 1) {
@@ -569,7 +599,7 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const StageArgs a) {
   } else {
     const float* cp = a.coef + (static_cast<size_t>(q) * a.nsegs + t.seg) * KG;
 #pragma unroll
-    for (int k = 0; k < KG; ++k) c[k] = cp[k];
+    for (int k = 0; k < KG; ++k) c[k] = __ldcg(cp + k);
   }
   const SI* x[KG];
 #pragma unroll
@@ -599,6 +629,95 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const StageArgs a) {
       if (y != nullptr) store_vec<OutTag, VW>(y, p0, lo, hi, aligned, val);
     } else {
       store_vec<OutTag, VW>(y, p0, lo, hi, aligned, val);
+    }
+  }
+}
+
+template <typename InTag, typename OutTag, int KG, bool MOM>
+__global__ void __launch_bounds__(kThreads) combine_kernel(const StageArgs a) {
+  combine_tile<InTag, OutTag, KG, MOM>(a, blockIdx.x, blockIdx.y);
+}
+
+// ------------------------------------------------------------- fused single-stage kernel
+//
+// One persistent kernel runs the whole fp32 pass of a single-stage call: CTAs claim
+// tasks from a host-built list (PipeArgs).  The list groups segments into waves of a
+// few tens of MB and interleaves the Gram tiles of wave w with the combine tiles of
+// wave w-1 (taken in reverse order), so the second read of the inputs finds them in
+// L2 instead of HBM.  A segment's coefficients are computed by the CTA that finishes
+// its last Gram chunk (the last tile of a chunk reduces the chunk; the last chunk of a
+// segment runs the tree) and published with a release store; its combine tiles wait
+// for that flag with an acquire load, bounded by a clock budget.
+
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_gpu(int* p, int v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// After a Gram tile: count it in its chunk; the chunk's last tile reduces the chunk and
+// counts it in its segment; the segment's last chunk computes the coefficients and
+// publishes them.  Called by the whole CTA.
+template <int KG>
+__device__ __forceinline__ void arrive_tile(const StageArgs& a, const PipeArgs& p, int tile_id) {
+  __shared__ int last;
+  const TileDesc t = a.tiles[tile_id];
+  const SegDesc sd = a.segs[t.seg];
+  const int c = sd.first_chunk + (tile_id - sd.first_tile) / kChunkTiles;
+  __threadfence();  // this CTA's partial is visible before it is counted
+  __syncthreads();
+  if (threadIdx.x == 0) last = atomicAdd(p.chunk_done + c, 1) == a.chunks[c].ntiles - 1;
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  reduce_chunk<KG>(a, c, 0);
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) last = atomicAdd(p.seg_done + t.seg, 1) == sd.nchunks - 1;
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  segment_coefficients<KG>(a, t.seg, 0);
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0 && !p.inject_no_ready) st_release_gpu(p.seg_ready + t.seg, 1);
+}
+
+// Thread 0 waits (bounded) for a segment's coefficients; returns 1 when published.
+__device__ __forceinline__ int wait_ready(const PipeArgs& p, int seg) {
+  if (ld_acquire_gpu(p.seg_ready + seg)) return 1;
+  const long long t0 = clock64();
+  for (;;) {
+    __nanosleep(128);
+    if (ld_acquire_gpu(p.seg_ready + seg)) return 1;
+    if (clock64() - t0 > p.spin_budget) {
+      atomicOr(p.error, 1);
+      return 0;
+    }
+  }
+}
+
+template <typename InTag, typename OutTag, int KG, bool MOM>
+__global__ void __launch_bounds__(kThreads, 3) pipeline_kernel(const StageArgs a, const PipeArgs p) {
+  __shared__ int s_task, s_ok;
+  for (;;) {
+    if (threadIdx.x == 0) s_task = atomicAdd(p.task_counter, 1);
+    __syncthreads();
+    const int ti = s_task;
+    __syncthreads();
+    if (ti >= p.ntasks) return;
+    const int task = __ldg(p.tasks + ti);
+    if (task >= 0) {
+      gram_tile<InTag, KG>(a, task, 0);
+      arrive_tile<KG>(a, p, task);
+    } else {
+      const int tile_id = task & 0x7FFFFFFF;
+      if (threadIdx.x == 0) s_ok = wait_ready(p, a.tiles[tile_id].seg);
+      __syncthreads();
+      if (s_ok) combine_tile<InTag, OutTag, KG, MOM>(a, tile_id, 0);
     }
   }
 }

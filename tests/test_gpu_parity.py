@@ -341,3 +341,44 @@ def test_well_conditioned_data_stays_on_the_fast_path(native):
     wl = workloads.make("resnet50_k8", device=DEV, shrink=16)
     ags.reduce(wl.grads, wl.seg_offsets)
     assert ags.recomputed_segments() == 0
+
+
+# ------------------------------------------------- both routes, and the bounded wait
+
+@pytest.mark.parametrize("name,shrink", [("resnet50_k8", 16), ("bert_large_k16", 256),
+                                         ("pair_1m", 1)])
+def test_fused_route_matches_oracle(native, monkeypatch, name, shrink):
+    """Single-stage calls run the three-kernel route by default; the fused persistent
+    kernel (ADASUM_ROUTE=fused) must agree with the oracle too."""
+    monkeypatch.setenv("ADASUM_ROUTE", "fused")
+    wl = workloads.make(name, device=DEV, shrink=shrink)
+    out = ags.reduce(wl.grads, wl.seg_offsets)
+    torch.cuda.synchronize()
+    check_against_oracle(wl.grads, wl.seg_offsets, out)
+
+
+def test_routes_agree(native, monkeypatch):
+    wl = workloads.make("bert_large_k16", device=DEV, shrink=128)
+    split = ags.reduce(wl.grads, wl.seg_offsets).clone()
+    monkeypatch.setenv("ADASUM_ROUTE", "fused")
+    monkeypatch.setenv("ADASUM_PIPE_TILE_KB", "256")   # same tiles, so the same sums
+    fused = ags.reduce(wl.grads, wl.seg_offsets)
+    torch.cuda.synchronize()
+    assert torch.equal(fused, split)
+
+
+def test_bounded_wait_reports_timeout(native, monkeypatch):
+    """A lost ready flag (injected on the host: the fused kernel never publishes) must
+    end in a status, not a hang: the combine tasks give up after their clock budget."""
+    grads = rand_grads(4, 50_000, torch.float32, seed=60)
+    assert ags.get_last_error() == ags.Status.OK
+    monkeypatch.setenv("ADASUM_ROUTE", "fused")
+    monkeypatch.setenv("ADASUM_FAULT_INJECT", "timeout")
+    ags.reduce(grads, [0, 20_000, 50_000])
+    torch.cuda.synchronize()
+    assert ags.get_last_error() == ags.Status.ERR_TIMEOUT
+    assert ags.get_last_error() == ags.Status.OK          # reading clears it
+    monkeypatch.delenv("ADASUM_FAULT_INJECT")
+    out = ags.reduce(grads, [0, 20_000, 50_000])          # the context is still usable
+    torch.cuda.synchronize()
+    check_against_oracle(grads, [0, 20_000, 50_000], out)
