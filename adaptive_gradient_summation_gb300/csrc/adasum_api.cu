@@ -21,6 +21,7 @@
 
 #include "../../include/adasum.h"
 #include "adasum_internal.h"
+#include "adasum_stream.cuh"
 
 namespace adasum {
 namespace {
@@ -29,12 +30,18 @@ constexpr int kVersion = 100;  // 0.1.0
 
 int elem_size(int dt) { return dt == kBF16 ? 2 : 4; }
 
-// Single-stage calls run the three-kernel route (Gram / coefficients / combine as
-// separate launches); ADASUM_ROUTE=fused selects the fused persistent kernel instead.
-bool route_fused() {
+// Route of a single-stage call: the three-kernel route (Gram / coefficients / combine
+// as separate launches), the streaming kernel (adasum_stream.cuh), or the dynamically
+// scheduled fused kernel.  ADASUM_ROUTE=kernels|stream|fused selects one explicitly.
+enum Route { kRouteKernels = 0, kRouteStream = 1, kRouteFused = 2 };
+
+int requested_route() {
   const char* v = std::getenv("ADASUM_ROUTE");
-  return v != nullptr && std::strcmp(v, "fused") == 0;
+  if (v != nullptr && std::strcmp(v, "fused") == 0) return kRouteFused;
+  if (v != nullptr && std::strcmp(v, "stream") == 0) return kRouteStream;
+  return kRouteKernels;
 }
+bool route_fused() { return requested_route() == kRouteFused; }
 
 // A positive integer from the environment (tuning knobs), else `dflt`.
 int64_t env_int(const char* name, int64_t dflt) {
@@ -90,6 +97,12 @@ struct Plan {
   int64_t wave_bytes = 0;
   int64_t tile_kb = 0;
   int64_t delay_pct = 0;
+  // streaming kernel: per-CTA task lists (CSR) and the round-robin start of each segment
+  int route = kRouteKernels;
+  int stream_grid = 0;
+  int stage_pos = 0;
+  int* d_task_ptr = nullptr;
+  int* d_seg_c0 = nullptr;
 };
 
 struct Workspace {
@@ -116,6 +129,10 @@ void free_plan(Plan& p) {
   if (p.d_segs) cudaFree(p.d_segs);
   if (p.d_chunks) cudaFree(p.d_chunks);
   if (p.d_tasks) cudaFree(p.d_tasks);
+  if (p.d_task_ptr) cudaFree(p.d_task_ptr);
+  if (p.d_seg_c0) cudaFree(p.d_seg_c0);
+  p.d_task_ptr = nullptr;
+  p.d_seg_c0 = nullptr;
   p.d_tiles = nullptr;
   p.d_segs = nullptr;
   p.d_chunks = nullptr;
@@ -204,13 +221,87 @@ int64_t tile_positions(int Kg, int dtype, int64_t N, int num_sms, bool fused) {
   return (T + 255) / 256 * 256;
 }
 
-adasum_status_t get_plan(Workspace& ws, const int64_t* offs, int L, int Kg0, int dtype,
+// Positions per stage of the streaming kernel: 64 KiB of input (rounded to 32).
+int stream_stage_pos(int Kg, int dtype) {
+  const int64_t kb = env_int("ADASUM_STREAM_STAGE_KB", 64);
+  return static_cast<int>(std::max<int64_t>(32, (kb << 10) / (int64_t(Kg) * elem_size(dtype)) / 32 * 32));
+}
+
+// Per-CTA task lists of the streaming kernel.  Segments are grouped into waves of about
+// wave_bytes of input; the tiles of a wave are dealt round robin to the G CTAs, and
+// every CTA runs  Gram(wave 0), Gram(wave 1), Combine(wave 0), Gram(wave 2),
+// Combine(wave 1), ..., Combine(last wave)  over its own share.  A combine task of
+// wave w therefore comes one wave after that wave's Gram tasks, on every CTA.
+void build_stream_tasks(const std::vector<SegDesc>& segs, int64_t bytes_per_pos,
+                        int64_t wave_bytes, int G, std::vector<int>& task_ptr,
+                        std::vector<int>& tasks, std::vector<int>& seg_c0) {
+  std::vector<std::vector<int>> waves;
+  int64_t cur = 0;
+  for (int s = 0; s < static_cast<int>(segs.size()); ++s) {
+    if (segs[s].ntiles == 0) continue;
+    const int64_t b = segs[s].len * bytes_per_pos;
+    if (waves.empty() || (cur > 0 && cur + b > wave_bytes)) {
+      waves.emplace_back();
+      cur = 0;
+    }
+    waves.back().push_back(s);
+    cur += b;
+  }
+  seg_c0.assign(segs.size(), 0);
+  std::vector<std::vector<int>> per(G);
+  std::vector<std::vector<int>> prev_b(G);
+  for (size_t w = 0; w <= waves.size(); ++w) {
+    std::vector<std::vector<int>> cur_b(G);
+    if (w < waves.size()) {
+      int j = 0;
+      std::vector<int> all;
+      for (int sg : waves[w]) {
+        seg_c0[sg] = j % G;
+        for (int i = 0; i < segs[sg].ntiles; ++i, ++j) {
+          per[j % G].push_back(segs[sg].first_tile + i);
+          all.push_back(segs[sg].first_tile + i);
+        }
+      }
+      int jb = 0;
+      for (auto it = all.rbegin(); it != all.rend(); ++it, ++jb)
+        cur_b[jb % G].push_back(static_cast<int>(0x80000000u | static_cast<uint32_t>(*it)));
+    }
+    for (int c = 0; c < G; ++c) per[c].insert(per[c].end(), prev_b[c].begin(), prev_b[c].end());
+    prev_b.swap(cur_b);
+  }
+  task_ptr.assign(G + 1, 0);
+  tasks.clear();
+  for (int c = 0; c < G; ++c) {
+    task_ptr[c] = static_cast<int>(tasks.size());
+    tasks.insert(tasks.end(), per[c].begin(), per[c].end());
+  }
+  task_ptr[G] = static_cast<int>(tasks.size());
+}
+
+template <typename T>
+adasum_status_t upload(T** dst, const std::vector<T>& v) {
+  if (cudaMalloc(dst, std::max<size_t>(1, v.size()) * sizeof(T)) != cudaSuccess) {
+    cudaGetLastError();
+    *dst = nullptr;
+    return ADASUM_ERR_NO_MEMORY;
+  }
+  // Synchronous copy: a plan is immutable once built, so no later call can race with it.
+  if (!v.empty() && cudaMemcpy(*dst, v.data(), v.size() * sizeof(T), cudaMemcpyHostToDevice) != cudaSuccess) {
+    cudaGetLastError();
+    return ADASUM_ERR_CUDA;
+  }
+  return ADASUM_OK;
+}
+
+adasum_status_t get_plan(Workspace& ws, const int64_t* offs, int L, int Kg0, int dtype, int route,
                          Plan** out) {
+  const int64_t wave = route == kRouteStream ? env_int("ADASUM_WAVE_MB", 24) << 20 : wave_budget_bytes();
   for (auto it = ws.plans.begin(); it != ws.plans.end(); ++it) {
-    if (it->Kg0 == Kg0 && it->dtype == dtype && (it->d_tasks != nullptr) == route_fused() &&
-        (it->d_tasks == nullptr || (it->wave_bytes == wave_budget_bytes() &&
-                                    it->tile_kb == (tile_bytes(true) >> 10) &&
-                                    it->delay_pct == env_int("ADASUM_PIPE_DELAY_PCT", 100))) &&
+    if (it->Kg0 == Kg0 && it->dtype == dtype && it->route == route &&
+        (route == kRouteKernels ||
+         (it->wave_bytes == wave && it->tile_kb == (tile_bytes(true) >> 10) &&
+          it->delay_pct == env_int("ADASUM_PIPE_DELAY_PCT", 100) &&
+          it->stage_pos == (route == kRouteStream ? stream_stage_pos(Kg0, dtype) : 0))) &&
         it->offsets.size() == static_cast<size_t>(L + 1) &&
         std::memcmp(it->offsets.data(), offs, sizeof(int64_t) * (L + 1)) == 0) {
       ws.plans.splice(ws.plans.begin(), ws.plans, it);
@@ -221,8 +312,12 @@ adasum_status_t get_plan(Workspace& ws, const int64_t* offs, int L, int Kg0, int
   int num_sms = 148;
   cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, ws.device);
   const int64_t N = offs[L];
-  const bool fused = Kg0 <= kMaxGroup && Kg0 > 1 && route_fused();
-  const int64_t T = tile_positions(Kg0, dtype, N, num_sms, fused);
+  int64_t T = 0;
+  if (route == kRouteStream) {
+    T = stream_stage_pos(Kg0, dtype);
+  } else {
+    T = tile_positions(Kg0, dtype, N, num_sms, route == kRouteFused);
+  }
   std::vector<TileDesc> tiles;
   std::vector<SegDesc> segs(L);
   std::vector<ChunkDesc> chunks;
@@ -245,7 +340,7 @@ adasum_status_t get_plan(Workspace& ws, const int64_t* offs, int L, int Kg0, int
       chunks.push_back(ChunkDesc{segs[s].first_tile + t, std::min(kChunkTiles, segs[s].ntiles - t)});
     segs[s].nchunks = static_cast<int32_t>(chunks.size()) - segs[s].first_chunk;
   }
-  if (tiles.size() > static_cast<size_t>(INT32_MAX)) return ADASUM_ERR_UNSUPPORTED;
+  if (tiles.size() > static_cast<size_t>(INT32_MAX / 2)) return ADASUM_ERR_UNSUPPORTED;
   if (ws.plans.size() >= 8) {
     free_plan(ws.plans.back());
     ws.plans.pop_back();
@@ -254,48 +349,37 @@ adasum_status_t get_plan(Workspace& ws, const int64_t* offs, int L, int Kg0, int
   p.offsets.assign(offs, offs + L + 1);
   p.Kg0 = Kg0;
   p.dtype = dtype;
+  p.route = route;
   p.ntiles = static_cast<int>(tiles.size());
   p.nsegs = L;
   p.nchunks = static_cast<int>(chunks.size());
-  if (cudaMalloc(&p.d_tiles, std::max<size_t>(1, tiles.size()) * sizeof(TileDesc)) != cudaSuccess ||
-      cudaMalloc(&p.d_segs, std::max<size_t>(1, segs.size()) * sizeof(SegDesc)) != cudaSuccess ||
-      cudaMalloc(&p.d_chunks, std::max<size_t>(1, chunks.size()) * sizeof(ChunkDesc)) != cudaSuccess) {
-    free_plan(p);
-    cudaGetLastError();
-    return ADASUM_ERR_NO_MEMORY;
-  }
-  // Synchronous copies: the plan is immutable once built, so no later call can race
-  // with them.  A new plan is built only for offsets not seen among the last eight.
-  if (cudaMemcpy(p.d_tiles, tiles.data(), tiles.size() * sizeof(TileDesc),
-                 cudaMemcpyHostToDevice) != cudaSuccess ||
-      cudaMemcpy(p.d_segs, segs.data(), segs.size() * sizeof(SegDesc),
-                 cudaMemcpyHostToDevice) != cudaSuccess ||
-      cudaMemcpy(p.d_chunks, chunks.data(), chunks.size() * sizeof(ChunkDesc),
-                 cudaMemcpyHostToDevice) != cudaSuccess) {
-    free_plan(p);
-    cudaGetLastError();
-    return ADASUM_ERR_CUDA;
-  }
-  if (fused) {
-    const int delay = static_cast<int>(
-        env_int("ADASUM_PIPE_DELAY_PCT", 100) * pipeline_grid(dtype, dtype, Kg0, 0, num_sms) / 100);
-    p.wave_bytes = wave_budget_bytes();
-    p.tile_kb = tile_bytes(true) >> 10;
-    p.delay_pct = env_int("ADASUM_PIPE_DELAY_PCT", 100);
+  p.wave_bytes = wave;
+  p.tile_kb = tile_bytes(true) >> 10;
+  p.delay_pct = env_int("ADASUM_PIPE_DELAY_PCT", 100);
+  adasum_status_t st = upload(&p.d_tiles, tiles);
+  if (!st) st = upload(&p.d_segs, segs);
+  if (!st) st = upload(&p.d_chunks, chunks);
+  if (!st && route == kRouteFused) {
+    const int delay = static_cast<int>(p.delay_pct * pipeline_grid(dtype, dtype, Kg0, 0, num_sms) / 100);
     const std::vector<int> tasks =
         build_tasks(segs, static_cast<int64_t>(Kg0) * elem_size(dtype), p.wave_bytes, delay);
     p.ntasks = static_cast<int>(tasks.size());
-    if (cudaMalloc(&p.d_tasks, std::max<size_t>(1, tasks.size()) * sizeof(int)) != cudaSuccess) {
-      free_plan(p);
-      cudaGetLastError();
-      return ADASUM_ERR_NO_MEMORY;
-    }
-    if (cudaMemcpy(p.d_tasks, tasks.data(), tasks.size() * sizeof(int), cudaMemcpyHostToDevice) !=
-        cudaSuccess) {
-      free_plan(p);
-      cudaGetLastError();
-      return ADASUM_ERR_CUDA;
-    }
+    st = upload(&p.d_tasks, tasks);
+  }
+  if (!st && route == kRouteStream) {
+    std::vector<int> task_ptr, tasks, seg_c0;
+    p.stage_pos = static_cast<int>(T);
+    p.stream_grid = std::min(num_sms, 256);  // the finisher sums at most 256 CTA partials
+    build_stream_tasks(segs, static_cast<int64_t>(Kg0) * elem_size(dtype), p.wave_bytes,
+                       p.stream_grid, task_ptr, tasks, seg_c0);
+    p.ntasks = static_cast<int>(tasks.size());
+    st = upload(&p.d_tasks, tasks);
+    if (!st) st = upload(&p.d_task_ptr, task_ptr);
+    if (!st) st = upload(&p.d_seg_c0, seg_c0);
+  }
+  if (st) {
+    free_plan(p);
+    return st;
   }
   ws.plans.push_front(std::move(p));
   *out = &ws.plans.front();
@@ -482,8 +566,13 @@ adasum_status_t reduce_impl(const void* const* grads, int K, const int64_t* offs
     }
   }
 
+  int route = kRouteKernels;
+  if (kg.size() == 1 && kg[0] > 1) {
+    route = requested_route();
+    if (route == kRouteStream && !stream_supported(dtype, kg[0])) route = kRouteKernels;
+  }
   Plan* plan = nullptr;
-  if (adasum_status_t st = get_plan(ws, offs, L, kg[0], dtype, &plan)) return st;
+  if (adasum_status_t st = get_plan(ws, offs, L, kg[0], dtype, route, &plan)) return st;
 
   // Workspace layout.
   size_t max_e_tiles = 0, max_e_chunks = 0, max_coef = 0, max_g = 1;
@@ -511,6 +600,10 @@ adasum_status_t reduce_impl(const void* const* grads, int K, const int64_t* offs
   const size_t o_ltiles = cv.take(static_cast<size_t>(plan->ntiles) * sizeof(int));
   const size_t o_lsegs = cv.take(static_cast<size_t>(L) * sizeof(int));
   const size_t o_ltiny = cv.take(static_cast<size_t>(L) * sizeof(int));
+  const size_t o_slots = cv.take(route == kRouteStream
+                                     ? static_cast<size_t>(L) * plan->stream_grid *
+                                           (static_cast<size_t>(kg[0]) * (kg[0] + 1) / 2) * sizeof(float)
+                                     : 0);
   // Stage outputs of every non-final stage: fp32 (fast pass) and fp64 (recompute).
   std::vector<size_t> off32(kg.size(), 0), off64(kg.size(), 0);
   for (size_t s = 0; s + 1 < kg.size(); ++s) {
@@ -575,8 +668,35 @@ adasum_status_t reduce_impl(const void* const* grads, int K, const int64_t* offs
     return a;
   };
 
-  // fp32 pass: one fused kernel for a single stage, else stage by stage.
-  const bool fused = kg.size() == 1 && kg[0] > 1 && plan->d_tasks != nullptr && route_fused();
+  // fp32 pass: one streaming or fused kernel for a single stage, else stage by stage.
+  if (route == kRouteStream) {
+    StageArgs a = make_args(0);
+    for (int k = 0; k < K; ++k) a.in[k] = grads[k];
+    a.out[0] = out;
+    a.skip_flagged = 1;
+    a.relerr = reinterpret_cast<float*>(base + o_rel0);
+    StreamArgs sa;
+    std::memset(&sa, 0, sizeof sa);
+    sa.task_ptr = plan->d_task_ptr;
+    sa.tasks = plan->d_tasks;
+    sa.seg_c0 = plan->d_seg_c0;
+    sa.slots = reinterpret_cast<float*>(base + o_slots);
+    sa.seg_count = seg_done;
+    sa.seg_ready = seg_ready;
+    sa.error = ws.d_error;
+    sa.spin_budget = 2000000000LL;  // about one second of SM clock
+    if (inject_timeout()) {
+      sa.inject_no_ready = 1;
+      sa.spin_budget = 200000LL;
+    }
+    sa.stage_pos = plan->stage_pos;
+    sa.row_bytes = plan->stage_pos * static_cast<int>(es) + kRowPad;
+    if (adasum_status_t st = launch_one(stream, [&](const char** n) {
+          return launch_stream(a, sa, dtype, mom ? 1 : 0, plan->stream_grid, stream, n);
+        }))
+      return st;
+  }
+  const bool fused = route == kRouteFused;
   if (fused) {
     StageArgs a = make_args(0);
     for (int k = 0; k < K; ++k) a.in[k] = grads[k];
@@ -602,7 +722,7 @@ adasum_status_t reduce_impl(const void* const* grads, int K, const int64_t* offs
         }))
       return st;
   }
-  for (size_t s = 0; s < kg.size() && !fused; ++s) {
+  for (size_t s = 0; s < kg.size() && route == kRouteKernels; ++s) {
     const bool last = s + 1 == kg.size();
     StageArgs a = make_args(s);
     if (s == 0) {

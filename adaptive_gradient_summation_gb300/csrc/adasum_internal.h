@@ -130,6 +130,13 @@ int launch_combine_f32in(const StageArgs& a, int out_dtype, int momentum, void* 
                          const char** name);
 int launch_combine_bf16in(const StageArgs& a, int out_dtype, int momentum, void* stream,
                           const char** name);
+// Streaming single-stage kernel (adasum_stream.cuh): one CTA per SM, cooperative launch.
+struct StreamArgs;
+bool stream_supported(int dtype, int Kg);
+int stream_smem_bytes(int dtype, int Kg, int stage_pos);
+int launch_stream(const StageArgs& a, const StreamArgs& s, int dtype, int momentum, int grid,
+                  void* stream, const char** name);
+
 // Fused single-stage kernel (K <= 16): grid = persistent CTAs, see PipeArgs.
 int launch_pipeline(const StageArgs& a, const PipeArgs& p, int in_dtype, int out_dtype,
                     int momentum, int grid, void* stream, const char** name);
