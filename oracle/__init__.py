@@ -55,6 +55,8 @@ def open_library(path: str):
                                          ctypes.POINTER(i64), ctypes.c_int,
                                          ctypes.c_int, vp, dp, dp, dp]
     lib.oracle_adasum_reduce.restype = ctypes.c_int
+    lib.oracle_adasum_chain.argtypes = lib.oracle_adasum_reduce.argtypes
+    lib.oracle_adasum_chain.restype = ctypes.c_int
     lib.oracle_adasum_pair.argtypes = [vp, vp, i64, ctypes.c_int, vp, dp]
     lib.oracle_adasum_pair.restype = ctypes.c_int
     lib.oracle_momentum_sgd.argtypes = [dp, i64, vp, vp, ctypes.c_double,
@@ -90,7 +92,7 @@ def _dptr(a):
 
 
 def adasum_reduce(grads, seg_offsets, *, want_out=True, want_mag=False, want_ortho=False,
-                  lib=None):
+                  lib=None, chain=False):
     """Adasum of K worker gradients, per segment, as a binary tree (fp64).
 
     grads: sequence of K 1-D arrays (all float32, or all uint16 bf16 bits) of equal length.
@@ -98,6 +100,8 @@ def adasum_reduce(grads, seg_offsets, *, want_out=True, want_mag=False, want_ort
     Returns a dict with ``out64`` (fp64 result), ``out`` (rounded to the input dtype),
     and optionally ``mag`` (magnitude bound per element) and ``ortho`` (per segment).
     ``lib`` selects another compiled copy of the oracle (default: the one built here).
+    ``chain=True`` uses the linear recursion g[0,n+1] = Adasum(g[0,n], g_{n+1}) instead of
+    the binary tree.
     """
     lib = _load(lib)
     grads = [np.ascontiguousarray(g) for g in grads]
@@ -118,7 +122,8 @@ def adasum_reduce(grads, seg_offsets, *, want_out=True, want_mag=False, want_ort
     out = np.empty(n, dtype=grads[0].dtype) if want_out else None
     mag = np.empty(n, dtype=np.float64) if want_mag else None
     ortho = np.empty(max(L, 0), dtype=np.float64) if want_ortho else None
-    rc = lib.oracle_adasum_reduce(ptrs, K, offs.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
+    fn = lib.oracle_adasum_chain if chain else lib.oracle_adasum_reduce
+    rc = fn(ptrs, K, offs.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
                                   L, code, None if out is None else out.ctypes.data,
                                   _dptr(out64), _dptr(mag), _dptr(ortho))
     if rc != 0:

@@ -18,6 +18,9 @@
  *     recursive application used in practice because it moves fewer bytes): level 0
  *     pairs (2i, 2i+1), the next level pairs the level-0 results the same way, log2(K)
  *     levels in all.
+ *   - The linear recursion the same section states first: g[0,n+1] = Adasum(g[0,n],
+ *     g_{n+1}), i.e. a chain folding the workers in from left to right
+ *     (oracle_adasum_chain).
  *   - Per-layer application (Section 3, after Figure 1): every segment of the flat
  *     gradient is combined on its own, with its own dot products and norms.
  *   - Special cases (Section 3, discussion after the tree): orthogonal inputs sum,
@@ -30,6 +33,9 @@
  *   - bf16 storage: inputs are decoded exactly, every intermediate stays in fp64, and
  *     the final result is rounded once, to nearest with ties to even.
  *   - Sums are taken in plain sequential order.
+ *   - A worker count that is not a power of two: at every level pairs (2i, 2i+1) are
+ *     combined and an unpaired last vector passes to the next level unchanged.  (This
+ *     equals padding with zero gradients, because Adasum(x, 0) = x.)
  *   - Fused Momentum-SGD (heavy ball): v' = mu v + A, w' = w - lr v', evaluated in fp64
  *     from the unrounded Adasum result A and rounded to fp32 at the end.
  *
@@ -93,7 +99,6 @@ static void store_elem(void *base, int dtype, int64_t i, double v) {
     ((uint16_t *)base)[i] = oracle_bf16_encode(v);
 }
 
-static int is_pow2(int k) { return k >= 1 && (k & (k - 1)) == 0; }
 
 /* One Adasum pair on fp64 vectors of length n, written to dst.  dst may equal a.
  * When mdst is given, it also carries the magnitude bound m = |alpha| m_a + |beta| m_b
@@ -115,16 +120,17 @@ static void adasum_pair_f64(double *dst, const double *a, const double *b, int64
   }
 }
 
-/* Adasum over K workers (K a power of two) for every segment [offs[s], offs[s+1]).
- *   grads  : K host pointers, each to offs[L] elements of `dtype`.
- *   out    : optional, offs[L] elements of `dtype`, the rounded result.
- *   out64  : optional, offs[L] doubles, the unrounded fp64 result.
- *   mag    : optional, offs[L] doubles, the magnitude bound m per element.
- *   ortho  : optional, L doubles, |A|^2 / sum_k |g_k|^2 per segment (NaN for 0/0).
- * Returns ORACLE_OK, ORACLE_ERR_ARG or ORACLE_ERR_NOMEM. */
-int oracle_adasum_reduce(const void *const *grads, int K, const int64_t *offs, int L,
-                         int dtype, void *out, double *out64, double *mag, double *ortho) {
-  if (!grads || !offs || !is_pow2(K) || L < 0) return ORACLE_ERR_ARG;
+/* Shared by the tree and the chain: validates arguments and, per segment, loads the K
+ * inputs into level[] (and their magnitudes), calls `combine` to reduce them into
+ * level[0], then writes the outputs. */
+typedef void (*combine_fn)(double *level, double *mlevel, int K, int64_t n);
+
+static void tree_levels(double *level, double *mlevel, int K, int64_t n);
+static void chain_levels(double *level, double *mlevel, int K, int64_t n);
+
+static int run_segments(const void *const *grads, int K, const int64_t *offs, int L, int dtype,
+                        void *out, double *out64, double *mag, double *ortho, combine_fn combine) {
+  if (!grads || !offs || K < 1 || L < 0) return ORACLE_ERR_ARG;
   if (dtype != ORACLE_F32 && dtype != ORACLE_BF16) return ORACLE_ERR_ARG;
   if (offs[0] < 0) return ORACLE_ERR_ARG;
   for (int s = 0; s < L; ++s)
@@ -156,20 +162,7 @@ int oracle_adasum_reduce(const void *const *grads, int K, const int64_t *offs, i
         if (mlevel) mlevel[(size_t)k * (size_t)n + j] = fabs(v[j]);
       }
     }
-    /* Binary tree: the pair (2i, 2i+1) of one level becomes vector i of the next.
-     * Writing result i into slot i is safe: slots 2i and 2i+1 are read first, and
-     * slots below 2i were already consumed by earlier pairs of the same level. */
-    for (int width = K; width > 1; width /= 2) {
-      for (int i = 0; i < width / 2; ++i) {
-        double *dst = level + (size_t)i * (size_t)n;
-        const double *a = level + (size_t)(2 * i) * (size_t)n;
-        const double *b = level + (size_t)(2 * i + 1) * (size_t)n;
-        double *mdst = mlevel ? mlevel + (size_t)i * (size_t)n : NULL;
-        const double *ma = mlevel ? mlevel + (size_t)(2 * i) * (size_t)n : NULL;
-        const double *mb = mlevel ? mlevel + (size_t)(2 * i + 1) * (size_t)n : NULL;
-        adasum_pair_f64(dst, a, b, n, mdst, ma, mb);
-      }
-    }
+    combine(level, mlevel, K, n);
     double rsq = 0.0;
     for (int64_t j = 0; j < n; ++j) {
       rsq += level[j] * level[j];
@@ -182,6 +175,56 @@ int oracle_adasum_reduce(const void *const *grads, int K, const int64_t *offs, i
     free(mlevel);
   }
   return ORACLE_OK;
+}
+
+/* Binary tree: the pair (2i, 2i+1) of one level becomes vector i of the next; with an odd
+ * count the last vector moves on unchanged.  Writing result i into slot i is safe: slots
+ * 2i and 2i+1 are read first, and slots below 2i were already consumed by earlier pairs
+ * of the same level (the carried vector's new slot width/2 likewise). */
+static void tree_levels(double *level, double *mlevel, int K, int64_t n) {
+  for (int width = K; width > 1; width = (width + 1) / 2) {
+    for (int i = 0; i < width / 2; ++i) {
+        double *dst = level + (size_t)i * (size_t)n;
+        const double *a = level + (size_t)(2 * i) * (size_t)n;
+        const double *b = level + (size_t)(2 * i + 1) * (size_t)n;
+        double *mdst = mlevel ? mlevel + (size_t)i * (size_t)n : NULL;
+        const double *ma = mlevel ? mlevel + (size_t)(2 * i) * (size_t)n : NULL;
+        const double *mb = mlevel ? mlevel + (size_t)(2 * i + 1) * (size_t)n : NULL;
+        adasum_pair_f64(dst, a, b, n, mdst, ma, mb);
+    }
+    if (width % 2 == 1) {
+      const size_t from = (size_t)(width - 1) * (size_t)n, to = (size_t)(width / 2) * (size_t)n;
+      memmove(level + to, level + from, (size_t)n * sizeof(double));
+      if (mlevel) memmove(mlevel + to, mlevel + from, (size_t)n * sizeof(double));
+    }
+  }
+}
+
+/* Linear chain: g[0,k] = Adasum(g[0,k-1], g_k), accumulated in slot 0. */
+static void chain_levels(double *level, double *mlevel, int K, int64_t n) {
+  for (int k = 1; k < K; ++k) {
+    const double *b = level + (size_t)k * (size_t)n;
+    adasum_pair_f64(level, level, b, n, mlevel, mlevel, mlevel ? mlevel + (size_t)k * (size_t)n : NULL);
+  }
+}
+
+/* Adasum over K workers (any K >= 1) as a binary tree, for every segment
+ * [offs[s], offs[s+1]).
+ *   grads  : K host pointers, each to offs[L] elements of `dtype`.
+ *   out    : optional, offs[L] elements of `dtype`, the rounded result.
+ *   out64  : optional, offs[L] doubles, the unrounded fp64 result.
+ *   mag    : optional, offs[L] doubles, the magnitude bound m per element.
+ *   ortho  : optional, L doubles, |A|^2 / sum_k |g_k|^2 per segment (NaN for 0/0).
+ * Returns ORACLE_OK, ORACLE_ERR_ARG or ORACLE_ERR_NOMEM. */
+int oracle_adasum_reduce(const void *const *grads, int K, const int64_t *offs, int L,
+                         int dtype, void *out, double *out64, double *mag, double *ortho) {
+  return run_segments(grads, K, offs, L, dtype, out, out64, mag, ortho, tree_levels);
+}
+
+/* The same outputs for the linear chain g[0,n+1] = Adasum(g[0,n], g_{n+1}). */
+int oracle_adasum_chain(const void *const *grads, int K, const int64_t *offs, int L,
+                        int dtype, void *out, double *out64, double *mag, double *ortho) {
+  return run_segments(grads, K, offs, L, dtype, out, out64, mag, ortho, chain_levels);
 }
 
 /* The two-worker case: one segment of n elements. */

@@ -84,6 +84,26 @@ def adasum_tree_exact(vectors):
     return adasum_pair_exact(left, right)
 
 
+def adasum_chain_exact(vectors):
+    """The linear recursion of the same section: g[0,n+1] = Adasum(g[0,n], g_{n+1})."""
+    acc = _vec(vectors[0])
+    for v in vectors[1:]:
+        acc = adasum_pair_exact(acc, v)
+    return acc
+
+
+def adasum_tree_exact_padded(vectors):
+    """A tree over any number of vectors, taken as the power-of-two tree over the
+    vectors followed by zero vectors (an unpaired node then meets a zero node, and
+    Adasum(x, 0) = x)."""
+    k = len(vectors)
+    p = 1
+    while p < k:
+        p *= 2
+    n = len(vectors[0])
+    return adasum_tree_exact(list(vectors) + [[0] * n] * (p - k))
+
+
 def adasum_tree_exact_segments(vectors, offsets):
     """Per-layer application: every segment [offs[s], offs[s+1]) on its own."""
     out = []

@@ -29,6 +29,9 @@ MUTANTS = {
     "bf16_truncates": ("double r = nearbyint(ldexp(ax, -q));", "double r = floor(ldexp(ax, -q));"),
     "momentum_no_mu": ("double vn = mu * (double)v[j] + A[j];", "double vn = (double)v[j] + A[j];"),
     "momentum_sign": ("double wn = (double)w[j] - lr * vn;", "double wn = (double)w[j] + lr * vn;"),
+    "carry_dropped": ("memmove(level + to, level + from, (size_t)n * sizeof(double));",
+                      "(void)from; (void)to;"),
+    "chain_skips_one": ("for (int k = 1; k < K; ++k) {", "for (int k = 2; k < K; ++k) {"),
 }
 
 
@@ -49,6 +52,18 @@ def _pins_pass(lib) -> bool:
             got = oracle.adasum_reduce(vecs, [0, n], lib=lib)["out64"]
             if not np.allclose(got, exp, rtol=1e-12, atol=1e-12):
                 return False
+    # odd worker counts: against the zero-padded exact tree
+    from exact_adasum import adasum_chain_exact, adasum_tree_exact_padded
+    for K in (3, 5, 7):
+        vecs = [rs.integers(-3, 4, size=5).astype(np.float32) for _ in range(K)]
+        exp = np.array([float(x) for x in adasum_tree_exact_padded(vecs)])
+        got = oracle.adasum_reduce(vecs, [0, 5], lib=lib)["out64"]
+        if not np.allclose(got, exp, rtol=1e-12, atol=1e-12):
+            return False
+        exp = np.array([float(x) for x in adasum_chain_exact(vecs)])
+        got = oracle.adasum_reduce(vecs, [0, 5], lib=lib, chain=True)["out64"]
+        if not np.allclose(got, exp, rtol=1e-12, atol=1e-12):
+            return False
     # zero operand
     b = f32([1.5, -2.0, 0.25])
     z = np.zeros(3, np.float32)

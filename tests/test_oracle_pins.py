@@ -19,7 +19,8 @@ import numpy as np
 import pytest
 import torch
 
-from exact_adasum import adasum_pair_exact, adasum_tree_exact, adasum_tree_exact_segments
+from exact_adasum import (adasum_chain_exact, adasum_pair_exact, adasum_tree_exact,
+                          adasum_tree_exact_padded, adasum_tree_exact_segments)
 
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
 
@@ -285,10 +286,57 @@ def test_momentum_matches_torch_sgd(oracle_mod, init):
 
 # ------------------------------------------------------------------------- bad arguments
 
-def test_rejects_non_power_of_two(oracle_mod):
-    vecs = f32([1, 2], [3, 4], [5, 6])
+def test_rejects_no_workers(oracle_mod):
     with pytest.raises(ValueError):
-        oracle_mod.adasum_reduce(vecs, [0, 2])
+        oracle_mod.adasum_reduce([], [0, 2])
+
+
+# ------------------------------------------------ any worker count, and the linear chain
+
+@pytest.mark.parametrize("K", [3, 5, 6, 7, 9, 12, 13])
+def test_odd_counts_carry_the_last_node(oracle_mod, K):
+    """Reading for worker counts that are not powers of two: pairs (2i, 2i+1) at every
+    level, an unpaired last node moves on unchanged.  Pinned two ways: exactly against
+    the power-of-two tree with zero vectors appended (Adasum(x, 0) = x), and bit for bit
+    against the oracle's own power-of-two path on the zero-padded input."""
+    rs = np.random.default_rng(100 + K)
+    n = 9
+    vecs = [rs.integers(-3, 4, size=n).astype(np.float32) for _ in range(K)]
+    exact = np.array([float(x) for x in adasum_tree_exact_padded(vecs)])
+    got = oracle_mod.adasum_reduce(vecs, [0, n])["out64"]
+    nrm = np.linalg.norm(exact)
+    assert np.linalg.norm(got - exact) <= 1e-13 * max(nrm, 1e-300)
+    p2 = 1 << (K - 1).bit_length()
+    padded = vecs + [np.zeros(n, np.float32)] * (p2 - K)
+    assert np.array_equal(got, oracle_mod.adasum_reduce(padded, [0, n])["out64"])
+
+
+@pytest.mark.parametrize("K", [2, 3, 4, 5, 8])
+def test_chain_matches_sequential_emulation_exactly(oracle_mod, K):
+    """The linear recursion g[0,n+1] = Adasum(g[0,n], g_{n+1}), pinned to the exact
+    sequential-emulation derivation applied left to right."""
+    rs = np.random.default_rng(200 + K)
+    for n in (1, 4, 11):
+        vecs = [rs.integers(-3, 4, size=n).astype(np.float32) for _ in range(K)]
+        exact = np.array([float(x) for x in adasum_chain_exact(vecs)])
+        got = oracle_mod.adasum_reduce(vecs, [0, n], chain=True)["out64"]
+        nrm = np.linalg.norm(exact)
+        if nrm == 0:
+            assert np.all(got == 0)
+        else:
+            assert np.linalg.norm(got - exact) <= 1e-13 * nrm
+
+
+def test_chain_and_tree_differ_from_four_workers(oracle_mod):
+    """Two and three workers give the same result either way; from four on the chain
+    and the tree pair different nodes."""
+    vecs = f32([1, 0, 0], [1, 2, 0], [0, 1, 3], [2, -1, 1])
+    for k in (2, 3):
+        assert np.array_equal(oracle_mod.adasum_reduce(vecs[:k], [0, 3])["out64"],
+                              oracle_mod.adasum_reduce(vecs[:k], [0, 3], chain=True)["out64"])
+    tree = oracle_mod.adasum_reduce(vecs, [0, 3])["out64"]
+    chain = oracle_mod.adasum_reduce(vecs, [0, 3], chain=True)["out64"]
+    assert not np.allclose(tree, chain, rtol=1e-6)
 
 
 def test_rejects_decreasing_offsets(oracle_mod):
