@@ -75,8 +75,9 @@ def _stream_handle(device, stream):
 
 
 def reduce(grads, seg_offsets=None, *, out: torch.Tensor | None = None,
-           stream: torch.cuda.Stream | None = None) -> torch.Tensor:
-    """Adasum of K worker gradients per segment (``adasum_reduce``).
+           stream: torch.cuda.Stream | None = None, chain: bool = False) -> torch.Tensor:
+    """Adasum of K worker gradients per segment (``adasum_reduce``; with ``chain=True``
+    the left-to-right recursion of ``adasum_reduce_chain``, K <= 16).
 
     grads: K 1-D CUDA tensors (float32 or bfloat16, equal length), or a K x N tensor.
     seg_offsets: L+1 offsets (segment s = [offs[s], offs[s+1])); None = one segment.
@@ -93,11 +94,12 @@ def reduce(grads, seg_offsets=None, *, out: torch.Tensor | None = None,
     lib = load_library()
     K = len(grads)
     ptrs = (ctypes.c_void_p * K)(*[g.data_ptr() for g in grads])
+    fn = lib.adasum_reduce_chain if chain else lib.adasum_reduce
     with torch.cuda.device(device):
-        st = lib.adasum_reduce(ptrs, K, offs.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
-                               offs.shape[0] - 1, _DTYPE_CODE[dtype],
-                               ctypes.c_void_p(out.data_ptr()), _stream_handle(device, stream))
-    check(st, "adasum_reduce")
+        st = fn(ptrs, K, offs.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
+                offs.shape[0] - 1, _DTYPE_CODE[dtype],
+                ctypes.c_void_p(out.data_ptr()), _stream_handle(device, stream))
+    check(st, "adasum_reduce_chain" if chain else "adasum_reduce")
     return out
 
 

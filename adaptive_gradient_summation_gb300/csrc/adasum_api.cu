@@ -504,14 +504,23 @@ struct Carver {
   }
 };
 
-adasum_status_t reduce_impl(const void* const* grads, int K, const int64_t* offs, int L,
+adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* offs, int L,
                             int dtype, void* out, float* master_w, float* momentum,
-                            float lr, float mu, cudaStream_t stream) {
+                            float lr, float mu, cudaStream_t stream, bool chain = false) {
   const bool mom = master_w != nullptr;
   if (dtype != kF32 && dtype != kBF16) return ADASUM_ERR_INVALID_ARG;
-  if (L < 0 || (L > 0 && offs == nullptr) || K < 1 || grads == nullptr)
+  if (L < 0 || (L > 0 && offs == nullptr) || K < 1 || grads_in == nullptr)
     return ADASUM_ERR_INVALID_ARG;
-  if (K > ADASUM_MAX_K || (K & (K - 1)) != 0) return ADASUM_ERR_UNSUPPORTED;
+  if (K > ADASUM_MAX_K || (chain && K > kMaxGroup)) return ADASUM_ERR_UNSUPPORTED;
+  // Pad the worker list to a power of two with zero (null) gradients: exact for the
+  // tree (an unpaired node meets a zero node, Adasum(x, 0) = x); the chain ignores them.
+  const int Kreal = K;
+  int P2 = 1;
+  while (P2 < K) P2 *= 2;
+  std::vector<const void*> padded(grads_in, grads_in + K);
+  padded.resize(P2, nullptr);
+  const void* const* grads = padded.data();
+  K = P2;
   if (L == 0) return ADASUM_OK;
   if (offs[0] != 0) return ADASUM_ERR_INVALID_ARG;
   for (int s = 0; s < L; ++s)
@@ -520,25 +529,24 @@ adasum_status_t reduce_impl(const void* const* grads, int K, const int64_t* offs
   if (N == 0) return ADASUM_OK;
   if (!mom && out == nullptr) return ADASUM_ERR_INVALID_ARG;
   if (mom && momentum == nullptr) return ADASUM_ERR_INVALID_ARG;
-  for (int k = 0; k < K; ++k)
+  for (int k = 0; k < Kreal; ++k)
     if (grads[k] == nullptr) return ADASUM_ERR_INVALID_ARG;
-
   const size_t es = elem_size(dtype);
   const size_t nbytes = static_cast<size_t>(N) * es;
   if (out) {
-    for (int k = 0; k < K; ++k)
+    for (int k = 0; k < Kreal; ++k)
       if (out != grads[k] && overlaps(out, nbytes, grads[k], nbytes)) return ADASUM_ERR_ALIAS;
   }
   if (mom) {
     const size_t fb = static_cast<size_t>(N) * sizeof(float);
     if (overlaps(master_w, fb, momentum, fb)) return ADASUM_ERR_ALIAS;
-    for (int k = 0; k < K; ++k)
+    for (int k = 0; k < Kreal; ++k)
       if (overlaps(master_w, fb, grads[k], nbytes) || overlaps(momentum, fb, grads[k], nbytes))
         return ADASUM_ERR_ALIAS;
     if (out && (overlaps(master_w, fb, out, nbytes) || overlaps(momentum, fb, out, nbytes)))
       return ADASUM_ERR_ALIAS;
   }
-  if (!mom && K == 1 && out == grads[0]) return ADASUM_OK;  // in-place copy of one input
+  if (!mom && Kreal == 1 && out == grads[0]) return ADASUM_OK;  // in-place copy of one input
 
   int device = 0;
   if (cudaGetDevice(&device) != cudaSuccess) {
@@ -567,7 +575,7 @@ adasum_status_t reduce_impl(const void* const* grads, int K, const int64_t* offs
   }
 
   int route = kRouteKernels;
-  if (kg.size() == 1 && kg[0] > 1) {
+  if (kg.size() == 1 && kg[0] > 1 && !chain && Kreal == K) {
     route = requested_route();
     if (route == kRouteStream && !stream_supported(dtype, kg[0])) route = kRouteKernels;
   }
@@ -630,7 +638,7 @@ adasum_status_t reduce_impl(const void* const* grads, int K, const int64_t* offs
   }
 
   bool all_aligned = aligned16(out) && (!mom || (aligned16(master_w) && aligned16(momentum)));
-  for (int k = 0; k < K; ++k) all_aligned = all_aligned && aligned16(grads[k]);
+  for (int k = 0; k < Kreal; ++k) all_aligned = all_aligned && aligned16(grads[k]);
 
   if (cudaMemsetAsync(seg_flag, 0, n_ints * sizeof(int), stream) != cudaSuccess)
     return ADASUM_ERR_CUDA;
@@ -657,7 +665,9 @@ adasum_status_t reduce_impl(const void* const* grads, int K, const int64_t* offs
     a.list_segs = reinterpret_cast<int*>(base + o_lsegs);
     a.list_tiny = reinterpret_cast<int*>(base + o_ltiny);
     a.list_count = list_count;
-    a.Ktotal = K;
+    a.Ktotal = chain ? Kreal : K;
+    a.mode = chain ? kModeChain : kModeTree;
+    a.Kreal = Kreal;
     const bool last = s + 1 == kg.size();
     if (last && mom) {
       a.master_w = master_w;
@@ -802,6 +812,13 @@ adasum_status_t adasum_reduce(const void* const* grads, int K, const int64_t* se
   std::lock_guard<std::mutex> lock(g_mu);
   return reduce_impl(grads, K, seg_offsets, L, static_cast<int>(dtype), out, nullptr,
                      nullptr, 0.f, 0.f, reinterpret_cast<cudaStream_t>(stream));
+}
+
+adasum_status_t adasum_reduce_chain(const void* const* grads, int K, const int64_t* seg_offsets,
+                                    int L, adasum_dtype_t dtype, void* out, adasum_stream_t stream) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  return reduce_impl(grads, K, seg_offsets, L, static_cast<int>(dtype), out, nullptr, nullptr, 0.f,
+                     0.f, reinterpret_cast<cudaStream_t>(stream), true);
 }
 
 adasum_status_t adasum_pair(const void* a, const void* b, int64_t n, adasum_dtype_t dtype,

@@ -88,7 +88,15 @@ struct StageArgs {
   int Ktotal;                 // all workers (the tiny-segment recompute runs the whole tree)
   int in_f64;                 // stage inputs are fp64 intermediates
   int out_f64;                // stage outputs are fp64 intermediates
+
+  // Combination order: kModeTree (binary tree, pairs (2i, 2i+1) per level) or kModeChain
+  // (g[0,k] = Adasum(g[0,k-1], g_k), left to right).  Kreal workers are real; a null
+  // input pointer is a zero gradient (worker counts are padded to a power of two with
+  // them, which is exact: an unpaired node meets a zero node and Adasum(x, 0) = x).
+  int mode;
+  int Kreal;
 };
+enum Mode : int { kModeTree = 0, kModeChain = 1 };
 
 // Gram-entry error model of the fp32 pass, relative to |g_i| |g_j|: products and
 // bounded-length fp32 sums, then compensated sums (a typical-case constant).

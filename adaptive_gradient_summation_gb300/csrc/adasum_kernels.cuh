@@ -89,6 +89,7 @@ __device__ __forceinline__ uint4 load_vec_raw(const typename ElemTraits<Tag>::St
                                               int64_t v, int64_t lo, int64_t hi,
                                               bool aligned) {
   constexpr int VW = ElemTraits<Tag>::kVW;
+  if (x == nullptr) return make_uint4(0u, 0u, 0u, 0u);  // a zero (padding) gradient
   const int64_t p0 = v * VW;
   if (aligned && p0 >= lo && p0 + VW <= hi) return ld16<P>(x + p0);
   uint32_t w[4] = {0u, 0u, 0u, 0u};
@@ -464,6 +465,83 @@ __device__ double coefficient_tree(const double (&G)[KG][KG], const double* eps,
   return ill ? 1e30 : rel;
 }
 
+// The linear recursion g[0,k] = Adasum(g[0,k-1], g_k), k = 1 .. kreal-1, in coefficient
+// space with the same error estimate as coefficient_tree (u = the running node, v = leaf
+// k).  Called by all 32 lanes of one warp; lane k < KG owns leaf k.
+template <int KG>
+__device__ double coefficient_chain(const double (&G)[KG][KG], const double* eps,
+                                    double gram_err, double* c_sh, double& c, bool& ill,
+                                    int kreal) {
+  const int lane = threadIdx.x & 31;
+  const bool on = lane < KG;
+  const int row = on ? lane : 0;
+  const double s = on ? sqrt(fmax(G[row][row], 0.0)) : 0.0;
+  const double e = on ? eps[row] : 0.0;
+  c = (lane == 0) ? 1.0 : 0.0;
+  double dc = 0.0;
+  bool bad = false;
+  if (on) c_sh[lane] = c;
+  __syncwarp();
+  for (int k = 1; k < kreal; ++k) {
+    const bool in_u = lane < k;
+    double row_u = 0.0;
+    if (on)
+      for (int j = 0; j < k; ++j) row_u = fma(c_sh[j], G[row][j], row_u);
+    const double pu = block_lane_sum(in_u ? c * row_u : 0.0, 32);
+    const double d = block_lane_sum(in_u ? c * G[row][k] : 0.0, 32);
+    const double Su = block_lane_sum(in_u ? c * c * s * s : 0.0, 32);
+    const double Du = sqrt(block_lane_sum(in_u ? (dc * dc + c * c * e * e) * s * s : 0.0, 32));
+    const double sk = sqrt(fmax(G[k][k], 0.0)), ek = eps[k];
+    const double pv = G[k][k], Sv = sk * sk, Dv = ek * sk;
+    const double nu = sqrt(fmax(pu, 0.0)), nv = sqrt(fmax(pv, 0.0));
+    const double err_pu = gram_err * Su + 2.0 * nu * Du;
+    const double err_pv = gram_err * Sv + 2.0 * nv * Dv;
+    const double err_d = gram_err * sqrt(Su * Sv) + (nu * Dv + nv * Du);
+    double alpha = 1.0, beta = 1.0, dalpha = 0.0, dbeta = 0.0;
+    if (pu != 0.0) {
+      alpha = 1.0 - d / (2.0 * pu);
+      dalpha = (err_d + fabs(d) * err_pu / fabs(pu)) / (2.0 * fabs(pu));
+      if (pu <= err_pu) bad = true;
+    } else if (Su > 0.0) {
+      bad = true;
+    }
+    if (pv != 0.0) {
+      beta = 1.0 - d / (2.0 * pv);
+      dbeta = (err_d + fabs(d) * err_pv / fabs(pv)) / (2.0 * fabs(pv));
+      if (pv <= err_pv) bad = true;
+    } else if (Sv > 0.0) {
+      bad = true;
+    }
+    if (in_u) {
+      dc = fma(fabs(alpha), dc, fabs(c) * dalpha);
+      c *= alpha;
+    } else if (lane == k) {
+      dc = dbeta;
+      c = beta;
+    }
+    __syncwarp();
+    if (on) c_sh[lane] = c;
+    __syncwarp();
+  }
+  double full = 0.0;
+  if (on)
+    for (int j = 0; j < KG; ++j) full = fma(c_sh[j], G[row][j], full);
+  const double P = block_lane_sum(c * full, 32);
+  const double S = block_lane_sum(c * c * s * s, 32);
+  const double D = sqrt(block_lane_sum((dc * dc + c * c * e * e) * s * s, 32));
+  ill = __any_sync(0xFFFFFFFFu, bad);
+  if (S == 0.0) return 0.0;
+  int levels = 1;
+  for (int k = KG; k > 1; k >>= 1) ++levels;
+  const double err_P = gram_err * S + 2.0 * sqrt(fmax(P, 0.0)) * D;
+  if (P <= err_P) {
+    ill = true;
+    return 1e30;
+  }
+  const double rel = (D + levels * 5.9604644775390625e-08 * sqrt(S)) / sqrt(P);
+  return ill ? 1e30 : rel;
+}
+
 // Per segment: the Gram matrix from the chunk sums (fp64, chunk order), the tree
 // coefficients, and the conditioning check (see coefficient_tree).
 // Called by a whole CTA.
@@ -489,7 +567,9 @@ __device__ __forceinline__ void segment_coefficients(const StageArgs& a, int seg
   if (threadIdx.x < 32) {
     double c = 0.0;
     bool ill = false;
-    const double rel = coefficient_tree<KG>(G, eps, kGramRelErr, snorm, c, ill);
+    const double rel = a.mode == kModeChain
+                           ? coefficient_chain<KG>(G, eps, kGramRelErr, snorm, c, ill, a.Kreal)
+                           : coefficient_tree<KG>(G, eps, kGramRelErr, snorm, c, ill);
     if (threadIdx.x < KG)
       a.coef[(static_cast<size_t>(q) * a.nsegs + seg) * KG + threadIdx.x] = static_cast<float>(c);
     if (threadIdx.x == 0) {
@@ -734,6 +814,7 @@ enum Kind { kKindF32 = 0, kKindBF16 = 1, kKindF64 = 2 };
 
 template <int IN>
 __device__ __forceinline__ double load_f64(const void* base, int64_t i) {
+  if (base == nullptr) return 0.0;  // a zero (padding) gradient
   if constexpr (IN == kKindF32) return static_cast<double>(static_cast<const float*>(base)[i]);
   if constexpr (IN == kKindBF16)
     return static_cast<double>(bf16_bits_to_float(static_cast<const uint16_t*>(base)[i]));
@@ -788,7 +869,8 @@ __global__ void __launch_bounds__(kThreads) tiny64_kernel(const StageArgs a) {
       val[top] = on ? load_f64<IN>(a.in[k], p) : 0.0;
       lvl[top] = 0;
       ++top;
-      while (top >= 2 && lvl[top - 1] == lvl[top - 2]) {
+      // the chain folds every new leaf into the running node; the tree merges equal levels
+      while (top >= 2 && (a.mode == kModeChain || lvl[top - 1] == lvl[top - 2])) {
         const double x = val[top - 2], y = val[top - 1];
         const double d = warp_sum64(x * y), pa = warp_sum64(x * x), pb = warp_sum64(y * y);
         const double alpha = 1.0 - (pa == 0.0 ? 0.0 : d / (2.0 * pa));
@@ -876,7 +958,10 @@ __global__ void __launch_bounds__(128) coef64_kernel(const StageArgs a) {
     if (threadIdx.x < 32) {
       double c = 0.0;
       bool ill = false;
-      coefficient_tree<KG>(G, zeros, 0.0, snorm, c, ill);
+      if (a.mode == kModeChain)
+        coefficient_chain<KG>(G, zeros, 0.0, snorm, c, ill, a.Kreal);
+      else
+        coefficient_tree<KG>(G, zeros, 0.0, snorm, c, ill);
       if (threadIdx.x < KG) a.coef64[(static_cast<size_t>(q) * a.nsegs + seg) * KG + threadIdx.x] = c;
     }
   }

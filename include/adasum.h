@@ -74,7 +74,7 @@ typedef enum {
 typedef enum {
   ADASUM_OK = 0,
   ADASUM_ERR_INVALID_ARG = 1,  /* null pointer, bad offsets, bad dtype, n < 0, ... */
-  ADASUM_ERR_UNSUPPORTED = 2,  /* K not a power of two in [1, 256] */
+  ADASUM_ERR_UNSUPPORTED = 2,  /* K outside [1, 256] (chain: [1, 16]), size limits */
   ADASUM_ERR_ALIAS = 3,        /* an output overlaps an input other than as allowed */
   ADASUM_ERR_NO_MEMORY = 4,    /* the workspace could not be grown */
   ADASUM_ERR_CUDA = 5,         /* a CUDA runtime call failed (launch, copy, ...) */
@@ -88,8 +88,11 @@ typedef enum {
  * adasum_reduce -- Adasum of K worker gradients, per segment, as a binary tree.
  *
  *   grads        host array of K device pointers; grads[k] points to N = seg_offsets[L]
- *                elements of `dtype` (worker k's flat gradient).  K must be a power of
- *                two, 1 <= K <= ADASUM_MAX_K; K = 1 copies grads[0] to out.
+ *                elements of `dtype` (worker k's flat gradient).  1 <= K <= ADASUM_MAX_K;
+ *                K = 1 copies grads[0] to out.  When K is not a power of two, every
+ *                level still pairs (2i, 2i+1) and an unpaired last node moves up
+ *                unchanged (the same as padding with zero gradients, since
+ *                Adasum(x, 0) = x).
  *   seg_offsets  host array of L+1 int64 offsets, seg_offsets[0] = 0, non-decreasing;
  *                segment s is positions [seg_offsets[s], seg_offsets[s+1]).  Empty
  *                segments are allowed.  L = 0 (or N = 0) is a no-op.
@@ -102,6 +105,17 @@ typedef enum {
 ADASUM_API adasum_status_t adasum_reduce(const void *const *grads, int K, const int64_t *seg_offsets,
                               int L, adasum_dtype_t dtype, void *out,
                               adasum_stream_t stream);
+
+/*
+ * adasum_reduce_chain -- the linear recursion of the same section of the paper,
+ * g[0,n+1] = Adasum(g[0,n], g_{n+1}): workers are folded in one at a time, left to
+ * right, instead of pairwise up a tree.  Same arguments and conventions as
+ * adasum_reduce; 1 <= K <= 16 (ADASUM_ERR_UNSUPPORTED above).
+ */
+ADASUM_API adasum_status_t adasum_reduce_chain(const void *const *grads, int K,
+                                               const int64_t *seg_offsets, int L,
+                                               adasum_dtype_t dtype, void *out,
+                                               adasum_stream_t stream);
 
 /*
  * adasum_pair -- Adasum(a, b) of two device vectors of n elements (one segment).

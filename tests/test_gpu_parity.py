@@ -263,7 +263,8 @@ def test_error_codes(native):
     g = rand_grads(4, 1000, torch.float32, seed=30)
     p = [t.data_ptr() for t in g]
     out = torch.empty(1000, device=DEV)
-    assert _raw_reduce(p[:3], 3, [0, 1000], 0, out.data_ptr()) == ags.Status.ERR_UNSUPPORTED
+    assert _raw_reduce(p[:3], 0, [0, 1000], 0, out.data_ptr()) == ags.Status.ERR_INVALID_ARG
+    assert _raw_reduce(p * 65, 260, [0, 1000], 0, out.data_ptr()) == ags.Status.ERR_UNSUPPORTED
     assert _raw_reduce(p, 4, [0, 600, 500, 1000], 0, out.data_ptr()) == ags.Status.ERR_INVALID_ARG
     assert _raw_reduce(p, 4, [1, 1000], 0, out.data_ptr()) == ags.Status.ERR_INVALID_ARG
     assert _raw_reduce(p, 4, [0, 1000], 7, out.data_ptr()) == ags.Status.ERR_INVALID_ARG
@@ -272,7 +273,7 @@ def test_error_codes(native):
     # output overlapping an input partially
     assert _raw_reduce(p, 4, [0, 1000], 0, g[1].data_ptr() + 8) == ags.Status.ERR_ALIAS
     with pytest.raises(ags.AdasumError):
-        ags.reduce(g[:3], [0, 1000])
+        ags.reduce(g * 5, [0, 1000], chain=True)      # the chain takes at most 16 workers
     assert ags.get_last_error() == ags.Status.OK
 
 
@@ -417,3 +418,42 @@ def test_stream_route_unaligned(native, monkeypatch):
     out = ags.reduce(grads, offs)
     torch.cuda.synchronize()
     check_against_oracle(grads, offs, out)
+
+
+# ------------------------------------------- any worker count; the linear chain
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("K", [3, 5, 6, 7, 11, 13, 24, 40, 100])
+def test_any_worker_count(native, K, dtype):
+    lengths = [1, 7, 0, 33, 4097, 300, 70_001]
+    offs = workloads.offsets_from_numels(lengths)
+    grads = rand_grads(K, int(offs[-1]), dtype, seed=90 + K)
+    out = ags.reduce(grads, offs)
+    torch.cuda.synchronize()
+    check_against_oracle(grads, offs, out)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("K", [2, 3, 4, 5, 8, 11, 16])
+def test_chain(native, K, dtype):
+    lengths = [1, 7, 0, 33, 4097, 300, 70_001]
+    offs = workloads.offsets_from_numels(lengths)
+    grads = rand_grads(K, int(offs[-1]), dtype, seed=110 + K)
+    out = ags.reduce(grads, offs, chain=True)
+    torch.cuda.synchronize()
+    ref = oracle.adasum_reduce([to_oracle_input(g) for g in grads], offs, chain=True,
+                               want_mag=dtype == torch.bfloat16)
+    got = to_f64(out)
+    if dtype == torch.float32:
+        check_fp32_segments(got, ref["out64"], offs)
+    else:
+        check_bf16_elements(got, ref["out64"], ref["mag"], K)
+
+
+def test_chain_cancelling_scalars_recomputed(native):
+    offs = np.arange(0, 301, dtype=np.int64)
+    grads = rand_grads(16, 300, torch.float32, seed=130, corr=0.0)
+    out = ags.reduce(grads, offs, chain=True)
+    torch.cuda.synchronize()
+    ref = oracle.adasum_reduce([to_oracle_input(g) for g in grads], offs, chain=True)
+    check_fp32_segments(to_f64(out), ref["out64"], offs)
