@@ -75,9 +75,12 @@ def _stream_handle(device, stream):
 
 
 def reduce(grads, seg_offsets=None, *, out: torch.Tensor | None = None,
-           stream: torch.cuda.Stream | None = None, chain: bool = False) -> torch.Tensor:
+           stream: torch.cuda.Stream | None = None, chain: bool = False,
+           orthogonality: bool = False):
     """Adasum of K worker gradients per segment (``adasum_reduce``; with ``chain=True``
-    the left-to-right recursion of ``adasum_reduce_chain``, K <= 16).
+    the left-to-right recursion of ``adasum_reduce_chain``, K <= 16; with
+    ``orthogonality=True`` also the per-segment metric |A|^2 / sum_k |g_k|^2 of
+    ``adasum_reduce_orthogonality``, returned as ``(out, ortho)``).
 
     grads: K 1-D CUDA tensors (float32 or bfloat16, equal length), or a K x N tensor.
     seg_offsets: L+1 offsets (segment s = [offs[s], offs[s+1])); None = one segment.
@@ -94,11 +97,22 @@ def reduce(grads, seg_offsets=None, *, out: torch.Tensor | None = None,
     lib = load_library()
     K = len(grads)
     ptrs = (ctypes.c_void_p * K)(*[g.data_ptr() for g in grads])
-    fn = lib.adasum_reduce_chain if chain else lib.adasum_reduce
+    L = offs.shape[0] - 1
+    offs_p = offs.ctypes.data_as(ctypes.POINTER(ctypes.c_int64))
     with torch.cuda.device(device):
-        st = fn(ptrs, K, offs.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
-                offs.shape[0] - 1, _DTYPE_CODE[dtype],
-                ctypes.c_void_p(out.data_ptr()), _stream_handle(device, stream))
+        if orthogonality:
+            if chain:
+                raise ValueError("the orthogonality metric is defined for the tree")
+            ortho = torch.empty(max(L, 0), dtype=torch.float32, device=device)
+            st = lib.adasum_reduce_orthogonality(ptrs, K, offs_p, L, _DTYPE_CODE[dtype],
+                                                 ctypes.c_void_p(out.data_ptr()),
+                                                 ctypes.c_void_p(ortho.data_ptr()),
+                                                 _stream_handle(device, stream))
+            check(st, "adasum_reduce_orthogonality")
+            return out, ortho
+        fn = lib.adasum_reduce_chain if chain else lib.adasum_reduce
+        st = fn(ptrs, K, offs_p, L, _DTYPE_CODE[dtype], ctypes.c_void_p(out.data_ptr()),
+                _stream_handle(device, stream))
     check(st, "adasum_reduce_chain" if chain else "adasum_reduce")
     return out
 

@@ -44,6 +44,9 @@ SIGNATURES = {
     "adasum_reduce": (ctypes.c_int, [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int,
                                      ctypes.POINTER(ctypes.c_int64), ctypes.c_int,
                                      ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]),
+    "adasum_reduce_orthogonality": (ctypes.c_int, [
+        ctypes.POINTER(ctypes.c_void_p), ctypes.c_int, ctypes.POINTER(ctypes.c_int64),
+        ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     "adasum_reduce_chain": (ctypes.c_int, [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int,
                                            ctypes.POINTER(ctypes.c_int64), ctypes.c_int,
                                            ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]),

@@ -506,7 +506,8 @@ struct Carver {
 
 adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* offs, int L,
                             int dtype, void* out, float* master_w, float* momentum,
-                            float lr, float mu, cudaStream_t stream, bool chain = false) {
+                            float lr, float mu, cudaStream_t stream, bool chain = false,
+                            float* ortho = nullptr) {
   const bool mom = master_w != nullptr;
   if (dtype != kF32 && dtype != kBF16) return ADASUM_ERR_INVALID_ARG;
   if (L < 0 || (L > 0 && offs == nullptr) || K < 1 || grads_in == nullptr)
@@ -517,6 +518,7 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
   const int Kreal = K;
   int P2 = 1;
   while (P2 < K) P2 *= 2;
+  if (ortho != nullptr && P2 == 1) P2 = 2;  // a zero partner: Adasum(g, 0) = g, and a Gram pass
   std::vector<const void*> padded(grads_in, grads_in + K);
   padded.resize(P2, nullptr);
   const void* const* grads = padded.data();
@@ -546,7 +548,7 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
     if (out && (overlaps(master_w, fb, out, nbytes) || overlaps(momentum, fb, out, nbytes)))
       return ADASUM_ERR_ALIAS;
   }
-  if (!mom && Kreal == 1 && out == grads[0]) return ADASUM_OK;  // in-place copy of one input
+  if (!mom && Kreal == 1 && out == grads[0] && ortho == nullptr) return ADASUM_OK;  // in-place copy
 
   int device = 0;
   if (cudaGetDevice(&device) != cudaSuccess) {
@@ -575,7 +577,7 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
   }
 
   int route = kRouteKernels;
-  if (kg.size() == 1 && kg[0] > 1 && !chain && Kreal == K) {
+  if (kg.size() == 1 && kg[0] > 1 && !chain && Kreal == K && ortho == nullptr) {
     route = requested_route();
     if (route == kRouteStream && !stream_supported(dtype, kg[0])) route = kRouteKernels;
   }
@@ -608,6 +610,8 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
   const size_t o_ltiles = cv.take(static_cast<size_t>(plan->ntiles) * sizeof(int));
   const size_t o_lsegs = cv.take(static_cast<size_t>(L) * sizeof(int));
   const size_t o_ltiny = cv.take(static_cast<size_t>(L) * sizeof(int));
+  const size_t o_onorm = cv.take(ortho ? static_cast<size_t>(L) * sizeof(double) : 0);
+  const size_t o_diag = cv.take(ortho ? static_cast<size_t>(groups[0]) * L * sizeof(double) : 0);
   const size_t o_slots = cv.take(route == kRouteStream
                                      ? static_cast<size_t>(L) * plan->stream_grid *
                                            (static_cast<size_t>(kg[0]) * (kg[0] + 1) / 2) * sizeof(float)
@@ -674,6 +678,10 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
       a.momentum = momentum;
       a.lr = lr;
       a.mu = mu;
+    }
+    if (ortho != nullptr) {
+      if (last) a.outnorm2 = reinterpret_cast<double*>(base + o_onorm);
+      if (s == 0) a.diag_sum = reinterpret_cast<double*>(base + o_diag);
     }
     return a;
   };
@@ -795,6 +803,14 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
     if (adasum_status_t st = run_stage64(a, in_dt, out_dt, (last && mom) ? 1 : 0, grid64, stream))
       return st;
   }
+  if (ortho != nullptr) {
+    if (adasum_status_t st = launch_one(stream, [&](const char** n) {
+          return launch_orthogonality(reinterpret_cast<double*>(base + o_onorm),
+                                      reinterpret_cast<double*>(base + o_diag), groups[0], L,
+                                      ortho, stream, n);
+        }))
+      return st;
+  }
   ws.last_flag_counts = list_count;
   return ADASUM_OK;
 }
@@ -812,6 +828,16 @@ adasum_status_t adasum_reduce(const void* const* grads, int K, const int64_t* se
   std::lock_guard<std::mutex> lock(g_mu);
   return reduce_impl(grads, K, seg_offsets, L, static_cast<int>(dtype), out, nullptr,
                      nullptr, 0.f, 0.f, reinterpret_cast<cudaStream_t>(stream));
+}
+
+adasum_status_t adasum_reduce_orthogonality(const void* const* grads, int K,
+                                            const int64_t* seg_offsets, int L,
+                                            adasum_dtype_t dtype, void* out, float* ortho,
+                                            adasum_stream_t stream) {
+  if (ortho == nullptr && L > 0) return ADASUM_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_mu);
+  return reduce_impl(grads, K, seg_offsets, L, static_cast<int>(dtype), out, nullptr, nullptr, 0.f,
+                     0.f, reinterpret_cast<cudaStream_t>(stream), false, ortho);
 }
 
 adasum_status_t adasum_reduce_chain(const void* const* grads, int K, const int64_t* seg_offsets,

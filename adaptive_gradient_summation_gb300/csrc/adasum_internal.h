@@ -95,6 +95,11 @@ struct StageArgs {
   // them, which is exact: an unpaired node meets a zero node and Adasum(x, 0) = x).
   int mode;
   int Kreal;
+
+  // Orthogonality metric (optional): |A|^2 of the final stage per segment, and the sum of
+  // the first stage's Gram diagonals per (group, segment).
+  double* outnorm2;           // [nsegs], final stage only
+  double* diag_sum;           // [G][nsegs], first stage only
 };
 enum Mode : int { kModeTree = 0, kModeChain = 1 };
 
@@ -153,6 +158,9 @@ int pipeline_grid(int in_dtype, int out_dtype, int Kg, int momentum, int num_sms
 int launch_reduce_chunks(const StageArgs& a, void* stream, const char** name);
 // fp64 path: build the flagged lists, then Gram / coefficients / combine over them.
 int launch_collect(const StageArgs& a, int grid, void* stream, const char** name);
+// ortho[s] = outnorm2[s] / sum_q diag_sum[q][s] (NaN when the sum is 0).
+int launch_orthogonality(const double* outnorm2, const double* diag_sum, int groups, int nsegs,
+                         float* ortho, void* stream, const char** name);
 int launch_tiny64(const StageArgs& a, int in_dtype, int out_dtype, int momentum, int grid,
                   void* stream, const char** name);
 int launch_gram64(const StageArgs& a, int in_dtype, int grid, void* stream, const char** name);

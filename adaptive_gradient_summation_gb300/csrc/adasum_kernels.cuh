@@ -396,7 +396,8 @@ __device__ __forceinline__ double block_lane_sum(double x, int W) {
 // (1e30 when ill-conditioned); lane k < KG receives its coefficient in `c`.
 template <int KG>
 __device__ double coefficient_tree(const double (&G)[KG][KG], const double* eps,
-                                   double gram_err, double* c_sh, double& c, bool& ill) {
+                                   double gram_err, double* c_sh, double& c, bool& ill,
+                                   double* P_out = nullptr) {
   static_assert(KG <= 32, "one lane per leaf");
   const int lane = threadIdx.x & 31;
   const bool on = lane < KG;
@@ -453,6 +454,7 @@ __device__ double coefficient_tree(const double (&G)[KG][KG], const double* eps,
   const double S = block_lane_sum(c * c * s * s, 32);
   const double D = sqrt(block_lane_sum((dc * dc + c * c * e * e) * s * s, 32));
   ill = __any_sync(0xFFFFFFFFu, bad);
+  if (P_out) *P_out = P;
   if (S == 0.0) return 0.0;  // every leaf is zero: the output is exactly zero
   int levels = 1;
   for (int k = KG; k > 1; k >>= 1) ++levels;
@@ -471,7 +473,7 @@ __device__ double coefficient_tree(const double (&G)[KG][KG], const double* eps,
 template <int KG>
 __device__ double coefficient_chain(const double (&G)[KG][KG], const double* eps,
                                     double gram_err, double* c_sh, double& c, bool& ill,
-                                    int kreal) {
+                                    int kreal, double* P_out = nullptr) {
   const int lane = threadIdx.x & 31;
   const bool on = lane < KG;
   const int row = on ? lane : 0;
@@ -530,6 +532,7 @@ __device__ double coefficient_chain(const double (&G)[KG][KG], const double* eps
   const double S = block_lane_sum(c * c * s * s, 32);
   const double D = sqrt(block_lane_sum((dc * dc + c * c * e * e) * s * s, 32));
   ill = __any_sync(0xFFFFFFFFu, bad);
+  if (P_out) *P_out = P;
   if (S == 0.0) return 0.0;
   int levels = 1;
   for (int k = KG; k > 1; k >>= 1) ++levels;
@@ -565,11 +568,17 @@ __device__ __forceinline__ void segment_coefficients(const StageArgs& a, int seg
     eps[k] = a.in_relerr ? static_cast<double>(a.in_relerr[static_cast<size_t>(q * KG + k) * a.nsegs + seg]) : 0.0;
   __syncthreads();
   if (threadIdx.x < 32) {
-    double c = 0.0;
+    double c = 0.0, P = 0.0;
     bool ill = false;
     const double rel = a.mode == kModeChain
-                           ? coefficient_chain<KG>(G, eps, kGramRelErr, snorm, c, ill, a.Kreal)
-                           : coefficient_tree<KG>(G, eps, kGramRelErr, snorm, c, ill);
+                           ? coefficient_chain<KG>(G, eps, kGramRelErr, snorm, c, ill, a.Kreal, &P)
+                           : coefficient_tree<KG>(G, eps, kGramRelErr, snorm, c, ill, &P);
+    if (threadIdx.x == 0 && a.outnorm2) a.outnorm2[seg] = P;
+    if (threadIdx.x == 0 && a.diag_sum) {
+      double tr = 0.0;
+      for (int k = 0; k < KG; ++k) tr += G[k][k];
+      a.diag_sum[static_cast<size_t>(q) * a.nsegs + seg] = tr;
+    }
     if (threadIdx.x < KG)
       a.coef[(static_cast<size_t>(q) * a.nsegs + seg) * KG + threadIdx.x] = static_cast<float>(c);
     if (threadIdx.x == 0) {
@@ -838,6 +847,16 @@ static __global__ void collect_kernel(const StageArgs a) {
   }
 }
 
+// The orthogonality metric of every segment: |A|^2 / sum_k |g_k|^2 (NaN when 0/0).
+static __global__ void orthogonality_kernel(const double* outnorm2, const double* diag_sum,
+                                            int groups, int nsegs, float* ortho) {
+  for (int s = blockIdx.x * blockDim.x + threadIdx.x; s < nsegs; s += gridDim.x * blockDim.x) {
+    double den = 0.0;
+    for (int q = 0; q < groups; ++q) den += diag_sum[static_cast<size_t>(q) * nsegs + s];
+    ortho[s] = den == 0.0 ? __int_as_float(0x7FC00000) : static_cast<float>(outnorm2[s] / den);
+  }
+}
+
 // Sum over the warp in a fixed butterfly order (every lane gets the same value).
 __device__ __forceinline__ double warp_sum64(double v) {
 #pragma unroll
@@ -880,6 +899,8 @@ __global__ void __launch_bounds__(kThreads) tiny64_kernel(const StageArgs a) {
         --top;
       }
     }
+    const double nrm2 = warp_sum64(val[0] * val[0]);
+    if (lane == 0 && a.outnorm2) a.outnorm2[a.list_tiny[li]] = nrm2;
     if (!on) continue;
     const double yv = val[0];
     if constexpr (MOM) {
@@ -956,12 +977,13 @@ __global__ void __launch_bounds__(128) coef64_kernel(const StageArgs a) {
     }
     __syncthreads();
     if (threadIdx.x < 32) {
-      double c = 0.0;
+      double c = 0.0, P = 0.0;
       bool ill = false;
       if (a.mode == kModeChain)
-        coefficient_chain<KG>(G, zeros, 0.0, snorm, c, ill, a.Kreal);
+        coefficient_chain<KG>(G, zeros, 0.0, snorm, c, ill, a.Kreal, &P);
       else
-        coefficient_tree<KG>(G, zeros, 0.0, snorm, c, ill);
+        coefficient_tree<KG>(G, zeros, 0.0, snorm, c, ill, &P);
+      if (threadIdx.x == 0 && a.outnorm2) a.outnorm2[seg] = P;
       if (threadIdx.x < KG) a.coef64[(static_cast<size_t>(q) * a.nsegs + seg) * KG + threadIdx.x] = c;
     }
   }

@@ -38,6 +38,15 @@ int combine64_k(const StageArgs& a, dim3 grid, void* stream, const char** name) 
 }
 }  // namespace
 
+int launch_orthogonality(const double* outnorm2, const double* diag_sum, int groups, int nsegs,
+                         float* ortho, void* stream, const char** name) {
+  *name = "orthogonality";
+  const int grid = (nsegs + kThreads - 1) / kThreads;
+  orthogonality_kernel<<<grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+      outnorm2, diag_sum, groups, nsegs, ortho);
+  return static_cast<int>(cudaGetLastError());
+}
+
 int launch_collect(const StageArgs& a, int grid, void* stream, const char** name) {
   *name = "collect";
   return launch(collect_kernel, dim3(grid), dim3(kThreads), a, stream);

@@ -107,6 +107,22 @@ ADASUM_API adasum_status_t adasum_reduce(const void *const *grads, int K, const 
                               adasum_stream_t stream);
 
 /*
+ * adasum_reduce_orthogonality -- adasum_reduce, and per segment the orthogonality metric
+ * of the paper's Figure 1 (Section 3):
+ *
+ *     ortho[s] = |Adasum(g_0..g_{K-1})|^2 / sum_k |g_k|^2     over segment s,
+ *
+ * which is 1 for mutually orthogonal gradients and 1/K for K parallel gradients of equal
+ * norm.  ortho is a DEVICE array of L floats; an all-zero (or empty) segment gives NaN.
+ * |A|^2 is the fp64 quadratic form of the final coefficients in the segment's Gram
+ * matrix (the fp64 recompute's, for recomputed segments), not the rounded output.
+ */
+ADASUM_API adasum_status_t adasum_reduce_orthogonality(const void *const *grads, int K,
+                                                       const int64_t *seg_offsets, int L,
+                                                       adasum_dtype_t dtype, void *out,
+                                                       float *ortho, adasum_stream_t stream);
+
+/*
  * adasum_reduce_chain -- the linear recursion of the same section of the paper,
  * g[0,n+1] = Adasum(g[0,n], g_{n+1}): workers are folded in one at a time, left to
  * right, instead of pairwise up a tree.  Same arguments and conventions as

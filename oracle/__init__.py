@@ -62,6 +62,11 @@ def open_library(path: str):
     lib.oracle_momentum_sgd.argtypes = [dp, i64, vp, vp, ctypes.c_double,
                                         ctypes.c_double, vp, vp]
     lib.oracle_momentum_sgd.restype = ctypes.c_int
+    lib.oracle_local_momentum_adasum.argtypes = [ctypes.POINTER(vp), ctypes.c_int,
+                                                 ctypes.POINTER(i64), ctypes.c_int, ctypes.c_int,
+                                                 ctypes.POINTER(vp), vp, ctypes.c_double,
+                                                 ctypes.c_double]
+    lib.oracle_local_momentum_adasum.restype = ctypes.c_int
     lib.oracle_bf16_encode.argtypes = [ctypes.c_double]
     lib.oracle_bf16_encode.restype = ctypes.c_uint16
     lib.oracle_bf16_decode.argtypes = [ctypes.c_uint16]
@@ -160,6 +165,26 @@ def momentum_sgd(A64, w, v, lr, mu, lib=None):
     if rc != 0:
         raise ValueError(f"oracle_momentum_sgd failed with code {rc}")
     return w_out, v_out
+
+
+def local_momentum_adasum(grads, seg_offsets, v, w, lr, mu, lib=None):
+    """Adasum after the optimizer: per-worker heavy-ball steps v_k' = mu v_k + g_k, then
+    w' = w + Adasum(-lr v_k').  Returns (v' list, w') as float32 arrays (copies)."""
+    lib = _load(lib)
+    grads = [np.ascontiguousarray(g) for g in grads]
+    K = len(grads)
+    code = _dtype_code(grads[0])
+    offs = np.ascontiguousarray(seg_offsets, dtype=np.int64)
+    vs = [np.array(x, dtype=np.float32, copy=True) for x in v]
+    w_out = np.array(w, dtype=np.float32, copy=True)
+    gp = (ctypes.c_void_p * K)(*[g.ctypes.data for g in grads])
+    vp = (ctypes.c_void_p * K)(*[x.ctypes.data for x in vs])
+    rc = lib.oracle_local_momentum_adasum(gp, K, offs.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
+                                          offs.shape[0] - 1, code, vp, w_out.ctypes.data,
+                                          float(lr), float(mu))
+    if rc != 0:
+        raise ValueError(f"oracle_local_momentum_adasum failed with code {rc}")
+    return vs, w_out
 
 
 def bf16_encode(x, lib=None) -> np.ndarray:

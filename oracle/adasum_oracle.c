@@ -38,6 +38,10 @@
  *     equals padding with zero gradients, because Adasum(x, 0) = x.)
  *   - Fused Momentum-SGD (heavy ball): v' = mu v + A, w' = w - lr v', evaluated in fp64
  *     from the unrounded Adasum result A and rounded to fp32 at the end.
+ *   - Adasum after the optimizer (Section 3, Figure 3): every worker k first takes its own
+ *     heavy-ball step on its own momentum, v_k' = mu v_k + g_k (stored in fp32, its state),
+ *     proposes the update -lr v_k', and the proposals are combined by Adasum and applied:
+ *     w' = w + Adasum(-lr v_0', ..., -lr v_{K-1}').
  *
  * Build: gcc -O2 -ffp-contract=off -fPIC -shared (no fast-math, no FMA contraction, so
  * x86-64 and aarch64 hosts give the same bits).
@@ -234,6 +238,59 @@ int oracle_adasum_pair(const void *a, const void *b, int64_t n, int dtype, void 
   const void *g[2] = {a, b};
   int64_t offs[2] = {0, n};
   return oracle_adasum_reduce(g, 2, offs, 1, dtype, out, out64, NULL, NULL);
+}
+
+/* Adasum after the optimizer: per-worker heavy-ball steps, then the workers' proposed
+ * updates combined by the Adasum tree and applied.
+ *   grads : K host pointers to N elements of `dtype`;  v : K host fp32 arrays (updated);
+ *   w     : fp32 weights (updated).
+ * v_k' = fp32(mu v_k + g_k) (evaluated in fp64, rounded once: the stored state);
+ * A = Adasum over the updates -lr v_k' (fp64, from the stored fp32 v_k');  w' = fp32(w + A). */
+int oracle_local_momentum_adasum(const void *const *grads, int K, const int64_t *offs, int L,
+                                 int dtype, float *const *v, float *w, double lr, double mu) {
+  if (!grads || !v || !w || K < 1 || L < 0 || !offs) return ORACLE_ERR_ARG;
+  const int64_t N = offs[L];
+  for (int k = 0; k < K; ++k)
+    for (int64_t j = 0; j < N; ++j)
+      v[k][j] = (float)(mu * (double)v[k][j] + load_elem(grads[k], dtype, j));
+  /* the proposed updates -lr v_k', exactly as fp64 values, stored as fp64 arrays */
+  double **upd = (double **)malloc((size_t)K * sizeof(double *));
+  if (!upd) return ORACLE_ERR_NOMEM;
+  for (int k = 0; k < K; ++k) upd[k] = NULL;
+  int rc = ORACLE_OK;
+  for (int k = 0; k < K && rc == ORACLE_OK; ++k) {
+    upd[k] = (double *)malloc((size_t)(N > 0 ? N : 1) * sizeof(double));
+    if (!upd[k]) rc = ORACLE_ERR_NOMEM;
+    else
+      for (int64_t j = 0; j < N; ++j) upd[k][j] = -lr * (double)v[k][j];
+  }
+  if (rc == ORACLE_OK) {
+    double *A = (double *)malloc((size_t)(N > 0 ? N : 1) * sizeof(double));
+    if (!A) {
+      rc = ORACLE_ERR_NOMEM;
+    } else {
+      /* per segment, the tree over the fp64 updates */
+      for (int s = 0; s < L && rc == ORACLE_OK; ++s) {
+        const int64_t base = offs[s], n = offs[s + 1] - offs[s];
+        if (n == 0) continue;
+        double *level = (double *)malloc((size_t)K * (size_t)n * sizeof(double));
+        if (!level) {
+          rc = ORACLE_ERR_NOMEM;
+          break;
+        }
+        for (int k = 0; k < K; ++k) memcpy(level + (size_t)k * (size_t)n, upd[k] + base, (size_t)n * sizeof(double));
+        tree_levels(level, NULL, K, n);
+        memcpy(A + base, level, (size_t)n * sizeof(double));
+        free(level);
+      }
+      if (rc == ORACLE_OK)
+        for (int64_t j = 0; j < N; ++j) w[j] = (float)((double)w[j] + A[j]);
+      free(A);
+    }
+  }
+  for (int k = 0; k < K; ++k) free(upd[k]);
+  free(upd);
+  return rc;
 }
 
 /* Heavy-ball Momentum-SGD step applied to the Adasum result A (fp64, unrounded):

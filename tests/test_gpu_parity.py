@@ -457,3 +457,41 @@ def test_chain_cancelling_scalars_recomputed(native):
     torch.cuda.synchronize()
     ref = oracle.adasum_reduce([to_oracle_input(g) for g in grads], offs, chain=True)
     check_fp32_segments(to_f64(out), ref["out64"], offs)
+
+
+# --------------------------------------------------------- orthogonality metric (Fig. 1)
+
+@pytest.mark.parametrize("K", [1, 2, 8, 16, 24, 64])
+def test_orthogonality_metric(native, K):
+    lengths = [1, 7, 0, 33, 4097, 300, 70_001]
+    offs = workloads.offsets_from_numels(lengths)
+    grads = rand_grads(K, int(offs[-1]), torch.float32, seed=140 + K)
+    grads[0][offs[2]:offs[2] + 0].zero_()
+    out, ortho = ags.reduce(grads, offs, orthogonality=True)
+    torch.cuda.synchronize()
+    ref = oracle.adasum_reduce([to_oracle_input(g) for g in grads], offs, want_ortho=True)
+    check_fp32_segments(to_f64(out), ref["out64"], offs)
+    got = ortho.double().cpu().numpy()
+    exp = ref["ortho"]
+    assert np.array_equal(np.isnan(got), np.isnan(exp))
+    ok = ~np.isnan(exp)
+    np.testing.assert_allclose(got[ok], exp[ok], rtol=2e-5)
+
+
+def test_orthogonality_claims_on_gpu(native):
+    """The paper's two reference values: 1 for mutually orthogonal gradients, 1/64 for 64
+    parallel gradients of equal norm."""
+    n, K = 6400, 64
+    gen = torch.Generator(device=DEV).manual_seed(150)
+    owner = torch.randint(0, K, (n,), generator=gen, device=DEV)
+    vals = torch.randn(n, generator=gen, device=DEV)
+    orth = [torch.where(owner == k, vals, torch.zeros_like(vals)) for k in range(K)]
+    s = torch.randn(n, generator=gen, device=DEV)
+    par = [s.clone() for _ in range(K)]
+    offs = [0, n, 2 * n]
+    grads = [torch.cat([a, b]) for a, b in zip(orth, par)]
+    _, ortho = ags.reduce(grads, offs, orthogonality=True)
+    torch.cuda.synchronize()
+    got = ortho.cpu().numpy()
+    assert got[0] == pytest.approx(1.0, rel=1e-6)
+    assert got[1] == pytest.approx(1.0 / 64, rel=1e-6)

@@ -343,3 +343,48 @@ def test_rejects_decreasing_offsets(oracle_mod):
     vecs = f32([1, 2, 3], [3, 4, 5])
     with pytest.raises(ValueError):
         oracle_mod.adasum_reduce(vecs, [0, 2, 1, 3])
+
+
+# ----------------------------------------------------- Adasum after the optimizer (Fig. 3)
+
+def test_local_momentum_updates_match_torch_sgd_per_worker(oracle_mod):
+    """Each worker's state update is torch.optim.SGD's momentum buffer update; with one
+    worker the whole step is torch's SGD step."""
+    rs = np.random.default_rng(300)
+    n, K = 57, 4
+    grads = [rs.standard_normal(n).astype(np.float32) for _ in range(K)]
+    v = [(rs.standard_normal(n) * 0.01).astype(np.float32) for _ in range(K)]
+    w = (rs.standard_normal(n) * 0.02).astype(np.float32)
+    lr, mu = float(np.float32(0.1)), float(np.float32(0.9))
+    v_new, _ = oracle_mod.local_momentum_adasum(grads, [0, n], v, w, lr, mu)
+    for k in range(K):
+        p = torch.nn.Parameter(torch.zeros(n, dtype=torch.float64))
+        opt = torch.optim.SGD([p], lr=lr, momentum=mu)
+        opt.state[p]["momentum_buffer"] = torch.from_numpy(v[k].astype(np.float64))
+        p.grad = torch.from_numpy(grads[k].astype(np.float64))
+        opt.step()
+        assert np.array_equal(v_new[k], opt.state[p]["momentum_buffer"].numpy().astype(np.float32))
+    # one worker: exactly SGD
+    _, w1 = oracle_mod.local_momentum_adasum(grads[:1], [0, n], v[:1], w, lr, mu)
+    p = torch.nn.Parameter(torch.from_numpy(w.astype(np.float64)))
+    opt = torch.optim.SGD([p], lr=lr, momentum=mu)
+    opt.state[p]["momentum_buffer"] = torch.from_numpy(v[0].astype(np.float64))
+    p.grad = torch.from_numpy(grads[0].astype(np.float64))
+    opt.step()
+    np.testing.assert_allclose(w1, p.detach().numpy().astype(np.float32), rtol=0, atol=1e-7)
+
+
+def test_local_momentum_first_step_equals_allreduce_then_step(oracle_mod):
+    """With zero momentum, Adasum after the optimizer and Adasum-then-heavy-ball agree
+    (scale equivariance: Adasum(-lr g) = -lr Adasum(g))."""
+    rs = np.random.default_rng(301)
+    n, K = 40, 8
+    grads = [rs.standard_normal(n).astype(np.float32) for _ in range(K)]
+    offs = [0, 13, 40]
+    w = (rs.standard_normal(n) * 0.02).astype(np.float32)
+    zeros = [np.zeros(n, np.float32) for _ in range(K)]
+    lr, mu = float(np.float32(0.1)), float(np.float32(0.9))
+    _, w_local = oracle_mod.local_momentum_adasum(grads, offs, zeros, w, lr, mu)
+    A = oracle_mod.adasum_reduce(grads, offs)["out64"]
+    w_r1, _ = oracle_mod.momentum_sgd(A, w, np.zeros(n, np.float32), lr, mu)
+    np.testing.assert_allclose(w_local, w_r1, rtol=0, atol=2e-8)
