@@ -22,7 +22,7 @@ import torch
 
 from ._native import AdasumError, KernelStat, Status, check, library_path, load_library
 
-__all__ = ["reduce", "pair", "pair_noalloc", "reduce_momentum_sgd", "reduce_from_host", "AdasumError",
+__all__ = ["reduce", "pair", "pair_noalloc", "reduce_momentum_sgd", "local_momentum_reduce", "reduce_from_host", "AdasumError",
            "Status", "load_library", "library_path", "get_last_error", "release_workspace",
            "launch_count", "recomputed_segments", "profile_enable", "profile_collect", "version"]
 
@@ -177,6 +177,33 @@ def reduce_momentum_sgd(grads, seg_offsets, master_w: torch.Tensor, momentum: to
             ctypes.c_void_p(0 if out is None else out.data_ptr()), _stream_handle(device, stream))
     check(st, "adasum_reduce_momentum_sgd")
     return master_w, momentum, out
+
+
+def local_momentum_reduce(grads, seg_offsets, momenta, master_w: torch.Tensor, *, lr: float,
+                          mu: float, stream: torch.cuda.Stream | None = None):
+    """Adasum after the optimizer (``adasum_local_momentum_reduce``): every worker k takes
+    its own heavy-ball step v_k <- mu v_k + g_k (``momenta[k]``, fp32, in place), then
+    w <- w - lr Adasum(v_0, ..., v_{K-1}) updates ``master_w`` in place."""
+    grads = _as_list(grads)
+    dtype, device, n = _check_grads(grads)
+    offs = _offsets(seg_offsets, n)
+    momenta = list(momenta)
+    if len(momenta) != len(grads):
+        raise ValueError("one momentum buffer per worker")
+    for t in momenta + [master_w]:
+        if t.dtype != torch.float32 or t.device != device or t.numel() != n or not t.is_contiguous():
+            raise ValueError(f"states must be contiguous float32 tensors of {n} elements on {device}")
+    lib = load_library()
+    K = len(grads)
+    gp = (ctypes.c_void_p * K)(*[g.data_ptr() for g in grads])
+    vp = (ctypes.c_void_p * K)(*[v.data_ptr() for v in momenta])
+    with torch.cuda.device(device):
+        st = lib.adasum_local_momentum_reduce(
+            gp, K, offs.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), offs.shape[0] - 1,
+            _DTYPE_CODE[dtype], vp, ctypes.c_void_p(master_w.data_ptr()), float(lr), float(mu),
+            _stream_handle(device, stream))
+    check(st, "adasum_local_momentum_reduce")
+    return master_w, momenta
 
 
 def reduce_from_host(grads_host: Sequence[torch.Tensor], seg_offsets=None, *,

@@ -58,6 +58,10 @@ SIGNATURES = {
         ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p]),
     "adasum_pair_noalloc": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
                                            ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]),
+    "adasum_local_momentum_reduce": (ctypes.c_int, [
+        ctypes.POINTER(ctypes.c_void_p), ctypes.c_int, ctypes.POINTER(ctypes.c_int64),
+        ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_void_p), ctypes.c_void_p,
+        ctypes.c_float, ctypes.c_float, ctypes.c_void_p]),
     "adasum_get_last_error": (ctypes.c_int, []),
     "adasum_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "adasum_release_workspace": (ctypes.c_int, []),

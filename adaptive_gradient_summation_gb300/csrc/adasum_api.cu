@@ -529,8 +529,7 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
     if (offs[s + 1] < offs[s]) return ADASUM_ERR_INVALID_ARG;
   const int64_t N = offs[L];
   if (N == 0) return ADASUM_OK;
-  if (!mom && out == nullptr) return ADASUM_ERR_INVALID_ARG;
-  if (mom && momentum == nullptr) return ADASUM_ERR_INVALID_ARG;
+  if (!mom && out == nullptr) return ADASUM_ERR_INVALID_ARG;  // (momentum null: plain step)
   for (int k = 0; k < Kreal; ++k)
     if (grads[k] == nullptr) return ADASUM_ERR_INVALID_ARG;
   const size_t es = elem_size(dtype);
@@ -541,11 +540,12 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
   }
   if (mom) {
     const size_t fb = static_cast<size_t>(N) * sizeof(float);
-    if (overlaps(master_w, fb, momentum, fb)) return ADASUM_ERR_ALIAS;
+    const size_t mb = momentum ? fb : 0;
+    if (overlaps(master_w, fb, momentum, mb)) return ADASUM_ERR_ALIAS;
     for (int k = 0; k < Kreal; ++k)
-      if (overlaps(master_w, fb, grads[k], nbytes) || overlaps(momentum, fb, grads[k], nbytes))
+      if (overlaps(master_w, fb, grads[k], nbytes) || overlaps(momentum, mb, grads[k], nbytes))
         return ADASUM_ERR_ALIAS;
-    if (out && (overlaps(master_w, fb, out, nbytes) || overlaps(momentum, fb, out, nbytes)))
+    if (out && (overlaps(master_w, fb, out, nbytes) || overlaps(momentum, mb, out, nbytes)))
       return ADASUM_ERR_ALIAS;
   }
   if (!mom && Kreal == 1 && out == grads[0] && ortho == nullptr) return ADASUM_OK;  // in-place copy
@@ -642,6 +642,7 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
   }
 
   bool all_aligned = aligned16(out) && (!mom || (aligned16(master_w) && aligned16(momentum)));
+  // (aligned16(nullptr) is true: absent buffers do not force the scalar path)
   for (int k = 0; k < Kreal; ++k) all_aligned = all_aligned && aligned16(grads[k]);
 
   if (cudaMemsetAsync(seg_flag, 0, n_ints * sizeof(int), stream) != cudaSuccess)
@@ -828,6 +829,46 @@ adasum_status_t adasum_reduce(const void* const* grads, int K, const int64_t* se
   std::lock_guard<std::mutex> lock(g_mu);
   return reduce_impl(grads, K, seg_offsets, L, static_cast<int>(dtype), out, nullptr,
                      nullptr, 0.f, 0.f, reinterpret_cast<cudaStream_t>(stream));
+}
+
+adasum_status_t adasum_local_momentum_reduce(const void* const* grads, int K,
+                                             const int64_t* seg_offsets, int L,
+                                             adasum_dtype_t grad_dtype, float* const* momenta,
+                                             float* master_w, float lr, float mu,
+                                             adasum_stream_t stream) {
+  if (grads == nullptr || momenta == nullptr || master_w == nullptr || K < 1 || L < 0 ||
+      (L > 0 && seg_offsets == nullptr))
+    return ADASUM_ERR_INVALID_ARG;
+  if (grad_dtype != ADASUM_F32 && grad_dtype != ADASUM_BF16) return ADASUM_ERR_INVALID_ARG;
+  if (K > ADASUM_MAX_K) return ADASUM_ERR_UNSUPPORTED;
+  if (L == 0 || seg_offsets[L] == 0) return ADASUM_OK;
+  const int64_t N = seg_offsets[L];
+  const size_t gb = static_cast<size_t>(N) * (grad_dtype == ADASUM_BF16 ? 2 : 4);
+  const size_t fb = static_cast<size_t>(N) * sizeof(float);
+  for (int k = 0; k < K; ++k) {
+    if (grads[k] == nullptr || momenta[k] == nullptr) return ADASUM_ERR_INVALID_ARG;
+    if (overlaps(momenta[k], fb, master_w, fb)) return ADASUM_ERR_ALIAS;
+    for (int j = 0; j < K; ++j)
+      if (overlaps(momenta[k], fb, grads[j], gb) || (j != k && overlaps(momenta[k], fb, momenta[j], fb)))
+        return ADASUM_ERR_ALIAS;
+  }
+  std::lock_guard<std::mutex> lock(g_mu);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int device = 0, num_sms = 148;
+  if (cudaGetDevice(&device) != cudaSuccess) return ADASUM_ERR_CUDA;
+  cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, device);
+  // every worker's own heavy-ball step on its own state
+  for (int k = 0; k < K; ++k) {
+    const int aligned = aligned16(grads[k]) && aligned16(momenta[k]);
+    if (adasum_status_t st = launch_one(s, [&](const char** n) {
+          return launch_local_momentum(grads[k], static_cast<int>(grad_dtype), momenta[k], N, mu,
+                                       aligned, num_sms, s, n);
+        }))
+      return st;
+  }
+  // Adasum of the proposed updates -lr v_k' = -lr Adasum(v_k'), applied: w -= lr A(v')
+  std::vector<const void*> vs(momenta, momenta + K);
+  return reduce_impl(vs.data(), K, seg_offsets, L, kF32, nullptr, master_w, nullptr, lr, 0.f, s);
 }
 
 adasum_status_t adasum_reduce_orthogonality(const void* const* grads, int K,

@@ -158,6 +158,9 @@ int pipeline_grid(int in_dtype, int out_dtype, int Kg, int momentum, int num_sms
 int launch_reduce_chunks(const StageArgs& a, void* stream, const char** name);
 // fp64 path: build the flagged lists, then Gram / coefficients / combine over them.
 int launch_collect(const StageArgs& a, int grid, void* stream, const char** name);
+// v = mu v + g for one worker (grad in `dtype`, state fp32).
+int launch_local_momentum(const void* g, int dtype, float* v, int64_t n, float mu, int aligned,
+                          int num_sms, void* stream, const char** name);
 // ortho[s] = outnorm2[s] / sum_q diag_sum[q][s] (NaN when the sum is 0).
 int launch_orthogonality(const double* outnorm2, const double* diag_sum, int groups, int nsegs,
                          float* ortho, void* stream, const char** name);

@@ -706,14 +706,19 @@ __device__ __forceinline__ void combine_tile(const StageArgs& a, int tile_id, in
     const int64_t p0 = v * VW;
     if constexpr (MOM) {
       float wv[VW], mv[VW];
-      load_f32_vec<VW>(a.momentum, p0, lo, hi, aligned, mv);
       load_f32_vec<VW>(a.master_w, p0, lo, hi, aligned, wv);
+      if (a.momentum != nullptr) {  // heavy ball: v' = mu v + A, w' = w - lr v'
+        load_f32_vec<VW>(a.momentum, p0, lo, hi, aligned, mv);
 #pragma unroll
-      for (int e = 0; e < VW; ++e) {
-        mv[e] = __fmaf_rn(a.mu, mv[e], val[e]);
-        wv[e] = __fmaf_rn(-a.lr, mv[e], wv[e]);
+        for (int e = 0; e < VW; ++e) {
+          mv[e] = __fmaf_rn(a.mu, mv[e], val[e]);
+          wv[e] = __fmaf_rn(-a.lr, mv[e], wv[e]);
+        }
+        store_vec<F32Tag, VW>(a.momentum, p0, lo, hi, aligned, mv);
+      } else {                      // plain step: w' = w - lr A
+#pragma unroll
+        for (int e = 0; e < VW; ++e) wv[e] = __fmaf_rn(-a.lr, val[e], wv[e]);
       }
-      store_vec<F32Tag, VW>(a.momentum, p0, lo, hi, aligned, mv);
       store_vec<F32Tag, VW>(a.master_w, p0, lo, hi, aligned, wv);
       if (y != nullptr) store_vec<OutTag, VW>(y, p0, lo, hi, aligned, val);
     } else {
@@ -811,6 +816,27 @@ __global__ void __launch_bounds__(kThreads, 3) pipeline_kernel(const StageArgs a
   }
 }
 
+// ------------------------------------------------ per-worker heavy-ball step (Fig. 3)
+
+// v = mu v + g for one worker (fp32 state; g widened from its storage type).
+template <typename Tag>
+__global__ void __launch_bounds__(kThreads) local_momentum_kernel(const void* g, float* v,
+                                                                  int64_t n, float mu, int aligned) {
+  using S = typename ElemTraits<Tag>::Storage;
+  constexpr int VW = ElemTraits<Tag>::kVW;
+  const S* x = static_cast<const S*>(g);
+  const int64_t nv = (n + VW - 1) / VW;
+  for (int64_t vi = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; vi < nv;
+       vi += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const uint4 r = load_vec_raw<Tag, kLoadStream>(x, vi, 0, n, aligned != 0);
+    float m[VW], out[VW];
+    load_f32_vec<VW>(v, vi * VW, 0, n, aligned != 0, m);
+#pragma unroll
+    for (int e = 0; e < VW; ++e) out[e] = __fmaf_rn(mu, m[e], vec_elem<Tag>(r, e));
+    store_vec<F32Tag, VW>(v, vi * VW, 0, n, aligned != 0, out);
+  }
+}
+
 // ---------------------------------------------------------------- fp64 recompute path
 //
 // Segments flagged by coef_kernel are recomputed here entirely in fp64: exact products
@@ -904,10 +930,12 @@ __global__ void __launch_bounds__(kThreads) tiny64_kernel(const StageArgs a) {
     if (!on) continue;
     const double yv = val[0];
     if constexpr (MOM) {
-      const double v = static_cast<double>(a.mu) * static_cast<double>(a.momentum[p]) + yv;
-      const double w = static_cast<double>(a.master_w[p]) - static_cast<double>(a.lr) * v;
-      a.momentum[p] = static_cast<float>(v);
-      a.master_w[p] = static_cast<float>(w);
+      double v = yv;
+      if (a.momentum != nullptr) {
+        v = static_cast<double>(a.mu) * static_cast<double>(a.momentum[p]) + yv;
+        a.momentum[p] = static_cast<float>(v);
+      }
+      a.master_w[p] = static_cast<float>(static_cast<double>(a.master_w[p]) - static_cast<double>(a.lr) * v);
       if (a.out[0] == nullptr) continue;
     }
     if constexpr (OUT == kKindF32) {
@@ -1018,10 +1046,12 @@ __global__ void __launch_bounds__(kThreads) combine64_kernel(const StageArgs a) 
     for (int64_t p = t.start + threadIdx.x; p < t.start + t.len; p += kThreads) {
       const double y = tree_combine64<IN, 0, KG, KG>(c, a, q, p);
       if constexpr (MOM) {
-        const double v = static_cast<double>(a.mu) * static_cast<double>(a.momentum[p]) + y;
-        const double w = static_cast<double>(a.master_w[p]) - static_cast<double>(a.lr) * v;
-        a.momentum[p] = static_cast<float>(v);
-        a.master_w[p] = static_cast<float>(w);
+        double v = y;
+        if (a.momentum != nullptr) {
+          v = static_cast<double>(a.mu) * static_cast<double>(a.momentum[p]) + y;
+          a.momentum[p] = static_cast<float>(v);
+        }
+        a.master_w[p] = static_cast<float>(static_cast<double>(a.master_w[p]) - static_cast<double>(a.lr) * v);
         if (a.out[q] == nullptr) continue;
       }
       if constexpr (OUT == kKindF64) {

@@ -1,5 +1,7 @@
 // launch_f64.cu -- launchers of the fp64 recompute path (flagged segments only) and of
 // the list-building kernel.
+#include <algorithm>
+
 #include "adasum_kernels.cuh"
 
 namespace adasum {
@@ -37,6 +39,19 @@ int combine64_k(const StageArgs& a, dim3 grid, void* stream, const char** name) 
   }
 }
 }  // namespace
+
+int launch_local_momentum(const void* g, int dtype, float* v, int64_t n, float mu, int aligned,
+                          int num_sms, void* stream, const char** name) {
+  *name = "local_momentum";
+  const int64_t vw = dtype == kBF16 ? 8 : 4;
+  const int64_t blocks = std::min<int64_t>((n / vw + kThreads) / kThreads, 8LL * num_sms);
+  const dim3 grid(static_cast<unsigned>(std::max<int64_t>(1, blocks)));
+  if (dtype == kBF16)
+    local_momentum_kernel<BF16Tag><<<grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(g, v, n, mu, aligned);
+  else
+    local_momentum_kernel<F32Tag><<<grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(g, v, n, mu, aligned);
+  return static_cast<int>(cudaGetLastError());
+}
 
 int launch_orthogonality(const double* outnorm2, const double* diag_sum, int groups, int nsegs,
                          float* ortho, void* stream, const char** name) {

@@ -164,6 +164,28 @@ ADASUM_API adasum_status_t adasum_reduce_momentum_sgd(const void *const *grads, 
                                            void *out_or_null, adasum_stream_t stream);
 
 /*
+ * adasum_local_momentum_reduce -- Adasum after the optimizer (paper, Section 3 and
+ * Figure 3): every worker first takes its own heavy-ball step on its own momentum,
+ *
+ *     v_k' = mu * v_k + g_k                       (per worker, fp32 state, in place)
+ *
+ * proposes the update -lr * v_k', and the proposals are combined by the Adasum tree and
+ * applied:  w' = w + Adasum(-lr v_0', ..., -lr v_{K-1}') = w - lr * Adasum(v_0', ...).
+ * (Adasum is scale-equivariant.)  With zero initial momenta the first step equals
+ * adasum_reduce_momentum_sgd's.
+ *   grads     K device pointers, N elements of grad_dtype each (not modified)
+ *   momenta   host array of K device pointers to fp32 states of N elements, updated
+ *   master_w  device fp32 weights of N elements, updated
+ * The states must not overlap each other, the gradients or the weights.
+ */
+ADASUM_API adasum_status_t adasum_local_momentum_reduce(const void *const *grads, int K,
+                                                        const int64_t *seg_offsets, int L,
+                                                        adasum_dtype_t grad_dtype,
+                                                        float *const *momenta, float *master_w,
+                                                        float lr, float mu,
+                                                        adasum_stream_t stream);
+
+/*
  * adasum_get_last_error -- the sticky device-side status of the current device
  * (ADASUM_OK or ADASUM_ERR_TIMEOUT), read after the caller has synchronised the stream
  * of the calls in question.  Reading clears it.  Host-side failures are returned by the

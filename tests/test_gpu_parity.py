@@ -495,3 +495,33 @@ def test_orthogonality_claims_on_gpu(native):
     got = ortho.cpu().numpy()
     assert got[0] == pytest.approx(1.0, rel=1e-6)
     assert got[1] == pytest.approx(1.0 / 64, rel=1e-6)
+
+
+# ------------------------------------------------ Adasum after the optimizer (Fig. 3)
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("K", [1, 4, 8, 13])
+def test_local_momentum_reduce(native, K, dtype):
+    lengths = [1, 7, 33, 4097, 300, 70_001]
+    offs = workloads.offsets_from_numels(lengths)
+    n = int(offs[-1])
+    grads = rand_grads(K, n, dtype, seed=160 + K)
+    gen = torch.Generator(device=DEV).manual_seed(161)
+    v = [0.01 * torch.randn(n, generator=gen, device=DEV) for _ in range(K)]
+    w = 0.02 * torch.randn(n, generator=gen, device=DEV)
+    v0 = [x.cpu().numpy() for x in v]
+    w0 = w.cpu().numpy()
+    lr, mu = 0.1, 0.9
+    ags.local_momentum_reduce(grads, offs, v, w, lr=lr, mu=mu)
+    torch.cuda.synchronize()
+    v_ref, w_ref = oracle.local_momentum_adasum([to_oracle_input(g) for g in grads], offs, v0, w0,
+                                                float(np.float32(lr)), float(np.float32(mu)))
+    for k in range(K):   # fma vs fp64-then-fp32: at most one fp32 rounding apart
+        got = v[k].cpu().numpy()
+        assert np.all(np.abs(got - v_ref[k]) <= np.spacing(np.abs(v_ref[k]).astype(np.float32)))
+    upd = oracle.adasum_reduce(v_ref, offs)["out64"]
+    for s in range(len(offs) - 1):
+        lo, hi = int(offs[s]), int(offs[s + 1])
+        dw = np.linalg.norm(w.cpu().numpy()[lo:hi].astype(np.float64) - w_ref[lo:hi])
+        tol = 1e-5 * lr * np.linalg.norm(upd[lo:hi]) + 2.0**-23 * np.linalg.norm(w_ref[lo:hi])
+        assert dw <= tol + 1e-30, s
