@@ -51,6 +51,13 @@ int64_t env_int(const char* name, int64_t dflt) {
   return x > 0 ? x : dflt;
 }
 
+// An on/off switch from the environment: "0" is off, anything else on, unset `dflt`.
+bool env_on(const char* name, bool dflt) {
+  const char* v = std::getenv(name);
+  if (v == nullptr || *v == '\0') return dflt;
+  return std::strcmp(v, "0") != 0;
+}
+
 
 // ------------------------------------------------------------------------ profiler
 
@@ -103,6 +110,19 @@ struct Plan {
   int stage_pos = 0;
   int* d_task_ptr = nullptr;
   int* d_seg_c0 = nullptr;
+  // small segments: held on chip (grouped by cluster size 1, 2, 4, 8, 16) or, up to
+  // kTinyDirect positions, one warp each; neither gets tiles.  The coefficient kernel
+  // then runs over the list of the remaining (tiled) segments.
+  int onchip_K = 0;  // padded worker count the grouping was made for (0: none)
+  int onchip_cmax = 0;
+  int onchip_count[5] = {0, 0, 0, 0, 0};
+  int onchip_first[5] = {0, 0, 0, 0, 0};
+  int* d_onchip = nullptr;
+  bool tiny_on = false;
+  int tiny_count = 0;
+  int* d_tiny = nullptr;
+  int ncoef = 0;
+  int* d_coef_list = nullptr;
 };
 
 struct Workspace {
@@ -131,6 +151,12 @@ void free_plan(Plan& p) {
   if (p.d_tasks) cudaFree(p.d_tasks);
   if (p.d_task_ptr) cudaFree(p.d_task_ptr);
   if (p.d_seg_c0) cudaFree(p.d_seg_c0);
+  if (p.d_onchip) cudaFree(p.d_onchip);
+  if (p.d_tiny) cudaFree(p.d_tiny);
+  if (p.d_coef_list) cudaFree(p.d_coef_list);
+  p.d_onchip = nullptr;
+  p.d_tiny = nullptr;
+  p.d_coef_list = nullptr;
   p.d_task_ptr = nullptr;
   p.d_seg_c0 = nullptr;
   p.d_tiles = nullptr;
@@ -294,10 +320,11 @@ adasum_status_t upload(T** dst, const std::vector<T>& v) {
 }
 
 adasum_status_t get_plan(Workspace& ws, const int64_t* offs, int L, int Kg0, int dtype, int route,
-                         Plan** out) {
+                         int onchip_K, int onchip_cmax, bool tiny_on, Plan** out) {
   const int64_t wave = route == kRouteStream ? env_int("ADASUM_WAVE_MB", 24) << 20 : wave_budget_bytes();
   for (auto it = ws.plans.begin(); it != ws.plans.end(); ++it) {
-    if (it->Kg0 == Kg0 && it->dtype == dtype && it->route == route &&
+    if (it->Kg0 == Kg0 && it->dtype == dtype && it->route == route && it->onchip_K == onchip_K &&
+        it->onchip_cmax == onchip_cmax && it->tiny_on == tiny_on &&
         (route == kRouteKernels ||
          (it->wave_bytes == wave && it->tile_kb == (tile_bytes(true) >> 10) &&
           it->delay_pct == env_int("ADASUM_PIPE_DELAY_PCT", 100) &&
@@ -321,12 +348,31 @@ adasum_status_t get_plan(Workspace& ws, const int64_t* offs, int L, int Kg0, int
   std::vector<TileDesc> tiles;
   std::vector<SegDesc> segs(L);
   std::vector<ChunkDesc> chunks;
+  std::vector<int> onchip[5], tiny;
+  const int64_t VW = dtype == kF32 ? 4 : 8;
+  const int64_t onchip_vecs = onchip_K > 0 ? onchip_positions(onchip_K) / VW : 0;
   for (int s = 0; s < L; ++s) {
     const int64_t lo = offs[s], hi = offs[s + 1];
     segs[s].start = lo;
     segs[s].len = hi - lo;
     segs[s].first_tile = static_cast<int32_t>(tiles.size());
-    if (hi > lo) {
+    bool small = false;
+    if (hi > lo && tiny_on && hi - lo <= kTinyDirect) {
+      tiny.push_back(s);
+      small = true;
+    }
+    if (hi > lo && !small && onchip_vecs > 0) {
+      // the smallest cluster whose CTAs hold the segment's 16-byte vectors
+      const int64_t nv = (hi + VW - 1) / VW - lo / VW;
+      for (int c = 0, C = 1; C <= onchip_cmax && c < 5; ++c, C *= 2) {
+        if ((nv + C - 1) / C <= onchip_vecs) {
+          onchip[c].push_back(s);
+          small = true;
+          break;
+        }
+      }
+    }
+    if (hi > lo && !small) {
       const int64_t base = lo / 32 * 32;
       for (int64_t b = base; b < hi; b += T) {
         const int64_t t0 = std::max(lo, b), t1 = std::min(hi, b + T);
@@ -356,7 +402,25 @@ adasum_status_t get_plan(Workspace& ws, const int64_t* offs, int L, int Kg0, int
   p.wave_bytes = wave;
   p.tile_kb = tile_bytes(true) >> 10;
   p.delay_pct = env_int("ADASUM_PIPE_DELAY_PCT", 100);
+  p.onchip_K = onchip_K;
+  p.onchip_cmax = onchip_cmax;
+  p.tiny_on = tiny_on;
+  p.tiny_count = static_cast<int>(tiny.size());
+  std::vector<int> onchip_all, coef_list;
+  for (int c = 0; c < 5; ++c) {
+    p.onchip_first[c] = static_cast<int>(onchip_all.size());
+    p.onchip_count[c] = static_cast<int>(onchip[c].size());
+    onchip_all.insert(onchip_all.end(), onchip[c].begin(), onchip[c].end());
+  }
+  const bool any_small = !onchip_all.empty() || !tiny.empty();
+  if (any_small)
+    for (int s = 0; s < L; ++s)
+      if (segs[s].ntiles > 0) coef_list.push_back(s);
+  p.ncoef = static_cast<int>(coef_list.size());
   adasum_status_t st = upload(&p.d_tiles, tiles);
+  if (!st && !onchip_all.empty()) st = upload(&p.d_onchip, onchip_all);
+  if (!st && !tiny.empty()) st = upload(&p.d_tiny, tiny);
+  if (!st && any_small) st = upload(&p.d_coef_list, coef_list);
   if (!st) st = upload(&p.d_segs, segs);
   if (!st) st = upload(&p.d_chunks, chunks);
   if (!st && route == kRouteFused) {
@@ -416,8 +480,9 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Host-side fault injection for the error-path tests: ADASUM_FAULT_INJECT=alloc makes
 // the next workspace growth fail as if cudaMalloc had; ADASUM_FAULT_INJECT=timeout makes
-// the fused kernel never publish segment coefficients and shortens its bounded wait, so
-// the wait runs out and the device status reports ADASUM_ERR_TIMEOUT.
+// the fused and streaming kernels never publish segment coefficients, and the
+// small-segment kernel expect 16 bulk-copy bytes that are never sent, with their bounded
+// waits shortened, so the waits run out and the device status reports ADASUM_ERR_TIMEOUT.
 bool inject_alloc_failure() {
   const char* v = std::getenv("ADASUM_FAULT_INJECT");
   return v != nullptr && std::strcmp(v, "alloc") == 0;
@@ -458,6 +523,7 @@ adasum_status_t launch_one(cudaStream_t stream, F&& f) {
 // conditioning check, combine (flagged segments are skipped and left to the fp64 path).
 adasum_status_t run_stage(StageArgs& a, int in_dtype, int out_dtype, int momentum,
                           cudaStream_t stream) {
+  if (a.ntiles == 0) return ADASUM_OK;  // every segment went to the small-segment kernels
   if (a.Kg > 1) {
     if (adasum_status_t st = launch_one(stream, [&](const char** n) {
           return in_dtype == kBF16 ? launch_gram_bf16(a, stream, n) : launch_gram_f32(a, stream, n);
@@ -581,8 +647,18 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
     route = requested_route();
     if (route == kRouteStream && !stream_supported(dtype, kg[0])) route = kRouteKernels;
   }
+  // Plain reductions: segments of at most kTinyDirect positions go to the warp kernel,
+  // small ones (up to 64 workers) to the on-chip kernel, the rest to the tiles.
+  const bool plain = route == kRouteKernels && !mom && !chain && ortho == nullptr && K >= 2 &&
+                     env_on("ADASUM_ONCHIP", true);
+  int onchip_K = 0, onchip_cmax = 0;
+  if (plain && K <= kOnchipMaxK) {
+    onchip_cmax = std::min<int>(onchip_max_cluster(dtype, K), env_int("ADASUM_ONCHIP_MAX_CLUSTER", 16));
+    if (onchip_cmax >= 1) onchip_K = K;
+  }
   Plan* plan = nullptr;
-  if (adasum_status_t st = get_plan(ws, offs, L, kg[0], dtype, route, &plan)) return st;
+  if (adasum_status_t st = get_plan(ws, offs, L, kg[0], dtype, route, onchip_K, onchip_cmax, plain, &plan))
+    return st;
 
   // Workspace layout.
   size_t max_e_tiles = 0, max_e_chunks = 0, max_coef = 0, max_g = 1;
@@ -596,9 +672,10 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
   const size_t inter32 = align_up(static_cast<size_t>(N) * sizeof(float), 256);
   const size_t inter64 = align_up(static_cast<size_t>(N) * sizeof(double), 256);
   Carver cv;
-  // One zeroed int region per call: segment flags, the 3 fp64-list counters, and the
-  // fused kernel's task counter, chunk counters, segment counters and ready flags.
-  const size_t n_ints = static_cast<size_t>(L) + 3 + 1 + plan->nchunks + 2 * static_cast<size_t>(L);
+  // One zeroed int region per call: segment flags, the 3 fp64-list counters and the
+  // small-segment kernel's recompute counter, and the fused kernel's task counter, chunk
+  // counters, segment counters and ready flags.
+  const size_t n_ints = static_cast<size_t>(L) + 4 + 1 + plan->nchunks + 2 * static_cast<size_t>(L);
   const size_t o_flags = cv.take(n_ints * sizeof(int));
   const size_t o_part = cv.take(max_e_tiles * sizeof(float));
   const size_t o_chunk = cv.take(max_e_chunks * sizeof(double));
@@ -628,7 +705,7 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
   char* base = static_cast<char*>(ws.buf);
   int* seg_flag = reinterpret_cast<int*>(base + o_flags);
   int* list_count = seg_flag + L;
-  int* task_counter = list_count + 3;
+  int* task_counter = list_count + 4;
   int* chunk_done = task_counter + 1;
   int* seg_done = chunk_done + plan->nchunks;
   int* seg_ready = seg_done + L;
@@ -671,6 +748,8 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
     a.list_tiny = reinterpret_cast<int*>(base + o_ltiny);
     a.list_count = list_count;
     a.Ktotal = chain ? Kreal : K;
+    a.seg_list = plan->d_coef_list;
+    a.nseg_list = plan->ncoef;
     a.mode = chain ? kModeChain : kModeTree;
     a.Kreal = Kreal;
     const bool last = s + 1 == kg.size();
@@ -686,6 +765,45 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
     }
     return a;
   };
+
+  // Tiny segments: one warp each.
+  if (plan->tiny_count > 0) {
+    TinyArgs ta;
+    std::memset(&ta, 0, sizeof ta);
+    for (int k = 0; k < K; ++k) ta.in[k] = grads[k];
+    ta.out = out;
+    ta.segs = plan->d_segs;
+    ta.list = plan->d_tiny;
+    ta.count = plan->tiny_count;
+    ta.K = K;
+    if (adasum_status_t st = launch_one(stream, [&](const char** n) { return launch_tiny_df(ta, dtype, stream, n); }))
+      return st;
+  }
+  // Small segments: whole tree on chip, one launch per cluster size.
+  if (plan->onchip_K > 0) {
+    OnchipArgs oa;
+    std::memset(&oa, 0, sizeof oa);
+    for (int k = 0; k < K; ++k) oa.in[k] = grads[k];
+    oa.out = out;
+    oa.segs = plan->d_segs;
+    oa.P = onchip_positions(K);
+    oa.aligned = all_aligned ? 1 : 0;
+    oa.error = ws.d_error;
+    oa.recomputed = list_count + 3;
+    oa.spin_budget = 2000000000LL;  // about one second of SM clock
+    if (inject_timeout()) {
+      oa.inject_extra_tx = 1;
+      oa.spin_budget = 200000LL;
+    }
+    for (int c = 0; c < 5; ++c) {
+      if (plan->onchip_count[c] == 0) continue;
+      oa.list = plan->d_onchip + plan->onchip_first[c];
+      if (adasum_status_t st = launch_one(stream, [&](const char** n) {
+            return launch_onchip(oa, dtype, K, plan->onchip_count[c], 1 << c, stream, n);
+          }))
+        return st;
+    }
+  }
 
   // fp32 pass: one streaming or fused kernel for a single stage, else stage by stage.
   if (route == kRouteStream) {
@@ -963,11 +1081,11 @@ int64_t adasum_recomputed_segments(void) {
   if (cudaGetDevice(&device) != cudaSuccess) return -1;
   Workspace& ws = workspace_for(device);
   if (ws.last_flag_counts == nullptr) return 0;
-  int counts[3] = {0, 0, 0};
+  int counts[4] = {0, 0, 0, 0};
   if (cudaDeviceSynchronize() != cudaSuccess ||
       cudaMemcpy(counts, ws.last_flag_counts, sizeof counts, cudaMemcpyDeviceToHost) != cudaSuccess)
     return -1;
-  return static_cast<int64_t>(counts[1]) + counts[2];
+  return static_cast<int64_t>(counts[1]) + counts[2] + counts[3];
 }
 
 int64_t adasum_launch_count(void) { return g_launches.load(); }

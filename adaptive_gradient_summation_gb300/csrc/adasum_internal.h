@@ -77,6 +77,8 @@ struct StageArgs {
   float* relerr;              // [G][nsegs] estimated relative error of this stage's output
   const float* in_relerr;     // [G*Kg][nsegs] same, of this stage's inputs (null = exact)
   int skip_flagged;           // combine: leave flagged segments to the fp64 path
+  const int* seg_list;        // coef: the segments to run (null: all nsegs)
+  int nseg_list;
 
   // fp64 path (only the segments listed by collect_kernel).
   double* partials64;         // [G][ntiles][E]
@@ -133,6 +135,38 @@ struct PipeArgs {
   int inject_no_ready;      // test hook: never publish (exercises the bounded wait)
 };
 
+// Small-segment kernel (adasum_onchip.cuh): one segment per CTA or thread-block cluster,
+// its K x n block held in shared memory, the whole tree evaluated on chip.
+constexpr int kOnchipMaxK = 64;
+// Shared memory per CTA for the block: K rows of P positions of 4 bytes each.
+constexpr int kOnchipDataBytes = 80 * 1024;
+__host__ __device__ constexpr int onchip_positions(int K) { return kOnchipDataBytes / (4 * K); }
+
+struct OnchipArgs {
+  const void* in[kOnchipMaxK];  // K leaves (K a power of two); null = a zero gradient
+  void* out;
+  const SegDesc* segs;
+  const int* list;              // the segments of this launch, one per cluster
+  int P;                        // positions per CTA, onchip_positions(K)
+  int aligned;                  // every in/out pointer is 16-byte aligned
+  int* error;                   // device status word (bit 2: a bulk-copy wait gave up)
+  int* recomputed;              // segments recomputed in double-float
+  long long spin_budget;        // clock64 cycles of the bulk-copy wait
+  int inject_extra_tx;          // test hook: expect 16 bytes that never arrive
+};
+
+// Segments of at most kTinyDirect positions (adasum_onchip.cuh): one warp each, the
+// tree on the values themselves in double-float arithmetic.
+constexpr int kTinyDirect = 32;
+struct TinyArgs {
+  const void* in[kMaxK];  // K leaves (K a power of two); null = a zero gradient
+  void* out;
+  const SegDesc* segs;
+  const int* list;        // the segments, one per warp
+  int count;
+  int K;
+};
+
 // Launchers, one translation unit per input element type (compiled in parallel).
 // Each enqueues one kernel on `stream` and returns its cudaError_t as int (0 = ok);
 // `name` receives a static string naming the kernel, for the optional profiler.
@@ -156,6 +190,13 @@ int launch_pipeline(const StageArgs& a, const PipeArgs& p, int in_dtype, int out
 int pipeline_grid(int in_dtype, int out_dtype, int Kg, int momentum, int num_sms);
 // Partial-Gram chunk sums (segments with many tiles), then coefficients.
 int launch_reduce_chunks(const StageArgs& a, void* stream, const char** name);
+// Small-segment kernel: `count` clusters of C CTAs over a.list[0..count).
+int launch_onchip(const OnchipArgs& a, int dtype, int K, int count, int C, void* stream,
+                  const char** name);
+// Largest cluster size (1..16, a power of two) the small-segment kernel can run with.
+int onchip_max_cluster(int dtype, int K);
+// Tiny segments, one warp each.
+int launch_tiny_df(const TinyArgs& a, int dtype, void* stream, const char** name);
 // fp64 path: build the flagged lists, then Gram / coefficients / combine over them.
 int launch_collect(const StageArgs& a, int grid, void* stream, const char** name);
 // v = mu v + g for one worker (grad in `dtype`, state fp32).

@@ -372,6 +372,12 @@ __device__ __forceinline__ double block_lane_sum(double x, int W) {
   return x;
 }
 
+// Sum over the aligned block of W lanes (fp32 version, for the error estimate).
+__device__ __forceinline__ float block_lane_sumf(float x, int W) {
+  for (int off = W >> 1; off > 0; off >>= 1) x += __shfl_xor_sync(0xFFFFFFFFu, x, off);
+  return x;
+}
+
 // The Adasum tree of one segment in coefficient space, in fp64, evaluated by one warp:
 // lane k < KG owns leaf k (its coefficient c_k).  Every tree node u is
 // sum_{k in u} c_k g_k over W = 2^level consecutive leaves; pairing u = [a0, a0+W) with
@@ -389,7 +395,10 @@ __device__ __forceinline__ double block_lane_sum(double x, int W) {
 // rounds at each of the log2(K)+1 levels of its pairwise sum.  The estimate follows
 // every node's norm and cross term through the tree: when a node's norm is no larger
 // than its own error (cancellation), or the estimated relative error of the output
-// exceeds the budget, the segment is flagged for the fp64 recompute.
+// exceeds the budget, the segment is flagged for the fp64 recompute.  The estimate
+// needs a few significant digits only, so it runs in fp32 (GB300's fp64 pipe is narrow)
+// on quantities divided by the largest squared leaf norm, which keeps them far from
+// fp32's range limits.
 //
 // Called by all 32 lanes of one warp.  G and eps are in shared memory, c_sh is shared
 // scratch of KG doubles.  Returns (in every lane) the estimated relative output error
@@ -402,10 +411,14 @@ __device__ double coefficient_tree(const double (&G)[KG][KG], const double* eps,
   const int lane = threadIdx.x & 31;
   const bool on = lane < KG;
   const int row = on ? lane : 0;
-  const double s = on ? sqrt(fmax(G[row][row], 0.0)) : 0.0;
-  const double e = on ? eps[row] : 0.0;
+  double gmax = on ? fmax(G[row][row], 0.0) : 0.0;
+  for (int off = 16; off > 0; off >>= 1) gmax = fmax(gmax, __shfl_xor_sync(0xFFFFFFFFu, gmax, off));
+  const double inv = gmax > 0.0 ? 1.0 / gmax : 0.0;  // scale of the estimate
+  const float ge = static_cast<float>(gram_err);
+  const float s2 = on ? static_cast<float>(fmax(G[row][row], 0.0) * inv) : 0.f;  // |g_k|^2, scaled
+  const float e = on ? static_cast<float>(eps[row]) : 0.f;
   c = on ? 1.0 : 0.0;
-  double dc = 0.0;
+  float dc = 0.f;  // estimated error of c
   bool bad = false;
   if (on) c_sh[lane] = c;
   __syncwarp();
@@ -422,49 +435,213 @@ __device__ double coefficient_tree(const double (&G)[KG][KG], const double* eps,
     const double d_half = block_lane_sum(c * row_sib, W);
     const double d = d_half + __shfl_xor_sync(0xFFFFFFFFu, d_half, W);
     const double dd = 0.5 * d;  // the two halves each hold the full cross term
-    const double S_self = block_lane_sum(c * c * s * s, W);
-    const double D_self = sqrt(block_lane_sum((dc * dc + c * c * e * e) * s * s, W));
-    const double S_sib = __shfl_xor_sync(0xFFFFFFFFu, S_self, W);
-    const double D_sib = __shfl_xor_sync(0xFFFFFFFFu, D_self, W);
     const double p_sib = __shfl_xor_sync(0xFFFFFFFFu, p_self, W);
-    const double n_self = sqrt(fmax(p_self, 0.0)), n_sib = sqrt(fmax(p_sib, 0.0));
-    const double err_p = gram_err * S_self + 2.0 * n_self * D_self;
-    const double err_d = gram_err * sqrt(S_self * S_sib) + (n_self * D_sib + n_sib * D_self);
-    double coef = 1.0, dcoef = 0.0;
+    const float cf = static_cast<float>(c);
+    const float S_self = block_lane_sumf(cf * cf * s2, W);
+    const float D_self = sqrtf(block_lane_sumf((dc * dc + cf * cf * e * e) * s2, W));
+    const float S_sib = __shfl_xor_sync(0xFFFFFFFFu, S_self, W);
+    const float D_sib = __shfl_xor_sync(0xFFFFFFFFu, D_self, W);
+    const float ps = static_cast<float>(p_self * inv), pb = static_cast<float>(p_sib * inv);
+    const float n_self = sqrtf(fmaxf(ps, 0.f)), n_sib = sqrtf(fmaxf(pb, 0.f));
+    const float err_p = ge * S_self + 2.f * n_self * D_self;
+    const float err_d = ge * sqrtf(S_self * S_sib) + (n_self * D_sib + n_sib * D_self);
+    double coef = 1.0;
+    float dcoef = 0.f;
     if (p_self != 0.0) {
       coef = 1.0 - dd / (2.0 * p_self);
-      dcoef = (err_d + fabs(dd) * err_p / fabs(p_self)) / (2.0 * fabs(p_self));
-      if (p_self <= err_p) bad = true;
-    } else if (S_self > 0.0) {
+      const float ap = fabsf(ps), add = fabsf(static_cast<float>(dd * inv));
+      dcoef = (err_d + add * err_p / ap) / (2.f * ap);
+      if (ps <= err_p) bad = true;
+    } else if (S_self > 0.f) {
       bad = true;  // a non-zero subtree cancelled to an exact zero norm
     }
     if (on) {
-      dc = fma(fabs(coef), dc, fabs(c) * dcoef);
+      dc = fmaf(fabsf(static_cast<float>(coef)), dc, fabsf(cf) * dcoef);
       c *= coef;
     }
     __syncwarp();
     if (on) c_sh[lane] = c;
     __syncwarp();
   }
-  // output: norm^2 = c^T G c, and its error terms
   double full = 0.0;
   if (on)
     for (int j = 0; j < KG; ++j) full = fma(c_sh[j], G[row][j], full);
   const double P = block_lane_sum(c * full, 32);
-  const double S = block_lane_sum(c * c * s * s, 32);
-  const double D = sqrt(block_lane_sum((dc * dc + c * c * e * e) * s * s, 32));
+  const float cf = static_cast<float>(c);
+  const float S = block_lane_sumf(cf * cf * s2, 32);
+  const float D = sqrtf(block_lane_sumf((dc * dc + cf * cf * e * e) * s2, 32));
   ill = __any_sync(0xFFFFFFFFu, bad);
   if (P_out) *P_out = P;
-  if (S == 0.0) return 0.0;  // every leaf is zero: the output is exactly zero
+  if (S == 0.f) return 0.0;  // every leaf is zero: the output is exactly zero
   int levels = 1;
   for (int k = KG; k > 1; k >>= 1) ++levels;
-  const double err_P = gram_err * S + 2.0 * sqrt(fmax(P, 0.0)) * D;
-  if (P <= err_P) {
+  const float Pf = static_cast<float>(P * inv);
+  const float err_P = ge * S + 2.f * sqrtf(fmaxf(Pf, 0.f)) * D;
+  if (Pf <= err_P) {
     ill = true;
     return 1e30;
   }
-  const double rel = (D + levels * 5.9604644775390625e-08 * sqrt(S)) / sqrt(P);
-  return ill ? 1e30 : rel;
+  const float rel = (D + levels * 5.9604644775390625e-08f * sqrtf(S)) / sqrtf(Pf);
+  return ill ? 1e30 : static_cast<double>(rel);
+}
+
+// ----------------------------------------------- double-float arithmetic (tree core)
+//
+// A value hi + lo held in two fp32 numbers, |lo| <= ulp(hi)/2: about 48 significant
+// bits from fp32 instructions, which GB300 issues 64 times faster than fp64.  Built from
+// the error-free transformations TwoSum (Knuth) and TwoProduct (one FMA), composed as in
+// Dekker, "A floating-point technique for extending the available precision" (1971);
+// the add is the short ("sloppy") variant, whose error is a few 2^-48 of the operands.
+// Every operation is commutative bit for bit, which keeps the tree's sibling symmetry.
+struct df32 {
+  float hi, lo;
+};
+
+__device__ __forceinline__ df32 df_two_sum(float a, float b) {
+  const float s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  const float err = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+  return {s, err};
+}
+// requires |a| >= |b| (or a == 0)
+__device__ __forceinline__ df32 df_fast_two_sum(float a, float b) {
+  const float s = __fadd_rn(a, b);
+  return {s, __fsub_rn(b, __fsub_rn(s, a))};
+}
+__device__ __forceinline__ df32 df_add(df32 x, df32 y) {
+  const df32 s = df_two_sum(x.hi, y.hi);
+  return df_fast_two_sum(s.hi, __fadd_rn(s.lo, __fadd_rn(x.lo, y.lo)));
+}
+__device__ __forceinline__ df32 df_neg(df32 x) { return {-x.hi, -x.lo}; }
+__device__ __forceinline__ df32 df_mul(df32 x, df32 y) {
+  const float p = __fmul_rn(x.hi, y.hi);
+  const float e = __fmaf_rn(x.hi, y.hi, -p);  // exact error of the product
+  const float cross = __fadd_rn(__fmul_rn(x.hi, y.lo), __fmul_rn(x.lo, y.hi));
+  return df_fast_two_sum(p, __fadd_rn(e, cross));
+}
+// y * q for a single float q (TwoProduct plus the low part)
+__device__ __forceinline__ df32 df_mul_f(df32 y, float q) {
+  const float p = __fmul_rn(y.hi, q);
+  const float e = __fmaf_rn(y.hi, q, -p);
+  return df_fast_two_sum(p, __fmaf_rn(y.lo, q, e));
+}
+// x / y by long division with fp32 quotient digits (three digits: ~48 bits)
+__device__ __forceinline__ df32 df_div(df32 x, df32 y) {
+  const float q1 = __fdiv_rn(x.hi, y.hi);
+  df32 r = df_add(x, df_neg(df_mul_f(y, q1)));
+  const float q2 = __fdiv_rn(r.hi, y.hi);
+  r = df_add(r, df_neg(df_mul_f(y, q2)));
+  const float q3 = __fdiv_rn(r.hi, y.hi);
+  return df_add(df_fast_two_sum(q1, q2), df32{q3, 0.f});
+}
+__device__ __forceinline__ df32 df_from_double(double v) {
+  const float hi = static_cast<float>(v);
+  return {hi, static_cast<float>(v - static_cast<double>(hi))};
+}
+__device__ __forceinline__ double df_to_double(df32 x) {
+  return static_cast<double>(x.hi) + static_cast<double>(x.lo);
+}
+__device__ __forceinline__ df32 df_shfl_xor(df32 x, int off) {
+  return {__shfl_xor_sync(0xFFFFFFFFu, x.hi, off), __shfl_xor_sync(0xFFFFFFFFu, x.lo, off)};
+}
+// Sum over the aligned block of W lanes (butterfly, the same value in every lane).
+__device__ __forceinline__ df32 df_block_sum(df32 x, int W) {
+  for (int off = W >> 1; off > 0; off >>= 1) x = df_add(x, df_shfl_xor(x, off));
+  return x;
+}
+
+// coefficient_tree in double-float arithmetic: the same tree, the same d (sum of the
+// two halves), the same fp32 error estimate, with every fp64 operation of the tree core
+// replaced by its double-float counterpart.  G is the Gram matrix as double-float
+// values; the tree runs on G times a power of two that brings the largest squared leaf
+// norm into [0.5, 1) (exact, and harmless: the coefficients are scale-invariant), and
+// P_out (|out|^2) is scaled back.  Lane k < KG receives its coefficient in c_out (fp32,
+// the double-float value rounded once).
+template <int KG>
+__device__ double coefficient_tree_df(const df32 (&G)[KG][KG], const double* eps,
+                                      double gram_err, df32* c_sh, float& c_out, bool& ill,
+                                      double* P_out = nullptr) {
+  static_assert(KG <= 32, "one lane per leaf");
+  const int lane = threadIdx.x & 31;
+  const bool on = lane < KG;
+  const int row = on ? lane : 0;
+  float gmax = on ? fmaxf(G[row][row].hi, 0.f) : 0.f;
+  for (int off = 16; off > 0; off >>= 1) gmax = fmaxf(gmax, __shfl_xor_sync(0xFFFFFFFFu, gmax, off));
+  int ex = 0;
+  if (gmax > 0.f) frexpf(gmax, &ex);
+  ex = ex < -120 ? -120 : (ex > 120 ? 120 : ex);
+  const float sc = ldexpf(1.f, -ex);
+  auto g = [&](int i, int j) { return df32{G[i][j].hi * sc, G[i][j].lo * sc}; };
+  const float ge = static_cast<float>(gram_err);
+  const float s2 = on ? fmaxf(G[row][row].hi * sc, 0.f) : 0.f;  // |g_k|^2, scaled
+  const float e = on ? static_cast<float>(eps[row]) : 0.f;
+  df32 c = {on ? 1.f : 0.f, 0.f};
+  float dc = 0.f;  // estimated error of c
+  bool bad = false;
+  if (on) c_sh[lane] = c;
+  __syncwarp();
+  for (int W = 1; W < KG; W *= 2) {
+    const int self0 = (lane / W) * W, sib0 = self0 ^ W;
+    df32 row_self = {0.f, 0.f}, row_sib = {0.f, 0.f};
+    if (on) {
+      for (int j = 0; j < W; ++j) {
+        row_self = df_add(df_mul(c_sh[self0 + j], g(row, self0 + j)), row_self);
+        row_sib = df_add(df_mul(c_sh[sib0 + j], g(row, sib0 + j)), row_sib);
+      }
+    }
+    const df32 p_self = df_block_sum(df_mul(c, row_self), W);
+    const df32 d_half = df_block_sum(df_mul(c, row_sib), W);
+    const df32 d = df_add(d_half, df_shfl_xor(d_half, W));
+    const df32 dd = {0.5f * d.hi, 0.5f * d.lo};  // the two halves each hold the full cross term
+    const df32 p_sib = df_shfl_xor(p_self, W);
+    const float cf = c.hi;
+    const float S_self = block_lane_sumf(cf * cf * s2, W);
+    const float D_self = sqrtf(block_lane_sumf((dc * dc + cf * cf * e * e) * s2, W));
+    const float S_sib = __shfl_xor_sync(0xFFFFFFFFu, S_self, W);
+    const float D_sib = __shfl_xor_sync(0xFFFFFFFFu, D_self, W);
+    const float ps = p_self.hi, pb = p_sib.hi;
+    const float n_self = sqrtf(fmaxf(ps, 0.f)), n_sib = sqrtf(fmaxf(pb, 0.f));
+    const float err_p = ge * S_self + 2.f * n_self * D_self;
+    const float err_d = ge * sqrtf(S_self * S_sib) + (n_self * D_sib + n_sib * D_self);
+    df32 coef = {1.f, 0.f};
+    float dcoef = 0.f;
+    if (ps != 0.f) {
+      coef = df_add(df32{1.f, 0.f}, df_neg(df_div(dd, df32{2.f * p_self.hi, 2.f * p_self.lo})));
+      const float ap = fabsf(ps);
+      dcoef = (err_d + fabsf(dd.hi) * err_p / ap) / (2.f * ap);
+      if (ps <= err_p) bad = true;
+    } else if (S_self > 0.f) {
+      bad = true;  // a non-zero subtree cancelled to an exact zero norm
+    }
+    if (on) {
+      dc = fmaf(fabsf(coef.hi), dc, fabsf(cf) * dcoef);
+      c = df_mul(c, coef);
+    }
+    __syncwarp();
+    if (on) c_sh[lane] = c;
+    __syncwarp();
+  }
+  df32 full = {0.f, 0.f};
+  if (on)
+    for (int j = 0; j < KG; ++j) full = df_add(df_mul(c_sh[j], g(row, j)), full);
+  const df32 P = df_block_sum(df_mul(c, full), 32);
+  const float cf = c.hi;
+  const float S = block_lane_sumf(cf * cf * s2, 32);
+  const float D = sqrtf(block_lane_sumf((dc * dc + cf * cf * e * e) * s2, 32));
+  ill = __any_sync(0xFFFFFFFFu, bad);
+  c_out = __fadd_rn(c.hi, c.lo);
+  if (P_out) *P_out = ldexp(df_to_double(P), ex);
+  if (S == 0.f) return 0.0;  // every leaf is zero: the output is exactly zero
+  int levels = 1;
+  for (int k = KG; k > 1; k >>= 1) ++levels;
+  const float Pf = P.hi;
+  const float err_P = ge * S + 2.f * sqrtf(fmaxf(Pf, 0.f)) * D;
+  if (Pf <= err_P) {
+    ill = true;
+    return 1e30;
+  }
+  const float rel = (D + levels * 5.9604644775390625e-08f * sqrtf(S)) / sqrtf(Pf);
+  return ill ? 1e30 : static_cast<double>(rel);
 }
 
 // The linear recursion g[0,k] = Adasum(g[0,k-1], g_k), k = 1 .. kreal-1, in coefficient
@@ -553,8 +730,10 @@ __device__ __forceinline__ void segment_coefficients(const StageArgs& a, int seg
   constexpr int E = tri_count(KG);
   const SegDesc sd = a.segs[seg];
   __shared__ double G[KG][KG];
+  __shared__ df32 Gd[KG][KG];
   __shared__ double eps[KG];
   __shared__ double snorm[KG];
+  __shared__ df32 c_sh[KG];
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     double sum = 0.0;
     const double* p = a.chunk_sums + (static_cast<size_t>(q) * a.nchunks + sd.first_chunk) * E + e;
@@ -563,6 +742,7 @@ __device__ __forceinline__ void segment_coefficients(const StageArgs& a, int seg
     tri_unpack(KG, e, i, j);
     G[i][j] = sum;
     G[j][i] = sum;
+    Gd[i][j] = Gd[j][i] = df_from_double(sum);
   }
   for (int k = threadIdx.x; k < KG; k += blockDim.x)
     eps[k] = a.in_relerr ? static_cast<double>(a.in_relerr[static_cast<size_t>(q * KG + k) * a.nsegs + seg]) : 0.0;
@@ -570,9 +750,14 @@ __device__ __forceinline__ void segment_coefficients(const StageArgs& a, int seg
   if (threadIdx.x < 32) {
     double c = 0.0, P = 0.0;
     bool ill = false;
-    const double rel = a.mode == kModeChain
-                           ? coefficient_chain<KG>(G, eps, kGramRelErr, snorm, c, ill, a.Kreal, &P)
-                           : coefficient_tree<KG>(G, eps, kGramRelErr, snorm, c, ill, &P);
+    double rel;
+    if (a.mode == kModeChain) {
+      rel = coefficient_chain<KG>(G, eps, kGramRelErr, snorm, c, ill, a.Kreal, &P);
+    } else {
+      float cf = 0.f;
+      rel = coefficient_tree_df<KG>(Gd, eps, kGramRelErr, c_sh, cf, ill, &P);
+      c = cf;
+    }
     if (threadIdx.x == 0 && a.outnorm2) a.outnorm2[seg] = P;
     if (threadIdx.x == 0 && a.diag_sum) {
       double tr = 0.0;
@@ -591,7 +776,7 @@ __device__ __forceinline__ void segment_coefficients(const StageArgs& a, int seg
 
 template <int KG>
 __global__ void __launch_bounds__(128) coef_kernel(const StageArgs a) {
-  segment_coefficients<KG>(a, blockIdx.x, blockIdx.y);
+  segment_coefficients<KG>(a, a.seg_list ? a.seg_list[blockIdx.x] : static_cast<int>(blockIdx.x), blockIdx.y);
 }
 
 // ----------------------------------------------------------- pass 2: combine (+ step)

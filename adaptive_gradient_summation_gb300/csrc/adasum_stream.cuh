@@ -27,6 +27,7 @@
 #pragma once
 
 #include "adasum_kernels.cuh"
+#include "adasum_ptx.cuh"
 
 namespace adasum {
 
@@ -51,52 +52,6 @@ struct StreamArgs {
   int inject_no_ready;      // test hook: never publish
 };
 
-// ------------------------------------------------------------------ PTX wrappers
-
-__device__ __forceinline__ uint32_t smem_addr(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void mbar_init(uint64_t* bar, int count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_fence_init() {
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
-      : "=r"(ok)
-      : "r"(smem_addr(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// Bounded wait on an mbarrier phase; false (and the error word set) when the budget ran out.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, long long budget, int* error) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const long long t0 = clock64();
-  while (!mbar_try_wait(bar, parity)) {
-    if (clock64() - t0 > budget) {
-      atomicOr(error, 2);
-      return false;
-    }
-  }
-  return true;
-}
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_addr(dst)),
-      "l"(src), "r"(bytes), "r"(smem_addr(bar))
-      : "memory");
-}
 // Barrier among the consumer warps only (the producer warp never joins it).
 __device__ __forceinline__ void consumers_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
@@ -252,9 +207,9 @@ __device__ __forceinline__ void consume_gram_simt(const TileDesc& t, const char*
 template <int KG>
 __device__ __forceinline__ void finish_segment(const StageArgs& a, const StreamArgs& s, int seg) {
   constexpr int E = tri_count(KG);
-  __shared__ double G[KG][KG];
+  __shared__ df32 G[KG][KG];
   __shared__ double eps[KG];
-  __shared__ double snorm[KG];
+  __shared__ df32 snorm[KG];
   const int ct = threadIdx.x - 32, lane = threadIdx.x & 31, cw = (threadIdx.x >> 5) - 1;
   const SegDesc sd = a.segs[seg];
   const int nctas = static_cast<int>(gridDim.x);
@@ -279,16 +234,15 @@ __device__ __forceinline__ void finish_segment(const StageArgs& a, const StreamA
     if (lane == 0) {
       int i, jj;
       tri_unpack(KG, e, i, jj);
-      G[i][jj] = sum;
-      G[jj][i] = sum;
+      G[i][jj] = G[jj][i] = df_from_double(sum);
     }
   }
   for (int k = ct; k < KG; k += kConsumers) eps[k] = 0.0;
   consumers_sync();
   if (ct < 32) {
-    double c = 0.0;
+    float c = 0.f;
     bool ill = false;
-    const double rel = coefficient_tree<KG>(G, eps, kGramRelErr, snorm, c, ill);
+    const double rel = coefficient_tree_df<KG>(G, eps, kGramRelErr, snorm, c, ill);
     if (ct < KG) a.coef[static_cast<size_t>(seg) * KG + ct] = static_cast<float>(c);
     if (ct == 0) {
       if (a.relerr) a.relerr[seg] = static_cast<float>(fmin(rel, 1e30));

@@ -35,7 +35,7 @@ int launch_reduce_chunks(const StageArgs& a, void* stream, const char** name) {
 }
 
 int launch_coef(const StageArgs& a, void* stream, const char** name) {
-  const dim3 grid(a.nsegs, a.G), block(128);
+  const dim3 grid(a.seg_list ? a.nseg_list : a.nsegs, a.G), block(128);
   switch (a.Kg) {
     case 2: *name = "coef<2>"; return launch(coef_kernel<2>, grid, block, a, stream);
     case 4: *name = "coef<4>"; return launch(coef_kernel<4>, grid, block, a, stream);

@@ -1,0 +1,163 @@
+// launch_onchip.cu -- launchers of the small-segment kernels (adasum_onchip.cuh): the
+// on-chip kernel, one launch per cluster size (1..16 CTAs, set at launch time), and the
+// one-warp-per-segment kernel for tiny segments.
+#include <mutex>
+#include <string>
+
+#include "adasum_onchip.cuh"
+
+namespace adasum {
+
+namespace {
+
+template <typename Tag, int KG1, int NG>
+cudaError_t configure(int C) {
+  auto kern = onchip_kernel<Tag, KG1, NG>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       onchip_dynamic_smem(KG1 * NG));
+  if (e == cudaSuccess && C > 8) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  return e;
+}
+
+template <typename Tag, int KG1, int NG>
+cudaLaunchConfig_t make_config(int count, int C, cudaStream_t stream, cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(count) * static_cast<unsigned>(C));
+  cfg.blockDim = dim3(kOnchipThreads);
+  cfg.dynamicSmemBytes = onchip_dynamic_smem(KG1 * NG);
+  cfg.stream = stream;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(C);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
+template <typename Tag, int KG1, int NG>
+int launch_k(const OnchipArgs& a, int count, int C, void* stream) {
+  cudaError_t e = configure<Tag, KG1, NG>(C);
+  if (e != cudaSuccess) return static_cast<int>(e);
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = make_config<Tag, KG1, NG>(count, C, static_cast<cudaStream_t>(stream), attr);
+  return static_cast<int>(cudaLaunchKernelEx(&cfg, onchip_kernel<Tag, KG1, NG>, a));
+}
+
+// Clusters of C CTAs that fit on the device at once (0: this cluster size cannot run).
+template <typename Tag, int KG1, int NG>
+int active_clusters(int C) {
+  if (configure<Tag, KG1, NG>(C) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = make_config<Tag, KG1, NG>(C, C, nullptr, attr);
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, onchip_kernel<Tag, KG1, NG>, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
+// Profiler names: onchip<dtype,K,cC> (K as groups of 16 when above 16).
+const char* kernel_name(bool f32, int K, int C) {
+  static std::string names[2][7][5];
+  int ki = 0, ci = 0;
+  for (int k = 2; k < K; k *= 2) ++ki;
+  for (int c = 1; c < C; c *= 2) ++ci;
+  std::string& n = names[f32 ? 0 : 1][ki][ci];
+  if (n.empty()) {
+    const std::string ks = K > 16 ? "16x" + std::to_string(K / 16) : std::to_string(K);
+    n = std::string("onchip<") + (f32 ? "f32," : "bf16,") + ks + ",c" + std::to_string(C) + ">";
+  }
+  return n.c_str();
+}
+
+template <typename Tag>
+int dispatch(const OnchipArgs& a, int K, int count, int C, void* stream, const char** name) {
+  constexpr bool f32 = sizeof(typename ElemTraits<Tag>::Storage) == 4;
+  *name = kernel_name(f32, K, C);
+  switch (K) {
+    case 2: return launch_k<Tag, 2, 1>(a, count, C, stream);
+    case 4: return launch_k<Tag, 4, 1>(a, count, C, stream);
+    case 8: return launch_k<Tag, 8, 1>(a, count, C, stream);
+    case 16: return launch_k<Tag, 16, 1>(a, count, C, stream);
+    case 32: return launch_k<Tag, 16, 2>(a, count, C, stream);
+    case 64: return launch_k<Tag, 16, 4>(a, count, C, stream);
+    default: return static_cast<int>(cudaErrorInvalidValue);
+  }
+}
+
+template <typename Tag>
+int clusters_for(int K, int C) {
+  switch (K) {
+    case 2: return active_clusters<Tag, 2, 1>(C);
+    case 4: return active_clusters<Tag, 4, 1>(C);
+    case 8: return active_clusters<Tag, 8, 1>(C);
+    case 16: return active_clusters<Tag, 16, 1>(C);
+    case 32: return active_clusters<Tag, 16, 2>(C);
+    case 64: return active_clusters<Tag, 16, 4>(C);
+    default: return 0;
+  }
+}
+
+}  // namespace
+
+int onchip_max_cluster(int dtype, int K) {
+  // cached per (device, dtype, K): the answer depends only on the kernel and the device
+  static std::mutex mu;
+  static int cache[64][2][7];
+  static bool init = false;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return 1;
+  }
+  int kidx = 0;
+  for (int k = 2; k < K; k *= 2) ++kidx;
+  if (kidx > 5 || (dtype != kF32 && dtype != kBF16)) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!init) {
+    for (auto& d : cache)
+      for (auto& t : d)
+        for (int& v : t) v = -1;
+    init = true;
+  }
+  int& slot = cache[dev][dtype][kidx];
+  if (slot < 0) {
+    slot = 1;
+    for (int C = kOnchipMaxCluster; C >= 2; C /= 2) {
+      const int n = dtype == kF32 ? clusters_for<F32Tag>(K, C) : clusters_for<BF16Tag>(K, C);
+      if (n > 0) {
+        slot = C;
+        break;
+      }
+    }
+  }
+  return slot;
+}
+
+int launch_onchip(const OnchipArgs& a, int dtype, int K, int count, int C, void* stream,
+                  const char** name) {
+  if (count <= 0) return 0;
+  return dtype == kF32 ? dispatch<F32Tag>(a, K, count, C, stream, name)
+                       : dispatch<BF16Tag>(a, K, count, C, stream, name);
+}
+
+int launch_tiny_df(const TinyArgs& a, int dtype, void* stream, const char** name) {
+  if (a.count <= 0) return 0;
+  const dim3 grid((a.count + kOnchipWarps - 1) / kOnchipWarps), block(kOnchipThreads);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (dtype == kF32) {
+    *name = "tiny_df<f32>";
+    tiny_df_kernel<F32Tag><<<grid, block, 0, s>>>(a);
+  } else {
+    *name = "tiny_df<bf16>";
+    tiny_df_kernel<BF16Tag><<<grid, block, 0, s>>>(a);
+  }
+  return static_cast<int>(cudaGetLastError());
+}
+
+}  // namespace adasum
