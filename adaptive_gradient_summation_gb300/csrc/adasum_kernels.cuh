@@ -525,13 +525,16 @@ __device__ __forceinline__ df32 df_mul_f(df32 y, float q) {
   const float e = __fmaf_rn(y.hi, q, -p);
   return df_fast_two_sum(p, __fmaf_rn(y.lo, q, e));
 }
-// x / y by long division with fp32 quotient digits (three digits: ~48 bits)
+// x / y by long division with fp32 quotient digits (three digits: ~48 bits).  A digit
+// only has to be close: the exact remainder carries its error into the next digit, so
+// the digits use the fast approximate division (|y| well inside fp32's normal range,
+// which the callers' power-of-two scaling provides).
 __device__ __forceinline__ df32 df_div(df32 x, df32 y) {
-  const float q1 = __fdiv_rn(x.hi, y.hi);
+  const float q1 = __fdividef(x.hi, y.hi);
   df32 r = df_add(x, df_neg(df_mul_f(y, q1)));
-  const float q2 = __fdiv_rn(r.hi, y.hi);
+  const float q2 = __fdividef(r.hi, y.hi);
   r = df_add(r, df_neg(df_mul_f(y, q2)));
-  const float q3 = __fdiv_rn(r.hi, y.hi);
+  const float q3 = __fdividef(r.hi, y.hi);
   return df_add(df_fast_two_sum(q1, q2), df32{q3, 0.f});
 }
 __device__ __forceinline__ df32 df_from_double(double v) {
@@ -584,10 +587,19 @@ __device__ double coefficient_tree_df(const df32 (&G)[KG][KG], const double* eps
     const int self0 = (lane / W) * W, sib0 = self0 ^ W;
     df32 row_self = {0.f, 0.f}, row_sib = {0.f, 0.f};
     if (on) {
-      for (int j = 0; j < W; ++j) {
-        row_self = df_add(df_mul(c_sh[self0 + j], g(row, self0 + j)), row_self);
-        row_sib = df_add(df_mul(c_sh[sib0 + j], g(row, sib0 + j)), row_sib);
+      // even and odd terms in two chains (the same order relative to the block start
+      // for every block, which is what the sibling symmetry needs)
+      df32 se = {0.f, 0.f}, so = {0.f, 0.f}, be = {0.f, 0.f}, bo = {0.f, 0.f};
+      for (int j = 0; j < W; j += 2) {
+        se = df_add(df_mul(c_sh[self0 + j], g(row, self0 + j)), se);
+        be = df_add(df_mul(c_sh[sib0 + j], g(row, sib0 + j)), be);
+        if (j + 1 < W) {
+          so = df_add(df_mul(c_sh[self0 + j + 1], g(row, self0 + j + 1)), so);
+          bo = df_add(df_mul(c_sh[sib0 + j + 1], g(row, sib0 + j + 1)), bo);
+        }
       }
+      row_self = df_add(se, so);
+      row_sib = df_add(be, bo);
     }
     const df32 p_self = df_block_sum(df_mul(c, row_self), W);
     const df32 d_half = df_block_sum(df_mul(c, row_sib), W);
@@ -608,7 +620,7 @@ __device__ double coefficient_tree_df(const df32 (&G)[KG][KG], const double* eps
     if (ps != 0.f) {
       coef = df_add(df32{1.f, 0.f}, df_neg(df_div(dd, df32{2.f * p_self.hi, 2.f * p_self.lo})));
       const float ap = fabsf(ps);
-      dcoef = (err_d + fabsf(dd.hi) * err_p / ap) / (2.f * ap);
+      dcoef = __fdividef(err_d + __fdividef(fabsf(dd.hi) * err_p, ap), 2.f * ap);
       if (ps <= err_p) bad = true;
     } else if (S_self > 0.f) {
       bad = true;  // a non-zero subtree cancelled to an exact zero norm
@@ -622,8 +634,14 @@ __device__ double coefficient_tree_df(const df32 (&G)[KG][KG], const double* eps
     __syncwarp();
   }
   df32 full = {0.f, 0.f};
-  if (on)
-    for (int j = 0; j < KG; ++j) full = df_add(df_mul(c_sh[j], g(row, j)), full);
+  if (on) {
+    df32 fe = {0.f, 0.f}, fo = {0.f, 0.f};
+    for (int j = 0; j < KG; j += 2) {
+      fe = df_add(df_mul(c_sh[j], g(row, j)), fe);
+      if (j + 1 < KG) fo = df_add(df_mul(c_sh[j + 1], g(row, j + 1)), fo);
+    }
+    full = df_add(fe, fo);
+  }
   const df32 P = df_block_sum(df_mul(c, full), 32);
   const float cf = c.hi;
   const float S = block_lane_sumf(cf * cf * s2, 32);

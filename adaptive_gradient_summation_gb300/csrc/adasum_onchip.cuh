@@ -63,16 +63,25 @@ __device__ __forceinline__ float elem_f32(const S* x, int64_t p) {
   }
 }
 
-// Element g of an output array from a double-float value, rounded once (bf16 through
-// its exact fp64 sum, so that it too is rounded once).
+// Element g of an output array from a double-float value times 2^ex, rounded once
+// (bf16 through its exact fp64 sum, so that it too is rounded once).
 template <typename S>
-__device__ __forceinline__ void store_df(S* out, int64_t g, df32 y) {
+__device__ __forceinline__ void store_df(S* out, int64_t g, df32 y, int ex) {
   if constexpr (sizeof(S) == 4) {
-    out[g] = __fadd_rn(y.hi, y.lo);
+    out[g] = ldexpf(__fadd_rn(y.hi, y.lo), ex);
   } else {
-    __nv_bfloat16 h = __double2bfloat16(df_to_double(y));
+    __nv_bfloat16 h = __double2bfloat16(ldexp(df_to_double(y), ex));
     out[g] = *reinterpret_cast<uint16_t*>(&h);
   }
+}
+
+// Exponent e with amax * 2^-e in [0.5, 1) (0 for amax == 0), kept where 2^-e is a normal
+// fp32 number.  Scaling a segment's values by 2^-e is exact and the tree is
+// scale-invariant; it keeps the squares of the double-float paths inside fp32's range.
+__device__ __forceinline__ int scale_exponent(float amax) {
+  int ex = 0;
+  if (amax > 0.f) frexpf(amax, &ex);
+  return ex < -125 ? -125 : (ex > 125 ? 125 : ex);
 }
 
 // Entry e of every CTA's copy of buf (the cluster's partials after an exchange), summed
@@ -249,13 +258,13 @@ __global__ void __launch_bounds__(kOnchipThreads, 2) onchip_kernel(const OnchipA
       const int i = bi * B + ij / B, j = bj * B + ij % B;
       if (i <= j) xg[q * E1 + tri_index(KG1, i, j)] = __fsub_rn(sum, comp);
     }
-    cluster_sync_all();
+    cta_or_cluster_sync(C);
     // the Gram matrices of this CTA's groups: compensated sums over the cluster, CTA order
     for (int e = tid; e < NG * E1; e += kOnchipThreads) {
       const int q = e / E1;
       if (static_cast<uint32_t>(q) % C != rank) continue;
-      float sum, comp;
-      cluster_kahan_sum(xg, e, C, sum, comp);
+      float sum = xg[e], comp = 0.f;
+      if (C > 1) cluster_kahan_sum(xg, e, C, sum, comp);
       const df32 g = df_fast_two_sum(sum, -comp);  // the compensated sum, as a double-float
       int i, j;
       tri_unpack(KG1, e % E1, i, j);
@@ -339,8 +348,8 @@ __global__ void __launch_bounds__(kOnchipThreads, 2) onchip_kernel(const OnchipA
       ++xi;
       if (rank == 0) {  // the top tree: CTA 0 of the cluster
         if (tid < E2) {
-          float sum, comp;
-          cluster_kahan_sum(xg, tid, C, sum, comp);
+          float sum = xg[tid], comp = 0.f;
+          if (C > 1) cluster_kahan_sum(xg, tid, C, sum, comp);
           const df32 g = df_fast_two_sum(sum, -comp);
           int i, j;
           tri_unpack(NG, tid, i, j);
@@ -387,6 +396,23 @@ __global__ void __launch_bounds__(kOnchipThreads, 2) onchip_kernel(const OnchipA
     const int rsd = 2 * rs / 8;  // row stride in double-floats
     df32* rows = reinterpret_cast<df32*>(data);
     int stride = 1;              // rows between consecutive nodes (level >= 1)
+    // the segment's largest |value| over the cluster sets the power-of-two scale
+    float amax = 0.f;
+    for (int idx = tid; idx < K * nvec; idx += kOnchipThreads) {
+      const uint4 x = *reinterpret_cast<const uint4*>(data + (idx / nvec) * rs + (idx % nvec) * 16);
+#pragma unroll
+      for (int e = 0; e < VW; ++e) amax = fmaxf(amax, fabsf(vec_elem<InTag>(x, e)));
+    }
+    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
+    float* xm = reinterpret_cast<float*>(xch[xi & 1]);
+    if (lane == 0) xm[warp] = amax;
+    cta_or_cluster_sync(C);
+    amax = 0.f;
+    for (uint32_t r = 0; r < C; ++r)
+      for (int w = 0; w < kOnchipWarps; ++w) amax = fmaxf(amax, map_rank(xm, r)[w]);
+    ++xi;
+    const int ex = scale_exponent(amax);
+    const float sc = ldexpf(1.f, -ex);
     for (int m = K; m > 1; m /= 2) {
       const bool leaves = m == K;
       df32* xd = reinterpret_cast<df32*>(xch[xi & 1]);
@@ -400,7 +426,7 @@ __global__ void __launch_bounds__(kOnchipThreads, 2) onchip_kernel(const OnchipA
             const uint4 y = *reinterpret_cast<const uint4*>(rb + v * 16);
 #pragma unroll
             for (int e = 0; e < VW; ++e) {
-              const df32 xe = {vec_elem<InTag>(x, e), 0.f}, ye = {vec_elem<InTag>(y, e), 0.f};
+              const df32 xe = {vec_elem<InTag>(x, e) * sc, 0.f}, ye = {vec_elem<InTag>(y, e) * sc, 0.f};
               d = df_add(df_mul(xe, ye), d);
               pa = df_add(df_mul(xe, xe), pa);
               pb = df_add(df_mul(ye, ye), pb);
@@ -425,11 +451,11 @@ __global__ void __launch_bounds__(kOnchipThreads, 2) onchip_kernel(const OnchipA
           xd[3 * i + 2] = pb;
         }
       }
-      cluster_sync_all();
+      cta_or_cluster_sync(C);
       for (int i = tid; i < m / 2; i += kOnchipThreads) {
-        const df32 d = cluster_df_sum(xd, 3 * i, C);
-        const df32 pa = cluster_df_sum(xd, 3 * i + 1, C);
-        const df32 pb = cluster_df_sum(xd, 3 * i + 2, C);
+        const df32 d = C > 1 ? cluster_df_sum(xd, 3 * i, C) : xd[3 * i];
+        const df32 pa = C > 1 ? cluster_df_sum(xd, 3 * i + 1, C) : xd[3 * i + 1];
+        const df32 pb = C > 1 ? cluster_df_sum(xd, 3 * i + 2, C) : xd[3 * i + 2];
         const df32 one = {1.f, 0.f};
         ab[i][0] = pa.hi == 0.f ? one : df_add(one, df_neg(df_div(d, df32{2.f * pa.hi, 2.f * pa.lo})));
         ab[i][1] = pb.hi == 0.f ? one : df_add(one, df_neg(df_div(d, df32{2.f * pb.hi, 2.f * pb.lo})));
@@ -444,8 +470,8 @@ __global__ void __launch_bounds__(kOnchipThreads, 2) onchip_kernel(const OnchipA
           const bool in = g >= s0 && g < s1;
           const S* ga = static_cast<const S*>(a.in[2 * i]);
           const S* gb = static_cast<const S*>(a.in[2 * i + 1]);
-          const df32 xa = {(in && ga != nullptr) ? elem_f32(ga, g) : 0.f, 0.f};
-          const df32 xb = {(in && gb != nullptr) ? elem_f32(gb, g) : 0.f, 0.f};
+          const df32 xa = {(in && ga != nullptr) ? elem_f32(ga, g) * sc : 0.f, 0.f};
+          const df32 xb = {(in && gb != nullptr) ? elem_f32(gb, g) * sc : 0.f, 0.f};
           rows[static_cast<size_t>(i) * rsd + p] = df_add(df_mul(al, xa), df_mul(be, xb));
         } else {
           df32* ra = rows + static_cast<size_t>(2 * i) * stride * rsd;
@@ -459,10 +485,10 @@ __global__ void __launch_bounds__(kOnchipThreads, 2) onchip_kernel(const OnchipA
     for (int p = tid; p < npos; p += kOnchipThreads) {
       const int64_t g = p0 + p;
       if (g < s0 || g >= s1) continue;
-      store_df(out, g, rows[p]);
+      store_df(out, g, rows[p], ex);
     }
   }
-  cluster_sync_all();  // no CTA leaves while another may still read its shared memory
+  if (C > 1) cluster_sync_all();  // no CTA leaves while another may still read its shared memory
 }
 
 // ------------------------------------------------------------------ tiny segments
@@ -483,12 +509,20 @@ __global__ void __launch_bounds__(kOnchipThreads) tiny_df_kernel(const TinyArgs 
   const SegDesc sd = a.segs[a.list[w]];
   const int64_t p = sd.start + lane;
   const bool on = lane < sd.len;
+  float amax = 0.f;
+  for (int k = 0; k < a.K; ++k) {
+    const S* x = static_cast<const S*>(a.in[k]);
+    if (on && x != nullptr) amax = fmaxf(amax, fabsf(elem_f32(x, p)));
+  }
+  for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
+  const int ex = scale_exponent(amax);
+  const float sc = ldexpf(1.f, -ex);
   df32 val[kMaxDepth];
   int lvl[kMaxDepth];
   int top = 0;
   for (int k = 0; k < a.K; ++k) {
     const S* x = static_cast<const S*>(a.in[k]);
-    val[top] = {(on && x != nullptr) ? elem_f32(x, p) : 0.f, 0.f};
+    val[top] = {(on && x != nullptr) ? elem_f32(x, p) * sc : 0.f, 0.f};
     lvl[top] = 0;
     ++top;
     while (top >= 2 && lvl[top - 1] == lvl[top - 2]) {
@@ -504,7 +538,7 @@ __global__ void __launch_bounds__(kOnchipThreads) tiny_df_kernel(const TinyArgs 
       --top;
     }
   }
-  if (on) store_df(static_cast<S*>(a.out), p, val[0]);
+  if (on) store_df(static_cast<S*>(a.out), p, val[0], ex);
 }
 
 

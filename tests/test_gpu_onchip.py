@@ -194,3 +194,15 @@ def test_tiny_segments_pair_symmetry_and_special_cases(native):
     mask = (torch.arange(n, device=DEV) % 3 == 0)
     x, y = torch.where(mask, a, 0.0), torch.where(mask, 0.0, b)
     assert torch.equal(ags.reduce([x, y], offs), x + y)
+
+
+@pytest.mark.parametrize("scale", [1e-20, 1e15])
+def test_tiny_segments_extreme_magnitudes(native, scale):
+    """The warp kernel scales each segment by a power of two before squaring, so values
+    whose squares fall outside fp32's range still combine correctly."""
+    lengths = [1, 5, 17, 32]
+    offs = workloads.offsets_from_numels(lengths)
+    grads = [g * scale for g in rand_grads(8, int(offs[-1]), torch.float32, seed=797, corr=0.4)]
+    out = ags.reduce(grads, offs)
+    torch.cuda.synchronize()
+    check_against_oracle(grads, offs, out)
