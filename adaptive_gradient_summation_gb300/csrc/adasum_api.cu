@@ -649,15 +649,16 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
   }
   // Plain reductions: segments of at most kTinyDirect positions go to the warp kernel,
   // small ones (up to 64 workers) to the on-chip kernel, the rest to the tiles.
-  const bool plain = route == kRouteKernels && !mom && !chain && ortho == nullptr && K >= 2 &&
-                     env_on("ADASUM_ONCHIP", true);
+  // (ADASUM_TINY=0 and ADASUM_ONCHIP=0 switch the two kernels off, for comparisons.)
+  const bool plain = route == kRouteKernels && !mom && !chain && ortho == nullptr && K >= 2;
+  const bool tiny_on = plain && env_on("ADASUM_TINY", true);
   int onchip_K = 0, onchip_cmax = 0;
-  if (plain && K <= kOnchipMaxK) {
+  if (plain && K <= kOnchipMaxK && env_on("ADASUM_ONCHIP", true)) {
     onchip_cmax = std::min<int>(onchip_max_cluster(dtype, K), env_int("ADASUM_ONCHIP_MAX_CLUSTER", 16));
     if (onchip_cmax >= 1) onchip_K = K;
   }
   Plan* plan = nullptr;
-  if (adasum_status_t st = get_plan(ws, offs, L, kg[0], dtype, route, onchip_K, onchip_cmax, plain, &plan))
+  if (adasum_status_t st = get_plan(ws, offs, L, kg[0], dtype, route, onchip_K, onchip_cmax, tiny_on, &plan))
     return st;
 
   // Workspace layout.
@@ -674,8 +675,8 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
   Carver cv;
   // One zeroed int region per call: segment flags, the 3 fp64-list counters and the
   // small-segment kernel's recompute counter, and the fused kernel's task counter, chunk
-  // counters, segment counters and ready flags.
-  const size_t n_ints = static_cast<size_t>(L) + 4 + 1 + plan->nchunks + 2 * static_cast<size_t>(L);
+  // counters, segment counters and ready flags, and the recompute's segment scales.
+  const size_t n_ints = static_cast<size_t>(L) + 4 + 1 + plan->nchunks + 3 * static_cast<size_t>(L);
   const size_t o_flags = cv.take(n_ints * sizeof(int));
   const size_t o_part = cv.take(max_e_tiles * sizeof(float));
   const size_t o_chunk = cv.take(max_e_chunks * sizeof(double));
@@ -709,6 +710,7 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
   int* chunk_done = task_counter + 1;
   int* seg_done = chunk_done + plan->nchunks;
   int* seg_ready = seg_done + L;
+  int* seg_exp = seg_ready + L;  // the fp64 recompute's per-segment scale
   if (ws.d_error == nullptr) {
     if (cudaMalloc(&ws.d_error, sizeof(int)) != cudaSuccess ||
         cudaMemset(ws.d_error, 0, sizeof(int)) != cudaSuccess) {
@@ -748,6 +750,7 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
     a.list_tiny = reinterpret_cast<int*>(base + o_ltiny);
     a.list_count = list_count;
     a.Ktotal = chain ? Kreal : K;
+    a.seg_exp = seg_exp;
     a.seg_list = plan->d_coef_list;
     a.nseg_list = plan->ncoef;
     a.mode = chain ? kModeChain : kModeTree;
@@ -881,12 +884,23 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
   }
 
   // fp64 recompute of the flagged segments (usually none: every kernel returns at once).
-  const int grid64 = std::max(1, std::min(plan->ntiles, 2 * num_sms));
+  // (the lists' lengths are on the device: enough CTAs for many flagged tiles, the
+  // surplus returns at once)
+  const int grid64 = std::max(1, std::min(plan->ntiles, 16 * num_sms));
   {
     StageArgs a = make_args(0);
     if (adasum_status_t st = launch_one(stream, [&](const char** n) {
           return launch_collect(a, std::max(1, std::min((L + kThreads - 1) / kThreads, 4 * num_sms)),
                                 stream, n);
+        }))
+      return st;
+  }
+  {
+    // the scale of every flagged segment's Gram (from the stage-0 inputs)
+    StageArgs a = make_args(0);
+    for (int k = 0; k < K; ++k) a.in[k] = grads[k];
+    if (adasum_status_t st = launch_one(stream, [&](const char** n) {
+          return launch_segmax(a, dtype, grid64, stream, n);
         }))
       return st;
   }

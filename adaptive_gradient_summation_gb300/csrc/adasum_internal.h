@@ -87,6 +87,7 @@ struct StageArgs {
   int* list_segs;             // flagged segments, list_count[1] of them
   int* list_tiny;             // flagged segments of at most kTinySeg positions, list_count[2]
   int* list_count;            // [3]
+  int* seg_exp;               // [nsegs] 1024 + exponent of the segment's largest |input| (0: all zero)
   int Ktotal;                 // all workers (the tiny-segment recompute runs the whole tree)
   int in_f64;                 // stage inputs are fp64 intermediates
   int out_f64;                // stage outputs are fp64 intermediates
@@ -207,6 +208,7 @@ int launch_orthogonality(const double* outnorm2, const double* diag_sum, int gro
                          float* ortho, void* stream, const char** name);
 int launch_tiny64(const StageArgs& a, int in_dtype, int out_dtype, int momentum, int grid,
                   void* stream, const char** name);
+int launch_segmax(const StageArgs& a, int in_dtype, int grid, void* stream, const char** name);
 int launch_gram64(const StageArgs& a, int in_dtype, int grid, void* stream, const char** name);
 int launch_coef64(const StageArgs& a, int grid, void* stream, const char** name);
 int launch_combine64(const StageArgs& a, int in_dtype, int out_dtype, int momentum, int grid,

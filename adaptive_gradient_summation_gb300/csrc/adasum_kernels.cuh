@@ -1150,13 +1150,48 @@ __global__ void __launch_bounds__(kThreads) tiny64_kernel(const StageArgs a) {
   }
 }
 
-// fp64 Gram of every flagged tile: the tile is staged through shared memory 64
-// positions at a time; thread e owns Gram entry e.
+// The largest |input| of every flagged segment, as 1024 + its binary exponent (atomic
+// max over the segment's tiles; 0 stays for an all-zero segment).  The recompute's Gram
+// scales its segment by the matching power of two.
+template <int IN>
+__global__ void __launch_bounds__(kThreads) segmax_kernel(const StageArgs a) {
+  __shared__ float wmax[kWarps];
+  const int count = a.list_count[0];
+  const int K = a.G * a.Kg;
+  for (int li = blockIdx.x; li < count; li += gridDim.x) {
+    const TileDesc t = a.tiles[a.list_tiles[li]];
+    float m = 0.f;
+    for (int k = 0; k < K; ++k) {
+      if (a.in[k] == nullptr) continue;
+      for (int p = threadIdx.x; p < t.len; p += kThreads)
+        m = fmaxf(m, fabsf(static_cast<float>(load_f64<IN>(a.in[k], t.start + p))));
+    }
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
+    if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float mm = 0.f;
+      for (int w = 0; w < kWarps; ++w) mm = fmaxf(mm, wmax[w]);
+      if (mm > 0.f) {
+        int ex = 0;
+        frexpf(mm, &ex);
+        atomicMax(a.seg_exp + t.seg, 1024 + ex);
+      }
+    }
+    __syncthreads();
+  }
+}
+
+// Gram matrix of every flagged tile, in double-float arithmetic: fp32 and bf16 inputs
+// are exact fp32 numbers, so every product is exact (TwoProduct) and only the sums round,
+// at about 2^-48.  The tile is staged through shared memory 64 positions at a time,
+// scaled by the segment's power of two (exact) so that the squares stay inside fp32's
+// range; thread e owns Gram entry e.  The partial is scaled back and stored in fp64.
 template <int IN, int KG>
 __global__ void __launch_bounds__(kThreads) gram64_kernel(const StageArgs a) {
   constexpr int E = tri_count(KG);
   constexpr int P = 64;
-  __shared__ double xs[KG][P];
+  __shared__ df32 xs[KG][P];
   const int q = blockIdx.y;
   const int count = a.list_count[0];
   int ei = 0, ej = 0;
@@ -1164,21 +1199,31 @@ __global__ void __launch_bounds__(kThreads) gram64_kernel(const StageArgs a) {
   for (int li = blockIdx.x; li < count; li += gridDim.x) {
     const int tile_id = a.list_tiles[li];
     const TileDesc t = a.tiles[tile_id];
-    double acc = 0.0;
+    const int enc = a.seg_exp[t.seg];
+    int ex = enc > 0 ? enc - 1024 : 0;
+    ex = ex < -125 ? -125 : (ex > 125 ? 125 : ex);
+    df32 se = {0.f, 0.f}, so = {0.f, 0.f};
     for (int64_t p0 = t.start; p0 < t.start + t.len; p0 += P) {
       const int64_t left = t.start + t.len - p0;
       const int np = left < P ? static_cast<int>(left) : P;
       __syncthreads();
       for (int idx = threadIdx.x; idx < KG * P; idx += kThreads) {
         const int k = idx / P, p = idx % P;
-        xs[k][p] = p < np ? load_f64<IN>(a.in[q * KG + k], p0 + p) : 0.0;
+        const double v = p < np ? ldexp(load_f64<IN>(a.in[q * KG + k], p0 + p), -ex) : 0.0;
+        xs[k][p] = IN == kKindF64 ? df_from_double(v) : df32{static_cast<float>(v), 0.f};
       }
       __syncthreads();
-      if (threadIdx.x < E)
-        for (int p = 0; p < np; ++p) acc = fma(xs[ei][p], xs[ej][p], acc);
+      if (threadIdx.x < E) {
+        for (int p = 0; p + 1 < np; p += 2) {
+          se = df_add(df_mul(xs[ei][p], xs[ej][p]), se);
+          so = df_add(df_mul(xs[ei][p + 1], xs[ej][p + 1]), so);
+        }
+        if (np & 1) se = df_add(df_mul(xs[ei][np - 1], xs[ej][np - 1]), se);
+      }
     }
     if (threadIdx.x < E)
-      a.partials64[(static_cast<size_t>(q) * a.ntiles + tile_id) * E + threadIdx.x] = acc;
+      a.partials64[(static_cast<size_t>(q) * a.ntiles + tile_id) * E + threadIdx.x] =
+          ldexp(df_to_double(df_add(se, so)), 2 * ex);
     __syncthreads();
   }
 }

@@ -80,6 +80,14 @@ int launch_tiny64(const StageArgs& a, int in_dtype, int out_dtype, int momentum,
             : launch(tiny64_kernel<kKindF32, kKindF32, false>, g, b, a, stream);
 }
 
+int launch_segmax(const StageArgs& a, int in_dtype, int grid, void* stream, const char** name) {
+  *name = "segmax";
+  switch (kind_of(in_dtype, 0)) {
+    case kKindF32: return launch(segmax_kernel<kKindF32>, dim3(grid), dim3(kThreads), a, stream);
+    default: return launch(segmax_kernel<kKindBF16>, dim3(grid), dim3(kThreads), a, stream);
+  }
+}
+
 int launch_gram64(const StageArgs& a, int in_dtype, int grid, void* stream, const char** name) {
   const dim3 g(grid, a.G);
   switch (kind_of(in_dtype, a.in_f64)) {

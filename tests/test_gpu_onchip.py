@@ -96,6 +96,7 @@ def test_mixed_with_tiled_segments(native, monkeypatch, K):
     ref = oracle_reduce(grads, offs)
     check_against_oracle(grads, offs, on, ref=ref)
     monkeypatch.setenv("ADASUM_ONCHIP", "0")
+    monkeypatch.setenv("ADASUM_TINY", "0")
     off = ags.reduce(grads, offs)
     torch.cuda.synchronize()
     check_against_oracle(grads, offs, off, ref=ref)

@@ -366,6 +366,7 @@ def test_routes_agree(native, monkeypatch):
     differently, so those are switched off for the comparison.)"""
     wl = workloads.make("bert_large_k16", device=DEV, shrink=128)
     monkeypatch.setenv("ADASUM_ONCHIP", "0")
+    monkeypatch.setenv("ADASUM_TINY", "0")
     split = ags.reduce(wl.grads, wl.seg_offsets).clone()
     monkeypatch.setenv("ADASUM_ROUTE", "fused")
     monkeypatch.setenv("ADASUM_PIPE_TILE_KB", "256")   # same tiles, so the same sums
