@@ -115,6 +115,7 @@ struct Plan {
   // then runs over the list of the remaining (tiled) segments.
   int onchip_K = 0;  // padded worker count the grouping was made for (0: none)
   int onchip_cmax = 0;
+  bool onchip_force = false;
   int onchip_count[5] = {0, 0, 0, 0, 0};
   int onchip_first[5] = {0, 0, 0, 0, 0};
   int* d_onchip = nullptr;
@@ -123,6 +124,14 @@ struct Plan {
   int* d_tiny = nullptr;
   int ncoef = 0;
   int* d_coef_list = nullptr;
+  // three-kernel route: tiles of at most kSmallTile positions take the warp Gram kernel
+  // (lists empty when there are none)
+  int nbig = 0, nsmall = 0;
+  int* d_big = nullptr;
+  int* d_small = nullptr;
+  // tiled segments the on-chip kernel could recompute if flagged, per cluster size
+  int rc_cmax = 0;
+  int rc_count[5] = {0, 0, 0, 0, 0};
 };
 
 struct Workspace {
@@ -154,6 +163,10 @@ void free_plan(Plan& p) {
   if (p.d_onchip) cudaFree(p.d_onchip);
   if (p.d_tiny) cudaFree(p.d_tiny);
   if (p.d_coef_list) cudaFree(p.d_coef_list);
+  if (p.d_big) cudaFree(p.d_big);
+  if (p.d_small) cudaFree(p.d_small);
+  p.d_big = nullptr;
+  p.d_small = nullptr;
   p.d_onchip = nullptr;
   p.d_tiny = nullptr;
   p.d_coef_list = nullptr;
@@ -320,11 +333,13 @@ adasum_status_t upload(T** dst, const std::vector<T>& v) {
 }
 
 adasum_status_t get_plan(Workspace& ws, const int64_t* offs, int L, int Kg0, int dtype, int route,
-                         int onchip_K, int onchip_cmax, bool tiny_on, Plan** out) {
+                         int onchip_K, int onchip_cmax, bool onchip_force, int rc_cmax, bool tiny_on,
+                         Plan** out) {
   const int64_t wave = route == kRouteStream ? env_int("ADASUM_WAVE_MB", 24) << 20 : wave_budget_bytes();
   for (auto it = ws.plans.begin(); it != ws.plans.end(); ++it) {
     if (it->Kg0 == Kg0 && it->dtype == dtype && it->route == route && it->onchip_K == onchip_K &&
-        it->onchip_cmax == onchip_cmax && it->tiny_on == tiny_on &&
+        it->onchip_cmax == onchip_cmax && it->onchip_force == onchip_force && it->rc_cmax == rc_cmax &&
+        it->tiny_on == tiny_on &&
         (route == kRouteKernels ||
          (it->wave_bytes == wave && it->tile_kb == (tile_bytes(true) >> 10) &&
           it->delay_pct == env_int("ADASUM_PIPE_DELAY_PCT", 100) &&
@@ -349,8 +364,21 @@ adasum_status_t get_plan(Workspace& ws, const int64_t* offs, int L, int Kg0, int
   std::vector<SegDesc> segs(L);
   std::vector<ChunkDesc> chunks;
   std::vector<int> onchip[5], tiny;
+  int rc_count[5] = {0, 0, 0, 0, 0};
   const int64_t VW = dtype == kF32 ? 4 : 8;
-  const int64_t onchip_vecs = onchip_K > 0 ? onchip_positions(onchip_K) / VW : 0;
+  int64_t onchip_vecs = onchip_K > 0 ? onchip_positions(onchip_K) / VW : 0;
+  if (onchip_vecs > 0) {
+    // The on-chip kernel pays off when small segments are numerous enough to fill the
+    // GPU by themselves (each CTA is latency-bound and takes half an SM); a few small
+    // segments ride along in the tiled passes at no measurable cost.
+    int64_t eligible = 0;
+    for (int s = 0; s < L; ++s) {
+      const int64_t lo = offs[s], hi = offs[s + 1];
+      const int64_t nv = (hi + VW - 1) / VW - lo / VW;
+      if (hi - lo > (tiny_on ? kTinyDirect : 0) && (nv + onchip_cmax - 1) / onchip_cmax <= onchip_vecs) ++eligible;
+    }
+    if (!onchip_force && eligible < 4 * static_cast<int64_t>(num_sms)) onchip_vecs = 0;
+  }
   for (int s = 0; s < L; ++s) {
     const int64_t lo = offs[s], hi = offs[s + 1];
     segs[s].start = lo;
@@ -371,6 +399,15 @@ adasum_status_t get_plan(Workspace& ws, const int64_t* offs, int L, int Kg0, int
           break;
         }
       }
+    }
+    if (hi > lo && !small && rc_cmax > 0) {
+      const int64_t nv = (hi + VW - 1) / VW - lo / VW;
+      const int64_t rc_vecs = onchip_positions(onchip_K) / VW;
+      for (int c = 0, C = 1; C <= rc_cmax && c < 5; ++c, C *= 2)
+        if ((nv + C - 1) / C <= rc_vecs) {
+          ++rc_count[c];
+          break;
+        }
     }
     if (hi > lo && !small) {
       const int64_t base = lo / 32 * 32;
@@ -404,6 +441,9 @@ adasum_status_t get_plan(Workspace& ws, const int64_t* offs, int L, int Kg0, int
   p.delay_pct = env_int("ADASUM_PIPE_DELAY_PCT", 100);
   p.onchip_K = onchip_K;
   p.onchip_cmax = onchip_cmax;
+  p.onchip_force = onchip_force;
+  p.rc_cmax = rc_cmax;
+  for (int c = 0; c < 5; ++c) p.rc_count[c] = rc_count[c];
   p.tiny_on = tiny_on;
   p.tiny_count = static_cast<int>(tiny.size());
   std::vector<int> onchip_all, coef_list;
@@ -417,7 +457,17 @@ adasum_status_t get_plan(Workspace& ws, const int64_t* offs, int L, int Kg0, int
     for (int s = 0; s < L; ++s)
       if (segs[s].ntiles > 0) coef_list.push_back(s);
   p.ncoef = static_cast<int>(coef_list.size());
+  std::vector<int> big, small_tiles;
+  if (route == kRouteKernels) {
+    for (int t = 0; t < static_cast<int>(tiles.size()); ++t)
+      (tiles[t].len <= kSmallTile ? small_tiles : big).push_back(t);
+    if (small_tiles.empty()) big.clear();
+  }
+  p.nbig = static_cast<int>(big.size());
+  p.nsmall = static_cast<int>(small_tiles.size());
   adasum_status_t st = upload(&p.d_tiles, tiles);
+  if (!st && p.nsmall > 0) st = upload(&p.d_big, big);
+  if (!st && p.nsmall > 0) st = upload(&p.d_small, small_tiles);
   if (!st && !onchip_all.empty()) st = upload(&p.d_onchip, onchip_all);
   if (!st && !tiny.empty()) st = upload(&p.d_tiny, tiny);
   if (!st && any_small) st = upload(&p.d_coef_list, coef_list);
@@ -525,10 +575,18 @@ adasum_status_t run_stage(StageArgs& a, int in_dtype, int out_dtype, int momentu
                           cudaStream_t stream) {
   if (a.ntiles == 0) return ADASUM_OK;  // every segment went to the small-segment kernels
   if (a.Kg > 1) {
-    if (adasum_status_t st = launch_one(stream, [&](const char** n) {
-          return in_dtype == kBF16 ? launch_gram_bf16(a, stream, n) : launch_gram_f32(a, stream, n);
-        }))
-      return st;
+    if (a.tile_list == nullptr || a.ntile_list > 0) {
+      if (adasum_status_t st = launch_one(stream, [&](const char** n) {
+            return in_dtype == kBF16 ? launch_gram_bf16(a, stream, n) : launch_gram_f32(a, stream, n);
+          }))
+        return st;
+    }
+    if (a.nsmall > 0) {
+      if (adasum_status_t st = launch_one(stream, [&](const char** n) {
+            return launch_gram_warp(a, in_dtype, stream, n);
+          }))
+        return st;
+    }
     if (adasum_status_t st = launch_one(stream, [&](const char** n) {
           return launch_reduce_chunks(a, stream, n);
         }))
@@ -649,16 +707,24 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
   }
   // Plain reductions: segments of at most kTinyDirect positions go to the warp kernel,
   // small ones (up to 64 workers) to the on-chip kernel, the rest to the tiles.
-  // (ADASUM_TINY=0 and ADASUM_ONCHIP=0 switch the two kernels off, for comparisons.)
+  // (ADASUM_TINY=0 and ADASUM_ONCHIP=0 switch the two kernels off, for comparisons;
+  // ADASUM_ONCHIP=force uses the on-chip kernel for every small segment, for tests.)
   const bool plain = route == kRouteKernels && !mom && !chain && ortho == nullptr && K >= 2;
   const bool tiny_on = plain && env_on("ADASUM_TINY", true);
   int onchip_K = 0, onchip_cmax = 0;
+  const char* onchip_env = std::getenv("ADASUM_ONCHIP");
+  const bool onchip_force = onchip_env != nullptr && std::strcmp(onchip_env, "force") == 0;
   if (plain && K <= kOnchipMaxK && env_on("ADASUM_ONCHIP", true)) {
-    onchip_cmax = std::min<int>(onchip_max_cluster(dtype, K), env_int("ADASUM_ONCHIP_MAX_CLUSTER", 16));
+    // clusters of up to 2 CTAs by default: larger clusters measured slower than the
+    // tiled route for the segments they add (ADASUM_ONCHIP_MAX_CLUSTER: up to 16)
+    onchip_cmax = std::min<int>(onchip_max_cluster(dtype, K), env_int("ADASUM_ONCHIP_MAX_CLUSTER", 2));
     if (onchip_cmax >= 1) onchip_K = K;
   }
+  // flagged tiled segments that fit are recomputed by the on-chip kernel
+  const int rc_cmax = (plain && K <= kOnchipMaxK && env_on("ADASUM_ONCHIP", true)) ? onchip_max_cluster(dtype, K) : 0;
   Plan* plan = nullptr;
-  if (adasum_status_t st = get_plan(ws, offs, L, kg[0], dtype, route, onchip_K, onchip_cmax, tiny_on, &plan))
+  if (adasum_status_t st = get_plan(ws, offs, L, kg[0], dtype, route, rc_cmax > 0 ? K : onchip_K, onchip_cmax,
+                                    onchip_force, rc_cmax, tiny_on, &plan))
     return st;
 
   // Workspace layout.
@@ -676,7 +742,7 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
   // One zeroed int region per call: segment flags, the 3 fp64-list counters and the
   // small-segment kernel's recompute counter, and the fused kernel's task counter, chunk
   // counters, segment counters and ready flags, and the recompute's segment scales.
-  const size_t n_ints = static_cast<size_t>(L) + 4 + 1 + plan->nchunks + 3 * static_cast<size_t>(L);
+  const size_t n_ints = static_cast<size_t>(L) + 4 + 1 + plan->nchunks + 3 * static_cast<size_t>(L) + 5;
   const size_t o_flags = cv.take(n_ints * sizeof(int));
   const size_t o_part = cv.take(max_e_tiles * sizeof(float));
   const size_t o_chunk = cv.take(max_e_chunks * sizeof(double));
@@ -688,6 +754,7 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
   const size_t o_ltiles = cv.take(static_cast<size_t>(plan->ntiles) * sizeof(int));
   const size_t o_lsegs = cv.take(static_cast<size_t>(L) * sizeof(int));
   const size_t o_ltiny = cv.take(static_cast<size_t>(L) * sizeof(int));
+  const size_t o_oclist = cv.take(plan->rc_cmax > 0 ? 5 * static_cast<size_t>(L) * sizeof(int) : 0);
   const size_t o_onorm = cv.take(ortho ? static_cast<size_t>(L) * sizeof(double) : 0);
   const size_t o_diag = cv.take(ortho ? static_cast<size_t>(groups[0]) * L * sizeof(double) : 0);
   const size_t o_slots = cv.take(route == kRouteStream
@@ -711,6 +778,7 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
   int* seg_done = chunk_done + plan->nchunks;
   int* seg_ready = seg_done + L;
   int* seg_exp = seg_ready + L;  // the fp64 recompute's per-segment scale
+  int* oc_count = seg_exp + L;   // flagged segments listed for the on-chip recompute
   if (ws.d_error == nullptr) {
     if (cudaMalloc(&ws.d_error, sizeof(int)) != cudaSuccess ||
         cudaMemset(ws.d_error, 0, sizeof(int)) != cudaSuccess) {
@@ -751,8 +819,21 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
     a.list_count = list_count;
     a.Ktotal = chain ? Kreal : K;
     a.seg_exp = seg_exp;
+    if (plan->rc_cmax > 0) {
+      a.oc_vecs = onchip_positions(K) / (dtype == kF32 ? 4 : 8);
+      a.oc_vw = dtype == kF32 ? 4 : 8;
+      a.oc_cmax = plan->rc_cmax;
+      a.oc_list = reinterpret_cast<int*>(base + o_oclist);
+      a.oc_count = oc_count;
+    }
     a.seg_list = plan->d_coef_list;
     a.nseg_list = plan->ncoef;
+    if (plan->nsmall > 0) {
+      a.tile_list = plan->d_big;
+      a.ntile_list = plan->nbig;
+      a.small_list = plan->d_small;
+      a.nsmall = plan->nsmall;
+    }
     a.mode = chain ? kModeChain : kModeTree;
     a.Kreal = Kreal;
     const bool last = s + 1 == kg.size();
@@ -892,6 +973,28 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
     if (adasum_status_t st = launch_one(stream, [&](const char** n) {
           return launch_collect(a, std::max(1, std::min((L + kThreads - 1) / kThreads, 4 * num_sms)),
                                 stream, n);
+        }))
+      return st;
+  }
+  // flagged segments that fit: the on-chip kernel's recompute, one launch per cluster size
+  // (the lists' lengths are on the device; surplus clusters return at once)
+  for (int c = 0; c < 5 && plan->rc_cmax > 0; ++c) {
+    if (plan->rc_count[c] == 0) continue;
+    OnchipArgs oa;
+    std::memset(&oa, 0, sizeof oa);
+    for (int k = 0; k < K; ++k) oa.in[k] = grads[k];
+    oa.out = out;
+    oa.segs = plan->d_segs;
+    oa.P = onchip_positions(K);
+    oa.aligned = all_aligned ? 1 : 0;
+    oa.error = ws.d_error;
+    oa.recomputed = list_count + 3;
+    oa.spin_budget = 2000000000LL;
+    oa.list = reinterpret_cast<int*>(base + o_oclist) + static_cast<size_t>(c) * L;
+    oa.dev_count = oc_count + c;
+    oa.recompute_only = 1;
+    if (adasum_status_t st = launch_one(stream, [&](const char** n) {
+          return launch_onchip(oa, dtype, K, plan->rc_count[c], 1 << c, stream, n);
         }))
       return st;
   }

@@ -48,6 +48,8 @@ struct ChunkDesc {
   int32_t ntiles;
 };
 constexpr int kChunkTiles = 32;
+// Tiles of at most this many positions get their Gram partial from one warp.
+constexpr int kSmallTile = 1024;
 
 // Arguments of one stage: G independent groups of Kg workers each, over the same
 // segments and tiles.  Group q reads in[q*Kg + k], k < Kg, and writes out[q].
@@ -79,6 +81,10 @@ struct StageArgs {
   int skip_flagged;           // combine: leave flagged segments to the fp64 path
   const int* seg_list;        // coef: the segments to run (null: all nsegs)
   int nseg_list;
+  const int* tile_list;       // Gram CTA kernels: the tiles to run (null: all ntiles)
+  int ntile_list;
+  const int* small_list;      // small tiles, one warp each (gram_warp_kernel)
+  int nsmall;
 
   // fp64 path (only the segments listed by collect_kernel).
   double* partials64;         // [G][ntiles][E]
@@ -88,6 +94,13 @@ struct StageArgs {
   int* list_tiny;             // flagged segments of at most kTinySeg positions, list_count[2]
   int* list_count;            // [3]
   int* seg_exp;               // [nsegs] 1024 + exponent of the segment's largest |input| (0: all zero)
+  // Flagged segments that fit the on-chip kernel (plain reductions of up to 64 workers)
+  // are listed per cluster size for its recompute instead of the fp64 path.
+  int oc_vecs;                // 16-byte vectors per CTA (0: none go there)
+  int oc_vw;                  // elements per 16-byte vector
+  int oc_cmax;                // largest cluster
+  int* oc_list;               // [5][nsegs]
+  int* oc_count;              // [5]
   int Ktotal;                 // all workers (the tiny-segment recompute runs the whole tree)
   int in_f64;                 // stage inputs are fp64 intermediates
   int out_f64;                // stage outputs are fp64 intermediates
@@ -154,6 +167,8 @@ struct OnchipArgs {
   int* recomputed;              // segments recomputed in double-float
   long long spin_budget;        // clock64 cycles of the bulk-copy wait
   int inject_extra_tx;          // test hook: expect 16 bytes that never arrive
+  const int* dev_count;         // when set: clusters at or past *dev_count return at once
+  int recompute_only;           // skip the fp32 pass (segments the fp32 pass flagged)
 };
 
 // Segments of at most kTinyDirect positions (adasum_onchip.cuh): one warp each, the
@@ -173,6 +188,8 @@ struct TinyArgs {
 // `name` receives a static string naming the kernel, for the optional profiler.
 int launch_gram_f32(const StageArgs& a, void* stream, const char** name);
 int launch_gram_bf16(const StageArgs& a, void* stream, const char** name);
+// Gram partials of a.small_list's tiles, one warp per (tile, group).
+int launch_gram_warp(const StageArgs& a, int in_dtype, void* stream, const char** name);
 int launch_coef(const StageArgs& a, void* stream, const char** name);
 int launch_combine_f32in(const StageArgs& a, int out_dtype, int momentum, void* stream,
                          const char** name);

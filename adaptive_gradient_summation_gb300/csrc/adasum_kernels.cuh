@@ -158,24 +158,22 @@ __device__ __forceinline__ void block_reduce_store(float (&acc)[E], float* __res
 
 // Gram partial of one tile with CUDA-core FMAs: every thread owns whole 16-byte
 // vectors (VW positions of all Kg workers) and accumulates the Kg(Kg+1)/2 products.
+// This thread's products over vectors first, first + step, ... of a tile (acc zeroed).
 template <typename Tag, int KG>
-__device__ __forceinline__ void gram_tile_simt(const StageArgs& a, int tile_id, int q) {
+__device__ __forceinline__ void gram_accumulate(const StageArgs& a, const TileDesc& t, int q,
+                                                int first, int step, float (&acc)[tri_count(KG)]) {
   using S = typename ElemTraits<Tag>::Storage;
   constexpr int VW = ElemTraits<Tag>::kVW;
   constexpr int E = tri_count(KG);
-  const TileDesc t = a.tiles[tile_id];
   const S* x[KG];
 #pragma unroll
   for (int k = 0; k < KG; ++k) x[k] = static_cast<const S*>(a.in[q * KG + k]);
   const bool aligned = a.aligned != 0;
   const int64_t lo = t.start, hi = t.start + t.len;
   const int64_t v0 = lo / VW, v1 = (hi + VW - 1) / VW;
-
-  float acc[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) acc[e] = 0.f;
-
-  for (int64_t v = v0 + threadIdx.x; v < v1; v += kThreads) {
+  for (int64_t v = v0 + first; v < v1; v += step) {
     uint4 r[KG];
 #pragma unroll
     for (int k = 0; k < KG; ++k) r[k] = load_vec_raw<Tag, kLoadKeep>(x[k], v, lo, hi, aligned);
@@ -191,12 +189,48 @@ __device__ __forceinline__ void gram_tile_simt(const StageArgs& a, int tile_id, 
           acc[tri_index(KG, i, j)] = __fmaf_rn(xe[i], xe[j], acc[tri_index(KG, i, j)]);
     }
   }
+}
+
+template <typename Tag, int KG>
+__device__ __forceinline__ void gram_tile_simt(const StageArgs& a, int tile_id, int q) {
+  constexpr int E = tri_count(KG);
+  float acc[E];
+  gram_accumulate<Tag, KG>(a, a.tiles[tile_id], q, threadIdx.x, kThreads, acc);
   block_reduce_store<E>(acc, a.partials + (static_cast<size_t>(q) * a.ntiles + tile_id) * E);
+}
+
+// Tile id of this CTA: the CTA kernels run over a.tile_list when the plan splits off
+// small tiles (which gram_warp_kernel takes), else over every tile.
+__device__ __forceinline__ int cta_tile(const StageArgs& a) {
+  return a.tile_list ? a.tile_list[blockIdx.x] : static_cast<int>(blockIdx.x);
 }
 
 template <typename Tag, int KG>
 __global__ void __launch_bounds__(kThreads) gram_simt_kernel(const StageArgs a) {
-  gram_tile_simt<Tag, KG>(a, blockIdx.x, blockIdx.y);
+  gram_tile_simt<Tag, KG>(a, cta_tile(a), blockIdx.y);
+}
+
+// Gram partials of small tiles, one warp per (tile, group): the lanes' partials are
+// summed by the warp's butterfly (a fixed order), with no block-wide reduction, so a
+// tile of a few hundred positions costs a warp, not a CTA.
+template <typename Tag, int KG>
+__global__ void __launch_bounds__(kThreads) gram_warp_kernel(const StageArgs a) {
+  constexpr int E = tri_count(KG);
+  const int w = blockIdx.x * kWarps + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (w >= a.nsmall) return;  // whole warps only
+  const int q = blockIdx.y;
+  const int tile_id = a.small_list[w];
+  float acc[E];
+  gram_accumulate<Tag, KG>(a, a.tiles[tile_id], q, lane, 32, acc);
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc[e] = __fadd_rn(acc[e], __shfl_xor_sync(0xFFFFFFFFu, acc[e], off));
+  }
+  float* dst = a.partials + (static_cast<size_t>(q) * a.ntiles + tile_id) * E;
+#pragma unroll
+  for (int e = 0; e < E; ++e)
+    if ((e & 31) == lane) dst[e] = acc[e];
 }
 
 // --------------------------------------------------- pass 1: Gram (tensor cores, bf16)
@@ -313,7 +347,7 @@ __device__ __forceinline__ void gram_tile_mma(const StageArgs& a, int tile_id, i
 
 template <int KG>
 __global__ void __launch_bounds__(kThreads) gram_mma_bf16_kernel(const StageArgs a) {
-  gram_tile_mma<KG>(a, blockIdx.x, blockIdx.y);
+  gram_tile_mma<KG>(a, cta_tile(a), blockIdx.y);
 }
 
 // Gram partial of one tile with the best engine for the element type and group size.
@@ -1069,6 +1103,18 @@ static __global__ void collect_kernel(const StageArgs a) {
     if (sd.len <= kTinySeg) {
       a.list_tiny[atomicAdd(&a.list_count[2], 1)] = s;
       continue;
+    }
+    if (a.oc_vecs > 0) {  // small enough for the on-chip kernel's recompute
+      const int vw = a.oc_vw;
+      const int64_t nv = (sd.start + sd.len + vw - 1) / vw - sd.start / vw;
+      int c = 0;
+      for (int C = 1; C <= a.oc_cmax; C *= 2, ++c) {
+        if ((nv + C - 1) / C <= a.oc_vecs) {
+          a.oc_list[static_cast<size_t>(c) * a.nsegs + atomicAdd(&a.oc_count[c], 1)] = s;
+          break;
+        }
+      }
+      if ((1 << c) <= a.oc_cmax) continue;
     }
     const int base = atomicAdd(&a.list_count[0], sd.ntiles);
     for (int t = 0; t < sd.ntiles; ++t) a.list_tiles[base + t] = sd.first_tile + t;

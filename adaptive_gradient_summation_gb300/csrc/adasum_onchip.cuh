@@ -160,6 +160,7 @@ __global__ void __launch_bounds__(kOnchipThreads, 2) onchip_kernel(const OnchipA
   float* red = reinterpret_cast<float*>(smem + K * rs);   // [SL][NB][B*B]
 
   const uint32_t C = cluster_nctarank(), rank = cluster_ctarank();
+  if (a.dev_count != nullptr && static_cast<int>(cluster_id_x()) >= *a.dev_count) return;  // whole clusters
   const SegDesc sd = a.segs[a.list[cluster_id_x()]];
   const int64_t s0 = sd.start, s1 = sd.start + sd.len;
   const int64_t vs0 = s0 / VW, vs1 = (s1 + VW - 1) / VW;
@@ -204,101 +205,104 @@ __global__ void __launch_bounds__(kOnchipThreads, 2) onchip_kernel(const OnchipA
     *reinterpret_cast<uint4*>(data + k * rs + j * 16) = load_vec_raw<InTag, kLoadKeep>(x, v, s0, s1, aligned);
   }
   if (!mbar_wait(&bar, 0, a.spin_budget, a.error)) mbar_wait(&bar, 0, a.spin_budget, a.error);
+  if (a.recompute_only && tid == 0) flag = 1;
   __syncthreads();
+  if (!a.recompute_only) {
 
-  // ---------------------------------------------------------------- stage 1: Gram
-  if (tid < NB * SL) {
-    const int slice = tid % SL, blk = tid / SL;
-    const int q = blk / NBG;
-    int bi, bj;
-    tri_unpack(NBS, blk % NBG, bi, bj);
-    const unsigned char* rowp = data + (q * KG1 + bi * B) * rs;
-    const unsigned char* colp = data + (q * KG1 + bj * B) * rs;
-    float acc[B][B];
-#pragma unroll
-    for (int i = 0; i < B; ++i)
-#pragma unroll
-      for (int j = 0; j < B; ++j) acc[i][j] = 0.f;
-    for (int v = slice; v < nvec; v += SL) {
-      uint4 rr[B], cc[B];
-#pragma unroll
-      for (int i = 0; i < B; ++i) {
-        rr[i] = *reinterpret_cast<const uint4*>(rowp + i * rs + v * 16);
-        cc[i] = *reinterpret_cast<const uint4*>(colp + i * rs + v * 16);
-      }
-#pragma unroll
-      for (int e = 0; e < VW; ++e) {
-        float xr[B], xc[B];
-#pragma unroll
-        for (int i = 0; i < B; ++i) {
-          xr[i] = vec_elem<InTag>(rr[i], e);
-          xc[i] = vec_elem<InTag>(cc[i], e);
-        }
-#pragma unroll
-        for (int i = 0; i < B; ++i)
-#pragma unroll
-          for (int j = 0; j < B; ++j) acc[i][j] = __fmaf_rn(xr[i], xc[j], acc[i][j]);
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < B; ++i)
-#pragma unroll
-      for (int j = 0; j < B; ++j) red[(slice * NB + blk) * (B * B) + i * B + j] = acc[i][j];
-  }
-  __syncthreads();
-  {
-    float* xg = reinterpret_cast<float*>(xch[xi & 1]);
-    for (int e = tid; e < NB * B * B; e += kOnchipThreads) {
-      float sum = 0.f, comp = 0.f;
-      for (int s = 0; s < SL; ++s) kahan_add(sum, comp, red[s * NB * B * B + e]);
-      const int blk = e / (B * B), ij = e % (B * B);
+    // ---------------------------------------------------------------- stage 1: Gram
+    if (tid < NB * SL) {
+      const int slice = tid % SL, blk = tid / SL;
       const int q = blk / NBG;
       int bi, bj;
       tri_unpack(NBS, blk % NBG, bi, bj);
-      const int i = bi * B + ij / B, j = bj * B + ij % B;
-      if (i <= j) xg[q * E1 + tri_index(KG1, i, j)] = __fsub_rn(sum, comp);
+      const unsigned char* rowp = data + (q * KG1 + bi * B) * rs;
+      const unsigned char* colp = data + (q * KG1 + bj * B) * rs;
+      float acc[B][B];
+#pragma unroll
+      for (int i = 0; i < B; ++i)
+#pragma unroll
+        for (int j = 0; j < B; ++j) acc[i][j] = 0.f;
+      for (int v = slice; v < nvec; v += SL) {
+        uint4 rr[B], cc[B];
+#pragma unroll
+        for (int i = 0; i < B; ++i) {
+          rr[i] = *reinterpret_cast<const uint4*>(rowp + i * rs + v * 16);
+          cc[i] = *reinterpret_cast<const uint4*>(colp + i * rs + v * 16);
+        }
+#pragma unroll
+        for (int e = 0; e < VW; ++e) {
+          float xr[B], xc[B];
+#pragma unroll
+          for (int i = 0; i < B; ++i) {
+            xr[i] = vec_elem<InTag>(rr[i], e);
+            xc[i] = vec_elem<InTag>(cc[i], e);
+          }
+#pragma unroll
+          for (int i = 0; i < B; ++i)
+#pragma unroll
+            for (int j = 0; j < B; ++j) acc[i][j] = __fmaf_rn(xr[i], xc[j], acc[i][j]);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < B; ++i)
+#pragma unroll
+        for (int j = 0; j < B; ++j) red[(slice * NB + blk) * (B * B) + i * B + j] = acc[i][j];
     }
-    cta_or_cluster_sync(C);
-    // the Gram matrices of this CTA's groups: compensated sums over the cluster, CTA order
-    for (int e = tid; e < NG * E1; e += kOnchipThreads) {
-      const int q = e / E1;
-      if (static_cast<uint32_t>(q) % C != rank) continue;
-      float sum = xg[e], comp = 0.f;
-      if (C > 1) cluster_kahan_sum(xg, e, C, sum, comp);
-      const df32 g = df_fast_two_sum(sum, -comp);  // the compensated sum, as a double-float
-      int i, j;
-      tri_unpack(KG1, e % E1, i, j);
-      G1[q][i][j] = g;
-      G1[q][j][i] = g;
+    __syncthreads();
+    {
+      float* xg = reinterpret_cast<float*>(xch[xi & 1]);
+      for (int e = tid; e < NB * B * B; e += kOnchipThreads) {
+        float sum = 0.f, comp = 0.f;
+        for (int s = 0; s < SL; ++s) kahan_add(sum, comp, red[s * NB * B * B + e]);
+        const int blk = e / (B * B), ij = e % (B * B);
+        const int q = blk / NBG;
+        int bi, bj;
+        tri_unpack(NBS, blk % NBG, bi, bj);
+        const int i = bi * B + ij / B, j = bj * B + ij % B;
+        if (i <= j) xg[q * E1 + tri_index(KG1, i, j)] = __fsub_rn(sum, comp);
+      }
+      cta_or_cluster_sync(C);
+      // the Gram matrices of this CTA's groups: compensated sums over the cluster, CTA order
+      for (int e = tid; e < NG * E1; e += kOnchipThreads) {
+        const int q = e / E1;
+        if (static_cast<uint32_t>(q) % C != rank) continue;
+        float sum = xg[e], comp = 0.f;
+        if (C > 1) cluster_kahan_sum(xg, e, C, sum, comp);
+        const df32 g = df_fast_two_sum(sum, -comp);  // the compensated sum, as a double-float
+        int i, j;
+        tri_unpack(KG1, e % E1, i, j);
+        G1[q][i][j] = g;
+        G1[q][j][i] = g;
+      }
+      ++xi;
     }
-    ++xi;
-  }
-  __syncthreads();
-  {
-    // warp w of CTA r evaluates group w * C + r
-    const int q = warp * static_cast<int>(C) + static_cast<int>(rank);
-    if (q < NG) {
-      float c = 0.f;
-      bool ill = false;
-      const double rel = coefficient_tree_df<KG1>(G1[q], zeros, kGramRelErr, csh[q], c, ill);
-      if (lane < KG1) tcoef[q][lane] = c;
-      if (lane == 0) {
-        trel[q] = rel;
-        tflag[q] = (ill || !(rel <= kRelErrBudget)) ? 1 : 0;
+    __syncthreads();
+    {
+      // warp w of CTA r evaluates group w * C + r
+      const int q = warp * static_cast<int>(C) + static_cast<int>(rank);
+      if (q < NG) {
+        float c = 0.f;
+        bool ill = false;
+        const double rel = coefficient_tree_df<KG1>(G1[q], zeros, kGramRelErr, csh[q], c, ill);
+        if (lane < KG1) tcoef[q][lane] = c;
+        if (lane == 0) {
+          trel[q] = rel;
+          tflag[q] = (ill || !(rel <= kRelErrBudget)) ? 1 : 0;
+        }
       }
     }
-  }
-  cta_or_cluster_sync(C);
-  if (tid < NG * KG1) {
-    const int q = tid / KG1, k = tid % KG1;
-    coef1[q][k] = *map_rank(&tcoef[q][k], static_cast<uint32_t>(q) % C);
-  }
-  if (tid < NG) {
-    rel1[tid] = *map_rank(&trel[tid], static_cast<uint32_t>(tid) % C);
-    if (*map_rank(&tflag[tid], static_cast<uint32_t>(tid) % C)) flag = 1;
-  }
-  __syncthreads();
+    cta_or_cluster_sync(C);
+    if (tid < NG * KG1) {
+      const int q = tid / KG1, k = tid % KG1;
+      coef1[q][k] = *map_rank(&tcoef[q][k], static_cast<uint32_t>(q) % C);
+    }
+    if (tid < NG) {
+      rel1[tid] = *map_rank(&trel[tid], static_cast<uint32_t>(tid) % C);
+      if (*map_rank(&tflag[tid], static_cast<uint32_t>(tid) % C)) flag = 1;
+    }
+    __syncthreads();
 
+  }  // fp32 pass: stage-1 Gram and trees
   S* const out = static_cast<S*>(a.out);
   if (!flag) {
     if constexpr (NG == 1) {

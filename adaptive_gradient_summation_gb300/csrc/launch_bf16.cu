@@ -13,7 +13,7 @@ int launch(Kernel k, dim3 grid, dim3 block, const StageArgs& a, void* stream) {
 }  // namespace
 
 int launch_gram_bf16(const StageArgs& a, void* stream, const char** name) {
-  const dim3 grid(a.ntiles, a.G), block(kThreads);
+  const dim3 grid(a.tile_list ? a.ntile_list : a.ntiles, a.G), block(kThreads);
   switch (a.Kg) {
     case 2: *name = "gram_simt<bf16,2>"; return launch(gram_simt_kernel<BF16Tag, 2>, grid, block, a, stream);
     case 4: *name = "gram_simt<bf16,4>"; return launch(gram_simt_kernel<BF16Tag, 4>, grid, block, a, stream);

@@ -13,12 +13,32 @@ int launch(Kernel k, dim3 grid, dim3 block, const StageArgs& a, void* stream) {
 }  // namespace
 
 int launch_gram_f32(const StageArgs& a, void* stream, const char** name) {
-  const dim3 grid(a.ntiles, a.G), block(kThreads);
+  const dim3 grid(a.tile_list ? a.ntile_list : a.ntiles, a.G), block(kThreads);
   switch (a.Kg) {
     case 2: *name = "gram_simt<f32,2>"; return launch(gram_simt_kernel<F32Tag, 2>, grid, block, a, stream);
     case 4: *name = "gram_simt<f32,4>"; return launch(gram_simt_kernel<F32Tag, 4>, grid, block, a, stream);
     case 8: *name = "gram_simt<f32,8>"; return launch(gram_simt_kernel<F32Tag, 8>, grid, block, a, stream);
     case 16: *name = "gram_simt<f32,16>"; return launch(gram_simt_kernel<F32Tag, 16>, grid, block, a, stream);
+    default: return static_cast<int>(cudaErrorInvalidValue);
+  }
+}
+
+int launch_gram_warp(const StageArgs& a, int in_dtype, void* stream, const char** name) {
+  const dim3 grid((a.nsmall + kWarps - 1) / kWarps, a.G), block(kThreads);
+  if (in_dtype == kF32) {
+    switch (a.Kg) {
+      case 2: *name = "gram_warp<f32,2>"; return launch(gram_warp_kernel<F32Tag, 2>, grid, block, a, stream);
+      case 4: *name = "gram_warp<f32,4>"; return launch(gram_warp_kernel<F32Tag, 4>, grid, block, a, stream);
+      case 8: *name = "gram_warp<f32,8>"; return launch(gram_warp_kernel<F32Tag, 8>, grid, block, a, stream);
+      case 16: *name = "gram_warp<f32,16>"; return launch(gram_warp_kernel<F32Tag, 16>, grid, block, a, stream);
+      default: return static_cast<int>(cudaErrorInvalidValue);
+    }
+  }
+  switch (a.Kg) {
+    case 2: *name = "gram_warp<bf16,2>"; return launch(gram_warp_kernel<BF16Tag, 2>, grid, block, a, stream);
+    case 4: *name = "gram_warp<bf16,4>"; return launch(gram_warp_kernel<BF16Tag, 4>, grid, block, a, stream);
+    case 8: *name = "gram_warp<bf16,8>"; return launch(gram_warp_kernel<BF16Tag, 8>, grid, block, a, stream);
+    case 16: *name = "gram_warp<bf16,16>"; return launch(gram_warp_kernel<BF16Tag, 16>, grid, block, a, stream);
     default: return static_cast<int>(cudaErrorInvalidValue);
   }
 }

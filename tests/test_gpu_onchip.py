@@ -3,8 +3,9 @@ cluster, held in shared memory, the whole tree on chip; and segments of at most 
 positions one warp each, the tree on the values in double-float arithmetic.
 
 Plain reductions send every segment of at most 32 positions to the warp kernel and, for
-up to 64 workers, every segment that fits in 16 CTAs' shared memory to the on-chip
-kernel; the rest take the tiled route.  These tests pick segment lengths around each
+up to 64 workers and when small segments are numerous, every segment that fits in a
+cluster's shared memory to the on-chip kernel; the rest take the tiled route.  (The
+tests here force the on-chip kernel for every small segment and allow clusters of 16.)  These tests pick segment lengths around each
 cluster-size boundary (1, 2, 4, 8, 16 CTAs), unaligned starts, padded worker counts,
 nearly cancelling sets (the on-chip recompute), segments mixed with tiled ones, and
 compare with the fp64 oracle at the stated tolerances.
@@ -22,6 +23,15 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
 DATA_BYTES = 80 * 1024  # shared memory per CTA for the K x P block (fp32-sized slots)
 TINY = 32               # segments up to this length: one warp each, double-float
+
+
+@pytest.fixture(autouse=True)
+def _onchip_for_every_small_segment(monkeypatch):
+    """By default the library uses the on-chip kernel only when small segments are
+    numerous (thousands); these tests use it for every small segment, with clusters of
+    up to 16 CTAs."""
+    monkeypatch.setenv("ADASUM_ONCHIP", "force")
+    monkeypatch.setenv("ADASUM_ONCHIP_MAX_CLUSTER", "16")
 
 
 def positions_per_cta(K):
@@ -207,3 +217,19 @@ def test_tiny_segments_extreme_magnitudes(native, scale):
     out = ags.reduce(grads, offs)
     torch.cuda.synchronize()
     check_against_oracle(grads, offs, out)
+
+
+@pytest.mark.parametrize("K", [2, 16])
+def test_flagged_tiled_segments(native, monkeypatch, K):
+    """Segments that take the tiled route and get flagged: those that fit 16 CTAs are
+    recomputed by the on-chip kernel, a longer one by the fp64 path; both within
+    tolerance."""
+    monkeypatch.setenv("ADASUM_ONCHIP", "1")     # the default routing (few segments: tiled)
+    cap16 = 16 * positions_per_cta(K)
+    lengths = [cap16 + 999, 5000, 700]
+    offs = workloads.offsets_from_numels(lengths)
+    grads = _cancelling_set(K, int(offs[-1]), torch.float32, seed=800 + K)
+    out = ags.reduce(grads, offs)
+    torch.cuda.synchronize()
+    check_against_oracle(grads, offs, out)
+    assert ags.recomputed_segments() == len(lengths)
