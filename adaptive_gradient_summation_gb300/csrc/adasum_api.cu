@@ -1007,7 +1007,7 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
         }))
       return st;
   }
-  {
+  if (!plan->tiny_on) {  // (with the warp kernel on, no tiled segment is that short)
     // flagged segments of at most kTinySeg positions: the whole tree, vector space
     StageArgs a = make_args(kg.size() - 1);
     for (int k = 0; k < K; ++k) a.in[k] = grads[k];

@@ -23,6 +23,7 @@
 #include <stdint.h>
 
 #include "adasum_internal.h"
+#include "adasum_ptx.cuh"
 
 namespace adasum {
 
@@ -207,6 +208,7 @@ __device__ __forceinline__ int cta_tile(const StageArgs& a) {
 
 template <typename Tag, int KG>
 __global__ void __launch_bounds__(kThreads) gram_simt_kernel(const StageArgs a) {
+  pdl_enter();
   gram_tile_simt<Tag, KG>(a, cta_tile(a), blockIdx.y);
 }
 
@@ -215,6 +217,7 @@ __global__ void __launch_bounds__(kThreads) gram_simt_kernel(const StageArgs a) 
 // tile of a few hundred positions costs a warp, not a CTA.
 template <typename Tag, int KG>
 __global__ void __launch_bounds__(kThreads) gram_warp_kernel(const StageArgs a) {
+  pdl_enter();
   constexpr int E = tri_count(KG);
   const int w = blockIdx.x * kWarps + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (w >= a.nsmall) return;  // whole warps only
@@ -347,6 +350,7 @@ __device__ __forceinline__ void gram_tile_mma(const StageArgs& a, int tile_id, i
 
 template <int KG>
 __global__ void __launch_bounds__(kThreads) gram_mma_bf16_kernel(const StageArgs a) {
+  pdl_enter();
   gram_tile_mma<KG>(a, cta_tile(a), blockIdx.y);
 }
 
@@ -385,6 +389,7 @@ __device__ __forceinline__ void reduce_chunk(const StageArgs& a, int c, int q) {
 
 template <int KG>
 __global__ void __launch_bounds__(kThreads) reduce_chunks_kernel(const StageArgs a) {
+  pdl_enter();
   reduce_chunk<KG>(a, blockIdx.x, blockIdx.y);
 }
 
@@ -828,6 +833,7 @@ __device__ __forceinline__ void segment_coefficients(const StageArgs& a, int seg
 
 template <int KG>
 __global__ void __launch_bounds__(128) coef_kernel(const StageArgs a) {
+  pdl_enter();
   segment_coefficients<KG>(a, a.seg_list ? a.seg_list[blockIdx.x] : static_cast<int>(blockIdx.x), blockIdx.y);
 }
 
@@ -966,6 +972,7 @@ __device__ __forceinline__ void combine_tile(const StageArgs& a, int tile_id, in
 
 template <typename InTag, typename OutTag, int KG, bool MOM>
 __global__ void __launch_bounds__(kThreads) combine_kernel(const StageArgs a) {
+  pdl_enter();
   combine_tile<InTag, OutTag, KG, MOM>(a, blockIdx.x, blockIdx.y);
 }
 
@@ -1059,6 +1066,7 @@ __global__ void __launch_bounds__(kThreads, 3) pipeline_kernel(const StageArgs a
 template <typename Tag>
 __global__ void __launch_bounds__(kThreads) local_momentum_kernel(const void* g, float* v,
                                                                   int64_t n, float mu, int aligned) {
+  pdl_enter();
   using S = typename ElemTraits<Tag>::Storage;
   constexpr int VW = ElemTraits<Tag>::kVW;
   const S* x = static_cast<const S*>(g);
@@ -1096,6 +1104,7 @@ __device__ __forceinline__ double load_f64(const void* base, int64_t i) {
 // Builds the lists of flagged tiles and segments (order of the lists is irrelevant:
 // every tile and segment is computed on its own).
 static __global__ void collect_kernel(const StageArgs a) {
+  pdl_enter();
   for (int s = blockIdx.x * blockDim.x + threadIdx.x; s < a.nsegs; s += gridDim.x * blockDim.x) {
     if (!a.seg_flag[s]) continue;
     const SegDesc sd = a.segs[s];
@@ -1125,6 +1134,7 @@ static __global__ void collect_kernel(const StageArgs a) {
 // The orthogonality metric of every segment: |A|^2 / sum_k |g_k|^2 (NaN when 0/0).
 static __global__ void orthogonality_kernel(const double* outnorm2, const double* diag_sum,
                                             int groups, int nsegs, float* ortho) {
+  pdl_enter();
   for (int s = blockIdx.x * blockDim.x + threadIdx.x; s < nsegs; s += gridDim.x * blockDim.x) {
     double den = 0.0;
     for (int q = 0; q < groups; ++q) den += diag_sum[static_cast<size_t>(q) * nsegs + s];
@@ -1146,6 +1156,7 @@ __device__ __forceinline__ double warp_sum64(double v) {
 // recomputed from the node values themselves, as in the definition.
 template <int IN, int OUT, bool MOM>
 __global__ void __launch_bounds__(kThreads) tiny64_kernel(const StageArgs a) {
+  pdl_enter();
   constexpr int kMaxDepth = 10;  // log2(kMaxK) + 2
   const int lane = threadIdx.x & 31;
   const int wid = (blockIdx.x * kThreads + threadIdx.x) >> 5;
@@ -1201,6 +1212,7 @@ __global__ void __launch_bounds__(kThreads) tiny64_kernel(const StageArgs a) {
 // scales its segment by the matching power of two.
 template <int IN>
 __global__ void __launch_bounds__(kThreads) segmax_kernel(const StageArgs a) {
+  pdl_enter();
   __shared__ float wmax[kWarps];
   const int count = a.list_count[0];
   const int K = a.G * a.Kg;
@@ -1235,6 +1247,7 @@ __global__ void __launch_bounds__(kThreads) segmax_kernel(const StageArgs a) {
 // range; thread e owns Gram entry e.  The partial is scaled back and stored in fp64.
 template <int IN, int KG>
 __global__ void __launch_bounds__(kThreads) gram64_kernel(const StageArgs a) {
+  pdl_enter();
   constexpr int E = tri_count(KG);
   constexpr int P = 64;
   __shared__ df32 xs[KG][P];
@@ -1277,6 +1290,7 @@ __global__ void __launch_bounds__(kThreads) gram64_kernel(const StageArgs a) {
 // fp64 coefficients of every flagged segment (plain tree, no error estimate needed).
 template <int KG>
 __global__ void __launch_bounds__(128) coef64_kernel(const StageArgs a) {
+  pdl_enter();
   constexpr int E = tri_count(KG);
   __shared__ double G[KG][KG];
   __shared__ double zeros[KG];
@@ -1325,6 +1339,7 @@ __device__ __forceinline__ double tree_combine64(const double (&c)[KG], const St
 // fp64 combine of every flagged tile (plus the fp64 heavy-ball step when requested).
 template <int IN, int OUT, int KG, bool MOM>
 __global__ void __launch_bounds__(kThreads) combine64_kernel(const StageArgs a) {
+  pdl_enter();
   const int q = blockIdx.y;
   const int count = a.list_count[0];
   for (int li = blockIdx.x; li < count; li += gridDim.x) {

@@ -118,6 +118,7 @@ __device__ __forceinline__ void cta_or_cluster_sync(uint32_t C) {
 
 template <typename InTag, int KG1, int NG>
 __global__ void __launch_bounds__(kOnchipThreads, 2) onchip_kernel(const OnchipArgs a) {
+  pdl_enter();
   using S = typename ElemTraits<InTag>::Storage;
   constexpr int VW = ElemTraits<InTag>::kVW;
   constexpr int K = KG1 * NG;
@@ -505,6 +506,7 @@ __global__ void __launch_bounds__(kOnchipThreads, 2) onchip_kernel(const OnchipA
 // Eight segments per CTA, no block barriers: the warps' latencies overlap.
 template <typename InTag>
 __global__ void __launch_bounds__(kOnchipThreads) tiny_df_kernel(const TinyArgs a) {
+  pdl_enter();
   using S = typename ElemTraits<InTag>::Storage;
   constexpr int kMaxDepth = 10;  // log2(kMaxK) + 2
   const int lane = threadIdx.x & 31;

@@ -59,6 +59,19 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// ------------------------------------------------------------------ dependent launch
+
+// First statement of every kernel of a call's chain.  The kernels are launched with
+// programmatic stream serialization, so the next kernel of the chain may be scheduled as
+// soon as every CTA of this one has run launch_dependents (its launch latency then
+// overlaps this kernel's tail), and wait blocks until the previous kernel of the stream
+// has completed and its memory is visible -- nothing is read or written before it.
+// (Launched without the attribute, both are no-ops.)
+__device__ __forceinline__ void pdl_enter() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ clusters
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {

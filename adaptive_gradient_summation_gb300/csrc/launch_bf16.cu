@@ -1,14 +1,14 @@
 // launch_bf16.cu -- launchers for bf16 gradients (tensor-core Gram for 8 and 16
 // workers, CUDA-core Gram for 2 and 4).
 #include "adasum_kernels.cuh"
+#include "adasum_launch.h"
 
 namespace adasum {
 
 namespace {
 template <typename Kernel>
 int launch(Kernel k, dim3 grid, dim3 block, const StageArgs& a, void* stream) {
-  k<<<grid, block, 0, static_cast<cudaStream_t>(stream)>>>(a);
-  return static_cast<int>(cudaGetLastError());
+  return launch_pdl(k, grid, block, 0, static_cast<cudaStream_t>(stream), a);
 }
 }  // namespace
 

@@ -1,14 +1,14 @@
 // launch_f32.cu -- launchers for fp32 inputs (user fp32 gradients and the fp32
 // intermediates of multi-stage trees) and for the per-segment coefficient kernel.
 #include "adasum_kernels.cuh"
+#include "adasum_launch.h"
 
 namespace adasum {
 
 namespace {
 template <typename Kernel>
 int launch(Kernel k, dim3 grid, dim3 block, const StageArgs& a, void* stream) {
-  k<<<grid, block, 0, static_cast<cudaStream_t>(stream)>>>(a);
-  return static_cast<int>(cudaGetLastError());
+  return launch_pdl(k, grid, block, 0, static_cast<cudaStream_t>(stream), a);
 }
 }  // namespace
 

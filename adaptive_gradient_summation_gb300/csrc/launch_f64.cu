@@ -3,14 +3,14 @@
 #include <algorithm>
 
 #include "adasum_kernels.cuh"
+#include "adasum_launch.h"
 
 namespace adasum {
 
 namespace {
 template <typename Kernel>
 int launch(Kernel k, dim3 grid, dim3 block, const StageArgs& a, void* stream) {
-  k<<<grid, block, 0, static_cast<cudaStream_t>(stream)>>>(a);
-  return static_cast<int>(cudaGetLastError());
+  return launch_pdl(k, grid, block, 0, static_cast<cudaStream_t>(stream), a);
 }
 
 int kind_of(int dtype, int is_f64) { return is_f64 ? kKindF64 : (dtype == kBF16 ? kKindBF16 : kKindF32); }
@@ -47,19 +47,18 @@ int launch_local_momentum(const void* g, int dtype, float* v, int64_t n, float m
   const int64_t blocks = std::min<int64_t>((n / vw + kThreads) / kThreads, 8LL * num_sms);
   const dim3 grid(static_cast<unsigned>(std::max<int64_t>(1, blocks)));
   if (dtype == kBF16)
-    local_momentum_kernel<BF16Tag><<<grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(g, v, n, mu, aligned);
-  else
-    local_momentum_kernel<F32Tag><<<grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(g, v, n, mu, aligned);
-  return static_cast<int>(cudaGetLastError());
+    return launch_pdl(local_momentum_kernel<BF16Tag>, grid, dim3(kThreads), 0, static_cast<cudaStream_t>(stream), g,
+                      v, n, mu, aligned);
+  return launch_pdl(local_momentum_kernel<F32Tag>, grid, dim3(kThreads), 0, static_cast<cudaStream_t>(stream), g, v,
+                    n, mu, aligned);
 }
 
 int launch_orthogonality(const double* outnorm2, const double* diag_sum, int groups, int nsegs,
                          float* ortho, void* stream, const char** name) {
   *name = "orthogonality";
   const int grid = (nsegs + kThreads - 1) / kThreads;
-  orthogonality_kernel<<<grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
-      outnorm2, diag_sum, groups, nsegs, ortho);
-  return static_cast<int>(cudaGetLastError());
+  return launch_pdl(orthogonality_kernel, dim3(grid), dim3(kThreads), 0, static_cast<cudaStream_t>(stream),
+                    outnorm2, diag_sum, groups, nsegs, ortho);
 }
 
 int launch_collect(const StageArgs& a, int grid, void* stream, const char** name) {

@@ -4,6 +4,7 @@
 #include <mutex>
 #include <string>
 
+#include "adasum_launch.h"
 #include "adasum_onchip.cuh"
 
 namespace adasum {
@@ -39,8 +40,11 @@ template <typename Tag, int KG1, int NG>
 int launch_k(const OnchipArgs& a, int count, int C, void* stream) {
   cudaError_t e = configure<Tag, KG1, NG>(C);
   if (e != cudaSuccess) return static_cast<int>(e);
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = make_config<Tag, KG1, NG>(count, C, static_cast<cudaStream_t>(stream), attr);
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see pdl_enter()
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.numAttrs = 2;
   return static_cast<int>(cudaLaunchKernelEx(&cfg, onchip_kernel<Tag, KG1, NG>, a));
 }
 
@@ -152,12 +156,10 @@ int launch_tiny_df(const TinyArgs& a, int dtype, void* stream, const char** name
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (dtype == kF32) {
     *name = "tiny_df<f32>";
-    tiny_df_kernel<F32Tag><<<grid, block, 0, s>>>(a);
-  } else {
-    *name = "tiny_df<bf16>";
-    tiny_df_kernel<BF16Tag><<<grid, block, 0, s>>>(a);
+    return launch_pdl(tiny_df_kernel<F32Tag>, grid, block, 0, s, a);
   }
-  return static_cast<int>(cudaGetLastError());
+  *name = "tiny_df<bf16>";
+  return launch_pdl(tiny_df_kernel<BF16Tag>, grid, block, 0, s, a);
 }
 
 }  // namespace adasum
