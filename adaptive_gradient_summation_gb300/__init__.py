@@ -208,9 +208,16 @@ def local_momentum_reduce(grads, seg_offsets, momenta, master_w: torch.Tensor, *
 
 def reduce_from_host(grads_host: Sequence[torch.Tensor], seg_offsets=None, *,
                      device: torch.device | str = "cuda", staging: list | None = None,
-                     out_host: torch.Tensor | None = None) -> torch.Tensor:
+                     out_host: torch.Tensor | None = None,
+                     chunk_bytes: int = 1 << 30) -> torch.Tensor:
     """End-to-end Adasum of gradients held in (preferably pinned) host memory: copy them
     to the device, run ``adasum_reduce``, copy the result back, and wait for it.
+
+    The segments are processed in groups of about ``chunk_bytes`` of input (a longer
+    segment is a group of its own): the copy of group i+1 runs on a copy stream while
+    group i is reduced, and each group's result is copied back on a third stream as soon
+    as it is ready, so the transfer time, not the sum of transfer and compute, sets the
+    pace.
 
     staging: optional list of K device tensors to copy into (reused across calls).
     out_host: optional host tensor for the result (pinned for an asynchronous copy).
@@ -220,15 +227,37 @@ def reduce_from_host(grads_host: Sequence[torch.Tensor], seg_offsets=None, *,
     n = grads_host[0].numel()
     dtype = grads_host[0].dtype
     device = torch.device(device)
+    offs = _offsets(seg_offsets, n)
     if staging is None:
         staging = [torch.empty(n, dtype=dtype, device=device) for _ in range(K)]
-    for dst, src in zip(staging, grads_host):
-        dst.copy_(src, non_blocking=True)
-    res = reduce(staging, seg_offsets)
     if out_host is None:
         out_host = torch.empty(n, dtype=dtype, pin_memory=True)
-    out_host.copy_(res, non_blocking=True)
-    torch.cuda.current_stream(device).synchronize()
+    res = torch.empty(n, dtype=dtype, device=device)
+    bytes_per_pos = K * grads_host[0].element_size()
+    groups, s0 = [], 0
+    L = offs.shape[0] - 1
+    for s in range(1, L + 1):
+        if (offs[s] - offs[s0]) * bytes_per_pos >= chunk_bytes or s == L:
+            groups.append((s0, s))
+            s0 = s
+    compute = torch.cuda.current_stream(device)
+    copy_in = torch.cuda.Stream(device)
+    copy_out = torch.cuda.Stream(device)
+    copy_in.wait_stream(compute)   # the staging buffers may still be read by earlier work
+    for a, b in groups:
+        p0, p1 = int(offs[a]), int(offs[b])
+        if p1 == p0:
+            continue
+        with torch.cuda.stream(copy_in):
+            for dst, src in zip(staging, grads_host):
+                dst[p0:p1].copy_(src[p0:p1], non_blocking=True)
+        compute.wait_stream(copy_in)
+        reduce([d[p0:p1] for d in staging], offs[a:b + 1] - p0, out=res[p0:p1])
+        copy_out.wait_stream(compute)
+        with torch.cuda.stream(copy_out):
+            out_host[p0:p1].copy_(res[p0:p1], non_blocking=True)
+    compute.wait_stream(copy_out)
+    compute.synchronize()
     return out_host
 
 

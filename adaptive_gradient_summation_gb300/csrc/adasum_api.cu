@@ -424,7 +424,7 @@ adasum_status_t get_plan(Workspace& ws, const int64_t* offs, int L, int Kg0, int
     segs[s].nchunks = static_cast<int32_t>(chunks.size()) - segs[s].first_chunk;
   }
   if (tiles.size() > static_cast<size_t>(INT32_MAX / 2)) return ADASUM_ERR_UNSUPPORTED;
-  if (ws.plans.size() >= 8) {
+  if (ws.plans.size() >= 32) {  // (a pipelined caller keeps one plan per segment group)
     free_plan(ws.plans.back());
     ws.plans.pop_back();
   }

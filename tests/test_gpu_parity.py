@@ -297,6 +297,20 @@ def test_host_end_to_end(native):
     check_against_oracle(wl.grads, wl.seg_offsets, out)
 
 
+@pytest.mark.parametrize("name", ["resnet50_k8", "bert_large_k16"])
+def test_host_end_to_end_pipelined(native, name):
+    """Many small segment groups (copy of group i+1 overlapping the reduce of group i,
+    results copied back per group) give the same answers as the oracle, twice in a row
+    with the same staging buffers."""
+    wl = workloads.make(name, device="cpu", shrink=64)
+    host = [g.pin_memory() for g in wl.grads]
+    staging = [torch.empty(wl.N, dtype=wl.dtype, device=DEV) for _ in range(wl.K)]
+    for _ in range(2):
+        out = ags.reduce_from_host(host, wl.seg_offsets, device=DEV, staging=staging,
+                                   chunk_bytes=1 << 20)
+        check_against_oracle(wl.grads, wl.seg_offsets, out)
+
+
 # ------------------------------------------------------- ill-conditioned segments (fp64)
 
 def _cancelling_set(K, n, dtype, seed, eps=1e-3):
