@@ -819,6 +819,9 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
     a.list_count = list_count;
     a.Ktotal = chain ? Kreal : K;
     a.seg_exp = seg_exp;
+    // up to 4 tiles (1 MiB) per combine CTA while the grid keeps 16 CTAs per SM
+    a.combine_tiles = static_cast<int>(std::max<int64_t>(
+        1, std::min<int64_t>(4, plan->ntiles / (16 * static_cast<int64_t>(num_sms)))));
     if (plan->rc_cmax > 0) {
       a.oc_vecs = onchip_positions(K) / (dtype == kF32 ? 4 : 8);
       a.oc_vw = dtype == kF32 ? 4 : 8;

@@ -85,6 +85,7 @@ struct StageArgs {
   int ntile_list;
   const int* small_list;      // small tiles, one warp each (gram_warp_kernel)
   int nsmall;
+  int combine_tiles;          // consecutive tiles per combine CTA (>= 1)
 
   // fp64 path (only the segments listed by collect_kernel).
   double* partials64;         // [G][ntiles][E]

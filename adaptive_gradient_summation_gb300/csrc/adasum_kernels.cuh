@@ -207,7 +207,8 @@ __device__ __forceinline__ int cta_tile(const StageArgs& a) {
 }
 
 template <typename Tag, int KG>
-__global__ void __launch_bounds__(kThreads) gram_simt_kernel(const StageArgs a) {
+// (up to 8 workers the 36 accumulators fit in 85 registers: three CTAs per SM)
+__global__ void __launch_bounds__(kThreads, KG <= 8 ? 3 : 1) gram_simt_kernel(const StageArgs a) {
   pdl_enter();
   gram_tile_simt<Tag, KG>(a, cta_tile(a), blockIdx.y);
 }
@@ -918,18 +919,17 @@ __device__ __forceinline__ void load_f32_vec(const float* x, int64_t p0, int64_t
 // (fp32), and out is written only when a.out[q] is not null.
 // (Coefficients and flags written by other CTAs are read through L2.)
 template <typename InTag, typename OutTag, int KG, bool MOM>
-__device__ __forceinline__ void combine_tile(const StageArgs& a, int tile_id, int q) {
+__device__ __forceinline__ void combine_range(const StageArgs& a, int seg, int64_t lo, int64_t hi, int q) {
   using SI = typename ElemTraits<InTag>::Storage;
   using SO = typename ElemTraits<OutTag>::Storage;
   constexpr int VW = ElemTraits<InTag>::kVW;
-  const TileDesc t = a.tiles[tile_id];
-  if (a.skip_flagged && __ldcg(a.seg_flag + t.seg)) return;  // left to the fp64 path
+  if (a.skip_flagged && __ldcg(a.seg_flag + seg)) return;  // left to the fp64 path
   const bool aligned = a.aligned != 0;
   float c[KG];
   if constexpr (KG == 1) {
     c[0] = 1.f;
   } else {
-    const float* cp = a.coef + (static_cast<size_t>(q) * a.nsegs + t.seg) * KG;
+    const float* cp = a.coef + (static_cast<size_t>(q) * a.nsegs + seg) * KG;
 #pragma unroll
     for (int k = 0; k < KG; ++k) c[k] = __ldcg(cp + k);
   }
@@ -937,7 +937,6 @@ __device__ __forceinline__ void combine_tile(const StageArgs& a, int tile_id, in
 #pragma unroll
   for (int k = 0; k < KG; ++k) x[k] = static_cast<const SI*>(a.in[q * KG + k]);
   SO* y = static_cast<SO*>(a.out[q]);
-  const int64_t lo = t.start, hi = t.start + t.len;
   const int64_t v0 = lo / VW, v1 = (hi + VW - 1) / VW;
   for (int64_t v = v0 + threadIdx.x; v < v1; v += kThreads) {
     uint4 r[KG];
@@ -970,10 +969,33 @@ __device__ __forceinline__ void combine_tile(const StageArgs& a, int tile_id, in
   }
 }
 
+// out = sum_k c_k g_k over one tile (see combine_range).
+template <typename InTag, typename OutTag, int KG, bool MOM>
+__device__ __forceinline__ void combine_tile(const StageArgs& a, int tile_id, int q) {
+  const TileDesc t = a.tiles[tile_id];
+  combine_range<InTag, OutTag, KG, MOM>(a, t.seg, t.start, t.start + t.len, q);
+}
+
 template <typename InTag, typename OutTag, int KG, bool MOM>
 __global__ void __launch_bounds__(kThreads) combine_kernel(const StageArgs a) {
   pdl_enter();
-  combine_tile<InTag, OutTag, KG, MOM>(a, blockIdx.x, blockIdx.y);
+  // a.combine_tiles consecutive tiles per CTA, consecutive tiles of one segment merged
+  // into one range: the prologue (coefficients, flag) is a dependent L2 round trip, and
+  // one long strided loop streams better than several short ones
+  const int t0 = blockIdx.x * a.combine_tiles;
+  const int t1 = min(a.ntiles, t0 + a.combine_tiles);
+  for (int t = t0; t < t1;) {
+    const TileDesc first = a.tiles[t];
+    int64_t hi = first.start + first.len;
+    int u = t + 1;
+    for (; u < t1; ++u) {
+      const TileDesc nx = a.tiles[u];
+      if (nx.seg != first.seg) break;
+      hi = nx.start + nx.len;
+    }
+    combine_range<InTag, OutTag, KG, MOM>(a, first.seg, first.start, hi, blockIdx.y);
+    t = u;
+  }
 }
 
 // ------------------------------------------------------------- fused single-stage kernel

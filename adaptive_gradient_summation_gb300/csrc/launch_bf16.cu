@@ -25,7 +25,7 @@ int launch_gram_bf16(const StageArgs& a, void* stream, const char** name) {
 
 template <typename OutTag, bool MOM>
 static int combine_bf16_k(const StageArgs& a, void* stream, const char** name) {
-  const dim3 grid(a.ntiles, a.G), block(kThreads);
+  const dim3 grid((a.ntiles + a.combine_tiles - 1) / a.combine_tiles, a.G), block(kThreads);
   switch (a.Kg) {
     case 1: *name = "combine<bf16,1>"; return launch(combine_kernel<BF16Tag, OutTag, 1, MOM>, grid, block, a, stream);
     case 2: *name = "combine<bf16,2>"; return launch(combine_kernel<BF16Tag, OutTag, 2, MOM>, grid, block, a, stream);

@@ -67,7 +67,7 @@ int launch_coef(const StageArgs& a, void* stream, const char** name) {
 
 template <typename OutTag, bool MOM>
 static int combine_f32_k(const StageArgs& a, void* stream, const char** name) {
-  const dim3 grid(a.ntiles, a.G), block(kThreads);
+  const dim3 grid((a.ntiles + a.combine_tiles - 1) / a.combine_tiles, a.G), block(kThreads);
   switch (a.Kg) {
     case 1: *name = "combine<f32,1>"; return launch(combine_kernel<F32Tag, OutTag, 1, MOM>, grid, block, a, stream);
     case 2: *name = "combine<f32,2>"; return launch(combine_kernel<F32Tag, OutTag, 2, MOM>, grid, block, a, stream);
