@@ -461,7 +461,12 @@ adasum_status_t get_plan(Workspace& ws, const int64_t* offs, int L, int Kg0, int
   if (route == kRouteKernels) {
     for (int t = 0; t < static_cast<int>(tiles.size()); ++t)
       (tiles[t].len <= kSmallTile ? small_tiles : big).push_back(t);
-    if (small_tiles.empty()) big.clear();
+    // a few small tiles cost nothing inside the CTA launch; a separate warp launch pays
+    // its own latency, worth it only when small tiles are numerous
+    if (small_tiles.size() < 2 * static_cast<size_t>(num_sms)) {
+      small_tiles.clear();
+      big.clear();
+    }
   }
   p.nbig = static_cast<int>(big.size());
   p.nsmall = static_cast<int>(small_tiles.size());

@@ -199,8 +199,9 @@ def algorithmic_bytes(kernel: str, wl, out_es: int) -> int:
     if kernel.startswith("gram"):
         return KN * es                      # every input element once
     if kernel.startswith("combine"):
-        extra = 16 * wl.N if wl.master_w is not None else 0
-        return KN * es + wl.N * out_es + extra
+        if wl.master_w is not None:   # the step writes w and v (fp32), not the output
+            return KN * es + 16 * wl.N
+        return KN * es + wl.N * out_es
     return 0
 
 
@@ -215,7 +216,9 @@ def run_ours(args):
     wl = workloads.make(args.workload, device=dev, shrink=args.shrink)
     es = torch.tensor([], dtype=wl.dtype).element_size()
     in_bytes = wl.K * wl.N * es
-    min_bytes = in_bytes + wl.N * es + (16 * wl.N if wl.master_w is not None else 0)
+    # minimum bytes of a step: every input once, plus the output, or, for the fused
+    # Momentum-SGD step (which runs with out=None), fp32 w and v read and written
+    min_bytes = in_bytes + (16 * wl.N if wl.master_w is not None else wl.N * es)
     out = torch.empty(wl.N, dtype=wl.dtype, device=dev)
 
     def step():
