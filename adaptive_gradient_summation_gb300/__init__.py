@@ -206,6 +206,21 @@ def local_momentum_reduce(grads, seg_offsets, momenta, master_w: torch.Tensor, *
     return master_w, momenta
 
 
+def segment_groups(offs, bytes_per_position: int, chunk_bytes: int) -> list:
+    """Consecutive segments grouped into runs of about ``chunk_bytes`` of input: a group
+    closes once it holds at least ``chunk_bytes`` (so a segment longer than that is a
+    group of its own) or at the last segment.  Returns [(first, end), ...] segment index
+    ranges that cover every segment once, in order."""
+    offs = np.asarray(offs, dtype=np.int64)
+    L = offs.shape[0] - 1
+    groups, s0 = [], 0
+    for s in range(1, L + 1):
+        if (offs[s] - offs[s0]) * bytes_per_position >= chunk_bytes or s == L:
+            groups.append((s0, s))
+            s0 = s
+    return groups
+
+
 def reduce_from_host(grads_host: Sequence[torch.Tensor], seg_offsets=None, *,
                      device: torch.device | str = "cuda", staging: list | None = None,
                      out_host: torch.Tensor | None = None,
@@ -233,13 +248,7 @@ def reduce_from_host(grads_host: Sequence[torch.Tensor], seg_offsets=None, *,
     if out_host is None:
         out_host = torch.empty(n, dtype=dtype, pin_memory=True)
     res = torch.empty(n, dtype=dtype, device=device)
-    bytes_per_pos = K * grads_host[0].element_size()
-    groups, s0 = [], 0
-    L = offs.shape[0] - 1
-    for s in range(1, L + 1):
-        if (offs[s] - offs[s0]) * bytes_per_pos >= chunk_bytes or s == L:
-            groups.append((s0, s))
-            s0 = s
+    groups = segment_groups(offs, K * grads_host[0].element_size(), chunk_bytes)
     compute = torch.cuda.current_stream(device)
     copy_in = torch.cuda.Stream(device)
     copy_out = torch.cuda.Stream(device)

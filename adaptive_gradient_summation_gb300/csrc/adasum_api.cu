@@ -126,6 +126,7 @@ struct Plan {
   int* d_coef_list = nullptr;
   // three-kernel route: tiles of at most kSmallTile positions take the warp Gram kernel
   // (lists empty when there are none)
+  bool warp_tiles = true;
   int nbig = 0, nsmall = 0;
   int* d_big = nullptr;
   int* d_small = nullptr;
@@ -334,12 +335,12 @@ adasum_status_t upload(T** dst, const std::vector<T>& v) {
 
 adasum_status_t get_plan(Workspace& ws, const int64_t* offs, int L, int Kg0, int dtype, int route,
                          int onchip_K, int onchip_cmax, bool onchip_force, int rc_cmax, bool tiny_on,
-                         Plan** out) {
+                         bool warp_tiles, Plan** out) {
   const int64_t wave = route == kRouteStream ? env_int("ADASUM_WAVE_MB", 24) << 20 : wave_budget_bytes();
   for (auto it = ws.plans.begin(); it != ws.plans.end(); ++it) {
     if (it->Kg0 == Kg0 && it->dtype == dtype && it->route == route && it->onchip_K == onchip_K &&
         it->onchip_cmax == onchip_cmax && it->onchip_force == onchip_force && it->rc_cmax == rc_cmax &&
-        it->tiny_on == tiny_on &&
+        it->tiny_on == tiny_on && it->warp_tiles == warp_tiles &&
         (route == kRouteKernels ||
          (it->wave_bytes == wave && it->tile_kb == (tile_bytes(true) >> 10) &&
           it->delay_pct == env_int("ADASUM_PIPE_DELAY_PCT", 100) &&
@@ -458,7 +459,7 @@ adasum_status_t get_plan(Workspace& ws, const int64_t* offs, int L, int Kg0, int
       if (segs[s].ntiles > 0) coef_list.push_back(s);
   p.ncoef = static_cast<int>(coef_list.size());
   std::vector<int> big, small_tiles;
-  if (route == kRouteKernels) {
+  if (route == kRouteKernels && warp_tiles) {
     for (int t = 0; t < static_cast<int>(tiles.size()); ++t)
       (tiles[t].len <= kSmallTile ? small_tiles : big).push_back(t);
     // a few small tiles cost nothing inside the CTA launch; a separate warp launch pays
@@ -468,6 +469,7 @@ adasum_status_t get_plan(Workspace& ws, const int64_t* offs, int L, int Kg0, int
       big.clear();
     }
   }
+  p.warp_tiles = warp_tiles;
   p.nbig = static_cast<int>(big.size());
   p.nsmall = static_cast<int>(small_tiles.size());
   adasum_status_t st = upload(&p.d_tiles, tiles);
@@ -713,7 +715,8 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
   // Plain reductions: segments of at most kTinyDirect positions go to the warp kernel,
   // small ones (up to 64 workers) to the on-chip kernel, the rest to the tiles.
   // (ADASUM_TINY=0 and ADASUM_ONCHIP=0 switch the two kernels off, for comparisons;
-  // ADASUM_ONCHIP=force uses the on-chip kernel for every small segment, for tests.)
+  // ADASUM_ONCHIP=force uses the on-chip kernel for every small segment, for tests;
+  // ADASUM_WARP_GRAM=0 keeps every tile on the CTA Gram kernels.)
   const bool plain = route == kRouteKernels && !mom && !chain && ortho == nullptr && K >= 2;
   const bool tiny_on = plain && env_on("ADASUM_TINY", true);
   int onchip_K = 0, onchip_cmax = 0;
@@ -729,7 +732,7 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
   const int rc_cmax = (plain && K <= kOnchipMaxK && env_on("ADASUM_ONCHIP", true)) ? onchip_max_cluster(dtype, K) : 0;
   Plan* plan = nullptr;
   if (adasum_status_t st = get_plan(ws, offs, L, kg[0], dtype, route, rc_cmax > 0 ? K : onchip_K, onchip_cmax,
-                                    onchip_force, rc_cmax, tiny_on, &plan))
+                                    onchip_force, rc_cmax, tiny_on, env_on("ADASUM_WARP_GRAM", true), &plan))
     return st;
 
   // Workspace layout.

@@ -376,11 +376,13 @@ def test_every_route_matches_oracle(native, monkeypatch, route, name, shrink):
 
 def test_routes_agree(native, monkeypatch):
     """The fused kernel and the three-kernel route sum the same tiles in the same order.
-    (Small segments normally go to the small-segment kernels, whose sums are blocked
-    differently, so those are switched off for the comparison.)"""
+    (Small segments normally go to the small-segment kernels and small tiles to the
+    warp Gram, whose sums are blocked differently, so those are switched off for the
+    comparison.)"""
     wl = workloads.make("bert_large_k16", device=DEV, shrink=128)
     monkeypatch.setenv("ADASUM_ONCHIP", "0")
     monkeypatch.setenv("ADASUM_TINY", "0")
+    monkeypatch.setenv("ADASUM_WARP_GRAM", "0")
     split = ags.reduce(wl.grads, wl.seg_offsets).clone()
     monkeypatch.setenv("ADASUM_ROUTE", "fused")
     monkeypatch.setenv("ADASUM_PIPE_TILE_KB", "256")   # same tiles, so the same sums
