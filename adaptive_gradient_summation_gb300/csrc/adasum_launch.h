@@ -3,9 +3,20 @@
 
 #include <cuda_runtime.h>
 
+#include <cstdlib>
+#include <cstring>
 #include <utility>
 
 namespace adasum {
+
+// Dependent launch is on unless ADASUM_PDL=0 (read once; for comparisons).
+inline bool pdl_enabled() {
+  static const bool on = [] {
+    const char* v = std::getenv("ADASUM_PDL");
+    return v == nullptr || std::strcmp(v, "0") != 0;
+  }();
+  return on;
+}
 
 // Launches `kernel` on `stream` with programmatic stream serialization: the kernel may be
 // scheduled while the previous kernel of the stream finishes (every kernel of the chain
@@ -23,7 +34,7 @@ inline int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sm
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
   return static_cast<int>(cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...));
 }
 

@@ -44,7 +44,7 @@ int launch_k(const OnchipArgs& a, int count, int C, void* stream) {
   cudaLaunchConfig_t cfg = make_config<Tag, KG1, NG>(count, C, static_cast<cudaStream_t>(stream), attr);
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see pdl_enter()
   attr[1].val.programmaticStreamSerializationAllowed = 1;
-  cfg.numAttrs = 2;
+  cfg.numAttrs = pdl_enabled() ? 2 : 1;
   return static_cast<int>(cudaLaunchKernelEx(&cfg, onchip_kernel<Tag, KG1, NG>, a));
 }
 
