@@ -716,13 +716,14 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
   // small ones (up to 64 workers) to the on-chip kernel, the rest to the tiles.
   // (ADASUM_TINY=0 and ADASUM_ONCHIP=0 switch the two kernels off, for comparisons;
   // ADASUM_ONCHIP=force uses the on-chip kernel for every small segment, for tests;
-  // ADASUM_WARP_GRAM=0 keeps every tile on the CTA Gram kernels.)
+  // ADASUM_WARP_GRAM=0 keeps every tile on the CTA Gram kernels; ADASUM_ONCHIP_FAST=0
+  // leaves the on-chip kernel its recompute only.)
   const bool plain = route == kRouteKernels && !mom && !chain && ortho == nullptr && K >= 2;
   const bool tiny_on = plain && env_on("ADASUM_TINY", true);
   int onchip_K = 0, onchip_cmax = 0;
   const char* onchip_env = std::getenv("ADASUM_ONCHIP");
   const bool onchip_force = onchip_env != nullptr && std::strcmp(onchip_env, "force") == 0;
-  if (plain && K <= kOnchipMaxK && env_on("ADASUM_ONCHIP", true)) {
+  if (plain && K <= kOnchipMaxK && env_on("ADASUM_ONCHIP", true) && env_on("ADASUM_ONCHIP_FAST", true)) {
     // clusters of up to 2 CTAs by default: larger clusters measured slower than the
     // tiled route for the segments they add (ADASUM_ONCHIP_MAX_CLUSTER: up to 16)
     onchip_cmax = std::min<int>(onchip_max_cluster(dtype, K), env_int("ADASUM_ONCHIP_MAX_CLUSTER", 2));
