@@ -233,3 +233,20 @@ def test_flagged_tiled_segments(native, monkeypatch, K):
     torch.cuda.synchronize()
     check_against_oracle(grads, offs, out)
     assert ags.recomputed_segments() == len(lengths)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_in_place_output(native, dtype):
+    """out may be one of the gradients: every kernel reads a segment's inputs before it
+    writes that segment's output (the recompute rereads level-0 inputs, which the fast
+    pass left untouched)."""
+    K = 16
+    cap = positions_per_cta(K)
+    lengths = [5, 32, 300, cap + 9, 3 * cap]
+    offs = workloads.offsets_from_numels(lengths)
+    n = int(offs[-1])
+    for grads in (rand_grads(K, n, dtype, seed=810), _cancelling_set(K, n, dtype, seed=811)):
+        keep = [g.clone() for g in grads]
+        ags.reduce(grads, offs, out=grads[5])
+        torch.cuda.synchronize()
+        check_against_oracle(keep, offs, grads[5])
