@@ -19,7 +19,11 @@
  *     the library copies the descriptor arrays before it returns, so the caller may
  *     free or reuse them at once;
  *   - are asynchronous and stream-ordered on `stream` (a cudaStream_t; NULL means the
- *     legacy default stream).  They return once the work is enqueued;
+ *     legacy default stream).  They return once the work is enqueued.  A call whose
+ *     segment layout (offsets, K, dtype) was seen by an earlier call on the device, and
+ *     whose workspace need that call already met, enqueues only memsets and kernels, so
+ *     it can be captured in a CUDA graph (the first call with a new layout uploads its
+ *     plan synchronously and may grow the workspace: make it before capturing);
  *   - never modify the gradient buffers (unless `out` is one of them) and never
  *     allocate or free caller memory; the library keeps its own per-device workspace,
  *     grown on demand with cudaMalloc and reused by later calls (see Workspace below);
@@ -35,7 +39,9 @@
  * fp32 products (exact for bf16 inputs) in fp32 partial sums of bounded length, then
  * combined across warps and tiles with compensated fp32 sums, in a fixed order, so
  * results are bitwise reproducible run to run.  The tree coefficients are computed in
- * fp64.
+ * double-float arithmetic (pairs of fp32 values, about 48 significant bits); segments of
+ * at most 32 positions, and segments whose error estimate flags them, are evaluated in
+ * vector space in double-float or fp64 (see adasum_recomputed_segments).
  *
  * Alignment: buffers aligned to 16 bytes take the vectorised path; others are accepted
  * and take a scalar-load path inside the same kernels (slower, same results).
