@@ -142,6 +142,10 @@ struct Workspace {
   std::list<Plan> plans;            // most recently used first
   int* last_flag_counts = nullptr;  // device counters of the last call's fp64 lists
   int* d_error = nullptr;           // device status word (bounded waits), kept for good
+  // a second stream for the tiny-segment kernel, forked from and joined back into the
+  // caller's stream within every call
+  cudaStream_t side = nullptr;
+  cudaEvent_t fork_ev = nullptr, join_ev = nullptr;
 };
 
 std::vector<Workspace> g_ws;
@@ -862,8 +866,29 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
     return a;
   };
 
-  // Tiny segments: one warp each.
+  // Tiny segments: one warp each, on the side stream.  The launch is a single wave of
+  // latency-bound warps (a K = 64 segment takes ~100 us), so it runs concurrently with
+  // the rest of the call instead of ahead of it; it is joined back before the call ends.
+  // (every return from here on, error or not, first makes `stream` wait for the side)
+  struct JoinGuard {
+    cudaStream_t stream;
+    cudaEvent_t ev = nullptr;
+    ~JoinGuard() {
+      if (ev != nullptr) cudaStreamWaitEvent(stream, ev, 0);
+    }
+  } join{stream};
   if (plan->tiny_count > 0) {
+    if (ws.side == nullptr) {
+      if (cudaStreamCreateWithFlags(&ws.side, cudaStreamNonBlocking) != cudaSuccess ||
+          cudaEventCreateWithFlags(&ws.fork_ev, cudaEventDisableTiming) != cudaSuccess ||
+          cudaEventCreateWithFlags(&ws.join_ev, cudaEventDisableTiming) != cudaSuccess) {
+        cudaGetLastError();
+        return ADASUM_ERR_CUDA;
+      }
+    }
+    if (cudaEventRecord(ws.fork_ev, stream) != cudaSuccess ||
+        cudaStreamWaitEvent(ws.side, ws.fork_ev, 0) != cudaSuccess)
+      return ADASUM_ERR_CUDA;
     TinyArgs ta;
     std::memset(&ta, 0, sizeof ta);
     for (int k = 0; k < K; ++k) ta.in[k] = grads[k];
@@ -872,8 +897,11 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
     ta.list = plan->d_tiny;
     ta.count = plan->tiny_count;
     ta.K = K;
-    if (adasum_status_t st = launch_one(stream, [&](const char** n) { return launch_tiny_df(ta, dtype, stream, n); }))
-      return st;
+    const adasum_status_t st_tiny =
+        launch_one(ws.side, [&](const char** n) { return launch_tiny_df(ta, dtype, ws.side, n); });
+    if (cudaEventRecord(ws.join_ev, ws.side) != cudaSuccess) return ADASUM_ERR_CUDA;
+    join.ev = ws.join_ev;
+    if (st_tiny) return st_tiny;
   }
   // Small segments: whole tree on chip, one launch per cluster size.
   if (plan->onchip_K > 0) {
@@ -1199,6 +1227,11 @@ adasum_status_t adasum_release_workspace(void) {
   ws.last_flag_counts = nullptr;
   for (auto& p : ws.plans) free_plan(p);
   ws.plans.clear();
+  if (ws.side) cudaStreamDestroy(ws.side);
+  if (ws.fork_ev) cudaEventDestroy(ws.fork_ev);
+  if (ws.join_ev) cudaEventDestroy(ws.join_ev);
+  ws.side = nullptr;
+  ws.fork_ev = ws.join_ev = nullptr;
   return ADASUM_OK;
 }
 

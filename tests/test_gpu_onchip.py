@@ -250,3 +250,30 @@ def test_in_place_output(native, dtype):
         ags.reduce(grads, offs, out=grads[5])
         torch.cuda.synchronize()
         check_against_oracle(keep, offs, grads[5])
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("K", [8, 64, 256])
+def test_wide_tiny_segments(native, K, dtype):
+    """Hundreds of segments of 33..128 positions next to tiny and larger ones."""
+    rs = np.random.default_rng(830 + K)
+    lengths = list(rs.integers(33, 129, size=400)) + [1, 32, 64, 65, 128, 129, 2000]
+    offs = workloads.offsets_from_numels(lengths)
+    grads = rand_grads(K, int(offs[-1]), dtype, seed=831 + K, corr=0.4)
+    out = ags.reduce(grads, offs)
+    torch.cuda.synchronize()
+    check_against_oracle(grads, offs, out)
+
+
+def test_wide_tiny_segments_cancelling_and_symmetric(native):
+    rs = np.random.default_rng(840)
+    lengths = list(rs.integers(33, 129, size=400))
+    offs = workloads.offsets_from_numels(lengths)
+    n = int(offs[-1])
+    grads = _cancelling_set(16, n, torch.float32, seed=841)
+    out = ags.reduce(grads, offs)
+    torch.cuda.synchronize()
+    check_against_oracle(grads, offs, out)
+    a, b = grads[0], grads[1]
+    assert torch.equal(ags.reduce([a, b], offs), ags.reduce([b, a], offs))
+    assert torch.equal(ags.reduce(grads[8:] + grads[:8], offs), out)   # sibling swap
