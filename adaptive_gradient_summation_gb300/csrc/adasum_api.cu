@@ -14,6 +14,7 @@
 #include <atomic>
 #include <cstdint>
 #include <cstring>
+#include <functional>
 #include <list>
 #include <mutex>
 #include <string>
@@ -135,6 +136,35 @@ struct Plan {
   int rc_count[5] = {0, 0, 0, 0, 0};
 };
 
+// A stream of the workspace with the two events that fork it from the caller's stream
+// and join it back (created on first use, destroyed by adasum_release_workspace).
+struct SideStream {
+  cudaStream_t stream = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+
+  // `side` waits for everything enqueued on `caller` so far.
+  adasum_status_t fork_from(cudaStream_t caller) {
+    if (stream == nullptr) {
+      if (cudaStreamCreateWithFlags(&stream, cudaStreamNonBlocking) != cudaSuccess ||
+          cudaEventCreateWithFlags(&fork, cudaEventDisableTiming) != cudaSuccess ||
+          cudaEventCreateWithFlags(&join, cudaEventDisableTiming) != cudaSuccess) {
+        cudaGetLastError();
+        return ADASUM_ERR_CUDA;
+      }
+    }
+    if (cudaEventRecord(fork, caller) != cudaSuccess || cudaStreamWaitEvent(stream, fork, 0) != cudaSuccess)
+      return ADASUM_ERR_CUDA;
+    return ADASUM_OK;
+  }
+  void destroy() {
+    if (stream) cudaStreamDestroy(stream);
+    if (fork) cudaEventDestroy(fork);
+    if (join) cudaEventDestroy(join);
+    stream = nullptr;
+    fork = join = nullptr;
+  }
+};
+
 struct Workspace {
   int device = -1;
   void* buf = nullptr;
@@ -142,10 +172,9 @@ struct Workspace {
   std::list<Plan> plans;            // most recently used first
   int* last_flag_counts = nullptr;  // device counters of the last call's fp64 lists
   int* d_error = nullptr;           // device status word (bounded waits), kept for good
-  // a second stream for the tiny-segment kernel, forked from and joined back into the
-  // caller's stream within every call
-  cudaStream_t side = nullptr;
-  cudaEvent_t fork_ev = nullptr, join_ev = nullptr;
+  // two more streams, each forked from and joined back into the caller's stream within
+  // a call: [0] the tiny-segment kernel, [1] the recompute of flagged segments
+  SideStream side[2];
 };
 
 std::vector<Workspace> g_ws;
@@ -581,10 +610,12 @@ adasum_status_t launch_one(cudaStream_t stream, F&& f) {
 }
 
 // fp32 pass of one stage (all groups): Gram partials, chunk sums, coefficients with the
-// conditioning check, combine (flagged segments are skipped and left to the fp64 path).
-adasum_status_t run_stage(StageArgs& a, int in_dtype, int out_dtype, int momentum,
-                          cudaStream_t stream) {
-  if (a.ntiles == 0) return ADASUM_OK;  // every segment went to the small-segment kernels
+// conditioning check, then `before_combine` (when given), then the combine (flagged
+// segments are skipped and left to the recompute).
+adasum_status_t run_stage(StageArgs& a, int in_dtype, int out_dtype, int momentum, cudaStream_t stream,
+                          const std::function<adasum_status_t()>& before_combine) {
+  if (a.ntiles == 0)  // every segment went to the small-segment kernels
+    return before_combine ? before_combine() : ADASUM_OK;
   if (a.Kg > 1) {
     if (a.tile_list == nullptr || a.ntile_list > 0) {
       if (adasum_status_t st = launch_one(stream, [&](const char** n) {
@@ -605,6 +636,8 @@ adasum_status_t run_stage(StageArgs& a, int in_dtype, int out_dtype, int momentu
     if (adasum_status_t st = launch_one(stream, [&](const char** n) { return launch_coef(a, stream, n); }))
       return st;
   }
+  if (before_combine)
+    if (adasum_status_t st = before_combine()) return st;
   return launch_one(stream, [&](const char** n) {
     return in_dtype == kBF16 ? launch_combine_bf16in(a, out_dtype, momentum, stream, n)
                              : launch_combine_f32in(a, out_dtype, momentum, stream, n);
@@ -866,29 +899,36 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
     return a;
   };
 
-  // Tiny segments: one warp each, on the side stream.  The launch is a single wave of
-  // latency-bound warps (a K = 64 segment takes ~100 us), so it runs concurrently with
-  // the rest of the call instead of ahead of it; it is joined back before the call ends.
-  // (every return from here on, error or not, first makes `stream` wait for the side)
+  // Work on the workspace's side streams is joined back into `stream` before the call
+  // returns, on every path (errors included): the guard records each forked side
+  // stream's join event and makes `stream` wait for it.
   struct JoinGuard {
-    cudaStream_t stream;
-    cudaEvent_t ev = nullptr;
-    ~JoinGuard() {
-      if (ev != nullptr) cudaStreamWaitEvent(stream, ev, 0);
-    }
-  } join{stream};
-  if (plan->tiny_count > 0) {
-    if (ws.side == nullptr) {
-      if (cudaStreamCreateWithFlags(&ws.side, cudaStreamNonBlocking) != cudaSuccess ||
-          cudaEventCreateWithFlags(&ws.fork_ev, cudaEventDisableTiming) != cudaSuccess ||
-          cudaEventCreateWithFlags(&ws.join_ev, cudaEventDisableTiming) != cudaSuccess) {
-        cudaGetLastError();
+    cudaStream_t caller;
+    SideStream* forked[2] = {nullptr, nullptr};
+    adasum_status_t join(int i) {
+      if (forked[i] == nullptr) return ADASUM_OK;
+      SideStream& sd = *forked[i];
+      forked[i] = nullptr;
+      if (cudaEventRecord(sd.join, sd.stream) != cudaSuccess || cudaStreamWaitEvent(caller, sd.join, 0) != cudaSuccess)
         return ADASUM_ERR_CUDA;
-      }
+      return ADASUM_OK;
     }
-    if (cudaEventRecord(ws.fork_ev, stream) != cudaSuccess ||
-        cudaStreamWaitEvent(ws.side, ws.fork_ev, 0) != cudaSuccess)
-      return ADASUM_ERR_CUDA;
+    adasum_status_t fork(SideStream& sd, int i) {
+      if (adasum_status_t st = sd.fork_from(caller)) return st;
+      forked[i] = &sd;
+      return ADASUM_OK;
+    }
+    ~JoinGuard() {
+      join(0);
+      join(1);
+    }
+  } joins{stream};
+
+  // Tiny segments: one warp each, on side stream 0.  The launch is a single wave of
+  // latency-bound warps (a K = 64 segment takes ~100 us), so it runs concurrently with
+  // the rest of the call instead of ahead of it.
+  if (plan->tiny_count > 0) {
+    if (adasum_status_t st = joins.fork(ws.side[0], 0)) return st;
     TinyArgs ta;
     std::memset(&ta, 0, sizeof ta);
     for (int k = 0; k < K; ++k) ta.in[k] = grads[k];
@@ -897,11 +937,10 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
     ta.list = plan->d_tiny;
     ta.count = plan->tiny_count;
     ta.K = K;
-    const adasum_status_t st_tiny =
-        launch_one(ws.side, [&](const char** n) { return launch_tiny_df(ta, dtype, ws.side, n); });
-    if (cudaEventRecord(ws.join_ev, ws.side) != cudaSuccess) return ADASUM_ERR_CUDA;
-    join.ev = ws.join_ev;
-    if (st_tiny) return st_tiny;
+    cudaStream_t side = ws.side[0].stream;
+    if (adasum_status_t st =
+            launch_one(side, [&](const char** n) { return launch_tiny_df(ta, dtype, side, n); }))
+      return st;
   }
   // Small segments: whole tree on chip, one launch per cluster size.
   if (plan->onchip_K > 0) {
@@ -983,6 +1022,95 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
         }))
       return st;
   }
+  // Recompute of the flagged segments, enqueued on `ts` (usually nothing is flagged and
+  // every kernel returns at once).  It needs the last stage's flags and nothing that the
+  // last combine writes: that combine skips the flagged segments, and these kernels write
+  // only the flagged segments' elements (edges masked per element), so the two run
+  // concurrently.
+  auto enqueue_recompute = [&](cudaStream_t ts) -> adasum_status_t {
+    // (the lists' lengths are on the device: enough CTAs for many flagged tiles, the
+    // surplus returns at once)
+    const int grid64 = std::max(1, std::min(plan->ntiles, 16 * num_sms));
+    {
+      StageArgs a = make_args(0);
+      if (adasum_status_t st = launch_one(ts, [&](const char** n) {
+            return launch_collect(a, std::max(1, std::min((L + kThreads - 1) / kThreads, 4 * num_sms)),
+                                  ts, n);
+          }))
+        return st;
+    }
+    // flagged segments that fit: the on-chip kernel's recompute, one launch per cluster size
+    // (the lists' lengths are on the device; surplus clusters return at once)
+    for (int c = 0; c < 5 && plan->rc_cmax > 0; ++c) {
+      if (plan->rc_count[c] == 0) continue;
+      OnchipArgs oa;
+      std::memset(&oa, 0, sizeof oa);
+      for (int k = 0; k < K; ++k) oa.in[k] = grads[k];
+      oa.out = out;
+      oa.segs = plan->d_segs;
+      oa.P = onchip_positions(K);
+      oa.aligned = all_aligned ? 1 : 0;
+      oa.error = ws.d_error;
+      oa.recomputed = list_count + 3;
+      oa.spin_budget = 2000000000LL;
+      oa.list = reinterpret_cast<int*>(base + o_oclist) + static_cast<size_t>(c) * L;
+      oa.dev_count = oc_count + c;
+      oa.recompute_only = 1;
+      if (adasum_status_t st = launch_one(ts, [&](const char** n) {
+            return launch_onchip(oa, dtype, K, plan->rc_count[c], 1 << c, ts, n);
+          }))
+        return st;
+    }
+    {
+      // the scale of every flagged segment's Gram (from the stage-0 inputs)
+      StageArgs a = make_args(0);
+      for (int k = 0; k < K; ++k) a.in[k] = grads[k];
+      if (adasum_status_t st = launch_one(ts, [&](const char** n) {
+            return launch_segmax(a, dtype, grid64, ts, n);
+          }))
+        return st;
+    }
+    if (!plan->tiny_on) {  // (with the warp kernel on, no tiled segment is that short)
+      // flagged segments of at most kTinySeg positions: the whole tree, vector space
+      StageArgs a = make_args(kg.size() - 1);
+      for (int k = 0; k < K; ++k) a.in[k] = grads[k];
+      a.out[0] = out;
+      if (adasum_status_t st = launch_one(ts, [&](const char** n) {
+            return launch_tiny64(a, dtype, dtype, mom ? 1 : 0, grid64, ts, n);
+          }))
+        return st;
+    }
+    for (size_t s = 0; s < kg.size(); ++s) {
+      const bool last = s + 1 == kg.size();
+      StageArgs a = make_args(s);
+      if (s == 0) {
+        for (int k = 0; k < K; ++k) a.in[k] = grads[k];
+      } else {
+        for (int i = 0; i < groups[s] * kg[s]; ++i)
+          a.in[i] = base + off64[s - 1] + i * inter64;
+        a.in_f64 = 1;
+      }
+      if (last) {
+        a.out[0] = out;
+      } else {
+        for (int q = 0; q < groups[s]; ++q)
+          a.out[q] = base + off64[s] + q * inter64;
+        a.out_f64 = 1;
+      }
+      const int in_dt = s == 0 ? dtype : kF32;
+      const int out_dt = last ? dtype : kF32;
+      if (adasum_status_t st = run_stage64(a, in_dt, out_dt, (last && mom) ? 1 : 0, grid64, ts))
+        return st;
+    }
+    return ADASUM_OK;
+  };
+  // side stream 1: forked once the last stage's coefficients (and flags) are known
+  auto fork_recompute = [&]() -> adasum_status_t {
+    if (adasum_status_t st = joins.fork(ws.side[1], 1)) return st;
+    return enqueue_recompute(ws.side[1].stream);
+  };
+  if (route != kRouteKernels)
+    if (adasum_status_t st = fork_recompute()) return st;
   for (size_t s = 0; s < kg.size() && route == kRouteKernels; ++s) {
     const bool last = s + 1 == kg.size();
     StageArgs a = make_args(s);
@@ -1001,85 +1129,13 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
     a.skip_flagged = 1;
     const int in_dt = s == 0 ? dtype : kF32;
     const int out_dt = last ? dtype : kF32;
-    if (adasum_status_t st = run_stage(a, in_dt, out_dt, (last && mom) ? 1 : 0, stream)) return st;
+    if (adasum_status_t st = run_stage(a, in_dt, out_dt, (last && mom) ? 1 : 0, stream,
+                                       last ? fork_recompute : std::function<adasum_status_t()>()))
+      return st;
   }
 
-  // fp64 recompute of the flagged segments (usually none: every kernel returns at once).
-  // (the lists' lengths are on the device: enough CTAs for many flagged tiles, the
-  // surplus returns at once)
-  const int grid64 = std::max(1, std::min(plan->ntiles, 16 * num_sms));
-  {
-    StageArgs a = make_args(0);
-    if (adasum_status_t st = launch_one(stream, [&](const char** n) {
-          return launch_collect(a, std::max(1, std::min((L + kThreads - 1) / kThreads, 4 * num_sms)),
-                                stream, n);
-        }))
-      return st;
-  }
-  // flagged segments that fit: the on-chip kernel's recompute, one launch per cluster size
-  // (the lists' lengths are on the device; surplus clusters return at once)
-  for (int c = 0; c < 5 && plan->rc_cmax > 0; ++c) {
-    if (plan->rc_count[c] == 0) continue;
-    OnchipArgs oa;
-    std::memset(&oa, 0, sizeof oa);
-    for (int k = 0; k < K; ++k) oa.in[k] = grads[k];
-    oa.out = out;
-    oa.segs = plan->d_segs;
-    oa.P = onchip_positions(K);
-    oa.aligned = all_aligned ? 1 : 0;
-    oa.error = ws.d_error;
-    oa.recomputed = list_count + 3;
-    oa.spin_budget = 2000000000LL;
-    oa.list = reinterpret_cast<int*>(base + o_oclist) + static_cast<size_t>(c) * L;
-    oa.dev_count = oc_count + c;
-    oa.recompute_only = 1;
-    if (adasum_status_t st = launch_one(stream, [&](const char** n) {
-          return launch_onchip(oa, dtype, K, plan->rc_count[c], 1 << c, stream, n);
-        }))
-      return st;
-  }
-  {
-    // the scale of every flagged segment's Gram (from the stage-0 inputs)
-    StageArgs a = make_args(0);
-    for (int k = 0; k < K; ++k) a.in[k] = grads[k];
-    if (adasum_status_t st = launch_one(stream, [&](const char** n) {
-          return launch_segmax(a, dtype, grid64, stream, n);
-        }))
-      return st;
-  }
-  if (!plan->tiny_on) {  // (with the warp kernel on, no tiled segment is that short)
-    // flagged segments of at most kTinySeg positions: the whole tree, vector space
-    StageArgs a = make_args(kg.size() - 1);
-    for (int k = 0; k < K; ++k) a.in[k] = grads[k];
-    a.out[0] = out;
-    if (adasum_status_t st = launch_one(stream, [&](const char** n) {
-          return launch_tiny64(a, dtype, dtype, mom ? 1 : 0, grid64, stream, n);
-        }))
-      return st;
-  }
-  for (size_t s = 0; s < kg.size(); ++s) {
-    const bool last = s + 1 == kg.size();
-    StageArgs a = make_args(s);
-    if (s == 0) {
-      for (int k = 0; k < K; ++k) a.in[k] = grads[k];
-    } else {
-      for (int i = 0; i < groups[s] * kg[s]; ++i)
-        a.in[i] = base + off64[s - 1] + i * inter64;
-      a.in_f64 = 1;
-    }
-    if (last) {
-      a.out[0] = out;
-    } else {
-      for (int q = 0; q < groups[s]; ++q)
-        a.out[q] = base + off64[s] + q * inter64;
-      a.out_f64 = 1;
-    }
-    const int in_dt = s == 0 ? dtype : kF32;
-    const int out_dt = last ? dtype : kF32;
-    if (adasum_status_t st = run_stage64(a, in_dt, out_dt, (last && mom) ? 1 : 0, grid64, stream))
-      return st;
-  }
   if (ortho != nullptr) {
+    if (adasum_status_t st = joins.join(1)) return st;  // the recompute's norms
     if (adasum_status_t st = launch_one(stream, [&](const char** n) {
           return launch_orthogonality(reinterpret_cast<double*>(base + o_onorm),
                                       reinterpret_cast<double*>(base + o_diag), groups[0], L,
@@ -1227,11 +1283,7 @@ adasum_status_t adasum_release_workspace(void) {
   ws.last_flag_counts = nullptr;
   for (auto& p : ws.plans) free_plan(p);
   ws.plans.clear();
-  if (ws.side) cudaStreamDestroy(ws.side);
-  if (ws.fork_ev) cudaEventDestroy(ws.fork_ev);
-  if (ws.join_ev) cudaEventDestroy(ws.join_ev);
-  ws.side = nullptr;
-  ws.fork_ev = ws.join_ev = nullptr;
+  for (auto& s : ws.side) s.destroy();
   return ADASUM_OK;
 }
 
