@@ -95,13 +95,13 @@ struct StageArgs {
   int* list_tiny;             // flagged segments of at most kTinySeg positions, list_count[2]
   int* list_count;            // [3]
   int* seg_exp;               // [nsegs] 1024 + exponent of the segment's largest |input| (0: all zero)
-  // Flagged segments that fit the on-chip kernel (plain reductions of up to 64 workers)
-  // are listed per cluster size for its recompute instead of the fp64 path.
+  // Flagged segments that fit the on-chip kernel's clusters of oc_cmax CTAs (plain
+  // reductions of up to 64 workers) are listed for its recompute instead of the fp64 path.
   int oc_vecs;                // 16-byte vectors per CTA (0: none go there)
   int oc_vw;                  // elements per 16-byte vector
-  int oc_cmax;                // largest cluster
-  int* oc_list;               // [5][nsegs]
-  int* oc_count;              // [5]
+  int oc_cmax;                // cluster size of the recompute launch
+  int* oc_list;               // [nsegs]
+  int* oc_count;              // [1]
   int Ktotal;                 // all workers (the tiny-segment recompute runs the whole tree)
   int in_f64;                 // stage inputs are fp64 intermediates
   int out_f64;                // stage outputs are fp64 intermediates
@@ -128,6 +128,11 @@ constexpr double kGramRelErr = 4.0 * 5.9604644775390625e-08;   // 4 u, u = 2^-24
 // cancelling test sets the realised error of the fp32 pass stayed below 0.16 times it,
 // so an estimate of 2.5e-5 keeps the realised error below 4e-6.
 constexpr double kRelErrBudget = 2.5e-5;
+// Factor on the measured coefficient error (coefficient_probe) where it replaces the
+// bound: the measurement follows one direction of the error model at a time, so it is
+// taken 4x.  Over random, correlated, parallel and partly cancelling sets the realised
+// error stayed below 0.08 times the resulting estimate.
+constexpr float kProbeSafety = 4.f;
 // Flagged segments of at most this many positions are recomputed in vector space (the
 // tree level by level on the values themselves, one warp per segment): there, nodes can
 // cancel almost exactly, which a Gram-matrix quadratic form cannot follow even in fp64.
@@ -161,14 +166,14 @@ struct OnchipArgs {
   const void* in[kOnchipMaxK];  // K leaves (K a power of two); null = a zero gradient
   void* out;
   const SegDesc* segs;
-  const int* list;              // the segments of this launch, one per cluster
+  const int* list;              // the segments of this launch, taken in turn by its clusters
   int P;                        // positions per CTA, onchip_positions(K)
   int aligned;                  // every in/out pointer is 16-byte aligned
   int* error;                   // device status word (bit 2: a bulk-copy wait gave up)
   int* recomputed;              // segments recomputed in double-float
   long long spin_budget;        // clock64 cycles of the bulk-copy wait
   int inject_extra_tx;          // test hook: expect 16 bytes that never arrive
-  const int* dev_count;         // when set: clusters at or past *dev_count return at once
+  const int* dev_count;         // when set: the list's length (else one entry per cluster)
   int recompute_only;           // skip the fp32 pass (segments the fp32 pass flagged)
 };
 
@@ -214,6 +219,7 @@ int launch_onchip(const OnchipArgs& a, int dtype, int K, int count, int C, void*
                   const char** name);
 // Largest cluster size (1..16, a power of two) the small-segment kernel can run with.
 int onchip_max_cluster(int dtype, int K);
+int onchip_resident_clusters(int dtype, int K, int C);
 // Tiny segments, one warp each.
 int launch_tiny_df(const TinyArgs& a, int dtype, void* stream, const char** name);
 // fp64 path: build the flagged lists, then Gram / coefficients / combine over them.

@@ -695,6 +695,108 @@ __device__ __forceinline__ df32 df_block_sum(df32 x, int W) {
   return x;
 }
 
+// Integer mixing for the probe's signs (xorshift-multiply rounds; any well-mixing
+// function would do).
+__device__ __forceinline__ uint32_t probe_mix(uint32_t x) {
+  x ^= x >> 16;
+  x *= 0x85EBCA6Bu;
+  x ^= x >> 13;
+  x *= 0xC2B2AE35u;
+  x ^= x >> 16;
+  return x;
+}
+
+// First-order size of the fp32 pass's coefficient error, measured instead of bounded.
+// The bound of coefficient_tree_df adds every error term with its worst sign at every
+// level; for strongly correlated leaves (near-parallel gradients) that compounds to
+// 100-1000x the error the pass really makes.  Here the tree is differentiated (forward
+// mode, fp32) along two perturbations E of the Gram matrix of the size the error model
+// gives each entry,
+//     E_ij = (gram_err s_ij + t_i eps_i + t_j eps_j) |g_i| |g_j|,
+// with signs s_ij, t_i = +-1 hashed from the entries' own values (so that permuting
+// the leaves permutes E with them: mirrored trees get the same answer bitwise), and the
+// output's change |sum_k dc_k g_k| = sqrt(dc^T G dc) is returned relative to |out|
+// (the larger of the two).  Gs is the Gram matrix times sc.  Called by all 32 lanes of
+// one warp; lanes >= KG run with clamped indices and zero weights.
+template <int KG>
+__device__ float coefficient_probe(const df32 (&G)[KG][KG], float sc, const double* eps, float ge) {
+  const int lane = threadIdx.x & 31;
+  const bool on = lane < KG;
+  const int row = on ? lane : 0;
+  auto g = [&](int i, int j) { return G[i][j].hi * sc; };
+  const float grr = fmaxf(g(row, row), 0.f);
+  const float nr = sqrtf(grr), er = on ? static_cast<float>(eps[row]) : 0.f;
+  auto tsign = [&](float gkk, int m) {
+    return (probe_mix(__float_as_uint(gkk) ^ (0x9E3779B9u * static_cast<uint32_t>(m + 1))) & 1u) ? 1.f : -1.f;
+  };
+  const float tr0 = tsign(grr, 0), tr1 = tsign(grr, 1);
+  // E_m(row, j), m = 0, 1
+  auto pert = [&](int j, float grj, float& e0, float& e1) {
+    const float gjj = fmaxf(g(j, j), 0.f);
+    const float ej = static_cast<float>(eps[j]);
+    const uint32_t h = probe_mix(__float_as_uint(grj) ^ probe_mix(__float_as_uint(grr * gjj)));
+    const float nn = nr * sqrtf(gjj);
+    e0 = (ge * ((h & 1u) ? 1.f : -1.f) + tr0 * er + tsign(gjj, 0) * ej) * nn;
+    e1 = (ge * ((h & 2u) ? 1.f : -1.f) + tr1 * er + tsign(gjj, 1) * ej) * nn;
+  };
+  float c = on ? 1.f : 0.f, t0 = 0.f, t1 = 0.f;
+  for (int W = 1; W < KG; W *= 2) {
+    const int self0 = (lane / W) * W, sib0 = self0 ^ W;
+    float gc_s = 0.f, gc_b = 0.f, gt0_b = 0.f, gt1_b = 0.f;
+    float ec0_s = 0.f, ec1_s = 0.f, ec0_b = 0.f, ec1_b = 0.f;
+    for (int j = 0; j < W; ++j) {
+      const int js = (self0 + j) & (KG - 1), jb = (sib0 + j) & (KG - 1);
+      const float cs = __shfl_sync(0xFFFFFFFFu, c, js), cb = __shfl_sync(0xFFFFFFFFu, c, jb);
+      const float t0b = __shfl_sync(0xFFFFFFFFu, t0, jb), t1b = __shfl_sync(0xFFFFFFFFu, t1, jb);
+      const float gs = g(row, js), gb = g(row, jb);
+      float es0, es1, eb0, eb1;
+      pert(js, gs, es0, es1);
+      pert(jb, gb, eb0, eb1);
+      gc_s = fmaf(cs, gs, gc_s);
+      gc_b = fmaf(cb, gb, gc_b);
+      gt0_b = fmaf(t0b, gb, gt0_b);
+      gt1_b = fmaf(t1b, gb, gt1_b);
+      ec0_s = fmaf(cs, es0, ec0_s);
+      ec1_s = fmaf(cs, es1, ec1_s);
+      ec0_b = fmaf(cb, eb0, ec0_b);
+      ec1_b = fmaf(cb, eb1, ec1_b);
+    }
+    // p = c_u^T G c_u and d = c_u^T G c_v with their derivatives; d (and d') as the mean
+    // of the two sides' sums, as in the tree itself
+    const float p = block_lane_sumf(c * gc_s, W);
+    float d = block_lane_sumf(c * gc_b, W);
+    d = 0.5f * (d + __shfl_xor_sync(0xFFFFFFFFu, d, W));
+    const float p0 = block_lane_sumf(fmaf(2.f * t0, gc_s, c * ec0_s), W);
+    const float p1 = block_lane_sumf(fmaf(2.f * t1, gc_s, c * ec1_s), W);
+    float d0 = block_lane_sumf(fmaf(t0, gc_b, c * (gt0_b + ec0_b)), W);
+    float d1 = block_lane_sumf(fmaf(t1, gc_b, c * (gt1_b + ec1_b)), W);
+    d0 = 0.5f * (d0 + __shfl_xor_sync(0xFFFFFFFFu, d0, W));
+    d1 = 0.5f * (d1 + __shfl_xor_sync(0xFFFFFFFFu, d1, W));
+    float a = 1.f, a0 = 0.f, a1 = 0.f;
+    if (p > 0.f) {
+      const float inv2p = 0.5f / p;
+      a = 1.f - d * inv2p;
+      a0 = (d * p0 / p - d0) * inv2p;
+      a1 = (d * p1 / p - d1) * inv2p;
+    }
+    t0 = fmaf(t0, a, c * a0);
+    t1 = fmaf(t1, a, c * a1);
+    c *= a;
+  }
+  float gc = 0.f, gt0 = 0.f, gt1 = 0.f;
+  for (int j = 0; j < KG; ++j) {
+    const float gj = g(row, j);
+    gc = fmaf(__shfl_sync(0xFFFFFFFFu, c, j), gj, gc);
+    gt0 = fmaf(__shfl_sync(0xFFFFFFFFu, t0, j), gj, gt0);
+    gt1 = fmaf(__shfl_sync(0xFFFFFFFFu, t1, j), gj, gt1);
+  }
+  const float P = block_lane_sumf(on ? c * gc : 0.f, 32);
+  const float q0 = block_lane_sumf(on ? t0 * gt0 : 0.f, 32);
+  const float q1 = block_lane_sumf(on ? t1 * gt1 : 0.f, 32);
+  if (!(P > 0.f)) return 1e30f;
+  return sqrtf(fmaxf(fmaxf(q0, q1), 0.f) / P);
+}
+
 // coefficient_tree in double-float arithmetic: the same tree, the same d (sum of the
 // two halves), the same fp32 error estimate, with every fp64 operation of the tree core
 // replaced by its double-float counterpart.  G is the Gram matrix as double-float
@@ -800,8 +902,18 @@ __device__ double coefficient_tree_df(const df32 (&G)[KG][KG], const double* eps
     ill = true;
     return 1e30;
   }
-  const float rel = (D + levels * 5.9604644775390625e-08f * sqrtf(S)) / sqrtf(Pf);
-  return ill ? 1e30 : static_cast<double>(rel);
+  if (ill) return 1e30;
+  const float rnd = levels * 5.9604644775390625e-08f * sqrtf(S);  // the combine's roundings
+  float rel = (D + rnd) / sqrtf(Pf);
+  if (rel > static_cast<float>(kRelErrBudget)) {
+    // The bound asks for a recompute: measure the coefficient error instead (every
+    // lane holds the same rel, so the whole warp takes this branch).  The inputs' own
+    // errors still reach the output directly, through their coefficients.
+    const float direct = sqrtf(block_lane_sumf(cf * cf * e * e * s2, 32));
+    const float probe = coefficient_probe<KG>(G, sc, eps, ge);
+    rel = fminf(rel, kProbeSafety * probe + (direct + rnd) / sqrtf(Pf));
+  }
+  return static_cast<double>(rel);
 }
 
 // The linear recursion g[0,k] = Adasum(g[0,k-1], g_k), k = 1 .. kreal-1, in coefficient
@@ -1240,14 +1352,10 @@ static __global__ void collect_kernel(const StageArgs a) {
     if (a.oc_vecs > 0) {  // small enough for the on-chip kernel's recompute
       const int vw = a.oc_vw;
       const int64_t nv = (sd.start + sd.len + vw - 1) / vw - sd.start / vw;
-      int c = 0;
-      for (int C = 1; C <= a.oc_cmax; C *= 2, ++c) {
-        if ((nv + C - 1) / C <= a.oc_vecs) {
-          a.oc_list[static_cast<size_t>(c) * a.nsegs + atomicAdd(&a.oc_count[c], 1)] = s;
-          break;
-        }
+      if ((nv + a.oc_cmax - 1) / a.oc_cmax <= a.oc_vecs) {
+        a.oc_list[atomicAdd(a.oc_count, 1)] = s;
+        continue;
       }
-      if ((1 << c) <= a.oc_cmax) continue;
     }
     const int base = atomicAdd(&a.list_count[0], sd.ntiles);
     for (int t = 0; t < sd.ntiles; ++t) a.list_tiles[base + t] = sd.first_tile + t;
