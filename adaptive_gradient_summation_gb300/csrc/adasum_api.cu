@@ -131,9 +131,12 @@ struct Plan {
   int nbig = 0, nsmall = 0;
   int* d_big = nullptr;
   int* d_small = nullptr;
-  // tiled segments the on-chip kernel could recompute if flagged, per cluster size
+  // tiled segments the on-chip kernel could recompute if flagged (clusters of rc_cmax
+  // CTAs), and whether any tiled segment is too long for it (else the fp64 path, which
+  // only ever receives those, is not launched)
   int rc_cmax = 0;
-  int rc_count[5] = {0, 0, 0, 0, 0};
+  int rc_count = 0;
+  bool need64 = true;
 };
 
 // A stream of the workspace with the two events that fork it from the caller's stream
@@ -398,7 +401,8 @@ adasum_status_t get_plan(Workspace& ws, const int64_t* offs, int L, int Kg0, int
   std::vector<SegDesc> segs(L);
   std::vector<ChunkDesc> chunks;
   std::vector<int> onchip[5], tiny;
-  int rc_count[5] = {0, 0, 0, 0, 0};
+  int rc_count = 0;
+  bool need64 = false;
   const int64_t VW = dtype == kF32 ? 4 : 8;
   int64_t onchip_vecs = onchip_K > 0 ? onchip_positions(onchip_K) / VW : 0;
   if (onchip_vecs > 0) {
@@ -434,14 +438,12 @@ adasum_status_t get_plan(Workspace& ws, const int64_t* offs, int L, int Kg0, int
         }
       }
     }
-    if (hi > lo && !small && rc_cmax > 0) {
+    if (hi > lo && !small) {
       const int64_t nv = (hi + VW - 1) / VW - lo / VW;
-      const int64_t rc_vecs = onchip_positions(onchip_K) / VW;
-      for (int c = 0, C = 1; C <= rc_cmax && c < 5; ++c, C *= 2)
-        if ((nv + C - 1) / C <= rc_vecs) {
-          ++rc_count[c];
-          break;
-        }
+      if (rc_cmax > 0 && (nv + rc_cmax - 1) / rc_cmax <= onchip_positions(onchip_K) / VW)
+        ++rc_count;
+      else
+        need64 = true;
     }
     if (hi > lo && !small) {
       const int64_t base = lo / 32 * 32;
@@ -477,7 +479,8 @@ adasum_status_t get_plan(Workspace& ws, const int64_t* offs, int L, int Kg0, int
   p.onchip_cmax = onchip_cmax;
   p.onchip_force = onchip_force;
   p.rc_cmax = rc_cmax;
-  for (int c = 0; c < 5; ++c) p.rc_count[c] = rc_count[c];
+  p.rc_count = rc_count;
+  p.need64 = need64 || !tiny_on;
   p.tiny_on = tiny_on;
   p.tiny_count = static_cast<int>(tiny.size());
   std::vector<int> onchip_all, coef_list;
@@ -788,7 +791,7 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
   // One zeroed int region per call: segment flags, the 3 fp64-list counters and the
   // small-segment kernel's recompute counter, and the fused kernel's task counter, chunk
   // counters, segment counters and ready flags, and the recompute's segment scales.
-  const size_t n_ints = static_cast<size_t>(L) + 4 + 1 + plan->nchunks + 3 * static_cast<size_t>(L) + 5;
+  const size_t n_ints = static_cast<size_t>(L) + 4 + 1 + plan->nchunks + 3 * static_cast<size_t>(L) + 1;
   const size_t o_flags = cv.take(n_ints * sizeof(int));
   const size_t o_part = cv.take(max_e_tiles * sizeof(float));
   const size_t o_chunk = cv.take(max_e_chunks * sizeof(double));
@@ -800,7 +803,7 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
   const size_t o_ltiles = cv.take(static_cast<size_t>(plan->ntiles) * sizeof(int));
   const size_t o_lsegs = cv.take(static_cast<size_t>(L) * sizeof(int));
   const size_t o_ltiny = cv.take(static_cast<size_t>(L) * sizeof(int));
-  const size_t o_oclist = cv.take(plan->rc_cmax > 0 ? 5 * static_cast<size_t>(L) * sizeof(int) : 0);
+  const size_t o_oclist = cv.take(plan->rc_cmax > 0 ? static_cast<size_t>(L) * sizeof(int) : 0);
   const size_t o_onorm = cv.take(ortho ? static_cast<size_t>(L) * sizeof(double) : 0);
   const size_t o_diag = cv.take(ortho ? static_cast<size_t>(groups[0]) * L * sizeof(double) : 0);
   const size_t o_slots = cv.take(route == kRouteStream
@@ -1039,10 +1042,12 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
           }))
         return st;
     }
-    // flagged segments that fit: the on-chip kernel's recompute, one launch per cluster size
-    // (the lists' lengths are on the device; surplus clusters return at once)
-    for (int c = 0; c < 5 && plan->rc_cmax > 0; ++c) {
-      if (plan->rc_count[c] == 0) continue;
+    // flagged segments that fit: the on-chip kernel's recompute, one launch of clusters of
+    // rc_cmax CTAs, no more than fit on the device at once (the list's length is on the
+    // device; each cluster takes every rc_clusters-th entry, surplus clusters return at once)
+    if (plan->rc_count > 0) {
+      const int resident = onchip_resident_clusters(dtype, K, plan->rc_cmax);
+      const int rc_clusters = std::max(1, std::min(plan->rc_count, resident));
       OnchipArgs oa;
       std::memset(&oa, 0, sizeof oa);
       for (int k = 0; k < K; ++k) oa.in[k] = grads[k];
@@ -1053,14 +1058,17 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
       oa.error = ws.d_error;
       oa.recomputed = list_count + 3;
       oa.spin_budget = 2000000000LL;
-      oa.list = reinterpret_cast<int*>(base + o_oclist) + static_cast<size_t>(c) * L;
-      oa.dev_count = oc_count + c;
+      oa.list = reinterpret_cast<int*>(base + o_oclist);
+      oa.dev_count = oc_count;
       oa.recompute_only = 1;
       if (adasum_status_t st = launch_one(ts, [&](const char** n) {
-            return launch_onchip(oa, dtype, K, plan->rc_count[c], 1 << c, ts, n);
+            return launch_onchip(oa, dtype, K, rc_clusters, plan->rc_cmax, ts, n);
           }))
         return st;
     }
+    // the fp64 path, for flagged segments too long for the on-chip kernel (not launched
+    // when there are none)
+    if (!plan->need64) return ADASUM_OK;
     {
       // the scale of every flagged segment's Gram (from the stage-0 inputs)
       StageArgs a = make_args(0);

@@ -161,8 +161,22 @@ __global__ void __launch_bounds__(kOnchipThreads, 2) onchip_kernel(const OnchipA
   float* red = reinterpret_cast<float*>(smem + K * rs);   // [SL][NB][B*B]
 
   const uint32_t C = cluster_nctarank(), rank = cluster_ctarank();
-  if (a.dev_count != nullptr && static_cast<int>(cluster_id_x()) >= *a.dev_count) return;  // whole clusters
-  const SegDesc sd = a.segs[a.list[cluster_id_x()]];
+  // cluster i takes list entries i, i + nclusters, ... (all CTAs of a cluster the same)
+  const int nclusters = static_cast<int>(gridDim.x / C);
+  const int nitems = a.dev_count != nullptr ? *a.dev_count : nclusters;
+  if (static_cast<int>(cluster_id_x()) >= nitems) return;  // whole clusters
+  const bool aligned = a.aligned != 0;
+  int xi = 0;  // exchange counter (buffers alternate)
+  if (tid == 0) {
+    mbar_init(&bar, 1);
+    mbar_fence_init();
+  }
+  if (tid < KG1) zeros[tid] = 0.0;
+  uint32_t phase = 0;
+  for (int item = static_cast<int>(cluster_id_x()); item < nitems; item += nclusters, phase ^= 1u) {
+  if (tid == 0) flag = 0;
+  __syncthreads();
+  const SegDesc sd = a.segs[a.list[item]];
   const int64_t s0 = sd.start, s1 = sd.start + sd.len;
   const int64_t vs0 = s0 / VW, vs1 = (s1 + VW - 1) / VW;
   const int64_t chunk = (vs1 - vs0 + C - 1) / C;
@@ -170,18 +184,9 @@ __global__ void __launch_bounds__(kOnchipThreads, 2) onchip_kernel(const OnchipA
   const int64_t cv1 = min(vs1, cv0 + chunk);
   const int nvec = static_cast<int>(cv1 - cv0);            // <= P / VW (host guarantees)
   const int64_t iv0 = max(cv0, (s0 + VW - 1) / VW), iv1 = min(cv1, s1 / VW);  // whole vectors
-  const bool aligned = a.aligned != 0;
   const bool bulk = aligned && iv1 > iv0;
-  int xi = 0;  // exchange counter (buffers alternate)
 
   // ---------------------------------------------------------------- load
-  if (tid == 0) {
-    flag = 0;
-    mbar_init(&bar, 1);
-    mbar_fence_init();
-  }
-  if (tid < KG1) zeros[tid] = 0.0;
-  __syncthreads();
   if (warp == 0) {
     if (lane == 0) {
       uint32_t bytes = 0;
@@ -205,7 +210,7 @@ __global__ void __launch_bounds__(kOnchipThreads, 2) onchip_kernel(const OnchipA
     if (bulk && x != nullptr && v >= iv0 && v < iv1) continue;
     *reinterpret_cast<uint4*>(data + k * rs + j * 16) = load_vec_raw<InTag, kLoadKeep>(x, v, s0, s1, aligned);
   }
-  if (!mbar_wait(&bar, 0, a.spin_budget, a.error)) mbar_wait(&bar, 0, a.spin_budget, a.error);
+  if (!mbar_wait(&bar, phase, a.spin_budget, a.error)) mbar_wait(&bar, phase, a.spin_budget, a.error);
   if (a.recompute_only && tid == 0) flag = 1;
   __syncthreads();
   if (!a.recompute_only) {
@@ -493,7 +498,11 @@ __global__ void __launch_bounds__(kOnchipThreads, 2) onchip_kernel(const OnchipA
       store_df(out, g, rows[p], ex);
     }
   }
-  if (C > 1) cluster_sync_all();  // no CTA leaves while another may still read its shared memory
+  // The next entry's bulk copies overwrite this CTA's shared memory: its own reads come
+  // first (proxy fence), and no CTA moves on (or leaves) while another may still read it.
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  cta_or_cluster_sync(C);
+  }  // list entries
 }
 
 // ------------------------------------------------------------------ tiny segments

@@ -109,38 +109,42 @@ int clusters_for(int K, int C) {
 
 }  // namespace
 
-int onchip_max_cluster(int dtype, int K) {
-  // cached per (device, dtype, K): the answer depends only on the kernel and the device
+// Clusters of C CTAs of the kernel for (dtype, K) that fit on the current device at
+// once, cached per (device, dtype, K, C): the answer depends only on the kernel and the
+// device.  -1 for an unsupported dtype or K or a device query that failed.
+int onchip_resident_clusters(int dtype, int K, int C) {
   static std::mutex mu;
-  static int cache[64][2][7];
+  static int cache[64][2][7][5];
   static bool init = false;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
     cudaGetLastError();
-    return 1;
+    return -1;
   }
-  int kidx = 0;
+  int kidx = 0, cidx = 0;
   for (int k = 2; k < K; k *= 2) ++kidx;
-  if (kidx > 5 || (dtype != kF32 && dtype != kBF16)) return 0;
+  for (int c = 1; c < C; c *= 2) ++cidx;
+  if (kidx > 5 || cidx > 4 || (dtype != kF32 && dtype != kBF16)) return -1;
   std::lock_guard<std::mutex> lock(mu);
   if (!init) {
     for (auto& d : cache)
       for (auto& t : d)
-        for (int& v : t) v = -1;
+        for (auto& k : t)
+          for (int& v : k) v = -1;
     init = true;
   }
-  int& slot = cache[dev][dtype][kidx];
-  if (slot < 0) {
-    slot = 1;
-    for (int C = kOnchipMaxCluster; C >= 2; C /= 2) {
-      const int n = dtype == kF32 ? clusters_for<F32Tag>(K, C) : clusters_for<BF16Tag>(K, C);
-      if (n > 0) {
-        slot = C;
-        break;
-      }
-    }
-  }
+  int& slot = cache[dev][dtype][kidx][cidx];
+  if (slot < 0) slot = dtype == kF32 ? clusters_for<F32Tag>(K, 1 << cidx) : clusters_for<BF16Tag>(K, 1 << cidx);
   return slot;
+}
+
+int onchip_max_cluster(int dtype, int K) {
+  int kidx = 0;
+  for (int k = 2; k < K; k *= 2) ++kidx;
+  if (kidx > 5 || (dtype != kF32 && dtype != kBF16)) return 0;
+  for (int C = kOnchipMaxCluster; C >= 2; C /= 2)
+    if (onchip_resident_clusters(dtype, K, C) > 0) return C;
+  return 1;
 }
 
 int launch_onchip(const OnchipArgs& a, int dtype, int K, int count, int C, void* stream,

@@ -236,6 +236,29 @@ def test_flagged_tiled_segments(native, monkeypatch, K):
 
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("K", [4, 16, 64])
+def test_flagged_segments_share_the_recompute_clusters(native, monkeypatch, K, dtype):
+    """With the fast pass off every segment is tiled; nearly cancelling ones are all
+    recomputed in one launch of the largest clusters.  Short segments leave some CTAs of
+    their cluster without a vector, and there are more flagged segments than clusters fit
+    on the device, so each cluster works through several list entries in turn."""
+    monkeypatch.setenv("ADASUM_ONCHIP", "1")
+    monkeypatch.setenv("ADASUM_ONCHIP_FAST", "0")
+    rs = np.random.default_rng(900 + K)
+    cap16 = 16 * positions_per_cta(K)
+    lengths = [33, 40, 47, 61, 100, 257, cap16 - 9, cap16] + list(rs.integers(33, 3 * TINY * 16, size=300))
+    offs = workloads.offsets_from_numels(lengths)
+    grads = _cancelling_set(K, int(offs[-1]), dtype, seed=910 + K)
+    out = ags.reduce(grads, offs)
+    torch.cuda.synchronize()
+    check_against_oracle(grads, offs, out)
+    assert ags.recomputed_segments() == len(lengths)
+    again = ags.reduce(grads, offs)
+    torch.cuda.synchronize()
+    assert torch.equal(out, again)  # the order clusters take the entries in is not visible
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 def test_in_place_output(native, dtype):
     """out may be one of the gradients: every kernel reads a segment's inputs before it
     writes that segment's output (the recompute rereads level-0 inputs, which the fast
