@@ -566,3 +566,50 @@ def test_cuda_graph_capture_and_replay(native, name, shrink):
         g.replay()
         torch.cuda.synchronize()
         assert torch.equal(out, ref)
+
+
+def _conditioning_sweep(K, n, seed):
+    """Segments of n positions, one per kind: parallel copies (power-of-two and arbitrary
+    scales), correlated sets up to rho = 0.999, mixed magnitudes, and pairs that cancel
+    partly at the first or second level (a fraction e of each vector survives)."""
+    rs = np.random.default_rng(seed)
+    segs = []
+    for _ in range(4):
+        s = rs.standard_normal(n)
+        segs.append([2.0 ** rs.integers(-2, 3) * s for _ in range(K)])
+    s = rs.standard_normal(n)
+    segs.append([rs.uniform(0.1, 10.0) * s for _ in range(K)])
+    for rho in (0.5, 0.9, 0.99, 0.999):
+        s = rs.standard_normal(n)
+        segs.append([rho * s + np.sqrt(1 - rho * rho) * rs.standard_normal(n) for _ in range(K)])
+    s = rs.standard_normal(n)
+    segs.append([10.0 ** rs.uniform(-3, 3) * (0.7 * s + 0.7 * rs.standard_normal(n)) for _ in range(K)])
+    for e in (0.7, 0.5, 0.3, 0.2, 0.1, 0.05):
+        for level in (0, 1):
+            g = []
+            for _ in range(K // 4):
+                a, b = rs.standard_normal(n), rs.standard_normal(n)
+                na = -(1 - e) * a + e * rs.standard_normal(n)
+                nb = -(1 - e) * b + e * rs.standard_normal(n)
+                g += [a, na, b, nb] if level == 0 else [a, b, na, nb]
+            segs.append(g)
+    grads = [torch.tensor(np.concatenate([seg[k] for seg in segs]), dtype=torch.float32, device=DEV)
+             for k in range(K)]
+    return grads, np.arange(len(segs) + 1, dtype=np.int64) * n
+
+
+@pytest.mark.parametrize("K", [16, 64])
+def test_conditioning_check_keeps_every_segment_accurate(native, K):
+    """The conditioning check lets the fp32 pass stand only where its error is far below
+    the tolerance: every segment, recomputed or not, within 4e-6 of the oracle (the
+    tolerance is 1e-5), on sets where the check's bound and its measured replacement
+    differ most (near-parallel, strongly correlated, partly cancelling)."""
+    grads, offs = _conditioning_sweep(K, 3000, seed=60 + K)
+    out = ags.reduce(grads, offs)
+    torch.cuda.synchronize()
+    ref = oracle_reduce(grads, offs)["out64"]
+    got = to_f64(out)
+    for s in range(len(offs) - 1):
+        lo, hi = int(offs[s]), int(offs[s + 1])
+        err = np.linalg.norm(got[lo:hi] - ref[lo:hi]) / np.linalg.norm(ref[lo:hi])
+        assert err <= 4e-6, (s, err)
