@@ -706,6 +706,34 @@ __device__ __forceinline__ uint32_t probe_mix(uint32_t x) {
   return x;
 }
 
+// Shared scratch of coefficient_tree_df<KG> (and of its probe), in floats: two node-Gram
+// buffers for each of three fp32 (or two double-float) matrices, and three per-node
+// arrays.
+__host__ __device__ constexpr int tree_scratch_floats(int KG) {
+  return 3 * ((KG / 2) * (KG / 2) + (KG / 4) * (KG / 4)) + 3 * KG;
+}
+
+// Sum over the 32 lanes in the order of the tree itself: siblings (lanes 2i, 2i+1)
+// first, then pairs of those, ... -- so swapping the children of any tree node swaps
+// the operands of one addition and leaves the sum bitwise unchanged.  Every lane gets it.
+__device__ __forceinline__ float tree_lane_sumf(float x) {
+  for (int off = 1; off < 32; off <<= 1) x += __shfl_xor_sync(0xFFFFFFFFu, x, off);
+  return x;
+}
+
+// Next level's node Gram entry (p, q), p <= q, from this level's entries of the four
+// children a = 2p, b = 2p+1, a' = 2q, b' = 2q+1 with coefficients al, be, al2, be2:
+//   H'(p,q) = (al al2 H(a,a') + be be2 H(b,b')) + (al be2 H(a,b') + be al2 H(b,a')).
+// The grouping pairs each term with its image under a swap of either node's children,
+// and every product is formed coefficient-times-coefficient first, so mirrored trees
+// (and the transposed entry) give bitwise the same value.
+template <typename T, typename Mul, typename Add>
+__device__ __forceinline__ T node_gram_entry(T al, T be, T al2, T be2, T haa, T hbb, T hab, T hba, Mul mul,
+                                             Add add) {
+  return add(add(mul(mul(al, al2), haa), mul(mul(be, be2), hbb)),
+             add(mul(mul(al, be2), hab), mul(mul(be, al2), hba)));
+}
+
 // First-order size of the fp32 pass's coefficient error, measured instead of bounded.
 // The bound of coefficient_tree_df adds every error term with its worst sign at every
 // level; for strongly correlated leaves (near-parallel gradients) that compounds to
@@ -714,101 +742,146 @@ __device__ __forceinline__ uint32_t probe_mix(uint32_t x) {
 // gives each entry,
 //     E_ij = (gram_err s_ij + t_i eps_i + t_j eps_j) |g_i| |g_j|,
 // with signs s_ij, t_i = +-1 hashed from the entries' own values (so that permuting
-// the leaves permutes E with them: mirrored trees get the same answer bitwise), and the
-// output's change |sum_k dc_k g_k| = sqrt(dc^T G dc) is returned relative to |out|
-// (the larger of the two).  Gs is the Gram matrix times sc.  Called by all 32 lanes of
-// one warp; lanes >= KG run with clamped indices and zero weights.
+// the leaves permutes E with them), and the output's change |sum_k dc_k g_k| =
+// sqrt(dc^T G dc) is returned relative to |out| (the larger of the two).  The tree runs
+// on node Gram matrices as in coefficient_tree_df, with their derivatives alongside.
+// Called by all 32 lanes of one warp; `scratch` holds tree_scratch_floats(KG) floats.
 template <int KG>
-__device__ float coefficient_probe(const df32 (&G)[KG][KG], float sc, const double* eps, float ge) {
+__device__ float coefficient_probe(const df32 (&G)[KG][KG], float sc, const double* eps, float ge,
+                                   float* scratch) {
+  constexpr int M1 = KG / 2, M2 = KG / 4;
   const int lane = threadIdx.x & 31;
   const bool on = lane < KG;
   const int row = on ? lane : 0;
+  float* hA = scratch;              // H, T0, T1 of even levels: [3][M1*M1]
+  float* hB = hA + 3 * M1 * M1;     // odd levels: [3][M2*M2]
+  float* na = hB + 3 * M2 * M2;     // node coefficient and its two derivatives: [3][KG]
   auto g = [&](int i, int j) { return G[i][j].hi * sc; };
-  const float grr = fmaxf(g(row, row), 0.f);
-  const float nr = sqrtf(grr), er = on ? static_cast<float>(eps[row]) : 0.f;
   auto tsign = [&](float gkk, int m) {
     return (probe_mix(__float_as_uint(gkk) ^ (0x9E3779B9u * static_cast<uint32_t>(m + 1))) & 1u) ? 1.f : -1.f;
   };
-  const float tr0 = tsign(grr, 0), tr1 = tsign(grr, 1);
-  // E_m(row, j), m = 0, 1
-  auto pert = [&](int j, float grj, float& e0, float& e1) {
-    const float gjj = fmaxf(g(j, j), 0.f);
-    const float ej = static_cast<float>(eps[j]);
-    const uint32_t h = probe_mix(__float_as_uint(grj) ^ probe_mix(__float_as_uint(grr * gjj)));
-    const float nn = nr * sqrtf(gjj);
-    e0 = (ge * ((h & 1u) ? 1.f : -1.f) + tr0 * er + tsign(gjj, 0) * ej) * nn;
-    e1 = (ge * ((h & 2u) ? 1.f : -1.f) + tr1 * er + tsign(gjj, 1) * ej) * nn;
+  // leaf-level perturbation E_m(i, j)
+  auto pert = [&](int i, int j, int m) {
+    const float gii = fmaxf(g(i, i), 0.f), gjj = fmaxf(g(j, j), 0.f);
+    const uint32_t h = probe_mix(__float_as_uint(g(i, j)) ^ probe_mix(__float_as_uint(gii * gjj)));
+    const float s = (h >> m) & 1u ? 1.f : -1.f;
+    const float ti = tsign(gii, m) * static_cast<float>(eps[i]), tj = tsign(gjj, m) * static_cast<float>(eps[j]);
+    return (ge * s + (ti + tj)) * (sqrtf(gii) * sqrtf(gjj));
   };
-  float c = on ? 1.f : 0.f, t0 = 0.f, t1 = 0.f;
-  for (int W = 1; W < KG; W *= 2) {
-    const int self0 = (lane / W) * W, sib0 = self0 ^ W;
-    float gc_s = 0.f, gc_b = 0.f, gt0_b = 0.f, gt1_b = 0.f;
-    float ec0_s = 0.f, ec1_s = 0.f, ec0_b = 0.f, ec1_b = 0.f;
-    for (int j = 0; j < W; ++j) {
-      const int js = (self0 + j) & (KG - 1), jb = (sib0 + j) & (KG - 1);
-      const float cs = __shfl_sync(0xFFFFFFFFu, c, js), cb = __shfl_sync(0xFFFFFFFFu, c, jb);
-      const float t0b = __shfl_sync(0xFFFFFFFFu, t0, jb), t1b = __shfl_sync(0xFFFFFFFFu, t1, jb);
-      const float gs = g(row, js), gb = g(row, jb);
-      float es0, es1, eb0, eb1;
-      pert(js, gs, es0, es1);
-      pert(jb, gb, eb0, eb1);
-      gc_s = fmaf(cs, gs, gc_s);
-      gc_b = fmaf(cb, gb, gc_b);
-      gt0_b = fmaf(t0b, gb, gt0_b);
-      gt1_b = fmaf(t1b, gb, gt1_b);
-      ec0_s = fmaf(cs, es0, ec0_s);
-      ec1_s = fmaf(cs, es1, ec1_s);
-      ec0_b = fmaf(cb, eb0, ec0_b);
-      ec1_b = fmaf(cb, eb1, ec1_b);
+  float c = on ? 1.f : 0.f, t0 = 0.f, t1 = 0.f;  // leaf coefficient and its derivatives
+  const float* H = nullptr;  // this level's node Gram and derivatives ([3][m*m]); null: the leaves
+  int m = KG;
+  for (int lvl = 0; m > 1; ++lvl, m >>= 1) {
+    auto h = [&](int k, int i, int j) -> float {
+      return H ? H[k * m * m + i * m + j] : (k == 0 ? g(i, j) : pert(i, j, k - 1));
+    };
+    {
+      const int n = lane < m ? lane : 0, sib = n ^ 1;
+      const float p = h(0, n, n), d = h(0, n, sib);
+      float a = 1.f, a0 = 0.f, a1 = 0.f;
+      if (p > 0.f) {
+        const float inv2p = 0.5f / p;
+        a = 1.f - d * inv2p;
+        a0 = (d * h(1, n, n) / p - h(1, n, sib)) * inv2p;
+        a1 = (d * h(2, n, n) / p - h(2, n, sib)) * inv2p;
+      }
+      if (lane < m) {
+        na[lane] = a;
+        na[KG + lane] = a0;
+        na[2 * KG + lane] = a1;
+      }
     }
-    // p = c_u^T G c_u and d = c_u^T G c_v with their derivatives; d (and d') as the mean
-    // of the two sides' sums, as in the tree itself
-    const float p = block_lane_sumf(c * gc_s, W);
-    float d = block_lane_sumf(c * gc_b, W);
-    d = 0.5f * (d + __shfl_xor_sync(0xFFFFFFFFu, d, W));
-    const float p0 = block_lane_sumf(fmaf(2.f * t0, gc_s, c * ec0_s), W);
-    const float p1 = block_lane_sumf(fmaf(2.f * t1, gc_s, c * ec1_s), W);
-    float d0 = block_lane_sumf(fmaf(t0, gc_b, c * (gt0_b + ec0_b)), W);
-    float d1 = block_lane_sumf(fmaf(t1, gc_b, c * (gt1_b + ec1_b)), W);
-    d0 = 0.5f * (d0 + __shfl_xor_sync(0xFFFFFFFFu, d0, W));
-    d1 = 0.5f * (d1 + __shfl_xor_sync(0xFFFFFFFFu, d1, W));
-    float a = 1.f, a0 = 0.f, a1 = 0.f;
-    if (p > 0.f) {
-      const float inv2p = 0.5f / p;
-      a = 1.f - d * inv2p;
-      a0 = (d * p0 / p - d0) * inv2p;
-      a1 = (d * p1 / p - d1) * inv2p;
+    __syncwarp();
+    if (on) {
+      const int anc = lane >> lvl;
+      const float a = na[anc];
+      t0 = fmaf(t0, a, c * na[KG + anc]);
+      t1 = fmaf(t1, a, c * na[2 * KG + anc]);
+      c *= a;
     }
-    t0 = fmaf(t0, a, c * a0);
-    t1 = fmaf(t1, a, c * a1);
-    c *= a;
+    const int mh = m / 2;
+    float* Hn = (H == hA) ? hB : hA;
+    auto mul = [](float x, float y) { return x * y; };
+    auto add = [](float x, float y) { return x + y; };
+    for (int t = lane; t < mh * (mh + 1) / 2; t += 32) {
+      int pi, qi;
+      tri_unpack(mh, t, pi, qi);
+      const int a = 2 * pi, b = 2 * pi + 1, a2 = 2 * qi, b2 = 2 * qi + 1;
+      const float al = na[a], be = na[b], al2 = na[a2], be2 = na[b2];
+      const float v = node_gram_entry(al, be, al2, be2, h(0, a, a2), h(0, b, b2), h(0, a, b2), h(0, b, a2), mul, add);
+      Hn[pi * mh + qi] = v;
+      Hn[qi * mh + pi] = v;
+      for (int k = 1; k <= 2; ++k) {
+        const float* da = na + k * KG;
+        // derivative of every term x y H: (x' y + x y') H + (x y) H'
+        auto dterm = [&](int x, int y, int i, int j) {
+          return fmaf(da[x] * na[y] + na[x] * da[y], h(0, i, j), (na[x] * na[y]) * h(k, i, j));
+        };
+        const float dv = (dterm(a, a2, a, a2) + dterm(b, b2, b, b2)) + (dterm(a, b2, a, b2) + dterm(b, a2, b, a2));
+        Hn[k * mh * mh + pi * mh + qi] = dv;
+        Hn[k * mh * mh + qi * mh + pi] = dv;
+      }
+    }
+    __syncwarp();
+    H = Hn;
   }
-  float gc = 0.f, gt0 = 0.f, gt1 = 0.f;
+  // |sum_k dc_k g_k|^2 = dc^T G dc, rows summed pairwise in leaf order
+  float r0[KG], r1[KG];
+#pragma unroll
   for (int j = 0; j < KG; ++j) {
     const float gj = g(row, j);
-    gc = fmaf(__shfl_sync(0xFFFFFFFFu, c, j), gj, gc);
-    gt0 = fmaf(__shfl_sync(0xFFFFFFFFu, t0, j), gj, gt0);
-    gt1 = fmaf(__shfl_sync(0xFFFFFFFFu, t1, j), gj, gt1);
+    r0[j] = __shfl_sync(0xFFFFFFFFu, t0, j) * gj;
+    r1[j] = __shfl_sync(0xFFFFFFFFu, t1, j) * gj;
   }
-  const float P = block_lane_sumf(on ? c * gc : 0.f, 32);
-  const float q0 = block_lane_sumf(on ? t0 * gt0 : 0.f, 32);
-  const float q1 = block_lane_sumf(on ? t1 * gt1 : 0.f, 32);
+#pragma unroll
+  for (int w = 1; w < KG; w *= 2)
+#pragma unroll
+    for (int j = 0; j < KG; j += 2 * w) {
+      r0[j] += r0[j + w];
+      r1[j] += r1[j + w];
+    }
+  const float q0 = tree_lane_sumf(on ? t0 * r0[0] : 0.f);
+  const float q1 = tree_lane_sumf(on ? t1 * r1[0] : 0.f);
+  const float P = H ? H[0] : g(0, 0);
   if (!(P > 0.f)) return 1e30f;
   return sqrtf(fmaxf(fmaxf(q0, q1), 0.f) / P);
 }
 
-// coefficient_tree in double-float arithmetic: the same tree, the same d (sum of the
-// two halves), the same fp32 error estimate, with every fp64 operation of the tree core
-// replaced by its double-float counterpart.  G is the Gram matrix as double-float
-// values; the tree runs on G times a power of two that brings the largest squared leaf
-// norm into [0.5, 1) (exact, and harmless: the coefficients are scale-invariant), and
-// P_out (|out|^2) is scaled back.  Lane k < KG receives its coefficient in c_out (fp32,
+// The Adasum tree of one segment in coefficient space, in double-float arithmetic,
+// evaluated by one warp on node Gram matrices.  A node u of the tree is sum_k c_k g_k
+// over its leaves; the nodes of one level have the Gram matrix H(u, v) = u . v (the
+// leaves' is G).  Pairing u = node 2i with its sibling v = node 2i+1:
+//     alpha = 1 - H(u,v) / (2 H(u,u))   (alpha = 1 when H(u,u) == 0: a zero node is a plain sum)
+//     beta  = 1 - H(u,v) / (2 H(v,v))
+// and the next level's node Gram follows from these coefficients and four entries of H
+// (node_gram_entry), so no dot product over the leaves is formed after the first
+// level.  Each leaf's coefficient is the product of its ancestors' alpha or beta.  The
+// tree runs on G times a power of two that brings the largest squared leaf norm into
+// [0.5, 1) (exact, and harmless: the coefficients are scale-invariant); P_out (|out|^2,
+// the root's H) is scaled back.  Lane k < KG receives its coefficient in c_out (fp32,
 // the double-float value rounded once).
+//
+// Alongside, a first-order estimate of the error of the fp32 pass.  Gram entries carry
+// errors of about gram_err |g_i||g_j| (independent, so quadratic forms add them in
+// quadrature), inputs carry relative errors eps (earlier stages), and the combine
+// rounds at each of the log2(K)+1 levels of its pairwise sum.  Per node it follows
+// S = sum c_k^2 |g_k|^2, the coefficient errors dc_k through R = sum dc_k^2 |g_k|^2 and
+// Q = sum |c_k| dc_k |g_k|^2, and E2 = sum c_k^2 eps_k^2 |g_k|^2, with the node's error
+// D = sqrt(R + E2).  When a node's norm is no larger than its own error (cancellation),
+// or the estimated relative error of the output exceeds the budget even after
+// coefficient_probe has measured the coefficient part, the segment is flagged for the
+// recompute.  The estimate needs a few significant digits only, so it runs in fp32.
+//
+// Called by all 32 lanes of one warp.  G and eps are in shared memory (G stored
+// symmetric), scratch is shared, tree_scratch_floats(KG) floats.  Returns (in every
+// lane) the estimated relative output error (1e30 when ill-conditioned).  Swapping the
+// children of any node leaves every result bitwise unchanged.
 template <int KG>
 __device__ double coefficient_tree_df(const df32 (&G)[KG][KG], const double* eps,
-                                      double gram_err, df32* c_sh, float& c_out, bool& ill,
+                                      double gram_err, float* scratch, float& c_out, bool& ill,
                                       double* P_out = nullptr) {
-  static_assert(KG <= 32, "one lane per leaf");
+  static_assert(KG >= 1 && KG <= 16 && (KG & (KG - 1)) == 0, "a power of two, one lane per leaf");
+  constexpr int M1 = KG / 2, M2 = KG / 4;
   const int lane = threadIdx.x & 31;
   const bool on = lane < KG;
   const int row = on ? lane : 0;
@@ -818,78 +891,74 @@ __device__ double coefficient_tree_df(const df32 (&G)[KG][KG], const double* eps
   if (gmax > 0.f) frexpf(gmax, &ex);
   ex = ex < -120 ? -120 : (ex > 120 ? 120 : ex);
   const float sc = ldexpf(1.f, -ex);
-  auto g = [&](int i, int j) { return df32{G[i][j].hi * sc, G[i][j].lo * sc}; };
   const float ge = static_cast<float>(gram_err);
+  df32* hA = reinterpret_cast<df32*>(scratch);  // node Gram of odd levels: [M1][M1]
+  df32* hB = hA + M1 * M1;                        // even levels from 2: [M2][M2]
+  df32* nc = hB + M2 * M2;                        // this level's node coefficients: [KG]
+  // node state (lane n < m holds node n of the current level; the leaves first)
   const float s2 = on ? fmaxf(G[row][row].hi * sc, 0.f) : 0.f;  // |g_k|^2, scaled
   const float e = on ? static_cast<float>(eps[row]) : 0.f;
-  df32 c = {on ? 1.f : 0.f, 0.f};
-  float dc = 0.f;  // estimated error of c
+  float S = s2, Q = 0.f, R = 0.f, E2 = e * e * s2;
+  df32 c = {on ? 1.f : 0.f, 0.f};  // lane k < KG: leaf k's coefficient
   bool bad = false;
-  if (on) c_sh[lane] = c;
-  __syncwarp();
-  for (int W = 1; W < KG; W *= 2) {
-    const int self0 = (lane / W) * W, sib0 = self0 ^ W;
-    df32 row_self = {0.f, 0.f}, row_sib = {0.f, 0.f};
-    if (on) {
-      // even and odd terms in two chains (the same order relative to the block start
-      // for every block, which is what the sibling symmetry needs)
-      df32 se = {0.f, 0.f}, so = {0.f, 0.f}, be = {0.f, 0.f}, bo = {0.f, 0.f};
-      for (int j = 0; j < W; j += 2) {
-        se = df_add(df_mul(c_sh[self0 + j], g(row, self0 + j)), se);
-        be = df_add(df_mul(c_sh[sib0 + j], g(row, sib0 + j)), be);
-        if (j + 1 < W) {
-          so = df_add(df_mul(c_sh[self0 + j + 1], g(row, self0 + j + 1)), so);
-          bo = df_add(df_mul(c_sh[sib0 + j + 1], g(row, sib0 + j + 1)), bo);
-        }
-      }
-      row_self = df_add(se, so);
-      row_sib = df_add(be, bo);
-    }
-    const df32 p_self = df_block_sum(df_mul(c, row_self), W);
-    const df32 d_half = df_block_sum(df_mul(c, row_sib), W);
-    const df32 d = df_add(d_half, df_shfl_xor(d_half, W));
-    const df32 dd = {0.5f * d.hi, 0.5f * d.lo};  // the two halves each hold the full cross term
-    const df32 p_sib = df_shfl_xor(p_self, W);
-    const float cf = c.hi;
-    const float S_self = block_lane_sumf(cf * cf * s2, W);
-    const float D_self = sqrtf(block_lane_sumf((dc * dc + cf * cf * e * e) * s2, W));
-    const float S_sib = __shfl_xor_sync(0xFFFFFFFFu, S_self, W);
-    const float D_sib = __shfl_xor_sync(0xFFFFFFFFu, D_self, W);
-    const float ps = p_self.hi, pb = p_sib.hi;
-    const float n_self = sqrtf(fmaxf(ps, 0.f)), n_sib = sqrtf(fmaxf(pb, 0.f));
-    const float err_p = ge * S_self + 2.f * n_self * D_self;
-    const float err_d = ge * sqrtf(S_self * S_sib) + (n_self * D_sib + n_sib * D_self);
+  const df32* H = nullptr;         // this level's node Gram ([m][m]); null: G
+  int m = KG;
+  for (int lvl = 0; m > 1; ++lvl, m >>= 1) {
+    auto h = [&](int i, int j) -> df32 {
+      return H ? H[i * m + j] : df32{G[i][j].hi * sc, G[i][j].lo * sc};
+    };
+    const bool node = lane < m;
+    const int n = node ? lane : 0, sib = n ^ 1;
+    const df32 p = h(n, n), d = h(n, sib);
+    const float D = sqrtf(R + E2);
+    const float S_sib = __shfl_xor_sync(0xFFFFFFFFu, S, 1);
+    const float D_sib = __shfl_xor_sync(0xFFFFFFFFu, D, 1);
+    const float ps = p.hi, n_self = sqrtf(fmaxf(ps, 0.f)), n_sib = sqrtf(fmaxf(h(sib, sib).hi, 0.f));
+    const float err_p = ge * S + 2.f * n_self * D;
+    const float err_d = ge * sqrtf(S * S_sib) + (n_self * D_sib + n_sib * D);
     df32 coef = {1.f, 0.f};
     float dcoef = 0.f;
     if (ps != 0.f) {
-      coef = df_add(df32{1.f, 0.f}, df_neg(df_div(dd, df32{2.f * p_self.hi, 2.f * p_self.lo})));
+      coef = df_add(df32{1.f, 0.f}, df_neg(df_div(d, df32{2.f * p.hi, 2.f * p.lo})));
       const float ap = fabsf(ps);
-      dcoef = __fdividef(err_d + __fdividef(fabsf(dd.hi) * err_p, ap), 2.f * ap);
-      if (ps <= err_p) bad = true;
-    } else if (S_self > 0.f) {
+      dcoef = __fdividef(err_d + __fdividef(fabsf(d.hi) * err_p, ap), 2.f * ap);
+      if (node && ps <= err_p) bad = true;
+    } else if (node && S > 0.f) {
       bad = true;  // a non-zero subtree cancelled to an exact zero norm
     }
-    if (on) {
-      dc = fmaf(fabsf(coef.hi), dc, fabsf(cf) * dcoef);
-      c = df_mul(c, coef);
+    if (node) nc[lane] = coef;
+    // the parent's state: node n' (lane n' < m/2) from its children 2n', 2n'+1
+    const float a2 = coef.hi * coef.hi, aa = fabsf(coef.hi);
+    const float Sc = a2 * S, Qc = fmaf(aa * dcoef, S, a2 * Q);
+    const float Rc = fmaf(dcoef * dcoef, S, fmaf(2.f * aa * dcoef, Q, a2 * R)), Ec = a2 * E2;
+    const int c0 = (2 * lane) & 31, c1 = (2 * lane + 1) & 31;
+    S = __shfl_sync(0xFFFFFFFFu, Sc, c0) + __shfl_sync(0xFFFFFFFFu, Sc, c1);
+    Q = __shfl_sync(0xFFFFFFFFu, Qc, c0) + __shfl_sync(0xFFFFFFFFu, Qc, c1);
+    R = __shfl_sync(0xFFFFFFFFu, Rc, c0) + __shfl_sync(0xFFFFFFFFu, Rc, c1);
+    E2 = __shfl_sync(0xFFFFFFFFu, Ec, c0) + __shfl_sync(0xFFFFFFFFu, Ec, c1);
+    __syncwarp();
+    if (on) c = df_mul(c, nc[lane >> lvl]);
+    const int mh = m / 2;
+    df32* Hn = (H == hA) ? hB : hA;
+    for (int t = lane; t < mh * (mh + 1) / 2; t += 32) {
+      int pi, qi;
+      tri_unpack(mh, t, pi, qi);
+      const int a = 2 * pi, b = 2 * pi + 1, a2i = 2 * qi, b2i = 2 * qi + 1;
+      const df32 v = node_gram_entry(
+          nc[a], nc[b], nc[a2i], nc[b2i], h(a, a2i), h(b, b2i), h(a, b2i), h(b, a2i),
+          [](df32 x, df32 y) { return df_mul(x, y); }, [](df32 x, df32 y) { return df_add(x, y); });
+      Hn[pi * mh + qi] = v;
+      Hn[qi * mh + pi] = v;
     }
     __syncwarp();
-    if (on) c_sh[lane] = c;
-    __syncwarp();
+    H = Hn;
   }
-  df32 full = {0.f, 0.f};
-  if (on) {
-    df32 fe = {0.f, 0.f}, fo = {0.f, 0.f};
-    for (int j = 0; j < KG; j += 2) {
-      fe = df_add(df_mul(c_sh[j], g(row, j)), fe);
-      if (j + 1 < KG) fo = df_add(df_mul(c_sh[j + 1], g(row, j + 1)), fo);
-    }
-    full = df_add(fe, fo);
-  }
-  const df32 P = df_block_sum(df_mul(c, full), 32);
-  const float cf = c.hi;
-  const float S = block_lane_sumf(cf * cf * s2, 32);
-  const float D = sqrtf(block_lane_sumf((dc * dc + cf * cf * e * e) * s2, 32));
+  // root: lane 0 holds its state; H[0] is |out|^2 (scaled)
+  S = __shfl_sync(0xFFFFFFFFu, S, 0);
+  R = __shfl_sync(0xFFFFFFFFu, R, 0);
+  E2 = __shfl_sync(0xFFFFFFFFu, E2, 0);
+  const df32 P = H ? H[0] : df32{G[0][0].hi * sc, G[0][0].lo * sc};  // (one leaf: its own norm)
+  const float D = sqrtf(R + E2);
   ill = __any_sync(0xFFFFFFFFu, bad);
   c_out = __fadd_rn(c.hi, c.lo);
   if (P_out) *P_out = ldexp(df_to_double(P), ex);
@@ -909,9 +978,9 @@ __device__ double coefficient_tree_df(const df32 (&G)[KG][KG], const double* eps
     // The bound asks for a recompute: measure the coefficient error instead (every
     // lane holds the same rel, so the whole warp takes this branch).  The inputs' own
     // errors still reach the output directly, through their coefficients.
-    const float direct = sqrtf(block_lane_sumf(cf * cf * e * e * s2, 32));
-    const float probe = coefficient_probe<KG>(G, sc, eps, ge);
-    rel = fminf(rel, kProbeSafety * probe + (direct + rnd) / sqrtf(Pf));
+    __syncwarp();
+    const float probe = coefficient_probe<KG>(G, sc, eps, ge, scratch);
+    rel = fminf(rel, kProbeSafety * probe + (sqrtf(E2) + rnd) / sqrtf(Pf));
   }
   return static_cast<double>(rel);
 }
@@ -1005,7 +1074,7 @@ __device__ __forceinline__ void segment_coefficients(const StageArgs& a, int seg
   __shared__ df32 Gd[KG][KG];
   __shared__ double eps[KG];
   __shared__ double snorm[KG];
-  __shared__ df32 c_sh[KG];
+  __shared__ float tree_sh[tree_scratch_floats(KG)];
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     double sum = 0.0;
     const double* p = a.chunk_sums + (static_cast<size_t>(q) * a.nchunks + sd.first_chunk) * E + e;
@@ -1027,7 +1096,7 @@ __device__ __forceinline__ void segment_coefficients(const StageArgs& a, int seg
       rel = coefficient_chain<KG>(G, eps, kGramRelErr, snorm, c, ill, a.Kreal, &P);
     } else {
       float cf = 0.f;
-      rel = coefficient_tree_df<KG>(Gd, eps, kGramRelErr, c_sh, cf, ill, &P);
+      rel = coefficient_tree_df<KG>(Gd, eps, kGramRelErr, tree_sh, cf, ill, &P);
       c = cf;
     }
     if (threadIdx.x == 0 && a.outnorm2) a.outnorm2[seg] = P;

@@ -137,7 +137,6 @@ __global__ void __launch_bounds__(kOnchipThreads, 2) onchip_kernel(const OnchipA
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ df32 G1[NG][KG1][KG1];
   __shared__ df32 G2[NG][NG];
-  __shared__ df32 csh[NG][KG1];
   __shared__ double zeros[KG1];
   __shared__ double rel1[NG];
   __shared__ df32 ab[K / 2][2];
@@ -158,7 +157,8 @@ __global__ void __launch_bounds__(kOnchipThreads, 2) onchip_kernel(const OnchipA
   const int P = a.P;
   const int rs = onchip_row_bytes(P);
   unsigned char* data = smem;                              // K rows of rs bytes
-  float* red = reinterpret_cast<float*>(smem + K * rs);   // [SL][NB][B*B]
+  float* red = reinterpret_cast<float*>(smem + K * rs);   // [SL][NB][B*B]; the trees' scratch after
+  static_assert(NG * tree_scratch_floats(KG1) * 4 <= kOnchipRedBytes, "tree scratch fits the Gram's");
 
   const uint32_t C = cluster_nctarank(), rank = cluster_ctarank();
   // cluster i takes list entries i, i + nclusters, ... (all CTAs of a cluster the same)
@@ -289,7 +289,7 @@ __global__ void __launch_bounds__(kOnchipThreads, 2) onchip_kernel(const OnchipA
       if (q < NG) {
         float c = 0.f;
         bool ill = false;
-        const double rel = coefficient_tree_df<KG1>(G1[q], zeros, kGramRelErr, csh[q], c, ill);
+        const double rel = coefficient_tree_df<KG1>(G1[q], zeros, kGramRelErr, red + q * tree_scratch_floats(KG1), c, ill);
         if (lane < KG1) tcoef[q][lane] = c;
         if (lane == 0) {
           trel[q] = rel;
@@ -370,7 +370,7 @@ __global__ void __launch_bounds__(kOnchipThreads, 2) onchip_kernel(const OnchipA
         if (warp == 0) {
           float c = 0.f;
           bool ill = false;
-          const double rel = coefficient_tree_df<NG>(G2, rel1, kGramRelErr, csh[0], c, ill);
+          const double rel = coefficient_tree_df<NG>(G2, rel1, kGramRelErr, red, c, ill);  // (red is free after stage 1)
           if (lane < NG) t2coef[lane] = c;
           if (lane == 0) t2flag = (ill || !(rel <= kRelErrBudget)) ? 1 : 0;
         }

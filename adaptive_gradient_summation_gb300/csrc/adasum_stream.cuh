@@ -209,7 +209,7 @@ __device__ __forceinline__ void finish_segment(const StageArgs& a, const StreamA
   constexpr int E = tri_count(KG);
   __shared__ df32 G[KG][KG];
   __shared__ double eps[KG];
-  __shared__ df32 snorm[KG];
+  __shared__ float tree_sh[tree_scratch_floats(KG)];
   const int ct = threadIdx.x - 32, lane = threadIdx.x & 31, cw = (threadIdx.x >> 5) - 1;
   const SegDesc sd = a.segs[seg];
   const int nctas = static_cast<int>(gridDim.x);
@@ -242,7 +242,7 @@ __device__ __forceinline__ void finish_segment(const StageArgs& a, const StreamA
   if (ct < 32) {
     float c = 0.f;
     bool ill = false;
-    const double rel = coefficient_tree_df<KG>(G, eps, kGramRelErr, snorm, c, ill);
+    const double rel = coefficient_tree_df<KG>(G, eps, kGramRelErr, tree_sh, c, ill);
     if (ct < KG) a.coef[static_cast<size_t>(seg) * KG + ct] = static_cast<float>(c);
     if (ct == 0) {
       if (a.relerr) a.relerr[seg] = static_cast<float>(fmin(rel, 1e30));
