@@ -23,7 +23,7 @@ LIB_PATH = os.path.join(PKG, LIB_NAME)
 SOURCES = ["adasum_api.cu", "launch_f32.cu", "launch_bf16.cu", "launch_f64.cu",
            "launch_pipe.cu", "launch_stream.cu", "launch_onchip.cu", "adasum_noalloc.cu"]
 HEADERS = ["adasum_internal.h", "adasum_kernels.cuh", "adasum_stream.cuh", "adasum_ptx.cuh",
-           "adasum_onchip.cuh", "adasum_launch.h"]
+           "adasum_onchip.cuh", "adasum_launch.h", "adasum_pair.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",

@@ -178,6 +178,9 @@ struct Workspace {
   // two more streams, each forked from and joined back into the caller's stream within
   // a call: [0] the tiny-segment kernel, [1] the recompute of flagged segments
   SideStream side[2];
+  // the fused pair kernel's partials, grid-barrier words and four zero counters
+  // (allocated and zeroed on its first use)
+  void* pair_buf = nullptr;
 };
 
 std::vector<Workspace> g_ws;
@@ -675,6 +678,66 @@ struct Carver {
   }
 };
 
+// The device status word of the workspace (bounded waits), created on first use.
+adasum_status_t ensure_error_word(Workspace& ws) {
+  if (ws.d_error != nullptr) return ADASUM_OK;
+  if (cudaMalloc(&ws.d_error, sizeof(int)) != cudaSuccess || cudaMemset(ws.d_error, 0, sizeof(int)) != cudaSuccess) {
+    cudaGetLastError();
+    ws.d_error = nullptr;
+    return ADASUM_ERR_NO_MEMORY;
+  }
+  return ADASUM_OK;
+}
+
+// Adasum(a, b) over one segment by the fused pair kernel (adasum_pair.cuh).  Returns
+// false, having enqueued nothing, when the kernel cannot run on this device or the
+// segment is longer than its CTAs hold; else sets *status.
+bool run_pair_fused(Workspace& ws, const void* a, const void* b, int64_t n, int dtype, void* out,
+                    cudaStream_t stream, adasum_status_t* status) {
+  const int cap = std::min(pair_fused_max_grid(dtype), kPairThreads);
+  const int64_t vw = dtype == kF32 ? 4 : 8;
+  const int64_t nv = (n + vw - 1) / vw;
+  const int64_t per_cta = static_cast<int64_t>(kPairThreads) * kPairVecs;
+  if (cap <= 0 || nv > cap * per_cta) return false;  // more than the registers of the CTAs hold
+  // one layout for every call (partials of up to kPairThreads CTAs, then the barrier
+  // words and the zero counters), so that the barrier's state stays where it was
+  const size_t part_bytes = align_up(static_cast<size_t>(kPairThreads) * 8 * sizeof(float), 256);
+  if (ws.pair_buf == nullptr) {
+    const size_t bytes = part_bytes + 256;
+    if (cudaMalloc(&ws.pair_buf, bytes) != cudaSuccess || cudaMemset(ws.pair_buf, 0, bytes) != cudaSuccess) {
+      cudaGetLastError();
+      if (ws.pair_buf) cudaFree(ws.pair_buf);
+      ws.pair_buf = nullptr;
+      *status = ADASUM_ERR_NO_MEMORY;
+      return true;
+    }
+  }
+  if (adasum_status_t st = ensure_error_word(ws)) {
+    *status = st;
+    return true;
+  }
+  const int grid = static_cast<int>(std::max<int64_t>(1, (nv + per_cta - 1) / per_cta));
+  char* base = static_cast<char*>(ws.pair_buf);
+  PairArgs pa;
+  std::memset(&pa, 0, sizeof pa);
+  pa.a = a;
+  pa.b = b;
+  pa.out = out;
+  pa.n = n;
+  pa.aligned = aligned16(a) && aligned16(b) && aligned16(out) ? 1 : 0;
+  pa.partials = reinterpret_cast<float*>(base);
+  pa.bar = reinterpret_cast<unsigned*>(base + part_bytes);
+  pa.error = ws.d_error;
+  pa.spin_budget = 2000000000LL;  // about one second of SM clock
+  if (inject_timeout()) {
+    pa.inject_no_arrival = 1;
+    pa.spin_budget = 200000LL;
+  }
+  *status = launch_one(stream, [&](const char** nm) { return launch_pair_fused(pa, dtype, grid, stream, nm); });
+  ws.last_flag_counts = reinterpret_cast<int*>(base + part_bytes + 64);  // zeros: nothing is recomputed
+  return true;
+}
+
 adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* offs, int L,
                             int dtype, void* out, float* master_w, float* momentum,
                             float lr, float mu, cudaStream_t stream, bool chain = false,
@@ -729,6 +792,14 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
   Workspace& ws = workspace_for(device);
   int num_sms = 148;
   cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, device);
+
+  // Two workers and one segment whose inputs fit well inside L2: one fused kernel
+  // (ADASUM_PAIR_FUSED=0 switches it off, for comparisons).
+  if (K == 2 && Kreal == 2 && L == 1 && !mom && !chain && ortho == nullptr &&
+      requested_route() == kRouteKernels && env_on("ADASUM_PAIR_FUSED", true)) {
+    adasum_status_t st = ADASUM_OK;
+    if (run_pair_fused(ws, grads[0], grads[1], N, dtype, out, stream, &st)) return st;
+  }
 
   // Stage structure: groups of at most 16 workers; K=1 is a single pass-2 "copy".
   std::vector<int> kg;  // workers per group, per stage
@@ -828,14 +899,7 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
   int* seg_ready = seg_done + L;
   int* seg_exp = seg_ready + L;  // the fp64 recompute's per-segment scale
   int* oc_count = seg_exp + L;   // flagged segments listed for the on-chip recompute
-  if (ws.d_error == nullptr) {
-    if (cudaMalloc(&ws.d_error, sizeof(int)) != cudaSuccess ||
-        cudaMemset(ws.d_error, 0, sizeof(int)) != cudaSuccess) {
-      cudaGetLastError();
-      ws.d_error = nullptr;
-      return ADASUM_ERR_NO_MEMORY;
-    }
-  }
+  if (adasum_status_t st = ensure_error_word(ws)) return st;
 
   bool all_aligned = aligned16(out) && (!mom || (aligned16(master_w) && aligned16(momentum)));
   // (aligned16(nullptr) is true: absent buffers do not force the scalar path)
@@ -1292,6 +1356,8 @@ adasum_status_t adasum_release_workspace(void) {
   for (auto& p : ws.plans) free_plan(p);
   ws.plans.clear();
   for (auto& s : ws.side) s.destroy();
+  if (ws.pair_buf) cudaFree(ws.pair_buf);
+  ws.pair_buf = nullptr;
   return ADASUM_OK;
 }
 

@@ -177,6 +177,25 @@ struct OnchipArgs {
   int recompute_only;           // skip the fp32 pass (segments the fp32 pass flagged)
 };
 
+// Two workers, one segment (adasum_pair.cuh): one cooperative kernel with one grid
+// barrier, double-float sums and combine, every thread holding up to kPairVecs 16-byte
+// vectors of each input in registers; segments of up to min(co-resident CTAs,
+// kPairThreads) * kPairThreads * kPairVecs vectors.
+constexpr int kPairThreads = 512;
+constexpr int kPairVecs = 4;
+struct PairArgs {
+  const void* a;
+  const void* b;
+  void* out;                    // may be a or b
+  int64_t n;
+  int aligned;                  // a, b and out are 16-byte aligned
+  float* partials;              // [grid][8]: each CTA's double-float sums and exponent
+  unsigned* bar;                // [2]: grid barrier (arrivals, generation), zero when allocated
+  int* error;                   // device status word (bit 4: the grid barrier gave up)
+  long long spin_budget;        // clock64 cycles of the barrier wait
+  int inject_no_arrival;        // test hook: wait at the barrier without arriving
+};
+
 // Segments of at most kTinyDirect positions (adasum_onchip.cuh): one warp each, the
 // tree on the values themselves in double-float arithmetic.
 constexpr int kTinyDirect = 32;
@@ -220,6 +239,9 @@ int launch_onchip(const OnchipArgs& a, int dtype, int K, int count, int C, void*
 // Largest cluster size (1..16, a power of two) the small-segment kernel can run with.
 int onchip_max_cluster(int dtype, int K);
 int onchip_resident_clusters(int dtype, int K, int C);
+// CTAs of the fused pair kernel that fit on the current device at once (0: none).
+int pair_fused_max_grid(int dtype);
+int launch_pair_fused(const PairArgs& a, int dtype, int grid, void* stream, const char** name);
 // Tiny segments, one warp each.
 int launch_tiny_df(const TinyArgs& a, int dtype, void* stream, const char** name);
 // fp64 path: build the flagged lists, then Gram / coefficients / combine over them.

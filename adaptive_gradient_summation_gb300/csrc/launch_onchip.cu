@@ -6,6 +6,7 @@
 
 #include "adasum_launch.h"
 #include "adasum_onchip.cuh"
+#include "adasum_pair.cuh"
 
 namespace adasum {
 
@@ -164,6 +165,48 @@ int launch_tiny_df(const TinyArgs& a, int dtype, void* stream, const char** name
   }
   *name = "tiny_df<bf16>";
   return launch_pdl(tiny_df_kernel<BF16Tag>, grid, block, 0, s, a);
+}
+
+int pair_fused_max_grid(int dtype) {
+  static std::mutex mu;
+  static int cache[64][2];
+  static bool init = false;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || (dtype != kF32 && dtype != kBF16)) {
+    cudaGetLastError();
+    return 0;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (!init) {
+    for (auto& d : cache) d[0] = d[1] = -1;
+    init = true;
+  }
+  int& slot = cache[dev][dtype];
+  if (slot < 0) {
+    int per_sm = 0, sms = 0;
+    const cudaError_t e1 =
+        dtype == kF32 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, pair_fused_kernel<F32Tag>, kPairThreads, 0)
+                      : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, pair_fused_kernel<BF16Tag>, kPairThreads, 0);
+    const cudaError_t e2 = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e1 != cudaSuccess || e2 != cudaSuccess) {
+      cudaGetLastError();
+      slot = 0;
+    } else {
+      slot = per_sm * sms;
+    }
+  }
+  return slot;
+}
+
+int launch_pair_fused(const PairArgs& a, int dtype, int grid, void* stream, const char** name) {
+  PairArgs copy = a;
+  void* args[] = {&copy};
+  const void* fn = dtype == kF32 ? reinterpret_cast<const void*>(pair_fused_kernel<F32Tag>)
+                                 : reinterpret_cast<const void*>(pair_fused_kernel<BF16Tag>);
+  *name = dtype == kF32 ? "pair_fused<f32>" : "pair_fused<bf16>";
+  const cudaError_t e = cudaLaunchCooperativeKernel(fn, dim3(grid), dim3(kPairThreads), args, 0,
+                                                    static_cast<cudaStream_t>(stream));
+  return static_cast<int>(e);
 }
 
 }  // namespace adasum

@@ -202,6 +202,8 @@ def algorithmic_bytes(kernel: str, wl, out_es: int) -> int:
         if wl.master_w is not None:   # the step writes w and v (fp32), not the output
             return KN * es + 16 * wl.N
         return KN * es + wl.N * out_es
+    if kernel.startswith("pair_fused"):
+        return KN * es + wl.N * out_es      # the whole pair in one kernel: read once, write once
     return 0
 
 
