@@ -71,20 +71,31 @@ __device__ __forceinline__ int pair_block_max(int e, int* sh) {
   return e;
 }
 
-// Double-float sum over the CTA, every term brought to exponent E first: x * 2^(2(e - E)).
-// Fixed order (warp butterfly, then warps in index order); thread 0 gets the result.
-__device__ __forceinline__ df32 pair_block_sum(df32 x, int e, int E, df32* sh) {
+// Double-float sums over the CTA of three values, every term brought to exponent E
+// first: x * 2^(2(e - E)).  A fixed order -- a butterfly within each warp, then one over
+// the warps' sums on the first lanes of warp 0 -- so every CTA that adds the same values
+// gets the same bits.  Thread 0 gets the results in v.
+__device__ __forceinline__ void pair_block_sum3(df32 (&v)[3], int e, int E, df32 (*sh)[kPairThreads / 32]) {
+  constexpr int kW = kPairThreads / 32;
   const float f = ldexpf(1.f, 2 * (e - E));
-  x = {x.hi * f, x.lo * f};
-  for (int off = 16; off > 0; off >>= 1) x = df_add(x, df_shfl_xor(x, off));
+#pragma unroll
+  for (int i = 0; i < 3; ++i) v[i] = {v[i].hi * f, v[i].lo * f};
+  for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+    for (int i = 0; i < 3; ++i) v[i] = df_add(v[i], df_shfl_xor(v[i], off));
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (lane == 0) sh[warp] = x;
+  if (lane == 0)
+#pragma unroll
+    for (int i = 0; i < 3; ++i) sh[i][warp] = v[i];
   __syncthreads();
-  df32 s = {0.f, 0.f};
-  if (threadIdx.x == 0)
-    for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) s = df_add(s, sh[w]);
+  if (warp == 0) {
+#pragma unroll
+    for (int i = 0; i < 3; ++i) v[i] = lane < kW ? sh[i][lane] : df32{0.f, 0.f};
+    for (int off = kW / 2; off > 0; off >>= 1)
+#pragma unroll
+      for (int i = 0; i < 3; ++i) v[i] = df_add(v[i], df_shfl_xor(v[i], off));
+  }
   __syncthreads();
-  return s;
 }
 
 __device__ __forceinline__ df32 pair_coefficient(df32 d, df32 p) {
@@ -97,7 +108,7 @@ __global__ void __launch_bounds__(kPairThreads) pair_fused_kernel(const PairArgs
   using S = typename ElemTraits<Tag>::Storage;
   constexpr int VW = ElemTraits<Tag>::kVW;
   constexpr int kWarpsPair = kPairThreads / 32;
-  __shared__ df32 sh[kWarpsPair];
+  __shared__ df32 sh[3][kWarpsPair];
   __shared__ int sh_e[kWarpsPair];
   __shared__ df32 coef[2];
   const S* x = static_cast<const S*>(a.a);
@@ -138,18 +149,17 @@ __global__ void __launch_bounds__(kPairThreads) pair_fused_kernel(const PairArgs
       sbb = df_add(sbb, df32{pbb, __fmaf_rn(w, w, -pbb)});
     }
   // the CTA's largest exponent, then its sums in that scale
-  int E = pair_block_max(ex_sum, sh_e);
-  const df32 bab = pair_block_sum(sab, ex_sum, E, sh);
-  const df32 baa = pair_block_sum(saa, ex_sum, E, sh);
-  const df32 bbb = pair_block_sum(sbb, ex_sum, E, sh);
+  const int E = pair_block_max(ex_sum, sh_e);
+  df32 cta[3] = {sab, saa, sbb};
+  pair_block_sum3(cta, ex_sum, E, sh);
   if (threadIdx.x == 0) {
     float* p = a.partials + 8 * static_cast<size_t>(blockIdx.x);
-    p[0] = bab.hi;
-    p[1] = bab.lo;
-    p[2] = baa.hi;
-    p[3] = baa.lo;
-    p[4] = bbb.hi;
-    p[5] = bbb.lo;
+    p[0] = cta[0].hi;
+    p[1] = cta[0].lo;
+    p[2] = cta[1].hi;
+    p[3] = cta[1].lo;
+    p[4] = cta[2].hi;
+    p[5] = cta[2].lo;
     p[6] = __int_as_float(E);
   }
 
@@ -171,12 +181,11 @@ __global__ void __launch_bounds__(kPairThreads) pair_fused_kernel(const PairArgs
       pe = __float_as_int(__ldcg(p + 6));
     }
     const int Eg = pair_block_max(pe, sh_e);
-    const df32 tab = pair_block_sum(pab, pe, Eg, sh);
-    const df32 taa = pair_block_sum(paa, pe, Eg, sh);
-    const df32 tbb = pair_block_sum(pbb, pe, Eg, sh);
+    df32 tot[3] = {pab, paa, pbb};
+    pair_block_sum3(tot, pe, Eg, sh);
     if (threadIdx.x == 0) {
-      coef[0] = pair_coefficient(tab, taa);
-      coef[1] = pair_coefficient(tab, tbb);
+      coef[0] = pair_coefficient(tot[0], tot[1]);
+      coef[1] = pair_coefficient(tot[0], tot[2]);
     }
   }
   __syncthreads();
