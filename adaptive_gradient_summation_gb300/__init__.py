@@ -293,12 +293,14 @@ def profile_enable(on: bool = True) -> None:
 
 
 def profile_collect() -> dict:
-    """{kernel name: (launches, total device ms)} since the last collect."""
+    """{kernel name: (launches, total device ms, total algorithmic bytes)} since the last
+    collect (bytes 0 for kernels the library does not rate)."""
     lib = load_library()
     cap = 64
     arr = (KernelStat * cap)()
     n = lib.adasum_profile_collect(arr, cap)
-    return {arr[i].name.decode(): (int(arr[i].launches), float(arr[i].total_ms))
+    return {arr[i].name.decode(): (int(arr[i].launches), float(arr[i].total_ms),
+                                   float(arr[i].total_bytes))
             for i in range(min(n, cap))}
 
 

@@ -36,7 +36,7 @@ class AdasumError(RuntimeError):
 
 class KernelStat(ctypes.Structure):
     _fields_ = [("name", ctypes.c_char * 64), ("launches", ctypes.c_int64),
-                ("total_ms", ctypes.c_double)]
+                ("total_ms", ctypes.c_double), ("total_bytes", ctypes.c_double)]
 
 
 #: Every symbol include/adasum.h declares, with (restype, argtypes).

@@ -65,6 +65,7 @@ bool env_on(const char* name, bool dflt) {
 struct ProfRecord {
   const char* name;
   cudaEvent_t start, stop;
+  double bytes;  // algorithmic bytes of the launch (0: not rated)
 };
 
 std::mutex g_mu;                   // serialises every entry point
@@ -131,6 +132,11 @@ struct Plan {
   int nbig = 0, nsmall = 0;
   int* d_big = nullptr;
   int* d_small = nullptr;
+  // positions each launch covers (for the profiler's algorithmic bytes): all tiles, the
+  // CTA Gram's and the warp Gram's tiles, each fast-pass launch's and the tiny kernel's
+  // segments
+  int64_t pos_tiles = 0, pos_big = 0, pos_small = 0, pos_tiny = 0;
+  int64_t pos_onchip[5] = {0, 0, 0, 0, 0};
   // tiled segments the on-chip kernel could recompute if flagged (clusters of rc_cmax
   // CTAs), and whether any tiled segment is too long for it (else the fp64 path, which
   // only ever receives those, is not launched)
@@ -511,6 +517,12 @@ adasum_status_t get_plan(Workspace& ws, const int64_t* offs, int L, int Kg0, int
   p.warp_tiles = warp_tiles;
   p.nbig = static_cast<int>(big.size());
   p.nsmall = static_cast<int>(small_tiles.size());
+  for (const TileDesc& t : tiles) p.pos_tiles += t.len;
+  for (int t : small_tiles) p.pos_small += tiles[t].len;
+  p.pos_big = p.pos_tiles - p.pos_small;
+  for (int s : tiny) p.pos_tiny += offs[s + 1] - offs[s];
+  for (int c = 0; c < 5; ++c)
+    for (int s : onchip[c]) p.pos_onchip[c] += offs[s + 1] - offs[s];
   adasum_status_t st = upload(&p.d_tiles, tiles);
   if (!st && p.nsmall > 0) st = upload(&p.d_big, big);
   if (!st && p.nsmall > 0) st = upload(&p.d_small, small_tiles);
@@ -588,13 +600,13 @@ bool inject_timeout() {
   return v != nullptr && std::strcmp(v, "timeout") == 0;
 }
 
-int record_launch(int rc, const char* name, cudaEvent_t start, cudaStream_t stream) {
+int record_launch(int rc, const char* name, cudaEvent_t start, cudaStream_t stream, double bytes) {
   if (rc != 0) return rc;
   g_launches.fetch_add(1, std::memory_order_relaxed);
   if (g_profiling && start) {
     cudaEvent_t stop = pool_event();
     cudaEventRecord(stop, stream);
-    g_prof_pending.push_back(ProfRecord{name, start, stop});
+    g_prof_pending.push_back(ProfRecord{name, start, stop, bytes});
   }
   return 0;
 }
@@ -606,33 +618,36 @@ cudaEvent_t maybe_start(cudaStream_t stream) {
   return e;
 }
 
-// Launch wrapper: counts launches and, when profiling, brackets them with events.
+// Launch wrapper: counts launches and, when profiling, brackets them with events and
+// records the launch's algorithmic bytes (the input it must read and the output it must
+// write; 0 for kernels whose work depends on what earlier kernels found).
 template <typename F>
-adasum_status_t launch_one(cudaStream_t stream, F&& f) {
+adasum_status_t launch_one(cudaStream_t stream, F&& f, double bytes = 0.0) {
   const char* name = "";
   cudaEvent_t e = maybe_start(stream);
   const int rc = f(&name);
-  return record_launch(rc, name, e, stream) ? ADASUM_ERR_CUDA : ADASUM_OK;
+  return record_launch(rc, name, e, stream, bytes) ? ADASUM_ERR_CUDA : ADASUM_OK;
 }
 
 // fp32 pass of one stage (all groups): Gram partials, chunk sums, coefficients with the
 // conditioning check, then `before_combine` (when given), then the combine (flagged
 // segments are skipped and left to the recompute).
+// bytes: the algorithmic bytes of the CTA Gram, the warp Gram and the combine launches.
 adasum_status_t run_stage(StageArgs& a, int in_dtype, int out_dtype, int momentum, cudaStream_t stream,
-                          const std::function<adasum_status_t()>& before_combine) {
+                          const std::function<adasum_status_t()>& before_combine, const double (&bytes)[3]) {
   if (a.ntiles == 0)  // every segment went to the small-segment kernels
     return before_combine ? before_combine() : ADASUM_OK;
   if (a.Kg > 1) {
     if (a.tile_list == nullptr || a.ntile_list > 0) {
       if (adasum_status_t st = launch_one(stream, [&](const char** n) {
             return in_dtype == kBF16 ? launch_gram_bf16(a, stream, n) : launch_gram_f32(a, stream, n);
-          }))
+          }, bytes[0]))
         return st;
     }
     if (a.nsmall > 0) {
       if (adasum_status_t st = launch_one(stream, [&](const char** n) {
             return launch_gram_warp(a, in_dtype, stream, n);
-          }))
+          }, bytes[1]))
         return st;
     }
     if (adasum_status_t st = launch_one(stream, [&](const char** n) {
@@ -647,7 +662,7 @@ adasum_status_t run_stage(StageArgs& a, int in_dtype, int out_dtype, int momentu
   return launch_one(stream, [&](const char** n) {
     return in_dtype == kBF16 ? launch_combine_bf16in(a, out_dtype, momentum, stream, n)
                              : launch_combine_f32in(a, out_dtype, momentum, stream, n);
-  });
+  }, bytes[2]);
 }
 
 // fp64 pass of one stage over the flagged lists.
@@ -733,7 +748,8 @@ bool run_pair_fused(Workspace& ws, const void* a, const void* b, int64_t n, int 
     pa.inject_no_arrival = 1;
     pa.spin_budget = 200000LL;
   }
-  *status = launch_one(stream, [&](const char** nm) { return launch_pair_fused(pa, dtype, grid, stream, nm); });
+  *status = launch_one(stream, [&](const char** nm) { return launch_pair_fused(pa, dtype, grid, stream, nm); },
+                       3.0 * static_cast<double>(n) * static_cast<double>(elem_size(dtype)));
   ws.last_flag_counts = reinterpret_cast<int*>(base + part_bytes + 64);  // zeros: nothing is recomputed
   return true;
 }
@@ -1005,8 +1021,8 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
     ta.count = plan->tiny_count;
     ta.K = K;
     cudaStream_t side = ws.side[0].stream;
-    if (adasum_status_t st =
-            launch_one(side, [&](const char** n) { return launch_tiny_df(ta, dtype, side, n); }))
+    if (adasum_status_t st = launch_one(side, [&](const char** n) { return launch_tiny_df(ta, dtype, side, n); },
+                                        static_cast<double>(plan->pos_tiny) * (Kreal + 1) * es))
       return st;
   }
   // Small segments: whole tree on chip, one launch per cluster size.
@@ -1030,7 +1046,7 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
       oa.list = plan->d_onchip + plan->onchip_first[c];
       if (adasum_status_t st = launch_one(stream, [&](const char** n) {
             return launch_onchip(oa, dtype, K, plan->onchip_count[c], 1 << c, stream, n);
-          }))
+          }, static_cast<double>(plan->pos_onchip[c]) * (Kreal + 1) * es))
         return st;
     }
   }
@@ -1201,8 +1217,17 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
     a.skip_flagged = 1;
     const int in_dt = s == 0 ? dtype : kF32;
     const int out_dt = last ? dtype : kF32;
+    // algorithmic bytes: each tile's inputs once, and the combine's outputs (or the
+    // momentum step's w and v, read and written)
+    const double es_in = static_cast<double>(elem_size(in_dt)), es_out = static_cast<double>(elem_size(out_dt));
+    const double nin = static_cast<double>(groups[s]) * kg[s];
+    const double big = static_cast<double>(plan->nsmall > 0 ? plan->pos_big : plan->pos_tiles);
+    const double out_b = (!last || out != nullptr) ? groups[s] * es_out : 0.0;
+    const double mom_b = (last && mom) ? (momentum != nullptr ? 16.0 : 8.0) : 0.0;
+    const double bytes[3] = {big * nin * es_in, static_cast<double>(plan->pos_small) * nin * es_in,
+                             static_cast<double>(plan->pos_tiles) * (nin * es_in + out_b + mom_b)};
     if (adasum_status_t st = run_stage(a, in_dt, out_dt, (last && mom) ? 1 : 0, stream,
-                                       last ? fork_recompute : std::function<adasum_status_t()>()))
+                                       last ? fork_recompute : std::function<adasum_status_t()>(), bytes))
       return st;
   }
 
@@ -1401,6 +1426,7 @@ int adasum_profile_collect(adasum_kernel_stat_t* stats, int max_stats) {
     }
     slot->launches += 1;
     slot->total_ms += ms;
+    slot->total_bytes += r.bytes;
     g_event_pool.push_back(r.start);
     g_event_pool.push_back(r.stop);
   }

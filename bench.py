@@ -12,7 +12,9 @@ per-launch events.
 
 Prints one JSON line (rank 0):
   value      input GB/s = K * N * bytes_per_element * steps / time, summed over ranks
-  roofline   the dominant kernel's algorithmic bytes / its CUDA-event time vs measured HBM
+  roofline   the dominant streaming kernel's algorithmic bytes per launch (counted by the
+             library from its plan: the tiles, segments or pair the launch covers) / its
+             mean CUDA-event time, vs the measured HBM copy bandwidth
   e2e        the same metric through reduce_from_host: H2D of the inputs, the reduction,
              D2H of the result, every step
   cpu_baseline  the fp64 CPU oracle on a bounded sample of the same workload
@@ -193,20 +195,6 @@ def time_oracle(grads, sub, oracle, reps=1):
 
 # ---------------------------------------------------------------------------- main arms
 
-def algorithmic_bytes(kernel: str, wl, out_es: int) -> int:
-    es = torch.tensor([], dtype=wl.dtype).element_size()
-    KN = wl.K * wl.N
-    if kernel.startswith("gram"):
-        return KN * es                      # every input element once
-    if kernel.startswith("combine"):
-        if wl.master_w is not None:   # the step writes w and v (fp32), not the output
-            return KN * es + 16 * wl.N
-        return KN * es + wl.N * out_es
-    if kernel.startswith("pair_fused"):
-        return KN * es + wl.N * out_es      # the whole pair in one kernel: read once, write once
-    return 0
-
-
 def run_ours(args):
     import adaptive_gradient_summation_gb300 as ags
     from adaptive_gradient_summation_gb300 import workloads
@@ -284,12 +272,18 @@ def run_ours(args):
     value = total_bytes / t_max / 1e9
     peak, peak_src = read_peaks()
 
-    # dominant kernel: the largest summed event time among the kernels whose algorithmic
-    # bytes are defined (the streaming passes; the small-segment kernels are latency-bound
-    # and the tiny-segment one runs concurrently on a second stream)
-    rated = {k: v for k, v in kstats.items() if algorithmic_bytes(k, wl, es)} or kstats
-    dom, (dom_n, dom_ms) = max(rated.items(), key=lambda kv: kv[1][1])
-    dom_bytes = algorithmic_bytes(dom, wl, es)
+    # dominant kernel: the largest summed event time among the streaming kernels (the
+    # Gram and combine passes, the fused pair kernel), with the algorithmic bytes the
+    # library counts for each launch from its plan (only the tiles, segments or pair that
+    # launch covers).  The small-segment kernels are latency-bound and are not rated here;
+    # the tiny-segment kernel runs concurrently on a second stream.
+    def launch_bytes(k):
+        n, _, b = kstats[k]
+        return b / n if n else 0
+    streaming = ("gram", "combine", "pair_fused")
+    rated = {k: v for k, v in kstats.items() if k.startswith(streaming) and launch_bytes(k)} or kstats
+    dom, (dom_n, dom_ms, _) = max(rated.items(), key=lambda kv: kv[1][1])
+    dom_bytes = launch_bytes(dom)
     dom_gbs = dom_bytes / (dom_ms / dom_n / 1e3) / 1e9 if dom_bytes else None
     traffic = None
     tpath = os.path.join(ROOT, "profiles", "traffic.json")
@@ -350,7 +344,8 @@ def run_ours(args):
                          "frac": round(dom_gbs / peak, 4) if dom_gbs else None,
                          "algorithmic_bytes_per_launch": dom_bytes,
                          "avg_launch_ms": round(dom_ms / dom_n, 4), "traffic": traffic},
-            "kernels": {k: {"launches": n, "total_ms": round(ms, 3)} for k, (n, ms) in kstats.items()},
+            "kernels": {k: {"launches": n, "total_ms": round(ms, 3), "bytes_per_launch": round(b / n) if n else 0}
+                        for k, (n, ms, b) in kstats.items()},
             "kernel_timing": ("CUDA events around every launch, in a second pass over the same %d "
                               "steps (%.4f ms per step with the events; the timed steps run without)"
                               % (args.steps, t_instr * 1e3 / args.steps)),

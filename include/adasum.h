@@ -264,6 +264,10 @@ typedef struct {
   char name[64];      /* kernel kind, e.g. "gram_mma<bf16,16>" */
   int64_t launches;   /* launches recorded since the last collect */
   double total_ms;    /* summed device time between CUDA events around each launch */
+  double total_bytes; /* summed algorithmic bytes of those launches: the input each must
+                         read and the output it must write (0 for kernels whose work is
+                         known only on the device, such as the recompute of flagged
+                         segments) */
 } adasum_kernel_stat_t;
 
 /*

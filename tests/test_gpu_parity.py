@@ -613,3 +613,39 @@ def test_conditioning_check_keeps_every_segment_accurate(native, K):
         lo, hi = int(offs[s]), int(offs[s + 1])
         err = np.linalg.norm(got[lo:hi] - ref[lo:hi]) / np.linalg.norm(ref[lo:hi])
         assert err <= 4e-6, (s, err)
+
+
+def test_profiler_counts_each_input_byte_once(native, monkeypatch):
+    """The profiler's algorithmic bytes (what bench.py's roofline divides by): in one
+    call, every input byte is counted by exactly one of the kernels that read the inputs
+    (the CTA and warp Gram kernels for tiled segments, the on-chip and tiny kernels for
+    small ones, which also count their output), and the combine counts the tiled
+    positions' inputs and outputs."""
+    monkeypatch.setenv("ADASUM_ONCHIP", "force")
+    K = 16
+    lengths = [5, 17, 32, 33, 200, 1000, 3000, 900, 70_000, 300_001, 12]
+    offs = workloads.offsets_from_numels(lengths)
+    N = int(offs[-1])
+    grads = rand_grads(K, N, torch.float32, seed=70)
+    ags.profile_enable(True)
+    ags.profile_collect()
+    ags.reduce(grads, offs)
+    torch.cuda.synchronize()
+    stats = ags.profile_collect()
+    ags.profile_enable(False)
+    b = {k: v[2] for k, v in stats.items()}
+    small = sum(v for k, v in b.items() if k.startswith(("onchip", "tiny_df")))
+    gram = sum(v for k, v in b.items() if k.startswith("gram") and not k.startswith("gram64"))
+    small_pos = small / ((K + 1) * 4)
+    assert small_pos == int(small_pos) and small_pos > 0
+    assert gram + small_pos * K * 4 == K * N * 4
+    combine = sum(v for k, v in b.items() if k.startswith("combine") and not k.startswith("combine64"))
+    assert combine == (N - small_pos) * (K + 1) * 4
+    a, c = grads[0][:100_000], grads[1][:100_000]
+    ags.profile_enable(True)
+    ags.profile_collect()
+    ags.pair(a, c)
+    torch.cuda.synchronize()
+    stats = ags.profile_collect()
+    ags.profile_enable(False)
+    assert stats["pair_fused<f32>"][2] == 3 * 100_000 * 4
