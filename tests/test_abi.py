@@ -59,3 +59,30 @@ def test_binding_refuses_cpu_tensors():
     import adaptive_gradient_summation_gb300 as ags
     with pytest.raises(ValueError):
         ags.reduce([torch.zeros(4), torch.zeros(4)])
+
+
+def test_kernel_stat_layout_matches_the_header(tmp_path):
+    """The binding's ctypes mirror of adasum_kernel_stat_t has the header's size and
+    field offsets (compiled with the host C compiler; no GPU)."""
+    import shutil
+    import subprocess
+    from adaptive_gradient_summation_gb300 import _native
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "layout.c"
+    src.write_text(
+        '#include <stddef.h>\n#include <stdio.h>\n#include "adasum.h"\n'
+        "int main(void) {\n"
+        '  printf("%zu %zu %zu %zu %zu\\n", sizeof(adasum_kernel_stat_t),\n'
+        "         offsetof(adasum_kernel_stat_t, name), offsetof(adasum_kernel_stat_t, launches),\n"
+        "         offsetof(adasum_kernel_stat_t, total_ms), offsetof(adasum_kernel_stat_t, total_bytes));\n"
+        "  return 0;\n}\n")
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    got = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True,
+                                          check=True).stdout.split()]
+    ks = _native.KernelStat
+    want = [ctypes.sizeof(ks), ks.name.offset, ks.launches.offset, ks.total_ms.offset,
+            ks.total_bytes.offset]
+    assert got == want
