@@ -191,7 +191,7 @@ struct PairArgs {
   int aligned;                  // a, b and out are 16-byte aligned
   float* partials;              // [grid][8]: each CTA's double-float sums and exponent
   unsigned* bar;                // [2]: grid barrier (arrivals, generation), zero when allocated
-  int* error;                   // device status word (bit 4: the grid barrier gave up)
+  int* error;                   // device status word (bit 8: the grid barrier gave up)
   long long spin_budget;        // clock64 cycles of the barrier wait
   int inject_no_arrival;        // test hook: wait at the barrier without arriving
 };

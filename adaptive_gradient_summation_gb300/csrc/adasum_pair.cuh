@@ -31,7 +31,7 @@ constexpr int kNoExponent = -1000;  // exponent of a thread or CTA that saw no d
 
 // Grid barrier for a cooperative launch: arrivals are counted in bar[0]; the CTA that
 // arrives last resets the count and advances the generation in bar[1], which the others
-// wait for (clock-bounded: bit 4 of the error word when the budget runs out).  The count
+// wait for (clock-bounded: bit 8 of the error word when the budget runs out).  The count
 // is back at zero after every barrier, so the state carries over from call to call, and
 // from one replay of a captured graph to the next.  no_arrival (the timeout test): the
 // CTA waits without arriving, so every wait runs out and the state stays as it was.
