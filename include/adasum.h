@@ -146,8 +146,8 @@ ADASUM_API adasum_status_t adasum_reduce_chain(const void *const *grads, int K,
  * Pairs that the GPU's co-resident CTAs hold in registers (about 1.2M fp32 or 5M bf16
  * elements on a GB300) run as one cooperative kernel: the three dot products in
  * double-float arithmetic with exact products, and the output the double-float value of
- * alpha a + beta b rounded once, i.e. within half an ulp of the exact result up to about
- * 2^-48 relative.  Longer pairs take the tiled route, within the stated tolerances.
+ * alpha a + beta b rounded once (that value lies within about 2^-48 (|alpha a| + |beta b|)
+ * of the exact one).  Longer pairs take the tiled route, within the stated tolerances.
  */
 ADASUM_API adasum_status_t adasum_pair(const void *a, const void *b, int64_t n, adasum_dtype_t dtype,
                             void *out, adasum_stream_t stream);
