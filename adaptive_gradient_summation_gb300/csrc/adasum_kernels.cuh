@@ -461,6 +461,130 @@ __device__ __forceinline__ void gram_tile_mma(const StageArgs& a, int tile_id, i
   }
 }
 
+// Three bf16 parts of two fp32 values, x = h + m + l exactly: h is x rounded to bf16,
+// m the remainder rounded, l what is left (each remainder is exact in fp32, and at most
+// 8 significant bits are left for l).  Packed in pairs, as the MMA fragments take them.
+__device__ __forceinline__ void split_bf16x3(float x0, float x1, uint32_t& h, uint32_t& m, uint32_t& l) {
+  h = pack_bf16x2(x0, x1);
+  const float r0 = x0 - bf16_lo(h), r1 = x1 - bf16_hi(h);
+  m = pack_bf16x2(r0, r1);
+  l = pack_bf16x2(r0 - bf16_lo(m), r1 - bf16_hi(m));
+}
+
+// Gram partial of one tile of fp32 gradients (16 workers) on the tensor cores.  Every
+// value is split into three bf16 parts (split_bf16x3) and x.y is taken as the six
+// largest of the nine part products, h.h + h.m + m.h + m.m + h.l + l.h: the three left
+// out are below 2^-23 |x||y| together, the size of one fp32 product's rounding.  The
+// layout, the MMA accumulation and the compensated folding are those of gram_tile_mma
+// (lane (g, t) holds positions [8t, 8t+8) of workers g and g+8 of each 32-position
+// chunk).  The products h.m and m.h reach entry (i, j) and entry (j, i) in opposite
+// order, so each off-diagonal entry is the mean of the two: permuting the workers then
+// permutes the Gram matrix bit for bit, as the sibling-swap symmetry needs.
+template <int KG>
+__device__ __forceinline__ void gram_tile_mma_f32(const StageArgs& a, int tile_id, int q) {
+  static_assert(KG == 16, "16 workers: two n-tiles of the m16n8k16 MMA");
+  constexpr int E = tri_count(KG);
+  constexpr int U = 2;        // chunks of 32 positions loaded per warp iteration
+  constexpr int kFold = 4;    // iterations accumulated in the MMA before a Kahan fold
+  const TileDesc t = a.tiles[tile_id];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g = lane >> 2, tq = lane & 3;
+  const float* xg = static_cast<const float*>(a.in[q * KG + g]);
+  const float* xh = static_cast<const float*>(a.in[q * KG + g + 8]);
+  const bool aligned = a.aligned != 0;
+  const int64_t lo = t.start, hi = t.start + t.len;
+  const int64_t c0 = lo >> 5, c1 = (hi + 31) >> 5;  // 32-position chunks
+
+  float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+  float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+  float e0[4] = {0.f, 0.f, 0.f, 0.f}, e1[4] = {0.f, 0.f, 0.f, 0.f};
+  int pending = 0;
+  for (int64_t c = c0 + warp; c < c1; c += kWarps * U) {
+    uint4 rg[U][2], rh[U][2];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t cu = c + static_cast<int64_t>(u) * kWarps;
+      const int64_t v = cu * 8 + tq * 2;  // float4 index of positions [32cu + 8t, +8)
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
+        rg[u][h2] = cu < c1 ? load_vec_raw<F32Tag, kLoadKeep>(xg, v + h2, lo, hi, aligned) : make_uint4(0u, 0u, 0u, 0u);
+        rh[u][h2] = cu < c1 ? load_vec_raw<F32Tag, kLoadKeep>(xh, v + h2, lo, hi, aligned) : make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      // parts of positions (0,1), (2,3), (4,5), (6,7): registers 0..3 as in gram_tile_mma
+      uint32_t gh[4], gm[4], gl[4], hh[4], hm[4], hl[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint4 a4 = rg[u][k >> 1], b4 = rh[u][k >> 1];
+        const float ga = __uint_as_float((k & 1) ? a4.z : a4.x), gb = __uint_as_float((k & 1) ? a4.w : a4.y);
+        const float ha = __uint_as_float((k & 1) ? b4.z : b4.x), hb = __uint_as_float((k & 1) ? b4.w : b4.y);
+        split_bf16x3(ga, gb, gh[k], gm[k], gl[k]);
+        split_bf16x3(ha, hb, hh[k], hm[k], hl[k]);
+      }
+      // d += A B for A = rows (g, g+8) of part pa, B = columns g (d0) and g+8 (d1) of part pb
+      auto mmas = [&](const uint32_t (&ag)[4], const uint32_t (&ah)[4], const uint32_t (&bg)[4],
+                      const uint32_t (&bh)[4]) {
+        mma_bf16_16816(d0, ag[0], ah[0], ag[1], ah[1], bg[0], bg[1]);
+        mma_bf16_16816(d0, ag[2], ah[2], ag[3], ah[3], bg[2], bg[3]);
+        mma_bf16_16816(d1, ag[0], ah[0], ag[1], ah[1], bh[0], bh[1]);
+        mma_bf16_16816(d1, ag[2], ah[2], ag[3], ah[3], bh[2], bh[3]);
+      };
+      mmas(gh, hh, gh, hh);
+      mmas(gh, hh, gm, hm);
+      mmas(gm, hm, gh, hh);
+      mmas(gm, hm, gm, hm);
+      mmas(gh, hh, gl, hl);
+      mmas(gl, hl, gh, hh);
+    }
+    if (++pending == kFold) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        kahan_add(s0[i], e0[i], d0[i]);
+        kahan_add(s1[i], e1[i], d1[i]);
+        d0[i] = 0.f;
+        d1[i] = 0.f;
+      }
+      pending = 0;
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    kahan_add(s0[i], e0[i], d0[i]);
+    kahan_add(s1[i], e1[i], d1[i]);
+  }
+  __shared__ float red[kWarps][KG * KG];
+  {
+    const int r0 = g, r1 = g + 8, cA = 2 * tq;
+    red[warp][r0 * KG + cA] = __fsub_rn(s0[0], e0[0]);
+    red[warp][r0 * KG + cA + 1] = __fsub_rn(s0[1], e0[1]);
+    red[warp][r1 * KG + cA] = __fsub_rn(s0[2], e0[2]);
+    red[warp][r1 * KG + cA + 1] = __fsub_rn(s0[3], e0[3]);
+    red[warp][r0 * KG + 8 + cA] = __fsub_rn(s1[0], e1[0]);
+    red[warp][r0 * KG + 8 + cA + 1] = __fsub_rn(s1[1], e1[1]);
+    red[warp][r1 * KG + 8 + cA] = __fsub_rn(s1[2], e1[2]);
+    red[warp][r1 * KG + 8 + cA + 1] = __fsub_rn(s1[3], e1[3]);
+  }
+  __syncthreads();
+  float* dst = a.partials + (static_cast<size_t>(q) * a.ntiles + tile_id) * E;
+  for (int idx = threadIdx.x; idx < KG * KG; idx += kThreads) {
+    const int i = idx / KG, j = idx % KG;
+    if (j < i) continue;
+    float s = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w)
+      s = __fadd_rn(s, i == j ? red[w][idx] : 0.5f * __fadd_rn(red[w][idx], red[w][j * KG + i]));
+    dst[tri_index(KG, i, j)] = s;
+  }
+}
+
+template <int KG>
+__global__ void __launch_bounds__(kThreads) gram_mma_f32_kernel(const StageArgs a) {
+  pdl_enter();
+  gram_tile_mma_f32<KG>(a, cta_tile(a), blockIdx.y);
+}
+
 template <int KG>
 __global__ void __launch_bounds__(kThreads) gram_mma_bf16_kernel(const StageArgs a) {
   pdl_enter();
