@@ -190,3 +190,17 @@ def test_fused_pair_dtypes_alternate(native):
         torch.cuda.synchronize()
         _check_rounded_once(a, b, out)
     assert ags.get_last_error() == ags.Status.OK
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_fused_pair_through_reduce_and_in_place_on_b(native, dtype):
+    """adasum_reduce with two workers and one segment is the same kernel as adasum_pair
+    (bitwise), and the output may also be the second operand."""
+    a, b = _pair(250_007, dtype, seed=21)
+    expect = ags.pair(a, b).clone()
+    via_reduce = ags.reduce([a, b], [0, a.numel()])
+    y = b.clone()
+    ags.reduce([a, y], [0, a.numel()], out=y)
+    torch.cuda.synchronize()
+    assert torch.equal(via_reduce, expect)
+    assert torch.equal(y, expect)
