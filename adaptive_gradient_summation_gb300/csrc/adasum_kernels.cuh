@@ -471,39 +471,34 @@ __device__ __forceinline__ void split_bf16x3(float x0, float x1, uint32_t& h, ui
   l = pack_bf16x2(r0 - bf16_lo(m), r1 - bf16_hi(m));
 }
 
-// Gram partial of one tile of fp32 gradients (16 workers) on the tensor cores.  Every
-// value is split into three bf16 parts (split_bf16x3) and x.y is taken as the six
-// largest of the nine part products, h.h + h.m + m.h + m.m + h.l + l.h: the three left
-// out are below 2^-23 |x||y| together, the size of one fp32 product's rounding.  The
-// layout, the MMA accumulation and the compensated folding are those of gram_tile_mma
-// (lane (g, t) holds positions [8t, 8t+8) of workers g and g+8 of each 32-position
-// chunk).  The products h.m and m.h reach entry (i, j) and entry (j, i) in opposite
-// order, so each off-diagonal entry is the mean of the two: permuting the workers then
-// permutes the Gram matrix bit for bit, as the sibling-swap symmetry needs.
+// One warp's share of the Gram of fp32 rows on the tensor cores (16 workers): the
+// 32-position chunks first, first + nw, first + 2 nw, ... of [lo, hi).  Every value is
+// split into three bf16 parts (split_bf16x3) and x.y is taken as the six largest of the
+// nine part products, h.h + h.m + m.h + m.m + h.l + l.h: the three left out are below
+// 2^-23 |x||y| together, the size of one fp32 product's rounding.  The layout, the MMA
+// accumulation and the compensated folding are those of gram_tile_mma (lane (g, t) holds
+// positions [8t, 8t+8) of workers g and g+8 of each chunk).  On return s0/e0 and s1/e1
+// hold the compensated sums of the lane's entries (columns 2t, 2t+1 and 8+2t, 9+2t of
+// rows g and g+8).
 template <int KG>
-__device__ __forceinline__ void gram_tile_mma_f32(const StageArgs& a, int tile_id, int q) {
+__device__ __forceinline__ void gram_chunks_mma_f32(const float* xg, const float* xh, int64_t lo, int64_t hi,
+                                                    bool aligned, int first, int nw, float (&s0)[4],
+                                                    float (&e0)[4], float (&s1)[4], float (&e1)[4]) {
   static_assert(KG == 16, "16 workers: two n-tiles of the m16n8k16 MMA");
-  constexpr int E = tri_count(KG);
   constexpr int U = 2;        // chunks of 32 positions loaded per warp iteration
   constexpr int kFold = 4;    // iterations accumulated in the MMA before a Kahan fold
-  const TileDesc t = a.tiles[tile_id];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int g = lane >> 2, tq = lane & 3;
-  const float* xg = static_cast<const float*>(a.in[q * KG + g]);
-  const float* xh = static_cast<const float*>(a.in[q * KG + g + 8]);
-  const bool aligned = a.aligned != 0;
-  const int64_t lo = t.start, hi = t.start + t.len;
+  const int lane = threadIdx.x & 31;
+  const int tq = lane & 3;
   const int64_t c0 = lo >> 5, c1 = (hi + 31) >> 5;  // 32-position chunks
-
   float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
-  float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
-  float e0[4] = {0.f, 0.f, 0.f, 0.f}, e1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) s0[i] = e0[i] = s1[i] = e1[i] = 0.f;
   int pending = 0;
-  for (int64_t c = c0 + warp; c < c1; c += kWarps * U) {
+  for (int64_t c = c0 + first; c < c1; c += static_cast<int64_t>(nw) * U) {
     uint4 rg[U][2], rh[U][2];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const int64_t cu = c + static_cast<int64_t>(u) * kWarps;
+      const int64_t cu = c + static_cast<int64_t>(u) * nw;
       const int64_t v = cu * 8 + tq * 2;  // float4 index of positions [32cu + 8t, +8)
 #pragma unroll
       for (int h2 = 0; h2 < 2; ++h2) {
@@ -554,18 +549,41 @@ __device__ __forceinline__ void gram_tile_mma_f32(const StageArgs& a, int tile_i
     kahan_add(s0[i], e0[i], d0[i]);
     kahan_add(s1[i], e1[i], d1[i]);
   }
+}
+
+// A lane's compensated sums into the KG x KG matrix m (row-major), as laid out by the MMA.
+__device__ __forceinline__ void store_lane_gram16(float* m, const float (&s0)[4], const float (&e0)[4],
+                                                  const float (&s1)[4], const float (&e1)[4]) {
+  constexpr int KG = 16;
+  const int lane = threadIdx.x & 31;
+  const int r0 = lane >> 2, r1 = r0 + 8, cA = 2 * (lane & 3);
+  m[r0 * KG + cA] = __fsub_rn(s0[0], e0[0]);
+  m[r0 * KG + cA + 1] = __fsub_rn(s0[1], e0[1]);
+  m[r1 * KG + cA] = __fsub_rn(s0[2], e0[2]);
+  m[r1 * KG + cA + 1] = __fsub_rn(s0[3], e0[3]);
+  m[r0 * KG + 8 + cA] = __fsub_rn(s1[0], e1[0]);
+  m[r0 * KG + 8 + cA + 1] = __fsub_rn(s1[1], e1[1]);
+  m[r1 * KG + 8 + cA] = __fsub_rn(s1[2], e1[2]);
+  m[r1 * KG + 8 + cA + 1] = __fsub_rn(s1[3], e1[3]);
+}
+
+// Gram partial of one tile of fp32 gradients (16 workers) on the tensor cores, all warps
+// of the CTA sharing its chunks (gram_chunks_mma_f32).  The products h.m and m.h reach
+// entry (i, j) and entry (j, i) in opposite order, so each off-diagonal entry is the
+// mean of the two: permuting the workers then permutes the Gram matrix bit for bit, as
+// the sibling-swap symmetry needs.
+template <int KG>
+__device__ __forceinline__ void gram_tile_mma_f32(const StageArgs& a, int tile_id, int q) {
+  static_assert(KG == 16, "16 workers");
+  constexpr int E = tri_count(KG);
+  const TileDesc t = a.tiles[tile_id];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g = lane >> 2;
+  float s0[4], e0[4], s1[4], e1[4];
+  gram_chunks_mma_f32<KG>(static_cast<const float*>(a.in[q * KG + g]), static_cast<const float*>(a.in[q * KG + g + 8]),
+                          t.start, t.start + t.len, a.aligned != 0, warp, kWarps, s0, e0, s1, e1);
   __shared__ float red[kWarps][KG * KG];
-  {
-    const int r0 = g, r1 = g + 8, cA = 2 * tq;
-    red[warp][r0 * KG + cA] = __fsub_rn(s0[0], e0[0]);
-    red[warp][r0 * KG + cA + 1] = __fsub_rn(s0[1], e0[1]);
-    red[warp][r1 * KG + cA] = __fsub_rn(s0[2], e0[2]);
-    red[warp][r1 * KG + cA + 1] = __fsub_rn(s0[3], e0[3]);
-    red[warp][r0 * KG + 8 + cA] = __fsub_rn(s1[0], e1[0]);
-    red[warp][r0 * KG + 8 + cA + 1] = __fsub_rn(s1[1], e1[1]);
-    red[warp][r1 * KG + 8 + cA] = __fsub_rn(s1[2], e1[2]);
-    red[warp][r1 * KG + 8 + cA + 1] = __fsub_rn(s1[3], e1[3]);
-  }
+  store_lane_gram16(red[warp], s0, e0, s1, e1);
   __syncthreads();
   float* dst = a.partials + (static_cast<size_t>(q) * a.ntiles + tile_id) * E;
   for (int idx = threadIdx.x; idx < KG * KG; idx += kThreads) {
@@ -576,6 +594,36 @@ __device__ __forceinline__ void gram_tile_mma_f32(const StageArgs& a, int tile_i
     for (int w = 0; w < kWarps; ++w)
       s = __fadd_rn(s, i == j ? red[w][idx] : 0.5f * __fadd_rn(red[w][idx], red[w][j * KG + i]));
     dst[tri_index(KG, i, j)] = s;
+  }
+}
+
+// Gram partials of small tiles of fp32 gradients (16 workers), one warp per (tile,
+// group), on the tensor cores (gram_chunks_mma_f32 with the warp alone on the tile);
+// each off-diagonal entry is the mean of its two mirror sums, as in gram_tile_mma_f32.
+template <int KG>
+__global__ void __launch_bounds__(kThreads, 3) gram_warp_mma_f32_kernel(const StageArgs a) {
+  pdl_enter();
+  static_assert(KG == 16, "16 workers");
+  constexpr int E = tri_count(KG);
+  __shared__ float red[kWarps][KG * KG];
+  const int wb = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int w = blockIdx.x * kWarps + wb;
+  if (w >= a.nsmall) return;  // whole warps only (no block barrier below)
+  const int q = blockIdx.y;
+  const int tile_id = a.small_list[w];
+  const TileDesc t = a.tiles[tile_id];
+  const int g = lane >> 2;
+  float s0[4], e0[4], s1[4], e1[4];
+  gram_chunks_mma_f32<KG>(static_cast<const float*>(a.in[q * KG + g]), static_cast<const float*>(a.in[q * KG + g + 8]),
+                          t.start, t.start + t.len, a.aligned != 0, 0, 1, s0, e0, s1, e1);
+  float* m = red[wb];
+  store_lane_gram16(m, s0, e0, s1, e1);
+  __syncwarp();
+  float* dst = a.partials + (static_cast<size_t>(q) * a.ntiles + tile_id) * E;
+  for (int e = lane; e < E; e += 32) {
+    int i, j;
+    tri_unpack(KG, e, i, j);
+    dst[e] = i == j ? m[i * KG + i] : 0.5f * __fadd_rn(m[i * KG + j], m[j * KG + i]);
   }
 }
 

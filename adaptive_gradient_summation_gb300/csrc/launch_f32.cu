@@ -58,7 +58,13 @@ int launch_gram_warp(const StageArgs& a, int in_dtype, void* stream, const char*
       case 2: *name = "gram_warp<f32,2>"; return launch(gram_warp_kernel<F32Tag, 2>, grid, block, a, stream);
       case 4: *name = "gram_warp<f32,4>"; return launch(gram_warp_kernel<F32Tag, 4>, grid, block, a, stream);
       case 8: *name = "gram_warp<f32,8>"; return launch(gram_warp_kernel<F32Tag, 8>, grid, block, a, stream);
-      case 16: *name = "gram_warp<f32,16>"; return launch(gram_warp_kernel<F32Tag, 16>, grid, block, a, stream);
+      case 16:
+        if (f32_mma_enabled()) {
+          *name = "gram_warp_mma<f32,16>";
+          return launch(gram_warp_mma_f32_kernel<16>, grid, block, a, stream);
+        }
+        *name = "gram_warp<f32,16>";
+        return launch(gram_warp_kernel<F32Tag, 16>, grid, block, a, stream);
       default: return static_cast<int>(cudaErrorInvalidValue);
     }
   }
