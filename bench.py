@@ -399,7 +399,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-sample-bytes", type=int, default=1 << 30)
+    ap.add_argument("--cpu-sample-bytes", type=int, default=5 << 30,
+                    help="input bytes of the CPU-baseline sample (about 10 s of the fp64 oracle)")
     ap.add_argument("--ref-sample-bytes", type=int, default=64 << 20)
     args = ap.parse_args()
     if args.impl == "reference":
