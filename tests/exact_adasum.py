@@ -113,3 +113,37 @@ def adasum_tree_exact_segments(vectors, offsets):
             continue
         out += adasum_tree_exact([v[lo:hi] for v in vectors])
     return out
+
+
+def _sequential_coefficients(first, second):
+    """Steps 1-5 on nodes carried as (vector, leaf coefficients): the corrected second
+    gradient subtracts alpha (second . first) second, so the effective gradient of the
+    two steps is  first + second - ((second . first) / |second|^2) second."""
+    (fv, fc), (sv, sc) = first, second
+    norm2 = _dot(sv, sv)
+    t = Fraction(0) if norm2 == 0 else _dot(sv, fv) / norm2
+    vec = [f + s - t * s for f, s in zip(fv, sv)]
+    coef = [f + s - t * s for f, s in zip(fc, sc)]
+    return vec, coef
+
+
+def adasum_tree_exact_coefficients(vectors):
+    """The binary tree of adasum_tree_exact, returning the leaf coefficients c_k of
+    out = sum_k c_k g_k (every node is a linear combination of the leaves; its
+    coefficients follow the same two averaged orders as its vector)."""
+    k = len(vectors)
+    if k == 0 or (k & (k - 1)):
+        raise ValueError("need a power-of-two number of vectors")
+
+    def node(lo, hi):
+        if hi - lo == 1:
+            c = [Fraction(0)] * k
+            c[lo] = Fraction(1)
+            return _vec(vectors[lo]), c
+        mid = (lo + hi) // 2
+        a, b = node(lo, mid), node(mid, hi)
+        ab, ba = _sequential_coefficients(a, b), _sequential_coefficients(b, a)
+        return ([(x + y) / 2 for x, y in zip(ab[0], ba[0])],
+                [(x + y) / 2 for x, y in zip(ab[1], ba[1])])
+
+    return node(0, k)[1]

@@ -32,7 +32,23 @@ MUTANTS = {
     "carry_dropped": ("memmove(level + to, level + from, (size_t)n * sizeof(double));",
                       "(void)from; (void)to;"),
     "chain_skips_one": ("for (int k = 1; k < K; ++k) {", "for (int k = 2; k < K; ++k) {"),
+    "mag_signed": ("fabs(alpha) * ma[j] + fabs(beta) * mb[j]", "alpha * ma[j] + beta * mb[j]"),
+    "mag_unweighted": ("fabs(alpha) * ma[j] + fabs(beta) * mb[j]", "ma[j] + mb[j]"),
+    "mag_coefficients_only": ("fabs(alpha) * ma[j] + fabs(beta) * mb[j]", "fabs(alpha) + fabs(beta)"),
+    "mag_inflated": ("fabs(alpha) * ma[j] + fabs(beta) * mb[j]",
+                     "2.0 * (fabs(alpha) * ma[j] + fabs(beta) * mb[j])"),
+    "mag_leaf_signed": ("mlevel[(size_t)k * (size_t)n + j] = fabs(v[j]);",
+                        "mlevel[(size_t)k * (size_t)n + j] = v[j];"),
 }
+
+# Magnitude bound m = |alpha| m_a + |beta| m_b, hand-worked (one case has alpha < 0 and
+# one negative inputs; see test_oracle_pins.py).
+MAG_PINS = [
+    ([[1, 0], [1, 1]], [1.25, 0.75]),
+    ([[1, 0], [3, 1]], [61 / 20, 17 / 20]),
+    ([[-1, 0], [-3, -1]], [61 / 20, 17 / 20]),
+    ([[1, 0], [0, 1], [1, 1], [2, -1]], [1439 / 580, 1013 / 580]),
+]
 
 
 def _pins_pass(lib) -> bool:
@@ -63,6 +79,11 @@ def _pins_pass(lib) -> bool:
         exp = np.array([float(x) for x in adasum_chain_exact(vecs)])
         got = oracle.adasum_reduce(vecs, [0, 5], lib=lib, chain=True)["out64"]
         if not np.allclose(got, exp, rtol=1e-12, atol=1e-12):
+            return False
+    # magnitude bound
+    for vecs, exp in MAG_PINS:
+        got = oracle.adasum_reduce([f32(v) for v in vecs], [0, 2], lib=lib, want_mag=True)["mag"]
+        if not np.allclose(got, exp, rtol=1e-14, atol=0):
             return False
     # zero operand
     b = f32([1.5, -2.0, 0.25])

@@ -231,6 +231,53 @@ def test_magnitude_bound_dominates(oracle_mod):
     assert np.all(r["mag"] >= np.abs(r["out64"]) * (1 - 1e-15))
 
 
+# The magnitude bound m sizes the fp32 floor of every bf16 tolerance, so it is pinned
+# exactly: at a pair, m = |alpha| m_a + |beta| m_b with m = |g| at the leaves.
+MAG_HAND = [
+    # a=(1,0), b=(1,1): alpha=1/2, beta=3/4 -> m = (1/2)(1,0) + (3/4)(1,1) = (5/4, 3/4)
+    ([[1, 0], [1, 1]], [Fraction(5, 4), Fraction(3, 4)]),
+    # a=(1,0), b=(3,1): a.b=3, |a|^2=1, |b|^2=10 -> alpha = 1 - 3/2 = -1/2 (negative),
+    #   beta = 1 - 3/20 = 17/20.  out = -(1/2)(1,0) + (17/20)(3,1) = (41/20, 17/20), but
+    #   m = (1/2)(1,0) + (17/20)(3,1) = (61/20, 17/20)
+    ([[1, 0], [3, 1]], [Fraction(61, 20), Fraction(17, 20)]),
+    # the same with every entry negated: the same coefficients, m from |g|: (61/20, 17/20)
+    ([[-1, 0], [-3, -1]], [Fraction(61, 20), Fraction(17, 20)]),
+    # tree over (1,0),(0,1),(1,1),(2,-1) (values in HAND above):
+    #   level 0: m = (1,1) for the orthogonal pair; (3/4)(1,1) + (9/10)(2,1) = (51/20, 33/20)
+    #   level 1: (2/5)(1,1) + (71/87)(51/20, 33/20) = (4317/1740, 3039/1740)
+    #          = (1439/580, 1013/580)   (out is (1439/580, 161/580))
+    ([[1, 0], [0, 1], [1, 1], [2, -1]], [Fraction(1439, 580), Fraction(1013, 580)]),
+]
+
+
+@pytest.mark.parametrize("vecs,expected", MAG_HAND)
+def test_magnitude_bound_hand_worked(oracle_mod, vecs, expected):
+    r = oracle_mod.adasum_reduce(f32(*vecs), [0, len(vecs[0])], want_mag=True)
+    assert np.allclose(r["mag"], [float(x) for x in expected], rtol=1e-15, atol=0)
+
+
+def test_magnitude_bound_closed_form(oracle_mod):
+    """m = sum_k |c_k| |g_k|, with the leaf coefficients c_k of out = sum_k c_k g_k taken
+    from the exact sequential-emulation derivation (not from the oracle).  Includes
+    near-parallel pairs of unequal length, where a coefficient is negative."""
+    from exact_adasum import adasum_tree_exact_coefficients
+    rs = np.random.default_rng(31)
+    seen_negative = False
+    for K in (2, 4, 8):
+        for trial in range(4):
+            n = 5
+            vecs = [rs.integers(-3, 4, size=n).astype(np.float32) for _ in range(K)]
+            if trial % 2:  # a longer near-parallel partner: a.b > 2|a|^2
+                vecs[1] = (3 * vecs[0] + rs.integers(-1, 2, size=n)).astype(np.float32)
+            c = adasum_tree_exact_coefficients(vecs)
+            seen_negative |= any(x < 0 for x in c)
+            m = [sum(abs(ck) * abs(Fraction(float(v[j]))) for ck, v in zip(c, vecs))
+                 for j in range(n)]
+            got = oracle_mod.adasum_reduce(vecs, [0, n], want_mag=True)["mag"]
+            assert np.allclose(got, [float(x) for x in m], rtol=1e-12, atol=1e-12), (K, trial)
+    assert seen_negative
+
+
 # ------------------------------------------------------------------- library-routine pins
 
 def test_bf16_encoder_matches_torch(oracle_mod):
