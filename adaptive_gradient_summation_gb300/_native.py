@@ -13,7 +13,6 @@ import threading
 from . import _build
 
 _lock = threading.Lock()
-_lib = None
 
 
 class Status(enum.IntEnum):
@@ -77,26 +76,45 @@ def library_path() -> str:
     return _build.LIB_PATH
 
 
-def load_library(build_if_missing: bool = False):
-    """Load (and declare) the native library.  Raises if it is not built."""
-    global _lib
+_libs = {}
+_active = None
+
+
+def _open(path: str, build_if_missing: bool, test_hooks: bool):
+    if not os.path.exists(path):
+        if not build_if_missing:
+            raise RuntimeError(
+                f"{os.path.basename(path)} is not built; run "
+                "`python -c 'import __graft_entry__ as g; g.build()'` first")
+        _build.build(test_hooks=test_hooks)
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+def load_library(build_if_missing: bool = False, test_hooks: bool = False):
+    """The library the binding calls: the product build, unless a test has made the test
+    build active (use_library).  ``test_hooks=True`` returns the test build itself.
+    Raises if the requested library is not built."""
     with _lock:
-        if _lib is not None:
-            return _lib
-        path = _build.LIB_PATH
-        if not os.path.exists(path):
-            if not build_if_missing:
-                raise RuntimeError(
-                    f"{os.path.basename(path)} is not built; run "
-                    "`python -c 'import __graft_entry__ as g; g.build()'` first")
-            _build.build()
-        lib = ctypes.CDLL(path)
-        for name, (res, args) in SIGNATURES.items():
-            fn = getattr(lib, name)
-            fn.restype = res
-            fn.argtypes = args
-        _lib = lib
-        return lib
+        if not test_hooks and _active is not None:
+            return _active
+        path = _build.TEST_LIB_PATH if test_hooks else _build.LIB_PATH
+        if path not in _libs:
+            _libs[path] = _open(path, build_if_missing, test_hooks)
+        return _libs[path]
+
+
+def use_library(lib):
+    """Make `lib` the library every binding call goes to (None: the product build);
+    returns the previous choice.  Tests use it to run on the test build."""
+    global _active
+    with _lock:
+        prev, _active = _active, lib
+    return prev
 
 
 def check(status: int, where: str) -> None:

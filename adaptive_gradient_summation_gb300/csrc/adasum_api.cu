@@ -22,7 +22,6 @@
 
 #include "../../include/adasum.h"
 #include "adasum_internal.h"
-#include "adasum_stream.cuh"
 
 namespace adasum {
 namespace {
@@ -31,30 +30,29 @@ constexpr int kVersion = 100;  // 0.1.0
 
 int elem_size(int dt) { return dt == kBF16 ? 2 : 4; }
 
-// Route of a single-stage call: the three-kernel route (Gram / coefficients / combine
-// as separate launches), the streaming kernel (adasum_stream.cuh), or the dynamically
-// scheduled fused kernel.  ADASUM_ROUTE=kernels|stream|fused selects one explicitly.
-enum Route { kRouteKernels = 0, kRouteStream = 1, kRouteFused = 2 };
-
-int requested_route() {
-  const char* v = std::getenv("ADASUM_ROUTE");
-  if (v != nullptr && std::strcmp(v, "fused") == 0) return kRouteFused;
-  if (v != nullptr && std::strcmp(v, "stream") == 0) return kRouteStream;
-  return kRouteKernels;
+// Switches for tests and comparisons.  Only a library built with -DADASUM_TEST_HOOKS
+// (the test build) reads them from the environment; the product library reads no
+// environment variable and always takes the defaults.
+const char* hook(const char* name) {
+#ifdef ADASUM_TEST_HOOKS
+  return std::getenv(name);
+#else
+  (void)name;
+  return nullptr;
+#endif
 }
-bool route_fused() { return requested_route() == kRouteFused; }
 
-// A positive integer from the environment (tuning knobs), else `dflt`.
+// A positive integer switch, else `dflt`.
 int64_t env_int(const char* name, int64_t dflt) {
-  const char* v = std::getenv(name);
+  const char* v = hook(name);
   if (v == nullptr) return dflt;
   const long long x = std::atoll(v);
   return x > 0 ? x : dflt;
 }
 
-// An on/off switch from the environment: "0" is off, anything else on, unset `dflt`.
+// An on/off switch: "0" is off, anything else on, unset `dflt`.
 bool env_on(const char* name, bool dflt) {
-  const char* v = std::getenv(name);
+  const char* v = hook(name);
   if (v == nullptr || *v == '\0') return dflt;
   return std::strcmp(v, "0") != 0;
 }
@@ -100,18 +98,6 @@ struct Plan {
   TileDesc* d_tiles = nullptr;
   SegDesc* d_segs = nullptr;
   ChunkDesc* d_chunks = nullptr;
-  // task list of the fused single-stage kernel (built when K <= 16)
-  int ntasks = 0;
-  int* d_tasks = nullptr;
-  int64_t wave_bytes = 0;
-  int64_t tile_kb = 0;
-  int64_t delay_pct = 0;
-  // streaming kernel: per-CTA task lists (CSR) and the round-robin start of each segment
-  int route = kRouteKernels;
-  int stream_grid = 0;
-  int stage_pos = 0;
-  int* d_task_ptr = nullptr;
-  int* d_seg_c0 = nullptr;
   // small segments: held on chip (grouped by cluster size 1, 2, 4, 8, 16) or, up to
   // kTinyDirect positions, one warp each; neither gets tiles.  The coefficient kernel
   // then runs over the list of the remaining (tiled) segments.
@@ -203,9 +189,6 @@ void free_plan(Plan& p) {
   if (p.d_tiles) cudaFree(p.d_tiles);
   if (p.d_segs) cudaFree(p.d_segs);
   if (p.d_chunks) cudaFree(p.d_chunks);
-  if (p.d_tasks) cudaFree(p.d_tasks);
-  if (p.d_task_ptr) cudaFree(p.d_task_ptr);
-  if (p.d_seg_c0) cudaFree(p.d_seg_c0);
   if (p.d_onchip) cudaFree(p.d_onchip);
   if (p.d_tiny) cudaFree(p.d_tiny);
   if (p.d_coef_list) cudaFree(p.d_coef_list);
@@ -216,151 +199,22 @@ void free_plan(Plan& p) {
   p.d_onchip = nullptr;
   p.d_tiny = nullptr;
   p.d_coef_list = nullptr;
-  p.d_task_ptr = nullptr;
-  p.d_seg_c0 = nullptr;
   p.d_tiles = nullptr;
   p.d_segs = nullptr;
   p.d_chunks = nullptr;
-  p.d_tasks = nullptr;
 }
 
-// Wave budget of the fused kernel (bytes of input per wave); ADASUM_WAVE_MB overrides.
-int64_t wave_budget_bytes() { return env_int("ADASUM_WAVE_MB", 32) << 20; }
+// Input bytes per tile of the tiled passes.
+constexpr int64_t kTileBytes = int64_t(256) << 10;
 
-// Task order of the fused kernel: consecutive segments are grouped into waves of about
-// wave_bytes of input; the list is  A(0), A(1)[:delay], A(1)[delay:] merged with B(0),
-// A(2)[:delay], A(2)[delay:] merged with B(1), ..., B(last), where A(w) are the Gram
-// tiles of wave w in order and B(w) its combine tiles in reverse order (the most
-// recently loaded data first).  `delay` Gram tasks separate a wave's last Gram task
-// from its first combine task, so a combine task rarely finds its segment unfinished.
-std::vector<int> build_tasks(const std::vector<SegDesc>& segs, int64_t bytes_per_pos,
-                             int64_t wave_bytes, int delay) {
-  std::vector<std::vector<int>> waves;
-  int64_t cur = 0;
-  for (int s = 0; s < static_cast<int>(segs.size()); ++s) {
-    if (segs[s].ntiles == 0) continue;
-    const int64_t b = segs[s].len * bytes_per_pos;
-    if (waves.empty() || (cur > 0 && cur + b > wave_bytes)) {
-      waves.emplace_back();
-      cur = 0;
-    }
-    waves.back().push_back(s);
-    cur += b;
-  }
-  auto gram_of = [&](const std::vector<int>& w) {
-    std::vector<int> t;
-    for (int s : w)
-      for (int i = 0; i < segs[s].ntiles; ++i) t.push_back(segs[s].first_tile + i);
-    return t;
-  };
-  auto combine_of = [&](const std::vector<int>& w) {
-    std::vector<int> t;
-    for (auto it = w.rbegin(); it != w.rend(); ++it)
-      for (int i = segs[*it].ntiles - 1; i >= 0; --i)
-        t.push_back(static_cast<int>(0x80000000u | static_cast<uint32_t>(segs[*it].first_tile + i)));
-    return t;
-  };
-  std::vector<int> tasks;
-  std::vector<int> pending_b;
-  for (size_t w = 0; w < waves.size(); ++w) {
-    const std::vector<int> A = gram_of(waves[w]);
-    size_t ia = 0;
-    if (!pending_b.empty()) {
-      const size_t d = std::min(A.size(), static_cast<size_t>(delay));
-      for (; ia < d; ++ia) tasks.push_back(A[ia]);
-      // merge the rest of A with pending_b in proportion
-      const size_t na = A.size() - ia, nb = pending_b.size();
-      size_t ea = 0, eb = 0;
-      while (ea < na || eb < nb) {
-        if (eb >= nb || (ea < na && ea * nb <= eb * na)) {
-          tasks.push_back(A[ia + ea]);
-          ++ea;
-        } else {
-          tasks.push_back(pending_b[eb]);
-          ++eb;
-        }
-      }
-    } else {
-      for (; ia < A.size(); ++ia) tasks.push_back(A[ia]);
-    }
-    pending_b = combine_of(waves[w]);
-  }
-  tasks.insert(tasks.end(), pending_b.begin(), pending_b.end());
-  return tasks;
-}
-
-// Input bytes per tile.  The fused kernel uses small tiles: the L2 has to hold every
-// byte read between a tile's Gram task and its combine task, and that distance grows
-// with (resident CTAs x tile size).  ADASUM_PIPE_TILE_KB overrides (for tuning).
-int64_t tile_bytes(bool fused) {
-  return fused ? env_int("ADASUM_PIPE_TILE_KB", 64) << 10 : int64_t(256) << 10;
-}
-
-int64_t tile_positions(int Kg, int dtype, int64_t N, int num_sms, bool fused) {
-  // About tile_bytes of input per tile, but enough tiles to give every SM a few.
+int64_t tile_positions(int Kg, int dtype, int64_t N, int num_sms) {
+  // About kTileBytes of input per tile, but enough tiles to give every SM a few.
   const int64_t bytes_per_pos = static_cast<int64_t>(Kg) * elem_size(dtype);
-  int64_t T = tile_bytes(fused) / bytes_per_pos;
+  int64_t T = kTileBytes / bytes_per_pos;
   const int64_t want = std::max<int64_t>(1, N / (4 * static_cast<int64_t>(num_sms)));
   T = std::min(T, want);
   T = std::max<int64_t>(256, std::min<int64_t>(T, 65536));
   return (T + 255) / 256 * 256;
-}
-
-// Positions per stage of the streaming kernel: 64 KiB of input (rounded to 32).
-int stream_stage_pos(int Kg, int dtype) {
-  const int64_t kb = env_int("ADASUM_STREAM_STAGE_KB", 64);
-  return static_cast<int>(std::max<int64_t>(32, (kb << 10) / (int64_t(Kg) * elem_size(dtype)) / 32 * 32));
-}
-
-// Per-CTA task lists of the streaming kernel.  Segments are grouped into waves of about
-// wave_bytes of input; the tiles of a wave are dealt round robin to the G CTAs, and
-// every CTA runs  Gram(wave 0), Gram(wave 1), Combine(wave 0), Gram(wave 2),
-// Combine(wave 1), ..., Combine(last wave)  over its own share.  A combine task of
-// wave w therefore comes one wave after that wave's Gram tasks, on every CTA.
-void build_stream_tasks(const std::vector<SegDesc>& segs, int64_t bytes_per_pos,
-                        int64_t wave_bytes, int G, std::vector<int>& task_ptr,
-                        std::vector<int>& tasks, std::vector<int>& seg_c0) {
-  std::vector<std::vector<int>> waves;
-  int64_t cur = 0;
-  for (int s = 0; s < static_cast<int>(segs.size()); ++s) {
-    if (segs[s].ntiles == 0) continue;
-    const int64_t b = segs[s].len * bytes_per_pos;
-    if (waves.empty() || (cur > 0 && cur + b > wave_bytes)) {
-      waves.emplace_back();
-      cur = 0;
-    }
-    waves.back().push_back(s);
-    cur += b;
-  }
-  seg_c0.assign(segs.size(), 0);
-  std::vector<std::vector<int>> per(G);
-  std::vector<std::vector<int>> prev_b(G);
-  for (size_t w = 0; w <= waves.size(); ++w) {
-    std::vector<std::vector<int>> cur_b(G);
-    if (w < waves.size()) {
-      int j = 0;
-      std::vector<int> all;
-      for (int sg : waves[w]) {
-        seg_c0[sg] = j % G;
-        for (int i = 0; i < segs[sg].ntiles; ++i, ++j) {
-          per[j % G].push_back(segs[sg].first_tile + i);
-          all.push_back(segs[sg].first_tile + i);
-        }
-      }
-      int jb = 0;
-      for (auto it = all.rbegin(); it != all.rend(); ++it, ++jb)
-        cur_b[jb % G].push_back(static_cast<int>(0x80000000u | static_cast<uint32_t>(*it)));
-    }
-    for (int c = 0; c < G; ++c) per[c].insert(per[c].end(), prev_b[c].begin(), prev_b[c].end());
-    prev_b.swap(cur_b);
-  }
-  task_ptr.assign(G + 1, 0);
-  tasks.clear();
-  for (int c = 0; c < G; ++c) {
-    task_ptr[c] = static_cast<int>(tasks.size());
-    tasks.insert(tasks.end(), per[c].begin(), per[c].end());
-  }
-  task_ptr[G] = static_cast<int>(tasks.size());
 }
 
 template <typename T>
@@ -378,18 +232,13 @@ adasum_status_t upload(T** dst, const std::vector<T>& v) {
   return ADASUM_OK;
 }
 
-adasum_status_t get_plan(Workspace& ws, const int64_t* offs, int L, int Kg0, int dtype, int route,
+adasum_status_t get_plan(Workspace& ws, const int64_t* offs, int L, int Kg0, int dtype,
                          int onchip_K, int onchip_cmax, bool onchip_force, int rc_cmax, bool tiny_on,
                          bool warp_tiles, Plan** out) {
-  const int64_t wave = route == kRouteStream ? env_int("ADASUM_WAVE_MB", 24) << 20 : wave_budget_bytes();
   for (auto it = ws.plans.begin(); it != ws.plans.end(); ++it) {
-    if (it->Kg0 == Kg0 && it->dtype == dtype && it->route == route && it->onchip_K == onchip_K &&
+    if (it->Kg0 == Kg0 && it->dtype == dtype && it->onchip_K == onchip_K &&
         it->onchip_cmax == onchip_cmax && it->onchip_force == onchip_force && it->rc_cmax == rc_cmax &&
         it->tiny_on == tiny_on && it->warp_tiles == warp_tiles &&
-        (route == kRouteKernels ||
-         (it->wave_bytes == wave && it->tile_kb == (tile_bytes(true) >> 10) &&
-          it->delay_pct == env_int("ADASUM_PIPE_DELAY_PCT", 100) &&
-          it->stage_pos == (route == kRouteStream ? stream_stage_pos(Kg0, dtype) : 0))) &&
         it->offsets.size() == static_cast<size_t>(L + 1) &&
         std::memcmp(it->offsets.data(), offs, sizeof(int64_t) * (L + 1)) == 0) {
       ws.plans.splice(ws.plans.begin(), ws.plans, it);
@@ -400,12 +249,7 @@ adasum_status_t get_plan(Workspace& ws, const int64_t* offs, int L, int Kg0, int
   int num_sms = 148;
   cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, ws.device);
   const int64_t N = offs[L];
-  int64_t T = 0;
-  if (route == kRouteStream) {
-    T = stream_stage_pos(Kg0, dtype);
-  } else {
-    T = tile_positions(Kg0, dtype, N, num_sms, route == kRouteFused);
-  }
+  const int64_t T = tile_positions(Kg0, dtype, N, num_sms);
   std::vector<TileDesc> tiles;
   std::vector<SegDesc> segs(L);
   std::vector<ChunkDesc> chunks;
@@ -477,13 +321,9 @@ adasum_status_t get_plan(Workspace& ws, const int64_t* offs, int L, int Kg0, int
   p.offsets.assign(offs, offs + L + 1);
   p.Kg0 = Kg0;
   p.dtype = dtype;
-  p.route = route;
   p.ntiles = static_cast<int>(tiles.size());
   p.nsegs = L;
   p.nchunks = static_cast<int>(chunks.size());
-  p.wave_bytes = wave;
-  p.tile_kb = tile_bytes(true) >> 10;
-  p.delay_pct = env_int("ADASUM_PIPE_DELAY_PCT", 100);
   p.onchip_K = onchip_K;
   p.onchip_cmax = onchip_cmax;
   p.onchip_force = onchip_force;
@@ -504,7 +344,7 @@ adasum_status_t get_plan(Workspace& ws, const int64_t* offs, int L, int Kg0, int
       if (segs[s].ntiles > 0) coef_list.push_back(s);
   p.ncoef = static_cast<int>(coef_list.size());
   std::vector<int> big, small_tiles;
-  if (route == kRouteKernels && warp_tiles) {
+  if (warp_tiles) {
     for (int t = 0; t < static_cast<int>(tiles.size()); ++t)
       (tiles[t].len <= kSmallTile ? small_tiles : big).push_back(t);
     // a few small tiles cost nothing inside the CTA launch; a separate warp launch pays
@@ -531,24 +371,6 @@ adasum_status_t get_plan(Workspace& ws, const int64_t* offs, int L, int Kg0, int
   if (!st && any_small) st = upload(&p.d_coef_list, coef_list);
   if (!st) st = upload(&p.d_segs, segs);
   if (!st) st = upload(&p.d_chunks, chunks);
-  if (!st && route == kRouteFused) {
-    const int delay = static_cast<int>(p.delay_pct * pipeline_grid(dtype, dtype, Kg0, 0, num_sms) / 100);
-    const std::vector<int> tasks =
-        build_tasks(segs, static_cast<int64_t>(Kg0) * elem_size(dtype), p.wave_bytes, delay);
-    p.ntasks = static_cast<int>(tasks.size());
-    st = upload(&p.d_tasks, tasks);
-  }
-  if (!st && route == kRouteStream) {
-    std::vector<int> task_ptr, tasks, seg_c0;
-    p.stage_pos = static_cast<int>(T);
-    p.stream_grid = std::min(num_sms, 256);  // the finisher sums at most 256 CTA partials
-    build_stream_tasks(segs, static_cast<int64_t>(Kg0) * elem_size(dtype), p.wave_bytes,
-                       p.stream_grid, task_ptr, tasks, seg_c0);
-    p.ntasks = static_cast<int>(tasks.size());
-    st = upload(&p.d_tasks, tasks);
-    if (!st) st = upload(&p.d_task_ptr, task_ptr);
-    if (!st) st = upload(&p.d_seg_c0, seg_c0);
-  }
   if (st) {
     free_plan(p);
     return st;
@@ -586,17 +408,18 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Host-side fault injection for the error-path tests: ADASUM_FAULT_INJECT=alloc makes
-// the next workspace growth fail as if cudaMalloc had; ADASUM_FAULT_INJECT=timeout makes
-// the fused and streaming kernels never publish segment coefficients, and the
-// small-segment kernel expect 16 bulk-copy bytes that are never sent, with their bounded
-// waits shortened, so the waits run out and the device status reports ADASUM_ERR_TIMEOUT.
+// Host-side fault injection for the error-path tests (test build only):
+// ADASUM_FAULT_INJECT=alloc makes the next workspace growth fail as if cudaMalloc had;
+// ADASUM_FAULT_INJECT=timeout makes the small-segment kernel expect 16 bulk-copy bytes
+// that are never sent and the fused pair kernel wait at a barrier no CTA arrives at,
+// with their bounded waits shortened, so the waits run out and the device status
+// reports ADASUM_ERR_TIMEOUT.
 bool inject_alloc_failure() {
-  const char* v = std::getenv("ADASUM_FAULT_INJECT");
+  const char* v = hook("ADASUM_FAULT_INJECT");
   return v != nullptr && std::strcmp(v, "alloc") == 0;
 }
 bool inject_timeout() {
-  const char* v = std::getenv("ADASUM_FAULT_INJECT");
+  const char* v = hook("ADASUM_FAULT_INJECT");
   return v != nullptr && std::strcmp(v, "timeout") == 0;
 }
 
@@ -812,7 +635,7 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
   // Two workers and one segment whose inputs fit well inside L2: one fused kernel
   // (ADASUM_PAIR_FUSED=0 switches it off, for comparisons).
   if (K == 2 && Kreal == 2 && L == 1 && !mom && !chain && ortho == nullptr &&
-      requested_route() == kRouteKernels && env_on("ADASUM_PAIR_FUSED", true)) {
+      env_on("ADASUM_PAIR_FUSED", true)) {
     adasum_status_t st = ADASUM_OK;
     if (run_pair_fused(ws, grads[0], grads[1], N, dtype, out, stream, &st)) return st;
   }
@@ -834,21 +657,16 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
     }
   }
 
-  int route = kRouteKernels;
-  if (kg.size() == 1 && kg[0] > 1 && !chain && Kreal == K && ortho == nullptr) {
-    route = requested_route();
-    if (route == kRouteStream && !stream_supported(dtype, kg[0])) route = kRouteKernels;
-  }
   // Plain reductions: segments of at most kTinyDirect positions go to the warp kernel,
   // small ones (up to 64 workers) to the on-chip kernel, the rest to the tiles.
   // (ADASUM_TINY=0 and ADASUM_ONCHIP=0 switch the two kernels off, for comparisons;
   // ADASUM_ONCHIP=force uses the on-chip kernel for every small segment, for tests;
   // ADASUM_WARP_GRAM=0 keeps every tile on the CTA Gram kernels; ADASUM_ONCHIP_FAST=0
   // leaves the on-chip kernel its recompute only.)
-  const bool plain = route == kRouteKernels && !mom && !chain && ortho == nullptr && K >= 2;
+  const bool plain = !mom && !chain && ortho == nullptr && K >= 2;
   const bool tiny_on = plain && env_on("ADASUM_TINY", true);
   int onchip_K = 0, onchip_cmax = 0;
-  const char* onchip_env = std::getenv("ADASUM_ONCHIP");
+  const char* onchip_env = hook("ADASUM_ONCHIP");
   const bool onchip_force = onchip_env != nullptr && std::strcmp(onchip_env, "force") == 0;
   if (plain && K <= kOnchipMaxK && env_on("ADASUM_ONCHIP", true) && env_on("ADASUM_ONCHIP_FAST", true)) {
     // clusters of up to 2 CTAs by default: larger clusters measured slower than the
@@ -859,7 +677,7 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
   // flagged tiled segments that fit are recomputed by the on-chip kernel
   const int rc_cmax = (plain && K <= kOnchipMaxK && env_on("ADASUM_ONCHIP", true)) ? onchip_max_cluster(dtype, K) : 0;
   Plan* plan = nullptr;
-  if (adasum_status_t st = get_plan(ws, offs, L, kg[0], dtype, route, rc_cmax > 0 ? K : onchip_K, onchip_cmax,
+  if (adasum_status_t st = get_plan(ws, offs, L, kg[0], dtype, rc_cmax > 0 ? K : onchip_K, onchip_cmax,
                                     onchip_force, rc_cmax, tiny_on, env_on("ADASUM_WARP_GRAM", true), &plan))
     return st;
 
@@ -876,9 +694,9 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
   const size_t inter64 = align_up(static_cast<size_t>(N) * sizeof(double), 256);
   Carver cv;
   // One zeroed int region per call: segment flags, the 3 fp64-list counters and the
-  // small-segment kernel's recompute counter, and the fused kernel's task counter, chunk
-  // counters, segment counters and ready flags, and the recompute's segment scales.
-  const size_t n_ints = static_cast<size_t>(L) + 4 + 1 + plan->nchunks + 3 * static_cast<size_t>(L) + 1;
+  // small-segment kernel's recompute counter, the recompute's segment scales, and the
+  // count of flagged segments listed for the on-chip recompute.
+  const size_t n_ints = 2 * static_cast<size_t>(L) + 5;
   const size_t o_flags = cv.take(n_ints * sizeof(int));
   const size_t o_part = cv.take(max_e_tiles * sizeof(float));
   const size_t o_chunk = cv.take(max_e_chunks * sizeof(double));
@@ -893,10 +711,6 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
   const size_t o_oclist = cv.take(plan->rc_cmax > 0 ? static_cast<size_t>(L) * sizeof(int) : 0);
   const size_t o_onorm = cv.take(ortho ? static_cast<size_t>(L) * sizeof(double) : 0);
   const size_t o_diag = cv.take(ortho ? static_cast<size_t>(groups[0]) * L * sizeof(double) : 0);
-  const size_t o_slots = cv.take(route == kRouteStream
-                                     ? static_cast<size_t>(L) * plan->stream_grid *
-                                           (static_cast<size_t>(kg[0]) * (kg[0] + 1) / 2) * sizeof(float)
-                                     : 0);
   // Stage outputs of every non-final stage: fp32 (fast pass) and fp64 (recompute).
   std::vector<size_t> off32(kg.size(), 0), off64(kg.size(), 0);
   for (size_t s = 0; s + 1 < kg.size(); ++s) {
@@ -909,11 +723,7 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
   char* base = static_cast<char*>(ws.buf);
   int* seg_flag = reinterpret_cast<int*>(base + o_flags);
   int* list_count = seg_flag + L;
-  int* task_counter = list_count + 4;
-  int* chunk_done = task_counter + 1;
-  int* seg_done = chunk_done + plan->nchunks;
-  int* seg_ready = seg_done + L;
-  int* seg_exp = seg_ready + L;  // the fp64 recompute's per-segment scale
+  int* seg_exp = list_count + 4;  // the fp64 recompute's per-segment scale
   int* oc_count = seg_exp + L;   // flagged segments listed for the on-chip recompute
   if (adasum_status_t st = ensure_error_word(ws)) return st;
 
@@ -1051,60 +861,6 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
     }
   }
 
-  // fp32 pass: one streaming or fused kernel for a single stage, else stage by stage.
-  if (route == kRouteStream) {
-    StageArgs a = make_args(0);
-    for (int k = 0; k < K; ++k) a.in[k] = grads[k];
-    a.out[0] = out;
-    a.skip_flagged = 1;
-    a.relerr = reinterpret_cast<float*>(base + o_rel0);
-    StreamArgs sa;
-    std::memset(&sa, 0, sizeof sa);
-    sa.task_ptr = plan->d_task_ptr;
-    sa.tasks = plan->d_tasks;
-    sa.seg_c0 = plan->d_seg_c0;
-    sa.slots = reinterpret_cast<float*>(base + o_slots);
-    sa.seg_count = seg_done;
-    sa.seg_ready = seg_ready;
-    sa.error = ws.d_error;
-    sa.spin_budget = 2000000000LL;  // about one second of SM clock
-    if (inject_timeout()) {
-      sa.inject_no_ready = 1;
-      sa.spin_budget = 200000LL;
-    }
-    sa.stage_pos = plan->stage_pos;
-    sa.row_bytes = plan->stage_pos * static_cast<int>(es) + kRowPad;
-    if (adasum_status_t st = launch_one(stream, [&](const char** n) {
-          return launch_stream(a, sa, dtype, mom ? 1 : 0, plan->stream_grid, stream, n);
-        }))
-      return st;
-  }
-  const bool fused = route == kRouteFused;
-  if (fused) {
-    StageArgs a = make_args(0);
-    for (int k = 0; k < K; ++k) a.in[k] = grads[k];
-    a.out[0] = out;
-    a.skip_flagged = 1;
-    PipeArgs pa;
-    std::memset(&pa, 0, sizeof pa);
-    pa.tasks = plan->d_tasks;
-    pa.ntasks = plan->ntasks;
-    pa.task_counter = task_counter;
-    pa.chunk_done = chunk_done;
-    pa.seg_done = seg_done;
-    pa.seg_ready = seg_ready;
-    pa.error = ws.d_error;
-    pa.spin_budget = 2000000000LL;  // about one second of SM clock
-    if (inject_timeout()) {
-      pa.inject_no_ready = 1;
-      pa.spin_budget = 200000LL;
-    }
-    const int grid = pipeline_grid(dtype, dtype, kg[0], mom ? 1 : 0, num_sms);
-    if (adasum_status_t st = launch_one(stream, [&](const char** n) {
-          return launch_pipeline(a, pa, dtype, dtype, mom ? 1 : 0, grid, stream, n);
-        }))
-      return st;
-  }
   // Recompute of the flagged segments, enqueued on `ts` (usually nothing is flagged and
   // every kernel returns at once).  It needs the last stage's flags and nothing that the
   // last combine writes: that combine skips the flagged segments, and these kernels write
@@ -1197,9 +953,7 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
     if (adasum_status_t st = joins.fork(ws.side[1], 1)) return st;
     return enqueue_recompute(ws.side[1].stream);
   };
-  if (route != kRouteKernels)
-    if (adasum_status_t st = fork_recompute()) return st;
-  for (size_t s = 0; s < kg.size() && route == kRouteKernels; ++s) {
+  for (size_t s = 0; s < kg.size(); ++s) {
     const bool last = s + 1 == kg.size();
     StageArgs a = make_args(s);
     if (s == 0) {

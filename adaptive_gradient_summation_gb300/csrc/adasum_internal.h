@@ -138,23 +138,6 @@ constexpr float kProbeSafety = 4.f;
 // cancel almost exactly, which a Gram-matrix quadratic form cannot follow even in fp64.
 constexpr int kTinySeg = 32;
 
-// Work list and synchronisation of the fused single-stage kernel (pipeline_kernel).
-// tasks[i] >= 0 is "Gram partial of tile tasks[i]"; tasks[i] < 0 is "combine of tile
-// tasks[i] & 0x7fffffff".  Every combine task comes after all Gram tasks of its
-// segment, and tasks are claimed in list order, so a combine task only ever waits for
-// work already claimed by a running CTA.
-struct PipeArgs {
-  const int* tasks;
-  int ntasks;
-  int* task_counter;        // next task to claim
-  int* chunk_done;          // [nchunks] Gram tiles finished per chunk
-  int* seg_done;            // [nsegs] chunks reduced per segment
-  int* seg_ready;           // [nsegs] 1 once the segment's coefficients are published
-  int* error;               // device status word: 1 = a bounded wait gave up
-  long long spin_budget;    // clock64 cycles a combine task waits before giving up
-  int inject_no_ready;      // test hook: never publish (exercises the bounded wait)
-};
-
 // Small-segment kernel (adasum_onchip.cuh): one segment per CTA or thread-block cluster,
 // its K x n block held in shared memory, the whole tree evaluated on chip.
 constexpr int kOnchipMaxK = 64;
@@ -220,17 +203,6 @@ int launch_combine_f32in(const StageArgs& a, int out_dtype, int momentum, void* 
                          const char** name);
 int launch_combine_bf16in(const StageArgs& a, int out_dtype, int momentum, void* stream,
                           const char** name);
-// Streaming single-stage kernel (adasum_stream.cuh): one CTA per SM, cooperative launch.
-struct StreamArgs;
-bool stream_supported(int dtype, int Kg);
-int stream_smem_bytes(int dtype, int Kg, int stage_pos);
-int launch_stream(const StageArgs& a, const StreamArgs& s, int dtype, int momentum, int grid,
-                  void* stream, const char** name);
-
-// Fused single-stage kernel (K <= 16): grid = persistent CTAs, see PipeArgs.
-int launch_pipeline(const StageArgs& a, const PipeArgs& p, int in_dtype, int out_dtype,
-                    int momentum, int grid, void* stream, const char** name);
-int pipeline_grid(int in_dtype, int out_dtype, int Kg, int momentum, int num_sms);
 // Partial-Gram chunk sums (segments with many tiles), then coefficients.
 int launch_reduce_chunks(const StageArgs& a, void* stream, const char** name);
 // Small-segment kernel: `count` clusters of C CTAs over a.list[0..count).

@@ -224,107 +224,6 @@ __global__ void __launch_bounds__(kThreads, KG <= 8 ? 3 : 1) gram_simt_kernel(co
   gram_tile_simt<Tag, KG>(a, cta_tile(a), blockIdx.y);
 }
 
-// Gram partial of one fp32 tile for groups of 16 workers (8 also compiles; there the
-// SIMT kernel measured faster: 0.139 vs 0.180 ms on ResNet-50), staged through shared
-// memory: the group's rows, SV vectors at a time (the next stage's loads are in flight
-// while the current one is multiplied), 4x4 register blocks of Gram entries per thread
-// over a slice of the positions, then the slices' sums (compensated, fixed order).  16
-// accumulators per thread instead of Kg(Kg+1)/2, so three CTAs fit on an SM where
-// gram_simt_kernel<f32,16> fits one.
-template <int KG>
-__global__ void __launch_bounds__(kThreads, 3) gram_blocked_kernel(const StageArgs a) {
-  pdl_enter();
-  static_assert(KG == 8 || KG == 16, "4x4 blocks");
-  constexpr int E = tri_count(KG);
-  constexpr int NBS = KG / 4, NBG = NBS * (NBS + 1) / 2;
-  constexpr int SL = kThreads / NBG;            // position slices: 25 (KG 16), 85 (KG 8)
-  constexpr int SV = KG == 16 ? 64 : 128;        // vectors per stage
-  constexpr int PER = KG * SV / kThreads;        // vectors each thread loads per stage: 4
-  constexpr int RS = SV * 4 + 4;                 // row stride in floats (+16 B: banks)
-  static_assert(SL * NBG * 16 <= KG * RS, "the slice sums reuse the stage buffer");
-  __shared__ __align__(16) float xs[KG * RS];
-  const int tile_id = cta_tile(a), q = blockIdx.y;
-  const TileDesc t = a.tiles[tile_id];
-  const bool aligned = a.aligned != 0;
-  const int64_t lo = t.start, hi = t.start + t.len;
-  const int64_t v0 = lo / 4, v1 = (hi + 3) / 4;
-  const int nstages = static_cast<int>((v1 - v0 + SV - 1) / SV);
-  const float* x[KG];
-#pragma unroll
-  for (int k = 0; k < KG; ++k) x[k] = static_cast<const float*>(a.in[q * KG + k]);
-
-  auto load_stage = [&](int st, uint4 (&r)[PER]) {
-#pragma unroll
-    for (int i = 0; i < PER; ++i) {
-      const int idx = threadIdx.x + i * kThreads, k = idx / SV, j = idx % SV;
-      const int64_t v = v0 + static_cast<int64_t>(st) * SV + j;
-      r[i] = v < v1 ? load_vec_raw<F32Tag, kLoadKeep>(x[k], v, lo, hi, aligned) : make_uint4(0u, 0u, 0u, 0u);
-    }
-  };
-  const bool active = threadIdx.x < NBG * SL;
-  const int slice = threadIdx.x % SL, blk = threadIdx.x / SL;
-  int bi = 0, bj = 0;
-  if (active) tri_unpack(NBS, blk, bi, bj);
-  float acc[4][4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-
-  uint4 nxt[PER];
-  load_stage(0, nxt);
-  for (int st = 0; st < nstages; ++st) {
-#pragma unroll
-    for (int i = 0; i < PER; ++i) {
-      const int idx = threadIdx.x + i * kThreads;
-      *reinterpret_cast<uint4*>(xs + (idx / SV) * RS + (idx % SV) * 4) = nxt[i];
-    }
-    __syncthreads();
-    if (st + 1 < nstages) load_stage(st + 1, nxt);  // in flight during the products
-    if (active) {
-      for (int j = slice; j < SV; j += SL) {
-        float4 rr[4], cc[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          rr[i] = *reinterpret_cast<const float4*>(xs + (bi * 4 + i) * RS + j * 4);
-          cc[i] = *reinterpret_cast<const float4*>(xs + (bj * 4 + i) * RS + j * 4);
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            acc[i][c] = __fmaf_rn(rr[i].x, cc[c].x, acc[i][c]);
-            acc[i][c] = __fmaf_rn(rr[i].y, cc[c].y, acc[i][c]);
-            acc[i][c] = __fmaf_rn(rr[i].z, cc[c].z, acc[i][c]);
-            acc[i][c] = __fmaf_rn(rr[i].w, cc[c].w, acc[i][c]);
-          }
-      }
-    }
-    __syncthreads();
-  }
-  // slice sums: red[slice][blk][16] in the stage buffer, then entry by entry in slice order
-  float* red = xs;
-  if (active) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-      for (int c = 0; c < 4; ++c) red[(slice * NBG + blk) * 16 + i * 4 + c] = acc[i][c];
-  }
-  __syncthreads();
-  float* dst = a.partials + (static_cast<size_t>(q) * a.ntiles + tile_id) * E;
-  for (int e = threadIdx.x; e < NBG * 16; e += kThreads) {
-    const int b = e / 16, ij = e % 16;
-    int ci, cj;
-    tri_unpack(NBS, b, ci, cj);
-    const int i = ci * 4 + ij / 4, j = cj * 4 + ij % 4;
-    if (i > j) continue;  // diagonal blocks: the lower half repeats the upper
-    float sum = 0.f, comp = 0.f;
-    for (int sl = 0; sl < SL; ++sl) kahan_add(sum, comp, red[(sl * NBG + b) * 16 + ij]);
-    dst[tri_index(KG, i, j)] = __fsub_rn(sum, comp);
-  }
-}
-
-
 // Gram partials of small tiles, one warp per (tile, group): the lanes' partials are
 // summed by the warp's butterfly (a fixed order), with no block-wide reduction, so a
 // tile of a few hundred positions costs a warp, not a CTA.
@@ -1456,16 +1355,7 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const StageArgs a) {
   }
 }
 
-// ------------------------------------------------------------- fused single-stage kernel
-//
-// One persistent kernel runs the whole fp32 pass of a single-stage call: CTAs claim
-// tasks from a host-built list (PipeArgs).  The list groups segments into waves of a
-// few tens of MB and interleaves the Gram tiles of wave w with the combine tiles of
-// wave w-1 (taken in reverse order), so the second read of the inputs finds them in
-// L2 instead of HBM.  A segment's coefficients are computed by the CTA that finishes
-// its last Gram chunk (the last tile of a chunk reduces the chunk; the last chunk of a
-// segment runs the tree) and published with a release store; its combine tiles wait
-// for that flag with an acquire load, bounded by a clock budget.
+// ------------------------------------------------------------- flags between CTAs
 
 __device__ __forceinline__ int ld_acquire_gpu(const int* p) {
   int v;
@@ -1476,69 +1366,6 @@ __device__ __forceinline__ void st_release_gpu(int* p, int v) {
   asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
-// After a Gram tile: count it in its chunk; the chunk's last tile reduces the chunk and
-// counts it in its segment; the segment's last chunk computes the coefficients and
-// publishes them.  Called by the whole CTA.
-template <int KG>
-__device__ __forceinline__ void arrive_tile(const StageArgs& a, const PipeArgs& p, int tile_id) {
-  __shared__ int last;
-  const TileDesc t = a.tiles[tile_id];
-  const SegDesc sd = a.segs[t.seg];
-  const int c = sd.first_chunk + (tile_id - sd.first_tile) / kChunkTiles;
-  __threadfence();  // this CTA's partial is visible before it is counted
-  __syncthreads();
-  if (threadIdx.x == 0) last = atomicAdd(p.chunk_done + c, 1) == a.chunks[c].ntiles - 1;
-  __syncthreads();
-  if (!last) return;
-  __threadfence();
-  reduce_chunk<KG>(a, c, 0);
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) last = atomicAdd(p.seg_done + t.seg, 1) == sd.nchunks - 1;
-  __syncthreads();
-  if (!last) return;
-  __threadfence();
-  segment_coefficients<KG>(a, t.seg, 0);
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0 && !p.inject_no_ready) st_release_gpu(p.seg_ready + t.seg, 1);
-}
-
-// Thread 0 waits (bounded) for a segment's coefficients; returns 1 when published.
-__device__ __forceinline__ int wait_ready(const PipeArgs& p, int seg) {
-  if (ld_acquire_gpu(p.seg_ready + seg)) return 1;
-  const long long t0 = clock64();
-  for (;;) {
-    __nanosleep(128);
-    if (ld_acquire_gpu(p.seg_ready + seg)) return 1;
-    if (clock64() - t0 > p.spin_budget) {
-      atomicOr(p.error, 1);
-      return 0;
-    }
-  }
-}
-
-template <typename InTag, typename OutTag, int KG, bool MOM>
-__global__ void __launch_bounds__(kThreads, 3) pipeline_kernel(const StageArgs a, const PipeArgs p) {
-  __shared__ int s_task, s_ok;
-  for (;;) {
-    if (threadIdx.x == 0) s_task = atomicAdd(p.task_counter, 1);
-    __syncthreads();
-    const int ti = s_task;
-    __syncthreads();
-    if (ti >= p.ntasks) return;
-    const int task = __ldg(p.tasks + ti);
-    if (task >= 0) {
-      gram_tile<InTag, KG>(a, task, 0);
-      arrive_tile<KG>(a, p, task);
-    } else {
-      const int tile_id = task & 0x7FFFFFFF;
-      if (threadIdx.x == 0) s_ok = wait_ready(p, a.tiles[tile_id].seg);
-      __syncthreads();
-      if (s_ok) combine_tile<InTag, OutTag, KG, MOM>(a, tile_id, 0);
-    }
-  }
-}
 
 // ------------------------------------------------ per-worker heavy-ball step (Fig. 3)
 

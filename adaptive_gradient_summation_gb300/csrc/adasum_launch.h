@@ -9,13 +9,18 @@
 
 namespace adasum {
 
-// Dependent launch is on unless ADASUM_PDL=0 (read once; for comparisons).
+// Dependent launch is on.  A test build (-DADASUM_TEST_HOOKS) switches it off with
+// ADASUM_PDL=0, for comparisons; the product library reads no environment.
 inline bool pdl_enabled() {
+#ifdef ADASUM_TEST_HOOKS
   static const bool on = [] {
     const char* v = std::getenv("ADASUM_PDL");
     return v == nullptr || std::strcmp(v, "0") != 0;
   }();
   return on;
+#else
+  return true;
+#endif
 }
 
 // Launches `kernel` on `stream` with programmatic stream serialization: the kernel may be

@@ -1,8 +1,5 @@
 // launch_f32.cu -- launchers for fp32 inputs (user fp32 gradients and the fp32
 // intermediates of multi-stage trees) and for the per-segment coefficient kernel.
-#include <cstdlib>
-#include <cstring>
-
 #include "adasum_kernels.cuh"
 #include "adasum_launch.h"
 
@@ -17,14 +14,6 @@ int launch(Kernel k, dim3 grid, dim3 block, const StageArgs& a, void* stream) {
 // its large grid fills the SMs with CTAs waiting on the previous kernel, and behind a
 // latency-bound kernel (the small-segment ones) that wait slowed the predecessor's tail
 // (K=64 set: 1.94 -> 1.74 ms per call without the attribute here).
-bool f32_mma_enabled() {
-  static const bool on = [] {
-    const char* v = std::getenv("ADASUM_F32_MMA");
-    return v == nullptr || *v == '\0' || std::strcmp(v, "0") != 0;
-  }();
-  return on;
-}
-
 template <typename Kernel>
 int launch_serial(Kernel k, dim3 grid, dim3 block, const StageArgs& a, void* stream) {
   k<<<grid, block, 0, static_cast<cudaStream_t>(stream)>>>(a);
@@ -38,15 +27,9 @@ int launch_gram_f32(const StageArgs& a, void* stream, const char** name) {
     case 2: *name = "gram_simt<f32,2>"; return launch_serial(gram_simt_kernel<F32Tag, 2>, grid, block, a, stream);
     case 4: *name = "gram_simt<f32,4>"; return launch_serial(gram_simt_kernel<F32Tag, 4>, grid, block, a, stream);
     case 8: *name = "gram_simt<f32,8>"; return launch_serial(gram_simt_kernel<F32Tag, 8>, grid, block, a, stream);
-    case 16:
-      // the tensor cores on an exact three-part bf16 split (ADASUM_F32_MMA=0: the blocked
-      // SIMT kernel, for comparisons)
-      if (f32_mma_enabled()) {
-        *name = "gram_mma<f32,16>";
-        return launch_serial(gram_mma_f32_kernel<16>, grid, block, a, stream);
-      }
-      *name = "gram_blocked<f32,16>";
-      return launch_serial(gram_blocked_kernel<16>, grid, block, a, stream);
+    case 16:  // the tensor cores on an exact three-part bf16 split
+      *name = "gram_mma<f32,16>";
+      return launch_serial(gram_mma_f32_kernel<16>, grid, block, a, stream);
     default: return static_cast<int>(cudaErrorInvalidValue);
   }
 }
@@ -59,12 +42,8 @@ int launch_gram_warp(const StageArgs& a, int in_dtype, void* stream, const char*
       case 4: *name = "gram_warp<f32,4>"; return launch(gram_warp_kernel<F32Tag, 4>, grid, block, a, stream);
       case 8: *name = "gram_warp<f32,8>"; return launch(gram_warp_kernel<F32Tag, 8>, grid, block, a, stream);
       case 16:
-        if (f32_mma_enabled()) {
-          *name = "gram_warp_mma<f32,16>";
-          return launch(gram_warp_mma_f32_kernel<16>, grid, block, a, stream);
-        }
-        *name = "gram_warp<f32,16>";
-        return launch(gram_warp_kernel<F32Tag, 16>, grid, block, a, stream);
+        *name = "gram_warp_mma<f32,16>";
+        return launch(gram_warp_mma_f32_kernel<16>, grid, block, a, stream);
       default: return static_cast<int>(cudaErrorInvalidValue);
     }
   }

@@ -31,3 +31,17 @@ def native():
     import adaptive_gradient_summation_gb300 as ags
     ags.load_library()
     return ags
+
+
+@pytest.fixture
+def hooks(native):
+    """Run the test on the test build of the library (built with -DADASUM_TEST_HOOKS),
+    which honours the ADASUM_* environment switches (forced routes, kernels switched off,
+    host-side fault injection); the product library reads no environment."""
+    from adaptive_gradient_summation_gb300 import _native
+    lib = _native.load_library(test_hooks=True)
+    prev = _native.use_library(lib)
+    try:
+        yield lib
+    finally:
+        _native.use_library(prev)

@@ -22,12 +22,31 @@ def test_header_declares_the_entry_points():
         assert required in names
 
 
-def test_library_builds_and_exports_every_declared_symbol():
+@pytest.mark.parametrize("test_hooks", [False, True])
+def test_library_builds_and_exports_every_declared_symbol(test_hooks):
     from adaptive_gradient_summation_gb300 import _build
-    path = _build.build()
+    path = _build.build(test_hooks=test_hooks)
     lib = ctypes.CDLL(path)
     for name in declared_functions():
         assert hasattr(lib, name), f"{name} declared in adasum.h but not exported"
+
+
+def test_product_library_reads_no_environment():
+    """Every environment read in the native sources sits inside an
+    `#ifdef ADASUM_TEST_HOOKS` block, so only the test build honours the switches."""
+    csrc = os.path.join(ROOT, "adaptive_gradient_summation_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        guarded = []
+        for no, line in enumerate(open(os.path.join(csrc, f)), 1):
+            t = line.strip()
+            if t.startswith("#if"):
+                guarded.append("ADASUM_TEST_HOOKS" in t and t.startswith("#ifdef"))
+            elif t.startswith("#else") and guarded:
+                guarded[-1] = False
+            elif t.startswith("#endif") and guarded:
+                guarded.pop()
+            if "getenv" in line and not t.startswith("//"):
+                assert any(guarded), f"{f}:{no} reads the environment outside the test build"
 
 
 def test_binding_declares_every_symbol():

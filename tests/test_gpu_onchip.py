@@ -26,10 +26,10 @@ TINY = 32               # segments up to this length: one warp each, double-floa
 
 
 @pytest.fixture(autouse=True)
-def _onchip_for_every_small_segment(monkeypatch):
+def _onchip_for_every_small_segment(monkeypatch, hooks):
     """By default the library uses the on-chip kernel only when small segments are
     numerous (thousands); these tests use it for every small segment, with clusters of
-    up to 16 CTAs."""
+    up to 16 CTAs (switches honoured by the test build of the library)."""
     monkeypatch.setenv("ADASUM_ONCHIP", "force")
     monkeypatch.setenv("ADASUM_ONCHIP_MAX_CLUSTER", "16")
 

@@ -129,7 +129,7 @@ def test_fused_pair_symmetric_and_special_cases(native, dtype):
     assert torch.equal(ags.pair(a, b), first)  # deterministic
 
 
-def test_fused_pair_agrees_with_tiled_route(native, monkeypatch):
+def test_fused_pair_agrees_with_tiled_route(native, hooks, monkeypatch):
     a, b = _pair(777_777, torch.float32, seed=17)
     fused = ags.pair(a, b).clone()
     monkeypatch.setenv("ADASUM_PAIR_FUSED", "0")
@@ -141,7 +141,7 @@ def test_fused_pair_agrees_with_tiled_route(native, monkeypatch):
     assert np.linalg.norm(to_f64(tiled) - ref) <= 1e-5 * nr
 
 
-def test_fused_pair_barrier_timeout_is_reported(native, monkeypatch):
+def test_fused_pair_barrier_timeout_is_reported(native, hooks, monkeypatch):
     """Every CTA waits at the grid barrier without arriving (injected on the host): the
     waits run out after their clock budget, the status word says so, and the next call
     (no injection) is correct -- the barrier's state was not disturbed."""

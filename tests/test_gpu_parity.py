@@ -277,7 +277,7 @@ def test_error_codes(native):
     assert ags.get_last_error() == ags.Status.OK
 
 
-def test_alloc_failure_is_reported(native, monkeypatch):
+def test_alloc_failure_is_reported(native, hooks, monkeypatch):
     ags.release_workspace()
     monkeypatch.setenv("ADASUM_FAULT_INJECT", "alloc")
     g = rand_grads(4, 100_000, torch.float32, seed=31)
@@ -356,89 +356,6 @@ def test_well_conditioned_data_stays_on_the_fast_path(native):
     wl = workloads.make("resnet50_k8", device=DEV, shrink=16)
     ags.reduce(wl.grads, wl.seg_offsets)
     assert ags.recomputed_segments() == 0
-
-
-# ------------------------------------------------- both routes, and the bounded wait
-
-@pytest.mark.parametrize("route", ["stream", "fused", "kernels"])
-@pytest.mark.parametrize("name,shrink", [("resnet50_k8", 16), ("bert_large_k16", 256),
-                                         ("pair_1m", 1), ("gpt_k8_momentum", 2048)])
-def test_every_route_matches_oracle(native, monkeypatch, route, name, shrink):
-    """Single-stage calls can run three ways (ADASUM_ROUTE): the three-kernel route, the
-    streaming kernel and the dynamically scheduled fused kernel; each must agree with
-    the oracle."""
-    monkeypatch.setenv("ADASUM_ROUTE", route)
-    wl = workloads.make(name, device=DEV, shrink=shrink)
-    out = ags.reduce(wl.grads, wl.seg_offsets)
-    torch.cuda.synchronize()
-    check_against_oracle(wl.grads, wl.seg_offsets, out)
-
-
-def test_routes_agree(native, monkeypatch):
-    """The fused kernel and the three-kernel route sum the same tiles in the same order.
-    (Small segments normally go to the small-segment kernels and small tiles to the
-    warp Gram, whose sums are blocked differently, so those are switched off for the
-    comparison.)"""
-    wl = workloads.make("bert_large_k16", device=DEV, shrink=128)
-    monkeypatch.setenv("ADASUM_ONCHIP", "0")
-    monkeypatch.setenv("ADASUM_TINY", "0")
-    monkeypatch.setenv("ADASUM_WARP_GRAM", "0")
-    split = ags.reduce(wl.grads, wl.seg_offsets).clone()
-    monkeypatch.setenv("ADASUM_ROUTE", "fused")
-    monkeypatch.setenv("ADASUM_PIPE_TILE_KB", "256")   # same tiles, so the same sums
-    fused = ags.reduce(wl.grads, wl.seg_offsets)
-    torch.cuda.synchronize()
-    assert torch.equal(fused, split)
-
-
-@pytest.mark.parametrize("route", ["stream", "fused"])
-def test_bounded_wait_reports_timeout(native, monkeypatch, route):
-    """A lost ready flag (injected on the host: the kernel never publishes a segment's
-    coefficients) must end in a status, not a hang: the combine tasks give up after
-    their clock budget."""
-    grads = rand_grads(4, 50_000, torch.float32, seed=60)
-    assert ags.get_last_error() == ags.Status.OK
-    monkeypatch.setenv("ADASUM_ROUTE", route)
-    monkeypatch.setenv("ADASUM_FAULT_INJECT", "timeout")
-    ags.reduce(grads, [0, 20_000, 50_000])
-    torch.cuda.synchronize()
-    assert ags.get_last_error() == ags.Status.ERR_TIMEOUT
-    assert ags.get_last_error() == ags.Status.OK          # reading clears it
-    monkeypatch.delenv("ADASUM_FAULT_INJECT")
-    out = ags.reduce(grads, [0, 20_000, 50_000])          # the context is still usable
-    torch.cuda.synchronize()
-    check_against_oracle(grads, [0, 20_000, 50_000], out)
-
-
-@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
-@pytest.mark.parametrize("K", [2, 4, 8, 16])
-def test_stream_route_edges(native, monkeypatch, K, dtype):
-    """Streaming kernel: ragged and unaligned segment boundaries, tiny and empty
-    segments, many waves, several tiles per CTA."""
-    if dtype == torch.float32 and K == 16:
-        pytest.skip("fp32 groups of 16 run the three-kernel route")
-    monkeypatch.setenv("ADASUM_ROUTE", "stream")
-    monkeypatch.setenv("ADASUM_WAVE_MB", "1")
-    lengths = [1, 7, 0, 31, 33, 4097, 300, 65537, 5, 12345, 1_000_003]
-    offs = workloads.offsets_from_numels(lengths)
-    grads = rand_grads(K, int(offs[-1]), dtype, seed=70 + K)
-    out = ags.reduce(grads, offs)
-    torch.cuda.synchronize()
-    check_against_oracle(grads, offs, out)
-    again = ags.reduce(grads, offs)
-    torch.cuda.synchronize()
-    assert torch.equal(out, again)                       # deterministic
-
-
-def test_stream_route_unaligned(native, monkeypatch):
-    monkeypatch.setenv("ADASUM_ROUTE", "stream")
-    K, n = 8, 200_003
-    base = rand_grads(K, n + 3, torch.bfloat16, seed=80)
-    grads = [g[1 + (k % 3): 1 + (k % 3) + n] for k, g in enumerate(base)]
-    offs = np.array([0, 3, 1000, 1001, 140_000, n], dtype=np.int64)
-    out = ags.reduce(grads, offs)
-    torch.cuda.synchronize()
-    check_against_oracle(grads, offs, out)
 
 
 # ------------------------------------------- any worker count; the linear chain
@@ -615,7 +532,7 @@ def test_conditioning_check_keeps_every_segment_accurate(native, K):
         assert err <= 4e-6, (s, err)
 
 
-def test_profiler_counts_each_input_byte_once(native, monkeypatch):
+def test_profiler_counts_each_input_byte_once(native, hooks, monkeypatch):
     """The profiler's algorithmic bytes (what bench.py's roofline divides by): in one
     call, every input byte is counted by exactly one of the kernels that read the inputs
     (the CTA and warp Gram kernels for tiled segments, the on-chip and tiny kernels for
