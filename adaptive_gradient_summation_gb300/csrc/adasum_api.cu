@@ -682,11 +682,13 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
     return st;
 
   // Workspace layout.
-  size_t max_e_tiles = 0, max_e_chunks = 0, max_coef = 0, max_g = 1;
+  size_t max_e_tiles = 0, max_e_chunks = 0, max_coef = 0, max_g = 1, max_k_tiles = 0, max_k_chunks = 0;
   for (size_t s = 0; s < kg.size(); ++s) {
     const size_t E = static_cast<size_t>(kg[s]) * (kg[s] + 1) / 2;
     max_e_tiles = std::max(max_e_tiles, groups[s] * plan->ntiles * E);
     max_e_chunks = std::max(max_e_chunks, groups[s] * plan->nchunks * E);
+    max_k_tiles = std::max(max_k_tiles, static_cast<size_t>(groups[s]) * plan->ntiles * kg[s]);
+    max_k_chunks = std::max(max_k_chunks, static_cast<size_t>(groups[s]) * plan->nchunks * kg[s]);
     max_coef = std::max(max_coef, static_cast<size_t>(groups[s]) * L * kg[s]);
     max_g = std::max(max_g, static_cast<size_t>(groups[s]));
   }
@@ -700,6 +702,8 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
   const size_t o_flags = cv.take(n_ints * sizeof(int));
   const size_t o_part = cv.take(max_e_tiles * sizeof(float));
   const size_t o_chunk = cv.take(max_e_chunks * sizeof(double));
+  const size_t o_tamax = cv.take(max_k_tiles * sizeof(float));
+  const size_t o_camax = cv.take(max_k_chunks * sizeof(float));
   const size_t o_coef = cv.take(max_coef * sizeof(float));
   const size_t o_rel0 = cv.take(max_g * L * sizeof(float));
   const size_t o_rel1 = cv.take(max_g * L * sizeof(float));
@@ -748,6 +752,8 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
     a.chunks = plan->d_chunks;
     a.partials = reinterpret_cast<float*>(base + o_part);
     a.chunk_sums = reinterpret_cast<double*>(base + o_chunk);
+    a.tile_amax = reinterpret_cast<float*>(base + o_tamax);
+    a.chunk_amax = reinterpret_cast<float*>(base + o_camax);
     a.coef = reinterpret_cast<float*>(base + o_coef);
     a.seg_flag = seg_flag;
     a.partials64 = reinterpret_cast<double*>(base + o_part64);

@@ -67,6 +67,10 @@ struct StageArgs {
   const ChunkDesc* chunks;
   float* partials;   // [G][ntiles][E] Gram partials, E = Kg(Kg+1)/2 (upper triangle)
   double* chunk_sums; // [G][nchunks][E] compensated sums of the partials of each chunk
+  // Range check of the fp32 pass (kRangeLo, kRangeHi): every worker's largest |input|
+  // per tile and per chunk (a zero or padding worker gives 0).
+  float* tile_amax;   // [G][ntiles][Kg]
+  float* chunk_amax;  // [G][nchunks][Kg]
   float* coef;       // [G][nsegs][Kg] tree coefficients
   // Fused heavy-ball step (final stage of adasum_reduce_momentum_sgd only).
   float* master_w;
@@ -123,6 +127,13 @@ enum Mode : int { kModeTree = 0, kModeChain = 1 };
 // Gram-entry error model of the fp32 pass, relative to |g_i| |g_j|: products and
 // bounded-length fp32 sums, then compensated sums (a typical-case constant).
 constexpr double kGramRelErr = 4.0 * 5.9604644775390625e-08;   // 4 u, u = 2^-24
+// Range of the fp32 pass.  It is accurate while every nonzero worker's largest |value|
+// in a segment lies in [2^-40, 2^40]: the products of the elements that matter then stay
+// far inside fp32's normal range (no underflow to subnormals or zero, no overflow of a
+// tile's sums).  A segment with a worker outside it is flagged like an ill-conditioned
+// one and recomputed by a path that scales by a power of two first.
+constexpr float kRangeLo = 0x1p-40f;
+constexpr float kRangeHi = 0x1p40f;
 // Estimated relative output error above which a segment is recomputed in fp64.  The
 // estimate is a conservative first-order bound: over random, correlated and nearly
 // cancelling test sets the realised error of the fp32 pass stayed below 0.16 times it,

@@ -134,6 +134,53 @@ __device__ __forceinline__ float vec_elem(const uint4& r, int e) {
   }
 }
 
+// Running largest |element| of one worker's 16-byte vectors, kept as the bits of
+// non-negative fp32 values (for those, unsigned order is value order; NaN sorts above
+// Inf).  bf16 vectors keep two 16-bit maxima packed in one word (per-halfword unsigned
+// max of the sign-cleared bf16 bits), merged by bits().
+template <typename Tag> struct AbsMax;
+template <> struct AbsMax<F32Tag> {
+  uint32_t m = 0u;
+  __device__ __forceinline__ void add(const uint4& r) {
+    m = max(m, max(max(r.x & 0x7FFFFFFFu, r.y & 0x7FFFFFFFu), max(r.z & 0x7FFFFFFFu, r.w & 0x7FFFFFFFu)));
+  }
+  __device__ __forceinline__ uint32_t bits() const { return m; }
+};
+template <> struct AbsMax<BF16Tag> {
+  uint32_t m = 0u;
+  __device__ __forceinline__ void add(const uint4& r) {
+    m = __vmaxu2(m, __vmaxu2(__vmaxu2(r.x & 0x7FFF7FFFu, r.y & 0x7FFF7FFFu),
+                             __vmaxu2(r.z & 0x7FFF7FFFu, r.w & 0x7FFF7FFFu)));
+  }
+  __device__ __forceinline__ uint32_t bits() const { return max(m << 16, m & 0xFFFF0000u); }
+};
+
+__device__ __forceinline__ uint32_t warp_max_u32(uint32_t v) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v = max(v, __shfl_xor_sync(0xFFFFFFFFu, v, off));
+  return v;
+}
+
+// Per-worker maxima of one tile (each thread's KG values, as AbsMax bits) over the CTA,
+// written to tile_amax[(q * ntiles + tile) * KG + k].  Called by the whole CTA.
+template <int KG>
+__device__ __forceinline__ void block_amax_store(const uint32_t (&m)[KG], float* __restrict__ dst) {
+  __shared__ uint32_t red[kThreads / 32][KG];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int k = 0; k < KG; ++k) {
+    const uint32_t v = warp_max_u32(m[k]);
+    if (lane == 0) red[warp][k] = v;
+  }
+  __syncthreads();
+  for (int k = threadIdx.x; k < KG; k += kThreads) {
+    uint32_t v = 0u;
+#pragma unroll
+    for (int w = 0; w < kThreads / 32; ++w) v = max(v, red[w][k]);
+    dst[k] = __uint_as_float(v);
+  }
+}
+
 // Kahan-compensated fp32 accumulation: sum - comp tracks the exact running sum to
 // about one rounding, whatever the number of terms.
 __device__ __forceinline__ void kahan_add(float& sum, float& comp, float x) {
@@ -170,10 +217,12 @@ __device__ __forceinline__ void block_reduce_store(float (&acc)[E], float* __res
 
 // Gram partial of one tile with CUDA-core FMAs: every thread owns whole 16-byte
 // vectors (VW positions of all Kg workers) and accumulates the Kg(Kg+1)/2 products.
-// This thread's products over vectors first, first + step, ... of a tile (acc zeroed).
+// This thread's products over vectors first, first + step, ... of a tile (acc zeroed),
+// and every worker's largest |element| among them (AbsMax bits).
 template <typename Tag, int KG>
 __device__ __forceinline__ void gram_accumulate(const StageArgs& a, const TileDesc& t, int q,
-                                                int first, int step, float (&acc)[tri_count(KG)]) {
+                                                int first, int step, float (&acc)[tri_count(KG)],
+                                                uint32_t (&amax)[KG]) {
   using S = typename ElemTraits<Tag>::Storage;
   constexpr int VW = ElemTraits<Tag>::kVW;
   constexpr int E = tri_count(KG);
@@ -185,10 +234,13 @@ __device__ __forceinline__ void gram_accumulate(const StageArgs& a, const TileDe
   const int64_t v0 = lo / VW, v1 = (hi + VW - 1) / VW;
 #pragma unroll
   for (int e = 0; e < E; ++e) acc[e] = 0.f;
+  AbsMax<Tag> am[KG];
   for (int64_t v = v0 + first; v < v1; v += step) {
     uint4 r[KG];
 #pragma unroll
     for (int k = 0; k < KG; ++k) r[k] = load_vec_raw<Tag, kLoadKeep>(x[k], v, lo, hi, aligned);
+#pragma unroll
+    for (int k = 0; k < KG; ++k) am[k].add(r[k]);
 #pragma unroll
     for (int e = 0; e < VW; ++e) {
       float xe[KG];
@@ -201,14 +253,18 @@ __device__ __forceinline__ void gram_accumulate(const StageArgs& a, const TileDe
           acc[tri_index(KG, i, j)] = __fmaf_rn(xe[i], xe[j], acc[tri_index(KG, i, j)]);
     }
   }
+#pragma unroll
+  for (int k = 0; k < KG; ++k) amax[k] = am[k].bits();
 }
 
 template <typename Tag, int KG>
 __device__ __forceinline__ void gram_tile_simt(const StageArgs& a, int tile_id, int q) {
   constexpr int E = tri_count(KG);
   float acc[E];
-  gram_accumulate<Tag, KG>(a, a.tiles[tile_id], q, threadIdx.x, kThreads, acc);
+  uint32_t amax[KG];
+  gram_accumulate<Tag, KG>(a, a.tiles[tile_id], q, threadIdx.x, kThreads, acc, amax);
   block_reduce_store<E>(acc, a.partials + (static_cast<size_t>(q) * a.ntiles + tile_id) * E);
+  block_amax_store<KG>(amax, a.tile_amax + (static_cast<size_t>(q) * a.ntiles + tile_id) * KG);
 }
 
 // Tile id of this CTA: the CTA kernels run over a.tile_list when the plan splits off
@@ -236,7 +292,8 @@ __global__ void __launch_bounds__(kThreads) gram_warp_kernel(const StageArgs a) 
   const int q = blockIdx.y;
   const int tile_id = a.small_list[w];
   float acc[E];
-  gram_accumulate<Tag, KG>(a, a.tiles[tile_id], q, lane, 32, acc);
+  uint32_t amax[KG];
+  gram_accumulate<Tag, KG>(a, a.tiles[tile_id], q, lane, 32, acc, amax);
 #pragma unroll
   for (int e = 0; e < E; ++e) {
 #pragma unroll
@@ -246,6 +303,12 @@ __global__ void __launch_bounds__(kThreads) gram_warp_kernel(const StageArgs a) 
 #pragma unroll
   for (int e = 0; e < E; ++e)
     if ((e & 31) == lane) dst[e] = acc[e];
+  float* mdst = a.tile_amax + (static_cast<size_t>(q) * a.ntiles + tile_id) * KG;
+#pragma unroll
+  for (int k = 0; k < KG; ++k) {
+    const uint32_t v = warp_max_u32(amax[k]);
+    if ((k & 31) == lane) mdst[k] = __uint_as_float(v);
+  }
 }
 
 // --------------------------------------------------- pass 1: Gram (tensor cores, bf16)
@@ -259,6 +322,34 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
       "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Lane (g, t) of the MMA fragment layout holds positions of workers g and g + 8.  Their
+// maxima (AbsMax bits) over the four lanes of each g, over the warp.
+__device__ __forceinline__ void mma_lane_amax(uint32_t& mg, uint32_t& mh) {
+  mg = max(mg, __shfl_xor_sync(0xFFFFFFFFu, mg, 1));
+  mg = max(mg, __shfl_xor_sync(0xFFFFFFFFu, mg, 2));
+  mh = max(mh, __shfl_xor_sync(0xFFFFFFFFu, mh, 1));
+  mh = max(mh, __shfl_xor_sync(0xFFFFFFFFu, mh, 2));
+}
+
+// The same over the CTA's warps, written to dst[0..KG).  Called by the whole CTA.
+template <int KG>
+__device__ __forceinline__ void mma_amax_store(uint32_t mg, uint32_t mh, float* __restrict__ dst) {
+  __shared__ uint32_t red[kWarps][16];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, g = lane >> 2;
+  mma_lane_amax(mg, mh);
+  if ((lane & 3) == 0) {
+    red[warp][g] = mg;
+    if (KG == 16) red[warp][g + 8] = mh;
+  }
+  __syncthreads();
+  for (int k = threadIdx.x; k < KG; k += kThreads) {
+    uint32_t v = 0u;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) v = max(v, red[w][k]);
+    dst[k] = __uint_as_float(v);
+  }
 }
 
 // Gram partial of one tile of bf16 gradients on the tensor cores (Kg = 8 or 16).
@@ -289,6 +380,7 @@ __device__ __forceinline__ void gram_tile_mma(const StageArgs& a, int tile_id, i
   float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
   float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
   float e0[4] = {0.f, 0.f, 0.f, 0.f}, e1[4] = {0.f, 0.f, 0.f, 0.f};
+  AbsMax<BF16Tag> amg, amh;
   int pending = 0;
   for (int64_t c = c0 + warp; c < c1; c += kWarps * U) {
     uint4 rg[U], rh[U];
@@ -307,6 +399,8 @@ __device__ __forceinline__ void gram_tile_mma(const StageArgs& a, int tile_id, i
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
+      amg.add(rg[u]);
+      amh.add(rh[u]);
       mma_bf16_16816(d0, rg[u].x, rh[u].x, rg[u].y, rh[u].y, rg[u].x, rg[u].y);
       mma_bf16_16816(d0, rg[u].z, rh[u].z, rg[u].w, rh[u].w, rg[u].z, rg[u].w);
       if constexpr (KG == 16) {
@@ -358,6 +452,7 @@ __device__ __forceinline__ void gram_tile_mma(const StageArgs& a, int tile_id, i
     for (int w = 0; w < kWarps; ++w) s = __fadd_rn(s, red[w][idx]);
     dst[tri_index(KG, i, j)] = s;
   }
+  mma_amax_store<KG>(amg.bits(), amh.bits(), a.tile_amax + (static_cast<size_t>(q) * a.ntiles + tile_id) * KG);
 }
 
 // Three bf16 parts of two fp32 values, x = h + m + l exactly: h is x rounded to bf16,
@@ -382,7 +477,8 @@ __device__ __forceinline__ void split_bf16x3(float x0, float x1, uint32_t& h, ui
 template <int KG>
 __device__ __forceinline__ void gram_chunks_mma_f32(const float* xg, const float* xh, int64_t lo, int64_t hi,
                                                     bool aligned, int first, int nw, float (&s0)[4],
-                                                    float (&e0)[4], float (&s1)[4], float (&e1)[4]) {
+                                                    float (&e0)[4], float (&s1)[4], float (&e1)[4],
+                                                    uint32_t& mg, uint32_t& mh) {
   static_assert(KG == 16, "16 workers: two n-tiles of the m16n8k16 MMA");
   constexpr int U = 2;        // chunks of 32 positions loaded per warp iteration
   constexpr int kFold = 4;    // iterations accumulated in the MMA before a Kahan fold
@@ -392,6 +488,7 @@ __device__ __forceinline__ void gram_chunks_mma_f32(const float* xg, const float
   float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int i = 0; i < 4; ++i) s0[i] = e0[i] = s1[i] = e1[i] = 0.f;
+  AbsMax<F32Tag> amg, amh;
   int pending = 0;
   for (int64_t c = c0 + first; c < c1; c += static_cast<int64_t>(nw) * U) {
     uint4 rg[U][2], rh[U][2];
@@ -407,6 +504,10 @@ __device__ __forceinline__ void gram_chunks_mma_f32(const float* xg, const float
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
+      amg.add(rg[u][0]);
+      amg.add(rg[u][1]);
+      amh.add(rh[u][0]);
+      amh.add(rh[u][1]);
       // parts of positions (0,1), (2,3), (4,5), (6,7): registers 0..3 as in gram_tile_mma
       uint32_t gh[4], gm[4], gl[4], hh[4], hm[4], hl[4];
 #pragma unroll
@@ -448,6 +549,8 @@ __device__ __forceinline__ void gram_chunks_mma_f32(const float* xg, const float
     kahan_add(s0[i], e0[i], d0[i]);
     kahan_add(s1[i], e1[i], d1[i]);
   }
+  mg = amg.bits();
+  mh = amh.bits();
 }
 
 // A lane's compensated sums into the KG x KG matrix m (row-major), as laid out by the MMA.
@@ -479,8 +582,9 @@ __device__ __forceinline__ void gram_tile_mma_f32(const StageArgs& a, int tile_i
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2;
   float s0[4], e0[4], s1[4], e1[4];
+  uint32_t mg, mh;
   gram_chunks_mma_f32<KG>(static_cast<const float*>(a.in[q * KG + g]), static_cast<const float*>(a.in[q * KG + g + 8]),
-                          t.start, t.start + t.len, a.aligned != 0, warp, kWarps, s0, e0, s1, e1);
+                          t.start, t.start + t.len, a.aligned != 0, warp, kWarps, s0, e0, s1, e1, mg, mh);
   __shared__ float red[kWarps][KG * KG];
   store_lane_gram16(red[warp], s0, e0, s1, e1);
   __syncthreads();
@@ -494,6 +598,7 @@ __device__ __forceinline__ void gram_tile_mma_f32(const StageArgs& a, int tile_i
       s = __fadd_rn(s, i == j ? red[w][idx] : 0.5f * __fadd_rn(red[w][idx], red[w][j * KG + i]));
     dst[tri_index(KG, i, j)] = s;
   }
+  mma_amax_store<KG>(mg, mh, a.tile_amax + (static_cast<size_t>(q) * a.ntiles + tile_id) * KG);
 }
 
 // Gram partials of small tiles of fp32 gradients (16 workers), one warp per (tile,
@@ -513,8 +618,9 @@ __global__ void __launch_bounds__(kThreads, 3) gram_warp_mma_f32_kernel(const St
   const TileDesc t = a.tiles[tile_id];
   const int g = lane >> 2;
   float s0[4], e0[4], s1[4], e1[4];
+  uint32_t mg, mh;
   gram_chunks_mma_f32<KG>(static_cast<const float*>(a.in[q * KG + g]), static_cast<const float*>(a.in[q * KG + g + 8]),
-                          t.start, t.start + t.len, a.aligned != 0, 0, 1, s0, e0, s1, e1);
+                          t.start, t.start + t.len, a.aligned != 0, 0, 1, s0, e0, s1, e1, mg, mh);
   float* m = red[wb];
   store_lane_gram16(m, s0, e0, s1, e1);
   __syncwarp();
@@ -523,6 +629,12 @@ __global__ void __launch_bounds__(kThreads, 3) gram_warp_mma_f32_kernel(const St
     int i, j;
     tri_unpack(KG, e, i, j);
     dst[e] = i == j ? m[i * KG + i] : 0.5f * __fadd_rn(m[i * KG + j], m[j * KG + i]);
+  }
+  mma_lane_amax(mg, mh);
+  if ((lane & 3) == 0) {
+    float* mdst = a.tile_amax + (static_cast<size_t>(q) * a.ntiles + tile_id) * KG;
+    mdst[g] = __uint_as_float(mg);
+    mdst[g + 8] = __uint_as_float(mh);
   }
 }
 
@@ -571,6 +683,14 @@ __device__ __forceinline__ void reduce_chunk(const StageArgs& a, int c, int q) {
     for (int t = 0; t < kChunkTiles; ++t) kahan_add(sum, comp, v[t]);
     a.chunk_sums[(static_cast<size_t>(q) * a.nchunks + c) * E + e] =
         static_cast<double>(sum) - static_cast<double>(comp);
+  }
+  // every worker's largest |input| over the chunk (NaN inputs do not count here: they
+  // reach the output through the sums)
+  for (int k = threadIdx.x; k < KG; k += blockDim.x) {
+    const float* p = a.tile_amax + (static_cast<size_t>(q) * a.ntiles + ch.first_tile) * KG + k;
+    float m = 0.f;
+    for (int t = 0; t < ch.ntiles; ++t) m = fmaxf(m, __ldcg(p + static_cast<size_t>(t) * KG));
+    a.chunk_amax[(static_cast<size_t>(q) * a.nchunks + c) * KG + k] = m;
   }
 }
 
@@ -1149,6 +1269,17 @@ __device__ __forceinline__ void segment_coefficients(const StageArgs& a, int seg
   __shared__ double eps[KG];
   __shared__ double snorm[KG];
   __shared__ float tree_sh[tree_scratch_floats(KG)];
+  __shared__ int out_of_range;
+  if (threadIdx.x == 0) out_of_range = 0;
+  __syncthreads();
+  // range check: a nonzero worker whose largest |input| lies outside [kRangeLo, kRangeHi]
+  // (an infinite one is left to propagate, like NaN)
+  for (int k = threadIdx.x; k < KG; k += blockDim.x) {
+    const float* p = a.chunk_amax + (static_cast<size_t>(q) * a.nchunks + sd.first_chunk) * KG + k;
+    float m = 0.f;
+    for (int t = 0; t < sd.nchunks; ++t) m = fmaxf(m, __ldcg(p + static_cast<size_t>(t) * KG));
+    if (m > 0.f && (m < kRangeLo || (m > kRangeHi && !isinf(m)))) out_of_range = 1;
+  }
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     double sum = 0.0;
     const double* p = a.chunk_sums + (static_cast<size_t>(q) * a.nchunks + sd.first_chunk) * E + e;
@@ -1183,7 +1314,7 @@ __device__ __forceinline__ void segment_coefficients(const StageArgs& a, int seg
       a.coef[(static_cast<size_t>(q) * a.nsegs + seg) * KG + threadIdx.x] = static_cast<float>(c);
     if (threadIdx.x == 0) {
       if (a.relerr) a.relerr[static_cast<size_t>(q) * a.nsegs + seg] = static_cast<float>(fmin(rel, 1e30));
-      if (a.seg_flag && sd.len > 0 && (ill || !(rel <= kRelErrBudget))) a.seg_flag[seg] = 1;
+      if (a.seg_flag && sd.len > 0 && (ill || !(rel <= kRelErrBudget) || out_of_range)) a.seg_flag[seg] = 1;
     }
   }
   __syncthreads();

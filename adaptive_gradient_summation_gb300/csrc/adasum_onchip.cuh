@@ -151,6 +151,7 @@ __global__ void __launch_bounds__(kOnchipThreads, 2) onchip_kernel(const OnchipA
   __shared__ int t2flag;
   __shared__ __align__(16) unsigned char xch[2][kXch];
   __shared__ int flag;
+  __shared__ uint32_t kmax[K];  // every worker's largest |input| in this CTA's share
   __shared__ __align__(8) uint64_t bar;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -214,6 +215,14 @@ __global__ void __launch_bounds__(kOnchipThreads, 2) onchip_kernel(const OnchipA
   if (a.recompute_only && tid == 0) flag = 1;
   __syncthreads();
   if (!a.recompute_only) {
+    // range check of the fp32 pass (kRangeLo, kRangeHi), evaluated after the next
+    // cluster barrier: this CTA's share first
+    for (int k = warp; k < K; k += kOnchipWarps) {
+      AbsMax<InTag> m;
+      for (int v = lane; v < nvec; v += 32) m.add(*reinterpret_cast<const uint4*>(data + k * rs + v * 16));
+      const uint32_t b = warp_max_u32(m.bits());
+      if (lane == 0) kmax[k] = b;
+    }
 
     // ---------------------------------------------------------------- stage 1: Gram
     if (tid < NB * SL) {
@@ -268,6 +277,16 @@ __global__ void __launch_bounds__(kOnchipThreads, 2) onchip_kernel(const OnchipA
         if (i <= j) xg[q * E1 + tri_index(KG1, i, j)] = __fsub_rn(sum, comp);
       }
       cta_or_cluster_sync(C);
+      // a nonzero worker whose largest |input| over the cluster is outside the range
+      // sends the segment to the recompute (every CTA reads the same values, so all
+      // take the same decision; Inf and NaN are left to propagate)
+      for (int k = tid; k < K; k += kOnchipThreads) {
+        uint32_t m = kmax[k];
+        for (uint32_t r = 0; r < C; ++r)
+          if (r != rank) m = max(m, *map_rank(&kmax[k], r));
+        const float mf = __uint_as_float(m);
+        if (mf > 0.f && (mf < kRangeLo || (mf > kRangeHi && !isinf(mf)))) flag = 1;
+      }
       // the Gram matrices of this CTA's groups: compensated sums over the cluster, CTA order
       for (int e = tid; e < NG * E1; e += kOnchipThreads) {
         const int q = e / E1;

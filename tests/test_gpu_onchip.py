@@ -219,6 +219,21 @@ def test_tiny_segments_extreme_magnitudes(native, scale):
     check_against_oracle(grads, offs, out)
 
 
+@pytest.mark.parametrize("scale", [1e-22, 1e25])
+@pytest.mark.parametrize("K", [4, 16, 64])
+def test_onchip_fast_pass_extreme_magnitudes(native, K, scale):
+    """Small segments held on chip whose squares leave fp32's range: the fast pass's
+    range check (every worker's largest |value| over the cluster) sends them to the
+    recompute, which scales them by a power of two first."""
+    lengths = [40, 300, 1000, 2 * positions_per_cta(K) + 7]
+    offs = workloads.offsets_from_numels(lengths)
+    grads = [g * scale for g in rand_grads(K, int(offs[-1]), torch.float32, seed=960 + K, corr=0.4)]
+    out = ags.reduce(grads, offs)
+    torch.cuda.synchronize()
+    check_against_oracle(grads, offs, out)
+    assert ags.recomputed_segments() == len(lengths)
+
+
 @pytest.mark.parametrize("K", [2, 16])
 def test_flagged_tiled_segments(native, monkeypatch, K):
     """Segments that take the tiled route and get flagged: those that fit 16 CTAs are

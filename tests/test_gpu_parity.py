@@ -358,6 +358,64 @@ def test_well_conditioned_data_stays_on_the_fast_path(native):
     assert ags.recomputed_segments() == 0
 
 
+# ------------------------------------------ magnitudes far outside fp32's comfortable range
+
+@pytest.mark.parametrize("scale", [1e-22, 1e-20, 1e20, 1e25])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("K", [2, 16, 64])
+def test_tiled_segments_extreme_magnitudes(native, K, dtype, scale):
+    """Tiled segments whose squares would underflow or overflow fp32: the fp32 pass finds
+    every worker's largest |value| outside [2^-40, 2^40], flags the segments, and the
+    recompute (which scales each segment by a power of two first) takes them: the
+    5,000-position segment on chip, the longer ones in the fp64 path.  (Three segments,
+    so two workers do not take the single-kernel pair route.)"""
+    lengths = [70_001, 5_000, 90_000]
+    offs = workloads.offsets_from_numels(lengths)
+    grads = [(g * scale).to(dtype)
+             for g in rand_grads(K, int(offs[-1]), torch.float32, seed=900 + K, corr=0.5)]
+    out = ags.reduce(grads, offs)
+    torch.cuda.synchronize()
+    check_against_oracle(grads, offs, out)
+    assert ags.recomputed_segments() == len(lengths)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_range_check_flags_only_segments_out_of_range(native, dtype):
+    """Only the segment outside the range is recomputed; values just inside the range
+    (largest |value| about 1e-11 > 2^-40) stay on the fp32 pass and are accurate."""
+    K = 16
+    lengths = [70_001, 90_000, 80_000]
+    offs = workloads.offsets_from_numels(lengths)
+    scales = torch.ones(int(offs[-1]), device=DEV)
+    scales[offs[1]:offs[2]] = 1e-24
+    scales[offs[2]:] = 2e-12
+    grads = [(g * scales).to(dtype)
+             for g in rand_grads(K, int(offs[-1]), torch.float32, seed=930, corr=0.5)]
+    out = ags.reduce(grads, offs)
+    torch.cuda.synchronize()
+    check_against_oracle(grads, offs, out)
+    assert ags.recomputed_segments() == 1
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_one_worker_far_smaller_than_the_others(native, dtype):
+    """One worker at about 1e-16 among workers of order 1: its squares lose their
+    precision in fp32 (and a smaller operand still moves the result: the pair subtracts
+    half the other's projection on it), so the range check sends the segment to the
+    recompute, where the segment's power-of-two scale keeps that worker's squares
+    normal."""
+    K = 8
+    lengths = [70_001, 33_000]
+    offs = workloads.offsets_from_numels(lengths)
+    grads = rand_grads(K, int(offs[-1]), torch.float32, seed=940, corr=0.5)
+    grads[3] = grads[3] * 1e-16
+    grads = [g.to(dtype) for g in grads]
+    out = ags.reduce(grads, offs)
+    torch.cuda.synchronize()
+    check_against_oracle(grads, offs, out)
+    assert ags.recomputed_segments() == len(lengths)
+
+
 # ------------------------------------------- any worker count; the linear chain
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
