@@ -67,15 +67,20 @@ __global__ void __launch_bounds__(kThreads) pair_gram_kernel(const void* a, cons
   block_reduce_store<3>(acc, scratch + 4 * tile);
 }
 
-// One CTA: compensated sums of the tile partials in tile order, then the coefficients
-// in fp64 (a zero-norm operand gets coefficient 1).
-__global__ void pair_coef_kernel(int ntiles, float* scratch) {
+// One CTA of three warps, warp w summing quantity w (a.b, |a|^2, |b|^2) of the tile
+// partials: lane l takes tiles l, l + 32, ... (compensated fp32, in tile order), then
+// the lanes' sums are added in fp64 by a fixed butterfly, so the result is the same bits
+// on every run.  Then the coefficients in fp64 (a zero-norm operand gets coefficient 1).
+constexpr int kCoefThreads = 96;
+__global__ void __launch_bounds__(kCoefThreads) pair_coef_kernel(int ntiles, float* scratch) {
   __shared__ double sums[3];
-  if (threadIdx.x < 3) {
-    float s = 0.f, comp = 0.f;
-    for (int t = 0; t < ntiles; ++t) kahan_add(s, comp, scratch[4 * t + threadIdx.x]);
-    sums[threadIdx.x] = static_cast<double>(s) - static_cast<double>(comp);
-  }
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float s = 0.f, comp = 0.f;
+  for (int t = lane; t < ntiles; t += 32) kahan_add(s, comp, scratch[4 * t + w]);
+  double v = static_cast<double>(s) - static_cast<double>(comp);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
+  if (lane == 0) sums[w] = v;
   __syncthreads();
   if (threadIdx.x == 0) {
     const double d = sums[0], p = sums[1], q = sums[2];
@@ -138,6 +143,17 @@ adasum_status_t scratch_for_current_device(float** out) {
   return ADASUM_OK;
 }
 
+// One launch through cudaLaunchKernelEx, whose return value is that launch's own error.
+template <typename... KArgs, typename... Args>
+cudaError_t launch(void (*kernel)(KArgs...), int grid, int block, cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 bool overlap(const void* p, const void* q, size_t bytes) {
   const uintptr_t x = reinterpret_cast<uintptr_t>(p), y = reinterpret_cast<uintptr_t>(q);
   return x < y + bytes && y < x + bytes;
@@ -165,14 +181,14 @@ extern "C" adasum_status_t adasum_pair_noalloc(const void* a, const void* b, int
                         reinterpret_cast<uintptr_t>(out)) & 15u) == 0;
   const int ntiles = static_cast<int>((n + kTile - 1) / kTile);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (dtype == ADASUM_BF16) {
-    pair_gram_kernel<BF16Tag><<<ntiles, kThreads, 0, s>>>(a, b, n, aligned, scratch);
-    pair_coef_kernel<<<1, 32, 0, s>>>(ntiles, scratch);
-    pair_combine_kernel<BF16Tag><<<ntiles, kThreads, 0, s>>>(a, b, out, n, aligned, scratch);
-  } else {
-    pair_gram_kernel<F32Tag><<<ntiles, kThreads, 0, s>>>(a, b, n, aligned, scratch);
-    pair_coef_kernel<<<1, 32, 0, s>>>(ntiles, scratch);
-    pair_combine_kernel<F32Tag><<<ntiles, kThreads, 0, s>>>(a, b, out, n, aligned, scratch);
-  }
-  return cudaGetLastError() == cudaSuccess ? ADASUM_OK : ADASUM_ERR_CUDA;
+  // Each launch's own return code decides the status (an error left pending by other
+  // code on this thread is neither reported as this call's nor cleared).
+  const bool bf16 = dtype == ADASUM_BF16;
+  if (launch(bf16 ? pair_gram_kernel<BF16Tag> : pair_gram_kernel<F32Tag>, ntiles, kThreads, s,
+             a, b, n, aligned, scratch) != cudaSuccess ||
+      launch(pair_coef_kernel, 1, kCoefThreads, s, ntiles, scratch) != cudaSuccess ||
+      launch(bf16 ? pair_combine_kernel<BF16Tag> : pair_combine_kernel<F32Tag>, ntiles, kThreads, s,
+             a, b, out, n, aligned, static_cast<const float*>(scratch)) != cudaSuccess)
+    return ADASUM_ERR_CUDA;
+  return ADASUM_OK;
 }

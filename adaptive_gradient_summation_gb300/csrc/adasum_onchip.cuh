@@ -216,12 +216,17 @@ __global__ void __launch_bounds__(kOnchipThreads, 2) onchip_kernel(const OnchipA
   __syncthreads();
   if (!a.recompute_only) {
     // range check of the fp32 pass (kRangeLo, kRangeHi), evaluated after the next
-    // cluster barrier: this CTA's share first
-    for (int k = warp; k < K; k += kOnchipWarps) {
+    // cluster barrier: this CTA's share first, TPR consecutive threads per row
+    {
+      constexpr int TPR = K >= 8 ? kOnchipThreads / K : 32;
+      const int k = tid / TPR, j = tid % TPR;
       AbsMax<InTag> m;
-      for (int v = lane; v < nvec; v += 32) m.add(*reinterpret_cast<const uint4*>(data + k * rs + v * 16));
-      const uint32_t b = warp_max_u32(m.bits());
-      if (lane == 0) kmax[k] = b;
+      if (k < K)
+        for (int v = j; v < nvec; v += TPR) m.add(*reinterpret_cast<const uint4*>(data + k * rs + v * 16));
+      uint32_t b = m.bits();
+#pragma unroll
+      for (int off = TPR / 2; off > 0; off >>= 1) b = max(b, __shfl_xor_sync(0xFFFFFFFFu, b, off));
+      if (k < K && j == 0) kmax[k] = b;
     }
 
     // ---------------------------------------------------------------- stage 1: Gram

@@ -43,6 +43,14 @@
  * at most 32 positions, and segments whose error estimate flags them, are evaluated in
  * vector space in double-float or fp64 (see adasum_recomputed_segments).
  *
+ * Range: the fp32 pass is used for a segment while every nonzero worker's largest |value|
+ * in it lies in [2^-40, 2^40] (squares and products then stay normal fp32 numbers).  A
+ * segment with a worker outside that range is detected and recomputed by a path that
+ * first scales the segment by a power of two, so any magnitude fp32 or bf16 can hold is
+ * combined to the stated accuracy.  The remaining limit: inside one segment, workers whose
+ * largest magnitudes differ by more than a factor of about 2^60 lose the smaller
+ * worker's precision (one power of two scales the whole segment).
+ *
  * Alignment: buffers aligned to 16 bytes take the vectorised path; others are accepted
  * and take a scalar-load path inside the same kernels (slower, same results).
  *
@@ -242,8 +250,12 @@ ADASUM_API int adasum_version(void);
  *
  * Limits and errors: 0 <= n <= ADASUM_NOALLOC_MAX_N, else ADASUM_ERR_INVALID_ARG (n < 0)
  * or ADASUM_ERR_UNSUPPORTED (n too large); out may equal a or b, other overlap is
- * ADASUM_ERR_ALIAS.  It runs the fp32 pass only: unlike adasum_pair it does not detect
- * and recompute ill-conditioned (strongly cancelling) inputs in fp64.
+ * ADASUM_ERR_ALIAS; argument errors are found before anything is enqueued.
+ * ADASUM_ERR_CUDA reports a failure of one of the call's own three launches (an error
+ * left pending by other code on the thread is neither reported nor cleared here).
+ * It runs the fp32 pass only: unlike adasum_pair it does not detect and recompute
+ * ill-conditioned (strongly cancelling) inputs in fp64, and it needs the largest |a_i|
+ * and |b_i| inside about [2^-40, 2^40], where their squares stay normal fp32 numbers.
  */
 #define ADASUM_NOALLOC_MAX_N 33554432
 ADASUM_API adasum_status_t adasum_pair_noalloc(const void *a, const void *b, int64_t n,
