@@ -206,67 +206,43 @@ def local_momentum_reduce(grads, seg_offsets, momenta, master_w: torch.Tensor, *
     return master_w, momenta
 
 
-def segment_groups(offs, bytes_per_position: int, chunk_bytes: int) -> list:
-    """Consecutive segments grouped into runs of about ``chunk_bytes`` of input: a group
-    closes once it holds at least ``chunk_bytes`` (so a segment longer than that is a
-    group of its own) or at the last segment.  Returns [(first, end), ...] segment index
-    ranges that cover every segment once, in order."""
-    offs = np.asarray(offs, dtype=np.int64)
-    L = offs.shape[0] - 1
-    groups, s0 = [], 0
-    for s in range(1, L + 1):
-        if (offs[s] - offs[s0]) * bytes_per_position >= chunk_bytes or s == L:
-            groups.append((s0, s))
-            s0 = s
-    return groups
-
-
 def reduce_from_host(grads_host: Sequence[torch.Tensor], seg_offsets=None, *,
-                     device: torch.device | str = "cuda", staging: list | None = None,
                      out_host: torch.Tensor | None = None,
-                     chunk_bytes: int = 1 << 30) -> torch.Tensor:
-    """End-to-end Adasum of gradients held in (preferably pinned) host memory: copy them
-    to the device, run ``adasum_reduce``, copy the result back, and wait for it.
+                     stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+    """End-to-end Adasum of gradients held in host memory (``adasum_reduce_host``): the
+    library copies them to the current device, combines them and copies the result back,
+    pipelining groups of whole segments so that transfers and compute overlap, and
+    returns once ``out_host`` holds the result.
 
-    The segments are processed in groups of about ``chunk_bytes`` of input (a longer
-    segment is a group of its own): the copy of group i+1 runs on a copy stream while
-    group i is reduced, and each group's result is copied back on a third stream as soon
-    as it is ready, so the transfer time, not the sum of transfer and compute, sets the
-    pace.
-
-    staging: optional list of K device tensors to copy into (reused across calls).
-    out_host: optional host tensor for the result (pinned for an asynchronous copy).
+    grads_host: K 1-D CPU tensors (float32 or bfloat16, equal length; pinned memory is
+    copied asynchronously at full speed).  out_host: optional CPU tensor for the result
+    (pinned by default); it may be one of the inputs.
     """
     grads_host = list(grads_host)
-    K = len(grads_host)
-    n = grads_host[0].numel()
-    dtype = grads_host[0].dtype
-    device = torch.device(device)
+    if not grads_host:
+        raise ValueError("need at least one gradient")
+    g0 = grads_host[0]
+    if g0.dtype not in _DTYPE_CODE:
+        raise TypeError(f"gradients must be float32 or bfloat16, got {g0.dtype}")
+    n = g0.numel()
+    for g in grads_host:
+        if g.device.type != "cpu" or g.dtype != g0.dtype or g.dim() != 1 or g.numel() != n \
+                or not g.is_contiguous():
+            raise ValueError("host gradients must be contiguous 1-D CPU tensors of one dtype and length")
     offs = _offsets(seg_offsets, n)
-    if staging is None:
-        staging = [torch.empty(n, dtype=dtype, device=device) for _ in range(K)]
     if out_host is None:
-        out_host = torch.empty(n, dtype=dtype, pin_memory=True)
-    res = torch.empty(n, dtype=dtype, device=device)
-    groups = segment_groups(offs, K * grads_host[0].element_size(), chunk_bytes)
-    compute = torch.cuda.current_stream(device)
-    copy_in = torch.cuda.Stream(device)
-    copy_out = torch.cuda.Stream(device)
-    copy_in.wait_stream(compute)   # the staging buffers may still be read by earlier work
-    for a, b in groups:
-        p0, p1 = int(offs[a]), int(offs[b])
-        if p1 == p0:
-            continue
-        with torch.cuda.stream(copy_in):
-            for dst, src in zip(staging, grads_host):
-                dst[p0:p1].copy_(src[p0:p1], non_blocking=True)
-        compute.wait_stream(copy_in)
-        reduce([d[p0:p1] for d in staging], offs[a:b + 1] - p0, out=res[p0:p1])
-        copy_out.wait_stream(compute)
-        with torch.cuda.stream(copy_out):
-            out_host[p0:p1].copy_(res[p0:p1], non_blocking=True)
-    compute.wait_stream(copy_out)
-    compute.synchronize()
+        out_host = torch.empty(n, dtype=g0.dtype, pin_memory=True)
+    elif (out_host.device.type != "cpu" or out_host.dtype != g0.dtype or out_host.numel() != n
+          or not out_host.is_contiguous()):
+        raise ValueError("out_host must be a contiguous CPU tensor like the gradients")
+    lib = load_library()
+    K = len(grads_host)
+    ptrs = (ctypes.c_void_p * K)(*[g.data_ptr() for g in grads_host])
+    device = torch.device("cuda", torch.cuda.current_device())
+    st = lib.adasum_reduce_host(ptrs, K, offs.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
+                                offs.shape[0] - 1, _DTYPE_CODE[g0.dtype],
+                                ctypes.c_void_p(out_host.data_ptr()), _stream_handle(device, stream))
+    check(st, "adasum_reduce_host")
     return out_host
 
 

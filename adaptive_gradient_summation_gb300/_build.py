@@ -6,7 +6,10 @@ Only the C ABI symbols of include/adasum.h are exported.
 
 Two variants are built from the same sources:
   libadasum_gb300.so       the product: reads no environment variable
-  libadasum_gb300_test.so  the test build (-DADASUM_TEST_HOOKS): also honours the
+  libadasum_gb300_test.so  the test build (-DADASUM_TEST_HOOKS -DADASUM_BOUNDS_CHECK):
+                           device-side index checks on every tile, chunk and segment
+                           descriptor (a failure sets a status bit, adasum_get_last_error
+                           reports ADASUM_ERR_BOUNDS; nothing traps), and it also honours the
                            switches the tests use to force a route, switch a kernel off
                            or inject a fault on the host (ADASUM_ONCHIP, ADASUM_TINY,
                            ADASUM_WARP_GRAM, ADASUM_ONCHIP_FAST, ADASUM_ONCHIP_MAX_CLUSTER,
@@ -29,7 +32,7 @@ LIB_NAME = "libadasum_gb300.so"
 LIB_PATH = os.path.join(PKG, LIB_NAME)
 TEST_LIB_NAME = "libadasum_gb300_test.so"
 TEST_LIB_PATH = os.path.join(PKG, TEST_LIB_NAME)
-TEST_FLAGS = ["-DADASUM_TEST_HOOKS"]
+TEST_FLAGS = ["-DADASUM_TEST_HOOKS", "-DADASUM_BOUNDS_CHECK"]
 
 SOURCES = ["adasum_api.cu", "launch_f32.cu", "launch_bf16.cu", "launch_f64.cu",
            "launch_onchip.cu", "adasum_noalloc.cu"]

@@ -23,6 +23,7 @@ class Status(enum.IntEnum):
     ERR_NO_MEMORY = 4
     ERR_CUDA = 5
     ERR_TIMEOUT = 6
+    ERR_BOUNDS = 7
 
 
 class AdasumError(RuntimeError):
@@ -43,6 +44,9 @@ SIGNATURES = {
     "adasum_reduce": (ctypes.c_int, [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int,
                                      ctypes.POINTER(ctypes.c_int64), ctypes.c_int,
                                      ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]),
+    "adasum_reduce_host": (ctypes.c_int, [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int,
+                                          ctypes.POINTER(ctypes.c_int64), ctypes.c_int,
+                                          ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]),
     "adasum_reduce_orthogonality": (ctypes.c_int, [
         ctypes.POINTER(ctypes.c_void_p), ctypes.c_int, ctypes.POINTER(ctypes.c_int64),
         ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
@@ -66,6 +70,7 @@ SIGNATURES = {
     "adasum_release_workspace": (ctypes.c_int, []),
     "adasum_version": (ctypes.c_int, []),
     "adasum_launch_count": (ctypes.c_int64, []),
+    "adasum_debug_workspace_guards": (ctypes.c_int64, []),
     "adasum_recomputed_segments": (ctypes.c_int64, []),
     "adasum_profile_enable": (ctypes.c_int, [ctypes.c_int]),
     "adasum_profile_collect": (ctypes.c_int, [ctypes.POINTER(KernelStat), ctypes.c_int]),

@@ -8,6 +8,7 @@
 // pass 2 (out = sum_k c_k g_k).  Trees of more than 16 leaves run as stages: 16-leaf
 // subtrees first (fp32 intermediates in the workspace), then the tree over their roots.
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <algorithm>
 #include <cstdlib>
@@ -57,6 +58,24 @@ bool env_on(const char* name, bool dflt) {
   return std::strcmp(v, "0") != 0;
 }
 
+
+// NVTX range over one phase of a call (what the host enqueues in it), for profilers
+// that collect NVTX ranges; inactive otherwise.
+struct Range {
+  explicit Range(const char* name) { nvtxRangePushA(name); }
+  void next(const char* name) {  // ends this phase and starts the next
+    nvtxRangePop();
+    nvtxRangePushA(name);
+  }
+  ~Range() { nvtxRangePop(); }
+  Range(const Range&) = delete;
+  Range& operator=(const Range&) = delete;
+};
+
+// Test build: every workspace region is followed by a guard band filled with a pattern
+// at the start of each call; adasum_debug_workspace_guards counts the bytes that lost it.
+constexpr size_t kGuardBytes = 256;
+constexpr unsigned char kGuardByte = 0xA5;
 
 // ------------------------------------------------------------------------ profiler
 
@@ -160,6 +179,48 @@ struct SideStream {
   }
 };
 
+// Device staging of adasum_reduce_host: two slots, each holding K input rows and one
+// output row of the largest segment group, and three streams (host-to-device copies,
+// reductions, device-to-host copies) with the events that order them.
+struct HostPipe {
+  void* buf = nullptr;
+  size_t cap = 0;
+  cudaStream_t in = nullptr, compute = nullptr, out = nullptr;
+  cudaEvent_t start = nullptr, h2d[2] = {nullptr, nullptr}, reduced[2] = {nullptr, nullptr},
+              d2h[2] = {nullptr, nullptr};
+
+  adasum_status_t init() {
+    if (in != nullptr) return ADASUM_OK;
+    bool ok = cudaStreamCreateWithFlags(&in, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&compute, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&out, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaEventCreateWithFlags(&start, cudaEventDisableTiming) == cudaSuccess;
+    for (int i = 0; i < 2 && ok; ++i)
+      ok = cudaEventCreateWithFlags(&h2d[i], cudaEventDisableTiming) == cudaSuccess &&
+           cudaEventCreateWithFlags(&reduced[i], cudaEventDisableTiming) == cudaSuccess &&
+           cudaEventCreateWithFlags(&d2h[i], cudaEventDisableTiming) == cudaSuccess;
+    if (!ok) {
+      cudaGetLastError();
+      destroy();
+      return ADASUM_ERR_CUDA;
+    }
+    return ADASUM_OK;
+  }
+  void destroy() {
+    for (cudaStream_t* st : {&in, &compute, &out}) {
+      if (*st) cudaStreamDestroy(*st);
+      *st = nullptr;
+    }
+    for (cudaEvent_t* e : {&start, &h2d[0], &h2d[1], &reduced[0], &reduced[1], &d2h[0], &d2h[1]}) {
+      if (*e) cudaEventDestroy(*e);
+      *e = nullptr;
+    }
+    if (buf) cudaFree(buf);
+    buf = nullptr;
+    cap = 0;
+  }
+};
+
 struct Workspace {
   int device = -1;
   void* buf = nullptr;
@@ -173,6 +234,8 @@ struct Workspace {
   // the fused pair kernel's partials, grid-barrier words and four zero counters
   // (allocated and zeroed on its first use)
   void* pair_buf = nullptr;
+  HostPipe host;                    // staging of adasum_reduce_host
+  std::vector<size_t> guards;       // test build: guard-band offsets of the last call
 };
 
 std::vector<Workspace> g_ws;
@@ -509,9 +572,14 @@ adasum_status_t run_stage64(StageArgs& a, int in_dtype, int out_dtype, int momen
 // Carves the workspace: returns the byte offset of a region of `bytes` and advances.
 struct Carver {
   size_t off = 0;
+  std::vector<size_t> guards;  // test build: a guard band after every region
   size_t take(size_t bytes) {
     const size_t at = off;
     off = align_up(off + bytes, 256);
+#ifdef ADASUM_TEST_HOOKS
+    guards.push_back(off);
+    off += kGuardBytes;
+#endif
     return at;
   }
 };
@@ -677,18 +745,20 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
   // flagged tiled segments that fit are recomputed by the on-chip kernel
   const int rc_cmax = (plain && K <= kOnchipMaxK && env_on("ADASUM_ONCHIP", true)) ? onchip_max_cluster(dtype, K) : 0;
   Plan* plan = nullptr;
+  Range phase("adasum:plan");
   if (adasum_status_t st = get_plan(ws, offs, L, kg[0], dtype, rc_cmax > 0 ? K : onchip_K, onchip_cmax,
                                     onchip_force, rc_cmax, tiny_on, env_on("ADASUM_WARP_GRAM", true), &plan))
     return st;
 
+  phase.next("adasum:workspace");
   // Workspace layout.
-  size_t max_e_tiles = 0, max_e_chunks = 0, max_coef = 0, max_g = 1, max_k_tiles = 0, max_k_chunks = 0;
+  size_t max_e_tiles = 0, max_e_chunks = 0, max_coef = 0, max_g = 1, max_g_tiles = 0, max_g_chunks = 0;
   for (size_t s = 0; s < kg.size(); ++s) {
     const size_t E = static_cast<size_t>(kg[s]) * (kg[s] + 1) / 2;
     max_e_tiles = std::max(max_e_tiles, groups[s] * plan->ntiles * E);
     max_e_chunks = std::max(max_e_chunks, groups[s] * plan->nchunks * E);
-    max_k_tiles = std::max(max_k_tiles, static_cast<size_t>(groups[s]) * plan->ntiles * kg[s]);
-    max_k_chunks = std::max(max_k_chunks, static_cast<size_t>(groups[s]) * plan->nchunks * kg[s]);
+    max_g_tiles = std::max(max_g_tiles, static_cast<size_t>(groups[s]) * plan->ntiles);
+    max_g_chunks = std::max(max_g_chunks, static_cast<size_t>(groups[s]) * plan->nchunks);
     max_coef = std::max(max_coef, static_cast<size_t>(groups[s]) * L * kg[s]);
     max_g = std::max(max_g, static_cast<size_t>(groups[s]));
   }
@@ -702,8 +772,8 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
   const size_t o_flags = cv.take(n_ints * sizeof(int));
   const size_t o_part = cv.take(max_e_tiles * sizeof(float));
   const size_t o_chunk = cv.take(max_e_chunks * sizeof(double));
-  const size_t o_tamax = cv.take(max_k_tiles * sizeof(float));
-  const size_t o_camax = cv.take(max_k_chunks * sizeof(float));
+  const size_t o_tnz = cv.take(max_g_tiles * sizeof(uint32_t));
+  const size_t o_cnz = cv.take(max_g_chunks * sizeof(uint32_t));
   const size_t o_coef = cv.take(max_coef * sizeof(float));
   const size_t o_rel0 = cv.take(max_g * L * sizeof(float));
   const size_t o_rel1 = cv.take(max_g * L * sizeof(float));
@@ -737,10 +807,17 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
 
   if (cudaMemsetAsync(seg_flag, 0, n_ints * sizeof(int), stream) != cudaSuccess)
     return ADASUM_ERR_CUDA;
+#ifdef ADASUM_TEST_HOOKS
+  ws.guards = cv.guards;
+  for (size_t g : ws.guards)
+    if (cudaMemsetAsync(base + g, kGuardByte, kGuardBytes, stream) != cudaSuccess) return ADASUM_ERR_CUDA;
+#endif
 
   auto make_args = [&](size_t s) {
     StageArgs a;
     std::memset(&a, 0, sizeof a);
+    a.n_total = N;
+    a.error = ws.d_error;
     a.Kg = kg[s];
     a.G = groups[s];
     a.aligned = all_aligned ? 1 : 0;
@@ -752,8 +829,8 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
     a.chunks = plan->d_chunks;
     a.partials = reinterpret_cast<float*>(base + o_part);
     a.chunk_sums = reinterpret_cast<double*>(base + o_chunk);
-    a.tile_amax = reinterpret_cast<float*>(base + o_tamax);
-    a.chunk_amax = reinterpret_cast<float*>(base + o_camax);
+    a.tile_nz = reinterpret_cast<uint32_t*>(base + o_tnz);
+    a.chunk_nz = reinterpret_cast<uint32_t*>(base + o_cnz);
     a.coef = reinterpret_cast<float*>(base + o_coef);
     a.seg_flag = seg_flag;
     a.partials64 = reinterpret_cast<double*>(base + o_part64);
@@ -823,6 +900,7 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
     }
   } joins{stream};
 
+  phase.next("adasum:small segments");
   // Tiny segments: one warp each, on side stream 0.  The launch is a single wave of
   // latency-bound warps (a K = 64 segment takes ~100 us), so it runs concurrently with
   // the rest of the call instead of ahead of it.
@@ -836,6 +914,8 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
     ta.list = plan->d_tiny;
     ta.count = plan->tiny_count;
     ta.K = K;
+    ta.n_total = N;
+    ta.error = ws.d_error;
     cudaStream_t side = ws.side[0].stream;
     if (adasum_status_t st = launch_one(side, [&](const char** n) { return launch_tiny_df(ta, dtype, side, n); },
                                         static_cast<double>(plan->pos_tiny) * (Kreal + 1) * es))
@@ -851,6 +931,7 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
     oa.P = onchip_positions(K);
     oa.aligned = all_aligned ? 1 : 0;
     oa.error = ws.d_error;
+    oa.n_total = N;
     oa.recomputed = list_count + 3;
     oa.spin_budget = 2000000000LL;  // about one second of SM clock
     if (inject_timeout()) {
@@ -873,6 +954,7 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
   // only the flagged segments' elements (edges masked per element), so the two run
   // concurrently.
   auto enqueue_recompute = [&](cudaStream_t ts) -> adasum_status_t {
+    Range recompute_range("adasum:recompute");
     // (the lists' lengths are on the device: enough CTAs for many flagged tiles, the
     // surplus returns at once)
     const int grid64 = std::max(1, std::min(plan->ntiles, 16 * num_sms));
@@ -898,6 +980,7 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
       oa.P = onchip_positions(K);
       oa.aligned = all_aligned ? 1 : 0;
       oa.error = ws.d_error;
+    oa.n_total = N;
       oa.recomputed = list_count + 3;
       oa.spin_budget = 2000000000LL;
       oa.list = reinterpret_cast<int*>(base + o_oclist);
@@ -959,6 +1042,7 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
     if (adasum_status_t st = joins.fork(ws.side[1], 1)) return st;
     return enqueue_recompute(ws.side[1].stream);
   };
+  phase.next("adasum:stages");
   for (size_t s = 0; s < kg.size(); ++s) {
     const bool last = s + 1 == kg.size();
     StageArgs a = make_args(s);
@@ -1004,6 +1088,127 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
   return ADASUM_OK;
 }
 
+// Input bytes (all K workers) per segment group of adasum_reduce_host; a longer segment
+// is a group of its own.
+constexpr int64_t kHostGroupBytes = int64_t(1) << 30;
+
+adasum_status_t reduce_host_impl(const void* const* host_grads, int K, const int64_t* offs, int L,
+                                 int dtype, void* host_out, cudaStream_t stream) {
+  if (dtype != kF32 && dtype != kBF16) return ADASUM_ERR_INVALID_ARG;
+  if (L < 0 || (L > 0 && offs == nullptr) || K < 1 || host_grads == nullptr) return ADASUM_ERR_INVALID_ARG;
+  if (K > ADASUM_MAX_K) return ADASUM_ERR_UNSUPPORTED;
+  if (L == 0) return ADASUM_OK;
+  if (offs[0] != 0) return ADASUM_ERR_INVALID_ARG;
+  for (int s = 0; s < L; ++s)
+    if (offs[s + 1] < offs[s]) return ADASUM_ERR_INVALID_ARG;
+  const int64_t N = offs[L];
+  if (N == 0) return ADASUM_OK;
+  if (host_out == nullptr) return ADASUM_ERR_INVALID_ARG;
+  const size_t es = elem_size(dtype);
+  const size_t nbytes = static_cast<size_t>(N) * es;
+  for (int k = 0; k < K; ++k) {
+    if (host_grads[k] == nullptr) return ADASUM_ERR_INVALID_ARG;
+    if (host_out != host_grads[k] && overlaps(host_out, nbytes, host_grads[k], nbytes)) return ADASUM_ERR_ALIAS;
+  }
+  // every buffer must be host memory (pinned, pageable or managed); a device pointer is
+  // an argument error
+  for (int k = 0; k <= K; ++k) {
+    cudaPointerAttributes attr;
+    if (cudaPointerGetAttributes(&attr, k < K ? host_grads[k] : host_out) != cudaSuccess) {
+      cudaGetLastError();
+      return ADASUM_ERR_CUDA;
+    }
+    if (attr.type == cudaMemoryTypeDevice) return ADASUM_ERR_INVALID_ARG;
+  }
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess) {
+    cudaGetLastError();
+    return ADASUM_ERR_CUDA;
+  }
+  Workspace& ws = workspace_for(device);
+  HostPipe& hp = ws.host;
+  if (adasum_status_t st = hp.init()) return st;
+
+  // groups of whole segments, about kHostGroupBytes of input each
+  std::vector<std::pair<int, int>> groups;
+  const int64_t row = static_cast<int64_t>(K) * static_cast<int64_t>(es);
+  int64_t slot_pos = 0;
+  for (int a = 0; a < L;) {
+    int b = a + 1;
+    while (b < L && (offs[b + 1] - offs[a]) * row <= kHostGroupBytes) ++b;
+    groups.emplace_back(a, b);
+    slot_pos = std::max(slot_pos, offs[b] - offs[a]);
+    a = b;
+  }
+  const size_t row_bytes = align_up(static_cast<size_t>(slot_pos) * es, 256);
+  const size_t slot_bytes = row_bytes * static_cast<size_t>(K + 1);
+  if (2 * slot_bytes > hp.cap) {
+    if (hp.buf) {
+      cudaDeviceSynchronize();  // earlier calls may still use the old staging
+      cudaFree(hp.buf);
+      hp.buf = nullptr;
+      hp.cap = 0;
+    }
+    if (cudaMalloc(&hp.buf, 2 * slot_bytes) != cudaSuccess) {
+      cudaGetLastError();
+      hp.buf = nullptr;
+      return ADASUM_ERR_NO_MEMORY;
+    }
+    hp.cap = 2 * slot_bytes;
+  }
+
+  // Work starts after everything already on the caller's stream (which may still be
+  // writing the host inputs).  Whatever happens, every copy has finished when the call
+  // returns, so the caller may reuse or free its host buffers at once.
+  struct Drain {
+    HostPipe& hp;
+    ~Drain() {
+      cudaStreamSynchronize(hp.in);
+      cudaStreamSynchronize(hp.compute);
+      cudaStreamSynchronize(hp.out);
+    }
+  } drain{hp};
+  if (cudaEventRecord(hp.start, stream) != cudaSuccess || cudaStreamWaitEvent(hp.in, hp.start, 0) != cudaSuccess)
+    return ADASUM_ERR_CUDA;
+  std::vector<const void*> slot_in(K);
+  std::vector<int64_t> goffs;
+  for (size_t i = 0; i < groups.size(); ++i) {
+    const int a = groups[i].first, b = groups[i].second, slot = static_cast<int>(i & 1);
+    const int64_t p0 = offs[a], p1 = offs[b];
+    if (p1 == p0) continue;
+    const size_t gbytes = static_cast<size_t>(p1 - p0) * es;
+    char* base = static_cast<char*>(hp.buf) + slot * slot_bytes;
+    // host -> device, once the reduction of the group that last used the slot is done
+    if (i >= 2 && cudaStreamWaitEvent(hp.in, hp.reduced[slot], 0) != cudaSuccess) return ADASUM_ERR_CUDA;
+    for (int k = 0; k < K; ++k) {
+      slot_in[k] = base + k * row_bytes;
+      if (cudaMemcpyAsync(base + k * row_bytes, static_cast<const char*>(host_grads[k]) + p0 * es, gbytes,
+                          cudaMemcpyHostToDevice, hp.in) != cudaSuccess)
+        return ADASUM_ERR_CUDA;
+    }
+    if (cudaEventRecord(hp.h2d[slot], hp.in) != cudaSuccess) return ADASUM_ERR_CUDA;
+    // the reduction, once the inputs are in and the slot's last result has left
+    void* slot_out = base + K * row_bytes;
+    if (cudaStreamWaitEvent(hp.compute, hp.h2d[slot], 0) != cudaSuccess) return ADASUM_ERR_CUDA;
+    if (i >= 2 && cudaStreamWaitEvent(hp.compute, hp.d2h[slot], 0) != cudaSuccess) return ADASUM_ERR_CUDA;
+    Range group_range("adasum_reduce_host:group");
+    goffs.assign(offs + a, offs + b + 1);
+    for (int64_t& o : goffs) o -= p0;
+    if (adasum_status_t st = reduce_impl(slot_in.data(), K, goffs.data(), b - a, dtype, slot_out, nullptr,
+                                         nullptr, 0.f, 0.f, hp.compute))
+      return st;
+    if (cudaEventRecord(hp.reduced[slot], hp.compute) != cudaSuccess) return ADASUM_ERR_CUDA;
+    // device -> host
+    if (cudaStreamWaitEvent(hp.out, hp.reduced[slot], 0) != cudaSuccess ||
+        cudaMemcpyAsync(static_cast<char*>(host_out) + p0 * es, slot_out, gbytes, cudaMemcpyDeviceToHost,
+                        hp.out) != cudaSuccess ||
+        cudaEventRecord(hp.d2h[slot], hp.out) != cudaSuccess)
+      return ADASUM_ERR_CUDA;
+  }
+  if (cudaStreamSynchronize(hp.out) != cudaSuccess) return ADASUM_ERR_CUDA;
+  return ADASUM_OK;
+}
+
 }  // namespace
 }  // namespace adasum
 
@@ -1011,10 +1216,19 @@ using namespace adasum;
 
 extern "C" {
 
+adasum_status_t adasum_reduce_host(const void* const* host_grads, int K, const int64_t* seg_offsets,
+                                   int L, adasum_dtype_t dtype, void* host_out, adasum_stream_t stream) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  Range range("adasum_reduce_host");
+  return reduce_host_impl(host_grads, K, seg_offsets, L, static_cast<int>(dtype), host_out,
+                          reinterpret_cast<cudaStream_t>(stream));
+}
+
 adasum_status_t adasum_reduce(const void* const* grads, int K, const int64_t* seg_offsets,
                               int L, adasum_dtype_t dtype, void* out,
                               adasum_stream_t stream) {
   std::lock_guard<std::mutex> lock(g_mu);
+  Range range("adasum_reduce");
   return reduce_impl(grads, K, seg_offsets, L, static_cast<int>(dtype), out, nullptr,
                      nullptr, 0.f, 0.f, reinterpret_cast<cudaStream_t>(stream));
 }
@@ -1041,6 +1255,7 @@ adasum_status_t adasum_local_momentum_reduce(const void* const* grads, int K,
         return ADASUM_ERR_ALIAS;
   }
   std::lock_guard<std::mutex> lock(g_mu);
+  Range range("adasum_local_momentum_reduce");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   int device = 0, num_sms = 148;
   if (cudaGetDevice(&device) != cudaSuccess) return ADASUM_ERR_CUDA;
@@ -1065,6 +1280,7 @@ adasum_status_t adasum_reduce_orthogonality(const void* const* grads, int K,
                                             adasum_stream_t stream) {
   if (ortho == nullptr && L > 0) return ADASUM_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lock(g_mu);
+  Range range("adasum_reduce_orthogonality");
   return reduce_impl(grads, K, seg_offsets, L, static_cast<int>(dtype), out, nullptr, nullptr, 0.f,
                      0.f, reinterpret_cast<cudaStream_t>(stream), false, ortho);
 }
@@ -1072,6 +1288,7 @@ adasum_status_t adasum_reduce_orthogonality(const void* const* grads, int K,
 adasum_status_t adasum_reduce_chain(const void* const* grads, int K, const int64_t* seg_offsets,
                                     int L, adasum_dtype_t dtype, void* out, adasum_stream_t stream) {
   std::lock_guard<std::mutex> lock(g_mu);
+  Range range("adasum_reduce_chain");
   return reduce_impl(grads, K, seg_offsets, L, static_cast<int>(dtype), out, nullptr, nullptr, 0.f,
                      0.f, reinterpret_cast<cudaStream_t>(stream), true);
 }
@@ -1082,6 +1299,7 @@ adasum_status_t adasum_pair(const void* a, const void* b, int64_t n, adasum_dtyp
   const void* g[2] = {a, b};
   const int64_t offs[2] = {0, n};
   std::lock_guard<std::mutex> lock(g_mu);
+  Range range("adasum_pair");
   return reduce_impl(g, 2, offs, 1, static_cast<int>(dtype), out, nullptr, nullptr, 0.f,
                      0.f, reinterpret_cast<cudaStream_t>(stream));
 }
@@ -1096,6 +1314,7 @@ adasum_status_t adasum_reduce_momentum_sgd(const void* const* grads, int K,
     if (L > 0 && seg_offsets != nullptr && seg_offsets[L] > 0) return ADASUM_ERR_INVALID_ARG;
   }
   std::lock_guard<std::mutex> lock(g_mu);
+  Range range("adasum_reduce_momentum_sgd");
   if (master_w == nullptr) return ADASUM_OK;
   return reduce_impl(grads, K, seg_offsets, L, static_cast<int>(grad_dtype), out_or_null,
                      master_w, momentum, lr, mu, reinterpret_cast<cudaStream_t>(stream));
@@ -1112,6 +1331,7 @@ adasum_status_t adasum_get_last_error(void) {
   if (cudaMemcpy(&h, ws.d_error, sizeof h, cudaMemcpyDeviceToHost) != cudaSuccess ||
       cudaMemset(ws.d_error, 0, sizeof h) != cudaSuccess)
     return ADASUM_ERR_CUDA;
+  if (h & kErrBounds) return ADASUM_ERR_BOUNDS;
   return h ? ADASUM_ERR_TIMEOUT : ADASUM_OK;
 }
 
@@ -1124,6 +1344,7 @@ const char* adasum_status_string(adasum_status_t s) {
     case ADASUM_ERR_NO_MEMORY: return "ADASUM_ERR_NO_MEMORY";
     case ADASUM_ERR_CUDA: return "ADASUM_ERR_CUDA";
     case ADASUM_ERR_TIMEOUT: return "ADASUM_ERR_TIMEOUT";
+    case ADASUM_ERR_BOUNDS: return "ADASUM_ERR_BOUNDS";
   }
   return "ADASUM_ERR_UNKNOWN";
 }
@@ -1143,10 +1364,32 @@ adasum_status_t adasum_release_workspace(void) {
   for (auto& s : ws.side) s.destroy();
   if (ws.pair_buf) cudaFree(ws.pair_buf);
   ws.pair_buf = nullptr;
+  ws.host.destroy();
   return ADASUM_OK;
 }
 
 int adasum_version(void) { return kVersion; }
+
+int64_t adasum_debug_workspace_guards(void) {
+#ifdef ADASUM_TEST_HOOKS
+  std::lock_guard<std::mutex> lock(g_mu);
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess) return -1;
+  Workspace& ws = workspace_for(device);
+  if (cudaDeviceSynchronize() != cudaSuccess || ws.buf == nullptr) return -1;
+  int64_t bad = 0;
+  unsigned char h[kGuardBytes];
+  for (size_t g : ws.guards) {
+    if (g + kGuardBytes > ws.cap || cudaMemcpy(h, static_cast<char*>(ws.buf) + g, kGuardBytes,
+                                               cudaMemcpyDeviceToHost) != cudaSuccess)
+      return -1;
+    for (size_t i = 0; i < kGuardBytes; ++i) bad += h[i] != kGuardByte;
+  }
+  return bad;
+#else
+  return -1;
+#endif
+}
 
 int64_t adasum_recomputed_segments(void) {
   std::lock_guard<std::mutex> lock(g_mu);

@@ -19,6 +19,20 @@
 
 namespace adasum {
 
+// Bits of the device status word (adasum_get_last_error): a bounded wait gave up, or
+// (test build only) an index check failed.
+constexpr int kErrTimeoutMask = 0xF;
+constexpr int kErrBounds = 0x10;
+
+// Device-side index checks, compiled in with -DADASUM_BOUNDS_CHECK (the test build): a
+// failed check sets kErrBounds in the status word and the caller skips the access.  It
+// never traps.  Without the flag every check is `true` and costs nothing.
+#ifdef ADASUM_BOUNDS_CHECK
+#define ADASUM_CHECK(err, cond) ((cond) ? true : (atomicOr((err), kErrBounds), false))
+#else
+#define ADASUM_CHECK(err, cond) true
+#endif
+
 constexpr int kMaxK = 256;        // largest worker count accepted
 constexpr int kMaxGroup = 16;     // workers combined in one Gram stage
 constexpr int kThreads = 256;     // threads per CTA of the tile kernels
@@ -56,6 +70,8 @@ constexpr int kSmallTile = 1024;
 struct StageArgs {
   const void* in[kMaxK];
   void* out[kMaxK / kMaxGroup];
+  int64_t n_total;   // positions of every input and output (bounds checks)
+  int* error;        // device status word (bounds checks)
   int Kg;          // workers per group: 1, 2, 4, 8 or 16
   int G;           // groups
   int aligned;     // every in/out pointer is 16-byte aligned
@@ -67,10 +83,10 @@ struct StageArgs {
   const ChunkDesc* chunks;
   float* partials;   // [G][ntiles][E] Gram partials, E = Kg(Kg+1)/2 (upper triangle)
   double* chunk_sums; // [G][nchunks][E] compensated sums of the partials of each chunk
-  // Range check of the fp32 pass (kRangeLo, kRangeHi): every worker's largest |input|
-  // per tile and per chunk (a zero or padding worker gives 0).
-  float* tile_amax;   // [G][ntiles][Kg]
-  float* chunk_amax;  // [G][nchunks][Kg]
+  // Range check of the fp32 pass (kDiagLoPerPos, kDiagHi): bit k set when worker k has a
+  // nonzero value in the tile / chunk (-0 counts as zero).
+  uint32_t* tile_nz;   // [G][ntiles]
+  uint32_t* chunk_nz;  // [G][nchunks]
   float* coef;       // [G][nsegs][Kg] tree coefficients
   // Fused heavy-ball step (final stage of adasum_reduce_momentum_sgd only).
   float* master_w;
@@ -127,13 +143,16 @@ enum Mode : int { kModeTree = 0, kModeChain = 1 };
 // Gram-entry error model of the fp32 pass, relative to |g_i| |g_j|: products and
 // bounded-length fp32 sums, then compensated sums (a typical-case constant).
 constexpr double kGramRelErr = 4.0 * 5.9604644775390625e-08;   // 4 u, u = 2^-24
-// Range of the fp32 pass.  It is accurate while every nonzero worker's largest |value|
-// in a segment lies in [2^-40, 2^40]: the products of the elements that matter then stay
-// far inside fp32's normal range (no underflow to subnormals or zero, no overflow of a
-// tile's sums).  A segment with a worker outside it is flagged like an ill-conditioned
-// one and recomputed by a path that scales by a power of two first.
-constexpr float kRangeLo = 0x1p-40f;
-constexpr float kRangeHi = 0x1p40f;
+// Range of the fp32 pass.  Products are exact in the Gram kernels except below 2^-126,
+// where a product may be flushed to zero (the tensor cores) or rounded to a subnormal:
+// at most n 2^-126 over a segment of n positions.  For every nonzero worker k the fp32
+// pass therefore needs its squared norm G_kk >= n 2^-96, which keeps what may be lost
+// below 2^-30 G_kk (and a worker whose squares all vanish, G_kk = 0, is still seen, by
+// its nonzero bit); and G_kk <= 2^80, which keeps every product and partial sum far from
+// fp32's overflow.  A segment outside is flagged like an ill-conditioned one and
+// recomputed by a path that scales by a power of two first.
+constexpr double kDiagLoPerPos = 0x1p-96;
+constexpr double kDiagHi = 0x1p80;
 // Estimated relative output error above which a segment is recomputed in fp64.  The
 // estimate is a conservative first-order bound: over random, correlated and nearly
 // cancelling test sets the realised error of the fp32 pass stayed below 0.16 times it,
@@ -164,6 +183,7 @@ struct OnchipArgs {
   int P;                        // positions per CTA, onchip_positions(K)
   int aligned;                  // every in/out pointer is 16-byte aligned
   int* error;                   // device status word (bit 2: a bulk-copy wait gave up)
+  int64_t n_total;              // positions of every input and the output (bounds checks)
   int* recomputed;              // segments recomputed in double-float
   long long spin_budget;        // clock64 cycles of the bulk-copy wait
   int inject_extra_tx;          // test hook: expect 16 bytes that never arrive
@@ -200,6 +220,8 @@ struct TinyArgs {
   const int* list;        // the segments, one per warp
   int count;
   int K;
+  int64_t n_total;        // positions of every input and the output (bounds checks)
+  int* error;             // device status word (bounds checks)
 };
 
 // Launchers, one translation unit per input element type (compiled in parallel).

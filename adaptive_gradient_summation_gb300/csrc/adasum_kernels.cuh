@@ -134,50 +134,38 @@ __device__ __forceinline__ float vec_elem(const uint4& r, int e) {
   }
 }
 
-// Running largest |element| of one worker's 16-byte vectors, kept as the bits of
-// non-negative fp32 values (for those, unsigned order is value order; NaN sorts above
-// Inf).  bf16 vectors keep two 16-bit maxima packed in one word (per-halfword unsigned
-// max of the sign-cleared bf16 bits), merged by bits().
-template <typename Tag> struct AbsMax;
-template <> struct AbsMax<F32Tag> {
-  uint32_t m = 0u;
-  __device__ __forceinline__ void add(const uint4& r) {
-    m = max(m, max(max(r.x & 0x7FFFFFFFu, r.y & 0x7FFFFFFFu), max(r.z & 0x7FFFFFFFu, r.w & 0x7FFFFFFFu)));
-  }
-  __device__ __forceinline__ uint32_t bits() const { return m; }
-};
-template <> struct AbsMax<BF16Tag> {
-  uint32_t m = 0u;
-  __device__ __forceinline__ void add(const uint4& r) {
-    m = __vmaxu2(m, __vmaxu2(__vmaxu2(r.x & 0x7FFF7FFFu, r.y & 0x7FFF7FFFu),
-                             __vmaxu2(r.z & 0x7FFF7FFFu, r.w & 0x7FFF7FFFu)));
-  }
-  __device__ __forceinline__ uint32_t bits() const { return max(m << 16, m & 0xFFFF0000u); }
-};
+// Nonzero test of a worker's values (for the range check): the OR of their raw bits,
+// whose sign bits are cleared at the end (so -0 counts as zero).
+template <typename Tag> struct MagBits;
+template <> struct MagBits<F32Tag> { static constexpr uint32_t kMask = 0x7FFFFFFFu; };
+template <> struct MagBits<BF16Tag> { static constexpr uint32_t kMask = 0x7FFF7FFFu; };
+__device__ __forceinline__ uint32_t vec_or(const uint4& r) { return r.x | r.y | r.z | r.w; }
 
-__device__ __forceinline__ uint32_t warp_max_u32(uint32_t v) {
+// Appends worker k's nonzero bit to a running mask: m = (m << 1) | (bits != 0), for
+// sign-cleared bits (bits + 0x7FFFFFFF has its top bit set exactly when bits >= 1).
+__device__ __forceinline__ uint32_t nz_push(uint32_t m, uint32_t bits) {
+  return __funnelshift_l(bits + 0x7FFFFFFFu, m, 1);
+}
+
+__device__ __forceinline__ uint32_t warp_or_u32(uint32_t v) {
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) v = max(v, __shfl_xor_sync(0xFFFFFFFFu, v, off));
+  for (int off = 16; off > 0; off >>= 1) v |= __shfl_xor_sync(0xFFFFFFFFu, v, off);
   return v;
 }
 
-// Per-worker maxima of one tile (each thread's KG values, as AbsMax bits) over the CTA,
-// written to tile_amax[(q * ntiles + tile) * KG + k].  Called by the whole CTA.
-template <int KG>
-__device__ __forceinline__ void block_amax_store(const uint32_t (&m)[KG], float* __restrict__ dst) {
-  __shared__ uint32_t red[kThreads / 32][KG];
+// OR of every thread's mask over the CTA, written to *dst by thread 0.  Called by the
+// whole CTA.
+__device__ __forceinline__ void block_or_store(uint32_t m, uint32_t* __restrict__ dst) {
+  __shared__ uint32_t red[kThreads / 32];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int k = 0; k < KG; ++k) {
-    const uint32_t v = warp_max_u32(m[k]);
-    if (lane == 0) red[warp][k] = v;
-  }
+  m = warp_or_u32(m);
+  if (lane == 0) red[warp] = m;
   __syncthreads();
-  for (int k = threadIdx.x; k < KG; k += kThreads) {
+  if (threadIdx.x == 0) {
     uint32_t v = 0u;
 #pragma unroll
-    for (int w = 0; w < kThreads / 32; ++w) v = max(v, red[w][k]);
-    dst[k] = __uint_as_float(v);
+    for (int w = 0; w < kThreads / 32; ++w) v |= red[w];
+    *dst = v;
   }
 }
 
@@ -188,6 +176,14 @@ __device__ __forceinline__ void kahan_add(float& sum, float& comp, float x) {
   const float t = __fadd_rn(sum, y);
   comp = __fsub_rn(__fsub_rn(t, sum), y);
   sum = t;
+}
+
+// ------------------------------------------------------- descriptor checks (test build)
+
+// A tile inside the buffers and its segment inside the segment table.
+__device__ __forceinline__ bool tile_ok(const StageArgs& a, int tile_id, const TileDesc& t) {
+  return ADASUM_CHECK(a.error, tile_id >= 0 && tile_id < a.ntiles && t.start >= 0 && t.len > 0 &&
+                                   t.start + t.len <= a.n_total && t.seg >= 0 && t.seg < a.nsegs);
 }
 
 // ------------------------------------------------------------- pass 1: Gram (SIMT)
@@ -218,11 +214,11 @@ __device__ __forceinline__ void block_reduce_store(float (&acc)[E], float* __res
 // Gram partial of one tile with CUDA-core FMAs: every thread owns whole 16-byte
 // vectors (VW positions of all Kg workers) and accumulates the Kg(Kg+1)/2 products.
 // This thread's products over vectors first, first + step, ... of a tile (acc zeroed),
-// and every worker's largest |element| among them (AbsMax bits).
+// and in nz bit k whether worker k had a nonzero value among them.
 template <typename Tag, int KG>
 __device__ __forceinline__ void gram_accumulate(const StageArgs& a, const TileDesc& t, int q,
                                                 int first, int step, float (&acc)[tri_count(KG)],
-                                                uint32_t (&amax)[KG]) {
+                                                uint32_t& nz) {
   using S = typename ElemTraits<Tag>::Storage;
   constexpr int VW = ElemTraits<Tag>::kVW;
   constexpr int E = tri_count(KG);
@@ -234,13 +230,15 @@ __device__ __forceinline__ void gram_accumulate(const StageArgs& a, const TileDe
   const int64_t v0 = lo / VW, v1 = (hi + VW - 1) / VW;
 #pragma unroll
   for (int e = 0; e < E; ++e) acc[e] = 0.f;
-  AbsMax<Tag> am[KG];
+  nz = 0u;
   for (int64_t v = v0 + first; v < v1; v += step) {
     uint4 r[KG];
 #pragma unroll
     for (int k = 0; k < KG; ++k) r[k] = load_vec_raw<Tag, kLoadKeep>(x[k], v, lo, hi, aligned);
+    uint32_t m = 0u;
 #pragma unroll
-    for (int k = 0; k < KG; ++k) am[k].add(r[k]);
+    for (int k = KG - 1; k >= 0; --k) m = nz_push(m, vec_or(r[k]) & MagBits<Tag>::kMask);
+    nz |= m;
 #pragma unroll
     for (int e = 0; e < VW; ++e) {
       float xe[KG];
@@ -253,18 +251,17 @@ __device__ __forceinline__ void gram_accumulate(const StageArgs& a, const TileDe
           acc[tri_index(KG, i, j)] = __fmaf_rn(xe[i], xe[j], acc[tri_index(KG, i, j)]);
     }
   }
-#pragma unroll
-  for (int k = 0; k < KG; ++k) amax[k] = am[k].bits();
 }
 
 template <typename Tag, int KG>
 __device__ __forceinline__ void gram_tile_simt(const StageArgs& a, int tile_id, int q) {
   constexpr int E = tri_count(KG);
   float acc[E];
-  uint32_t amax[KG];
-  gram_accumulate<Tag, KG>(a, a.tiles[tile_id], q, threadIdx.x, kThreads, acc, amax);
+  uint32_t nz;
+  if (!tile_ok(a, tile_id, a.tiles[tile_id])) return;  // (uniform over the CTA)
+  gram_accumulate<Tag, KG>(a, a.tiles[tile_id], q, threadIdx.x, kThreads, acc, nz);
   block_reduce_store<E>(acc, a.partials + (static_cast<size_t>(q) * a.ntiles + tile_id) * E);
-  block_amax_store<KG>(amax, a.tile_amax + (static_cast<size_t>(q) * a.ntiles + tile_id) * KG);
+  block_or_store(nz, a.tile_nz + static_cast<size_t>(q) * a.ntiles + tile_id);
 }
 
 // Tile id of this CTA: the CTA kernels run over a.tile_list when the plan splits off
@@ -292,8 +289,9 @@ __global__ void __launch_bounds__(kThreads) gram_warp_kernel(const StageArgs a) 
   const int q = blockIdx.y;
   const int tile_id = a.small_list[w];
   float acc[E];
-  uint32_t amax[KG];
-  gram_accumulate<Tag, KG>(a, a.tiles[tile_id], q, lane, 32, acc, amax);
+  uint32_t nz;
+  if (!tile_ok(a, tile_id, a.tiles[tile_id])) return;  // (uniform over the warp)
+  gram_accumulate<Tag, KG>(a, a.tiles[tile_id], q, lane, 32, acc, nz);
 #pragma unroll
   for (int e = 0; e < E; ++e) {
 #pragma unroll
@@ -303,12 +301,8 @@ __global__ void __launch_bounds__(kThreads) gram_warp_kernel(const StageArgs a) 
 #pragma unroll
   for (int e = 0; e < E; ++e)
     if ((e & 31) == lane) dst[e] = acc[e];
-  float* mdst = a.tile_amax + (static_cast<size_t>(q) * a.ntiles + tile_id) * KG;
-#pragma unroll
-  for (int k = 0; k < KG; ++k) {
-    const uint32_t v = warp_max_u32(amax[k]);
-    if ((k & 31) == lane) mdst[k] = __uint_as_float(v);
-  }
+  nz = warp_or_u32(nz);
+  if (lane == 0) a.tile_nz[static_cast<size_t>(q) * a.ntiles + tile_id] = nz;
 }
 
 // --------------------------------------------------- pass 1: Gram (tensor cores, bf16)
@@ -324,32 +318,13 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Lane (g, t) of the MMA fragment layout holds positions of workers g and g + 8.  Their
-// maxima (AbsMax bits) over the four lanes of each g, over the warp.
-__device__ __forceinline__ void mma_lane_amax(uint32_t& mg, uint32_t& mh) {
-  mg = max(mg, __shfl_xor_sync(0xFFFFFFFFu, mg, 1));
-  mg = max(mg, __shfl_xor_sync(0xFFFFFFFFu, mg, 2));
-  mh = max(mh, __shfl_xor_sync(0xFFFFFFFFu, mh, 1));
-  mh = max(mh, __shfl_xor_sync(0xFFFFFFFFu, mh, 2));
-}
-
-// The same over the CTA's warps, written to dst[0..KG).  Called by the whole CTA.
-template <int KG>
-__device__ __forceinline__ void mma_amax_store(uint32_t mg, uint32_t mh, float* __restrict__ dst) {
-  __shared__ uint32_t red[kWarps][16];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, g = lane >> 2;
-  mma_lane_amax(mg, mh);
-  if ((lane & 3) == 0) {
-    red[warp][g] = mg;
-    if (KG == 16) red[warp][g + 8] = mh;
-  }
-  __syncthreads();
-  for (int k = threadIdx.x; k < KG; k += kThreads) {
-    uint32_t v = 0u;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) v = max(v, red[w][k]);
-    dst[k] = __uint_as_float(v);
-  }
+// Lane (g, t) of the MMA fragment layout holds positions of workers g and g + 8: its
+// nonzero bits from the ORs of those workers' raw values (sign bits cleared here).
+template <typename Tag>
+__device__ __forceinline__ uint32_t mma_lane_nz(uint32_t org, uint32_t orh) {
+  const int g = (threadIdx.x & 31) >> 2;
+  return (((org & MagBits<Tag>::kMask) != 0u) ? 1u << g : 0u) |
+         (((orh & MagBits<Tag>::kMask) != 0u) ? 1u << (g + 8) : 0u);
 }
 
 // Gram partial of one tile of bf16 gradients on the tensor cores (Kg = 8 or 16).
@@ -369,6 +344,7 @@ __device__ __forceinline__ void gram_tile_mma(const StageArgs& a, int tile_id, i
   constexpr int U = 4;        // chunks of 32 positions loaded per warp iteration
   constexpr int kFold = 4;    // iterations accumulated in the MMA before a Kahan fold
   const TileDesc t = a.tiles[tile_id];
+  if (!tile_ok(a, tile_id, t)) return;  // (uniform over the CTA)
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, tq = lane & 3;
   const uint16_t* xg = static_cast<const uint16_t*>(a.in[q * KG + g]);
@@ -380,7 +356,7 @@ __device__ __forceinline__ void gram_tile_mma(const StageArgs& a, int tile_id, i
   float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
   float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
   float e0[4] = {0.f, 0.f, 0.f, 0.f}, e1[4] = {0.f, 0.f, 0.f, 0.f};
-  AbsMax<BF16Tag> amg, amh;
+  uint32_t org = 0u, orh = 0u;  // raw-bit ORs of workers g and g + 8 (range check)
   int pending = 0;
   for (int64_t c = c0 + warp; c < c1; c += kWarps * U) {
     uint4 rg[U], rh[U];
@@ -399,8 +375,8 @@ __device__ __forceinline__ void gram_tile_mma(const StageArgs& a, int tile_id, i
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      amg.add(rg[u]);
-      amh.add(rh[u]);
+      org |= vec_or(rg[u]);
+      orh |= vec_or(rh[u]);
       mma_bf16_16816(d0, rg[u].x, rh[u].x, rg[u].y, rh[u].y, rg[u].x, rg[u].y);
       mma_bf16_16816(d0, rg[u].z, rh[u].z, rg[u].w, rh[u].w, rg[u].z, rg[u].w);
       if constexpr (KG == 16) {
@@ -452,7 +428,7 @@ __device__ __forceinline__ void gram_tile_mma(const StageArgs& a, int tile_id, i
     for (int w = 0; w < kWarps; ++w) s = __fadd_rn(s, red[w][idx]);
     dst[tri_index(KG, i, j)] = s;
   }
-  mma_amax_store<KG>(amg.bits(), amh.bits(), a.tile_amax + (static_cast<size_t>(q) * a.ntiles + tile_id) * KG);
+  block_or_store(mma_lane_nz<BF16Tag>(org, orh), a.tile_nz + static_cast<size_t>(q) * a.ntiles + tile_id);
 }
 
 // Three bf16 parts of two fp32 values, x = h + m + l exactly: h is x rounded to bf16,
@@ -478,7 +454,7 @@ template <int KG>
 __device__ __forceinline__ void gram_chunks_mma_f32(const float* xg, const float* xh, int64_t lo, int64_t hi,
                                                     bool aligned, int first, int nw, float (&s0)[4],
                                                     float (&e0)[4], float (&s1)[4], float (&e1)[4],
-                                                    uint32_t& mg, uint32_t& mh) {
+                                                    uint32_t& org, uint32_t& orh) {
   static_assert(KG == 16, "16 workers: two n-tiles of the m16n8k16 MMA");
   constexpr int U = 2;        // chunks of 32 positions loaded per warp iteration
   constexpr int kFold = 4;    // iterations accumulated in the MMA before a Kahan fold
@@ -488,7 +464,7 @@ __device__ __forceinline__ void gram_chunks_mma_f32(const float* xg, const float
   float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int i = 0; i < 4; ++i) s0[i] = e0[i] = s1[i] = e1[i] = 0.f;
-  AbsMax<F32Tag> amg, amh;
+  org = orh = 0u;  // raw-bit ORs of workers g and g + 8 (range check)
   int pending = 0;
   for (int64_t c = c0 + first; c < c1; c += static_cast<int64_t>(nw) * U) {
     uint4 rg[U][2], rh[U][2];
@@ -504,10 +480,8 @@ __device__ __forceinline__ void gram_chunks_mma_f32(const float* xg, const float
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      amg.add(rg[u][0]);
-      amg.add(rg[u][1]);
-      amh.add(rh[u][0]);
-      amh.add(rh[u][1]);
+      org |= vec_or(rg[u][0]) | vec_or(rg[u][1]);
+      orh |= vec_or(rh[u][0]) | vec_or(rh[u][1]);
       // parts of positions (0,1), (2,3), (4,5), (6,7): registers 0..3 as in gram_tile_mma
       uint32_t gh[4], gm[4], gl[4], hh[4], hm[4], hl[4];
 #pragma unroll
@@ -549,8 +523,6 @@ __device__ __forceinline__ void gram_chunks_mma_f32(const float* xg, const float
     kahan_add(s0[i], e0[i], d0[i]);
     kahan_add(s1[i], e1[i], d1[i]);
   }
-  mg = amg.bits();
-  mh = amh.bits();
 }
 
 // A lane's compensated sums into the KG x KG matrix m (row-major), as laid out by the MMA.
@@ -579,6 +551,7 @@ __device__ __forceinline__ void gram_tile_mma_f32(const StageArgs& a, int tile_i
   static_assert(KG == 16, "16 workers");
   constexpr int E = tri_count(KG);
   const TileDesc t = a.tiles[tile_id];
+  if (!tile_ok(a, tile_id, t)) return;  // (uniform over the CTA)
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2;
   float s0[4], e0[4], s1[4], e1[4];
@@ -598,7 +571,7 @@ __device__ __forceinline__ void gram_tile_mma_f32(const StageArgs& a, int tile_i
       s = __fadd_rn(s, i == j ? red[w][idx] : 0.5f * __fadd_rn(red[w][idx], red[w][j * KG + i]));
     dst[tri_index(KG, i, j)] = s;
   }
-  mma_amax_store<KG>(mg, mh, a.tile_amax + (static_cast<size_t>(q) * a.ntiles + tile_id) * KG);
+  block_or_store(mma_lane_nz<F32Tag>(mg, mh), a.tile_nz + static_cast<size_t>(q) * a.ntiles + tile_id);
 }
 
 // Gram partials of small tiles of fp32 gradients (16 workers), one warp per (tile,
@@ -616,6 +589,7 @@ __global__ void __launch_bounds__(kThreads, 3) gram_warp_mma_f32_kernel(const St
   const int q = blockIdx.y;
   const int tile_id = a.small_list[w];
   const TileDesc t = a.tiles[tile_id];
+  if (!tile_ok(a, tile_id, t)) return;  // (uniform over the warp)
   const int g = lane >> 2;
   float s0[4], e0[4], s1[4], e1[4];
   uint32_t mg, mh;
@@ -630,12 +604,8 @@ __global__ void __launch_bounds__(kThreads, 3) gram_warp_mma_f32_kernel(const St
     tri_unpack(KG, e, i, j);
     dst[e] = i == j ? m[i * KG + i] : 0.5f * __fadd_rn(m[i * KG + j], m[j * KG + i]);
   }
-  mma_lane_amax(mg, mh);
-  if ((lane & 3) == 0) {
-    float* mdst = a.tile_amax + (static_cast<size_t>(q) * a.ntiles + tile_id) * KG;
-    mdst[g] = __uint_as_float(mg);
-    mdst[g + 8] = __uint_as_float(mh);
-  }
+  const uint32_t nz = warp_or_u32(mma_lane_nz<F32Tag>(mg, mh));
+  if (lane == 0) a.tile_nz[static_cast<size_t>(q) * a.ntiles + tile_id] = nz;
 }
 
 // Three CTAs per SM (at most 85 registers, a few spilled): its loads' latency is what
@@ -672,6 +642,9 @@ template <int KG>
 __device__ __forceinline__ void reduce_chunk(const StageArgs& a, int c, int q) {
   constexpr int E = tri_count(KG);
   const ChunkDesc ch = a.chunks[c];
+  if (!ADASUM_CHECK(a.error, c < a.nchunks && ch.first_tile >= 0 && ch.ntiles >= 1 &&
+                                 ch.ntiles <= kChunkTiles && ch.first_tile + ch.ntiles <= a.ntiles))
+    return;
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     const float* p = a.partials + (static_cast<size_t>(q) * a.ntiles + ch.first_tile) * E + e;
     float v[kChunkTiles];
@@ -684,13 +657,12 @@ __device__ __forceinline__ void reduce_chunk(const StageArgs& a, int c, int q) {
     a.chunk_sums[(static_cast<size_t>(q) * a.nchunks + c) * E + e] =
         static_cast<double>(sum) - static_cast<double>(comp);
   }
-  // every worker's largest |input| over the chunk (NaN inputs do not count here: they
-  // reach the output through the sums)
-  for (int k = threadIdx.x; k < KG; k += blockDim.x) {
-    const float* p = a.tile_amax + (static_cast<size_t>(q) * a.ntiles + ch.first_tile) * KG + k;
-    float m = 0.f;
-    for (int t = 0; t < ch.ntiles; ++t) m = fmaxf(m, __ldcg(p + static_cast<size_t>(t) * KG));
-    a.chunk_amax[(static_cast<size_t>(q) * a.nchunks + c) * KG + k] = m;
+  // the workers with a nonzero value in the chunk
+  if (threadIdx.x == 0) {
+    const uint32_t* p = a.tile_nz + static_cast<size_t>(q) * a.ntiles + ch.first_tile;
+    uint32_t m = 0u;
+    for (int t = 0; t < ch.ntiles; ++t) m |= __ldcg(p + t);
+    a.chunk_nz[static_cast<size_t>(q) * a.nchunks + c] = m;
   }
 }
 
@@ -1264,22 +1236,15 @@ template <int KG>
 __device__ __forceinline__ void segment_coefficients(const StageArgs& a, int seg, int q) {
   constexpr int E = tri_count(KG);
   const SegDesc sd = a.segs[seg];
+  if (!ADASUM_CHECK(a.error, seg >= 0 && seg < a.nsegs && sd.start >= 0 && sd.start + sd.len <= a.n_total &&
+                                 sd.first_chunk >= 0 && sd.first_chunk + sd.nchunks <= a.nchunks))
+    return;  // (uniform over the CTA)
   __shared__ double G[KG][KG];
   __shared__ df32 Gd[KG][KG];
   __shared__ double eps[KG];
   __shared__ double snorm[KG];
   __shared__ float tree_sh[tree_scratch_floats(KG)];
-  __shared__ int out_of_range;
-  if (threadIdx.x == 0) out_of_range = 0;
-  __syncthreads();
-  // range check: a nonzero worker whose largest |input| lies outside [kRangeLo, kRangeHi]
-  // (an infinite one is left to propagate, like NaN)
-  for (int k = threadIdx.x; k < KG; k += blockDim.x) {
-    const float* p = a.chunk_amax + (static_cast<size_t>(q) * a.nchunks + sd.first_chunk) * KG + k;
-    float m = 0.f;
-    for (int t = 0; t < sd.nchunks; ++t) m = fmaxf(m, __ldcg(p + static_cast<size_t>(t) * KG));
-    if (m > 0.f && (m < kRangeLo || (m > kRangeHi && !isinf(m)))) out_of_range = 1;
-  }
+  __shared__ uint32_t seg_nz;
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     double sum = 0.0;
     const double* p = a.chunk_sums + (static_cast<size_t>(q) * a.nchunks + sd.first_chunk) * E + e;
@@ -1292,6 +1257,12 @@ __device__ __forceinline__ void segment_coefficients(const StageArgs& a, int seg
   }
   for (int k = threadIdx.x; k < KG; k += blockDim.x)
     eps[k] = a.in_relerr ? static_cast<double>(a.in_relerr[static_cast<size_t>(q * KG + k) * a.nsegs + seg]) : 0.0;
+  if (threadIdx.x == 0) {  // the workers with a nonzero value in the segment
+    uint32_t nz = 0u;
+    const uint32_t* p = a.chunk_nz + static_cast<size_t>(q) * a.nchunks + sd.first_chunk;
+    for (int t = 0; t < sd.nchunks; ++t) nz |= __ldcg(p + t);
+    seg_nz = nz;
+  }
   __syncthreads();
   if (threadIdx.x < 32) {
     double c = 0.0, P = 0.0;
@@ -1313,6 +1284,12 @@ __device__ __forceinline__ void segment_coefficients(const StageArgs& a, int seg
     if (threadIdx.x < KG)
       a.coef[(static_cast<size_t>(q) * a.nsegs + seg) * KG + threadIdx.x] = static_cast<float>(c);
     if (threadIdx.x == 0) {
+      // range check (kDiagLoPerPos, kDiagHi): a nonzero worker whose squared norm is too
+      // small for the segment's length, or too large (NaN compares false: it propagates)
+      bool out_of_range = false;
+      const double lo = static_cast<double>(sd.len) * kDiagLoPerPos;
+      for (int k = 0; k < KG; ++k)
+        if ((seg_nz >> k) & 1u) out_of_range |= G[k][k] < lo || G[k][k] > kDiagHi;
       if (a.relerr) a.relerr[static_cast<size_t>(q) * a.nsegs + seg] = static_cast<float>(fmin(rel, 1e30));
       if (a.seg_flag && sd.len > 0 && (ill || !(rel <= kRelErrBudget) || out_of_range)) a.seg_flag[seg] = 1;
     }
@@ -1411,6 +1388,7 @@ __device__ __forceinline__ void combine_range(const StageArgs& a, int seg, int64
   using SI = typename ElemTraits<InTag>::Storage;
   using SO = typename ElemTraits<OutTag>::Storage;
   constexpr int VW = ElemTraits<InTag>::kVW;
+  if (!ADASUM_CHECK(a.error, seg >= 0 && seg < a.nsegs && lo >= 0 && lo <= hi && hi <= a.n_total)) return;
   if (a.skip_flagged && __ldcg(a.seg_flag + seg)) return;  // left to the fp64 path
   const bool aligned = a.aligned != 0;
   float c[KG];
@@ -1598,6 +1576,7 @@ __global__ void __launch_bounds__(kThreads) tiny64_kernel(const StageArgs a) {
   const int count = a.list_count[2];
   for (int li = wid; li < count; li += nwarps) {
     const SegDesc sd = a.segs[a.list_tiny[li]];
+    if (!ADASUM_CHECK(a.error, sd.start >= 0 && sd.len <= 32 && sd.start + sd.len <= a.n_total)) continue;
     const int n = static_cast<int>(sd.len);
     const int64_t p = sd.start + lane;
     const bool on = lane < n;
@@ -1652,6 +1631,7 @@ __global__ void __launch_bounds__(kThreads) segmax_kernel(const StageArgs a) {
   const int K = a.G * a.Kg;
   for (int li = blockIdx.x; li < count; li += gridDim.x) {
     const TileDesc t = a.tiles[a.list_tiles[li]];
+    if (!tile_ok(a, a.list_tiles[li], t)) continue;  // (uniform over the CTA)
     float m = 0.f;
     for (int k = 0; k < K; ++k) {
       if (a.in[k] == nullptr) continue;
@@ -1692,6 +1672,7 @@ __global__ void __launch_bounds__(kThreads) gram64_kernel(const StageArgs a) {
   for (int li = blockIdx.x; li < count; li += gridDim.x) {
     const int tile_id = a.list_tiles[li];
     const TileDesc t = a.tiles[tile_id];
+    if (!tile_ok(a, tile_id, t)) continue;  // (uniform over the CTA)
     const int enc = a.seg_exp[t.seg];
     int ex = enc > 0 ? enc - 1024 : 0;
     ex = ex < -125 ? -125 : (ex > 125 ? 125 : ex);
@@ -1735,6 +1716,9 @@ __global__ void __launch_bounds__(128) coef64_kernel(const StageArgs a) {
   for (int li = blockIdx.x; li < count; li += gridDim.x) {
     const int seg = a.list_segs[li];
     const SegDesc sd = a.segs[seg];
+    if (!ADASUM_CHECK(a.error, seg >= 0 && seg < a.nsegs && sd.first_tile >= 0 &&
+                                   sd.first_tile + sd.ntiles <= a.ntiles))
+      continue;  // (uniform over the CTA)
     __syncthreads();
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
       double sum = 0.0;
@@ -1778,6 +1762,7 @@ __global__ void __launch_bounds__(kThreads) combine64_kernel(const StageArgs a) 
   const int count = a.list_count[0];
   for (int li = blockIdx.x; li < count; li += gridDim.x) {
     const TileDesc t = a.tiles[a.list_tiles[li]];
+    if (!tile_ok(a, a.list_tiles[li], t)) continue;  // (uniform over the CTA)
     double c[KG];
     if constexpr (KG == 1) {
       c[0] = 1.0;

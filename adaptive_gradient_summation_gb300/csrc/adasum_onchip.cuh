@@ -151,7 +151,7 @@ __global__ void __launch_bounds__(kOnchipThreads, 2) onchip_kernel(const OnchipA
   __shared__ int t2flag;
   __shared__ __align__(16) unsigned char xch[2][kXch];
   __shared__ int flag;
-  __shared__ uint32_t kmax[K];  // every worker's largest |input| in this CTA's share
+  __shared__ uint32_t knz[K];   // OR of every worker's raw bits in this CTA's share
   __shared__ __align__(8) uint64_t bar;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -181,6 +181,10 @@ __global__ void __launch_bounds__(kOnchipThreads, 2) onchip_kernel(const OnchipA
   const int64_t s0 = sd.start, s1 = sd.start + sd.len;
   const int64_t vs0 = s0 / VW, vs1 = (s1 + VW - 1) / VW;
   const int64_t chunk = (vs1 - vs0 + C - 1) / C;
+  if (!ADASUM_CHECK(a.error, sd.start >= 0 && sd.len >= 0 && s1 <= a.n_total && chunk * VW <= P)) {
+    phase ^= 1u;  // nothing was armed for this entry: keep the barrier phase
+    continue;     // (uniform over the cluster: every CTA reads the same descriptor)
+  }
   const int64_t cv0 = min(vs1, vs0 + static_cast<int64_t>(rank) * chunk);
   const int64_t cv1 = min(vs1, cv0 + chunk);
   const int nvec = static_cast<int>(cv1 - cv0);            // <= P / VW (host guarantees)
@@ -215,18 +219,17 @@ __global__ void __launch_bounds__(kOnchipThreads, 2) onchip_kernel(const OnchipA
   if (a.recompute_only && tid == 0) flag = 1;
   __syncthreads();
   if (!a.recompute_only) {
-    // range check of the fp32 pass (kRangeLo, kRangeHi), evaluated after the next
-    // cluster barrier: this CTA's share first, TPR consecutive threads per row
+    // range check of the fp32 pass (kDiagLoPerPos, kDiagHi), completed with the trees:
+    // which workers have a nonzero value in this CTA's share, TPR threads per row
     {
       constexpr int TPR = K >= 8 ? kOnchipThreads / K : 32;
       const int k = tid / TPR, j = tid % TPR;
-      AbsMax<InTag> m;
+      uint32_t b = 0u;
       if (k < K)
-        for (int v = j; v < nvec; v += TPR) m.add(*reinterpret_cast<const uint4*>(data + k * rs + v * 16));
-      uint32_t b = m.bits();
+        for (int v = j; v < nvec; v += TPR) b |= vec_or(*reinterpret_cast<const uint4*>(data + k * rs + v * 16));
 #pragma unroll
-      for (int off = TPR / 2; off > 0; off >>= 1) b = max(b, __shfl_xor_sync(0xFFFFFFFFu, b, off));
-      if (k < K && j == 0) kmax[k] = b;
+      for (int off = TPR / 2; off > 0; off >>= 1) b |= __shfl_xor_sync(0xFFFFFFFFu, b, off);
+      if (k < K && j == 0) knz[k] = b & MagBits<InTag>::kMask;
     }
 
     // ---------------------------------------------------------------- stage 1: Gram
@@ -282,16 +285,6 @@ __global__ void __launch_bounds__(kOnchipThreads, 2) onchip_kernel(const OnchipA
         if (i <= j) xg[q * E1 + tri_index(KG1, i, j)] = __fsub_rn(sum, comp);
       }
       cta_or_cluster_sync(C);
-      // a nonzero worker whose largest |input| over the cluster is outside the range
-      // sends the segment to the recompute (every CTA reads the same values, so all
-      // take the same decision; Inf and NaN are left to propagate)
-      for (int k = tid; k < K; k += kOnchipThreads) {
-        uint32_t m = kmax[k];
-        for (uint32_t r = 0; r < C; ++r)
-          if (r != rank) m = max(m, *map_rank(&kmax[k], r));
-        const float mf = __uint_as_float(m);
-        if (mf > 0.f && (mf < kRangeLo || (mf > kRangeHi && !isinf(mf)))) flag = 1;
-      }
       // the Gram matrices of this CTA's groups: compensated sums over the cluster, CTA order
       for (int e = tid; e < NG * E1; e += kOnchipThreads) {
         const int q = e / E1;
@@ -316,8 +309,20 @@ __global__ void __launch_bounds__(kOnchipThreads, 2) onchip_kernel(const OnchipA
         const double rel = coefficient_tree_df<KG1>(G1[q], zeros, kGramRelErr, red + q * tree_scratch_floats(KG1), c, ill);
         if (lane < KG1) tcoef[q][lane] = c;
         if (lane == 0) {
+          // range check: a worker of the group with a nonzero value anywhere in the
+          // cluster's share and a squared norm too small for the segment's length, or too
+          // large, sends the segment to the recompute (NaN compares false: it propagates)
+          bool out_of_range = false;
+          const double lo = static_cast<double>(sd.len) * kDiagLoPerPos;
+          for (int i = 0; i < KG1; ++i) {
+            uint32_t nz = knz[q * KG1 + i];
+            for (uint32_t r = 0; r < C; ++r)
+              if (r != rank) nz |= *map_rank(&knz[q * KG1 + i], r);
+            const double d = df_to_double(G1[q][i][i]);
+            if (nz != 0u && (d < lo || d > kDiagHi)) out_of_range = true;
+          }
           trel[q] = rel;
-          tflag[q] = (ill || !(rel <= kRelErrBudget)) ? 1 : 0;
+          tflag[q] = (ill || !(rel <= kRelErrBudget) || out_of_range) ? 1 : 0;
         }
       }
     }
@@ -546,6 +551,7 @@ __global__ void __launch_bounds__(kOnchipThreads) tiny_df_kernel(const TinyArgs 
   const int w = blockIdx.x * kOnchipWarps + (threadIdx.x >> 5);
   if (w >= a.count) return;  // whole warps only
   const SegDesc sd = a.segs[a.list[w]];
+  if (!ADASUM_CHECK(a.error, sd.start >= 0 && sd.len <= kTinyDirect && sd.start + sd.len <= a.n_total)) return;
   const int64_t p = sd.start + lane;
   const bool on = lane < sd.len;
   float amax = 0.f;

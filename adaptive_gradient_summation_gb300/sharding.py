@@ -71,14 +71,17 @@ def sharded_reduce(grads, seg_offsets, *, group=None, out: torch.Tensor | None =
         part = [g[lo:hi] for g in grads]
         sub = offs[lo_s:hi_s + 1] - lo
         reduce_fn(part, sub, out[lo:hi])
-    # all-gather the partitions: pad every rank's piece to the longest, gather, trim
+    # all-gather the partitions: pad every rank's piece to the longest, gather, trim.
+    # gloo gathers host tensors, so device results travel through host copies there.
     sizes = [int(offs[bounds[r + 1]] - offs[bounds[r]]) for r in range(world)]
     width = max(max(sizes), 1)
-    piece = torch.zeros(width, dtype=out.dtype, device=out.device)
-    piece[: hi - lo] = out[lo:hi]
+    via_host = out.device.type == "cuda" and dist.get_backend(group) == "gloo"
+    gdev = torch.device("cpu") if via_host else out.device
+    piece = torch.zeros(width, dtype=out.dtype, device=gdev)
+    piece[: hi - lo] = out[lo:hi].to(gdev)
     gathered = [torch.empty_like(piece) for _ in range(world)]
     dist.all_gather(gathered, piece, group=group)
     for r in range(world):
         a, b = int(offs[bounds[r]]), int(offs[bounds[r + 1]])
-        out[a:b] = gathered[r][: b - a]
+        out[a:b] = gathered[r][: b - a].to(out.device)
     return out

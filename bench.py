@@ -15,7 +15,8 @@ Prints one JSON line (rank 0):
   roofline   the dominant streaming kernel's algorithmic bytes per launch (counted by the
              library from its plan: the tiles, segments or pair the launch covers) / its
              mean CUDA-event time, vs the measured HBM copy bandwidth
-  e2e        the same metric through reduce_from_host: H2D of the inputs, the reduction,
+  e2e        the same metric through the C-ABI host-buffer call adasum_reduce_host: H2D of
+             the inputs, the reduction,
              D2H of the result, every step
   cpu_baseline  the fp64 CPU oracle on a bounded sample of the same workload
 
@@ -296,21 +297,20 @@ def run_ours(args):
     # end to end through host memory
     e2e = None
     if not args.no_e2e:
+        # one C-ABI call per step (adasum_reduce_host): pinned host inputs in, the
+        # combined result back in pinned host memory, the call returning when it is there
         host = [g.cpu().pin_memory() for g in wl.grads]
-        staging = [torch.empty_like(g) for g in wl.grads]
         out_host = torch.empty(wl.N, dtype=wl.dtype, pin_memory=True)
-        ags.reduce_from_host(host, wl.seg_offsets, device=dev, staging=staging,
-                             out_host=out_host)
+        ags.reduce_from_host(host, wl.seg_offsets, out_host=out_host)
         barrier(dist)
         t0 = time.perf_counter()
         for _ in range(args.e2e_steps):
-            ags.reduce_from_host(host, wl.seg_offsets, device=dev, staging=staging,
-                                 out_host=out_host)
+            ags.reduce_from_host(host, wl.seg_offsets, out_host=out_host)
         te = max_over_ranks(time.perf_counter() - t0, dist)
         e2e = {"value": round(sum_over_ranks(in_bytes * args.e2e_steps, dist) / te / 1e9, 3),
                "unit": UNIT, "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": wl.N * es,
-               "steps": args.e2e_steps}
-        del host, staging
+               "steps": args.e2e_steps, "entry_point": "adasum_reduce_host"}
+        del host
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:

@@ -43,11 +43,13 @@
  * at most 32 positions, and segments whose error estimate flags them, are evaluated in
  * vector space in double-float or fp64 (see adasum_recomputed_segments).
  *
- * Range: the fp32 pass is used for a segment while every nonzero worker's largest |value|
- * in it lies in [2^-40, 2^40] (squares and products then stay normal fp32 numbers).  A
- * segment with a worker outside that range is detected and recomputed by a path that
- * first scales the segment by a power of two, so any magnitude fp32 or bf16 can hold is
- * combined to the stated accuracy.  The remaining limit: inside one segment, workers whose
+ * Range: the fp32 pass is used for a segment while every worker with a nonzero value in
+ * it has a squared norm between n * 2^-96 and 2^80 (n: the segment's length): then what
+ * fp32 loses to underflow (products below 2^-126) stays below 2^-30 of that norm and
+ * nothing overflows.  A segment outside that range (a worker with tiny or huge values,
+ * including one whose squares all vanish in fp32) is detected and recomputed by a path
+ * that first scales the segment by a power of two, so any magnitude fp32 or bf16 can
+ * hold is combined to the stated accuracy.  The remaining limit: inside one segment, workers whose
  * largest magnitudes differ by more than a factor of about 2^60 lose the smaller
  * worker's precision (one power of two scales the whole segment).
  *
@@ -92,7 +94,10 @@ typedef enum {
   ADASUM_ERR_ALIAS = 3,        /* an output overlaps an input other than as allowed */
   ADASUM_ERR_NO_MEMORY = 4,    /* the workspace could not be grown */
   ADASUM_ERR_CUDA = 5,         /* a CUDA runtime call failed (launch, copy, ...) */
-  ADASUM_ERR_TIMEOUT = 6       /* a device-side bounded wait gave up */
+  ADASUM_ERR_TIMEOUT = 6,      /* a device-side bounded wait gave up */
+  ADASUM_ERR_BOUNDS = 7        /* test build only (-DADASUM_BOUNDS_CHECK): a device-side index
+                                  check found an access outside the call's buffers and
+                                  skipped it; the product library never reports it */
 } adasum_status_t;
 
 /* Largest worker count accepted. */
@@ -119,6 +124,37 @@ typedef enum {
 ADASUM_API adasum_status_t adasum_reduce(const void *const *grads, int K, const int64_t *seg_offsets,
                               int L, adasum_dtype_t dtype, void *out,
                               adasum_stream_t stream);
+
+/*
+ * adasum_reduce_host -- adasum_reduce end to end from HOST memory: the K gradients are
+ * copied to the device, combined, and the result copied back, in one call that returns
+ * once host_out holds the result.  The paper exposes Adasum as an option of the
+ * allreduce a training script already calls (Section 3, the Horovod allreduce and
+ * DistributedOptimizer option); this is that single call for gradients held in host
+ * memory, with the transfers inside it.
+ *
+ *   host_grads   host array of K HOST pointers, each to N = seg_offsets[L] elements of
+ *                `dtype`.  Page-locked memory (cudaHostAlloc, cudaHostRegister) is copied
+ *                asynchronously at full speed; pageable memory works, more slowly.
+ *   seg_offsets, L, dtype, K   as for adasum_reduce.
+ *   host_out     HOST pointer to N elements; it may be exactly one of host_grads[k]; any
+ *                other overlap is ADASUM_ERR_ALIAS.
+ *   stream       the copies start after the work already enqueued on it (which may still
+ *                be writing the inputs).
+ * Pipelining: whole segments are grouped into about 1 GiB of input (a longer segment is a
+ * group of its own) and groups go through two device staging slots of the library
+ * workspace (grown with cudaMalloc) on three library streams, so the copy of group i+1
+ * to the device, the combine of group i and the copy of group i-1 back overlap.  One
+ * cudaMemcpyAsync per worker row and group.
+ * Blocking: returns when the result is in host_out; on any error, only after every copy
+ * it started has finished, so the caller may free its buffers at once.
+ * Errors: as adasum_reduce; a device pointer given as a host buffer is
+ * ADASUM_ERR_INVALID_ARG.
+ */
+ADASUM_API adasum_status_t adasum_reduce_host(const void *const *host_grads, int K,
+                                              const int64_t *seg_offsets, int L,
+                                              adasum_dtype_t dtype, void *host_out,
+                                              adasum_stream_t stream);
 
 /*
  * adasum_reduce_orthogonality -- adasum_reduce, and per segment the orthogonality metric
@@ -206,7 +242,8 @@ ADASUM_API adasum_status_t adasum_local_momentum_reduce(const void *const *grads
 
 /*
  * adasum_get_last_error -- the sticky device-side status of the current device
- * (ADASUM_OK or ADASUM_ERR_TIMEOUT), read after the caller has synchronised the stream
+ * (ADASUM_OK, ADASUM_ERR_TIMEOUT, or in the test build ADASUM_ERR_BOUNDS), read after
+ * the caller has synchronised the stream
  * of the calls in question.  Reading clears it.  Host-side failures are returned by the
  * entry points themselves and are not repeated here.
  */
@@ -255,7 +292,8 @@ ADASUM_API int adasum_version(void);
  * left pending by other code on the thread is neither reported nor cleared here).
  * It runs the fp32 pass only: unlike adasum_pair it does not detect and recompute
  * ill-conditioned (strongly cancelling) inputs in fp64, and it needs the largest |a_i|
- * and |b_i| inside about [2^-40, 2^40], where their squares stay normal fp32 numbers.
+ * and |b_i| inside about [2^-40, 2^40], where their squares stay normal fp32 numbers
+ * (outside it the result is not checked).
  */
 #define ADASUM_NOALLOC_MAX_N 33554432
 ADASUM_API adasum_status_t adasum_pair_noalloc(const void *a, const void *b, int64_t n,
@@ -263,6 +301,16 @@ ADASUM_API adasum_status_t adasum_pair_noalloc(const void *a, const void *b, int
                                                adasum_stream_t stream);
 
 /* ---- Instrumentation (used by the benchmark; not needed for normal use) ---------- */
+
+/*
+ * adasum_debug_workspace_guards -- for the test build of the library only
+ * (libadasum_gb300_test.so, compiled with -DADASUM_TEST_HOOKS): every region of the
+ * workspace is followed by a 256-byte guard band, filled with a pattern by each call;
+ * this synchronises the current device and returns how many guard bytes of the last
+ * call's layout lost the pattern (0: every kernel wrote only inside its regions).  The
+ * product library has no guard bands and returns -1.
+ */
+ADASUM_API int64_t adasum_debug_workspace_guards(void);
 
 /*
  * adasum_recomputed_segments -- synchronises the current device and returns how many

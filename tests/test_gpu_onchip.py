@@ -223,7 +223,8 @@ def test_tiny_segments_extreme_magnitudes(native, scale):
 @pytest.mark.parametrize("K", [4, 16, 64])
 def test_onchip_fast_pass_extreme_magnitudes(native, K, scale):
     """Small segments held on chip whose squares leave fp32's range: the fast pass's
-    range check (every worker's largest |value| over the cluster) sends them to the
+    range check (a worker with a nonzero value and a squared norm below n 2^-96 or above
+    2^80, over the cluster) sends them to the
     recompute, which scales them by a power of two first."""
     lengths = [40, 300, 1000, 2 * positions_per_cta(K) + 7]
     offs = workloads.offsets_from_numels(lengths)
