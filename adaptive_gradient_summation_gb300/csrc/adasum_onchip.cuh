@@ -308,19 +308,19 @@ __global__ void __launch_bounds__(kOnchipThreads, 2) onchip_kernel(const OnchipA
         bool ill = false;
         const double rel = coefficient_tree_df<KG1>(G1[q], zeros, kGramRelErr, red + q * tree_scratch_floats(KG1), c, ill);
         if (lane < KG1) tcoef[q][lane] = c;
+        // range check, lane i for worker i of the group: a nonzero value anywhere in the
+        // cluster's share and a squared norm too small for the segment's length, or too
+        // large, sends the segment to the recompute (NaN compares false: it propagates)
+        bool out_of_range = false;
+        if (lane < KG1) {
+          uint32_t nz = knz[q * KG1 + lane];
+          for (uint32_t r = 0; r < C; ++r)
+            if (r != rank) nz |= *map_rank(&knz[q * KG1 + lane], r);
+          const double d = df_to_double(G1[q][lane][lane]);
+          out_of_range = nz != 0u && (d < static_cast<double>(sd.len) * kDiagLoPerPos || d > kDiagHi);
+        }
+        out_of_range = __any_sync(0xFFFFFFFFu, out_of_range);
         if (lane == 0) {
-          // range check: a worker of the group with a nonzero value anywhere in the
-          // cluster's share and a squared norm too small for the segment's length, or too
-          // large, sends the segment to the recompute (NaN compares false: it propagates)
-          bool out_of_range = false;
-          const double lo = static_cast<double>(sd.len) * kDiagLoPerPos;
-          for (int i = 0; i < KG1; ++i) {
-            uint32_t nz = knz[q * KG1 + i];
-            for (uint32_t r = 0; r < C; ++r)
-              if (r != rank) nz |= *map_rank(&knz[q * KG1 + i], r);
-            const double d = df_to_double(G1[q][i][i]);
-            if (nz != 0u && (d < lo || d > kDiagHi)) out_of_range = true;
-          }
           trel[q] = rel;
           tflag[q] = (ill || !(rel <= kRelErrBudget) || out_of_range) ? 1 : 0;
         }
