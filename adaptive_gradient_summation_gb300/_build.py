@@ -35,9 +35,9 @@ TEST_LIB_PATH = os.path.join(PKG, TEST_LIB_NAME)
 TEST_FLAGS = ["-DADASUM_TEST_HOOKS", "-DADASUM_BOUNDS_CHECK"]
 
 SOURCES = ["adasum_api.cu", "launch_f32.cu", "launch_bf16.cu", "launch_f64.cu",
-           "launch_onchip.cu", "launch_reuse.cu", "adasum_noalloc.cu"]
+           "launch_onchip.cu", "adasum_noalloc.cu"]
 HEADERS = ["adasum_internal.h", "adasum_kernels.cuh", "adasum_ptx.cuh",
-           "adasum_onchip.cuh", "adasum_launch.h", "adasum_pair.cuh", "adasum_reuse.cuh"]
+           "adasum_onchip.cuh", "adasum_launch.h", "adasum_pair.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",

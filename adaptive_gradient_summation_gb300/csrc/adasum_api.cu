@@ -30,7 +30,6 @@ namespace {
 constexpr int kVersion = 100;  // 0.1.0
 
 int elem_size(int dt) { return dt == kBF16 ? 2 : 4; }
-size_t tri_count_host(int K) { return static_cast<size_t>(K) * (K + 1) / 2; }
 
 // Switches for tests and comparisons.  Only a library built with -DADASUM_TEST_HOOKS
 // (the test build) reads them from the environment; the product library reads no
@@ -149,12 +148,6 @@ struct Plan {
   int rc_cmax = 0;
   int rc_count = 0;
   bool need64 = true;
-  // reuse route (a persistent kernel of reuse_grid CTAs; 0: not built)
-  int reuse_grid = 0;
-  int reuse_nsteps = 0;
-  ReuseStep* d_rsteps = nullptr;
-  int* d_rflush = nullptr;    // [nsegs][reuse_grid]
-  int* d_rcontrib = nullptr;  // [nsegs]
 };
 
 // A stream of the workspace with the two events that fork it from the caller's stream
@@ -264,12 +257,6 @@ void free_plan(Plan& p) {
   if (p.d_coef_list) cudaFree(p.d_coef_list);
   if (p.d_big) cudaFree(p.d_big);
   if (p.d_small) cudaFree(p.d_small);
-  if (p.d_rsteps) cudaFree(p.d_rsteps);
-  if (p.d_rflush) cudaFree(p.d_rflush);
-  if (p.d_rcontrib) cudaFree(p.d_rcontrib);
-  p.d_rsteps = nullptr;
-  p.d_rflush = nullptr;
-  p.d_rcontrib = nullptr;
   p.d_big = nullptr;
   p.d_small = nullptr;
   p.d_onchip = nullptr;
@@ -293,74 +280,6 @@ int64_t tile_positions(int Kg, int dtype, int64_t N, int num_sms) {
   return (T + 255) / 256 * 256;
 }
 
-// Step list of the reuse route.  Consecutive segments are grouped into units of at least
-// unit_bytes of input (so that a unit's Gram outlasts the coefficient step of the one
-// before); every unit's Gram goes in steps of about step_bytes; a unit's combine step is
-// placed once lag_bytes of later Gram steps have gone by (by then its coefficients are
-// published, and its last-read bytes are still in L2), the last units' at the end.  Each
-// Gram step loads its unit's last keep_bytes with the L2 evict_last policy.  flush[s][c]
-// is the last step in which CTA c sees segment s (-1: never), contrib[s] how many CTAs
-// see it.  Segments without tiles (empty, or taken by the small-segment kernels) are
-// left out.
-void build_reuse(const std::vector<SegDesc>& segs, int64_t bytes_per_pos, int grid, int64_t unit_bytes,
-                 int64_t step_bytes, int64_t lag_bytes, int64_t keep_bytes, std::vector<ReuseStep>& steps,
-                 std::vector<int>& flush, std::vector<int>& contrib) {
-  const int L = static_cast<int>(segs.size());
-  struct Pending {
-    int lo, hi;
-    int64_t p0, p1, done_at;
-  };
-  std::vector<Pending> pending;
-  size_t next_c = 0;
-  int64_t cum = 0;
-  auto emit_ready_combines = [&](bool all) {
-    while (next_c < pending.size() && (all || cum >= pending[next_c].done_at + lag_bytes)) {
-      const Pending& u = pending[next_c++];
-      steps.push_back(ReuseStep{u.p0, u.p1, 0, 1, u.lo, u.hi, 0});
-    }
-  };
-  for (int s = 0; s < L;) {
-    const int lo = s;
-    int64_t bytes = 0;
-    while (s < L && bytes < unit_bytes) bytes += segs[s++].len * bytes_per_pos;
-    bool tiled = false;
-    for (int t = lo; t < s; ++t) tiled |= segs[t].ntiles > 0;
-    const int64_t p0 = segs[lo].start, p1 = segs[s - 1].start + segs[s - 1].len;
-    if (!tiled || p1 <= p0) continue;
-    const int64_t nsub = std::max<int64_t>(1, (bytes + step_bytes - 1) / step_bytes);
-    const int64_t keep_from = std::max(p0, p1 - keep_bytes / bytes_per_pos);
-    for (int64_t j = 0; j < nsub; ++j) {
-      const int64_t q0 = j == 0 ? p0 : std::max(p0, (p0 + (p1 - p0) * j / nsub) / 32 * 32);
-      const int64_t q1 = j + 1 == nsub ? p1 : std::max(p0, (p0 + (p1 - p0) * (j + 1) / nsub) / 32 * 32);
-      if (q1 <= q0) continue;
-      steps.push_back(ReuseStep{q0, q1, keep_from, 0, lo, s, 0});
-      cum += (q1 - q0) * bytes_per_pos;
-      emit_ready_combines(false);
-    }
-    pending.push_back(Pending{lo, s, p0, p1, cum});
-  }
-  emit_ready_combines(true);
-  flush.assign(static_cast<size_t>(L) * grid, -1);
-  contrib.assign(L, 0);
-  for (int si = 0; si < static_cast<int>(steps.size()); ++si) {
-    const ReuseStep& st = steps[si];
-    if (st.kind != 0) continue;
-    for (int c = 0; c < grid; ++c) {
-      int64_t a, b;
-      reuse_share(st.p0, st.p1, c, grid, a, b);
-      if (b <= a) continue;
-      for (int t = st.seg_lo; t < st.seg_hi; ++t) {
-        const SegDesc& sd = segs[t];
-        if (sd.start >= b) break;
-        if (sd.ntiles == 0 || std::min(b, sd.start + sd.len) <= std::max(a, sd.start)) continue;
-        flush[static_cast<size_t>(t) * grid + c] = si;
-      }
-    }
-  }
-  for (int t = 0; t < L; ++t)
-    for (int c = 0; c < grid; ++c) contrib[t] += flush[static_cast<size_t>(t) * grid + c] >= 0;
-}
-
 template <typename T>
 adasum_status_t upload(T** dst, const std::vector<T>& v) {
   if (cudaMalloc(dst, std::max<size_t>(1, v.size()) * sizeof(T)) != cudaSuccess) {
@@ -378,11 +297,11 @@ adasum_status_t upload(T** dst, const std::vector<T>& v) {
 
 adasum_status_t get_plan(Workspace& ws, const int64_t* offs, int L, int Kg0, int dtype,
                          int onchip_K, int onchip_cmax, bool onchip_force, int rc_cmax, bool tiny_on,
-                         bool warp_tiles, int reuse_grid, Plan** out) {
+                         bool warp_tiles, Plan** out) {
   for (auto it = ws.plans.begin(); it != ws.plans.end(); ++it) {
     if (it->Kg0 == Kg0 && it->dtype == dtype && it->onchip_K == onchip_K &&
         it->onchip_cmax == onchip_cmax && it->onchip_force == onchip_force && it->rc_cmax == rc_cmax &&
-        it->tiny_on == tiny_on && it->warp_tiles == warp_tiles && it->reuse_grid == reuse_grid &&
+        it->tiny_on == tiny_on && it->warp_tiles == warp_tiles &&
         it->offsets.size() == static_cast<size_t>(L + 1) &&
         std::memcmp(it->offsets.data(), offs, sizeof(int64_t) * (L + 1)) == 0) {
       ws.plans.splice(ws.plans.begin(), ws.plans, it);
@@ -515,19 +434,6 @@ adasum_status_t get_plan(Workspace& ws, const int64_t* offs, int L, int Kg0, int
   if (!st && any_small) st = upload(&p.d_coef_list, coef_list);
   if (!st) st = upload(&p.d_segs, segs);
   if (!st) st = upload(&p.d_chunks, chunks);
-  if (!st && reuse_grid > 0) {
-    std::vector<ReuseStep> rsteps;
-    std::vector<int> rflush, rcontrib;
-    build_reuse(segs, static_cast<int64_t>(Kg0) * elem_size(dtype), reuse_grid,
-                env_int("ADASUM_REUSE_UNIT_MB", 24) << 20, env_int("ADASUM_REUSE_STEP_MB", 16) << 20,
-                env_int("ADASUM_REUSE_LAG_MB", 32) << 20, env_int("ADASUM_REUSE_KEEP_MB", 64) << 20, rsteps,
-                rflush, rcontrib);
-    p.reuse_grid = reuse_grid;
-    p.reuse_nsteps = static_cast<int>(rsteps.size());
-    st = upload(&p.d_rsteps, rsteps);
-    if (!st) st = upload(&p.d_rflush, rflush);
-    if (!st) st = upload(&p.d_rcontrib, rcontrib);
-  }
   if (st) {
     free_plan(p);
     return st;
@@ -838,17 +744,10 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
   }
   // flagged tiled segments that fit are recomputed by the on-chip kernel
   const int rc_cmax = (plain && K <= kOnchipMaxK && env_on("ADASUM_ONCHIP", true)) ? onchip_max_cluster(dtype, K) : 0;
-  // Single-stage bf16 reductions of 8 or 16 workers: the persistent reuse kernel, whose
-  // second read of each input comes from L2 (ADASUM_REUSE switches it in the test build).
-  int reuse_grid = 0;
-  if (plain && kg.size() == 1 && (kg[0] == 8 || kg[0] == 16) && dtype == kBF16 && Kreal == K &&
-      env_on("ADASUM_REUSE", false))
-    reuse_grid = static_cast<int>(std::min<int64_t>(reuse_max_grid(kg[0]), env_int("ADASUM_REUSE_GRID", 1 << 20)));
   Plan* plan = nullptr;
   Range phase("adasum:plan");
   if (adasum_status_t st = get_plan(ws, offs, L, kg[0], dtype, rc_cmax > 0 ? K : onchip_K, onchip_cmax,
-                                    onchip_force, rc_cmax, tiny_on, env_on("ADASUM_WARP_GRAM", true),
-                                    reuse_grid, &plan))
+                                    onchip_force, rc_cmax, tiny_on, env_on("ADASUM_WARP_GRAM", true), &plan))
     return st;
 
   phase.next("adasum:workspace");
@@ -869,8 +768,7 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
   // One zeroed int region per call: segment flags, the 3 fp64-list counters and the
   // small-segment kernel's recompute counter, the recompute's segment scales, and the
   // count of flagged segments listed for the on-chip recompute.
-  const bool reuse = plan->reuse_grid > 0;
-  const size_t n_ints = 2 * static_cast<size_t>(L) + 5 + (reuse ? 3 * static_cast<size_t>(L) : 0);
+  const size_t n_ints = 2 * static_cast<size_t>(L) + 5;
   const size_t o_flags = cv.take(n_ints * sizeof(int));
   const size_t o_part = cv.take(max_e_tiles * sizeof(float));
   const size_t o_chunk = cv.take(max_e_chunks * sizeof(double));
@@ -886,8 +784,6 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
   const size_t o_ltiny = cv.take(static_cast<size_t>(L) * sizeof(int));
   const size_t o_oclist = cv.take(plan->rc_cmax > 0 ? static_cast<size_t>(L) * sizeof(int) : 0);
   const size_t o_onorm = cv.take(ortho ? static_cast<size_t>(L) * sizeof(double) : 0);
-  const size_t acc_bytes = reuse ? static_cast<size_t>(L) * tri_count_host(kg[0]) * kAccDigits * sizeof(long long) : 0;
-  const size_t o_racc = cv.take(acc_bytes);
   const size_t o_diag = cv.take(ortho ? static_cast<size_t>(groups[0]) * L * sizeof(double) : 0);
   // Stage outputs of every non-final stage: fp32 (fast pass) and fp64 (recompute).
   std::vector<size_t> off32(kg.size(), 0), off64(kg.size(), 0);
@@ -903,9 +799,6 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
   int* list_count = seg_flag + L;
   int* seg_exp = list_count + 4;  // the fp64 recompute's per-segment scale
   int* oc_count = seg_exp + L;   // flagged segments listed for the on-chip recompute
-  int* r_count = oc_count + 1;   // reuse route: contributions, ready flags, nonzero bits
-  int* r_ready = r_count + L;
-  int* r_nz = r_ready + L;
   if (adasum_status_t st = ensure_error_word(ws)) return st;
 
   bool all_aligned = aligned16(out) && (!mom || (aligned16(master_w) && aligned16(momentum)));
@@ -914,7 +807,6 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
 
   if (cudaMemsetAsync(seg_flag, 0, n_ints * sizeof(int), stream) != cudaSuccess)
     return ADASUM_ERR_CUDA;
-  if (reuse && cudaMemsetAsync(base + o_racc, 0, acc_bytes, stream) != cudaSuccess) return ADASUM_ERR_CUDA;
 #ifdef ADASUM_TEST_HOOKS
   ws.guards = cv.guards;
   for (size_t g : ws.guards)
@@ -1150,38 +1042,8 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
     if (adasum_status_t st = joins.fork(ws.side[1], 1)) return st;
     return enqueue_recompute(ws.side[1].stream);
   };
-  if (reuse) {
-    phase.next("adasum:reuse");
-    ReuseArgs ra;
-    std::memset(&ra, 0, sizeof ra);
-    for (int k = 0; k < K; ++k) ra.in[k] = grads[k];
-    ra.out = out;
-    ra.n_total = N;
-    ra.segs = plan->d_segs;
-    ra.nsegs = L;
-    ra.steps = plan->d_rsteps;
-    ra.nsteps = plan->reuse_nsteps;
-    ra.flush_step = plan->d_rflush;
-    ra.contrib = plan->d_rcontrib;
-    ra.count = r_count;
-    ra.ready = r_ready;
-    ra.acc = reinterpret_cast<long long*>(base + o_racc);
-    ra.seg_nz = reinterpret_cast<uint32_t*>(r_nz);
-    ra.coef = reinterpret_cast<float*>(base + o_coef);
-    ra.seg_flag = seg_flag;
-    ra.aligned = all_aligned ? 1 : 0;
-    ra.error = ws.d_error;
-    ra.spin_budget = 2000000000LL;  // about one second of SM clock
-    ra.serial_flush = env_on("ADASUM_REUSE_SERIAL_FLUSH", false) ? 1 : 0;
-    // algorithmic bytes: every tiled position's inputs read once, its output written once
-    if (adasum_status_t st = launch_one(stream, [&](const char** n) {
-          return launch_reuse(ra, kg[0], plan->reuse_grid, stream, n);
-        }, static_cast<double>(plan->pos_tiles) * (K + 1) * es))
-      return st;
-    if (adasum_status_t st = fork_recompute()) return st;
-  }
   phase.next("adasum:stages");
-  for (size_t s = 0; s < kg.size() && !reuse; ++s) {
+  for (size_t s = 0; s < kg.size(); ++s) {
     const bool last = s + 1 == kg.size();
     StageArgs a = make_args(s);
     if (s == 0) {

@@ -191,55 +191,6 @@ struct OnchipArgs {
   int recompute_only;           // skip the fp32 pass (segments the fp32 pass flagged)
 };
 
-// The reuse route (adasum_reuse.cuh): one persistent kernel runs Gram steps and, a few
-// tens of MB later, reverse combine steps over the same segments, so the second read of
-// each input hits L2.  Every CTA follows the same step list over its own share of the
-// positions of each step.
-constexpr int kReuseThreads = 512;   // 15 streaming warps and a finisher warp
-constexpr int kAccDigits = 10;       // exact Gram accumulators: 10 signed 32-bit digits
-struct ReuseStep {
-  int64_t p0, p1;       // positions of the step (a contiguous run of the flat gradient)
-  int64_t keep_from;    // Gram step: positions >= keep_from are loaded L2 evict_last
-  int kind;             // 0: Gram (forward), 1: combine (reverse)
-  int seg_lo, seg_hi;   // segments of the step's unit
-  int pad;
-};
-struct ReuseArgs {
-  const void* in[kMaxGroup];
-  void* out;
-  int64_t n_total;
-  const SegDesc* segs;
-  int nsegs;
-  const ReuseStep* steps;
-  int nsteps;
-  const int* flush_step;   // [nsegs][grid]: the step after which a CTA adds its partial
-  const int* contrib;      // [nsegs] contributions each segment waits for (0: not on the route)
-  int* count;              // [nsegs] contributions arrived (zeroed per call)
-  int* ready;              // [nsegs] coefficients published (zeroed per call)
-  long long* acc;          // [nsegs][E][kAccDigits] exact Gram sums (zeroed per call)
-  uint32_t* seg_nz;        // [nsegs] workers with a nonzero value (zeroed per call)
-  float* coef;             // [nsegs][KG]
-  int* seg_flag;           // [nsegs] 1: left to the recompute path
-  int aligned;
-  int* error;              // device status word (bit 0: a bounded wait gave up)
-  long long spin_budget;
-  int serial_flush;        // test build: flush with a barrier of the streaming warps
-};
-// This CTA's positions [a, b) of a step: the step's 32-position chunks dealt in equal
-// contiguous runs (host and device compute the same split).
-__host__ __device__ inline void reuse_share(int64_t p0, int64_t p1, int cta, int ncta, int64_t& a, int64_t& b) {
-  const int64_t c0 = p0 >> 5, c1 = (p1 + 31) >> 5;
-  const int64_t w = (c1 - c0 + ncta - 1) / ncta;
-  const int64_t x0 = c0 + w * cta < c1 ? c0 + w * cta : c1;
-  const int64_t x1 = x0 + w < c1 ? x0 + w : c1;
-  a = p0 > (x0 << 5) ? p0 : (x0 << 5);
-  b = p1 < (x1 << 5) ? p1 : (x1 << 5);
-  if (b < a) b = a;
-}
-// Persistent reuse kernel for KG = 8 or 16 bf16 workers: `grid` CTAs, all co-resident.
-int reuse_max_grid(int KG);
-int launch_reuse(const ReuseArgs& a, int KG, int grid, void* stream, const char** name);
-
 // Two workers, one segment (adasum_pair.cuh): one cooperative kernel with one grid
 // barrier, double-float sums and combine, every thread holding up to kPairVecs 16-byte
 // vectors of each input in registers; segments of up to min(co-resident CTAs,
