@@ -844,6 +844,7 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
     // up to 4 tiles (1 MiB) per combine CTA while the grid keeps 16 CTAs per SM
     a.combine_tiles = static_cast<int>(std::max<int64_t>(
         1, std::min<int64_t>(4, plan->ntiles / (16 * static_cast<int64_t>(num_sms)))));
+    a.num_sms = num_sms;
     if (plan->rc_cmax > 0) {
       a.oc_vecs = onchip_positions(K) / (dtype == kF32 ? 4 : 8);
       a.oc_vw = dtype == kF32 ? 4 : 8;
@@ -901,26 +902,6 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
   } joins{stream};
 
   phase.next("adasum:small segments");
-  // Tiny segments: one warp each, on side stream 0.  The launch is a single wave of
-  // latency-bound warps (a K = 64 segment takes ~100 us), so it runs concurrently with
-  // the rest of the call instead of ahead of it.
-  if (plan->tiny_count > 0) {
-    if (adasum_status_t st = joins.fork(ws.side[0], 0)) return st;
-    TinyArgs ta;
-    std::memset(&ta, 0, sizeof ta);
-    for (int k = 0; k < K; ++k) ta.in[k] = grads[k];
-    ta.out = out;
-    ta.segs = plan->d_segs;
-    ta.list = plan->d_tiny;
-    ta.count = plan->tiny_count;
-    ta.K = K;
-    ta.n_total = N;
-    ta.error = ws.d_error;
-    cudaStream_t side = ws.side[0].stream;
-    if (adasum_status_t st = launch_one(side, [&](const char** n) { return launch_tiny_df(ta, dtype, side, n); },
-                                        static_cast<double>(plan->pos_tiny) * (Kreal + 1) * es))
-      return st;
-  }
   // Small segments: whole tree on chip, one launch per cluster size.
   if (plan->onchip_K > 0) {
     OnchipArgs oa;
@@ -946,6 +927,28 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
           }, static_cast<double>(plan->pos_onchip[c]) * (Kreal + 1) * es))
         return st;
     }
+  }
+
+  // Tiny segments: one warp each, on side stream 0, forked after the on-chip launches.
+  // The launch is a wave of latency-bound warps, so it runs concurrently with the tiled
+  // passes (bandwidth-bound) instead of ahead of them; forked earlier, its CTAs held the
+  // registers the on-chip CTAs need.
+  if (plan->tiny_count > 0) {
+    if (adasum_status_t st = joins.fork(ws.side[0], 0)) return st;
+    TinyArgs ta;
+    std::memset(&ta, 0, sizeof ta);
+    for (int k = 0; k < K; ++k) ta.in[k] = grads[k];
+    ta.out = out;
+    ta.segs = plan->d_segs;
+    ta.list = plan->d_tiny;
+    ta.count = plan->tiny_count;
+    ta.K = K;
+    ta.n_total = N;
+    ta.error = ws.d_error;
+    cudaStream_t side = ws.side[0].stream;
+    if (adasum_status_t st = launch_one(side, [&](const char** n) { return launch_tiny_df(ta, dtype, side, n); },
+                                        static_cast<double>(plan->pos_tiny) * (Kreal + 1) * es))
+      return st;
   }
 
   // Recompute of the flagged segments, enqueued on `ts` (usually nothing is flagged and

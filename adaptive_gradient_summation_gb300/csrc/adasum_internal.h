@@ -106,6 +106,8 @@ struct StageArgs {
   const int* small_list;      // small tiles, one warp each (gram_warp_kernel)
   int nsmall;
   int combine_tiles;          // consecutive tiles per combine CTA (>= 1)
+  int num_sms;                // SMs of the device (launch shapes)
+  int coef_per_warp;          // coefficient kernel: one item per warp (else per CTA)
 
   // fp64 path (only the segments listed by collect_kernel).
   double* partials64;         // [G][ntiles][E]

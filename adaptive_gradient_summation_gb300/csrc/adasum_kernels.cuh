@@ -873,10 +873,10 @@ __device__ __forceinline__ uint32_t probe_mix(uint32_t x) {
 }
 
 // Shared scratch of coefficient_tree_df<KG> (and of its probe), in floats: two node-Gram
-// buffers for each of three fp32 (or two double-float) matrices, and three per-node
-// arrays.
+// buffers for each of three fp32 (or two double-float) matrices, three per-node arrays,
+// and the leaves' input errors in fp32.
 __host__ __device__ constexpr int tree_scratch_floats(int KG) {
-  return 3 * ((KG / 2) * (KG / 2) + (KG / 4) * (KG / 4)) + 3 * KG;
+  return 3 * ((KG / 2) * (KG / 2) + (KG / 4) * (KG / 4)) + 4 * KG;
 }
 
 // Sum over the 32 lanes in the order of the tree itself: siblings (lanes 2i, 2i+1)
@@ -911,9 +911,10 @@ __device__ __forceinline__ T node_gram_entry(T al, T be, T al2, T be2, T haa, T 
 // the leaves permutes E with them), and the output's change |sum_k dc_k g_k| =
 // sqrt(dc^T G dc) is returned relative to |out| (the larger of the two).  The tree runs
 // on node Gram matrices as in coefficient_tree_df, with their derivatives alongside.
-// Called by all 32 lanes of one warp; `scratch` holds tree_scratch_floats(KG) floats.
+// Called by all 32 lanes of one warp; `scratch` holds the first tree_scratch_floats(KG) -
+// KG floats of the tree's scratch, eps the leaves' input errors (fp32, shared).
 template <int KG>
-__device__ float coefficient_probe(const df32 (&G)[KG][KG], float sc, const double* eps, float ge,
+__device__ float coefficient_probe(const df32 (&G)[KG][KG], float sc, const float* eps, float ge,
                                    float* scratch) {
   constexpr int M1 = KG / 2, M2 = KG / 4;
   const int lane = threadIdx.x & 31;
@@ -931,7 +932,7 @@ __device__ float coefficient_probe(const df32 (&G)[KG][KG], float sc, const doub
     const float gii = fmaxf(g(i, i), 0.f), gjj = fmaxf(g(j, j), 0.f);
     const uint32_t h = probe_mix(__float_as_uint(g(i, j)) ^ probe_mix(__float_as_uint(gii * gjj)));
     const float s = (h >> m) & 1u ? 1.f : -1.f;
-    const float ti = tsign(gii, m) * static_cast<float>(eps[i]), tj = tsign(gjj, m) * static_cast<float>(eps[j]);
+    const float ti = tsign(gii, m) * eps[i], tj = tsign(gjj, m) * eps[j];
     return (ge * s + (ti + tj)) * (sqrtf(gii) * sqrtf(gjj));
   };
   float c = on ? 1.f : 0.f, t0 = 0.f, t1 = 0.f;  // leaf coefficient and its derivatives
@@ -1064,6 +1065,8 @@ __device__ double coefficient_tree_df(const df32 (&G)[KG][KG], const double* eps
   // node state (lane n < m holds node n of the current level; the leaves first)
   const float s2 = on ? fmaxf(G[row][row].hi * sc, 0.f) : 0.f;  // |g_k|^2, scaled
   const float e = on ? static_cast<float>(eps[row]) : 0.f;
+  float* const epsf = scratch + 3 * (M1 * M1 + M2 * M2) + 3 * KG;  // for the probe
+  if (on) epsf[lane] = e;
   float S = s2, Q = 0.f, R = 0.f, E2 = e * e * s2;
   df32 c = {on ? 1.f : 0.f, 0.f};  // lane k < KG: leaf k's coefficient
   bool bad = false;
@@ -1145,7 +1148,7 @@ __device__ double coefficient_tree_df(const df32 (&G)[KG][KG], const double* eps
     // lane holds the same rel, so the whole warp takes this branch).  The inputs' own
     // errors still reach the output directly, through their coefficients.
     __syncwarp();
-    const float probe = coefficient_probe<KG>(G, sc, eps, ge, scratch);
+    const float probe = coefficient_probe<KG>(G, sc, epsf, ge, scratch);
     rel = fminf(rel, kProbeSafety * probe + (sqrtf(E2) + rnd) / sqrtf(Pf));
   }
   return static_cast<double>(rel);
@@ -1229,78 +1232,133 @@ __device__ double coefficient_chain(const double (&G)[KG][KG], const double* eps
   return ill ? 1e30 : rel;
 }
 
-// Per segment: the Gram matrix from the chunk sums (fp64, chunk order), the tree
-// coefficients, and the conditioning check (see coefficient_tree).
-// Called by a whole CTA.
+// Items (segment, worker group) per CTA of the coefficient kernel when items are many:
+// one per warp, since a tree is a long chain of dependent steps on one warp and an SM
+// keeps many of them in flight.  With few items (fewer than a few per SM) each CTA takes
+// one and all its threads gather the Gram matrix: a long segment has many chunk sums.
+constexpr int kCoefWarps = 4;
+
+// Shared scratch of one item of the coefficient kernel.
 template <int KG>
-__device__ __forceinline__ void segment_coefficients(const StageArgs& a, int seg, int q) {
+struct CoefScratch {
+  double G[KG][KG];
+  df32 Gd[KG][KG];
+  double eps[KG];
+  double snorm[KG];
+  float tree[tree_scratch_floats(KG)];
+};
+
+// The Gram matrix of (segment, group) from its chunk sums (fp64, in chunk order: the
+// loads are issued eight at a time and added in order) and the input errors, by threads
+// first, first + step, ...
+template <int KG>
+__device__ __forceinline__ void coef_gather(const StageArgs& a, const SegDesc& sd, int seg, int q,
+                                            CoefScratch<KG>& sh, int first, int step) {
   constexpr int E = tri_count(KG);
-  const SegDesc sd = a.segs[seg];
-  if (!ADASUM_CHECK(a.error, seg >= 0 && seg < a.nsegs && sd.start >= 0 && sd.start + sd.len <= a.n_total &&
-                                 sd.first_chunk >= 0 && sd.first_chunk + sd.nchunks <= a.nchunks))
-    return;  // (uniform over the CTA)
-  __shared__ double G[KG][KG];
-  __shared__ df32 Gd[KG][KG];
-  __shared__ double eps[KG];
-  __shared__ double snorm[KG];
-  __shared__ float tree_sh[tree_scratch_floats(KG)];
-  __shared__ uint32_t seg_nz;
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    double sum = 0.0;
+  constexpr int U = 8;
+  for (int e = first; e < E; e += step) {
     const double* p = a.chunk_sums + (static_cast<size_t>(q) * a.nchunks + sd.first_chunk) * E + e;
-    for (int t = 0; t < sd.nchunks; ++t) sum += __ldcg(p + static_cast<size_t>(t) * E);
+    double sum = 0.0;
+    int t = 0;
+    for (; t + U <= sd.nchunks; t += U) {
+      double v[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) v[u] = __ldcg(p + static_cast<size_t>(t + u) * E);
+#pragma unroll
+      for (int u = 0; u < U; ++u) sum += v[u];
+    }
+    for (; t < sd.nchunks; ++t) sum += __ldcg(p + static_cast<size_t>(t) * E);
     int i, j;
     tri_unpack(KG, e, i, j);
-    G[i][j] = sum;
-    G[j][i] = sum;
-    Gd[i][j] = Gd[j][i] = df_from_double(sum);
+    sh.G[i][j] = sum;
+    sh.G[j][i] = sum;
+    sh.Gd[i][j] = sh.Gd[j][i] = df_from_double(sum);
   }
-  for (int k = threadIdx.x; k < KG; k += blockDim.x)
-    eps[k] = a.in_relerr ? static_cast<double>(a.in_relerr[static_cast<size_t>(q * KG + k) * a.nsegs + seg]) : 0.0;
-  if (threadIdx.x == 0) {  // the workers with a nonzero value in the segment
-    uint32_t nz = 0u;
-    const uint32_t* p = a.chunk_nz + static_cast<size_t>(q) * a.nchunks + sd.first_chunk;
-    for (int t = 0; t < sd.nchunks; ++t) nz |= __ldcg(p + t);
-    seg_nz = nz;
-  }
-  __syncthreads();
-  if (threadIdx.x < 32) {
-    double c = 0.0, P = 0.0;
-    bool ill = false;
-    double rel;
-    if (a.mode == kModeChain) {
-      rel = coefficient_chain<KG>(G, eps, kGramRelErr, snorm, c, ill, a.Kreal, &P);
-    } else {
-      float cf = 0.f;
-      rel = coefficient_tree_df<KG>(Gd, eps, kGramRelErr, tree_sh, cf, ill, &P);
-      c = cf;
-    }
-    if (threadIdx.x == 0 && a.outnorm2) a.outnorm2[seg] = P;
-    if (threadIdx.x == 0 && a.diag_sum) {
-      double tr = 0.0;
-      for (int k = 0; k < KG; ++k) tr += G[k][k];
-      a.diag_sum[static_cast<size_t>(q) * a.nsegs + seg] = tr;
-    }
-    if (threadIdx.x < KG)
-      a.coef[(static_cast<size_t>(q) * a.nsegs + seg) * KG + threadIdx.x] = static_cast<float>(c);
-    if (threadIdx.x == 0) {
-      // range check (kDiagLoPerPos, kDiagHi): a nonzero worker whose squared norm is too
-      // small for the segment's length, or too large (NaN compares false: it propagates)
-      bool out_of_range = false;
-      const double lo = static_cast<double>(sd.len) * kDiagLoPerPos;
-      for (int k = 0; k < KG; ++k)
-        if ((seg_nz >> k) & 1u) out_of_range |= G[k][k] < lo || G[k][k] > kDiagHi;
-      if (a.relerr) a.relerr[static_cast<size_t>(q) * a.nsegs + seg] = static_cast<float>(fmin(rel, 1e30));
-      if (a.seg_flag && sd.len > 0 && (ill || !(rel <= kRelErrBudget) || out_of_range)) a.seg_flag[seg] = 1;
-    }
-  }
-  __syncthreads();
+  for (int k = first; k < KG; k += step)
+    sh.eps[k] = a.in_relerr ? static_cast<double>(a.in_relerr[static_cast<size_t>(q * KG + k) * a.nsegs + seg]) : 0.0;
 }
 
+// The tree coefficients of (segment, group) and the conditioning and range checks (see
+// coefficient_tree_df), once coef_gather has filled sh.  Called by the 32 lanes of one
+// warp.
 template <int KG>
-__global__ void __launch_bounds__(128) coef_kernel(const StageArgs a) {
+__device__ __forceinline__ void coef_tree(const StageArgs& a, const SegDesc& sd, int seg, int q,
+                                          CoefScratch<KG>& sh) {
+  const int lane = threadIdx.x & 31;
+  // the workers with a nonzero value in the segment
+  uint32_t seg_nz = 0u;
+  {
+    const uint32_t* p = a.chunk_nz + static_cast<size_t>(q) * a.nchunks + sd.first_chunk;
+    for (int t = lane; t < sd.nchunks; t += 32) seg_nz |= __ldcg(p + t);
+    seg_nz = warp_or_u32(seg_nz);
+  }
+  double c = 0.0, P = 0.0;
+  bool ill = false;
+  double rel;
+  // (|out|^2 is read back only for the orthogonality metric: fp64 work otherwise saved)
+  double* const want_P = a.outnorm2 ? &P : nullptr;
+  if (a.mode == kModeChain) {
+    rel = coefficient_chain<KG>(sh.G, sh.eps, kGramRelErr, sh.snorm, c, ill, a.Kreal, want_P);
+  } else {
+    float cf = 0.f;
+    rel = coefficient_tree_df<KG>(sh.Gd, sh.eps, kGramRelErr, sh.tree, cf, ill, want_P);
+    c = cf;
+  }
+  if (lane == 0 && a.outnorm2) a.outnorm2[seg] = P;
+  if (lane == 0 && a.diag_sum) {
+    double tr = 0.0;
+    for (int k = 0; k < KG; ++k) tr += sh.G[k][k];
+    a.diag_sum[static_cast<size_t>(q) * a.nsegs + seg] = tr;
+  }
+  if (lane < KG) a.coef[(static_cast<size_t>(q) * a.nsegs + seg) * KG + lane] = static_cast<float>(c);
+  // range check (kDiagLoPerPos, kDiagHi), lane k for worker k: a nonzero worker whose
+  // squared norm is too small for the segment's length, or too large (NaN compares
+  // false: it propagates)
+  bool out_of_range = false;
+  if (lane < KG && ((seg_nz >> lane) & 1u)) {
+    const double d = sh.G[lane][lane];
+    out_of_range = d < static_cast<double>(sd.len) * kDiagLoPerPos || d > kDiagHi;
+  }
+  out_of_range = __any_sync(0xFFFFFFFFu, out_of_range);
+  if (lane == 0) {
+    if (a.relerr) a.relerr[static_cast<size_t>(q) * a.nsegs + seg] = static_cast<float>(fmin(rel, 1e30));
+    if (a.seg_flag && sd.len > 0 && (ill || !(rel <= kRelErrBudget) || out_of_range)) a.seg_flag[seg] = 1;
+  }
+}
+
+// The descriptor of item `item` of the (group, listed segment) pairs, checked.
+__device__ __forceinline__ bool coef_item(const StageArgs& a, int item, int& seg, int& q, SegDesc& sd) {
+  const int nlist = a.seg_list ? a.nseg_list : a.nsegs;
+  q = item / nlist;
+  const int i = item - q * nlist;
+  seg = a.seg_list ? a.seg_list[i] : i;
+  sd = a.segs[seg];
+  return ADASUM_CHECK(a.error, seg >= 0 && seg < a.nsegs && sd.start >= 0 && sd.start + sd.len <= a.n_total &&
+                                   sd.first_chunk >= 0 && sd.first_chunk + sd.nchunks <= a.nchunks);
+}
+
+// a.coef_per_warp: warp w of CTA b takes item b * kCoefWarps + w; else CTA b takes item
+// b, all its threads gather, warp 0 runs the tree.
+template <int KG>
+__global__ void __launch_bounds__(32 * kCoefWarps) coef_kernel(const StageArgs a) {
   pdl_enter();
-  segment_coefficients<KG>(a, a.seg_list ? a.seg_list[blockIdx.x] : static_cast<int>(blockIdx.x), blockIdx.y);
+  __shared__ CoefScratch<KG> sh[kCoefWarps];
+  const int warp = threadIdx.x >> 5;
+  const int items = (a.seg_list ? a.nseg_list : a.nsegs) * a.G;
+  int seg, q;
+  SegDesc sd;
+  if (a.coef_per_warp) {
+    const int item = blockIdx.x * kCoefWarps + warp;
+    if (item >= items || !coef_item(a, item, seg, q, sd)) return;  // whole warps
+    coef_gather<KG>(a, sd, seg, q, sh[warp], threadIdx.x & 31, 32);
+    __syncwarp();
+    coef_tree<KG>(a, sd, seg, q, sh[warp]);
+  } else {
+    if (static_cast<int>(blockIdx.x) >= items || !coef_item(a, blockIdx.x, seg, q, sd)) return;  // (uniform)
+    coef_gather<KG>(a, sd, seg, q, sh[0], threadIdx.x, blockDim.x);
+    __syncthreads();
+    if (warp == 0) coef_tree<KG>(a, sd, seg, q, sh[0]);
+  }
 }
 
 // ----------------------------------------------------------- pass 2: combine (+ step)

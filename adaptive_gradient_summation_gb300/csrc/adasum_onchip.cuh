@@ -538,10 +538,77 @@ __global__ void __launch_bounds__(kOnchipThreads, 2) onchip_kernel(const OnchipA
 //
 // Segments of at most kTinyDirect positions: one warp each, lane j holding position j
 // of every node, the tree evaluated on the values themselves in double-float arithmetic
-// -- no Gram matrix, no error estimate, no second pass.  Leaves are read left to right
-// and a node is formed as soon as both of its children exist (depth first), which
-// visits the same pairs (2i, 2i+1) at every level as the level-by-level definition.
-// Eight segments per CTA, no block barriers: the warps' latencies overlap.
+// -- no Gram matrix, no error estimate, no second pass.  Eight segments per CTA, no
+// block barriers: the warps' latencies overlap.
+
+// One node: Adasum of two nodes held one position per lane (every lane calls it).
+// Out of line: a 64-leaf tree makes 63 calls, and one copy of the code keeps the
+// instruction cache warm for all the warps of an SM.
+__device__ __noinline__ df32 tiny_node(df32 xa, df32 xb) {
+  const df32 d = df_warp_sum(df_mul(xa, xb));
+  const df32 pa = df_warp_sum(df_mul(xa, xa));
+  const df32 pb = df_warp_sum(df_mul(xb, xb));
+  const df32 one = {1.f, 0.f};
+  const df32 al = pa.hi == 0.f ? one : df_add(one, df_neg(df_div(d, df32{2.f * pa.hi, 2.f * pa.lo})));
+  const df32 be = pb.hi == 0.f ? one : df_add(one, df_neg(df_div(d, df32{2.f * pb.hi, 2.f * pb.lo})));
+  return df_add(df_mul(al, xa), df_mul(be, xb));
+}
+
+// The subtree over leaves [LO, LO + CNT) of values already in registers.
+template <int LO, int CNT, int KP>
+__device__ __forceinline__ df32 tiny_subtree(const float (&v)[KP]) {
+  if constexpr (CNT == 1) {
+    return df32{v[LO], 0.f};
+  } else {
+    const df32 left = tiny_subtree<LO, CNT / 2, KP>(v);
+    const df32 right = tiny_subtree<LO + CNT / 2, CNT / 2, KP>(v);
+    return tiny_node(left, right);
+  }
+}
+
+// Warp w of the launch takes list entry w.  Returns false (after recording a failed
+// descriptor check) when the entry is not one this kernel may touch.
+__device__ __forceinline__ bool tiny_entry(const TinyArgs& a, int w, SegDesc& sd) {
+  sd = a.segs[a.list[w]];
+  return ADASUM_CHECK(a.error, sd.start >= 0 && sd.len <= kTinyDirect && sd.start + sd.len <= a.n_total);
+}
+
+// K = KP leaves (a power of two up to 64): every value is loaded at once into
+// registers, read once, prescaled by the power of two of the segment's largest |value|,
+// and the tree runs from registers (its pairs (2i, 2i+1) at every level).
+template <typename InTag, int KP>
+__global__ void __launch_bounds__(kOnchipThreads) tiny_reg_kernel(const TinyArgs a) {
+  pdl_enter();
+  using S = typename ElemTraits<InTag>::Storage;
+  const int lane = threadIdx.x & 31;
+  const int w = blockIdx.x * kOnchipWarps + (threadIdx.x >> 5);
+  if (w >= a.count) return;  // whole warps only
+  SegDesc sd;
+  if (!tiny_entry(a, w, sd)) return;
+  const int64_t p = sd.start + lane;
+  const bool on = lane < sd.len;
+  float v[KP];
+#pragma unroll
+  for (int k = 0; k < KP; ++k) {
+    const S* x = static_cast<const S*>(a.in[k]);
+    v[k] = (on && x != nullptr) ? elem_f32(x, p) : 0.f;
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int k = 0; k < KP; ++k) amax = fmaxf(amax, fabsf(v[k]));
+  for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
+  const int ex = scale_exponent(amax);
+  const float sc = ldexpf(1.f, -ex);
+#pragma unroll
+  for (int k = 0; k < KP; ++k) v[k] *= sc;
+  const df32 r = tiny_subtree<0, KP, KP>(v);
+  if (on) store_df(static_cast<S*>(a.out), p, r, ex);
+}
+
+// Any K (a power of two up to kMaxK): a max pass over the inputs, then the leaves read
+// again left to right and a node formed as soon as both of its children exist (depth
+// first), which visits the same pairs (2i, 2i+1) at every level as the level-by-level
+// definition.
 template <typename InTag>
 __global__ void __launch_bounds__(kOnchipThreads) tiny_df_kernel(const TinyArgs a) {
   pdl_enter();
@@ -550,8 +617,8 @@ __global__ void __launch_bounds__(kOnchipThreads) tiny_df_kernel(const TinyArgs 
   const int lane = threadIdx.x & 31;
   const int w = blockIdx.x * kOnchipWarps + (threadIdx.x >> 5);
   if (w >= a.count) return;  // whole warps only
-  const SegDesc sd = a.segs[a.list[w]];
-  if (!ADASUM_CHECK(a.error, sd.start >= 0 && sd.len <= kTinyDirect && sd.start + sd.len <= a.n_total)) return;
+  SegDesc sd;
+  if (!tiny_entry(a, w, sd)) return;
   const int64_t p = sd.start + lane;
   const bool on = lane < sd.len;
   float amax = 0.f;
@@ -571,14 +638,7 @@ __global__ void __launch_bounds__(kOnchipThreads) tiny_df_kernel(const TinyArgs 
     lvl[top] = 0;
     ++top;
     while (top >= 2 && lvl[top - 1] == lvl[top - 2]) {
-      const df32 xa = val[top - 2], xb = val[top - 1];
-      const df32 d = df_warp_sum(df_mul(xa, xb));
-      const df32 pa = df_warp_sum(df_mul(xa, xa));
-      const df32 pb = df_warp_sum(df_mul(xb, xb));
-      const df32 one = {1.f, 0.f};
-      const df32 al = pa.hi == 0.f ? one : df_add(one, df_neg(df_div(d, df32{2.f * pa.hi, 2.f * pa.lo})));
-      const df32 be = pb.hi == 0.f ? one : df_add(one, df_neg(df_div(d, df32{2.f * pb.hi, 2.f * pb.lo})));
-      val[top - 2] = df_add(df_mul(al, xa), df_mul(be, xb));
+      val[top - 2] = tiny_node(val[top - 2], val[top - 1]);
       lvl[top - 2] += 1;
       --top;
     }

@@ -67,8 +67,12 @@ int launch_reduce_chunks(const StageArgs& a, void* stream, const char** name) {
   }
 }
 
-int launch_coef(const StageArgs& a, void* stream, const char** name) {
-  const dim3 grid(a.seg_list ? a.nseg_list : a.nsegs, a.G), block(128);
+int launch_coef(const StageArgs& args, void* stream, const char** name) {
+  // several trees per CTA only when there are many more items than SMs
+  StageArgs a = args;
+  const int items = (a.seg_list ? a.nseg_list : a.nsegs) * a.G;
+  a.coef_per_warp = items >= 8 * a.num_sms ? 1 : 0;
+  const dim3 grid(a.coef_per_warp ? (items + kCoefWarps - 1) / kCoefWarps : items), block(32 * kCoefWarps);
   switch (a.Kg) {
     case 2: *name = "coef<2>"; return launch(coef_kernel<2>, grid, block, a, stream);
     case 4: *name = "coef<4>"; return launch(coef_kernel<4>, grid, block, a, stream);

@@ -155,16 +155,32 @@ int launch_onchip(const OnchipArgs& a, int dtype, int K, int count, int C, void*
                        : dispatch<BF16Tag>(a, K, count, C, stream, name);
 }
 
+namespace {
+template <typename Tag>
+int launch_tiny_tag(const TinyArgs& a, dim3 grid, dim3 block, cudaStream_t s) {
+  switch (a.K) {
+    case 2: return launch_pdl(tiny_reg_kernel<Tag, 2>, grid, block, 0, s, a);
+    case 4: return launch_pdl(tiny_reg_kernel<Tag, 4>, grid, block, 0, s, a);
+    case 8: return launch_pdl(tiny_reg_kernel<Tag, 8>, grid, block, 0, s, a);
+    case 16: return launch_pdl(tiny_reg_kernel<Tag, 16>, grid, block, 0, s, a);
+    case 32: return launch_pdl(tiny_reg_kernel<Tag, 32>, grid, block, 0, s, a);
+    case 64: return launch_pdl(tiny_reg_kernel<Tag, 64>, grid, block, 0, s, a);
+    default: return launch_pdl(tiny_df_kernel<Tag>, grid, block, 0, s, a);
+  }
+}
+}  // namespace
+
 int launch_tiny_df(const TinyArgs& a, int dtype, void* stream, const char** name) {
   if (a.count <= 0) return 0;
   const dim3 grid((a.count + kOnchipWarps - 1) / kOnchipWarps), block(kOnchipThreads);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bool reg = a.K <= 64;
   if (dtype == kF32) {
-    *name = "tiny_df<f32>";
-    return launch_pdl(tiny_df_kernel<F32Tag>, grid, block, 0, s, a);
+    *name = reg ? "tiny_reg<f32>" : "tiny_df<f32>";
+    return launch_tiny_tag<F32Tag>(a, grid, block, s);
   }
-  *name = "tiny_df<bf16>";
-  return launch_pdl(tiny_df_kernel<BF16Tag>, grid, block, 0, s, a);
+  *name = reg ? "tiny_reg<bf16>" : "tiny_df<bf16>";
+  return launch_tiny_tag<BF16Tag>(a, grid, block, s);
 }
 
 int pair_fused_max_grid(int dtype) {

@@ -288,7 +288,7 @@ def run_ours(args):
     dom_gbs = dom_bytes / (dom_ms / dom_n / 1e3) / 1e9 if dom_bytes else None
     traffic = None
     tpath = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(tpath):
+    if args.shrink == 1 and os.path.exists(tpath):  # (the figures are per full-size launch)
         try:
             traffic = json.load(open(tpath)).get(args.workload, {}).get(dom)
         except Exception:

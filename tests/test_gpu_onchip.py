@@ -181,7 +181,7 @@ def test_bulk_copy_wait_reports_timeout(native, monkeypatch):
 
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
-@pytest.mark.parametrize("K", [2, 7, 64, 128, 256])
+@pytest.mark.parametrize("K", [2, 4, 7, 16, 32, 64, 128, 256])
 def test_tiny_segments_one_warp_each(native, K, dtype):
     """Lengths 1..32 (and 33, just past the warp kernel) at every worker count, including
     those above the on-chip kernel's 64."""
@@ -191,6 +191,22 @@ def test_tiny_segments_one_warp_each(native, K, dtype):
     out = ags.reduce(grads, offs)
     torch.cuda.synchronize()
     check_against_oracle(grads, offs, out)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_tiny_kernels_agree_bitwise(native, dtype):
+    """Up to 64 workers the warp kernel holds every value in registers; above, it reads
+    the leaves in turn.  64 more zero workers add a zero right subtree, and Adasum(x, 0) =
+    x exactly, so 128 workers must reproduce the 64-worker bits."""
+    lengths = list(range(1, 33)) * 4
+    offs = workloads.offsets_from_numels(lengths)
+    grads = rand_grads(64, int(offs[-1]), dtype, seed=797, corr=0.5)
+    zeros = [torch.zeros_like(grads[0]) for _ in range(64)]
+    a = ags.reduce(grads, offs)
+    b = ags.reduce(grads + zeros, offs)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+    check_against_oracle(grads, offs, a)
 
 
 def test_tiny_segments_pair_symmetry_and_special_cases(native):

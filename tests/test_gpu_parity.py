@@ -670,7 +670,7 @@ def test_profiler_counts_each_input_byte_once(native, hooks, monkeypatch):
     stats = ags.profile_collect()
     ags.profile_enable(False)
     b = {k: v[2] for k, v in stats.items()}
-    small = sum(v for k, v in b.items() if k.startswith(("onchip", "tiny_df")))
+    small = sum(v for k, v in b.items() if k.startswith(("onchip", "tiny")))
     gram = sum(v for k, v in b.items() if k.startswith("gram") and not k.startswith("gram64"))
     small_pos = small / ((K + 1) * 4)
     assert small_pos == int(small_pos) and small_pos > 0
