@@ -1338,11 +1338,14 @@ __device__ __forceinline__ bool coef_item(const StageArgs& a, int item, int& seg
 }
 
 // a.coef_per_warp: warp w of CTA b takes item b * kCoefWarps + w; else CTA b takes item
-// b, all its threads gather, warp 0 runs the tree.
+// b, all its threads gather, warp 0 runs the tree.  Dynamic shared memory: one
+// CoefScratch per item of the CTA (a kernel that declared the four statically measured
+// slower in the per-CTA layout, between its neighbours' launches).
 template <int KG>
 __global__ void __launch_bounds__(32 * kCoefWarps) coef_kernel(const StageArgs a) {
   pdl_enter();
-  __shared__ CoefScratch<KG> sh[kCoefWarps];
+  extern __shared__ __align__(16) unsigned char coef_smem[];
+  CoefScratch<KG>* const sh = reinterpret_cast<CoefScratch<KG>*>(coef_smem);
   const int warp = threadIdx.x >> 5;
   const int items = (a.seg_list ? a.nseg_list : a.nsegs) * a.G;
   int seg, q;
