@@ -128,6 +128,7 @@ struct Plan {
   int* d_onchip = nullptr;
   bool tiny_on = false;
   int tiny_count = 0;
+  int tiny_c8 = 0, tiny_c16 = 0;  // d_tiny: segments of <= 8 positions, then <= 16, then the rest
   int* d_tiny = nullptr;
   int ncoef = 0;
   int* d_coef_list = nullptr;
@@ -395,6 +396,15 @@ adasum_status_t get_plan(Workspace& ws, const int64_t* offs, int L, int Kg0, int
   p.need64 = need64 || !tiny_on;
   p.tiny_on = tiny_on;
   p.tiny_count = static_cast<int>(tiny.size());
+  // the warp kernel packs 4 segments of <= 8 positions, or 2 of <= 16, into a warp
+  std::stable_partition(tiny.begin(), tiny.end(), [&](int s) { return offs[s + 1] - offs[s] <= 8; });
+  std::stable_partition(tiny.begin(), tiny.end(), [&](int s) { return offs[s + 1] - offs[s] <= 16; });
+  p.tiny_c8 = p.tiny_c16 = 0;
+  for (int s : tiny) {
+    const int64_t n = offs[s + 1] - offs[s];
+    if (n <= 8) ++p.tiny_c8;
+    else if (n <= 16) ++p.tiny_c16;
+  }
   std::vector<int> onchip_all, coef_list;
   for (int c = 0; c < 5; ++c) {
     p.onchip_first[c] = static_cast<int>(onchip_all.size());
@@ -942,6 +952,8 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
     ta.segs = plan->d_segs;
     ta.list = plan->d_tiny;
     ta.count = plan->tiny_count;
+    ta.count8 = plan->tiny_c8;
+    ta.count16 = plan->tiny_c16;
     ta.K = K;
     ta.n_total = N;
     ta.error = ws.d_error;

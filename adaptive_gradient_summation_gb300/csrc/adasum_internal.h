@@ -107,7 +107,6 @@ struct StageArgs {
   int nsmall;
   int combine_tiles;          // consecutive tiles per combine CTA (>= 1)
   int num_sms;                // SMs of the device (launch shapes)
-  int coef_per_warp;          // coefficient kernel: one item per warp (else per CTA)
 
   // fp64 path (only the segments listed by collect_kernel).
   double* partials64;         // [G][ntiles][E]
@@ -219,8 +218,10 @@ struct TinyArgs {
   const void* in[kMaxK];  // K leaves (K a power of two); null = a zero gradient
   void* out;
   const SegDesc* segs;
-  const int* list;        // the segments, one per warp
+  const int* list;        // the segments: count8 of <= 8 positions, then count16 of <= 16,
+                          // then the rest
   int count;
+  int count8, count16;
   int K;
   int64_t n_total;        // positions of every input and the output (bounds checks)
   int* error;             // device status word (bounds checks)

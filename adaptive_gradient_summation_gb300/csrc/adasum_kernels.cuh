@@ -1232,10 +1232,11 @@ __device__ double coefficient_chain(const double (&G)[KG][KG], const double* eps
   return ill ? 1e30 : rel;
 }
 
-// Items (segment, worker group) per CTA of the coefficient kernel when items are many:
-// one per warp, since a tree is a long chain of dependent steps on one warp and an SM
-// keeps many of them in flight.  With few items (fewer than a few per SM) each CTA takes
-// one and all its threads gather the Gram matrix: a long segment has many chunk sums.
+// Items (segment, worker group) per CTA of the coefficient step when items are many:
+// one per warp (coef_warp_kernel), since a tree is a long chain of dependent steps on one
+// warp and an SM keeps many of them in flight.  With few items (fewer than a few per SM)
+// each CTA takes one (coef_kernel) and all its threads gather the Gram matrix: a long
+// segment has many chunk sums.
 constexpr int kCoefWarps = 4;
 
 // Shared scratch of one item of the coefficient kernel.
@@ -1337,31 +1338,36 @@ __device__ __forceinline__ bool coef_item(const StageArgs& a, int item, int& seg
                                    sd.first_chunk >= 0 && sd.first_chunk + sd.nchunks <= a.nchunks);
 }
 
-// a.coef_per_warp: warp w of CTA b takes item b * kCoefWarps + w; else CTA b takes item
-// b, all its threads gather, warp 0 runs the tree.  Dynamic shared memory: one
-// CoefScratch per item of the CTA (a kernel that declared the four statically measured
-// slower in the per-CTA layout, between its neighbours' launches).
+// Few items: CTA b takes item b, all its threads gather, warp 0 runs the tree.  (A
+// single kernel holding both layouts needed more registers and made the calls with few
+// items measurably slower: ResNet-50, 0.311 -> 0.315 ms.)
 template <int KG>
 __global__ void __launch_bounds__(32 * kCoefWarps) coef_kernel(const StageArgs a) {
   pdl_enter();
-  extern __shared__ __align__(16) unsigned char coef_smem[];
-  CoefScratch<KG>* const sh = reinterpret_cast<CoefScratch<KG>*>(coef_smem);
-  const int warp = threadIdx.x >> 5;
+  __shared__ CoefScratch<KG> sh;
   const int items = (a.seg_list ? a.nseg_list : a.nsegs) * a.G;
   int seg, q;
   SegDesc sd;
-  if (a.coef_per_warp) {
-    const int item = blockIdx.x * kCoefWarps + warp;
-    if (item >= items || !coef_item(a, item, seg, q, sd)) return;  // whole warps
-    coef_gather<KG>(a, sd, seg, q, sh[warp], threadIdx.x & 31, 32);
-    __syncwarp();
-    coef_tree<KG>(a, sd, seg, q, sh[warp]);
-  } else {
-    if (static_cast<int>(blockIdx.x) >= items || !coef_item(a, blockIdx.x, seg, q, sd)) return;  // (uniform)
-    coef_gather<KG>(a, sd, seg, q, sh[0], threadIdx.x, blockDim.x);
-    __syncthreads();
-    if (warp == 0) coef_tree<KG>(a, sd, seg, q, sh[0]);
-  }
+  if (static_cast<int>(blockIdx.x) >= items || !coef_item(a, blockIdx.x, seg, q, sd)) return;  // (uniform)
+  coef_gather<KG>(a, sd, seg, q, sh, threadIdx.x, blockDim.x);
+  __syncthreads();
+  if (threadIdx.x < 32) coef_tree<KG>(a, sd, seg, q, sh);
+}
+
+// Many items: warp w of CTA b takes item b * kCoefWarps + w.
+template <int KG>
+__global__ void __launch_bounds__(32 * kCoefWarps) coef_warp_kernel(const StageArgs a) {
+  pdl_enter();
+  __shared__ CoefScratch<KG> sh[kCoefWarps];
+  const int warp = threadIdx.x >> 5;
+  const int items = (a.seg_list ? a.nseg_list : a.nsegs) * a.G;
+  const int item = blockIdx.x * kCoefWarps + warp;
+  int seg, q;
+  SegDesc sd;
+  if (item >= items || !coef_item(a, item, seg, q, sd)) return;  // whole warps
+  coef_gather<KG>(a, sd, seg, q, sh[warp], threadIdx.x & 31, 32);
+  __syncwarp();
+  coef_tree<KG>(a, sd, seg, q, sh[warp]);
 }
 
 // ----------------------------------------------------------- pass 2: combine (+ step)

@@ -541,13 +541,14 @@ __global__ void __launch_bounds__(kOnchipThreads, 2) onchip_kernel(const OnchipA
 // -- no Gram matrix, no error estimate, no second pass.  Eight segments per CTA, no
 // block barriers: the warps' latencies overlap.
 
-// One node: Adasum of two nodes held one position per lane (every lane calls it).
-// Out of line: a 64-leaf tree makes 63 calls, and one copy of the code keeps the
-// instruction cache warm for all the warps of an SM.
-__device__ __noinline__ df32 tiny_node(df32 xa, df32 xb) {
-  const df32 d = df_warp_sum(df_mul(xa, xb));
-  const df32 pa = df_warp_sum(df_mul(xa, xa));
-  const df32 pb = df_warp_sum(df_mul(xb, xb));
+// One node: Adasum of two nodes held one position per lane, the dot products summed
+// over aligned groups of gw lanes (one segment per group; every lane calls it).  Out of
+// line: a 64-leaf tree makes 63 calls, and one copy of the code keeps the instruction
+// cache warm for all the warps of an SM.
+__device__ __noinline__ df32 tiny_node(df32 xa, df32 xb, int gw) {
+  const df32 d = df_block_sum(df_mul(xa, xb), gw);
+  const df32 pa = df_block_sum(df_mul(xa, xa), gw);
+  const df32 pb = df_block_sum(df_mul(xb, xb), gw);
   const df32 one = {1.f, 0.f};
   const df32 al = pa.hi == 0.f ? one : df_add(one, df_neg(df_div(d, df32{2.f * pa.hi, 2.f * pa.lo})));
   const df32 be = pb.hi == 0.f ? one : df_add(one, df_neg(df_div(d, df32{2.f * pb.hi, 2.f * pb.lo})));
@@ -556,37 +557,58 @@ __device__ __noinline__ df32 tiny_node(df32 xa, df32 xb) {
 
 // The subtree over leaves [LO, LO + CNT) of values already in registers.
 template <int LO, int CNT, int KP>
-__device__ __forceinline__ df32 tiny_subtree(const float (&v)[KP]) {
+__device__ __forceinline__ df32 tiny_subtree(const float (&v)[KP], int gw) {
   if constexpr (CNT == 1) {
     return df32{v[LO], 0.f};
   } else {
-    const df32 left = tiny_subtree<LO, CNT / 2, KP>(v);
-    const df32 right = tiny_subtree<LO + CNT / 2, CNT / 2, KP>(v);
-    return tiny_node(left, right);
+    const df32 left = tiny_subtree<LO, CNT / 2, KP>(v, gw);
+    const df32 right = tiny_subtree<LO + CNT / 2, CNT / 2, KP>(v, gw);
+    return tiny_node(left, right, gw);
   }
 }
 
-// Warp w of the launch takes list entry w.  Returns false (after recording a failed
-// descriptor check) when the entry is not one this kernel may touch.
-__device__ __forceinline__ bool tiny_entry(const TinyArgs& a, int w, SegDesc& sd) {
-  sd = a.segs[a.list[w]];
+// List entry e, checked; false (after recording a failed check) when the entry is not
+// one the kernel may touch.
+__device__ __forceinline__ bool tiny_entry(const TinyArgs& a, int e, SegDesc& sd) {
+  sd = a.segs[a.list[e]];
   return ADASUM_CHECK(a.error, sd.start >= 0 && sd.len <= kTinyDirect && sd.start + sd.len <= a.n_total);
 }
 
-// K = KP leaves (a power of two up to 64): every value is loaded at once into
-// registers, read once, prescaled by the power of two of the segment's largest |value|,
-// and the tree runs from registers (its pairs (2i, 2i+1) at every level).
+// K = KP leaves (a power of two up to 64).  A warp takes 4 segments of at most 8
+// positions, or 2 of at most 16, or 1 (lane groups of gw = 8, 16 or 32; list order:
+// count8, count16, the rest).  Every value is loaded at once into registers, read once,
+// prescaled by the power of two of its segment's largest |value|, and the tree runs from
+// registers (its pairs (2i, 2i+1) at every level).  Sums over a group equal the sums over
+// the whole warp of the one-segment layout bit for bit: the other lanes hold zeros, and
+// adding a zero is exact.
 template <typename InTag, int KP>
 __global__ void __launch_bounds__(kOnchipThreads) tiny_reg_kernel(const TinyArgs a) {
   pdl_enter();
   using S = typename ElemTraits<InTag>::Storage;
   const int lane = threadIdx.x & 31;
   const int w = blockIdx.x * kOnchipWarps + (threadIdx.x >> 5);
-  if (w >= a.count) return;  // whole warps only
-  SegDesc sd;
-  if (!tiny_entry(a, w, sd)) return;
-  const int64_t p = sd.start + lane;
-  const bool on = lane < sd.len;
+  const int w8 = (a.count8 + 3) / 4, w16 = (a.count16 + 1) / 2;
+  const int c32 = a.count - a.count8 - a.count16;
+  if (w >= w8 + w16 + c32) return;  // whole warps only
+  int gw, e, end;
+  if (w < w8) {
+    gw = 8;
+    e = 4 * w + (lane >> 3);
+    end = a.count8;
+  } else if (w < w8 + w16) {
+    gw = 16;
+    e = a.count8 + 2 * (w - w8) + (lane >> 4);
+    end = a.count8 + a.count16;
+  } else {
+    gw = 32;
+    e = a.count8 + a.count16 + (w - w8 - w16);
+    end = a.count;
+  }
+  SegDesc sd = {};
+  const bool seg_ok = e < end && tiny_entry(a, e, sd);  // (lanes of a group agree)
+  const int pos = lane & (gw - 1);
+  const int64_t p = sd.start + pos;
+  const bool on = seg_ok && pos < sd.len;
   float v[KP];
 #pragma unroll
   for (int k = 0; k < KP; ++k) {
@@ -596,12 +618,12 @@ __global__ void __launch_bounds__(kOnchipThreads) tiny_reg_kernel(const TinyArgs
   float amax = 0.f;
 #pragma unroll
   for (int k = 0; k < KP; ++k) amax = fmaxf(amax, fabsf(v[k]));
-  for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
+  for (int off = gw >> 1; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
   const int ex = scale_exponent(amax);
   const float sc = ldexpf(1.f, -ex);
 #pragma unroll
   for (int k = 0; k < KP; ++k) v[k] *= sc;
-  const df32 r = tiny_subtree<0, KP, KP>(v);
+  const df32 r = tiny_subtree<0, KP, KP>(v, gw);
   if (on) store_df(static_cast<S*>(a.out), p, r, ex);
 }
 
@@ -638,7 +660,7 @@ __global__ void __launch_bounds__(kOnchipThreads) tiny_df_kernel(const TinyArgs 
     lvl[top] = 0;
     ++top;
     while (top >= 2 && lvl[top - 1] == lvl[top - 2]) {
-      val[top - 2] = tiny_node(val[top - 2], val[top - 1]);
+      val[top - 2] = tiny_node(val[top - 2], val[top - 1], 32);
       lvl[top - 2] += 1;
       --top;
     }

@@ -67,19 +67,25 @@ int launch_reduce_chunks(const StageArgs& a, void* stream, const char** name) {
   }
 }
 
-int launch_coef(const StageArgs& args, void* stream, const char** name) {
+int launch_coef(const StageArgs& a, void* stream, const char** name) {
   // several trees per CTA only when there are many more items than SMs
-  StageArgs a = args;
   const int items = (a.seg_list ? a.nseg_list : a.nsegs) * a.G;
-  a.coef_per_warp = items >= 8 * a.num_sms ? 1 : 0;
-  const dim3 grid(a.coef_per_warp ? (items + kCoefWarps - 1) / kCoefWarps : items), block(32 * kCoefWarps);
-  const int per_cta = a.coef_per_warp ? kCoefWarps : 1;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (items >= 8 * a.num_sms) {
+    const dim3 grid((items + kCoefWarps - 1) / kCoefWarps), block(32 * kCoefWarps);
+    switch (a.Kg) {
+      case 2: *name = "coef<2>"; return launch(coef_warp_kernel<2>, grid, block, a, stream);
+      case 4: *name = "coef<4>"; return launch(coef_warp_kernel<4>, grid, block, a, stream);
+      case 8: *name = "coef<8>"; return launch(coef_warp_kernel<8>, grid, block, a, stream);
+      case 16: *name = "coef<16>"; return launch(coef_warp_kernel<16>, grid, block, a, stream);
+      default: return static_cast<int>(cudaErrorInvalidValue);
+    }
+  }
+  const dim3 grid(items), block(32 * kCoefWarps);
   switch (a.Kg) {
-    case 2: *name = "coef<2>"; return launch_pdl(coef_kernel<2>, grid, block, per_cta * sizeof(CoefScratch<2>), s, a);
-    case 4: *name = "coef<4>"; return launch_pdl(coef_kernel<4>, grid, block, per_cta * sizeof(CoefScratch<4>), s, a);
-    case 8: *name = "coef<8>"; return launch_pdl(coef_kernel<8>, grid, block, per_cta * sizeof(CoefScratch<8>), s, a);
-    case 16: *name = "coef<16>"; return launch_pdl(coef_kernel<16>, grid, block, per_cta * sizeof(CoefScratch<16>), s, a);
+    case 2: *name = "coef<2>"; return launch(coef_kernel<2>, grid, block, a, stream);
+    case 4: *name = "coef<4>"; return launch(coef_kernel<4>, grid, block, a, stream);
+    case 8: *name = "coef<8>"; return launch(coef_kernel<8>, grid, block, a, stream);
+    case 16: *name = "coef<16>"; return launch(coef_kernel<16>, grid, block, a, stream);
     default: return static_cast<int>(cudaErrorInvalidValue);
   }
 }

@@ -172,9 +172,11 @@ int launch_tiny_tag(const TinyArgs& a, dim3 grid, dim3 block, cudaStream_t s) {
 
 int launch_tiny_df(const TinyArgs& a, int dtype, void* stream, const char** name) {
   if (a.count <= 0) return 0;
-  const dim3 grid((a.count + kOnchipWarps - 1) / kOnchipWarps), block(kOnchipThreads);
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool reg = a.K <= 64;
+  // warps: the register kernel packs short segments (see tiny_reg_kernel)
+  const int warps = reg ? (a.count8 + 3) / 4 + (a.count16 + 1) / 2 + (a.count - a.count8 - a.count16) : a.count;
+  const dim3 grid((warps + kOnchipWarps - 1) / kOnchipWarps), block(kOnchipThreads);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (dtype == kF32) {
     *name = reg ? "tiny_reg<f32>" : "tiny_df<f32>";
     return launch_tiny_tag<F32Tag>(a, grid, block, s);
