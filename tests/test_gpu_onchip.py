@@ -139,6 +139,36 @@ def test_cancelling_segments_recomputed_on_chip(native, K, dtype):
     assert ags.recomputed_segments() == sum(n > TINY for n in lengths)
 
 
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_segments_flagged_at_the_top_tree(native, dtype):
+    """More one-CTA segments than CTAs fit at once (each CTA then loads its next segment
+    while it finishes the current one), some of them cancelling only at the last level:
+    workers 0-31 near +s, workers 32-63 near -(1 - 1e-3) s.  Those are flagged by the
+    top tree, after the next segment's rows were issued, and recomputed from reloaded
+    rows; every segment must match the oracle."""
+    K = 64
+    rs = np.random.default_rng(781)
+    lengths = [int(n) for n in rs.integers(33, positions_per_cta(K) + 1, size=700)]
+    offs = workloads.offsets_from_numels(lengths)
+    n = int(offs[-1])
+    gen = torch.Generator(device=DEV).manual_seed(782)
+    s_ = torch.randn(n, generator=gen, device=DEV)
+    top = torch.zeros(n, dtype=torch.bool, device=DEV)
+    cancelling = [i for i in range(len(lengths)) if i % 7 == 3]
+    for i in cancelling:
+        top[offs[i]:offs[i + 1]] = True
+    grads = []
+    for k in range(K):
+        z = torch.randn(n, generator=gen, device=DEV)
+        sign = 1.0 if k < K // 2 else -(1 - 1e-3)
+        grads.append(torch.where(top, sign * s_ + 0.01 * z, 0.6 * s_ + 0.8 * z).to(dtype))
+    out = ags.reduce(grads, offs)
+    torch.cuda.synchronize()
+    check_against_oracle(grads, offs, out)
+    assert ags.recomputed_segments() >= len(cancelling)
+    assert ags.get_last_error() == ags.Status.OK
+
+
 def test_recompute_pair_is_bitwise_symmetric(native):
     """The on-chip recompute keeps the pair operator's exact commutativity."""
     a, b = _cancelling_set(2, 3000, torch.float32, seed=771)
