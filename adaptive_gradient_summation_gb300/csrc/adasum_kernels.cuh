@@ -431,6 +431,13 @@ __device__ __forceinline__ void gram_tile_mma(const StageArgs& a, int tile_id, i
   block_or_store(mma_lane_nz<BF16Tag>(org, orh), a.tile_nz + static_cast<size_t>(q) * a.ntiles + tile_id);
 }
 
+// 2x of both halves of a packed bf16 pair (exact: x + x).
+__device__ __forceinline__ uint32_t bf16x2_twice(uint32_t v) {
+  uint32_t r;
+  asm("add.rn.bf16x2 %0, %1, %1;" : "=r"(r) : "r"(v));
+  return r;
+}
+
 // Three bf16 parts of two fp32 values, x = h + m + l exactly: h is x rounded to bf16,
 // m the remainder rounded, l what is left (each remainder is exact in fp32, and at most
 // 8 significant bits are left for l).  Packed in pairs, as the MMA fragments take them.
@@ -445,7 +452,10 @@ __device__ __forceinline__ void split_bf16x3(float x0, float x1, uint32_t& h, ui
 // 32-position chunks first, first + nw, first + 2 nw, ... of [lo, hi).  Every value is
 // split into three bf16 parts (split_bf16x3) and x.y is taken as the six largest of the
 // nine part products, h.h + h.m + m.h + m.m + h.l + l.h: the three left out are below
-// 2^-23 |x||y| together, the size of one fp32 product's rounding.  The layout, the MMA
+// 2^-23 |x||y| together, the size of one fp32 product's rounding.  Four MMA products
+// per chunk carry them: the lane accumulates R = h.h + m.m + h.(2m) + h.(2l), whose
+// diagonal is the six products' sum and whose mirror sum R_ij + R_ji is twice it (the
+// callers take (R_ij + R_ji) / 2).  The layout, the MMA
 // accumulation and the compensated folding are those of gram_tile_mma (lane (g, t) holds
 // positions [8t, 8t+8) of workers g and g+8 of each chunk).  On return s0/e0 and s1/e1
 // hold the compensated sums of the lane's entries (columns 2t, 2t+1 and 8+2t, 9+2t of
@@ -500,12 +510,20 @@ __device__ __forceinline__ void gram_chunks_mma_f32(const float* xg, const float
         mma_bf16_16816(d1, ag[0], ah[0], ag[1], ah[1], bh[0], bh[1]);
         mma_bf16_16816(d1, ag[2], ah[2], ag[3], ah[3], bh[2], bh[3]);
       };
+      // R = h.h + m.m + h.(2m) + h.(2l): the mirror sum R_ij + R_ji is twice the six
+      // products' sum (h.m and m.h, h.l and l.h meet there), and its diagonal R_ii is that
+      // sum itself; doubling a bf16 value is exact
       mmas(gh, hh, gh, hh);
-      mmas(gh, hh, gm, hm);
-      mmas(gm, hm, gh, hh);
       mmas(gm, hm, gm, hm);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        gm[k] = bf16x2_twice(gm[k]);
+        hm[k] = bf16x2_twice(hm[k]);
+        gl[k] = bf16x2_twice(gl[k]);
+        hl[k] = bf16x2_twice(hl[k]);
+      }
+      mmas(gh, hh, gm, hm);
       mmas(gh, hh, gl, hl);
-      mmas(gl, hl, gh, hh);
     }
     if (++pending == kFold) {
 #pragma unroll
@@ -542,10 +560,10 @@ __device__ __forceinline__ void store_lane_gram16(float* m, const float (&s0)[4]
 }
 
 // Gram partial of one tile of fp32 gradients (16 workers) on the tensor cores, all warps
-// of the CTA sharing its chunks (gram_chunks_mma_f32).  The products h.m and m.h reach
-// entry (i, j) and entry (j, i) in opposite order, so each off-diagonal entry is the
-// mean of the two: permuting the workers then permutes the Gram matrix bit for bit, as
-// the sibling-swap symmetry needs.
+// of the CTA sharing its chunks (gram_chunks_mma_f32).  The lanes hold R (see there), so
+// each off-diagonal entry is the mean of R_ij and R_ji: the six products' sum, and
+// symmetric by construction, so permuting the workers permutes the Gram matrix bit for
+// bit, as the sibling-swap symmetry needs.
 template <int KG>
 __device__ __forceinline__ void gram_tile_mma_f32(const StageArgs& a, int tile_id, int q) {
   static_assert(KG == 16, "16 workers");
