@@ -118,7 +118,7 @@ struct Plan {
   SegDesc* d_segs = nullptr;
   ChunkDesc* d_chunks = nullptr;
   // small segments: held on chip (grouped by cluster size 1, 2, 4, 8, 16) or, up to
-  // kTinyDirect positions, one warp each; neither gets tiles.  The coefficient kernel
+  // kTinyDirect positions, on the warp kernel; neither gets tiles.  The coefficient kernel
   // then runs over the list of the remaining (tiled) segments.
   int onchip_K = 0;  // padded worker count the grouping was made for (0: none)
   int onchip_cmax = 0;
@@ -939,7 +939,7 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
     }
   }
 
-  // Tiny segments: one warp each, on side stream 0, forked after the on-chip launches.
+  // Tiny segments: the warp kernel, on side stream 0, forked after the on-chip launches.
   // The launch is a wave of latency-bound warps, so it runs concurrently with the tiled
   // passes (bandwidth-bound) instead of ahead of them; forked earlier, its CTAs held the
   // registers the on-chip CTAs need.

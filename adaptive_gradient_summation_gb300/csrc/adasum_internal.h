@@ -211,8 +211,8 @@ struct PairArgs {
   int inject_no_arrival;        // test hook: wait at the barrier without arriving
 };
 
-// Segments of at most kTinyDirect positions (adasum_onchip.cuh): one warp each, the
-// tree on the values themselves in double-float arithmetic.
+// Segments of at most kTinyDirect positions (adasum_onchip.cuh): a warp or a lane group
+// each, the tree on the values themselves in double-float arithmetic.
 constexpr int kTinyDirect = 32;
 struct TinyArgs {
   const void* in[kMaxK];  // K leaves (K a power of two); null = a zero gradient
@@ -250,7 +250,7 @@ int onchip_resident_clusters(int dtype, int K, int C);
 // CTAs of the fused pair kernel that fit on the current device at once (0: none).
 int pair_fused_max_grid(int dtype);
 int launch_pair_fused(const PairArgs& a, int dtype, int grid, void* stream, const char** name);
-// Tiny segments, one warp each.
+// Tiny segments (the warp kernel).
 int launch_tiny_df(const TinyArgs& a, int dtype, void* stream, const char** name);
 // fp64 path: build the flagged lists, then Gram / coefficients / combine over them.
 int launch_collect(const StageArgs& a, int grid, void* stream, const char** name);

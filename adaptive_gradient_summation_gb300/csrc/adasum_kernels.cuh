@@ -6,16 +6,21 @@
 // pairs (2i, 2i+1) at every level.  The tree is linear in the leaves, so its result is
 // out = sum_k c_k g_k, and every dot product it needs is a quadratic form of the
 // segment's Gram matrix.  The kernels here are:
-//   gram_*     pass 1: Gram partials of one tile (upper triangle, fp32), one HBM read
-//   coef       per segment: sum the tile partials (compensated fp32, fixed order), run
-//              the tree on the Gram matrix in fp64, emit c_0..c_{K-1}
+//   gram_*     pass 1: Gram partials of one tile (upper triangle, fp32), one HBM read,
+//              with each worker's nonzero bits for the range check
+//   reduce_chunks, coef / coef_warp
+//              per segment: sum the tile partials (compensated, fixed order), run the
+//              tree on the Gram matrix in double-float with its error estimate, emit
+//              c_0..c_{K-1} and the recompute flag
 //   combine    pass 2: out = sum_k c_k g_k, evaluated as a pairwise tree that mirrors
 //              the Adasum tree (so swapping sibling subtrees is bitwise symmetric),
 //              optionally followed by a heavy-ball Momentum-SGD step
+//   *64        the fp64 recompute of flagged segments
 // This path is HBM-bound (a few FMAs per byte), so it is written around coalesced
-// 128-bit loads and a grid of tiles that keeps every SM streaming.  The bf16 Gram uses
-// the tensor cores through mma.sync: bf16 x bf16 products are exact in fp32, and the
-// 16x16 Gram of a 16-worker group is a true (tiny) dense contraction.
+// 128-bit loads and a grid of tiles that keeps every SM streaming.  The Gram of 8- and
+// 16-worker groups uses the tensor cores through mma.sync: bf16 x bf16 products are
+// exact in fp32, fp32 values are split exactly into bf16 parts, and the 16x16 Gram of
+// a group is a true (tiny) dense contraction.
 #pragma once
 
 #include <cuda_bf16.h>

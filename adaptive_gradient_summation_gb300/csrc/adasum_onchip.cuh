@@ -1,7 +1,8 @@
 // adasum_onchip.cuh -- the small-segment path (sm_103a): one segment per CTA or per
 // thread-block cluster, every worker's slice of the segment read from HBM once into
 // shared memory (bulk copies), and the whole Adasum tree evaluated on chip; and, for
-// segments of at most 32 positions, one warp per segment.
+// segments of at most 32 positions, one warp (or a group of 8 or 16 of its lanes) per
+// segment.
 //
 // "Scaling Distributed Training with Adaptive Summation", Section 3: each layer is
 // combined on its own by the binary tree of Adasum(a, b) = (1 - a.b/(2|a|^2)) a +
@@ -536,10 +537,10 @@ __global__ void __launch_bounds__(kOnchipThreads, 2) onchip_kernel(const OnchipA
 
 // ------------------------------------------------------------------ tiny segments
 //
-// Segments of at most kTinyDirect positions: one warp each, lane j holding position j
-// of every node, the tree evaluated on the values themselves in double-float arithmetic
-// -- no Gram matrix, no error estimate, no second pass.  Eight segments per CTA, no
-// block barriers: the warps' latencies overlap.
+// Segments of at most kTinyDirect positions: a warp, or an aligned group of 8 or 16 of
+// its lanes, per segment, lane j holding position j of every node, the tree evaluated on
+// the values themselves in double-float arithmetic -- no Gram matrix, no error
+// estimate, no second pass.  No block barriers: the warps' latencies overlap.
 
 // One node: Adasum of two nodes held one position per lane, the dot products summed
 // over aligned groups of gw lanes (one segment per group; every lane calls it).  Out of
