@@ -321,7 +321,8 @@ adasum_status_t get_plan(Workspace& ws, const int64_t* offs, int L, int Kg0, int
   int rc_count = 0;
   bool need64 = false;
   const int64_t VW = dtype == kF32 ? 4 : 8;
-  int64_t onchip_vecs = onchip_K > 0 ? onchip_positions(onchip_K) / VW : 0;
+  // the on-chip fast pass (onchip_cmax > 0): segments it may hold, in 16-byte vectors
+  int64_t onchip_vecs = (onchip_K > 0 && onchip_cmax > 0) ? onchip_positions(onchip_K) / VW : 0;
   if (onchip_vecs > 0) {
     // The on-chip kernel pays off when small segments are numerous enough to fill the
     // GPU by themselves (each CTA is latency-bound and takes half an SM); a few small
@@ -737,18 +738,22 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
 
   // Plain reductions: segments of at most kTinyDirect positions go to the warp kernel,
   // small ones (up to 64 workers) to the on-chip kernel, the rest to the tiles.
-  // (ADASUM_TINY=0 and ADASUM_ONCHIP=0 switch the two kernels off, for comparisons;
-  // ADASUM_ONCHIP=force uses the on-chip kernel for every small segment, for tests;
-  // ADASUM_WARP_GRAM=0 keeps every tile on the CTA Gram kernels; ADASUM_ONCHIP_FAST=0
-  // leaves the on-chip kernel its recompute only.)
+  // Small segments take the tiled route; the on-chip kernel recomputes the flagged ones
+  // that fit a cluster.  Its fp32 fast pass (every level of a small segment on chip in one
+  // pass) measured slower than the tiled route at every worker count and dtype on the
+  // 10,000-segment layout, so the product library does not use it; the test build turns
+  // it on with ADASUM_ONCHIP_FAST=1 (segments that fit 2 CTAs, or ADASUM_ONCHIP_MAX_CLUSTER,
+  // when they are numerous) or ADASUM_ONCHIP=force (every segment it holds, whatever
+  // their number, unless ADASUM_ONCHIP_FAST=0).
+  // (ADASUM_TINY=0 and ADASUM_ONCHIP=0 switch the warp kernel and the on-chip kernel off,
+  // for comparisons; ADASUM_WARP_GRAM=0 keeps every tile on the CTA Gram kernels.)
   const bool plain = !mom && !chain && ortho == nullptr && K >= 2;
   const bool tiny_on = plain && env_on("ADASUM_TINY", true);
   int onchip_K = 0, onchip_cmax = 0;
   const char* onchip_env = hook("ADASUM_ONCHIP");
   const bool onchip_force = onchip_env != nullptr && std::strcmp(onchip_env, "force") == 0;
-  if (plain && K <= kOnchipMaxK && env_on("ADASUM_ONCHIP", true) && env_on("ADASUM_ONCHIP_FAST", true)) {
-    // clusters of up to 2 CTAs by default: larger clusters measured slower than the
-    // tiled route for the segments they add (ADASUM_ONCHIP_MAX_CLUSTER: up to 16)
+  if (plain && K <= kOnchipMaxK && env_on("ADASUM_ONCHIP", true) &&
+      env_on("ADASUM_ONCHIP_FAST", onchip_force)) {
     onchip_cmax = std::min<int>(onchip_max_cluster(dtype, K), env_int("ADASUM_ONCHIP_MAX_CLUSTER", 2));
     if (onchip_cmax >= 1) onchip_K = K;
   }

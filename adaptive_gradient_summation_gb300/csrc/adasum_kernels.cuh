@@ -342,32 +342,32 @@ __device__ __forceinline__ uint32_t mma_lane_nz(uint32_t org, uint32_t orh) {
 // the same registers serve as the A operand (workers x positions) and as the B operand
 // (positions x workers).  Two k-steps of 16 cover the 32 positions; the two n-tiles
 // give columns 0-7 and 8-15 of G.
+// One warp's share of the Gram of bf16 rows on the tensor cores (8 or 16 workers): the
+// 32-position chunks first, first + nw, first + 2 nw, ... of [lo, hi), lane (g, t)
+// holding positions [8t, 8t+8) of workers g and g+8 of each chunk, which serve as both
+// MMA operands (G = X X^T).  On return s0/e0 and s1/e1 hold the compensated sums of the
+// lane's entries (columns 2t, 2t+1 and 8+2t, 9+2t of rows g and g+8), org/orh the raw-bit
+// ORs of workers g and g + 8 (range check).
 template <int KG>
-__device__ __forceinline__ void gram_tile_mma(const StageArgs& a, int tile_id, int q) {
+__device__ __forceinline__ void gram_chunks_mma_bf16(const uint16_t* xg, const uint16_t* xh, int64_t lo, int64_t hi,
+                                                     bool aligned, int first, int nw, float (&s0)[4],
+                                                     float (&e0)[4], float (&s1)[4], float (&e1)[4],
+                                                     uint32_t& org, uint32_t& orh) {
   static_assert(KG == 8 || KG == 16, "tensor-core Gram handles 8 or 16 workers");
-  constexpr int E = tri_count(KG);
   constexpr int U = 4;        // chunks of 32 positions loaded per warp iteration
   constexpr int kFold = 4;    // iterations accumulated in the MMA before a Kahan fold
-  const TileDesc t = a.tiles[tile_id];
-  if (!tile_ok(a, tile_id, t)) return;  // (uniform over the CTA)
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int g = lane >> 2, tq = lane & 3;
-  const uint16_t* xg = static_cast<const uint16_t*>(a.in[q * KG + g]);
-  const uint16_t* xh = KG == 16 ? static_cast<const uint16_t*>(a.in[q * KG + g + 8]) : nullptr;
-  const bool aligned = a.aligned != 0;
-  const int64_t lo = t.start, hi = t.start + t.len;
+  const int tq = threadIdx.x & 3;
   const int64_t c0 = lo >> 5, c1 = (hi + 31) >> 5;  // 32-position chunks
-
   float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
-  float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
-  float e0[4] = {0.f, 0.f, 0.f, 0.f}, e1[4] = {0.f, 0.f, 0.f, 0.f};
-  uint32_t org = 0u, orh = 0u;  // raw-bit ORs of workers g and g + 8 (range check)
+#pragma unroll
+  for (int i = 0; i < 4; ++i) s0[i] = e0[i] = s1[i] = e1[i] = 0.f;
+  org = orh = 0u;
   int pending = 0;
-  for (int64_t c = c0 + warp; c < c1; c += kWarps * U) {
+  for (int64_t c = c0 + first; c < c1; c += static_cast<int64_t>(nw) * U) {
     uint4 rg[U], rh[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const int64_t cu = c + static_cast<int64_t>(u) * kWarps;
+      const int64_t cu = c + static_cast<int64_t>(u) * nw;
       const int64_t v = cu * 4 + tq;
       if (cu < c1) {
         rg[u] = load_vec_raw<BF16Tag, kLoadKeep>(xg, v, lo, hi, aligned);
@@ -405,6 +405,21 @@ __device__ __forceinline__ void gram_tile_mma(const StageArgs& a, int tile_id, i
     kahan_add(s0[i], e0[i], d0[i]);
     kahan_add(s1[i], e1[i], d1[i]);
   }
+}
+
+template <int KG>
+__device__ __forceinline__ void gram_tile_mma(const StageArgs& a, int tile_id, int q) {
+  static_assert(KG == 8 || KG == 16, "tensor-core Gram handles 8 or 16 workers");
+  constexpr int E = tri_count(KG);
+  const TileDesc t = a.tiles[tile_id];
+  if (!tile_ok(a, tile_id, t)) return;  // (uniform over the CTA)
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g = lane >> 2, tq = lane & 3;
+  const uint16_t* xg = static_cast<const uint16_t*>(a.in[q * KG + g]);
+  const uint16_t* xh = KG == 16 ? static_cast<const uint16_t*>(a.in[q * KG + g + 8]) : nullptr;
+  float s0[4], e0[4], s1[4], e1[4];
+  uint32_t org, orh;
+  gram_chunks_mma_bf16<KG>(xg, xh, t.start, t.start + t.len, a.aligned != 0, warp, kWarps, s0, e0, s1, e1, org, orh);
 
   // Each warp now holds its full KG x KG partial, one distinct entry per register:
   // s0[0..1] = G[g][2t..2t+1], s0[2..3] = G[g+8][2t..2t+1], s1 likewise for columns
@@ -628,6 +643,41 @@ __global__ void __launch_bounds__(kThreads, 3) gram_warp_mma_f32_kernel(const St
     dst[e] = i == j ? m[i * KG + i] : 0.5f * __fadd_rn(m[i * KG + j], m[j * KG + i]);
   }
   const uint32_t nz = warp_or_u32(mma_lane_nz<F32Tag>(mg, mh));
+  if (lane == 0) a.tile_nz[static_cast<size_t>(q) * a.ntiles + tile_id] = nz;
+}
+
+// Gram partials of small tiles of bf16 gradients (16 workers), one warp per (tile,
+// group), on the tensor cores (gram_chunks_mma_bf16 with the warp alone on the tile).
+// The bf16 Gram needs no mirror mean: h.h products are symmetric as they stand.
+template <int KG>
+__global__ void __launch_bounds__(kThreads) gram_warp_mma_bf16_kernel(const StageArgs a) {
+  pdl_enter();
+  static_assert(KG == 16, "16 workers");
+  constexpr int E = tri_count(KG);
+  __shared__ float red[kWarps][KG * KG];
+  const int wb = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int w = blockIdx.x * kWarps + wb;
+  if (w >= a.nsmall) return;  // whole warps only (no block barrier below)
+  const int q = blockIdx.y;
+  const int tile_id = a.small_list[w];
+  const TileDesc t = a.tiles[tile_id];
+  if (!tile_ok(a, tile_id, t)) return;  // (uniform over the warp)
+  const int g = lane >> 2;
+  float s0[4], e0[4], s1[4], e1[4];
+  uint32_t mg, mh;
+  gram_chunks_mma_bf16<KG>(static_cast<const uint16_t*>(a.in[q * KG + g]),
+                           static_cast<const uint16_t*>(a.in[q * KG + g + 8]), t.start, t.start + t.len,
+                           a.aligned != 0, 0, 1, s0, e0, s1, e1, mg, mh);
+  float* m = red[wb];
+  store_lane_gram16(m, s0, e0, s1, e1);
+  __syncwarp();
+  float* dst = a.partials + (static_cast<size_t>(q) * a.ntiles + tile_id) * E;
+  for (int e = lane; e < E; e += 32) {
+    int i, j;
+    tri_unpack(KG, e, i, j);
+    dst[e] = m[i * KG + j];
+  }
+  const uint32_t nz = warp_or_u32(mma_lane_nz<BF16Tag>(mg, mh));
   if (lane == 0) a.tile_nz[static_cast<size_t>(q) * a.ntiles + tile_id] = nz;
 }
 

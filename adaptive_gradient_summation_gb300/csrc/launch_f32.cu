@@ -51,7 +51,9 @@ int launch_gram_warp(const StageArgs& a, int in_dtype, void* stream, const char*
     case 2: *name = "gram_warp<bf16,2>"; return launch(gram_warp_kernel<BF16Tag, 2>, grid, block, a, stream);
     case 4: *name = "gram_warp<bf16,4>"; return launch(gram_warp_kernel<BF16Tag, 4>, grid, block, a, stream);
     case 8: *name = "gram_warp<bf16,8>"; return launch(gram_warp_kernel<BF16Tag, 8>, grid, block, a, stream);
-    case 16: *name = "gram_warp<bf16,16>"; return launch(gram_warp_kernel<BF16Tag, 16>, grid, block, a, stream);
+    case 16:  // the tensor cores, as in the CTA Gram
+      *name = "gram_warp_mma<bf16,16>";
+      return launch(gram_warp_mma_bf16_kernel<16>, grid, block, a, stream);
     default: return static_cast<int>(cudaErrorInvalidValue);
   }
 }

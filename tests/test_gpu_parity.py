@@ -49,6 +49,17 @@ def test_workload_shapes_small(native, name, shrink):
     check_against_oracle(wl.grads, wl.seg_offsets, out)
 
 
+@pytest.mark.parametrize("K", [16, 32])
+def test_small_segment_layout_bf16(native, K):
+    """The 10,000-segment layout (a quarter of each length) in bf16 with 16-worker groups:
+    hundreds of short tiles on the tensor-core warp Gram, the rest on the CTA Gram."""
+    wl = workloads.make("small_segments_k64", device=DEV, shrink=4)
+    grads = [g.to(torch.bfloat16) for g in wl.grads[:K]]
+    out = ags.reduce(grads, wl.seg_offsets)
+    torch.cuda.synchronize()
+    check_against_oracle(grads, wl.seg_offsets, out)
+
+
 @pytest.mark.parametrize("init", ["zero", "random"])
 def test_momentum_small(native, init):
     wl = workloads.make("gpt_k8_momentum", device=DEV, shrink=2048, momentum_init=init)
@@ -232,15 +243,9 @@ def test_segments_are_independent(native):
         assert err <= 2e-5 * np.linalg.norm(ref), s
 
 
-@pytest.mark.parametrize("K,dtype", [(8, torch.float32), (16, torch.bfloat16), (64, torch.float32)])
-def test_relocated_layers_are_bitwise_identical(native, K, dtype):
-    """Per-layer application, bit for bit under re-layout: the same layers laid out in
-    another order give every layer exactly the same bits.  Every length is a multiple of
-    32 positions, so each layer keeps its grouping of partial sums wherever it lands, and
-    the call's size and the route of every segment (warp kernel, on-chip clusters of one
-    and two CTAs, tiles) are unchanged."""
+def _relocation_case(K, dtype):
     rng = np.random.default_rng(41 + K)
-    lengths = [32 * int(x) for x in rng.integers(1, 21, size=700)]  # tiny and on-chip sizes
+    lengths = [32 * int(x) for x in rng.integers(1, 21, size=700)]  # tiny and short segments
     lengths += [32 * 3125, 32 * 97, 65_536, 32 * 4099]               # tiled
     perm = rng.permutation(len(lengths))
     offs_a = workloads.offsets_from_numels(lengths)
@@ -252,6 +257,24 @@ def test_relocated_layers_are_bitwise_identical(native, K, dtype):
     torch.cuda.synchronize()
     for j, i in enumerate(perm):
         assert torch.equal(out_a[offs_a[i]:offs_a[i + 1]], out_b[offs_b[j]:offs_b[j + 1]]), (i, lengths[i])
+
+
+@pytest.mark.parametrize("K,dtype", [(8, torch.float32), (16, torch.bfloat16), (64, torch.float32)])
+def test_relocated_layers_are_bitwise_identical(native, K, dtype):
+    """Per-layer application, bit for bit under re-layout: the same layers laid out in
+    another order give every layer exactly the same bits.  Every length is a multiple of
+    32 positions, so each layer keeps its grouping of partial sums wherever it lands, and
+    the call's size and the route of every segment (warp kernel, CTA and warp Gram tiles)
+    are unchanged."""
+    _relocation_case(K, dtype)
+
+
+@pytest.mark.parametrize("K,dtype", [(16, torch.bfloat16), (64, torch.float32)])
+def test_relocated_layers_bitwise_on_chip(native, hooks, monkeypatch, K, dtype):
+    """The same with the on-chip fast pass of the test build (clusters of one and two CTAs
+    for the short segments)."""
+    monkeypatch.setenv("ADASUM_ONCHIP_FAST", "1")
+    _relocation_case(K, dtype)
 
 
 def test_scale_equivariance_power_of_two(native):
