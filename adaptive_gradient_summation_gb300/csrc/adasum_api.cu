@@ -529,9 +529,10 @@ adasum_status_t launch_one(cudaStream_t stream, F&& f, double bytes = 0.0) {
 // fp32 pass of one stage (all groups): Gram partials, chunk sums, coefficients with the
 // conditioning check, then `before_combine` (when given), then the combine (flagged
 // segments are skipped and left to the recompute).
-// bytes: the algorithmic bytes of the CTA Gram, the warp Gram and the combine launches.
+// bytes: the algorithmic bytes of the CTA Gram, the warp Gram, the CTA combine and the
+// warp combine launches (the warp launches take the short tiles when they have a list).
 adasum_status_t run_stage(StageArgs& a, int in_dtype, int out_dtype, int momentum, cudaStream_t stream,
-                          const std::function<adasum_status_t()>& before_combine, const double (&bytes)[3]) {
+                          const std::function<adasum_status_t()>& before_combine, const double (&bytes)[4]) {
   if (a.ntiles == 0)  // every segment went to the small-segment kernels
     return before_combine ? before_combine() : ADASUM_OK;
   if (a.Kg > 1) {
@@ -556,10 +557,28 @@ adasum_status_t run_stage(StageArgs& a, int in_dtype, int out_dtype, int momentu
   }
   if (before_combine)
     if (adasum_status_t st = before_combine()) return st;
-  return launch_one(stream, [&](const char** n) {
-    return in_dtype == kBF16 ? launch_combine_bf16in(a, out_dtype, momentum, stream, n)
-                             : launch_combine_f32in(a, out_dtype, momentum, stream, n);
-  }, bytes[2]);
+  // Short tiles get a warp each when groups have 8 or more workers; with fewer, the
+  // per-tile work is small and one CTA over every tile measured faster.
+  StageArgs c = a;
+  const bool warp_combine = a.nsmall > 0 && a.Kg >= 8;
+  if (!warp_combine) {
+    c.tile_list = nullptr;
+    c.ntile_list = 0;
+    c.nsmall = 0;
+  }
+  const int n = c.tile_list ? c.ntile_list : c.ntiles;
+  c.combine_tiles = static_cast<int>(
+      std::max<int64_t>(1, std::min<int64_t>(4, n / (16 * static_cast<int64_t>(std::max(1, c.num_sms))))));
+  for (int warp = 0; warp < 2; ++warp) {
+    if (warp ? c.nsmall == 0 : n == 0) continue;
+    const double b = warp ? bytes[3] : (warp_combine ? bytes[2] : bytes[2] + bytes[3]);
+    if (adasum_status_t st = launch_one(stream, [&](const char** nm) {
+          return in_dtype == kBF16 ? launch_combine_bf16in(c, out_dtype, momentum, warp, stream, nm)
+                                   : launch_combine_f32in(c, out_dtype, momentum, warp, stream, nm);
+        }, b))
+      return st;
+  }
+  return ADASUM_OK;
 }
 
 // fp64 pass of one stage over the flagged lists.
@@ -857,8 +876,7 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
     a.Ktotal = chain ? Kreal : K;
     a.seg_exp = seg_exp;
     // up to 4 tiles (1 MiB) per combine CTA while the grid keeps 16 CTAs per SM
-    a.combine_tiles = static_cast<int>(std::max<int64_t>(
-        1, std::min<int64_t>(4, plan->ntiles / (16 * static_cast<int64_t>(num_sms)))));
+    a.combine_tiles = 1;  // (set per launch by run_stage)
     a.num_sms = num_sms;
     if (plan->rc_cmax > 0) {
       a.oc_vecs = onchip_positions(K) / (dtype == kF32 ? 4 : 8);
@@ -1088,8 +1106,9 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
     const double big = static_cast<double>(plan->nsmall > 0 ? plan->pos_big : plan->pos_tiles);
     const double out_b = (!last || out != nullptr) ? groups[s] * es_out : 0.0;
     const double mom_b = (last && mom) ? (momentum != nullptr ? 16.0 : 8.0) : 0.0;
-    const double bytes[3] = {big * nin * es_in, static_cast<double>(plan->pos_small) * nin * es_in,
-                             static_cast<double>(plan->pos_tiles) * (nin * es_in + out_b + mom_b)};
+    const double per_pos = nin * es_in + out_b + mom_b;  // the combine's bytes per position
+    const double small = static_cast<double>(plan->nsmall > 0 ? plan->pos_small : 0);
+    const double bytes[4] = {big * nin * es_in, small * nin * es_in, big * per_pos, small * per_pos};
     if (adasum_status_t st = run_stage(a, in_dt, out_dt, (last && mom) ? 1 : 0, stream,
                                        last ? fork_recompute : std::function<adasum_status_t()>(), bytes))
       return st;

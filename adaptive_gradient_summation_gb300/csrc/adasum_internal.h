@@ -105,7 +105,8 @@ struct StageArgs {
   int ntile_list;
   const int* small_list;      // small tiles, one warp each (gram_warp_kernel)
   int nsmall;
-  int combine_tiles;          // consecutive tiles per combine CTA (>= 1)
+  int combine_tiles;          // consecutive tiles per combine CTA (>= 1; up to 4 while the
+                              //   grid keeps 16 CTAs per SM)
   int num_sms;                // SMs of the device (launch shapes)
 
   // fp64 path (only the segments listed by collect_kernel).
@@ -235,9 +236,9 @@ int launch_gram_bf16(const StageArgs& a, void* stream, const char** name);
 // Gram partials of a.small_list's tiles, one warp per (tile, group).
 int launch_gram_warp(const StageArgs& a, int in_dtype, void* stream, const char** name);
 int launch_coef(const StageArgs& a, void* stream, const char** name);
-int launch_combine_f32in(const StageArgs& a, int out_dtype, int momentum, void* stream,
+int launch_combine_f32in(const StageArgs& a, int out_dtype, int momentum, int warp, void* stream,
                          const char** name);
-int launch_combine_bf16in(const StageArgs& a, int out_dtype, int momentum, void* stream,
+int launch_combine_bf16in(const StageArgs& a, int out_dtype, int momentum, int warp, void* stream,
                           const char** name);
 // Partial-Gram chunk sums (segments with many tiles), then coefficients.
 int launch_reduce_chunks(const StageArgs& a, void* stream, const char** name);

@@ -711,38 +711,59 @@ __device__ __forceinline__ void gram_tile(const StageArgs& a, int tile_id, int q
 // Sum the fp32 tile partials of one chunk of at most kChunkTiles tiles (compensated,
 // in tile order) into one fp64 value per Gram entry.
 // (Partials written by other CTAs are read through L2, never a possibly stale L1.)
+// Chunks per CTA of the chunk-sum kernel when chunks are many: most chunks of a layout
+// with many short segments hold one tile, and a CTA per chunk would leave most of its
+// threads idle.  With few chunks, one per CTA spreads them over the SMs.
+constexpr int kChunksPerCta = 8;
+
+// Entry e of chunk c (group q): the compensated sum of its tiles' partials, in tile
+// order, as an fp64 value.
 template <int KG>
-__device__ __forceinline__ void reduce_chunk(const StageArgs& a, int c, int q) {
+__device__ __forceinline__ void reduce_chunk_entry(const StageArgs& a, const ChunkDesc& ch, int c, int e, int q) {
   constexpr int E = tri_count(KG);
-  const ChunkDesc ch = a.chunks[c];
-  if (!ADASUM_CHECK(a.error, c < a.nchunks && ch.first_tile >= 0 && ch.ntiles >= 1 &&
-                                 ch.ntiles <= kChunkTiles && ch.first_tile + ch.ntiles <= a.ntiles))
-    return;
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    const float* p = a.partials + (static_cast<size_t>(q) * a.ntiles + ch.first_tile) * E + e;
-    float v[kChunkTiles];
+  const float* p = a.partials + (static_cast<size_t>(q) * a.ntiles + ch.first_tile) * E + e;
+  float v[kChunkTiles];
 #pragma unroll
-    for (int t = 0; t < kChunkTiles; ++t)
-      v[t] = t < ch.ntiles ? __ldcg(p + static_cast<size_t>(t) * E) : 0.f;  // issued together
-    float sum = 0.f, comp = 0.f;
+  for (int t = 0; t < kChunkTiles; ++t)
+    v[t] = t < ch.ntiles ? __ldcg(p + static_cast<size_t>(t) * E) : 0.f;  // issued together
+  float sum = 0.f, comp = 0.f;
 #pragma unroll
-    for (int t = 0; t < kChunkTiles; ++t) kahan_add(sum, comp, v[t]);
-    a.chunk_sums[(static_cast<size_t>(q) * a.nchunks + c) * E + e] =
-        static_cast<double>(sum) - static_cast<double>(comp);
-  }
-  // the workers with a nonzero value in the chunk
-  if (threadIdx.x == 0) {
-    const uint32_t* p = a.tile_nz + static_cast<size_t>(q) * a.ntiles + ch.first_tile;
-    uint32_t m = 0u;
-    for (int t = 0; t < ch.ntiles; ++t) m |= __ldcg(p + t);
-    a.chunk_nz[static_cast<size_t>(q) * a.nchunks + c] = m;
-  }
+  for (int t = 0; t < kChunkTiles; ++t) kahan_add(sum, comp, v[t]);
+  a.chunk_sums[(static_cast<size_t>(q) * a.nchunks + c) * E + e] = static_cast<double>(sum) - static_cast<double>(comp);
 }
 
+__device__ __forceinline__ bool chunk_ok(const StageArgs& a, int c, ChunkDesc& ch) {
+  ch = a.chunks[c];
+  return ADASUM_CHECK(a.error, c < a.nchunks && ch.first_tile >= 0 && ch.ntiles >= 1 &&
+                                   ch.ntiles <= kChunkTiles && ch.first_tile + ch.ntiles <= a.ntiles);
+}
+
+// CTA b: chunks b * per ... (per = the chunks over the grid: 1 or kChunksPerCta), every
+// (chunk, entry) pair to one thread, and the OR of each chunk's per-tile nonzero words
+// (range check).
 template <int KG>
 __global__ void __launch_bounds__(kThreads) reduce_chunks_kernel(const StageArgs a) {
   pdl_enter();
-  reduce_chunk<KG>(a, blockIdx.x, blockIdx.y);
+  constexpr int E = tri_count(KG);
+  const int q = blockIdx.y;
+  const int per = min(kChunksPerCta, (a.nchunks + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x));
+  const int c0 = blockIdx.x * per;
+  for (int idx = threadIdx.x; idx < per * E; idx += kThreads) {
+    const int c = c0 + idx / E, e = idx % E;
+    ChunkDesc ch;
+    if (c >= a.nchunks || !chunk_ok(a, c, ch)) continue;
+    reduce_chunk_entry<KG>(a, ch, c, e, q);
+  }
+  if (static_cast<int>(threadIdx.x) < per) {
+    const int c = c0 + threadIdx.x;
+    ChunkDesc ch;
+    if (c < a.nchunks && chunk_ok(a, c, ch)) {
+      const uint32_t* p = a.tile_nz + static_cast<size_t>(q) * a.ntiles + ch.first_tile;
+      uint32_t m = 0u;
+      for (int t = 0; t < ch.ntiles; ++t) m |= __ldcg(p + t);
+      a.chunk_nz[static_cast<size_t>(q) * a.nchunks + c] = m;
+    }
+  }
 }
 
 
@@ -1524,7 +1545,8 @@ __device__ __forceinline__ void load_f32_vec(const float* x, int64_t p0, int64_t
 // (fp32), and out is written only when a.out[q] is not null.
 // (Coefficients and flags written by other CTAs are read through L2.)
 template <typename InTag, typename OutTag, int KG, bool MOM>
-__device__ __forceinline__ void combine_range(const StageArgs& a, int seg, int64_t lo, int64_t hi, int q) {
+__device__ __forceinline__ void combine_range(const StageArgs& a, int seg, int64_t lo, int64_t hi, int q,
+                                              int first, int step) {
   using SI = typename ElemTraits<InTag>::Storage;
   using SO = typename ElemTraits<OutTag>::Storage;
   constexpr int VW = ElemTraits<InTag>::kVW;
@@ -1544,7 +1566,7 @@ __device__ __forceinline__ void combine_range(const StageArgs& a, int seg, int64
   for (int k = 0; k < KG; ++k) x[k] = static_cast<const SI*>(a.in[q * KG + k]);
   SO* y = static_cast<SO*>(a.out[q]);
   const int64_t v0 = lo / VW, v1 = (hi + VW - 1) / VW;
-  for (int64_t v = v0 + threadIdx.x; v < v1; v += kThreads) {
+  for (int64_t v = v0 + first; v < v1; v += step) {
     uint4 r[KG];
 #pragma unroll
     for (int k = 0; k < KG; ++k) r[k] = load_vec_raw<InTag, kLoadStream>(x[k], v, lo, hi, aligned);
@@ -1575,33 +1597,50 @@ __device__ __forceinline__ void combine_range(const StageArgs& a, int seg, int64
   }
 }
 
-// out = sum_k c_k g_k over one tile (see combine_range).
-template <typename InTag, typename OutTag, int KG, bool MOM>
-__device__ __forceinline__ void combine_tile(const StageArgs& a, int tile_id, int q) {
-  const TileDesc t = a.tiles[tile_id];
-  combine_range<InTag, OutTag, KG, MOM>(a, t.seg, t.start, t.start + t.len, q);
+// The tile at entry i of a list of tile ids (all tiles when the list is null), checked.
+__device__ __forceinline__ bool list_tile(const StageArgs& a, const int* list, int i, TileDesc& t) {
+  const int id = list ? list[i] : i;
+  if (!ADASUM_CHECK(a.error, id >= 0 && id < a.ntiles)) return false;
+  t = a.tiles[id];
+  return true;
 }
 
 template <typename InTag, typename OutTag, int KG, bool MOM>
 __global__ void __launch_bounds__(kThreads) combine_kernel(const StageArgs a) {
   pdl_enter();
-  // a.combine_tiles consecutive tiles per CTA, consecutive tiles of one segment merged
-  // into one range: the prologue (coefficients, flag) is a dependent L2 round trip, and
-  // one long strided loop streams better than several short ones
+  // a.combine_tiles consecutive tiles per CTA (of a.tile_list when short tiles have a
+  // launch of their own), adjacent tiles of one segment merged into one range: the
+  // prologue (coefficients, flag) is a dependent L2 round trip, and one long strided
+  // loop streams better than several short ones
+  const int n = a.tile_list ? a.ntile_list : a.ntiles;
   const int t0 = blockIdx.x * a.combine_tiles;
-  const int t1 = min(a.ntiles, t0 + a.combine_tiles);
+  const int t1 = min(n, t0 + a.combine_tiles);
   for (int t = t0; t < t1;) {
-    const TileDesc first = a.tiles[t];
+    TileDesc first;
+    if (!list_tile(a, a.tile_list, t, first)) return;  // (uniform over the CTA)
     int64_t hi = first.start + first.len;
     int u = t + 1;
     for (; u < t1; ++u) {
-      const TileDesc nx = a.tiles[u];
-      if (nx.seg != first.seg) break;
+      TileDesc nx;
+      if (!list_tile(a, a.tile_list, u, nx) || nx.seg != first.seg || nx.start != hi) break;
       hi = nx.start + nx.len;
     }
-    combine_range<InTag, OutTag, KG, MOM>(a, first.seg, first.start, hi, blockIdx.y);
+    combine_range<InTag, OutTag, KG, MOM>(a, first.seg, first.start, hi, blockIdx.y, threadIdx.x, kThreads);
     t = u;
   }
+}
+
+// Short tiles (a.small_list, at most kSmallTile positions), one warp each: a CTA per
+// tile would leave most of its threads without a vector and run its tiles' coefficient
+// loads one after another.
+template <typename InTag, typename OutTag, int KG, bool MOM>
+__global__ void __launch_bounds__(kThreads) combine_warp_kernel(const StageArgs a) {
+  pdl_enter();
+  const int w = blockIdx.x * kWarps + (threadIdx.x >> 5);
+  if (w >= a.nsmall) return;  // whole warps only (no block barrier below)
+  TileDesc t;
+  if (!list_tile(a, a.small_list, w, t)) return;
+  combine_range<InTag, OutTag, KG, MOM>(a, t.seg, t.start, t.start + t.len, blockIdx.y, threadIdx.x & 31, 32);
 }
 
 // ------------------------------------------------------------- flags between CTAs

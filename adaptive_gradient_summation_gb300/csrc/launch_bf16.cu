@@ -33,8 +33,20 @@ int launch_gram_bf16(const StageArgs& a, void* stream, const char** name) {
 }
 
 template <typename OutTag, bool MOM>
-static int combine_bf16_k(const StageArgs& a, void* stream, const char** name) {
-  const dim3 grid((a.ntiles + a.combine_tiles - 1) / a.combine_tiles, a.G), block(kThreads);
+static int combine_bf16_k(const StageArgs& a, int warp, void* stream, const char** name) {
+  if (warp) {  // short tiles, one warp each
+    const dim3 grid((a.nsmall + kWarps - 1) / kWarps, a.G), block(kThreads);
+    switch (a.Kg) {
+      case 1: *name = "combine_warp<bf16,1>"; return launch(combine_warp_kernel<BF16Tag, OutTag, 1, MOM>, grid, block, a, stream);
+      case 2: *name = "combine_warp<bf16,2>"; return launch(combine_warp_kernel<BF16Tag, OutTag, 2, MOM>, grid, block, a, stream);
+      case 4: *name = "combine_warp<bf16,4>"; return launch(combine_warp_kernel<BF16Tag, OutTag, 4, MOM>, grid, block, a, stream);
+      case 8: *name = "combine_warp<bf16,8>"; return launch(combine_warp_kernel<BF16Tag, OutTag, 8, MOM>, grid, block, a, stream);
+      case 16: *name = "combine_warp<bf16,16>"; return launch(combine_warp_kernel<BF16Tag, OutTag, 16, MOM>, grid, block, a, stream);
+      default: return static_cast<int>(cudaErrorInvalidValue);
+    }
+  }
+  const int n = a.tile_list ? a.ntile_list : a.ntiles;
+  const dim3 grid((n + a.combine_tiles - 1) / a.combine_tiles, a.G), block(kThreads);
   switch (a.Kg) {
     case 1: *name = "combine<bf16,1>"; return launch(combine_kernel<BF16Tag, OutTag, 1, MOM>, grid, block, a, stream);
     case 2: *name = "combine<bf16,2>"; return launch(combine_kernel<BF16Tag, OutTag, 2, MOM>, grid, block, a, stream);
@@ -45,13 +57,13 @@ static int combine_bf16_k(const StageArgs& a, void* stream, const char** name) {
   }
 }
 
-int launch_combine_bf16in(const StageArgs& a, int out_dtype, int momentum, void* stream,
+int launch_combine_bf16in(const StageArgs& a, int out_dtype, int momentum, int warp, void* stream,
                           const char** name) {
   if (out_dtype == kF32)
-    return momentum ? combine_bf16_k<F32Tag, true>(a, stream, name)
-                    : combine_bf16_k<F32Tag, false>(a, stream, name);
-  return momentum ? combine_bf16_k<BF16Tag, true>(a, stream, name)
-                  : combine_bf16_k<BF16Tag, false>(a, stream, name);
+    return momentum ? combine_bf16_k<F32Tag, true>(a, warp, stream, name)
+                    : combine_bf16_k<F32Tag, false>(a, warp, stream, name);
+  return momentum ? combine_bf16_k<BF16Tag, true>(a, warp, stream, name)
+                  : combine_bf16_k<BF16Tag, false>(a, warp, stream, name);
 }
 
 }  // namespace adasum

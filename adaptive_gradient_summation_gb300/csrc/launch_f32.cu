@@ -59,7 +59,8 @@ int launch_gram_warp(const StageArgs& a, int in_dtype, void* stream, const char*
 }
 
 int launch_reduce_chunks(const StageArgs& a, void* stream, const char** name) {
-  const dim3 grid(a.nchunks, a.G), block(kThreads);
+  const int per = a.nchunks >= 16 * a.num_sms ? kChunksPerCta : 1;
+  const dim3 grid((a.nchunks + per - 1) / per, a.G), block(kThreads);
   switch (a.Kg) {
     case 2: *name = "reduce_chunks<2>"; return launch(reduce_chunks_kernel<2>, grid, block, a, stream);
     case 4: *name = "reduce_chunks<4>"; return launch(reduce_chunks_kernel<4>, grid, block, a, stream);
@@ -93,8 +94,20 @@ int launch_coef(const StageArgs& a, void* stream, const char** name) {
 }
 
 template <typename OutTag, bool MOM>
-static int combine_f32_k(const StageArgs& a, void* stream, const char** name) {
-  const dim3 grid((a.ntiles + a.combine_tiles - 1) / a.combine_tiles, a.G), block(kThreads);
+static int combine_f32_k(const StageArgs& a, int warp, void* stream, const char** name) {
+  if (warp) {  // short tiles, one warp each
+    const dim3 grid((a.nsmall + kWarps - 1) / kWarps, a.G), block(kThreads);
+    switch (a.Kg) {
+      case 1: *name = "combine_warp<f32,1>"; return launch(combine_warp_kernel<F32Tag, OutTag, 1, MOM>, grid, block, a, stream);
+      case 2: *name = "combine_warp<f32,2>"; return launch(combine_warp_kernel<F32Tag, OutTag, 2, MOM>, grid, block, a, stream);
+      case 4: *name = "combine_warp<f32,4>"; return launch(combine_warp_kernel<F32Tag, OutTag, 4, MOM>, grid, block, a, stream);
+      case 8: *name = "combine_warp<f32,8>"; return launch(combine_warp_kernel<F32Tag, OutTag, 8, MOM>, grid, block, a, stream);
+      case 16: *name = "combine_warp<f32,16>"; return launch(combine_warp_kernel<F32Tag, OutTag, 16, MOM>, grid, block, a, stream);
+      default: return static_cast<int>(cudaErrorInvalidValue);
+    }
+  }
+  const int n = a.tile_list ? a.ntile_list : a.ntiles;
+  const dim3 grid((n + a.combine_tiles - 1) / a.combine_tiles, a.G), block(kThreads);
   switch (a.Kg) {
     case 1: *name = "combine<f32,1>"; return launch(combine_kernel<F32Tag, OutTag, 1, MOM>, grid, block, a, stream);
     case 2: *name = "combine<f32,2>"; return launch(combine_kernel<F32Tag, OutTag, 2, MOM>, grid, block, a, stream);
@@ -105,13 +118,13 @@ static int combine_f32_k(const StageArgs& a, void* stream, const char** name) {
   }
 }
 
-int launch_combine_f32in(const StageArgs& a, int out_dtype, int momentum, void* stream,
+int launch_combine_f32in(const StageArgs& a, int out_dtype, int momentum, int warp, void* stream,
                          const char** name) {
   if (out_dtype == kF32)
-    return momentum ? combine_f32_k<F32Tag, true>(a, stream, name)
-                    : combine_f32_k<F32Tag, false>(a, stream, name);
-  return momentum ? combine_f32_k<BF16Tag, true>(a, stream, name)
-                  : combine_f32_k<BF16Tag, false>(a, stream, name);
+    return momentum ? combine_f32_k<F32Tag, true>(a, warp, stream, name)
+                    : combine_f32_k<F32Tag, false>(a, warp, stream, name);
+  return momentum ? combine_f32_k<BF16Tag, true>(a, warp, stream, name)
+                  : combine_f32_k<BF16Tag, false>(a, warp, stream, name);
 }
 
 }  // namespace adasum
