@@ -862,7 +862,7 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
     a.segs = plan->d_segs;
     a.chunks = plan->d_chunks;
     a.partials = reinterpret_cast<float*>(base + o_part);
-    a.chunk_sums = reinterpret_cast<double*>(base + o_chunk);
+    a.chunk_sums = reinterpret_cast<float2*>(base + o_chunk);
     a.tile_nz = reinterpret_cast<uint32_t*>(base + o_tnz);
     a.chunk_nz = reinterpret_cast<uint32_t*>(base + o_cnz);
     a.coef = reinterpret_cast<float*>(base + o_coef);

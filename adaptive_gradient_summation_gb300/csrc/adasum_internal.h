@@ -82,7 +82,8 @@ struct StageArgs {
   const SegDesc* segs;
   const ChunkDesc* chunks;
   float* partials;   // [G][ntiles][E] Gram partials, E = Kg(Kg+1)/2 (upper triangle)
-  double* chunk_sums; // [G][nchunks][E] compensated sums of the partials of each chunk
+  float2* chunk_sums; // [G][nchunks][E] compensated sums of the partials of each chunk, as
+                      //   double-float (hi, lo) pairs
   // Range check of the fp32 pass (kDiagLoPerPos, kDiagHi): bit k set when worker k has a
   // nonzero value in the tile / chunk (-0 counts as zero).
   uint32_t* tile_nz;   // [G][ntiles]

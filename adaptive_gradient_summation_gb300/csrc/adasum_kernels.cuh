@@ -717,7 +717,7 @@ __device__ __forceinline__ void gram_tile(const StageArgs& a, int tile_id, int q
 constexpr int kChunksPerCta = 8;
 
 // Entry e of chunk c (group q): the compensated sum of its tiles' partials, in tile
-// order, as an fp64 value.
+// order, stored as the double-float pair sum - comp (an exact TwoSum of the two).
 template <int KG>
 __device__ __forceinline__ void reduce_chunk_entry(const StageArgs& a, const ChunkDesc& ch, int c, int e, int q) {
   constexpr int E = tri_count(KG);
@@ -729,7 +729,9 @@ __device__ __forceinline__ void reduce_chunk_entry(const StageArgs& a, const Chu
   float sum = 0.f, comp = 0.f;
 #pragma unroll
   for (int t = 0; t < kChunkTiles; ++t) kahan_add(sum, comp, v[t]);
-  a.chunk_sums[(static_cast<size_t>(q) * a.nchunks + c) * E + e] = static_cast<double>(sum) - static_cast<double>(comp);
+  const float s = __fsub_rn(sum, comp), bb = __fsub_rn(s, sum);
+  const float err = __fadd_rn(__fsub_rn(sum, __fsub_rn(s, bb)), __fsub_rn(-comp, bb));
+  a.chunk_sums[(static_cast<size_t>(q) * a.nchunks + c) * E + e] = make_float2(s, err);
 }
 
 __device__ __forceinline__ bool chunk_ok(const StageArgs& a, int c, ChunkDesc& ch) {
@@ -1343,31 +1345,35 @@ struct CoefScratch {
   float tree[tree_scratch_floats(KG)];
 };
 
-// The Gram matrix of (segment, group) from its chunk sums (fp64, in chunk order: the
-// loads are issued eight at a time and added in order) and the input errors, by threads
-// first, first + step, ...
+// The Gram matrix of (segment, group) from its chunk sums (double-float, added in chunk
+// order; the loads are issued eight at a time) and the input errors, by threads first,
+// first + step, ...  The fp64 copy G is filled only for the chain's coefficient step and
+// the orthogonality metric's trace.
 template <int KG>
 __device__ __forceinline__ void coef_gather(const StageArgs& a, const SegDesc& sd, int seg, int q,
                                             CoefScratch<KG>& sh, int first, int step) {
   constexpr int E = tri_count(KG);
   constexpr int U = 8;
+  const bool want_fp64 = a.mode == kModeChain || a.diag_sum != nullptr;
   for (int e = first; e < E; e += step) {
-    const double* p = a.chunk_sums + (static_cast<size_t>(q) * a.nchunks + sd.first_chunk) * E + e;
-    double sum = 0.0;
+    const float2* p = a.chunk_sums + (static_cast<size_t>(q) * a.nchunks + sd.first_chunk) * E + e;
+    df32 sum = {0.f, 0.f};
     int t = 0;
     for (; t + U <= sd.nchunks; t += U) {
-      double v[U];
+      float2 v[U];
 #pragma unroll
       for (int u = 0; u < U; ++u) v[u] = __ldcg(p + static_cast<size_t>(t + u) * E);
 #pragma unroll
-      for (int u = 0; u < U; ++u) sum += v[u];
+      for (int u = 0; u < U; ++u) sum = df_add(sum, df32{v[u].x, v[u].y});
     }
-    for (; t < sd.nchunks; ++t) sum += __ldcg(p + static_cast<size_t>(t) * E);
+    for (; t < sd.nchunks; ++t) {
+      const float2 v = __ldcg(p + static_cast<size_t>(t) * E);
+      sum = df_add(sum, df32{v.x, v.y});
+    }
     int i, j;
     tri_unpack(KG, e, i, j);
-    sh.G[i][j] = sum;
-    sh.G[j][i] = sum;
-    sh.Gd[i][j] = sh.Gd[j][i] = df_from_double(sum);
+    sh.Gd[i][j] = sh.Gd[j][i] = sum;
+    if (want_fp64) sh.G[i][j] = sh.G[j][i] = df_to_double(sum);
   }
   for (int k = first; k < KG; k += step)
     sh.eps[k] = a.in_relerr ? static_cast<double>(a.in_relerr[static_cast<size_t>(q * KG + k) * a.nsegs + seg]) : 0.0;
@@ -1411,8 +1417,9 @@ __device__ __forceinline__ void coef_tree(const StageArgs& a, const SegDesc& sd,
   // false: it propagates)
   bool out_of_range = false;
   if (lane < KG && ((seg_nz >> lane) & 1u)) {
-    const double d = sh.G[lane][lane];
-    out_of_range = d < static_cast<double>(sd.len) * kDiagLoPerPos || d > kDiagHi;
+    const float d = sh.Gd[lane][lane].hi;  // (fp32 holds both bounds exactly)
+    out_of_range = d < static_cast<float>(sd.len) * static_cast<float>(kDiagLoPerPos) ||
+                   d > static_cast<float>(kDiagHi);
   }
   out_of_range = __any_sync(0xFFFFFFFFu, out_of_range);
   if (lane == 0) {
