@@ -132,7 +132,8 @@ struct Plan {
   int* d_tiny = nullptr;
   int ncoef = 0;
   int* d_coef_list = nullptr;
-  // three-kernel route: tiles of at most kSmallTile positions take the warp Gram kernel
+  // three-kernel route: short tiles (kSmallTileF32, kSmallTileBF16, kSmallTileSimt) take
+  // the warp Gram kernel
   // (lists empty when there are none)
   bool warp_tiles = true;
   int nbig = 0, nsmall = 0;
@@ -419,8 +420,9 @@ adasum_status_t get_plan(Workspace& ws, const int64_t* offs, int L, int Kg0, int
   p.ncoef = static_cast<int>(coef_list.size());
   std::vector<int> big, small_tiles;
   if (warp_tiles) {
+    const int small_tile = Kg0 < kMaxGroup ? kSmallTileSimt : (dtype == kF32 ? kSmallTileF32 : kSmallTileBF16);
     for (int t = 0; t < static_cast<int>(tiles.size()); ++t)
-      (tiles[t].len <= kSmallTile ? small_tiles : big).push_back(t);
+      (tiles[t].len <= small_tile ? small_tiles : big).push_back(t);
     // a few small tiles cost nothing inside the CTA launch; a separate warp launch pays
     // its own latency, worth it only when small tiles are numerous
     if (small_tiles.size() < 2 * static_cast<size_t>(num_sms)) {

@@ -62,8 +62,15 @@ struct ChunkDesc {
   int32_t ntiles;
 };
 constexpr int kChunkTiles = 32;
-// Tiles of at most this many positions get their Gram partial from one warp.
-constexpr int kSmallTile = 1024;
+// Tiles of at most this many positions get their Gram partial, and with groups of 8 or
+// more workers their combine, from one warp: 16-worker groups (the tensor-core warp
+// Gram) with fp32 / bf16 inputs, and smaller groups (the SIMT warp Gram).  Measured on a
+// layout of 10,000 segments of 1..4096 positions: 512 and 2048 against 1024 took fp32
+// K = 64 from 0.900 to 0.889 ms and bf16 K = 64 from 0.876 to 0.864 ms; 2048 made bf16
+// K = 8 slower (0.124 -> 0.135 ms).
+constexpr int kSmallTileF32 = 512;
+constexpr int kSmallTileBF16 = 2048;
+constexpr int kSmallTileSimt = 1024;
 
 // Arguments of one stage: G independent groups of Kg workers each, over the same
 // segments and tiles.  Group q reads in[q*Kg + k], k < Kg, and writes out[q].

@@ -1637,9 +1637,9 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const StageArgs a) {
   }
 }
 
-// Short tiles (a.small_list, at most kSmallTile positions), one warp each: a CTA per
-// tile would leave most of its threads without a vector and run its tiles' coefficient
-// loads one after another.
+// Short tiles (a.small_list: kSmallTileF32, kSmallTileBF16 or kSmallTileSimt positions at
+// most), one warp each: a CTA per tile would leave most of its threads without a vector and run its
+// tiles' coefficient loads one after another.
 template <typename InTag, typename OutTag, int KG, bool MOM>
 __global__ void __launch_bounds__(kThreads) combine_warp_kernel(const StageArgs a) {
   pdl_enter();
