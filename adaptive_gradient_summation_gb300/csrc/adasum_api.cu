@@ -117,6 +117,10 @@ struct Plan {
   TileDesc* d_tiles = nullptr;
   SegDesc* d_segs = nullptr;
   ChunkDesc* d_chunks = nullptr;
+  // the chunks of segments with more than one (the chunk-sum kernel's work; a segment of
+  // one chunk is summed by the coefficient kernel from its tile partials)
+  int nmulti = 0;
+  int* d_multi = nullptr;
   // small segments: held on chip (grouped by cluster size 1, 2, 4, 8, 16) or, up to
   // kTinyDirect positions, on the warp kernel; neither gets tiles.  The coefficient kernel
   // then runs over the list of the remaining (tiled) segments.
@@ -254,6 +258,7 @@ void free_plan(Plan& p) {
   if (p.d_tiles) cudaFree(p.d_tiles);
   if (p.d_segs) cudaFree(p.d_segs);
   if (p.d_chunks) cudaFree(p.d_chunks);
+  if (p.d_multi) cudaFree(p.d_multi);
   if (p.d_onchip) cudaFree(p.d_onchip);
   if (p.d_tiny) cudaFree(p.d_tiny);
   if (p.d_coef_list) cudaFree(p.d_coef_list);
@@ -267,6 +272,7 @@ void free_plan(Plan& p) {
   p.d_tiles = nullptr;
   p.d_segs = nullptr;
   p.d_chunks = nullptr;
+  p.d_multi = nullptr;
 }
 
 // Input bytes per tile of the tiled passes.
@@ -447,6 +453,14 @@ adasum_status_t get_plan(Workspace& ws, const int64_t* offs, int L, int Kg0, int
   if (!st && any_small) st = upload(&p.d_coef_list, coef_list);
   if (!st) st = upload(&p.d_segs, segs);
   if (!st) st = upload(&p.d_chunks, chunks);
+  {
+    std::vector<int> multi;
+    for (int s2 = 0; s2 < L; ++s2)
+      if (segs[s2].nchunks > 1)
+        for (int c = 0; c < segs[s2].nchunks; ++c) multi.push_back(segs[s2].first_chunk + c);
+    p.nmulti = static_cast<int>(multi.size());
+    if (!st && !multi.empty()) st = upload(&p.d_multi, multi);
+  }
   if (st) {
     free_plan(p);
     return st;
@@ -550,10 +564,11 @@ adasum_status_t run_stage(StageArgs& a, int in_dtype, int out_dtype, int momentu
           }, bytes[1]))
         return st;
     }
-    if (adasum_status_t st = launch_one(stream, [&](const char** n) {
-          return launch_reduce_chunks(a, stream, n);
-        }))
-      return st;
+    if (a.nmulti > 0)
+      if (adasum_status_t st = launch_one(stream, [&](const char** n) {
+            return launch_reduce_chunks(a, stream, n);
+          }))
+        return st;
     if (adasum_status_t st = launch_one(stream, [&](const char** n) { return launch_coef(a, stream, n); }))
       return st;
   }
@@ -863,6 +878,8 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
     a.tiles = plan->d_tiles;
     a.segs = plan->d_segs;
     a.chunks = plan->d_chunks;
+    a.multi_chunks = plan->d_multi;
+    a.nmulti = plan->nmulti;
     a.partials = reinterpret_cast<float*>(base + o_part);
     a.chunk_sums = reinterpret_cast<float2*>(base + o_chunk);
     a.tile_nz = reinterpret_cast<uint32_t*>(base + o_tnz);

@@ -90,11 +90,13 @@ struct StageArgs {
   const ChunkDesc* chunks;
   float* partials;   // [G][ntiles][E] Gram partials, E = Kg(Kg+1)/2 (upper triangle)
   float2* chunk_sums; // [G][nchunks][E] compensated sums of the partials of each chunk, as
-                      //   double-float (hi, lo) pairs
+                      //   double-float (hi, lo) pairs (chunks of multi-chunk segments only)
+  const int* multi_chunks;  // the chunks of segments with more than one chunk
+  int nmulti;
   // Range check of the fp32 pass (kDiagLoPerPos, kDiagHi): bit k set when worker k has a
   // nonzero value in the tile / chunk (-0 counts as zero).
   uint32_t* tile_nz;   // [G][ntiles]
-  uint32_t* chunk_nz;  // [G][nchunks]
+  uint32_t* chunk_nz;  // [G][nchunks] (chunks of multi-chunk segments only)
   float* coef;       // [G][nsegs][Kg] tree coefficients
   // Fused heavy-ball step (final stage of adasum_reduce_momentum_sgd only).
   float* master_w;

@@ -716,10 +716,10 @@ __device__ __forceinline__ void gram_tile(const StageArgs& a, int tile_id, int q
 // threads idle.  With few chunks, one per CTA spreads them over the SMs.
 constexpr int kChunksPerCta = 8;
 
-// Entry e of chunk c (group q): the compensated sum of its tiles' partials, in tile
-// order, stored as the double-float pair sum - comp (an exact TwoSum of the two).
+// Entry e of a chunk (group q): the compensated sum of its tiles' partials, in tile
+// order, as the double-float pair sum - comp (an exact TwoSum of the two).
 template <int KG>
-__device__ __forceinline__ void reduce_chunk_entry(const StageArgs& a, const ChunkDesc& ch, int c, int e, int q) {
+__device__ __forceinline__ float2 chunk_entry(const StageArgs& a, const ChunkDesc& ch, int e, int q) {
   constexpr int E = tri_count(KG);
   const float* p = a.partials + (static_cast<size_t>(q) * a.ntiles + ch.first_tile) * E + e;
   float v[kChunkTiles];
@@ -731,7 +731,15 @@ __device__ __forceinline__ void reduce_chunk_entry(const StageArgs& a, const Chu
   for (int t = 0; t < kChunkTiles; ++t) kahan_add(sum, comp, v[t]);
   const float s = __fsub_rn(sum, comp), bb = __fsub_rn(s, sum);
   const float err = __fadd_rn(__fsub_rn(sum, __fsub_rn(s, bb)), __fsub_rn(-comp, bb));
-  a.chunk_sums[(static_cast<size_t>(q) * a.nchunks + c) * E + e] = make_float2(s, err);
+  return make_float2(s, err);
+}
+
+// The OR of a chunk's per-tile nonzero words (range check), group q.
+__device__ __forceinline__ uint32_t chunk_nonzero(const StageArgs& a, const ChunkDesc& ch, int q) {
+  const uint32_t* p = a.tile_nz + static_cast<size_t>(q) * a.ntiles + ch.first_tile;
+  uint32_t m = 0u;
+  for (int t = 0; t < ch.ntiles; ++t) m |= __ldcg(p + t);
+  return m;
 }
 
 __device__ __forceinline__ bool chunk_ok(const StageArgs& a, int c, ChunkDesc& ch) {
@@ -740,31 +748,30 @@ __device__ __forceinline__ bool chunk_ok(const StageArgs& a, int c, ChunkDesc& c
                                    ch.ntiles <= kChunkTiles && ch.first_tile + ch.ntiles <= a.ntiles);
 }
 
-// CTA b: chunks b * per ... (per = the chunks over the grid: 1 or kChunksPerCta), every
-// (chunk, entry) pair to one thread, and the OR of each chunk's per-tile nonzero words
-// (range check).
+// The chunks of multi-chunk segments (a.multi_chunks): CTA b takes entries b * per ...
+// (per = the entries over the grid: 1 or kChunksPerCta), every (chunk, entry) pair to one
+// thread, and the OR of each chunk's per-tile nonzero words (range check).
 template <int KG>
 __global__ void __launch_bounds__(kThreads) reduce_chunks_kernel(const StageArgs a) {
   pdl_enter();
   constexpr int E = tri_count(KG);
   const int q = blockIdx.y;
-  const int per = min(kChunksPerCta, (a.nchunks + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x));
-  const int c0 = blockIdx.x * per;
+  const int n = a.nmulti;
+  const int per = min(kChunksPerCta, (n + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x));
+  const int i0 = blockIdx.x * per;
   for (int idx = threadIdx.x; idx < per * E; idx += kThreads) {
-    const int c = c0 + idx / E, e = idx % E;
+    const int i = i0 + idx / E, e = idx % E;
+    if (i >= n) continue;
+    const int c = a.multi_chunks[i];
     ChunkDesc ch;
-    if (c >= a.nchunks || !chunk_ok(a, c, ch)) continue;
-    reduce_chunk_entry<KG>(a, ch, c, e, q);
+    if (!chunk_ok(a, c, ch)) continue;
+    a.chunk_sums[(static_cast<size_t>(q) * a.nchunks + c) * E + e] = chunk_entry<KG>(a, ch, e, q);
   }
   if (static_cast<int>(threadIdx.x) < per) {
-    const int c = c0 + threadIdx.x;
+    const int i = i0 + threadIdx.x;
     ChunkDesc ch;
-    if (c < a.nchunks && chunk_ok(a, c, ch)) {
-      const uint32_t* p = a.tile_nz + static_cast<size_t>(q) * a.ntiles + ch.first_tile;
-      uint32_t m = 0u;
-      for (int t = 0; t < ch.ntiles; ++t) m |= __ldcg(p + t);
-      a.chunk_nz[static_cast<size_t>(q) * a.nchunks + c] = m;
-    }
+    if (i < n && chunk_ok(a, a.multi_chunks[i], ch))
+      a.chunk_nz[static_cast<size_t>(q) * a.nchunks + a.multi_chunks[i]] = chunk_nonzero(a, ch, q);
   }
 }
 
@@ -1355,10 +1362,17 @@ __device__ __forceinline__ void coef_gather(const StageArgs& a, const SegDesc& s
   constexpr int E = tri_count(KG);
   constexpr int U = 8;
   const bool want_fp64 = a.mode == kModeChain || a.diag_sum != nullptr;
+  ChunkDesc one = {};
+  const bool single = sd.nchunks == 1 && chunk_ok(a, sd.first_chunk, one);
   for (int e = first; e < E; e += step) {
     const float2* p = a.chunk_sums + (static_cast<size_t>(q) * a.nchunks + sd.first_chunk) * E + e;
     df32 sum = {0.f, 0.f};
     int t = 0;
+    if (single) {  // the chunk-sum kernel left this segment's one chunk to this kernel
+      const float2 v = chunk_entry<KG>(a, one, e, q);
+      sum = df_add(sum, df32{v.x, v.y});
+      t = 1;
+    }
     for (; t + U <= sd.nchunks; t += U) {
       float2 v[U];
 #pragma unroll
@@ -1388,11 +1402,14 @@ __device__ __forceinline__ void coef_tree(const StageArgs& a, const SegDesc& sd,
   const int lane = threadIdx.x & 31;
   // the workers with a nonzero value in the segment
   uint32_t seg_nz = 0u;
-  {
+  ChunkDesc one;
+  if (sd.nchunks == 1 && chunk_ok(a, sd.first_chunk, one)) {
+    if (lane == 0) seg_nz = chunk_nonzero(a, one, q);
+  } else {
     const uint32_t* p = a.chunk_nz + static_cast<size_t>(q) * a.nchunks + sd.first_chunk;
     for (int t = lane; t < sd.nchunks; t += 32) seg_nz |= __ldcg(p + t);
-    seg_nz = warp_or_u32(seg_nz);
   }
+  seg_nz = warp_or_u32(seg_nz);
   double c = 0.0, P = 0.0;
   bool ill = false;
   double rel;

@@ -59,8 +59,8 @@ int launch_gram_warp(const StageArgs& a, int in_dtype, void* stream, const char*
 }
 
 int launch_reduce_chunks(const StageArgs& a, void* stream, const char** name) {
-  const int per = a.nchunks >= 16 * a.num_sms ? kChunksPerCta : 1;
-  const dim3 grid((a.nchunks + per - 1) / per, a.G), block(kThreads);
+  const int per = a.nmulti >= 16 * a.num_sms ? kChunksPerCta : 1;
+  const dim3 grid((a.nmulti + per - 1) / per, a.G), block(kThreads);
   switch (a.Kg) {
     case 2: *name = "reduce_chunks<2>"; return launch(reduce_chunks_kernel<2>, grid, block, a, stream);
     case 4: *name = "reduce_chunks<4>"; return launch(reduce_chunks_kernel<4>, grid, block, a, stream);
