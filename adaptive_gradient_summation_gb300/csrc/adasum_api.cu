@@ -981,10 +981,10 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
     }
   }
 
-  // Tiny segments: the warp kernel, on side stream 0, forked after the on-chip launches.
-  // The launch is a wave of latency-bound warps, so it runs concurrently with the tiled
-  // passes (bandwidth-bound) instead of ahead of them; forked earlier, its CTAs held the
-  // registers the on-chip CTAs need.
+  // Tiny segments: the warp kernel, on side stream 0.  The launch is a wave of
+  // compute-bound warps, so it runs beside the tiled passes (bandwidth-bound) instead of
+  // ahead of them.  (It is forked after the on-chip fast pass when the test build runs
+  // that: forked before, its CTAs held registers the on-chip CTAs need.)
   if (plan->tiny_count > 0) {
     if (adasum_status_t st = joins.fork(ws.side[0], 0)) return st;
     TinyArgs ta;

@@ -580,8 +580,8 @@ __device__ __forceinline__ bool tiny_entry(const TinyArgs& a, int e, SegDesc& sd
 // count8, count16, the rest).  Every value is loaded at once into registers, read once,
 // prescaled by the power of two of its segment's largest |value|, and the tree runs from
 // registers (its pairs (2i, 2i+1) at every level).  Sums over a group equal the sums over
-// the whole warp of the one-segment layout bit for bit: the other lanes hold zeros, and
-// adding a zero is exact.
+// the whole warp of the one-segment layout: the other lanes hold zeros, and adding a zero
+// is exact (it can only turn an exact -0 into +0).
 template <typename InTag, int KP>
 __global__ void __launch_bounds__(kOnchipThreads) tiny_reg_kernel(const TinyArgs a) {
   pdl_enter();
