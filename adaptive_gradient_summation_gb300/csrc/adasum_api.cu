@@ -773,14 +773,13 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
   }
 
   // Plain reductions: segments of at most kTinyDirect positions go to the warp kernel,
-  // small ones (up to 64 workers) to the on-chip kernel, the rest to the tiles.
-  // Small segments take the tiled route; the on-chip kernel recomputes the flagged ones
-  // that fit a cluster.  Its fp32 fast pass (every level of a small segment on chip in one
-  // pass) measured slower than the tiled route at every worker count and dtype on the
-  // 10,000-segment layout, so the product library does not use it; the test build turns
-  // it on with ADASUM_ONCHIP_FAST=1 (segments that fit 2 CTAs, or ADASUM_ONCHIP_MAX_CLUSTER,
-  // when they are numerous) or ADASUM_ONCHIP=force (every segment it holds, whatever
-  // their number, unless ADASUM_ONCHIP_FAST=0).
+  // the rest to the tiles; the on-chip kernel recomputes the flagged ones that fit a
+  // cluster.  The on-chip kernel's fp32 fast pass (every level of a small segment on chip
+  // in one pass) measured slower than the tiled route at every worker count and dtype on
+  // the 10,000-segment layout, so the product library does not use it; the test build
+  // turns it on with ADASUM_ONCHIP_FAST=1 (segments that fit 2 CTAs, or
+  // ADASUM_ONCHIP_MAX_CLUSTER, when they are numerous) or ADASUM_ONCHIP=force (every
+  // segment it holds, whatever their number, unless ADASUM_ONCHIP_FAST=0).
   // (ADASUM_TINY=0 and ADASUM_ONCHIP=0 switch the warp kernel and the on-chip kernel off,
   // for comparisons; ADASUM_WARP_GRAM=0 keeps every tile on the CTA Gram kernels.)
   const bool plain = !mom && !chain && ortho == nullptr && K >= 2;
