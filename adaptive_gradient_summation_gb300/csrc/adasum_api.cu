@@ -277,6 +277,19 @@ void free_plan(Plan& p) {
 
 // Input bytes per tile of the tiled passes.
 constexpr int64_t kTileBytes = int64_t(256) << 10;
+// When segments that fit one tile but are longer than this many positions hold at least
+// a quarter of the tiled positions, each of them is cut into tiles of this many
+// positions on the 32-position grid, all of them short tiles (one warp for the Gram and,
+// with 8 or more workers per group, for the combine).  A whole-CTA tile of a few
+// thousand positions leaves most of its warps waiting on the slowest one and on the
+// block reduction.  Measured on a layout of 10,000 segments of 1..4096 positions: fp32
+// K = 16 took 0.227 ms uncut, 0.193 cut at 512 positions (0.198 at 256); bf16 K = 16
+// 0.237 ms uncut, 0.187 cut at 1024 (0.193 at 512); K = 64 0.873 -> 0.835 ms (fp32) and
+// 0.841 -> 0.766 ms (bf16).  On the BERT-Large set such segments hold almost none of the
+// positions, and cutting them measured slower (3.340 -> 3.362 ms): their 318 short tiles
+// then take a warp launch of their own.
+constexpr int64_t kSplitTileF32 = 512;
+constexpr int64_t kSplitTileBF16 = 1024;
 
 int64_t tile_positions(int Kg, int dtype, int64_t N, int num_sms) {
   // About kTileBytes of input per tile, but enough tiles to give every SM a few.
@@ -342,6 +355,18 @@ adasum_status_t get_plan(Workspace& ws, const int64_t* offs, int L, int Kg0, int
     }
     if (!onchip_force && eligible < 4 * static_cast<int64_t>(num_sms)) onchip_vecs = 0;
   }
+  // whether segments that fit one tile are cut into short tiles (kSplitTileF32)
+  const int64_t Ts = dtype == kF32 ? kSplitTileF32 : kSplitTileBF16;
+  bool split = false;
+  if (warp_tiles) {
+    int64_t tiled = 0, cut = 0;
+    for (int s = 0; s < L; ++s) {
+      const int64_t n = offs[s + 1] - offs[s];
+      if (n > kTinyDirect) tiled += n;
+      if (n > Ts && n <= T) cut += n;
+    }
+    split = cut > 0 && 4 * cut >= tiled;
+  }
   for (int s = 0; s < L; ++s) {
     const int64_t lo = offs[s], hi = offs[s + 1];
     segs[s].start = lo;
@@ -372,8 +397,9 @@ adasum_status_t get_plan(Workspace& ws, const int64_t* offs, int L, int Kg0, int
     }
     if (hi > lo && !small) {
       const int64_t base = lo / 32 * 32;
-      for (int64_t b = base; b < hi; b += T) {
-        const int64_t t0 = std::max(lo, b), t1 = std::min(hi, b + T);
+      const int64_t step = (split && hi - lo <= T && hi - lo > Ts) ? Ts : T;
+      for (int64_t b = base; b < hi; b += step) {
+        const int64_t t0 = std::max(lo, b), t1 = std::min(hi, b + step);
         if (t1 <= t0) continue;
         tiles.push_back(TileDesc{t0, static_cast<int32_t>(t1 - t0), s});
       }

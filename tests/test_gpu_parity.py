@@ -49,6 +49,24 @@ def test_workload_shapes_small(native, name, shrink):
     check_against_oracle(wl.grads, wl.seg_offsets, out)
 
 
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("K", [4, 8, 16])
+def test_segments_cut_into_short_tiles(native, K, dtype):
+    """Segments that fit one tile hold nearly every position here (1,200 of 513..4,096
+    positions, 2.8M in all, so a tile spans at least 4,096 positions), and the planner
+    cuts each of them into short tiles of 512 (fp32) or 1,024 (bf16) positions: the warp
+    Gram kernels (SIMT for groups of 4 and 8, tensor cores for 16), the warp combine for
+    groups of 8 and more, the CTA combine over every tile for groups of 4."""
+    rng = np.random.default_rng(55 + K)
+    lengths = [int(x) for x in rng.integers(513, 4097, size=1200)]
+    lengths[7:7] = [0, 1, 31, 33, 512]
+    offs = workloads.offsets_from_numels(lengths)
+    grads = rand_grads(K, int(offs[-1]), dtype, seed=55 + K)
+    out = ags.reduce(grads, offs)
+    torch.cuda.synchronize()
+    check_against_oracle(grads, offs, out)
+
+
 @pytest.mark.parametrize("K", [16, 32])
 def test_small_segment_layout_bf16(native, K):
     """The 10,000-segment layout (a quarter of each length) in bf16 with 16-worker groups:
