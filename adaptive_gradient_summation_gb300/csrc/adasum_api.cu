@@ -934,7 +934,7 @@ adasum_status_t reduce_impl(const void* const* grads_in, int K, const int64_t* o
     if (plan->nsmall > 0) {
       a.tile_list = plan->d_big;
       a.ntile_list = plan->nbig;
-      a.small_list = plan->d_small;
+      a.small_list = plan->nbig > 0 ? plan->d_small : nullptr;  // (null: every tile, in order)
       a.nsmall = plan->nsmall;
     }
     a.mode = chain ? kModeChain : kModeTree;

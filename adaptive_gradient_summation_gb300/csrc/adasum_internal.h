@@ -113,7 +113,8 @@ struct StageArgs {
   int nseg_list;
   const int* tile_list;       // Gram CTA kernels: the tiles to run (null: all ntiles)
   int ntile_list;
-  const int* small_list;      // small tiles, one warp each (gram_warp_kernel)
+  const int* small_list;      // small tiles, one warp each (gram_warp_kernel); null when
+                              // every tile is small (entry i is then tile i)
   int nsmall;
   int combine_tiles;          // consecutive tiles per combine CTA (>= 1; up to 4 while the
                               //   grid keeps 16 CTAs per SM)

@@ -292,7 +292,7 @@ __global__ void __launch_bounds__(kThreads) gram_warp_kernel(const StageArgs a) 
   const int w = blockIdx.x * kWarps + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (w >= a.nsmall) return;  // whole warps only
   const int q = blockIdx.y;
-  const int tile_id = a.small_list[w];
+  const int tile_id = a.small_list ? a.small_list[w] : w;
   float acc[E];
   uint32_t nz;
   if (!tile_ok(a, tile_id, a.tiles[tile_id])) return;  // (uniform over the warp)
@@ -468,6 +468,49 @@ __device__ __forceinline__ void split_bf16x3(float x0, float x1, uint32_t& h, ui
   l = pack_bf16x2(r0 - bf16_lo(m), r1 - bf16_hi(m));
 }
 
+// One 32-position chunk of the fp32 tensor-core Gram: lane (g, t) holds positions
+// [8t, 8t+8) of workers g (rg) and g + 8 (rh) as two 16-byte vectors each.  Every value
+// is split into three bf16 parts (split_bf16x3), and d0 (columns g) and d1 (columns
+// g + 8) accumulate R = h.h + m.m + h.(2m) + h.(2l) (see gram_chunks_mma_f32); org and
+// orh collect the raw bits (range check).
+__device__ __forceinline__ void gram_mma_f32_chunk(const uint4 (&rg)[2], const uint4 (&rh)[2], float (&d0)[4],
+                                                   float (&d1)[4], uint32_t& org, uint32_t& orh) {
+  org |= vec_or(rg[0]) | vec_or(rg[1]);
+  orh |= vec_or(rh[0]) | vec_or(rh[1]);
+  // parts of positions (0,1), (2,3), (4,5), (6,7): registers 0..3 as in gram_tile_mma
+  uint32_t gh[4], gm[4], gl[4], hh[4], hm[4], hl[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const uint4 a4 = rg[k >> 1], b4 = rh[k >> 1];
+    const float ga = __uint_as_float((k & 1) ? a4.z : a4.x), gb = __uint_as_float((k & 1) ? a4.w : a4.y);
+    const float ha = __uint_as_float((k & 1) ? b4.z : b4.x), hb = __uint_as_float((k & 1) ? b4.w : b4.y);
+    split_bf16x3(ga, gb, gh[k], gm[k], gl[k]);
+    split_bf16x3(ha, hb, hh[k], hm[k], hl[k]);
+  }
+  // d += A B for A = rows (g, g+8) of part pa, B = columns g (d0) and g+8 (d1) of part pb
+  auto mmas = [&](const uint32_t (&ag)[4], const uint32_t (&ah)[4], const uint32_t (&bg)[4],
+                  const uint32_t (&bh)[4]) {
+    mma_bf16_16816(d0, ag[0], ah[0], ag[1], ah[1], bg[0], bg[1]);
+    mma_bf16_16816(d0, ag[2], ah[2], ag[3], ah[3], bg[2], bg[3]);
+    mma_bf16_16816(d1, ag[0], ah[0], ag[1], ah[1], bh[0], bh[1]);
+    mma_bf16_16816(d1, ag[2], ah[2], ag[3], ah[3], bh[2], bh[3]);
+  };
+  // R = h.h + m.m + h.(2m) + h.(2l): the mirror sum R_ij + R_ji is twice the six
+  // products' sum (h.m and m.h, h.l and l.h meet there), and its diagonal R_ii is that
+  // sum itself; doubling a bf16 value is exact
+  mmas(gh, hh, gh, hh);
+  mmas(gm, hm, gm, hm);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    gm[k] = bf16x2_twice(gm[k]);
+    hm[k] = bf16x2_twice(hm[k]);
+    gl[k] = bf16x2_twice(gl[k]);
+    hl[k] = bf16x2_twice(hl[k]);
+  }
+  mmas(gh, hh, gm, hm);
+  mmas(gh, hh, gl, hl);
+}
+
 // One warp's share of the Gram of fp32 rows on the tensor cores (16 workers): the
 // 32-position chunks first, first + nw, first + 2 nw, ... of [lo, hi).  Every value is
 // split into three bf16 parts (split_bf16x3) and x.y is taken as the six largest of the
@@ -509,42 +552,7 @@ __device__ __forceinline__ void gram_chunks_mma_f32(const float* xg, const float
       }
     }
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      org |= vec_or(rg[u][0]) | vec_or(rg[u][1]);
-      orh |= vec_or(rh[u][0]) | vec_or(rh[u][1]);
-      // parts of positions (0,1), (2,3), (4,5), (6,7): registers 0..3 as in gram_tile_mma
-      uint32_t gh[4], gm[4], gl[4], hh[4], hm[4], hl[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const uint4 a4 = rg[u][k >> 1], b4 = rh[u][k >> 1];
-        const float ga = __uint_as_float((k & 1) ? a4.z : a4.x), gb = __uint_as_float((k & 1) ? a4.w : a4.y);
-        const float ha = __uint_as_float((k & 1) ? b4.z : b4.x), hb = __uint_as_float((k & 1) ? b4.w : b4.y);
-        split_bf16x3(ga, gb, gh[k], gm[k], gl[k]);
-        split_bf16x3(ha, hb, hh[k], hm[k], hl[k]);
-      }
-      // d += A B for A = rows (g, g+8) of part pa, B = columns g (d0) and g+8 (d1) of part pb
-      auto mmas = [&](const uint32_t (&ag)[4], const uint32_t (&ah)[4], const uint32_t (&bg)[4],
-                      const uint32_t (&bh)[4]) {
-        mma_bf16_16816(d0, ag[0], ah[0], ag[1], ah[1], bg[0], bg[1]);
-        mma_bf16_16816(d0, ag[2], ah[2], ag[3], ah[3], bg[2], bg[3]);
-        mma_bf16_16816(d1, ag[0], ah[0], ag[1], ah[1], bh[0], bh[1]);
-        mma_bf16_16816(d1, ag[2], ah[2], ag[3], ah[3], bh[2], bh[3]);
-      };
-      // R = h.h + m.m + h.(2m) + h.(2l): the mirror sum R_ij + R_ji is twice the six
-      // products' sum (h.m and m.h, h.l and l.h meet there), and its diagonal R_ii is that
-      // sum itself; doubling a bf16 value is exact
-      mmas(gh, hh, gh, hh);
-      mmas(gm, hm, gm, hm);
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        gm[k] = bf16x2_twice(gm[k]);
-        hm[k] = bf16x2_twice(hm[k]);
-        gl[k] = bf16x2_twice(gl[k]);
-        hl[k] = bf16x2_twice(hl[k]);
-      }
-      mmas(gh, hh, gm, hm);
-      mmas(gh, hh, gl, hl);
-    }
+    for (int u = 0; u < U; ++u) gram_mma_f32_chunk(rg[u], rh[u], d0, d1, org, orh);
     if (++pending == kFold) {
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
@@ -560,6 +568,111 @@ __device__ __forceinline__ void gram_chunks_mma_f32(const float* xg, const float
   for (int i = 0; i < 4; ++i) {
     kahan_add(s0[i], e0[i], d0[i]);
     kahan_add(s1[i], e1[i], d1[i]);
+  }
+}
+
+// The warp ring of gram_chunks_mma_f32_staged: kGramStages chunks of 16 rows, each row
+// 32 positions and 4 floats of padding (a row of 144 bytes puts the 8 lanes of each
+// quarter-warp's 16-byte reads, rows g and columns 8t, on distinct banks).
+constexpr int kGramStages = 3;
+constexpr int kGramStageRow = 36;
+constexpr int kGramStageFloats = 16 * kGramStageRow;
+constexpr size_t kGramWarpRingBytes = sizeof(float) * kWarps * kGramStages * kGramStageFloats;
+
+// gram_chunks_mma_f32 for one warp alone on [lo, hi) of 16-byte aligned rows, with the
+// loads decoupled from the tensor-core work: each chunk's 16 rows x 32 positions are
+// copied into the warp's ring (cp.async, 16 bytes a copy, each row's 128 bytes by 8
+// lanes) kGramStages - 1 chunks ahead of the chunk being multiplied, so a warp always has
+// two chunks in flight without holding them in registers.  The chunks are multiplied in
+// order with the same fold every 8 chunks as gram_chunks_mma_f32 with one warp, so the
+// two give the same bits.  Rows are read up to the end of the buffers (n_total) and
+// never past it (the copy's zero fill); positions outside [lo, hi) are zeroed after the
+// read.  Rows of padding workers (null) stay zero in the ring.
+__device__ __forceinline__ void gram_chunks_mma_f32_staged(const void* const* rows, int64_t lo, int64_t hi,
+                                                           int64_t n_total, float* ring, float (&s0)[4],
+                                                           float (&e0)[4], float (&s1)[4], float (&e1)[4],
+                                                           uint32_t& org, uint32_t& orh) {
+  constexpr int kFoldChunks = 8;
+  const int lane = threadIdx.x & 31;
+  const int g = lane >> 2, tq = lane & 3;
+  const int64_t c0 = lo >> 5, c1 = (hi + 31) >> 5;
+  // this lane copies 16-byte vector cv of rows r0, r0 + 4, r0 + 8, r0 + 12 of each chunk
+  const int r0 = lane >> 3, cv = lane & 7;
+  const float* src[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    src[j] = static_cast<const float*>(rows[r0 + 4 * j]);
+    if (src[j] == nullptr) {
+#pragma unroll
+      for (int st = 0; st < kGramStages; ++st)
+        *reinterpret_cast<uint4*>(ring + st * kGramStageFloats + (r0 + 4 * j) * kGramStageRow + cv * 4) =
+            make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+  const uint32_t ring_s = smem_addr(ring);
+  auto issue = [&](int64_t c, int slot) {
+    if (c < c1) {
+      const int64_t p = c * 32 + cv * 4;
+      const int64_t left = n_total - p;
+      const int bytes = left >= 4 ? 16 : (left > 0 ? static_cast<int>(left) * 4 : 0);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (src[j] == nullptr) continue;
+        const uint32_t dst = ring_s + 4u * static_cast<uint32_t>(slot * kGramStageFloats +
+                                                                 (r0 + 4 * j) * kGramStageRow + cv * 4);
+        cp_async16(dst, bytes > 0 ? src[j] + p : src[j], bytes);
+      }
+    }
+    cp_async_commit();  // (an empty group past the end keeps the wait count uniform)
+  };
+  float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) s0[i] = e0[i] = s1[i] = e1[i] = 0.f;
+  org = orh = 0u;
+#pragma unroll
+  for (int st = 0; st < kGramStages - 1; ++st) issue(c0 + st, st);
+  int pending = 0;
+  for (int64_t c = c0; c < c1; ++c) {
+    const int i = static_cast<int>(c - c0);
+    __syncwarp();  // every lane has read the slot that is refilled next
+    issue(c + kGramStages - 1, (i + kGramStages - 1) % kGramStages);
+    cp_async_wait<kGramStages - 1>();
+    __syncwarp();  // the other lanes' copies of chunk c are visible
+    const float* sl = ring + (i % kGramStages) * kGramStageFloats;
+    uint4 rg[2], rh[2];
+#pragma unroll
+    for (int h2 = 0; h2 < 2; ++h2) {
+      rg[h2] = *reinterpret_cast<const uint4*>(sl + g * kGramStageRow + 8 * tq + 4 * h2);
+      rh[h2] = *reinterpret_cast<const uint4*>(sl + (g + 8) * kGramStageRow + 8 * tq + 4 * h2);
+    }
+    if (c * 32 < lo || c * 32 + 32 > hi) {  // the segment's first or last chunk
+      const int64_t p0 = c * 32 + 8 * tq;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        if (p0 + e >= lo && p0 + e < hi) continue;
+        uint32_t* vg = reinterpret_cast<uint32_t*>(&rg[e >> 2]);
+        uint32_t* vh = reinterpret_cast<uint32_t*>(&rh[e >> 2]);
+        vg[e & 3] = 0u;
+        vh[e & 3] = 0u;
+      }
+    }
+    gram_mma_f32_chunk(rg, rh, d0, d1, org, orh);
+    if (++pending == kFoldChunks) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        kahan_add(s0[k], e0[k], d0[k]);
+        kahan_add(s1[k], e1[k], d1[k]);
+        d0[k] = 0.f;
+        d1[k] = 0.f;
+      }
+      pending = 0;
+    }
+  }
+  cp_async_wait<0>();  // (only empty groups are left)
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    kahan_add(s0[k], e0[k], d0[k]);
+    kahan_add(s1[k], e1[k], d1[k]);
   }
 }
 
@@ -625,14 +738,21 @@ __global__ void __launch_bounds__(kThreads, 3) gram_warp_mma_f32_kernel(const St
   const int w = blockIdx.x * kWarps + wb;
   if (w >= a.nsmall) return;  // whole warps only (no block barrier below)
   const int q = blockIdx.y;
-  const int tile_id = a.small_list[w];
+  const int tile_id = a.small_list ? a.small_list[w] : w;
   const TileDesc t = a.tiles[tile_id];
   if (!tile_ok(a, tile_id, t)) return;  // (uniform over the warp)
   const int g = lane >> 2;
   float s0[4], e0[4], s1[4], e1[4];
   uint32_t mg, mh;
-  gram_chunks_mma_f32<KG>(static_cast<const float*>(a.in[q * KG + g]), static_cast<const float*>(a.in[q * KG + g + 8]),
-                          t.start, t.start + t.len, a.aligned != 0, 0, 1, s0, e0, s1, e1, mg, mh);
+  if (a.aligned) {  // launched with kGramWarpRingBytes of dynamic shared memory
+    extern __shared__ __align__(16) float gram_ring[];
+    gram_chunks_mma_f32_staged(a.in + q * KG, t.start, t.start + t.len, a.n_total,
+                               gram_ring + wb * kGramStages * kGramStageFloats, s0, e0, s1, e1, mg, mh);
+  } else {
+    gram_chunks_mma_f32<KG>(static_cast<const float*>(a.in[q * KG + g]),
+                            static_cast<const float*>(a.in[q * KG + g + 8]), t.start, t.start + t.len, false, 0,
+                            1, s0, e0, s1, e1, mg, mh);
+  }
   float* m = red[wb];
   store_lane_gram16(m, s0, e0, s1, e1);
   __syncwarp();
@@ -650,7 +770,7 @@ __global__ void __launch_bounds__(kThreads, 3) gram_warp_mma_f32_kernel(const St
 // group), on the tensor cores (gram_chunks_mma_bf16 with the warp alone on the tile).
 // The bf16 Gram needs no mirror mean: h.h products are symmetric as they stand.
 template <int KG>
-__global__ void __launch_bounds__(kThreads) gram_warp_mma_bf16_kernel(const StageArgs a) {
+__global__ void __launch_bounds__(kThreads, 3) gram_warp_mma_bf16_kernel(const StageArgs a) {
   pdl_enter();
   static_assert(KG == 16, "16 workers");
   constexpr int E = tri_count(KG);
@@ -659,7 +779,7 @@ __global__ void __launch_bounds__(kThreads) gram_warp_mma_bf16_kernel(const Stag
   const int w = blockIdx.x * kWarps + wb;
   if (w >= a.nsmall) return;  // whole warps only (no block barrier below)
   const int q = blockIdx.y;
-  const int tile_id = a.small_list[w];
+  const int tile_id = a.small_list ? a.small_list[w] : w;
   const TileDesc t = a.tiles[tile_id];
   if (!tile_ok(a, tile_id, t)) return;  // (uniform over the warp)
   const int g = lane >> 2;
@@ -1575,8 +1695,16 @@ __device__ __forceinline__ void combine_range(const StageArgs& a, int seg, int64
   using SO = typename ElemTraits<OutTag>::Storage;
   constexpr int VW = ElemTraits<InTag>::kVW;
   if (!ADASUM_CHECK(a.error, seg >= 0 && seg < a.nsegs && lo >= 0 && lo <= hi && hi <= a.n_total)) return;
-  if (a.skip_flagged && __ldcg(a.seg_flag + seg)) return;  // left to the fp64 path
   const bool aligned = a.aligned != 0;
+  const SI* x[KG];
+#pragma unroll
+  for (int k = 0; k < KG; ++k) x[k] = static_cast<const SI*>(a.in[q * KG + k]);
+  SO* y = static_cast<SO*>(a.out[q]);
+  const int64_t v0 = lo / VW, v1 = (hi + VW - 1) / VW;
+  // The skip flag and the coefficients are requested together, before the first
+  // vectors' loads, and waited on after them: one memory round trip before the stream
+  // starts, not three (a warp's short tile is only a few vectors long).
+  const int flagged = a.skip_flagged ? __ldcg(a.seg_flag + seg) : 0;
   float c[KG];
   if constexpr (KG == 1) {
     c[0] = 1.f;
@@ -1585,20 +1713,27 @@ __device__ __forceinline__ void combine_range(const StageArgs& a, int seg, int64
 #pragma unroll
     for (int k = 0; k < KG; ++k) c[k] = __ldcg(cp + k);
   }
-  const SI* x[KG];
-#pragma unroll
-  for (int k = 0; k < KG; ++k) x[k] = static_cast<const SI*>(a.in[q * KG + k]);
-  SO* y = static_cast<SO*>(a.out[q]);
-  const int64_t v0 = lo / VW, v1 = (hi + VW - 1) / VW;
-  for (int64_t v = v0 + first; v < v1; v += step) {
+  if constexpr (MOM) {
+    // the next vectors' loads are issued before this vector's w and v are read and
+    // written (GPT-style set, K = 8 bf16: 9.08 -> 9.00 ms per step; without the
+    // momentum step the same order made the one-warp tiles slower)
+    int64_t v = v0 + first;
     uint4 r[KG];
+    if (v < v1) {
 #pragma unroll
-    for (int k = 0; k < KG; ++k) r[k] = load_vec_raw<InTag, kLoadStream>(x[k], v, lo, hi, aligned);
-    float val[VW];
+      for (int k = 0; k < KG; ++k) r[k] = load_vec_raw<InTag, kLoadStream>(x[k], v, lo, hi, aligned);
+    }
+    if (flagged) return;  // left to the recompute
+    while (v < v1) {
+      float val[VW];
 #pragma unroll
-    for (int e = 0; e < VW; ++e) val[e] = tree_combine<InTag, 0, KG, KG>(c, r, e);
-    const int64_t p0 = v * VW;
-    if constexpr (MOM) {
+      for (int e = 0; e < VW; ++e) val[e] = tree_combine<InTag, 0, KG, KG>(c, r, e);
+      const int64_t p0 = v * VW;
+      v += step;
+      if (v < v1) {
+#pragma unroll
+        for (int k = 0; k < KG; ++k) r[k] = load_vec_raw<InTag, kLoadStream>(x[k], v, lo, hi, aligned);
+      }
       float wv[VW], mv[VW];
       load_f32_vec<VW>(a.master_w, p0, lo, hi, aligned, wv);
       if (a.momentum != nullptr) {  // heavy ball: v' = mu v + A, w' = w - lr v'
@@ -1615,8 +1750,17 @@ __device__ __forceinline__ void combine_range(const StageArgs& a, int seg, int64
       }
       store_vec<F32Tag, VW>(a.master_w, p0, lo, hi, aligned, wv);
       if (y != nullptr) store_vec<OutTag, VW>(y, p0, lo, hi, aligned, val);
-    } else {
-      store_vec<OutTag, VW>(y, p0, lo, hi, aligned, val);
+    }
+  } else {
+    for (int64_t v = v0 + first; v < v1; v += step) {
+      uint4 r[KG];
+#pragma unroll
+      for (int k = 0; k < KG; ++k) r[k] = load_vec_raw<InTag, kLoadStream>(x[k], v, lo, hi, aligned);
+      if (flagged) return;  // left to the recompute
+      float val[VW];
+#pragma unroll
+      for (int e = 0; e < VW; ++e) val[e] = tree_combine<InTag, 0, KG, KG>(c, r, e);
+      store_vec<OutTag, VW>(y, v * VW, lo, hi, aligned, val);
     }
   }
 }

@@ -41,9 +41,17 @@ int launch_gram_warp(const StageArgs& a, int in_dtype, void* stream, const char*
       case 2: *name = "gram_warp<f32,2>"; return launch(gram_warp_kernel<F32Tag, 2>, grid, block, a, stream);
       case 4: *name = "gram_warp<f32,4>"; return launch(gram_warp_kernel<F32Tag, 4>, grid, block, a, stream);
       case 8: *name = "gram_warp<f32,8>"; return launch(gram_warp_kernel<F32Tag, 8>, grid, block, a, stream);
-      case 16:
+      case 16: {
         *name = "gram_warp_mma<f32,16>";
-        return launch(gram_warp_mma_f32_kernel<16>, grid, block, a, stream);
+        if (!a.aligned) return launch(gram_warp_mma_f32_kernel<16>, grid, block, a, stream);
+        // aligned rows: the staged kernel, with its warps' copy rings in dynamic shared memory
+        static const int attr = static_cast<int>(cudaFuncSetAttribute(
+            gram_warp_mma_f32_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            static_cast<int>(kGramWarpRingBytes)));
+        if (attr != 0) return attr;
+        return launch_pdl(gram_warp_mma_f32_kernel<16>, grid, block, kGramWarpRingBytes,
+                          static_cast<cudaStream_t>(stream), a);
+      }
       default: return static_cast<int>(cudaErrorInvalidValue);
     }
   }
