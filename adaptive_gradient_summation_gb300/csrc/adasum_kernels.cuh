@@ -578,6 +578,9 @@ constexpr int kGramStages = 3;
 constexpr int kGramStageRow = 36;
 constexpr int kGramStageFloats = 16 * kGramStageRow;
 constexpr size_t kGramWarpRingBytes = sizeof(float) * kWarps * kGramStages * kGramStageFloats;
+// CTAs per SM of the staged kernel (its launch bound: 80 registers; at 4 CTAs, 64
+// registers spilled and the K = 64 set took 0.891 ms against 0.777)
+constexpr int kGramStagedCtas = 3;
 
 // gram_chunks_mma_f32 for one warp alone on [lo, hi) of 16-byte aligned rows, with the
 // loads decoupled from the tensor-core work: each chunk's 16 rows x 32 positions are
@@ -725,14 +728,34 @@ __device__ __forceinline__ void gram_tile_mma_f32(const StageArgs& a, int tile_i
   block_or_store(mma_lane_nz<F32Tag>(mg, mh), a.tile_nz + static_cast<size_t>(q) * a.ntiles + tile_id);
 }
 
+// A warp's Gram partial of one tile from the lanes' compensated sums (m: the warp's
+// 256 floats of shared memory): each off-diagonal entry is the mean of its two mirror
+// sums, as in gram_tile_mma_f32.
+__device__ __forceinline__ void warp_gram16_store(const StageArgs& a, int q, int tile_id, float* m,
+                                                  const float (&s0)[4], const float (&e0)[4],
+                                                  const float (&s1)[4], const float (&e1)[4], uint32_t mg,
+                                                  uint32_t mh) {
+  constexpr int KG = 16, E = tri_count(KG);
+  const int lane = threadIdx.x & 31;
+  store_lane_gram16(m, s0, e0, s1, e1);
+  __syncwarp();
+  float* dst = a.partials + (static_cast<size_t>(q) * a.ntiles + tile_id) * E;
+  for (int e = lane; e < E; e += 32) {
+    int i, j;
+    tri_unpack(KG, e, i, j);
+    dst[e] = i == j ? m[i * KG + i] : 0.5f * __fadd_rn(m[i * KG + j], m[j * KG + i]);
+  }
+  const uint32_t nz = warp_or_u32(mma_lane_nz<F32Tag>(mg, mh));
+  if (lane == 0) a.tile_nz[static_cast<size_t>(q) * a.ntiles + tile_id] = nz;
+}
+
 // Gram partials of small tiles of fp32 gradients (16 workers), one warp per (tile,
-// group), on the tensor cores (gram_chunks_mma_f32 with the warp alone on the tile);
-// each off-diagonal entry is the mean of its two mirror sums, as in gram_tile_mma_f32.
+// group), on the tensor cores (gram_chunks_mma_f32 with the warp alone on the tile):
+// rows that are not all 16-byte aligned.
 template <int KG>
 __global__ void __launch_bounds__(kThreads, 3) gram_warp_mma_f32_kernel(const StageArgs a) {
   pdl_enter();
   static_assert(KG == 16, "16 workers");
-  constexpr int E = tri_count(KG);
   __shared__ float red[kWarps][KG * KG];
   const int wb = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int w = blockIdx.x * kWarps + wb;
@@ -744,26 +767,32 @@ __global__ void __launch_bounds__(kThreads, 3) gram_warp_mma_f32_kernel(const St
   const int g = lane >> 2;
   float s0[4], e0[4], s1[4], e1[4];
   uint32_t mg, mh;
-  if (a.aligned) {  // launched with kGramWarpRingBytes of dynamic shared memory
-    extern __shared__ __align__(16) float gram_ring[];
-    gram_chunks_mma_f32_staged(a.in + q * KG, t.start, t.start + t.len, a.n_total,
-                               gram_ring + wb * kGramStages * kGramStageFloats, s0, e0, s1, e1, mg, mh);
-  } else {
-    gram_chunks_mma_f32<KG>(static_cast<const float*>(a.in[q * KG + g]),
-                            static_cast<const float*>(a.in[q * KG + g + 8]), t.start, t.start + t.len, false, 0,
-                            1, s0, e0, s1, e1, mg, mh);
-  }
-  float* m = red[wb];
-  store_lane_gram16(m, s0, e0, s1, e1);
-  __syncwarp();
-  float* dst = a.partials + (static_cast<size_t>(q) * a.ntiles + tile_id) * E;
-  for (int e = lane; e < E; e += 32) {
-    int i, j;
-    tri_unpack(KG, e, i, j);
-    dst[e] = i == j ? m[i * KG + i] : 0.5f * __fadd_rn(m[i * KG + j], m[j * KG + i]);
-  }
-  const uint32_t nz = warp_or_u32(mma_lane_nz<F32Tag>(mg, mh));
-  if (lane == 0) a.tile_nz[static_cast<size_t>(q) * a.ntiles + tile_id] = nz;
+  gram_chunks_mma_f32<KG>(static_cast<const float*>(a.in[q * KG + g]), static_cast<const float*>(a.in[q * KG + g + 8]),
+                          t.start, t.start + t.len, a.aligned != 0, 0, 1, s0, e0, s1, e1, mg, mh);
+  warp_gram16_store(a, q, tile_id, red[wb], s0, e0, s1, e1, mg, mh);
+}
+
+// The same for 16-byte aligned rows, staged through each warp's ring in dynamic shared
+// memory (gram_chunks_mma_f32_staged; launched with kGramWarpRingBytes).  The ring's
+// first slot takes the warp's 16 x 16 sums once the copies have drained.
+template <int KG>
+__global__ void __launch_bounds__(kThreads, kGramStagedCtas) gram_warp_staged_f32_kernel(const StageArgs a) {
+  pdl_enter();
+  static_assert(KG == 16, "16 workers");
+  extern __shared__ __align__(16) float gram_ring[];
+  const int wb = threadIdx.x >> 5;
+  const int w = blockIdx.x * kWarps + wb;
+  if (w >= a.nsmall) return;  // whole warps only (no block barrier below)
+  const int q = blockIdx.y;
+  const int tile_id = a.small_list ? a.small_list[w] : w;
+  const TileDesc t = a.tiles[tile_id];
+  if (!tile_ok(a, tile_id, t)) return;  // (uniform over the warp)
+  float s0[4], e0[4], s1[4], e1[4];
+  uint32_t mg, mh;
+  float* ring = gram_ring + wb * kGramStages * kGramStageFloats;
+  gram_chunks_mma_f32_staged(a.in + q * KG, t.start, t.start + t.len, a.n_total, ring, s0, e0, s1, e1, mg, mh);
+  __syncwarp();  // every lane is done reading the ring
+  warp_gram16_store(a, q, tile_id, ring, s0, e0, s1, e1, mg, mh);
 }
 
 // Gram partials of small tiles of bf16 gradients (16 workers), one warp per (tile,

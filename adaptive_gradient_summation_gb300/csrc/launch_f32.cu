@@ -46,10 +46,10 @@ int launch_gram_warp(const StageArgs& a, int in_dtype, void* stream, const char*
         if (!a.aligned) return launch(gram_warp_mma_f32_kernel<16>, grid, block, a, stream);
         // aligned rows: the staged kernel, with its warps' copy rings in dynamic shared memory
         static const int attr = static_cast<int>(cudaFuncSetAttribute(
-            gram_warp_mma_f32_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            gram_warp_staged_f32_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
             static_cast<int>(kGramWarpRingBytes)));
         if (attr != 0) return attr;
-        return launch_pdl(gram_warp_mma_f32_kernel<16>, grid, block, kGramWarpRingBytes,
+        return launch_pdl(gram_warp_staged_f32_kernel<16>, grid, block, kGramWarpRingBytes,
                           static_cast<cudaStream_t>(stream), a);
       }
       default: return static_cast<int>(cudaErrorInvalidValue);

@@ -135,6 +135,32 @@ def test_unaligned_pointers(native, dtype):
     check_against_oracle(grads, offs, out)
 
 
+@pytest.mark.parametrize("K", [16, 64])
+def test_staged_and_register_loads_agree_bitwise(native, K):
+    """The fp32 warp Gram of 16-worker groups stages 16-byte aligned rows through
+    shared memory (cp.async) and loads other rows into registers; both multiply the same
+    chunks in the same order, so the same values give the same bits.  Here the inputs
+    are the same values, once in 16-byte aligned buffers and once one element off, on a
+    layout whose tiles are all short (segments cut into 512-position tiles, ragged ends
+    near the end of the buffers included)."""
+    rng = np.random.default_rng(80 + K)
+    lengths = [int(x) for x in rng.integers(33, 4097, size=1200)] + [1, 4095, 37]
+    offs = workloads.offsets_from_numels(lengths)
+    n = int(offs[-1])
+    grads = rand_grads(K, n, torch.float32, seed=80 + K)
+    shifted = []
+    for g in grads:
+        buf = torch.empty(n + 1, dtype=torch.float32, device=DEV)
+        buf[1:].copy_(g)
+        shifted.append(buf[1:])
+    out_a = ags.reduce(grads, offs)
+    out_b = ags.reduce(shifted, offs)
+    torch.cuda.synchronize()
+    assert torch.equal(out_a, out_b)
+    if K == 16:
+        check_against_oracle(grads, offs, out_a)
+
+
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 def test_in_place(native, dtype):
     K = 4
