@@ -382,12 +382,11 @@ __device__ __forceinline__ void gram_chunks_mma_bf16(const uint16_t* xg, const u
     for (int u = 0; u < U; ++u) {
       org |= vec_or(rg[u]);
       orh |= vec_or(rh[u]);
+      // (the two accumulators' MMAs alternate, so each waits on its own chain only)
       mma_bf16_16816(d0, rg[u].x, rh[u].x, rg[u].y, rh[u].y, rg[u].x, rg[u].y);
+      if constexpr (KG == 16) mma_bf16_16816(d1, rg[u].x, rh[u].x, rg[u].y, rh[u].y, rh[u].x, rh[u].y);
       mma_bf16_16816(d0, rg[u].z, rh[u].z, rg[u].w, rh[u].w, rg[u].z, rg[u].w);
-      if constexpr (KG == 16) {
-        mma_bf16_16816(d1, rg[u].x, rh[u].x, rg[u].y, rh[u].y, rh[u].x, rh[u].y);
-        mma_bf16_16816(d1, rg[u].z, rh[u].z, rg[u].w, rh[u].w, rh[u].z, rh[u].w);
-      }
+      if constexpr (KG == 16) mma_bf16_16816(d1, rg[u].z, rh[u].z, rg[u].w, rh[u].w, rh[u].z, rh[u].w);
     }
     if (++pending == kFold) {
 #pragma unroll
@@ -487,17 +486,19 @@ __device__ __forceinline__ void gram_mma_f32_chunk(const uint4 (&rg)[2], const u
     split_bf16x3(ga, gb, gh[k], gm[k], gl[k]);
     split_bf16x3(ha, hb, hh[k], hm[k], hl[k]);
   }
-  // d += A B for A = rows (g, g+8) of part pa, B = columns g (d0) and g+8 (d1) of part pb
+  // d += A B for A = rows (g, g+8) of part pa, B = columns g (d0) and g+8 (d1) of part
+  // pb; the two accumulators' MMAs alternate, so each waits on its own chain only
   auto mmas = [&](const uint32_t (&ag)[4], const uint32_t (&ah)[4], const uint32_t (&bg)[4],
                   const uint32_t (&bh)[4]) {
     mma_bf16_16816(d0, ag[0], ah[0], ag[1], ah[1], bg[0], bg[1]);
-    mma_bf16_16816(d0, ag[2], ah[2], ag[3], ah[3], bg[2], bg[3]);
     mma_bf16_16816(d1, ag[0], ah[0], ag[1], ah[1], bh[0], bh[1]);
+    mma_bf16_16816(d0, ag[2], ah[2], ag[3], ah[3], bg[2], bg[3]);
     mma_bf16_16816(d1, ag[2], ah[2], ag[3], ah[3], bh[2], bh[3]);
   };
   // R = h.h + m.m + h.(2m) + h.(2l): the mirror sum R_ij + R_ji is twice the six
   // products' sum (h.m and m.h, h.l and l.h meet there), and its diagonal R_ii is that
-  // sum itself; doubling a bf16 value is exact
+  // sum itself; doubling a bf16 value is exact (doubling h instead, 8 adds for 16,
+  // made the kernels spill)
   mmas(gh, hh, gh, hh);
   mmas(gm, hm, gm, hm);
 #pragma unroll
