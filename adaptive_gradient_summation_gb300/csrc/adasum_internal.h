@@ -69,17 +69,22 @@ constexpr int kChunkTiles = 32;
 // K = 64 from 0.900 to 0.889 ms and bf16 K = 64 from 0.876 to 0.864 ms; 2048 made bf16
 // K = 8 slower (0.124 -> 0.135 ms).
 constexpr int kSmallTileF32 = 512;
-// CTAs per SM, for each of grid.y's groups, of the short-tile combine's grid, whose
+// 256-thread CTAs per SM, for each of grid.y's groups, of the short-tile combine's grid, whose
 // warps loop over the tiles (each warp takes every W-th tile).  Measured on the
 // 10,000-segment layout against one CTA per eight tiles: fp32 K = 64 0.768 -> 0.764 ms,
 // bf16 K = 64 0.758 -> 0.733 ms.  8 per SM gained less (0.766 ms).  A single wave of
 // the CTAs that fit, for the combine and the warp Grams alike, measured 0.801 ms: with
 // 15 tiles of unequal length per warp, warps sat idle at the end.  The warp Grams keep one
-// CTA per eight tiles.
+// CTA per eight tiles.  The CTAs are two warps (kCombineWarpThreads; the grid holds as
+// many warps as four 256-thread CTAs per SM), so a warp that has run out of tiles holds
+// its registers only until its one sibling is done: fp32 K = 64 0.768 -> 0.762 ms, bf16
+// K = 64 0.727 -> 0.696 ms against eight-warp CTAs; one-warp CTAs measured the same.
 constexpr int kWarpTileCtasPerSm = 4;
+constexpr int kCombineWarpThreads = 64;
 inline int warp_tile_grid(int ntiles, int num_sms) {
-  const int need = (ntiles + kThreads / 32 - 1) / (kThreads / 32);
-  const int cap = kWarpTileCtasPerSm * (num_sms > 0 ? num_sms : 1);
+  const int wpb = kCombineWarpThreads / 32;
+  const int need = (ntiles + wpb - 1) / wpb;
+  const int cap = kWarpTileCtasPerSm * (kThreads / kCombineWarpThreads) * (num_sms > 0 ? num_sms : 1);
   return need < cap ? need : cap;
 }
 constexpr int kSmallTileBF16 = 2048;

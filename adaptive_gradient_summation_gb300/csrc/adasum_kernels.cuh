@@ -1844,14 +1844,15 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const StageArgs a) {
 // Short tiles (a.small_list: kSmallTileF32, kSmallTileBF16 or kSmallTileSimt positions at
 // most), one warp each: a CTA per tile would leave most of its threads without a vector and run its
 // tiles' coefficient loads one after another.
-// Each warp takes tiles w, w + W, w + 2W, ... (W the grid's warps: a few CTAs per SM,
-// warp_tile_grid), so warps stay resident across tiles instead of a CTA of eight
-// one-tile warps retiring for each eight tiles.
+// Each warp takes tiles w, w + W, w + 2W, ... (W the grid's warps: a few per SM,
+// warp_tile_grid, in CTAs of kCombineWarpThreads), so warps stay resident across tiles
+// instead of a CTA of eight one-tile warps retiring for each eight tiles.
 template <typename InTag, typename OutTag, int KG, bool MOM>
 __global__ void __launch_bounds__(kThreads) combine_warp_kernel(const StageArgs a) {
   pdl_enter();
-  const int W = static_cast<int>(gridDim.x) * kWarps;
-  for (int w = blockIdx.x * kWarps + (threadIdx.x >> 5); w < a.nsmall; w += W) {  // (whole warps)
+  const int wpb = static_cast<int>(blockDim.x) >> 5;
+  const int W = static_cast<int>(gridDim.x) * wpb;
+  for (int w = blockIdx.x * wpb + (threadIdx.x >> 5); w < a.nsmall; w += W) {  // (whole warps)
     TileDesc t;
     if (!list_tile(a, a.small_list, w, t)) return;
     combine_range<InTag, OutTag, KG, MOM>(a, t.seg, t.start, t.start + t.len, blockIdx.y, threadIdx.x & 31, 32);

@@ -35,7 +35,7 @@ int launch_gram_bf16(const StageArgs& a, void* stream, const char** name) {
 template <typename OutTag, bool MOM>
 static int combine_bf16_k(const StageArgs& a, int warp, void* stream, const char** name) {
   if (warp) {  // short tiles, one warp each
-    const dim3 grid(warp_tile_grid(a.nsmall, a.num_sms), a.G), block(kThreads);
+    const dim3 grid(warp_tile_grid(a.nsmall, a.num_sms), a.G), block(kCombineWarpThreads);
     switch (a.Kg) {
       case 1: *name = "combine_warp<bf16,1>"; return launch(combine_warp_kernel<BF16Tag, OutTag, 1, MOM>, grid, block, a, stream);
       case 2: *name = "combine_warp<bf16,2>"; return launch(combine_warp_kernel<BF16Tag, OutTag, 2, MOM>, grid, block, a, stream);

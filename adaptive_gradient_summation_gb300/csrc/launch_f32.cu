@@ -104,7 +104,7 @@ int launch_coef(const StageArgs& a, void* stream, const char** name) {
 template <typename OutTag, bool MOM>
 static int combine_f32_k(const StageArgs& a, int warp, void* stream, const char** name) {
   if (warp) {  // short tiles, one warp each
-    const dim3 grid(warp_tile_grid(a.nsmall, a.num_sms), a.G), block(kThreads);
+    const dim3 grid(warp_tile_grid(a.nsmall, a.num_sms), a.G), block(kCombineWarpThreads);
     switch (a.Kg) {
       case 1: *name = "combine_warp<f32,1>"; return launch(combine_warp_kernel<F32Tag, OutTag, 1, MOM>, grid, block, a, stream);
       case 2: *name = "combine_warp<f32,2>"; return launch(combine_warp_kernel<F32Tag, OutTag, 2, MOM>, grid, block, a, stream);
