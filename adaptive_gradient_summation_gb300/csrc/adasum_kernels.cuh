@@ -291,7 +291,7 @@ template <typename Tag, int KG>
 __global__ void __launch_bounds__(kThreads) gram_warp_kernel(const StageArgs a) {
   pdl_enter();
   constexpr int E = tri_count(KG);
-  const int w = blockIdx.x * kWarps + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  const int w = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (w >= a.nsmall) return;  // whole warps only
   const int q = blockIdx.y;
   const int tile_id = a.small_list ? a.small_list[w] : w;
@@ -580,7 +580,12 @@ __device__ __forceinline__ void gram_chunks_mma_f32(const float* xg, const float
 constexpr int kGramStages = 3;
 constexpr int kGramStageRow = 36;
 constexpr int kGramStageFloats = 16 * kGramStageRow;
-constexpr size_t kGramWarpRingBytes = sizeof(float) * kWarps * kGramStages * kGramStageFloats;
+// Threads per CTA of the one-warp-per-tile Gram kernels: two warps, so a CTA that holds
+// a finished warp retires as soon as its one sibling is done (eight-warp CTAs waited on
+// the slowest of eight tiles: the fp32 K = 64 set 0.762 -> 0.753 ms, bf16 K = 64 on its
+// layout 0.697 -> 0.682 ms).
+constexpr int kGramWarpThreads = 64;
+constexpr size_t kGramWarpRingBytes = sizeof(float) * (kGramWarpThreads / 32) * kGramStages * kGramStageFloats;
 // CTAs per SM of the staged kernel (its launch bound: 80 registers; at 4 CTAs, 64
 // registers spilled and the K = 64 set took 0.891 ms against 0.777)
 constexpr int kGramStagedCtas = 3;
@@ -761,7 +766,7 @@ __global__ void __launch_bounds__(kThreads, 3) gram_warp_mma_f32_kernel(const St
   static_assert(KG == 16, "16 workers");
   __shared__ float red[kWarps][KG * KG];
   const int wb = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int w = blockIdx.x * kWarps + wb;
+  const int w = blockIdx.x * (blockDim.x >> 5) + wb;
   if (w >= a.nsmall) return;  // whole warps only (no block barrier below)
   const int q = blockIdx.y;
   const int tile_id = a.small_list ? a.small_list[w] : w;
@@ -784,7 +789,7 @@ __global__ void __launch_bounds__(kThreads, kGramStagedCtas) gram_warp_staged_f3
   static_assert(KG == 16, "16 workers");
   extern __shared__ __align__(16) float gram_ring[];
   const int wb = threadIdx.x >> 5;
-  const int w = blockIdx.x * kWarps + wb;
+  const int w = blockIdx.x * (blockDim.x >> 5) + wb;
   if (w >= a.nsmall) return;  // whole warps only (no block barrier below)
   const int q = blockIdx.y;
   const int tile_id = a.small_list ? a.small_list[w] : w;
@@ -808,7 +813,7 @@ __global__ void __launch_bounds__(kThreads, 3) gram_warp_mma_bf16_kernel(const S
   constexpr int E = tri_count(KG);
   __shared__ float red[kWarps][KG * KG];
   const int wb = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int w = blockIdx.x * kWarps + wb;
+  const int w = blockIdx.x * (blockDim.x >> 5) + wb;
   if (w >= a.nsmall) return;  // whole warps only (no block barrier below)
   const int q = blockIdx.y;
   const int tile_id = a.small_list ? a.small_list[w] : w;

@@ -35,7 +35,8 @@ int launch_gram_f32(const StageArgs& a, void* stream, const char** name) {
 }
 
 int launch_gram_warp(const StageArgs& a, int in_dtype, void* stream, const char** name) {
-  const dim3 grid((a.nsmall + kWarps - 1) / kWarps, a.G), block(kThreads);
+  constexpr int wpb = kGramWarpThreads / 32;
+  const dim3 grid((a.nsmall + wpb - 1) / wpb, a.G), block(kGramWarpThreads);
   if (in_dtype == kF32) {
     switch (a.Kg) {
       case 2: *name = "gram_warp<f32,2>"; return launch(gram_warp_kernel<F32Tag, 2>, grid, block, a, stream);
